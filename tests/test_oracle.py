@@ -1,0 +1,365 @@
+"""Pins for the CPU oracle: each check ties the oracle to something other than
+itself (a hand-written table, a closed form, an invariant the pages state, a brute
+force search, or an independent restatement in plain Python loops)."""
+import math
+import os
+
+import numpy as np
+import pytest
+
+import kvarn_synth as synth
+from oracle import kvarn_oracle as o
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden_rows(name):
+    rows = []
+    for line in open(os.path.join(GOLDEN, name)):
+        line = line.strip()
+        if line and not line.startswith("#"):
+            rows.append(line.split())
+    return rows
+
+
+def _tile(seed=0):
+    k, v, q = synth.single_tile(seed)
+    return k.T.astype(np.float64), v.T.astype(np.float64), q.astype(np.float64)
+
+
+# ------------------------------------------------------------------ Hadamard (stage 2)
+def test_hadamard_matches_hand_written_order_8():
+    want = np.array([[float(x) for x in r] for r in _golden_rows("hadamard_8.txt")])
+    assert np.array_equal(o.sylvester_hadamard(8) * np.sqrt(8), want)
+
+
+def test_hadamard_orthonormal_symmetric():
+    h = o.sylvester_hadamard(128)
+    assert np.abs(h @ h.T - np.eye(128)).max() < 1e-14
+    assert np.array_equal(h, h.T)
+    assert np.all(np.abs(np.abs(h) * np.sqrt(128) - 1) < 1e-14)
+
+
+def test_hadamard_is_kron_power_of_h2():
+    h2 = np.array([[1.0, 1.0], [1.0, -1.0]])
+    h = np.ones((1, 1))
+    for _ in range(7):
+        h = np.kron(h2, h)
+    assert np.array_equal(o.sylvester_hadamard(128) * np.sqrt(128), h)
+
+
+def test_rotation_preserves_norms_and_scores():
+    rng = np.random.default_rng(1)
+    x = rng.standard_normal((128, 40))
+    q = rng.standard_normal((5, 128))
+    xr = o.rotate(x)
+    assert np.allclose(np.linalg.norm(xr, axis=0), np.linalg.norm(x, axis=0), rtol=1e-13)
+    qr = o.rotate(q.T).T
+    assert np.allclose(qr @ xr, q @ x, rtol=1e-12, atol=1e-12)
+
+
+# ------------------------------------------------------------------ fp16 rounding
+def _all_finite_halves():
+    bits = np.arange(0, 0x7C00, dtype=np.uint16)          # +0 .. largest finite
+    pos = bits.view(np.float16).astype(np.float64)
+    return pos, bits
+
+
+def _brute_rne(x):
+    """Nearest binary16 by search over every finite positive half; ties -> even bits."""
+    vals, bits = _all_finite_halves()
+    out = np.empty_like(x)
+    for n, xv in enumerate(x):
+        a = abs(xv)
+        j = np.searchsorted(vals, a)
+        if j == 0:
+            r = vals[0]
+        elif j >= len(vals):
+            r = vals[-1] if a <= 65520.0 else np.inf
+        else:
+            lo, hi = vals[j - 1], vals[j]
+            if a - lo < hi - a:
+                r = lo
+            elif a - lo > hi - a:
+                r = hi
+            else:
+                r = lo if bits[j - 1] % 2 == 0 else hi
+        out[n] = math.copysign(r, xv)
+    return out
+
+
+def test_fp16_golden_encodings():
+    for val, bits in _golden_rows("fp16_bits.txt"):
+        got = np.array([o.fp16_rne(float(val))]).astype(np.float16).view(np.uint16)[0]
+        assert got == int(bits, 16), (val, hex(got), bits)
+
+
+def test_fp16_rne_matches_brute_force():
+    rng = np.random.default_rng(2)
+    x = np.concatenate([
+        rng.standard_normal(3000) * 10.0 ** rng.uniform(-7, 4.5, 3000),
+        # exact midpoints between neighbouring halves, both parities
+        (np.arange(1000, 1100, dtype=np.uint16).view(np.float16).astype(np.float64)
+         + np.arange(1001, 1101, dtype=np.uint16).view(np.float16).astype(np.float64)) / 2,
+    ])
+    assert np.array_equal(o.fp16_rne(x), _brute_rne(x))
+
+
+# ------------------------------------------------------------------ normalisation (stage 3)
+def test_first_column_pass_closed_form():
+    """With no row scale yet, a rotated column's mean is x_0 / sqrt(n) and its mean
+    square is |x|^2 / n (H orthonormal, first Sylvester row all ones), so its
+    variance is sum_{k >= 1} x_k^2 / n, computed here from the unrotated tile."""
+    kx, vx, _ = _tile(0)
+    for x in (kx, vx):
+        lr, lc = o.normalise(o.rotate(x), n_iters=1)
+        var = (x[1:] ** 2).sum(axis=0) / 128.0
+        assert np.allclose(lc, 0.5 * np.log(var + o.EPS), rtol=0, atol=1e-12)
+
+
+def test_final_pass_is_a_row_pass_to_unit_variance():
+    kx, vx, _ = _tile(3)
+    for x in (kx, vx):
+        xr = o.rotate(x)
+        lr, lc = o.normalise(xr)
+        z = xr * np.exp(-lr)[:, None] * np.exp(-lc)[None, :]
+        assert np.abs(z.var(axis=1) - 1.0).max() < 1e-4       # rows: exactly v / (v + eps)
+
+
+def test_column_scaling_equivariance_fixes_order_and_sign():
+    """With eps = 0, scaling token j by beta_j shifts lc_j by log beta_j and changes
+    nothing else, because the first pass is a column pass."""
+    kx, _, _ = _tile(4)
+    xr = o.rotate(kx)
+    beta = np.exp(np.random.default_rng(5).uniform(-2, 2, 128))
+    lr0, lc0 = o.normalise(xr, eps=0.0)
+    lr1, lc1 = o.normalise(xr * beta[None, :], eps=0.0)
+    assert np.allclose(lr1, lr0, atol=1e-10)
+    assert np.allclose(lc1 - lc0, np.log(beta), atol=1e-10)
+
+
+def test_normalisation_equalises_column_spread():
+    """Stage 3 equalises the variance inside the tile: the spread of the column
+    log-stds, measured before each column pass, never grows."""
+    k, v = synth.prefill_kv(128, 8, seed=11)
+    for h in range(8):
+        for x in (k[:, h, :].T, v[:, h, :].T):
+            trace = []
+            o.normalise(o.rotate(x.astype(np.float64)), trace=trace)
+            spread = [t.std() for t in trace]
+            assert all(b <= a * (1 + 1e-9) for a, b in zip(spread, spread[1:])), spread
+
+
+def test_many_iterations_reach_doubly_normalised_tile():
+    kx, _, _ = _tile(6)
+    xr = o.rotate(kx)
+    lr, lc = o.normalise(xr, n_iters=60, eps=0.0)
+    z = xr * np.exp(-lr)[:, None] * np.exp(-lc)[None, :]
+    assert np.abs(z.var(axis=1) - 1).max() < 1e-9
+    assert np.abs(z.var(axis=0) - 1).max() < 1e-3
+
+
+# ------------------------------------------------------------------ RTN (stage 4)
+def _brute_codes(y, s, z, bits, axis):
+    levels = np.arange(2 ** bits, dtype=np.float64)
+    zz, ss = np.expand_dims(z, axis), np.expand_dims(s, axis)
+    grid = zz[..., None] + ss[..., None] * levels            # [..., levels]
+    err = np.abs(y[..., None] - grid)
+    # nearest grid point; on an exact tie floor(x + 1/2) takes the upper level
+    best = err.shape[-1] - 1 - np.argmin(err[..., ::-1], axis=-1)
+    return best
+
+
+def test_rtn_is_nearest_grid_point_and_bounded():
+    kx, vx, _ = _tile(7)
+    for x, kind, bits, axis in ((kx, "K", 4, -1), (vx, "V", 2, -2)):
+        qd = o.quantize_tensor(x, kind)
+        codes, s, z, y = qd["codes"], qd["s"], qd["z"], qd["y"]
+        assert codes.max() <= 2 ** bits - 1
+        assert np.array_equal(codes, _brute_codes(y, s, z, bits, axis))
+        assert np.array_equal(o.fp16_rne(s), s) and np.array_equal(o.fp16_rne(z), z)
+        deq = np.expand_dims(z, axis) + codes * np.expand_dims(s, axis)
+        ulp = lambda a: np.spacing(np.abs(a).astype(np.float16)).astype(np.float64)
+        bound = (np.expand_dims(s / 2 + ulp(z) / 2 + (2 ** bits - 1) * ulp(s) / 2, axis))
+        assert (np.abs(y - deq) <= bound * (1 + 1e-12)).all()
+        # the group extremes land on the end codes
+        assert (np.take_along_axis(codes, np.expand_dims(y.argmin(axis), axis), axis) == 0).all()
+        assert (np.take_along_axis(codes, np.expand_dims(y.argmax(axis), axis), axis) == 2 ** bits - 1).all()
+
+
+def test_key_groups_are_channels_and_value_groups_are_tokens():
+    """Stage 4: key scales per channel, value scales per token. Scaling one token's
+    values or one channel's keys only moves that group's (s, z)."""
+    kx, vx, _ = _tile(8)
+    kq = o.quantize_tensor(kx, "K")
+    vq = o.quantize_tensor(vx, "V")
+    assert kq["s"].shape == (128,) and vq["s"].shape == (128,)
+    y = kq["y"]
+    assert np.allclose(kq["z"], o.fp16_rne(y.min(axis=1)))
+    y = vq["y"]
+    assert np.allclose(vq["z"], o.fp16_rne(y.min(axis=0)))
+
+
+def test_method_beats_plain_rtn_on_outlier_keys():
+    """The rotation and normalisation exist to cut quantisation error on keys with
+    outlier channels (KVarN README, stages 2 and 3)."""
+    k, v = synth.prefill_kv(128, 8, seed=12)
+    worse = 0
+    for h in range(8):
+        x = k[:, h, :].T.astype(np.float64)
+        qd = o.quantize_tensor(x, "K")
+        xhat = o.dequant_tensor(qd["codes"], qd["r"], qd["c"], qd["s"], qd["z"], "K")
+        e_kvarn = np.linalg.norm(xhat - x)
+        # plain asymmetric 4-bit RTN per channel, no rotation or normalisation
+        codes, s, z, _ = o.rtn(x, 4, axis=-1)
+        e_plain = np.linalg.norm(z[:, None] + codes * s[:, None] - x)
+        worse += e_kvarn >= e_plain
+    assert worse == 0
+
+
+def test_dequant_error_bounded_by_half_step():
+    kx, vx, _ = _tile(9)
+    for x, kind in ((kx, "K"), (vx, "V")):
+        qd = o.quantize_tensor(x, kind)
+        xr_hat = o.dequant_tensor(qd["codes"], qd["r"], qd["c"], qd["s"], qd["z"], kind, rotated=True)
+        s = qd["s"][:, None] if kind == "K" else qd["s"][None, :]
+        scale = qd["r"][:, None] * qd["c"][None, :]
+        assert (np.abs(qd["xr"] - xr_hat) <= scale * s * 0.5 * (1 + 2e-3) + 1e-9).all()
+
+
+def test_degenerate_tiles_stay_finite():
+    zero = np.zeros((128, 128))
+    const = np.full((128, 128), 3.0)
+    spike = np.zeros((128, 128)); spike[5, 7] = 60000.0
+    big = np.full((128, 128), 65504.0); big[::2] *= -1
+    for x in (zero, const, spike, big):
+        for kind in ("K", "V"):
+            qd = o.quantize_tensor(x, kind)
+            for name in ("r", "c", "s", "z"):
+                assert np.all(np.isfinite(qd[name])), (kind, name)
+            xhat = o.dequant_tensor(qd["codes"], qd["r"], qd["c"], qd["s"], qd["z"], kind)
+            assert np.all(np.isfinite(xhat))
+    qd = o.quantize_tensor(zero, "K")
+    assert (qd["codes"] == 0).all() and (qd["z"] == 0).all()
+
+
+# ------------------------------------------------------------------ packed layout
+def test_layout_spots_match_hand_computed_table():
+    for tensor, ch, tok, byte, shift in _golden_rows("record_layout_spots.txt"):
+        f = o.k_code_position if tensor == "K" else o.v_code_position
+        assert f(int(ch), int(tok)) == (int(byte), int(shift)), (tensor, ch, tok)
+
+
+def test_pack_roundtrip_and_single_code_positions():
+    rng = np.random.default_rng(13)
+    kq = dict(codes=rng.integers(0, 16, (3, 128, 128)).astype(np.uint8))
+    vq = dict(codes=rng.integers(0, 4, (3, 128, 128)).astype(np.uint8))
+    for d in (kq, vq):
+        for n in ("r", "c", "s", "z"):
+            d[n] = o.fp16_rne(rng.standard_normal((3, 128)))
+    rec = o.pack_record(kq, vq)
+    k2, v2 = o.unpack_record(rec)
+    assert np.array_equal(k2["codes"], kq["codes"]) and np.array_equal(v2["codes"], vq["codes"])
+    for n in ("r", "c", "s", "z"):
+        assert np.array_equal(k2[n], kq[n]) and np.array_equal(v2[n], vq[n])
+    # every code value at a sample of positions lands alone at its documented bits
+    for (i, t) in [(0, 0), (9, 100), (127, 1), (64, 64), (33, 17)]:
+        for val in range(16):
+            kc = np.zeros((128, 128), np.uint8); kc[i, t] = val
+            vc = np.zeros((128, 128), np.uint8); vc[i, t] = val & 3
+            zero = {n: np.zeros(128) for n in ("r", "c", "s", "z")}
+            r = o.pack_record(dict(codes=kc, **zero), dict(codes=vc, **zero))
+            b, sh = o.k_code_position(i, t)
+            assert r[b] == val << sh and np.count_nonzero(r[:8192]) == (val != 0)
+            b, sh = o.v_code_position(i, t)
+            assert r[b] == (val & 3) << sh and np.count_nonzero(r[8192:12288]) == ((val & 3) != 0)
+
+
+def test_compression_ratio_within_pages_claim():
+    """14336 bytes per (K, V) tile-head vs 65536 fp16 bytes: 4.571x, inside the
+    3-5x KV-capacity claim (KVarN README, introduction)."""
+    assert o.RECORD_BYTES == 14336
+    assert abs(o.compression_ratio() - 65536 / 14336) < 1e-12
+    assert 3.0 <= o.compression_ratio() <= 5.0
+
+
+# ------------------------------------------------------------------ attention
+def _loop_attention(q, k, v):
+    out = []
+    for qh in q:
+        scores = [sum(qh[c] * kt[c] for c in range(len(qh))) / math.sqrt(len(qh)) for kt in k]
+        mx = max(scores)
+        w = [math.exp(s - mx) for s in scores]
+        tot = sum(w)
+        out.append([sum(w[t] * v[t][c] for t in range(len(k))) / tot for c in range(len(qh))])
+    return np.array(out)
+
+
+def test_attend_matches_plain_loops():
+    rng = np.random.default_rng(14)
+    q = rng.standard_normal((2, 128)); k = rng.standard_normal((5, 128)) * 3; v = rng.standard_normal((5, 128))
+    assert np.allclose(o.attend(q, k, v), _loop_attention(q.tolist(), k.tolist(), v.tolist()), atol=1e-12)
+
+
+def test_rotated_domain_attention_equals_plain():
+    """q rotated by H against rotated dequantised tiles, then output un-rotated by
+    H^T, equals attention over the un-rotated tiles (the rotation is orthonormal)."""
+    kx, vx, q = _tile(15)
+    rec, _, _ = o.quantize_tiles(kx.T, vx.T)
+    kr, vr = o.dequant_record(rec, rotated=True)
+    k, v = o.dequant_record(rec)
+    plain = o.attend(q, k.T, v.T)
+    h = o.sylvester_hadamard(128)
+    rot = o.attend(q @ h.T, kr.T, vr.T) @ h
+    assert np.allclose(plain, rot, atol=1e-12)
+
+
+def test_split_merge_identity():
+    """Attention over two token sets merged by log-sum-exp equals the whole."""
+    rng = np.random.default_rng(16)
+    q = rng.standard_normal((8, 128)); k = rng.standard_normal((300, 128)); v = rng.standard_normal((300, 128))
+    parts = []
+    for sl in (slice(0, 128), slice(128, 300)):
+        s = q @ k[sl].T / np.sqrt(128)
+        m = s.max(axis=1, keepdims=True)
+        p = np.exp(s - m)
+        parts.append((m, p.sum(axis=1, keepdims=True), p @ v[sl]))
+    M = np.maximum(parts[0][0], parts[1][0])
+    L = sum(l * np.exp(m - M) for m, l, _ in parts)
+    A = sum(a * np.exp(m - M) for m, _, a in parts)
+    assert np.allclose(A / L, o.attend(q, k, v), atol=1e-12)
+
+
+def test_decode_reads_cache_and_workspace():
+    k, v = synth.prefill_kv(300, 2, seed=17)
+    q = synth.queries(1, 4, seed=17).astype(np.float64)
+    cache = np.zeros((4, 2, o.RECORD_BYTES), np.uint8)
+    slots = np.concatenate([np.arange(128) + 3 * 128, np.arange(128) + 1 * 128])
+    o.quantize_into_cache(k[:256], v[:256], slots, cache)
+    ws = np.zeros((1, 2, 2, 128, 128), np.float16)
+    ws[0, :, 0, :44] = k[256:].transpose(1, 0, 2)
+    ws[0, :, 1, :44] = v[256:].transpose(1, 0, 2)
+    out = o.decode(q, cache, ws, np.array([[3, 1, 0, 0]]), np.array([300]))
+    for h in range(2):
+        kh, vh = o.dequant_record(cache[[3, 1], h])
+        kt = np.concatenate([kh[0].T, kh[1].T, k[256:, h].astype(np.float64)])
+        vt = np.concatenate([vh[0].T, vh[1].T, v[256:, h].astype(np.float64)])
+        assert np.allclose(out[0, 2 * h:2 * h + 2], o.attend(q[0, 2 * h:2 * h + 2], kt, vt), atol=1e-13)
+
+
+def test_append_builds_same_cache_as_prefill():
+    hkv = 2
+    k, v = synth.prefill_kv(300, hkv, seed=18)
+    bt = np.array([[2, 0, 3]], np.int32)
+    ws = np.zeros((1, hkv, 2, 128, 128), np.float16)
+    cache = np.zeros((4, hkv, o.RECORD_BYTES), np.uint8)
+    L = np.array([0])
+    for t in range(300):
+        ws, cache, L = o.append(k[t:t + 1], v[t:t + 1], L, bt, ws, cache)
+    assert L[0] == 300
+    ref = np.zeros_like(cache)
+    slots = np.concatenate([np.arange(128) + 2 * 128, np.arange(128) + 0 * 128])
+    o.quantize_into_cache(k[:256], v[:256], slots, ref)
+    assert np.array_equal(cache, ref)
+    assert np.array_equal(ws[0, :, 0, :44], k[256:].transpose(1, 0, 2))
+    assert np.array_equal(ws[0, :, 1, :44], v[256:].transpose(1, 0, 2))
