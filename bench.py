@@ -1,0 +1,412 @@
+"""Benchmark of the KVarN hot path on GB300.
+
+One step = one pass of the whole path over one batch:
+  1. kvarn_quantize_tiles: prefill quantize of 16 sequences x 16384 tokens, 8
+     kv-heads, head_dim 128 (1.074 GB of fp16 K+V in, 235 MB of records out);
+  2. kvarn_decode_attention: GQA decode (64 q-heads over 8 kv-heads) for 64
+     sequences x 16384 tokens over the packed cache (939.5 MB of records read).
+The cache holds K/V drawn and quantized like the prefill batch. Metric:
+(fp16 K+V bytes consumed + packed bytes read) / step time, in GB/s; per-kernel
+GB/s, decode tokens/s and fractions of the measured HBM peak are reported beside
+it. Every input is larger than L2 (129 MB), so no flush is needed between steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Under torchrun (N > 1) each rank runs the same per-GPU workload on its own GPU
+(weak scaling, no data-path collective); timing is the max over ranks.
+--impl reference times the CPU oracle (float64 NumPy restatement of the method)
+on a bounded sample of the same workload on this host's cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+PREFILL = dict(n_seqs=16, seq_len=16384, n_kv_heads=8, seed=1)
+DECODE = dict(n_seqs=64, seq_len=16384, n_kv_heads=8, n_q_heads=64, seed=2)
+RECORD = 14336
+WORKLOAD = "prefill_quantize_16x16k + decode_attn_64x16k_gqa64/8"
+
+
+def hbm_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out = ""
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in self.lines:
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, val in zip(names, f[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm.sort()
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- traffic from profiles
+def profiled_traffic(kernel: str):
+    """DRAM bytes per launch recorded in profiles/<kernel>.md for the current source
+    (null when the kernel source changed since the capture)."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}.md")
+    src = os.path.join(ROOT, "kv_cache_quantization_x128_gb300", "csrc",
+                       "quantize.cu" if kernel.startswith("quantize") else "decode.cu")
+    try:
+        text = open(path).read()
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    except OSError:
+        return None
+    m = re.search(r"dram_bytes_per_full_launch:\s*([0-9.eE+]+)", text)
+    s = re.search(r"source_sha256_16:\s*([0-9a-f]+)", text)
+    if not m or not s or s.group(1) != sha:
+        return None
+    return float(m.group(1))
+
+
+# ----------------------------------------------------------------------------- GPU arm
+def setup_gpu(torch, kv, synth, dev):
+    import numpy as np
+    p, d = PREFILL, DECODE
+    n_tok = p["n_seqs"] * p["seq_len"]
+    hkv = p["n_kv_heads"]
+    k, v = synth.prefill_kv(n_tok, hkv, seed=p["seed"])
+    kh = torch.from_numpy(k.view(np.int16)).view(torch.float16).pin_memory()
+    vh = torch.from_numpy(v.view(np.int16)).view(torch.float16).pin_memory()
+    kd, vd = kh.to(dev), vh.to(dev)
+    n_blocks = d["n_seqs"] * d["seq_len"] // 128
+    max_blocks = d["seq_len"] // 128
+    perm = synth.block_permutation(n_blocks, d["seed"])
+    cache = torch.zeros(n_blocks, hkv, RECORD, dtype=torch.uint8, device=dev)
+    meta = kv.make_meta(hkv, d["n_q_heads"], n_blocks, max_blocks_per_seq=max_blocks)
+    # fill the whole cache by quantizing the prefill batch into 4 disjoint block sets
+    per = n_tok // 128
+    slot_sets = []
+    for r in range(n_blocks // per):
+        blocks = perm[r * per:(r + 1) * per]
+        t = np.arange(n_tok, dtype=np.int64)
+        slot_sets.append(torch.from_numpy(blocks[t // 128] * 128 + t % 128).to(dev))
+        kv.kvarn_quantize_tiles(kd, vd, slot_sets[-1], cache, meta)
+    bt = torch.from_numpy(perm.reshape(d["n_seqs"], max_blocks).astype(np.int32)).to(dev)
+    lens = torch.full((d["n_seqs"],), d["seq_len"], dtype=torch.int32, device=dev)
+    q = torch.from_numpy(synth.queries(d["n_seqs"], d["n_q_heads"], d["seed"]).view(np.int16)).view(torch.float16)
+    qh = q.pin_memory()
+    qd = qh.to(dev)
+    out = torch.empty_like(qd)
+    scratch = torch.empty(kv.decode_scratch_bytes(meta, d["n_seqs"]), dtype=torch.uint8, device=dev)
+    torch.cuda.synchronize()
+    assert kv.kvarn_device_flags() == 0
+    return dict(kd=kd, vd=vd, kh=kh, vh=vh, slots=slot_sets[0], cache=cache, meta=meta, bt=bt, lens=lens,
+                qd=qd, qh=qh, out=out, out_h=torch.empty(out.shape, dtype=torch.float16).pin_memory(),
+                scratch=scratch, slots_h=slot_sets[0].cpu().pin_memory(), bt_h=bt.cpu().pin_memory(),
+                lens_h=lens.cpu().pin_memory())
+
+
+def run_gpu(args):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    import kv_cache_quantization_x128_gb300 as kv
+    import kvarn_synth as synth
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    S = setup_gpu(torch, kv, synth, dev)
+    stream = torch.cuda.current_stream()
+
+    def step(events=None):
+        if events:
+            events[0].record(stream)
+        kv.kvarn_quantize_tiles(S["kd"], S["vd"], S["slots"], S["cache"], S["meta"])
+        if events:
+            events[1].record(stream)
+        kv.kvarn_decode_attention(S["qd"], S["cache"], None, S["bt"], S["lens"], S["out"], S["scratch"], S["meta"])
+        if events:
+            events[2].record(stream)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t0.record(stream)
+        for i in range(args.steps):
+            step(evs[i])
+        t1.record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    total_ms = t0.elapsed_time(t1)
+    q_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    d_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    assert kv.kvarn_device_flags() == 0
+
+    # end to end through the C ABI with host buffers: inputs H2D, result D2H inside the region
+    def e2e_step():
+        S["kd"].copy_(S["kh"], non_blocking=True)
+        S["vd"].copy_(S["vh"], non_blocking=True)
+        S["slots"].copy_(S["slots_h"], non_blocking=True)
+        S["qd"].copy_(S["qh"], non_blocking=True)
+        S["bt"].copy_(S["bt_h"], non_blocking=True)
+        S["lens"].copy_(S["lens_h"], non_blocking=True)
+        step()
+        S["out_h"].copy_(S["out"], non_blocking=True)
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    e2e_ms = e0.elapsed_time(e1)
+    h2d = sum(S[n].numel() * S[n].element_size() for n in ("kh", "vh", "slots_h", "qh", "bt_h", "lens_h"))
+    d2h = S["out_h"].numel() * 2
+
+    # max over ranks
+    if world > 1:
+        t = torch.tensor([total_ms, e2e_ms, max(q_ms), max(d_ms)], dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms, e2e_ms = float(t[0]), float(t[1])
+
+    p, d = PREFILL, DECODE
+    q_bytes = p["n_seqs"] * p["seq_len"] * p["n_kv_heads"] * 128 * 2 * 2
+    d_bytes = d["n_seqs"] * (d["seq_len"] // 128) * d["n_kv_heads"] * RECORD
+    step_bytes = q_bytes + d_bytes
+    ms = total_ms / args.steps
+    peak, peak_kind = hbm_peak()
+    qm, dm = float(np.median(q_ms)), float(np.median(d_ms))
+    q_gbs, d_gbs = q_bytes / (qm * 1e-3) / 1e9, d_bytes / (dm * 1e-3) / 1e9
+    # dominant kernel roofline (time share): both kernels are reported, the larger share leads
+    kq = dict(bound="hbm", achieved=round(q_gbs, 1), peak=peak, unit="GB/s", frac=round(q_gbs / peak, 4),
+              traffic=profiled_traffic("quantize_kernel"), kernel="quantize_kernel",
+              algorithmic_bytes_per_launch=q_bytes, peak_kind=peak_kind)
+    kd = dict(bound="hbm", achieved=round(d_gbs, 1), peak=peak, unit="GB/s", frac=round(d_gbs / peak, 4),
+              traffic=profiled_traffic("decode_split_kernel"), kernel="decode_split_kernel+decode_merge_kernel",
+              algorithmic_bytes_per_launch=d_bytes, peak_kind=peak_kind)
+    dominant = kq if qm >= dm else kd
+    res = {
+        "metric": "quantize GB/s (fp16 KV in) + paged decode-attn GB/s, % of GB300 HBM peak",
+        "value": round(world * step_bytes / (ms * 1e-3) / 1e9, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "quantize": PREFILL, "decode": DECODE, "preset": "kvarn_k4v2_g128",
+                   "n_iters": 4, "l2": "every input > L2 (129 MB); no flush",
+                   "parallelism": f"replicas x{world}"},
+        "quantize_gbs": round(q_gbs, 1),
+        "quantize_frac_hbm": round(q_gbs / peak, 4),
+        "decode_gbs": round(d_gbs, 1),
+        "decode_frac_hbm": round(d_gbs / peak, 4),
+        "decode_tokens_per_s": round(d["n_seqs"] / (dm * 1e-3), 1),
+        "quantize_ms": round(qm, 4),
+        "decode_ms": round(dm, 4),
+        "compression_ratio": round(2 * 128 * 128 * 2 / RECORD, 4),
+        "roofline": dominant,
+        "roofline_kernels": [kq, kd],
+        "e2e": {"value": round(world * step_bytes / (e2e_ms / args.steps * 1e-3) / 1e9, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
+        "gpu_launches": args.steps * 3,
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+# ----------------------------------------------------------------------------- CPU oracle arms
+_ORACLE_SNIPPET = r"""
+import json, os, sys, time
+sys.path.insert(0, {root!r})
+import numpy as np
+import kvarn_synth as synth
+from oracle import kvarn_oracle as o
+budget = {budget}
+p, d = {p!r}, {d!r}
+# quantize sample: consecutive tiles of the prefill batch
+n_tiles = {n_q_tiles}
+k, v = synth.prefill_kv(n_tiles // p["n_kv_heads"] * 128, p["n_kv_heads"], seed=p["seed"])
+pairs = [(c, h) for c in range(n_tiles // p["n_kv_heads"]) for h in range(p["n_kv_heads"])]
+t0 = time.perf_counter()
+done_q = 0
+for b0 in range(0, len(pairs), 32):
+    part = pairs[b0:b0 + 32]
+    kt = np.stack([k[c * 128:(c + 1) * 128, h] for c, h in part])
+    vt = np.stack([v[c * 128:(c + 1) * 128, h] for c, h in part])
+    o.quantize_tiles(kt, vt)
+    done_q += len(part)
+    if time.perf_counter() - t0 > budget / 2:
+        break
+tq = time.perf_counter() - t0
+# decode sample: (sequence, kv-head) pairs over full 16384-token contexts of random records
+max_blocks = d["seq_len"] // 128
+recs = synth.random_records(max_blocks, d["seed"], 14336, 12288).reshape(max_blocks, 1, -1)
+q = synth.queries(1, d["n_q_heads"], d["seed"]).astype(np.float64)
+g = d["n_q_heads"] // d["n_kv_heads"]
+t0 = time.perf_counter()
+done_d = 0
+while time.perf_counter() - t0 < budget / 2 or done_d == 0:
+    o.decode_one(q[0, :g], recs, None, np.arange(max_blocks), d["seq_len"], 0)
+    done_d += 1
+td = time.perf_counter() - t0
+print(json.dumps(dict(tq=tq, nq=done_q, td=td, nd=done_d)))
+"""
+
+
+def _oracle_sample(seconds: float):
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    code = _ORACLE_SNIPPET.format(root=ROOT, budget=seconds, p=PREFILL, d=DECODE, n_q_tiles=4096)
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env)
+    if r.returncode != 0:
+        raise RuntimeError(r.stderr[-2000:])
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def cpu_baseline(seconds: float):
+    s = _oracle_sample(seconds)
+    q_bytes_per_tile = 2 * 128 * 128 * 2
+    d_bytes_per_pair = (DECODE["seq_len"] // 128) * RECORD
+    # the step's time on the oracle, extrapolated from the measured per-unit rates
+    n_q_units = PREFILL["n_seqs"] * PREFILL["seq_len"] // 128 * PREFILL["n_kv_heads"]
+    n_d_units = DECODE["n_seqs"] * DECODE["n_kv_heads"]
+    t_step = n_q_units * s["tq"] / s["nq"] + n_d_units * s["td"] / s["nd"]
+    step_bytes = n_q_units * q_bytes_per_tile + n_d_units * d_bytes_per_pair
+    return {"value": round(step_bytes / t_step / 1e9, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": (f"{s['nq']} tile-heads quantized ({s['tq']:.1f} s) and {s['nd']} (sequence, kv-head) "
+                       f"decodes at 16384 tokens ({s['td']:.1f} s) on 1 host core, float64 NumPy; the step "
+                       f"time is extrapolated from these per-unit rates"),
+            "quantize_gbs": round(s["nq"] * q_bytes_per_tile / s["tq"] / 1e9, 6),
+            "decode_gbs": round(s["nd"] * d_bytes_per_pair / s["td"] / 1e9, 6)}
+
+
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    per_step = max(2.0, args.cpu_seconds / max(1, args.steps))
+    for _ in range(args.warmup):
+        _oracle_sample(1.0)
+    vals = []
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        vals.append(cpu_baseline(per_step))
+    wall = time.perf_counter() - t0
+    import statistics
+    value = statistics.median(v["value"] for v in vals)
+    step_bytes = (PREFILL["n_seqs"] * PREFILL["seq_len"] * PREFILL["n_kv_heads"] * 128 * 4
+                  + DECODE["n_seqs"] * (DECODE["seq_len"] // 128) * DECODE["n_kv_heads"] * RECORD)
+    res = {
+        "impl": "reference",
+        "metric": "quantize GB/s (fp16 KV in) + paged decode-attn GB/s, % of GB300 HBM peak",
+        "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(step_bytes / (value * 1e9) * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "quantize": PREFILL, "decode": DECODE, "preset": "kvarn_k4v2_g128"},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": vals[0]["sample"]},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "wall_s": round(wall, 1),
+    }
+    print(json.dumps(res), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=20.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

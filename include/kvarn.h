@@ -1,0 +1,202 @@
+/*
+ * kvarn.h - C ABI of libkvarn: KVarN per-tile KV-cache quantization and paged
+ * decode attention over the quantized cache, for NVIDIA GB300 (sm_103a).
+ *
+ * Method (KVarN README, huawei-csl/KVarN, "How KVarN works", stages 1-4): the KV
+ * cache is quantized in tiles of 128 tokens per kv-head. Each fp16 tile
+ * X [128 channels x 128 tokens] is (2) rotated along channels by an orthonormal
+ * Hadamard matrix H, (3) variance-normalised by alternating column-wise and
+ * row-wise std normalisation in log space (Sinkhorn style), keeping the row scale
+ * vector r and column scale vector c, and (4) quantized by asymmetric
+ * round-to-nearest: keys at 4 bits with (scale, zero) per channel, values at 2
+ * bits with (scale, zero) per token. The preset is kvarn_k4v2_g128 with block
+ * size fixed at 128 (one paged block = one tile) and float16 compute (README,
+ * quick start and note). Decode attention reads the packed blocks through the
+ * block table, re-applies the scales on read (stage 4), rotates q by the same H
+ * (scores are unchanged by an orthonormal rotation, stage 2) and un-rotates the
+ * output by H^T. A partial last tile stays in a small fp16 decode workspace until
+ * it holds 128 tokens (README, capacity tip: a small fixed decode workspace).
+ *
+ * Readings fixed by this library where the pages are silent:
+ *   H = Sylvester Hadamard of order 128 / sqrt(128) (natural order, H = H^T).
+ *   Normalisation: n_iters iterations (preset 4), each a column pass then a row
+ *   pass; variance is the population variance about the mean; eps is added to
+ *   the variance; data are divided, not centred.
+ *   r, c, s clamped to [2^-14, 65504] and z to [-65504, 65504], then rounded to
+ *   fp16 (nearest even). z = fp16(group min), s = fp16((group max - z)/(2^b-1)),
+ *   code = clamp(floor((y - z)/s + 1/2), 0, 2^b - 1), y = X_r / (r_i c_j).
+ *   Decode: softmax scale 1/sqrt(128); q-head h uses kv-head h / (Hq/Hkv); no
+ *   mask (all seq_len tokens are attended).
+ *
+ * ---------------------------------------------------------------------------
+ * Packed record: 14336 bytes per (physical block, kv-head). The cache is
+ * uint8 [num_blocks][num_kv_heads][14336], device memory owned by the caller.
+ *   [    0,  8192)  K codes, 4 bits, token-major: token t owns bytes
+ *                   [64t, 64t+64) = four 16-byte groups g = (i>>1)&3, each four
+ *                   little-endian 32-bit words w = i>>5; channel i sits in nibble
+ *                   p = 4(i&1) + 2((i>>4)&1) + ((i>>3)&1) (bits 4p..4p+3) of word w.
+ *   [ 8192, 12288)  V codes, 2 bits, channel-major: channel i lives in 512-byte
+ *                   panel i>>4; 16-byte cell (i&7)*4 + ((t>>1)&3) of the panel
+ *                   holds 8 bytes for the channel with bit 3 clear followed by 8
+ *                   bytes for its partner i|8; each 8 bytes are two words
+ *                   u = t>>6; token t sits in crumb
+ *                   p = 8(t&1) + 2((t>>4)&3) + ((t>>3)&1) (bits 2p..2p+1).
+ *   [12288, 13312)  K metadata, fp16 [4][128]: r (per channel), c (per token),
+ *                   s (per channel), z (per channel).
+ *   [13312, 14336)  V metadata, fp16 [4][128]: r (per channel), c (per token),
+ *                   s (per token), z (per token).
+ * Dequantised rotated tile: X_r[i][j] = r_i c_j (code_ij * s + z), (s, z) taken
+ * per channel i for K and per token j for V; the tile is H * X_r.
+ * The code orders follow the register fragments of the decode kernel's
+ * m16n8k16 tensor-core operands, so a thread's operands are contiguous bytes.
+ *
+ * Decode workspace: fp16 [max_seqs][num_kv_heads][2 (K,V)][128 tokens][128 ch],
+ * raw (unrotated, unquantised) tokens of each sequence's partial last tile;
+ * token L of a sequence is at slot L % 128.
+ * ---------------------------------------------------------------------------
+ * Conventions for every call:
+ *   - fp16 buffers are IEEE binary16 bit patterns (uint16_t), device memory.
+ *   - All pointers are device pointers unless stated; all must be 16-byte
+ *     aligned (KVARN_EALIGN otherwise). The library allocates nothing: every
+ *     buffer is allocated and owned by the caller.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream). Work is queued
+ *     asynchronously; a KVARN_OK return means the launches were queued.
+ *   - Argument errors are detected on the host before anything is launched and
+ *     leave device memory untouched. Data errors that only the device can see
+ *     (a block index outside [0, num_blocks), a slot mapping that does not fill
+ *     whole blocks, a sequence longer than its block table) make the kernels
+ *     skip the affected tile and set a bit in a device flag word, read and
+ *     cleared by kvarn_device_flags().
+ *   - The calls keep no host state besides the per-thread error message; the
+ *     device flag word is shared by every call on a device.
+ */
+#ifndef KVARN_H
+#define KVARN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define KVARN_API __attribute__((visibility("default")))
+#else
+#define KVARN_API
+#endif
+
+#define KVARN_HEAD_DIM 128
+#define KVARN_BLOCK_SIZE 128
+#define KVARN_RECORD_BYTES 14336
+#define KVARN_MAX_GQA_GROUP 8
+
+typedef enum {
+  KVARN_OK = 0,
+  KVARN_EINVAL = 1,        /* null pointer, negative size, inconsistent sizes   */
+  KVARN_EUNSUPPORTED = 2,  /* head_dim/block_size/bits/group outside the preset */
+  KVARN_EALIGN = 3,        /* a pointer is not 16-byte aligned                   */
+  KVARN_ESCRATCH = 4,      /* decode scratch smaller than the size query         */
+  KVARN_ECUDA = 5          /* a CUDA call or launch failed (see kvarn_last_error) */
+} kvarn_status;
+
+/* Device flag bits reported by kvarn_device_flags(). */
+#define KVARN_FLAG_BAD_SLOTS 0x1u      /* prefill chunk not one whole block: skipped  */
+#define KVARN_FLAG_BAD_BLOCK 0x2u      /* block index outside [0, num_blocks): skipped */
+#define KVARN_FLAG_BAD_LENGTH 0x4u     /* seq_len > max_blocks_per_seq*128: clipped   */
+#define KVARN_FLAG_WAIT_TIMEOUT 0x8u   /* a bounded wait on a copy gave up            */
+
+typedef struct {
+  int32_t num_kv_heads;       /* Hkv >= 1                                         */
+  int32_t num_q_heads;        /* Hq, a multiple of Hkv with Hq/Hkv <= 8           */
+  int32_t head_dim;           /* must be 128                                      */
+  int32_t block_size;         /* must be 128                                      */
+  int32_t k_bits;             /* must be 4                                        */
+  int32_t v_bits;             /* must be 2                                        */
+  int32_t n_iters;            /* normalisation iterations, 1..16 (preset 4)       */
+  float eps;                  /* added to each variance, > 0 (preset 1e-6)        */
+  int64_t num_blocks;         /* physical blocks in the cache                     */
+  int32_t max_blocks_per_seq; /* row length of block_tables                       */
+  int32_t reserved;           /* must be 0                                        */
+} kvarn_meta;
+
+/* Bytes of one (block, kv-head) record: 14336. */
+KVARN_API size_t kvarn_record_bytes(void);
+
+/* Bytes of the whole paged cache: num_blocks * num_kv_heads * 14336; 0 if meta is
+ * invalid. */
+KVARN_API size_t kvarn_cache_bytes(const kvarn_meta* meta);
+
+/* Bytes of a decode workspace for `max_seqs` sequences:
+ * max_seqs * num_kv_heads * 2 * 128 * 128 * 2; 0 if meta is invalid. */
+KVARN_API size_t kvarn_workspace_bytes(const kvarn_meta* meta, int32_t max_seqs);
+
+/* Bytes of device scratch kvarn_decode_attention needs for `n_seqs` sequences
+ * (partial softmax states of the context splits); depends on max_blocks_per_seq.
+ * 0 if meta is invalid. */
+KVARN_API size_t kvarn_decode_scratch_bytes(const kvarn_meta* meta, int32_t n_seqs);
+
+/*
+ * Prefill write. Quantizes whole tiles of fresh K/V into the paged cache
+ * (stages 2-4 of "How KVarN works").
+ *   k, v          fp16 [n_tokens][num_kv_heads][128], token-major (vLLM layout).
+ *   slot_mapping  int64 [n_tokens]; every run of 128 tokens [t0, t0+128) must map
+ *                 to one block at consecutive offsets: slot[t0+k] = 128*b + k.
+ *                 A run that does not, or whose block b is outside
+ *                 [0, num_blocks), is skipped and flagged.
+ *   n_tokens      >= 0 and a multiple of 128 (partial tiles belong in the decode
+ *                 workspace, see kvarn_append_decode).
+ *   cache         uint8 [num_blocks][num_kv_heads][14336]; written records only.
+ */
+KVARN_API kvarn_status kvarn_quantize_tiles(const uint16_t* k, const uint16_t* v,
+                                  const int64_t* slot_mapping, int64_t n_tokens,
+                                  uint8_t* cache, const kvarn_meta* meta, void* stream);
+
+/*
+ * Decode-step write. For each sequence s with L = seq_lens[s] stored tokens,
+ * writes the new token into workspace[s][h][*][L % 128][*]; when that completes
+ * the partial tile (L % 128 == 127) the tile is quantized into block
+ * block_tables[s][L / 128] for every kv-head.
+ *   k_new, v_new  fp16 [n_seqs][num_kv_heads][128].
+ *   seq_lens      int32 [n_seqs], lengths before the append, >= 0.
+ *   seq_lens_out  int32 [n_seqs] or NULL: receives seq_lens[s] + 1. Must not
+ *                 alias seq_lens.
+ *   block_tables  int32 [n_seqs][max_blocks_per_seq].
+ *   workspace     fp16, see the workspace layout above; sequence s uses row s.
+ */
+KVARN_API kvarn_status kvarn_append_decode(const uint16_t* k_new, const uint16_t* v_new,
+                                 const int32_t* seq_lens, int32_t* seq_lens_out,
+                                 const int32_t* block_tables, int32_t n_seqs,
+                                 uint16_t* workspace, uint8_t* cache,
+                                 const kvarn_meta* meta, void* stream);
+
+/*
+ * Decode attention for one new query per sequence over its L = seq_lens[s]
+ * tokens: floor(L/128) packed tiles read through block_tables, plus L % 128
+ * workspace tokens. GQA: q-head h reads kv-head h / (Hq/Hkv).
+ *   q             fp16 [n_seqs][num_q_heads][128].
+ *   n_seqs        0..65535.
+ *   workspace     fp16 workspace (may be NULL only if every L % 128 == 0; tail
+ *                 tokens of a sequence without a workspace are not attended and
+ *                 KVARN_FLAG_BAD_LENGTH is set).
+ *   out           fp16 [n_seqs][num_q_heads][128]; a sequence with L == 0 gets 0.
+ *   scratch       device buffer of >= kvarn_decode_scratch_bytes(meta, n_seqs).
+ */
+KVARN_API kvarn_status kvarn_decode_attention(const uint16_t* q, const uint8_t* cache,
+                                    const uint16_t* workspace, const int32_t* block_tables,
+                                    const int32_t* seq_lens, int32_t n_seqs, uint16_t* out,
+                                    void* scratch, size_t scratch_bytes,
+                                    const kvarn_meta* meta, void* stream);
+
+/* Copies the device flag word of the current device to *flags (host pointer)
+ * after synchronising `stream`, then clears it. */
+KVARN_API kvarn_status kvarn_device_flags(uint32_t* flags, void* stream);
+
+/* Message of the last error returned on the calling host thread ("" if none). */
+KVARN_API const char* kvarn_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVARN_H */

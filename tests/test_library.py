@@ -1,0 +1,115 @@
+"""libkvarn loads, exports every entry point declared in include/kvarn.h, and rejects
+bad arguments on the host before touching the GPU (these calls return before any
+CUDA call, so they run without a GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER_DIR = os.path.join(ROOT, "include")
+
+
+@pytest.fixture(scope="module")
+def kv():
+    import __graft_entry__
+    if not os.path.exists(os.path.join(ROOT, "kv_cache_quantization_x128_gb300", "libkvarn.so")):
+        __graft_entry__.build()
+    import kv_cache_quantization_x128_gb300 as kv
+    return kv
+
+
+def _declared_functions():
+    names = []
+    for fn in sorted(os.listdir(HEADER_DIR)):
+        if fn.endswith(".h"):
+            text = open(os.path.join(HEADER_DIR, fn)).read()
+            names += re.findall(r"KVARN_API\s+[\w\s\*]+?\b(kvarn_\w+)\s*\(", text)
+    return names
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    for must in ("kvarn_quantize_tiles", "kvarn_append_decode", "kvarn_decode_attention",
+                 "kvarn_decode_scratch_bytes", "kvarn_last_error"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(kv):
+    lib = ctypes.CDLL(kv.LIB_PATH)
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+    assert set(_declared_functions()) <= set(kv._SIGS)
+
+
+def test_meta_struct_layout(kv):
+    assert ctypes.sizeof(kv.KvarnMeta) == 48
+    assert kv.KvarnMeta.num_blocks.offset == 32
+
+
+def test_size_queries(kv):
+    m = kv.make_meta(8, 64, num_blocks=2048, max_blocks_per_seq=128)
+    assert kv.record_bytes() == 14336
+    assert kv.cache_bytes(m) == 2048 * 8 * 14336
+    assert kv.workspace_bytes(m, 4) == 4 * 8 * 2 * 128 * 128 * 2
+    assert kv.decode_scratch_bytes(m, 64) > 0
+    bad = kv.make_meta(8, 64, 16)
+    bad.head_dim = 64
+    assert kv.cache_bytes(bad) == 0
+
+
+def _raw(kv, name):
+    return getattr(kv._lib, name)
+
+
+A = ctypes.c_void_p(0x10000)          # aligned fake device address (never dereferenced)
+MIS = ctypes.c_void_p(0x10008)        # not 16-byte aligned
+
+
+@pytest.mark.parametrize("field,value,status", [
+    ("head_dim", 64, 2), ("block_size", 16, 2), ("k_bits", 2, 2), ("v_bits", 4, 2),
+    ("num_q_heads", 12, 1), ("n_iters", 0, 1), ("n_iters", 17, 1), ("num_kv_heads", 0, 1),
+    ("reserved", 1, 1),
+])
+def test_quantize_rejects_bad_meta(kv, field, value, status):
+    m = kv.make_meta(8, 64, 16)
+    setattr(m, field, value)
+    st = _raw(kv, "kvarn_quantize_tiles")(A, A, A, 128, A, ctypes.byref(m), None)
+    assert st == status
+    assert kv._lib.kvarn_last_error().decode()
+
+
+def test_group_larger_than_eight_unsupported(kv):
+    m = kv.make_meta(2, 32, 16)
+    assert _raw(kv, "kvarn_decode_attention")(A, A, A, A, A, 1, A, A, 1 << 20, ctypes.byref(m), None) == 2
+
+
+def test_quantize_rejects_partial_tiles_and_nulls(kv):
+    m = kv.make_meta(8, 64, 16)
+    q = _raw(kv, "kvarn_quantize_tiles")
+    assert q(A, A, A, 100, A, ctypes.byref(m), None) == 1          # not a multiple of 128
+    assert q(A, A, A, -128, A, ctypes.byref(m), None) == 1
+    assert q(None, A, A, 128, A, ctypes.byref(m), None) == 1       # NULL k
+    assert q(A, MIS, A, 128, A, ctypes.byref(m), None) == 3        # misaligned v
+    assert q(A, A, A, 128, A, None, None) == 1                     # NULL meta
+    assert q(A, A, A, 0, A, ctypes.byref(m), None) == 0            # nothing to do
+
+
+def test_append_rejects_aliasing_and_nulls(kv):
+    m = kv.make_meta(8, 64, 16, max_blocks_per_seq=4)
+    ap = _raw(kv, "kvarn_append_decode")
+    assert ap(A, A, A, A, A, 4, A, A, ctypes.byref(m), None) == 1   # seq_lens_out aliases seq_lens
+    assert ap(A, A, None, None, A, 4, A, A, ctypes.byref(m), None) == 1
+    assert ap(A, A, A, None, A, -1, A, A, ctypes.byref(m), None) == 1
+    m0 = kv.make_meta(8, 64, 16, max_blocks_per_seq=0)
+    assert ap(A, A, A, None, A, 4, A, A, ctypes.byref(m0), None) == 1
+
+
+def test_decode_rejects_small_scratch(kv):
+    m = kv.make_meta(8, 64, 1024, max_blocks_per_seq=128)
+    need = kv.decode_scratch_bytes(m, 4)
+    dec = _raw(kv, "kvarn_decode_attention")
+    assert dec(A, A, A, A, A, 4, A, A, need - 16, ctypes.byref(m), None) == 4
+    assert dec(A, A, A, A, A, 4, A, None, need, ctypes.byref(m), None) == 1     # NULL scratch
+    assert dec(A, A, A, A, A, 4, None, A, need, ctypes.byref(m), None) == 1     # NULL out
