@@ -1,55 +1,56 @@
-// KVarN tile quantization kernels (stages 2-4 of "How KVarN works", KVarN README):
+// KVarN tile quantization (KVarN README, "How KVarN works", stages 2-4):
 // Hadamard rotation along channels, log-space column/row variance normalisation,
 // asymmetric round-to-nearest (4-bit keys per channel, 2-bit values per token) and
 // packing into the 14336-byte record documented in kvarn.h.
 //
-// One persistent CTA per SM (256 threads) walks (tile, kv-head) work items. The
-// next item's 2 x 128 token rows are fetched by 1-D bulk copies (TMA) into a
-// second shared-memory buffer while the current one is processed; the finished
-// record is staged in shared memory and written by one 14336-byte bulk store.
-//
-// Thread roles. Thread t pairs with t^1 (adjacent lanes): e = 16*warp + lane/2,
-// half = lane & 1.
-//   column role: token j = e, channels [64*half, 64*half+64)  -> registers xc[64]
-//   row role   : channel i = e, tokens [64*half, 64*half+64) -> registers xr[64]
-// Both copies of the rotated tile live in registers, so every column pass and
-// every row pass is a thread-local loop plus one shuffle with the partner lane.
+// One persistent CTA per SM, 512 threads in two independent 8-warp groups: group 0
+// quantizes the K tile and group 1 the V tile of each (block, kv-head) work item.
+// Per item and group:
+//   1. cp.async copies the next item's 128 token rows (fp16) into the group's spare
+//      shared-memory buffer, in the no-swizzle K-major canonical UMMA layout;
+//   2. one thread issues tcgen05.mma twice over K = 128: D1 = H X^T (TMEM lanes =
+//      channels, columns = tokens) and D2 = X H (lanes = tokens, columns =
+//      channels), with H the +-1 Sylvester matrix (exact in fp16) and fp32
+//      accumulation; the 1/sqrt(128) factor is folded into the statistics;
+//   3. each column pass reads D2 and each row pass reads D1 straight from TMEM
+//      (tcgen05.ld 16x64b: two threads per line, 64 values each), so both passes
+//      are thread-local loops plus one shuffle with the partner thread;
+//   4. fp16 scales, RTN, packing into a shared-memory stage, and two bulk stores of
+//      the group's part of the record.
+// The groups share only the Hadamard operand and the TMEM allocation (256 columns
+// each), so one group's MMA latency and barriers overlap the other's arithmetic.
 #include "kvarn_common.cuh"
 #include "kvarn_launch.h"
+#include "kvarn_tc.cuh"
 
 namespace kvarn {
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kRowPitch = 272;                     // padded smem row of 256 B of fp16
-constexpr int kInTile = kB * kRowPitch;            // 34816 B per (tensor, tile)
-constexpr int kVecPad = 132;                       // 128 floats + 4 words of padding
+constexpr int kGroupThreads = 256;
+constexpr int kThreads = 2 * kGroupThreads;
+constexpr int kTileOp = kB * kD * 2;              // 32768 B: one fp16 128x128 operand
+constexpr int kStageK = 8192 + 1024;              // K codes + K metadata
+constexpr int kStageV = 4096 + 1024;              // V codes + V metadata
+constexpr int kVec = 136;                         // parity-split vector (even at 0, odd at 68)
+constexpr int kNumVec = 6;                        // a, b, g (2^-3.5/r), hc (1/c), w, c0
 
-// dynamic shared memory layout (bytes)
-constexpr int kOffIn = 0;                                  // [2 bufs][K,V][kInTile]
-constexpr int kOffT = kOffIn + 4 * kInTile;                // fp32 [128][128] transpose
-constexpr int kOffStage = kOffT + kD * kB * 4;             // packed record
-constexpr int kOffA = kOffStage + kRec;                    // a_i (inverse row scales)
-constexpr int kOffB = kOffA + kVecPad * 4;                 // b_j (inverse column scales)
-constexpr int kOffG = kOffB + kVecPad * 4;                 // 1 / r_i (fp16 r)
-constexpr int kOffHc = kOffG + kVecPad * 4;                // 1 / c_j (fp16 c)
-constexpr int kOffW = kOffHc + kVecPad * 4;                // per group: G*inv_s or inv_s
-constexpr int kOffC0 = kOffW + kVecPad * 4;                // per group: 0.5 - z*inv_s
-constexpr int kOffBar = kOffC0 + kVecPad * 4;              // 2 mbarriers
-constexpr int kOffDst = kOffBar + 16;                      // int64 dst record per buffer
-constexpr int kSmemBytes = kOffDst + 16;
+constexpr int kOffH = 0;
+constexpr int kOffIn = kOffH + kTileOp;                        // [group][buf] operands
+constexpr int kOffStageK = kOffIn + 4 * kTileOp;               // [buf]
+constexpr int kOffStageV = kOffStageK + 2 * kStageK;           // [buf]
+constexpr int kOffVec = kOffStageV + 2 * kStageV;              // [group][vector][kVec] fp32
+constexpr int kOffBar = kOffVec + 2 * kNumVec * kVec * 4;      // mma barriers [group]
+constexpr int kOffTmem = kOffBar + 16;
+constexpr int kSmemBytes = kOffTmem + 16;
+static_assert(kSmemBytes <= 232448, "quantize shared memory");
+static_assert(kOffIn % 1024 == 0 && kOffStageK % 16 == 0 && kOffStageV % 16 == 0 && kOffVec % 16 == 0, "align");
 
-static_assert(kSmemBytes <= 232448, "quantize smem");
-static_assert(kOffT % 16 == 0 && kOffStage % 16 == 0 && kOffBar % 8 == 0, "align");
+enum { kVA = 0, kVB = 1, kVG = 2, kVHc = 3, kVW = 4, kVC0 = 5 };
 
-__device__ __forceinline__ int vpad(int i) { return i + ((i >> 6) << 2); }
+// position of entry e in a parity-split vector
+__device__ __forceinline__ int ps(int e) { return (e & 1) * 68 + (e >> 1); }
 
-// Swizzled float index of element (token j, channel i) in the transpose buffer.
-__device__ __forceinline__ int tidx(int j, int i) {
-  const int c = i >> 2;
-  const int x = (((j & 3) << 1) | ((c >> 4) & 1)) ^ (((j >> 6) & 1) << 2);
-  return j * kD + ((c ^ x) << 2) + (i & 3);
-}
+constexpr float kVarScale = 1.0f / 128.0f;   // (2^-3.5)^2: statistics of the +-1 transform
 
 // ------------------------------------------------------------------ work sources
 struct PrefillSource {
@@ -60,29 +61,37 @@ struct PrefillSource {
   int hkv;
   int64_t num_blocks;
 
-  // Warp-wide: validates item `w` and returns its record index (block*hkv + head)
-  // or -1 (skip); sets the K/V row base pointers and row stride in elements.
-  __device__ int64_t resolve(int64_t w, const uint16_t*& kb, const uint16_t*& vb, int64_t& stride,
-                             unsigned* flags) const {
-    const int lane = threadIdx.x & 31;
+  // Row 0 of tensor `g` (0 = K, 1 = V) of item w and the row stride (elements);
+  // false if the item needs no copy.
+  __device__ bool rows(int64_t w, int g, const uint16_t*& base, int64_t& stride) const {
     const int64_t chunk = w / hkv;
     const int h = static_cast<int>(w - chunk * hkv);
-    const int64_t t0 = chunk * kB;
-    const int64_t base = slot[t0];
-    bool ok = base >= 0 && (base % kB) == 0 && base / kB < num_blocks;
-    for (int m = 0; m < 4; ++m) {
-      const int r = lane + 32 * m;
-      ok = ok && slot[t0 + r] == base + r;
-    }
-    ok = __all_sync(0xffffffffu, ok);
+    stride = static_cast<int64_t>(hkv) * kD;
+    base = (g ? v : k) + chunk * kB * stride + static_cast<int64_t>(h) * kD;
+    return true;
+  }
+  // Slot entries this thread checks for item w, loaded one item ahead of use.
+  struct Check {
+    int64_t base = -1, mine = -1;
+  };
+  __device__ Check prepare(int64_t w, int gt) const {
+    const int64_t t0 = (w / hkv) * kB;
+    Check c;
+    c.base = slot[t0];
+    c.mine = gt < kB ? slot[t0 + gt] : c.base + gt;
+    return c;
+  }
+  // Group-wide (all 256 threads, barrier `bar_id`): record index of item w or -1.
+  __device__ int64_t resolve(int64_t w, const Check& c, int gt, int bar_id, unsigned* flags) const {
+    const int64_t chunk = w / hkv;
+    const int h = static_cast<int>(w - chunk * hkv);
+    bool ok = c.base >= 0 && (c.base % kB) == 0 && c.base / kB < num_blocks && c.mine == c.base + gt;
+    ok = named_bar_and(bar_id, kGroupThreads, ok);
     if (!ok) {
-      if (lane == 0) raise_flag(flags, KVARN_FLAG_BAD_SLOTS);
+      if (gt == 0) raise_flag(flags, KVARN_FLAG_BAD_SLOTS);
       return -1;
     }
-    stride = static_cast<int64_t>(hkv) * kD;
-    kb = k + t0 * stride + static_cast<int64_t>(h) * kD;
-    vb = v + t0 * stride + static_cast<int64_t>(h) * kD;
-    return (base / kB) * hkv + h;
+    return (c.base / kB) * hkv + h;
   }
 };
 
@@ -95,309 +104,260 @@ struct AppendSource {
   int max_blocks;
   int64_t num_blocks;
 
-  __device__ int64_t resolve(int64_t w, const uint16_t*& kb, const uint16_t*& vb, int64_t& stride,
-                             unsigned* flags) const {
-    const int lane = threadIdx.x & 31;
+  __device__ bool completes(int64_t w) const {
+    const int L = seq_lens[w / hkv];
+    return L >= 0 && (L % kB) == kB - 1;
+  }
+  __device__ bool rows(int64_t w, int g, const uint16_t*& base, int64_t& stride) const {
+    if (!completes(w)) return false;
     const int64_t s = w / hkv;
     const int h = static_cast<int>(w - s * hkv);
-    const int L = seq_lens[s];
-    if (L < 0 || (L % kB) != kB - 1) return -1;  // this token does not complete a tile
-    const int bi = L / kB;
+    stride = kD;
+    base = ws + ((s * hkv + h) * 2 + g) * static_cast<int64_t>(kB * kD);
+    return true;
+  }
+  struct Check {};
+  __device__ Check prepare(int64_t, int) const { return Check{}; }
+  __device__ int64_t resolve(int64_t w, const Check&, int gt, int bar_id, unsigned* flags) const {
+    named_bar(bar_id, kGroupThreads);   // copies of the item are visible to the group
+    if (!completes(w)) return -1;
+    const int64_t s = w / hkv;
+    const int h = static_cast<int>(w - s * hkv);
+    const int bi = seq_lens[s] / kB;
     if (bi >= max_blocks) {
-      if (lane == 0) raise_flag(flags, KVARN_FLAG_BAD_LENGTH);
+      if (gt == 0) raise_flag(flags, KVARN_FLAG_BAD_LENGTH);
       return -1;
     }
     const int64_t blk = block_tables[s * max_blocks + bi];
     if (blk < 0 || blk >= num_blocks) {
-      if (lane == 0) raise_flag(flags, KVARN_FLAG_BAD_BLOCK);
+      if (gt == 0) raise_flag(flags, KVARN_FLAG_BAD_BLOCK);
       return -1;
     }
-    stride = kD;
-    kb = ws + ((s * hkv + h) * 2 + 0) * static_cast<int64_t>(kB * kD);
-    vb = ws + ((s * hkv + h) * 2 + 1) * static_cast<int64_t>(kB * kD);
     return blk * hkv + h;
   }
 };
 
-// Warp 0: resolve item `w` into buffer `buf` and start its copies.
+// Group `g` copies the 128 rows of its tensor for item w into `dst` (canonical layout).
 template <class Src>
-__device__ void prefetch(const Src& src, int64_t w, int buf, uint8_t* smem, unsigned* flags) {
-  const int lane = threadIdx.x & 31;
-  const uint16_t* kb = nullptr;
-  const uint16_t* vb = nullptr;
-  int64_t stride = 0;
-  const int64_t dst = src.resolve(w, kb, vb, stride, flags);
-  int64_t* s_dst = reinterpret_cast<int64_t*>(smem + kOffDst);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
-  if (lane == 0) s_dst[buf] = dst;
-  if (dst < 0) return;
-  if (lane == 0) mbar_arrive_expect_tx(&bars[buf], 2u * kB * kD * 2u);
-  __syncwarp();
-  uint8_t* in_k = smem + kOffIn + (buf * 2 + 0) * kInTile;
-  uint8_t* in_v = smem + kOffIn + (buf * 2 + 1) * kInTile;
-  for (int m = 0; m < 4; ++m) {
-    const int r = lane + 32 * m;
-    bulk_g2s(in_k + r * kRowPitch, kb + r * stride, kD * 2, &bars[buf]);
-    bulk_g2s(in_v + r * kRowPitch, vb + r * stride, kD * 2, &bars[buf]);
+__device__ __forceinline__ void load_tile(const Src& src, int64_t w, int g, int gt, uint8_t* dst) {
+  const uint16_t* base;
+  int64_t stride;
+  if (!src.rows(w, g, base, stride)) return;
+  const int gw = gt >> 5, t = gt & 31;
+#pragma unroll
+  for (int m = 0; m < 8; ++m) {
+    const int combo = gw + 8 * m;                // 0..63
+    const int j = 8 * (combo & 15) + (t & 7);    // token (row)
+    const int c8 = 4 * (combo >> 4) + (t >> 3);  // 16-byte chunk along channels
+    cp_async16(dst + canon_offset(j, 8 * c8), base + j * stride + 8 * c8);
   }
 }
 
-__device__ __forceinline__ void h8_to_f(const uint4& u, float* f) {
-  const __half2* h = reinterpret_cast<const __half2*>(&u);
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const float2 t = __half22float2(h[q]);
-    f[2 * q] = t.x;
-    f[2 * q + 1] = t.y;
-  }
+__device__ __forceinline__ void load_vec4(const float* v, int p, int q, float& a0, float& a1, float& a2, float& a3) {
+  const float4 w = reinterpret_cast<const float4*>(v + p * 68)[q];
+  a0 = w.x; a1 = w.y; a2 = w.z; a3 = w.w;
 }
 
-// Column pass (col role, data xc over channels, weights w = a) or row pass (row
-// role, data xr over tokens, weights w = b): returns the population variance of
-// w_k * x_k over the 128 entries of this thread's line (both halves).
-__device__ __forceinline__ float line_variance(const float* x, const float* wvec, int half) {
-  const float4* w4 = reinterpret_cast<const float4*>(wvec + vpad(64 * half));
-  float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
+// Population variance over the pair's 128 values of w_e * x_e, where the thread
+// holds entries e = p + 2k, k < 64, and w is a parity-split vector.
+__device__ __forceinline__ float pair_variance(const float (&x)[64], const float* wv, int p) {
+  float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
 #pragma unroll
   for (int q = 0; q < 16; ++q) {
-    const float4 w = w4[q];
-    p0 = fmaf(w.x, x[4 * q + 0], p0);
-    p1 = fmaf(w.y, x[4 * q + 1], p1);
-    p2 = fmaf(w.z, x[4 * q + 2], p2);
-    p3 = fmaf(w.w, x[4 * q + 3], p3);
+    float w0, w1, w2, w3;
+    load_vec4(wv, p, q, w0, w1, w2, w3);
+    s0 = fmaf(w0, x[4 * q + 0], s0);
+    s1 = fmaf(w1, x[4 * q + 1], s1);
+    s2 = fmaf(w2, x[4 * q + 2], s2);
+    s3 = fmaf(w3, x[4 * q + 3], s3);
   }
-  float s1 = (p0 + p1) + (p2 + p3);
-  s1 += __shfl_xor_sync(0xffffffffu, s1, 1);
-  const float mean = s1 * (1.0f / 128.0f);
-  p0 = p1 = p2 = p3 = 0.f;
+  float s = (s0 + s1) + (s2 + s3);
+  s += __shfl_xor_sync(0xffffffffu, s, 2);
+  const float mean = s * (1.0f / 128.0f);
+  s0 = s1 = s2 = s3 = 0.f;
 #pragma unroll
   for (int q = 0; q < 16; ++q) {
-    const float4 w = w4[q];
-    const float t0 = fmaf(w.x, x[4 * q + 0], -mean);
-    const float t1 = fmaf(w.y, x[4 * q + 1], -mean);
-    const float t2 = fmaf(w.z, x[4 * q + 2], -mean);
-    const float t3 = fmaf(w.w, x[4 * q + 3], -mean);
-    p0 = fmaf(t0, t0, p0);
-    p1 = fmaf(t1, t1, p1);
-    p2 = fmaf(t2, t2, p2);
-    p3 = fmaf(t3, t3, p3);
+    float w0, w1, w2, w3;
+    load_vec4(wv, p, q, w0, w1, w2, w3);
+    const float d0 = fmaf(w0, x[4 * q + 0], -mean);
+    const float d1 = fmaf(w1, x[4 * q + 1], -mean);
+    const float d2 = fmaf(w2, x[4 * q + 2], -mean);
+    const float d3 = fmaf(w3, x[4 * q + 3], -mean);
+    s0 = fmaf(d0, d0, s0);
+    s1 = fmaf(d1, d1, s1);
+    s2 = fmaf(d2, d2, s2);
+    s3 = fmaf(d3, d3, s3);
   }
-  float s2 = (p0 + p1) + (p2 + p3);
-  s2 += __shfl_xor_sync(0xffffffffu, s2, 1);
-  return s2 * (1.0f / 128.0f);
+  s = (s0 + s1) + (s2 + s3);
+  s += __shfl_xor_sync(0xffffffffu, s, 2);
+  return s * (1.0f / 128.0f);
 }
 
 __device__ __forceinline__ uint32_t code_bits(float v, float top) {
-  // floor(v) of clamp(v, 0, top) through a round-down add of 2^23; the low bits of
-  // the sum are the integer code (exact for 0 <= v < 2^22).
+  // floor(clamp(v, 0, top)) through a round-down add of 2^23 (exact for 0 <= v < 2^22)
   const float c = fminf(fmaxf(v, 0.0f), top);
   return __float_as_uint(__fadd_rd(c, 8388608.0f)) - 0x4B000000u;
 }
 
-// Stages 2-4 for one tensor (kind 0 = K, 1 = V) of the current item.
+// Quantize the tensor of group g (0 = K, 1 = V) of the current item from TMEM;
+// writes the group's stage (codes + metadata). `line`/`p` locate the thread's half
+// line, `ta1`/`ta2` are its TMEM addresses of D1 and D2.
 template <int kKind>
-__device__ __forceinline__ void quantize_tensor(const uint8_t* tin, uint8_t* smem, float eps, int n_iters) {
-  const int tid = threadIdx.x;
-  const int e = ((tid >> 5) << 4) + ((tid & 31) >> 1);
-  const int half = tid & 1;
-  float* T = reinterpret_cast<float*>(smem + kOffT);
-  float* sa = reinterpret_cast<float*>(smem + kOffA);
-  float* sb = reinterpret_cast<float*>(smem + kOffB);
-  float* sG = reinterpret_cast<float*>(smem + kOffG);
-  float* sHc = reinterpret_cast<float*>(smem + kOffHc);
-  float* sW = reinterpret_cast<float*>(smem + kOffW);
-  float* sC0 = reinterpret_cast<float*>(smem + kOffC0);
-  uint8_t* stage = smem + kOffStage;
-  uint16_t* meta = reinterpret_cast<uint16_t*>(stage + (kKind == 0 ? kKMetaOff : kVMetaOff));
+__device__ __forceinline__ void quantize_group(float* vec, uint8_t* stage, uint32_t ta1, uint32_t ta2, int line,
+                                               int p, int n_iters, float eps, int bar_id) {
+  float* va = vec + kVA * kVec;
+  float* vb = vec + kVB * kVec;
+  float* vg = vec + kVG * kVec;
+  float* vh = vec + kVHc * kVec;
+  float* vw = vec + kVW * kVec;
+  float* vc0 = vec + kVC0 * kVec;
+  uint16_t* meta = reinterpret_cast<uint16_t*>(stage + (kKind == 0 ? 8192 : 4096));
+  const int pl = ps(line);
+  if (p == 0) {
+    va[pl] = 1.0f;
+    vb[pl] = 1.0f;
+  }
+  named_bar(bar_id, kGroupThreads);
 
-  // ---- stage 2: Hadamard rotation of token j = e along channels (col role)
-  float xc[64];
-  {
-    const uint8_t* row = tin + e * kRowPitch;
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      float fo[8], fp[8];
-      h8_to_f(*reinterpret_cast<const uint4*>(row + half * 128 + q * 16), fo);
-      h8_to_f(*reinterpret_cast<const uint4*>(row + (half ^ 1) * 128 + q * 16), fp);
-#pragma unroll
-      for (int u = 0; u < 8; ++u) xc[8 * q + u] = half ? (fp[u] - fo[u]) : (fo[u] + fp[u]);
-    }
-#pragma unroll
-    for (int s = 32; s >= 1; s >>= 1) {
-#pragma unroll
-      for (int i = 0; i < 64; ++i) {
-        if ((i & s) == 0) {
-          const float u = xc[i], w = xc[i + s];
-          xc[i] = u + w;
-          xc[i + s] = u - w;
-        }
-      }
-    }
-#pragma unroll
-    for (int i = 0; i < 64; ++i) xc[i] *= kInvSqrt128;
-  }
-  // transpose through shared memory into the row role
-#pragma unroll
-  for (int c4 = 0; c4 < 16; ++c4) {
-    const int i0 = 64 * half + 4 * c4;
-    *reinterpret_cast<float4*>(T + tidx(e, i0)) = make_float4(xc[4 * c4], xc[4 * c4 + 1], xc[4 * c4 + 2], xc[4 * c4 + 3]);
-  }
-  if (half == 0) {
-    sa[vpad(e)] = 1.0f;
-    sb[vpad(e)] = 1.0f;
-  }
-  __syncthreads();
-  float xr[64];
-#pragma unroll
-  for (int s = 0; s < 64; ++s) xr[s] = T[tidx(64 * half + s, e)];
-
-  // ---- stage 3: n_iters x (column pass, row pass), product form of the log scales
+  float x[64];
   for (int it = 0; it < n_iters; ++it) {
+    // column pass: token j = line, channels e = p + 2k (D2), weights a
+    tmem_ld_16x64b_x64(ta2, x);
     {
-      const float var = line_variance(xc, sa, half);       // var_i(a_i x_ij), token j = e
-      if (half == 0) {
-        const float b = sb[vpad(e)];
-        sb[vpad(e)] = b / sqrtf(fmaf(b * b, var, eps));
+      const float var = pair_variance(x, va, p) * kVarScale;
+      if (p == 0) {
+        const float b = vb[pl];
+        vb[pl] = b / sqrtf(fmaf(b * b, var, eps));
       }
     }
-    __syncthreads();
+    named_bar(bar_id, kGroupThreads);
+    // row pass: channel i = line, tokens e = p + 2k (D1), weights b
+    tmem_ld_16x64b_x64(ta1, x);
     {
-      const float var = line_variance(xr, sb, half);       // var_j(b_j x_ij), channel i = e
-      if (half == 0) {
-        const float a = sa[vpad(e)];
-        sa[vpad(e)] = a / sqrtf(fmaf(a * a, var, eps));
+      const float var = pair_variance(x, vb, p) * kVarScale;
+      if (p == 0) {
+        const float a = va[pl];
+        va[pl] = a / sqrtf(fmaf(a * a, var, eps));
       }
     }
-    __syncthreads();
+    named_bar(bar_id, kGroupThreads);
   }
 
-  // ---- fp16 scales r (per channel) and c (per token)
-  if (half == 0) {
-    const uint16_t rb = f2h_bits(clampf(1.0f / sa[vpad(e)], kFp16MinNormal, kFp16Max));
-    const uint16_t cb = f2h_bits(clampf(1.0f / sb[vpad(e)], kFp16MinNormal, kFp16Max));
-    meta[0 * 128 + e] = rb;
-    meta[1 * 128 + e] = cb;
-    sG[vpad(e)] = 1.0f / h2f_bits(rb);
-    sHc[vpad(e)] = 1.0f / h2f_bits(cb);
+  // fp16 scales: r per channel (line as channel), c per token (line as token)
+  if (p == 0) {
+    const uint16_t rb = f2h_bits(clampf(1.0f / va[pl], kFp16MinNormal, kFp16Max));
+    const uint16_t cb = f2h_bits(clampf(1.0f / vb[pl], kFp16MinNormal, kFp16Max));
+    meta[0 * 128 + line] = rb;
+    meta[1 * 128 + line] = cb;
+    vg[pl] = kInvSqrt128 / h2f_bits(rb);   // the +-1 transform's 2^-3.5 is folded here
+    vh[pl] = 1.0f / h2f_bits(cb);
   }
-  __syncthreads();
+  named_bar(bar_id, kGroupThreads);
 
-  // ---- stage 4: RTN. y_ij = (x_ij * (1/c_j)) * (1/r_i).
   constexpr float kLevels = kKind == 0 ? 15.0f : 3.0f;
-  if (kKind == 0) {
-    // key groups: channel i = e over tokens (row role)
-    const float g = sG[vpad(e)];
+  // group extremes of y = (x * hc_j) * g_i: keys per channel (D1 rows), values per
+  // token (D2 rows); two halves of 64 columns (registers k = 32 hh + kl)
+  {
     float mn = INFINITY, mx = -INFINITY;
-    {
-      const float4* h4 = reinterpret_cast<const float4*>(sHc + vpad(64 * half));
+#pragma unroll 1
+    for (int hh = 0; hh < 2; ++hh) {
+      float xh[32];
+      tmem_ld_16x64b_x32((kKind == 0 ? ta1 : ta2) + 64 * hh, xh);
+      if (kKind == 0) {
+        const float g = vg[pl];
 #pragma unroll
-      for (int q = 0; q < 16; ++q) {
-        const float4 w = h4[q];
-        const float y0 = (xr[4 * q + 0] * w.x) * g, y1 = (xr[4 * q + 1] * w.y) * g;
-        const float y2 = (xr[4 * q + 2] * w.z) * g, y3 = (xr[4 * q + 3] * w.w) * g;
-        mn = fminf(fminf(mn, y0), fminf(y1, fminf(y2, y3)));
-        mx = fmaxf(fmaxf(mx, y0), fmaxf(y1, fmaxf(y2, y3)));
+        for (int q = 0; q < 8; ++q) {
+          float h0, h1, h2, h3;
+          load_vec4(vh, p, 8 * hh + q, h0, h1, h2, h3);
+          const float y0 = (xh[4 * q] * h0) * g, y1 = (xh[4 * q + 1] * h1) * g;
+          const float y2 = (xh[4 * q + 2] * h2) * g, y3 = (xh[4 * q + 3] * h3) * g;
+          mn = fminf(fminf(mn, y0), fminf(y1, fminf(y2, y3)));
+          mx = fmaxf(fmaxf(mx, y0), fmaxf(y1, fmaxf(y2, y3)));
+        }
+      } else {
+        const float hc = vh[pl];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          float g0, g1, g2, g3;
+          load_vec4(vg, p, 8 * hh + q, g0, g1, g2, g3);
+          const float y0 = (xh[4 * q] * hc) * g0, y1 = (xh[4 * q + 1] * hc) * g1;
+          const float y2 = (xh[4 * q + 2] * hc) * g2, y3 = (xh[4 * q + 3] * hc) * g3;
+          mn = fminf(fminf(mn, y0), fminf(y1, fminf(y2, y3)));
+          mx = fmaxf(fmaxf(mx, y0), fmaxf(y1, fmaxf(y2, y3)));
+        }
       }
-      mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, 1));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
     }
-    if (half == 0) {
+    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, 2));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    if (p == 0) {
       const uint16_t zb = f2h_bits(clampf(mn, -kFp16Max, kFp16Max));
       const float z = h2f_bits(zb);
       const uint16_t sbits = f2h_bits(clampf(fmaxf(mx - z, 0.0f) / kLevels, kFp16MinNormal, kFp16Max));
       const float inv_s = 1.0f / h2f_bits(sbits);
-      meta[2 * 128 + e] = sbits;
-      meta[3 * 128 + e] = zb;
-      sW[vpad(e)] = g * inv_s;
-      sC0[vpad(e)] = fmaf(-z, inv_s, 0.5f);
+      meta[2 * 128 + line] = sbits;
+      meta[3 * 128 + line] = zb;
+      vw[pl] = (kKind == 0 ? vg[pl] : vh[pl]) * inv_s;
+      vc0[pl] = fmaf(-z, inv_s, 0.5f);
     }
-    __syncthreads();
-    // codes in the col role: token j = e, channels 64*half + k
-    const float hc = sHc[vpad(e)];
-    const float4* w4 = reinterpret_cast<const float4*>(sW + vpad(64 * half));
-    const float4* c4 = reinterpret_cast<const float4*>(sC0 + vpad(64 * half));
-    uint32_t code[64];
+  }
+  named_bar(bar_id, kGroupThreads);
+
+  // codes: keys token-major (D2 rows: token = line, channels e = p + 2k), values
+  // channel-major (D1 rows: channel = line, tokens e = p + 2k); half hh holds
+  // k = 32 hh + kl, i.e. key words w = 2hh, 2hh + 1 and value word u = hh
+  const float own = kKind == 0 ? vh[pl] : vg[pl];
+#pragma unroll 1
+  for (int hh = 0; hh < 2; ++hh) {
+    float xh[32];
+    tmem_ld_16x64b_x32((kKind == 0 ? ta2 : ta1) + 64 * hh, xh);
+    if (kKind == 0) {
+      // channel e = 32w + 16a + 8b + 2g4 + p -> k = 16w + 8a + 4b + g4, nibble 4p + 2a + b of word w
+      uint32_t part[2][4] = {{0, 0, 0, 0}, {0, 0, 0, 0}};   // [w - 2hh][g4]
 #pragma unroll
-    for (int q = 0; q < 16; ++q) {
-      const float4 w = w4[q], c = c4[q];
-      code[4 * q + 0] = code_bits(fmaf(xc[4 * q + 0] * hc, w.x, c.x), kLevels);
-      code[4 * q + 1] = code_bits(fmaf(xc[4 * q + 1] * hc, w.y, c.y), kLevels);
-      code[4 * q + 2] = code_bits(fmaf(xc[4 * q + 2] * hc, w.z, c.z), kLevels);
-      code[4 * q + 3] = code_bits(fmaf(xc[4 * q + 3] * hc, w.w, c.w), kLevels);
-    }
-    // pack: channel i = 32w + 16a + 8b + 2g + h, nibble p = 4h + 2a + b of word w
+      for (int q = 0; q < 8; ++q) {
+        float w0, w1, w2, w3, c0, c1, c2, c3;
+        load_vec4(vw, p, 8 * hh + q, w0, w1, w2, w3);
+        load_vec4(vc0, p, 8 * hh + q, c0, c1, c2, c3);
+        const float ws[4] = {w0, w1, w2, w3}, cs[4] = {c0, c1, c2, c3};
 #pragma unroll
-    for (int g4 = 0; g4 < 4; ++g4) {
-      uint32_t words[2];
-#pragma unroll
-      for (int wl = 0; wl < 2; ++wl) {
-        uint32_t word = 0;
-#pragma unroll
-        for (int p = 0; p < 8; ++p) {
-          const int h = p >> 2, a = (p >> 1) & 1, b = p & 1;
-          const int k = 32 * wl + 16 * a + 8 * b + 2 * g4 + h;   // channel - 64*half
-          word |= code[k] << (4 * p);
-        }
-        words[wl] = word;
-      }
-      *reinterpret_cast<uint2*>(stage + kKCodeOff + e * 64 + g4 * 16 + half * 8) = make_uint2(words[0], words[1]);
-    }
-  } else {
-    // value groups: token j = e over channels (col role)
-    const float hc = sHc[vpad(e)];
-    float mn = INFINITY, mx = -INFINITY;
-    {
-      const float4* g4v = reinterpret_cast<const float4*>(sG + vpad(64 * half));
-#pragma unroll
-      for (int q = 0; q < 16; ++q) {
-        const float4 w = g4v[q];
-        const float y0 = (xc[4 * q + 0] * hc) * w.x, y1 = (xc[4 * q + 1] * hc) * w.y;
-        const float y2 = (xc[4 * q + 2] * hc) * w.z, y3 = (xc[4 * q + 3] * hc) * w.w;
-        mn = fminf(fminf(mn, y0), fminf(y1, fminf(y2, y3)));
-        mx = fmaxf(fmaxf(mx, y0), fmaxf(y1, fmaxf(y2, y3)));
-      }
-      mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, 1));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-    }
-    if (half == 0) {
-      const uint16_t zb = f2h_bits(clampf(mn, -kFp16Max, kFp16Max));
-      const float z = h2f_bits(zb);
-      const uint16_t sbits = f2h_bits(clampf(fmaxf(mx - z, 0.0f) / kLevels, kFp16MinNormal, kFp16Max));
-      const float inv_s = 1.0f / h2f_bits(sbits);
-      meta[2 * 128 + e] = sbits;
-      meta[3 * 128 + e] = zb;
-      sW[vpad(e)] = hc * inv_s;
-      sC0[vpad(e)] = fmaf(-z, inv_s, 0.5f);
-    }
-    __syncthreads();
-    // codes in the row role: channel i = e, tokens j = 64*half + s
-    const float g = sG[vpad(e)];
-    const float4* w4 = reinterpret_cast<const float4*>(sW + vpad(64 * half));
-    const float4* c4 = reinterpret_cast<const float4*>(sC0 + vpad(64 * half));
-    uint32_t code[64];
-#pragma unroll
-    for (int q = 0; q < 16; ++q) {
-      const float4 w = w4[q], c = c4[q];
-      code[4 * q + 0] = code_bits(fmaf(xr[4 * q + 0] * g, w.x, c.x), kLevels);
-      code[4 * q + 1] = code_bits(fmaf(xr[4 * q + 1] * g, w.y, c.y), kLevels);
-      code[4 * q + 2] = code_bits(fmaf(xr[4 * q + 2] * g, w.z, c.z), kLevels);
-      code[4 * q + 3] = code_bits(fmaf(xr[4 * q + 3] * g, w.w, c.w), kLevels);
-    }
-    // pack: token t = 64*half + s, crumb p = 8(t&1) + 2((t>>4)&3) + ((t>>3)&1) of
-    // word u = half in cell (i&7)*4 + ((t>>1)&3) of panel i>>4, slot (i>>3)&1.
-    const int i = e;
-    uint8_t* panel = stage + kVCodeOff + (i >> 4) * 512 + ((i >> 3) & 1) * 8 + half * 4;
-#pragma unroll
-    for (int g4 = 0; g4 < 4; ++g4) {
-      uint32_t word = 0;
-#pragma unroll
-      for (int s = 0; s < 64; ++s) {
-        if (((s >> 1) & 3) == g4) {
-          const int p = 8 * (s & 1) + 2 * ((s >> 4) & 3) + ((s >> 3) & 1);
-          word |= code[s] << (2 * p);
+        for (int u = 0; u < 4; ++u) {
+          const int kl = 4 * q + u;
+          const int wl = kl >> 4, a = (kl >> 3) & 1, b = (kl >> 2) & 1, g4 = kl & 3;
+          const uint32_t code = code_bits(fmaf(xh[kl] * own, ws[u], cs[u]), kLevels);
+          part[wl][g4] |= code << (4 * (2 * a + b) + 16 * p);
         }
       }
-      *reinterpret_cast<uint32_t*>(panel + ((i & 7) * 4 + g4) * 16) = word;
+      uint8_t* row = stage + line * 64;
+#pragma unroll
+      for (int g4 = 0; g4 < 4; ++g4) {
+        const uint32_t f0 = part[0][g4] | __shfl_xor_sync(0xffffffffu, part[0][g4], 2);
+        const uint32_t f1 = part[1][g4] | __shfl_xor_sync(0xffffffffu, part[1][g4], 2);
+        if (p == hh) *reinterpret_cast<uint2*>(row + g4 * 16 + hh * 8) = make_uint2(f0, f1);
+      }
+    } else {
+      // token e = 64u + 16k2 + 8b + 2g4 + p -> k = 32u + 8k2 + 4b + g4, crumb 8p + 2k2 + b of word u
+      uint32_t part[4] = {0, 0, 0, 0};   // [g4], word u = hh
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        float w0, w1, w2, w3, c0, c1, c2, c3;
+        load_vec4(vw, p, 8 * hh + q, w0, w1, w2, w3);
+        load_vec4(vc0, p, 8 * hh + q, c0, c1, c2, c3);
+        const float ws[4] = {w0, w1, w2, w3}, cs[4] = {c0, c1, c2, c3};
+#pragma unroll
+        for (int uu = 0; uu < 4; ++uu) {
+          const int kl = 4 * q + uu;
+          const int k2 = (kl >> 3) & 3, b = (kl >> 2) & 1, g4 = kl & 3;
+          const uint32_t code = code_bits(fmaf(xh[kl] * own, ws[uu], cs[uu]), kLevels);
+          part[g4] |= code << (2 * (2 * k2 + b) + 16 * p);
+        }
+      }
+      const int i = line;
+      uint8_t* panel = stage + (i >> 4) * 512 + ((i >> 3) & 1) * 8;
+#pragma unroll
+      for (int g4 = 0; g4 < 4; ++g4) {
+        const uint32_t f = part[g4] | __shfl_xor_sync(0xffffffffu, part[g4], 2);
+        if (p == hh) *reinterpret_cast<uint32_t*>(panel + ((i & 7) * 4 + g4) * 16 + hh * 4) = f;
+      }
     }
   }
 }
@@ -405,49 +365,112 @@ __device__ __forceinline__ void quantize_tensor(const uint8_t* tin, uint8_t* sme
 template <class Src>
 __global__ void __launch_bounds__(kThreads, 1)
     quantize_kernel(Src src, uint8_t* __restrict__ cache, int n_iters, float eps, unsigned* flags) {
-  extern __shared__ __align__(128) uint8_t smem[];
+  extern __shared__ __align__(1024) uint8_t smem[];
   const int tid = threadIdx.x;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
-  const int64_t* s_dst = reinterpret_cast<const int64_t*>(smem + kOffDst);
-  int64_t item = blockIdx.x;
-  if (item >= src.n_items) return;
+  const int grp = tid / kGroupThreads;     // 0 = K, 1 = V
+  const int gt = tid % kGroupThreads;
+  const int bar_id = 1 + grp;
+  uint64_t* mma_bar = reinterpret_cast<uint64_t*>(smem + kOffBar);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffTmem);
+  if (static_cast<int64_t>(blockIdx.x) >= src.n_items) return;
+
+  // Sylvester +-1 Hadamard operand (H[i][k] = (-1)^popcount(i & k)), canonical layout
+  for (int e = tid; e < kD * kD; e += kThreads) {
+    const int i = e >> 7, kk = e & 127;
+    *reinterpret_cast<uint16_t*>(smem + kOffH + canon_offset(i, kk)) = (__popc(i & kk) & 1) ? 0xBC00u : 0x3C00u;
+  }
   if (tid == 0) {
-    mbar_init(&bars[0], 1);
-    mbar_init(&bars[1], 1);
+    mbar_init(&mma_bar[0], 1);
+    mbar_init(&mma_bar[1], 1);
     fence_mbar_init();
   }
+  if (tid < 32) tmem_alloc(tmem_slot, 512);
+  fence_proxy_async_smem();
+  tc_fence_before();
   __syncthreads();
-  if (tid < 32) prefetch(src, item, 0, smem, flags);
-  __syncthreads();
-  uint32_t parity = 0;
-  for (int k = 0;; ++k) {
-    const int cur = k & 1;
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  // this thread's half line in TMEM
+  const int gw = gt >> 5, t = gt & 31;
+  const uint32_t lane0 = 32 * (gw & 3) + 16 * (gw >> 2);
+  const int line = static_cast<int>(lane0) + (t >> 2) + 8 * (t & 1);
+  const int p = (t >> 1) & 1;
+  const uint32_t d1 = tmem_addr(tmem, 0, 256 * grp);
+  const uint32_t d2 = d1 + 128;
+  const uint32_t ta1 = tmem_addr(tmem, lane0, 256 * grp);
+  const uint32_t ta2 = ta1 + 128;
+  float* vec = reinterpret_cast<float*>(smem + kOffVec) + grp * kNumVec * kVec;
+  const uint32_t sh = smem_u32(smem + kOffH);
+  constexpr uint32_t kIdesc = idesc_f16_f32(128, 128);
+
+  int64_t item = blockIdx.x;
+  load_tile(src, item, grp, gt, smem + kOffIn + (grp * 2 + 0) * kTileOp);
+  cp_async_commit();
+  typename Src::Check check = src.prepare(item, gt);
+  uint32_t mma_parity = 0;
+  bool alive = true;
+  for (int k = 0; item < src.n_items; ++k, item += gridDim.x) {
+    const int buf = k & 1;
     const int64_t next = item + gridDim.x;
-    if (tid < 32 && next < src.n_items) prefetch(src, next, cur ^ 1, smem, flags);
-    const int64_t dst = s_dst[cur];
-    if (dst >= 0) {
-      const bool ok = mbar_wait(&bars[cur], (parity >> cur) & 1u, flags);
-      parity ^= 1u << cur;
-      if (__syncthreads_and(ok)) {
-        if (tid == 0) bulk_wait_read_all();  // previous record has left the stage
-        quantize_tensor<0>(smem + kOffIn + (cur * 2 + 0) * kInTile, smem, eps, n_iters);
-        __syncthreads();
-        quantize_tensor<1>(smem + kOffIn + (cur * 2 + 1) * kInTile, smem, eps, n_iters);
-        fence_proxy_async_smem();
-        __syncthreads();
-        if (tid == 0) {
-          bulk_s2g(cache + dst * static_cast<int64_t>(kRec), smem + kOffStage, kRec);
-          bulk_commit();
-        }
-      } else {
-        break;
-      }
+    typename Src::Check check_next{};
+    if (next < src.n_items) {
+      load_tile(src, next, grp, gt, smem + kOffIn + (grp * 2 + (buf ^ 1)) * kTileOp);
+      check_next = src.prepare(next, gt);
     }
-    __syncthreads();
-    item = next;
-    if (item >= src.n_items) break;
+    cp_async_commit();
+    cp_async_wait<1>();               // this item's copies (all but the newest group)
+    fence_proxy_async_smem();         // ... visible to the tensor core
+    tc_fence_before();
+    const int64_t dst = src.resolve(item, check, gt, bar_id, flags);   // includes a group barrier
+    check = check_next;
+    tc_fence_after();
+    if (dst < 0 || !alive) continue;
+    uint8_t* stage = smem + (grp == 0 ? kOffStageK + buf * kStageK : kOffStageV + buf * kStageV);
+    if (gt == 0) {
+      const uint32_t sx = smem_u32(smem + kOffIn + (grp * 2 + buf) * kTileOp);
+#pragma unroll
+      for (int s = 0; s < 8; ++s) {
+        const uint64_t dh = smem_desc_kmajor(sh + 256 * s);
+        const uint64_t dx = smem_desc_kmajor(sx + 256 * s);
+        umma_f16(d1, dh, dx, kIdesc, s > 0);   // D1[i][j] = sum_k H[i][k] X[j][k]
+        umma_f16(d2, dx, dh, kIdesc, s > 0);   // D2[j][i] = sum_k X[j][k] H[i][k]
+      }
+      umma_commit(&mma_bar[grp]);
+      bulk_wait_read<1>();              // the stage written two items ago has been stored
+    }
+    const bool ok = mbar_wait(&mma_bar[grp], mma_parity, flags);
+    mma_parity ^= 1;
+    tc_fence_after();
+    if (!named_bar_and(bar_id, kGroupThreads, ok)) {
+      alive = false;                    // the tensor core never signalled: stop (flag raised)
+      continue;
+    }
+    if (grp == 0)
+      quantize_group<0>(vec, stage, ta1, ta2, line, p, n_iters, eps, bar_id);
+    else
+      quantize_group<1>(vec, stage, ta1, ta2, line, p, n_iters, eps, bar_id);
+    fence_proxy_async_smem();
+    tc_fence_before();
+    named_bar(bar_id, kGroupThreads);
+    if (gt == 0) {
+      uint8_t* rec = cache + dst * static_cast<int64_t>(kRec);
+      if (grp == 0) {
+        bulk_s2g(rec + kKCodeOff, stage, 8192);
+        bulk_s2g(rec + kKMetaOff, stage + 8192, 1024);
+      } else {
+        bulk_s2g(rec + kVCodeOff, stage, 4096);
+        bulk_s2g(rec + kVMetaOff, stage + 4096, 1024);
+      }
+      bulk_commit();
+    }
   }
-  if (tid == 0) bulk_wait_all();
+  cp_async_wait<0>();
+  if (gt == 0) bulk_wait_all();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (tid < 32) tmem_dealloc(tmem, 512);
 }
 
 int sm_count() {
