@@ -32,7 +32,7 @@ constexpr int kTileOp = kB * kD * 2;              // 32768 B: one fp16 128x128 o
 constexpr int kStageK = 8192 + 1024;              // K codes + K metadata
 constexpr int kStageV = 4096 + 1024;              // V codes + V metadata
 constexpr int kVec = 136;                         // parity-split vector (even at 0, odd at 68)
-constexpr int kNumVec = 6;                        // a, b, g (2^-3.5/r), hc (1/c), w, c0
+constexpr int kNumVec = 8;                        // a, b, g (2^-3.5/r), hc (1/c), w, c0, mc, mr
 
 constexpr int kOffH = 0;
 constexpr int kOffIn = kOffH + kTileOp;                        // [group][buf] operands
@@ -45,7 +45,7 @@ constexpr int kSmemBytes = kOffTmem + 16;
 static_assert(kSmemBytes <= 232448, "quantize shared memory");
 static_assert(kOffIn % 1024 == 0 && kOffStageK % 16 == 0 && kOffStageV % 16 == 0 && kOffVec % 16 == 0, "align");
 
-enum { kVA = 0, kVB = 1, kVG = 2, kVHc = 3, kVW = 4, kVC0 = 5 };
+enum { kVA = 0, kVB = 1, kVG = 2, kVHc = 3, kVW = 4, kVC0 = 5, kVMc = 6, kVMr = 7 };
 
 // position of entry e in a parity-split vector
 __device__ __forceinline__ int ps(int e) { return (e & 1) * 68 + (e >> 1); }
@@ -153,58 +153,86 @@ __device__ __forceinline__ void load_tile(const Src& src, int64_t w, int g, int 
   }
 }
 
-__device__ __forceinline__ void load_vec4(const float* v, int p, int q, float& a0, float& a1, float& a2, float& a3) {
-  const float4 w = reinterpret_cast<const float4*>(v + p * 68)[q];
-  a0 = w.x; a1 = w.y; a2 = w.z; a3 = w.w;
+// Population variance and mean over the pair's 128 values of w_e * x_e, where the
+// thread's line in TMEM is at `taddr` (entries e = p + 2k, k < 64, streamed in two
+// halves of 32) and w is a parity-split vector. One sweep accumulates the first
+// two moments about a shift close to the mean (the line's mean from the previous
+// iteration); if the shift was far from the mean (mean square more than twice the
+// variance, or a non-positive variance), a second sweep recomputes the moments
+// about the exact mean, so the result keeps the accuracy of a centred two-pass
+// variance.
+__device__ __forceinline__ float pair_moments(uint32_t taddr, const float* wv, int p, float shift, float& mean) {
+  const float2 nsh = make_float2(-shift, -shift);
+  float2 s0 = make_float2(0.f, 0.f), s1 = s0, q0 = s0, q1 = s0;
+#pragma unroll 1
+  for (int hh = 0; hh < 2; ++hh) {
+    float x[32];
+    tmem_ld_16x64b_x32(taddr + 64 * hh, x);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const float4 w = reinterpret_cast<const float4*>(wv + p * 68)[8 * hh + q];
+      const float2 d0 = __ffma2_rn(make_float2(w.x, w.y), make_float2(x[4 * q], x[4 * q + 1]), nsh);
+      const float2 d1 = __ffma2_rn(make_float2(w.z, w.w), make_float2(x[4 * q + 2], x[4 * q + 3]), nsh);
+      s0 = __fadd2_rn(s0, d0);
+      s1 = __fadd2_rn(s1, d1);
+      q0 = __ffma2_rn(d0, d0, q0);
+      q1 = __ffma2_rn(d1, d1, q1);
+    }
+  }
+  float s = (s0.x + s0.y) + (s1.x + s1.y), m2 = (q0.x + q0.y) + (q1.x + q1.y);
+  s += __shfl_xor_sync(0xffffffffu, s, 2);
+  m2 += __shfl_xor_sync(0xffffffffu, m2, 2);
+  float d = s * (1.0f / 128.0f);
+  const float msq = m2 * (1.0f / 128.0f);
+  float var = msq - d * d;
+  const bool recentre = !(msq <= 2.0f * var);   // shift far from the mean, or var <= 0
+  // The second sweep holds warp-collective instructions (tcgen05.ld, shuffles), so
+  // the whole warp runs it when any pair needs it; other pairs keep their result.
+  if (__any_sync(0xffffffffu, recentre)) {
+    const float c = shift + d;
+    const float2 nc = make_float2(-c, -c);
+    float2 r0 = make_float2(0.f, 0.f), r1 = r0;
+#pragma unroll 1
+    for (int hh = 0; hh < 2; ++hh) {
+      float x[32];
+      tmem_ld_16x64b_x32(taddr + 64 * hh, x);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const float4 w = reinterpret_cast<const float4*>(wv + p * 68)[8 * hh + q];
+        const float2 e0 = __ffma2_rn(make_float2(w.x, w.y), make_float2(x[4 * q], x[4 * q + 1]), nc);
+        const float2 e1 = __ffma2_rn(make_float2(w.z, w.w), make_float2(x[4 * q + 2], x[4 * q + 3]), nc);
+        r0 = __ffma2_rn(e0, e0, r0);
+        r1 = __ffma2_rn(e1, e1, r1);
+      }
+    }
+    float r = (r0.x + r0.y) + (r1.x + r1.y);
+    r += __shfl_xor_sync(0xffffffffu, r, 2);
+    if (recentre) {
+      var = r * (1.0f / 128.0f);
+      shift = c;
+      d = 0.f;
+    }
+  }
+  mean = shift + d;
+  return fmaxf(var, 0.0f);
 }
 
-// Population variance over the pair's 128 values of w_e * x_e, where the thread
-// holds entries e = p + 2k, k < 64, and w is a parity-split vector.
-__device__ __forceinline__ float pair_variance(const float (&x)[64], const float* wv, int p) {
-  float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
-#pragma unroll
-  for (int q = 0; q < 16; ++q) {
-    float w0, w1, w2, w3;
-    load_vec4(wv, p, q, w0, w1, w2, w3);
-    s0 = fmaf(w0, x[4 * q + 0], s0);
-    s1 = fmaf(w1, x[4 * q + 1], s1);
-    s2 = fmaf(w2, x[4 * q + 2], s2);
-    s3 = fmaf(w3, x[4 * q + 3], s3);
-  }
-  float s = (s0 + s1) + (s2 + s3);
-  s += __shfl_xor_sync(0xffffffffu, s, 2);
-  const float mean = s * (1.0f / 128.0f);
-  s0 = s1 = s2 = s3 = 0.f;
-#pragma unroll
-  for (int q = 0; q < 16; ++q) {
-    float w0, w1, w2, w3;
-    load_vec4(wv, p, q, w0, w1, w2, w3);
-    const float d0 = fmaf(w0, x[4 * q + 0], -mean);
-    const float d1 = fmaf(w1, x[4 * q + 1], -mean);
-    const float d2 = fmaf(w2, x[4 * q + 2], -mean);
-    const float d3 = fmaf(w3, x[4 * q + 3], -mean);
-    s0 = fmaf(d0, d0, s0);
-    s1 = fmaf(d1, d1, s1);
-    s2 = fmaf(d2, d2, s2);
-    s3 = fmaf(d3, d3, s3);
-  }
-  s = (s0 + s1) + (s2 + s3);
-  s += __shfl_xor_sync(0xffffffffu, s, 2);
-  return s * (1.0f / 128.0f);
-}
-
-__device__ __forceinline__ uint32_t code_bits(float v, float top) {
-  // floor(clamp(v, 0, top)) through a round-down add of 2^23 (exact for 0 <= v < 2^22)
-  const float c = fminf(fmaxf(v, 0.0f), top);
-  return __float_as_uint(__fadd_rd(c, 8388608.0f)) - 0x4B000000u;
+// v / sqrt(u): reciprocal square root refined by one Newton-Raphson step
+// (y1 = y0 + y0 (1 - u y0^2) / 2), then one multiply.
+__device__ __forceinline__ float div_sqrt(float v, float u) {
+  const float y0 = rsqrtf(u);
+  const float e = fmaf(-u * y0, y0, 1.0f);
+  const float y1 = fmaf(0.5f * y0, e, y0);
+  return v * y1;
 }
 
 // Quantize the tensor of group g (0 = K, 1 = V) of the current item from TMEM;
-// writes the group's stage (codes + metadata). `line`/`p` locate the thread's half
-// line, `ta1`/`ta2` are its TMEM addresses of D1 and D2.
+// writes the group's stage (codes + metadata). `tile` is the item's fp16 operand
+// (canonical layout), `line`/`p` locate the thread's half line, `ta1`/`ta2` are
+// its TMEM addresses of D1 and D2.
 template <int kKind>
-__device__ __forceinline__ void quantize_group(float* vec, uint8_t* stage, uint32_t ta1, uint32_t ta2, int line,
-                                               int p, int n_iters, float eps, int bar_id) {
+__device__ __forceinline__ void quantize_group(float* vec, uint8_t* stage, const uint8_t* tile, uint32_t ta1,
+                                               uint32_t ta2, int line, int p, int n_iters, float eps, int bar_id) {
   float* va = vec + kVA * kVec;
   float* vb = vec + kVB * kVec;
   float* vg = vec + kVG * kVec;
@@ -219,25 +247,32 @@ __device__ __forceinline__ void quantize_group(float* vec, uint8_t* stage, uint3
   }
   named_bar(bar_id, kGroupThreads);
 
-  float x[64];
+  float* vmc = vec + kVMc * kVec;
+  float* vmr = vec + kVMr * kVec;
   for (int it = 0; it < n_iters; ++it) {
-    // column pass: token j = line, channels e = p + 2k (D2), weights a
-    tmem_ld_16x64b_x64(ta2, x);
+    // column pass: token j = line, channels e = p + 2k (D2), weights a; the first
+    // shift is exact: with a = 1 the mean of a +-1 Hadamard column is the token's
+    // channel-0 input value
     {
-      const float var = pair_variance(x, va, p) * kVarScale;
+      const float shift = it == 0 ? __half2float(*reinterpret_cast<const __half*>(tile + canon_offset(line, 0)))
+                                  : vmc[pl];
+      float mean;
+      const float var = pair_moments(ta2, va, p, shift, mean) * kVarScale;
       if (p == 0) {
         const float b = vb[pl];
-        vb[pl] = b / sqrtf(fmaf(b * b, var, eps));
+        vb[pl] = div_sqrt(b, fmaf(b * b, var, eps));
+        vmc[pl] = mean;
       }
     }
     named_bar(bar_id, kGroupThreads);
     // row pass: channel i = line, tokens e = p + 2k (D1), weights b
-    tmem_ld_16x64b_x64(ta1, x);
     {
-      const float var = pair_variance(x, vb, p) * kVarScale;
+      float mean;
+      const float var = pair_moments(ta1, vb, p, it == 0 ? 0.0f : vmr[pl], mean) * kVarScale;
       if (p == 0) {
         const float a = va[pl];
-        va[pl] = a / sqrtf(fmaf(a * a, var, eps));
+        va[pl] = div_sqrt(a, fmaf(a * a, var, eps));
+        vmr[pl] = mean;
       }
     }
     named_bar(bar_id, kGroupThreads);
@@ -263,32 +298,21 @@ __device__ __forceinline__ void quantize_group(float* vec, uint8_t* stage, uint3
     for (int hh = 0; hh < 2; ++hh) {
       float xh[32];
       tmem_ld_16x64b_x32((kKind == 0 ? ta1 : ta2) + 64 * hh, xh);
-      if (kKind == 0) {
-        const float g = vg[pl];
+      // y = (x * hc_j) * g_i; the factor that is constant along the thread's line is
+      // positive, so it multiplies the extremes afterwards (same rounding as per element)
+      const float* vv = kKind == 0 ? vh : vg;
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          float h0, h1, h2, h3;
-          load_vec4(vh, p, 8 * hh + q, h0, h1, h2, h3);
-          const float y0 = (xh[4 * q] * h0) * g, y1 = (xh[4 * q + 1] * h1) * g;
-          const float y2 = (xh[4 * q + 2] * h2) * g, y3 = (xh[4 * q + 3] * h3) * g;
-          mn = fminf(fminf(mn, y0), fminf(y1, fminf(y2, y3)));
-          mx = fmaxf(fmaxf(mx, y0), fmaxf(y1, fmaxf(y2, y3)));
-        }
-      } else {
-        const float hc = vh[pl];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          float g0, g1, g2, g3;
-          load_vec4(vg, p, 8 * hh + q, g0, g1, g2, g3);
-          const float y0 = (xh[4 * q] * hc) * g0, y1 = (xh[4 * q + 1] * hc) * g1;
-          const float y2 = (xh[4 * q + 2] * hc) * g2, y3 = (xh[4 * q + 3] * hc) * g3;
-          mn = fminf(fminf(mn, y0), fminf(y1, fminf(y2, y3)));
-          mx = fmaxf(fmaxf(mx, y0), fmaxf(y1, fmaxf(y2, y3)));
-        }
+      for (int q = 0; q < 8; ++q) {
+        const float4 w = reinterpret_cast<const float4*>(vv + p * 68)[8 * hh + q];
+        const float2 y0 = __fmul2_rn(make_float2(xh[4 * q], xh[4 * q + 1]), make_float2(w.x, w.y));
+        const float2 y1 = __fmul2_rn(make_float2(xh[4 * q + 2], xh[4 * q + 3]), make_float2(w.z, w.w));
+        mn = fminf(fminf(mn, y0.x), fminf(y0.y, fminf(y1.x, y1.y)));
+        mx = fmaxf(fmaxf(mx, y0.x), fmaxf(y0.y, fmaxf(y1.x, y1.y)));
       }
     }
-    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, 2));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    const float line_factor = kKind == 0 ? vg[pl] : vh[pl];
+    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, 2)) * line_factor;
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2)) * line_factor;
     if (p == 0) {
       const uint16_t zb = f2h_bits(clampf(mn, -kFp16Max, kFp16Max));
       const float z = h2f_bits(zb);
@@ -306,56 +330,66 @@ __device__ __forceinline__ void quantize_group(float* vec, uint8_t* stage, uint3
   // channel-major (D1 rows: channel = line, tokens e = p + 2k); half hh holds
   // k = 32 hh + kl, i.e. key words w = 2hh, 2hh + 1 and value word u = hh
   const float own = kKind == 0 ? vh[pl] : vg[pl];
+  const float2 own2 = make_float2(own, own);
 #pragma unroll 1
   for (int hh = 0; hh < 2; ++hh) {
     float xh[32];
     tmem_ld_16x64b_x32((kKind == 0 ? ta2 : ta1) + 64 * hh, xh);
-    if (kKind == 0) {
-      // channel e = 32w + 16a + 8b + 2g4 + p -> k = 16w + 8a + 4b + g4, nibble 4p + 2a + b of word w
-      uint32_t part[2][4] = {{0, 0, 0, 0}, {0, 0, 0, 0}};   // [w - 2hh][g4]
+    // v = (x * own) * w_e + c0_e = (y - z) / s + 1/2, clamped to [0, levels]; the
+    // round-down add of 2^23 leaves 0x4B000000 + floor(v) in the bits, and each
+    // word accumulates (bits << shift) with the 0x4B000000 terms removed at the end
+    uint32_t part[2][4] = {{0, 0, 0, 0}, {0, 0, 0, 0}};
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        float w0, w1, w2, w3, c0, c1, c2, c3;
-        load_vec4(vw, p, 8 * hh + q, w0, w1, w2, w3);
-        load_vec4(vc0, p, 8 * hh + q, c0, c1, c2, c3);
-        const float ws[4] = {w0, w1, w2, w3}, cs[4] = {c0, c1, c2, c3};
+    for (int q = 0; q < 8; ++q) {
+      const float4 w = reinterpret_cast<const float4*>(vw + p * 68)[8 * hh + q];
+      const float4 c = reinterpret_cast<const float4*>(vc0 + p * 68)[8 * hh + q];
+      const float2 v0 = __ffma2_rn(__fmul2_rn(make_float2(xh[4 * q], xh[4 * q + 1]), own2), make_float2(w.x, w.y),
+                                   make_float2(c.x, c.y));
+      const float2 v1 = __ffma2_rn(__fmul2_rn(make_float2(xh[4 * q + 2], xh[4 * q + 3]), own2),
+                                   make_float2(w.z, w.w), make_float2(c.z, c.w));
+      const float2 lo = make_float2(fminf(fmaxf(v0.x, 0.f), kLevels), fminf(fmaxf(v0.y, 0.f), kLevels));
+      const float2 hi = make_float2(fminf(fmaxf(v1.x, 0.f), kLevels), fminf(fmaxf(v1.y, 0.f), kLevels));
+      const float2 f0 = __fadd2_rd(lo, make_float2(8388608.0f, 8388608.0f));
+      const float2 f1 = __fadd2_rd(hi, make_float2(8388608.0f, 8388608.0f));
+      const uint32_t bits[4] = {__float_as_uint(f0.x), __float_as_uint(f0.y), __float_as_uint(f1.x),
+                                __float_as_uint(f1.y)};
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int kl = 4 * q + u;
+      for (int u = 0; u < 4; ++u) {
+        const int kl = 4 * q + u;
+        if (kKind == 0) {
+          // channel e = 32w + 16a + 8b + 2g4 + p -> k = 16w + 8a + 4b + g4, nibble 4p + 2a + b of word w
           const int wl = kl >> 4, a = (kl >> 3) & 1, b = (kl >> 2) & 1, g4 = kl & 3;
-          const uint32_t code = code_bits(fmaf(xh[kl] * own, ws[u], cs[u]), kLevels);
-          part[wl][g4] |= code << (4 * (2 * a + b) + 16 * p);
+          part[wl][g4] += bits[u] << (4 * (2 * a + b) + 16 * p);
+        } else {
+          // token e = 64u + 16k2 + 8b + 2g4 + p -> k = 32u + 8k2 + 4b + g4, crumb 8p + 2k2 + b of word u
+          const int k2 = (kl >> 3) & 3, b = (kl >> 2) & 1, g4 = kl & 3;
+          part[0][g4] += bits[u] << (2 * (2 * k2 + b) + 16 * p);
         }
       }
+    }
+    if (kKind == 0) {
+      // each word got 4 nibbles (a, b) from this thread: remove their 0x4B000000 terms
+      const uint32_t bias = 0x4B000000u * ((1u << (16 * p)) * (1u + (1u << 4) + (1u << 8) + (1u << 12)));
       uint8_t* row = stage + line * 64;
 #pragma unroll
       for (int g4 = 0; g4 < 4; ++g4) {
-        const uint32_t f0 = part[0][g4] | __shfl_xor_sync(0xffffffffu, part[0][g4], 2);
-        const uint32_t f1 = part[1][g4] | __shfl_xor_sync(0xffffffffu, part[1][g4], 2);
+        const uint32_t m0 = part[0][g4] - bias, m1 = part[1][g4] - bias;
+        const uint32_t f0 = m0 | __shfl_xor_sync(0xffffffffu, m0, 2);
+        const uint32_t f1 = m1 | __shfl_xor_sync(0xffffffffu, m1, 2);
         if (p == hh) *reinterpret_cast<uint2*>(row + g4 * 16 + hh * 8) = make_uint2(f0, f1);
       }
     } else {
-      // token e = 64u + 16k2 + 8b + 2g4 + p -> k = 32u + 8k2 + 4b + g4, crumb 8p + 2k2 + b of word u
-      uint32_t part[4] = {0, 0, 0, 0};   // [g4], word u = hh
+      // each word got 8 crumbs (k2, b) from this thread
+      uint32_t geo = 0;
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        float w0, w1, w2, w3, c0, c1, c2, c3;
-        load_vec4(vw, p, 8 * hh + q, w0, w1, w2, w3);
-        load_vec4(vc0, p, 8 * hh + q, c0, c1, c2, c3);
-        const float ws[4] = {w0, w1, w2, w3}, cs[4] = {c0, c1, c2, c3};
-#pragma unroll
-        for (int uu = 0; uu < 4; ++uu) {
-          const int kl = 4 * q + uu;
-          const int k2 = (kl >> 3) & 3, b = (kl >> 2) & 1, g4 = kl & 3;
-          const uint32_t code = code_bits(fmaf(xh[kl] * own, ws[uu], cs[uu]), kLevels);
-          part[g4] |= code << (2 * (2 * k2 + b) + 16 * p);
-        }
-      }
+      for (int j = 0; j < 8; ++j) geo += 1u << (2 * j);
+      const uint32_t bias = 0x4B000000u * ((1u << (16 * p)) * geo);
       const int i = line;
       uint8_t* panel = stage + (i >> 4) * 512 + ((i >> 3) & 1) * 8;
 #pragma unroll
       for (int g4 = 0; g4 < 4; ++g4) {
-        const uint32_t f = part[g4] | __shfl_xor_sync(0xffffffffu, part[g4], 2);
+        const uint32_t m = part[0][g4] - bias;
+        const uint32_t f = m | __shfl_xor_sync(0xffffffffu, m, 2);
         if (p == hh) *reinterpret_cast<uint32_t*>(panel + ((i & 7) * 4 + g4) * 16 + hh * 4) = f;
       }
     }
@@ -446,10 +480,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       alive = false;                    // the tensor core never signalled: stop (flag raised)
       continue;
     }
+    const uint8_t* tile = smem + kOffIn + (grp * 2 + buf) * kTileOp;
     if (grp == 0)
-      quantize_group<0>(vec, stage, ta1, ta2, line, p, n_iters, eps, bar_id);
+      quantize_group<0>(vec, stage, tile, ta1, ta2, line, p, n_iters, eps, bar_id);
     else
-      quantize_group<1>(vec, stage, ta1, ta2, line, p, n_iters, eps, bar_id);
+      quantize_group<1>(vec, stage, tile, ta1, ta2, line, p, n_iters, eps, bar_id);
     fence_proxy_async_smem();
     tc_fence_before();
     named_bar(bar_id, kGroupThreads);
