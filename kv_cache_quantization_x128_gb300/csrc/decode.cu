@@ -1,20 +1,27 @@
 // KVarN paged decode attention over the packed cache (KVarN README, "How KVarN
-// works": scales are re-applied on read; the orthonormal rotation keeps
+// works": the scales are re-applied on read; the orthonormal rotation keeps
 // attention scores, so q is rotated by the same H and the output un-rotated).
 //
-// decode_split_kernel: grid (split, kv-head, sequence). Each CTA streams up to
-// kTilesPerSplit packed tiles of one (sequence, kv-head) through 1-D bulk copies
-// (one 14336-byte record per tile) and runs the GQA group (up to 8 q-heads) on
-// m16n8k16 tensor-core MMAs with an online softmax in the log2 domain:
-//   QK^T: A = q' = q_r * r^K * s^K per channel (fp16 hi part in rows 0-7, fp16 lo
-//         part in rows 8-15, so the product carries ~22 bits of q'), B = 4-bit key
-//         codes converted to fp16 in registers; score_j = c^K_j (D_hi + D_lo + beta),
-//         beta = sum_i q_r,i r^K_i z^K_i.
-//   PV:   A = p' = p_j c^V_j s^V_j (hi / lo rows), B = 2-bit value codes;
-//         acc_i += r^V_i (D_hi + D_lo + gamma), gamma = sum_j p_j c^V_j z^V_j.
-// Partial (max, sum, acc) per split go to scratch; decode_merge_kernel merges the
-// splits with the fp16 workspace tokens of the partial last tile, un-rotates the
-// accumulator by H^T and normalises.
+// Three launches:
+//   decode_scan_kernel  - exclusive prefix of full tiles per sequence (scratch);
+//   decode_split_kernel - persistent, one CTA per SM, 7 warps. The flattened tile
+//     space (sequence, kv-head, tile) is cut into one contiguous range per warp
+//     (stream-K), so ragged batches balance to a tile. Each warp streams its
+//     range through two private 14336-byte bulk-copy (TMA) stages and runs its
+//     GQA group (up to 8 q-heads) on m16n8k16 tensor-core MMAs, with an online
+//     softmax in the log2 domain:
+//       QK^T: A = q' = q_r r^K s^K per channel, fp16 hi part in rows 0-7 and fp16
+//             lo part in rows 8-15 (q' carried to ~22 bits), B = 4-bit key codes
+//             turned into fp16 in registers; score_j = c^K_j (D_hi + D_lo + beta),
+//             beta = sum_i q_r,i r^K_i z^K_i;
+//       PV:   A = p' = p_j c^V_j s^V_j (hi/lo rows), B = 2-bit value codes;
+//             acc_i += r^V_i (D_hi + D_lo + gamma), gamma = sum_j p_j c^V_j z^V_j.
+//     Four independent accumulator chains keep the MMA pipe busy. When a warp's
+//     range crosses into a new (sequence, kv-head) it writes a partial record
+//     (acc, running max, running sum) for the one it leaves;
+//   decode_merge_kernel - per (sequence, kv-head): merges the partial records of
+//     the warps that covered it with the fp16 workspace tokens of the partial
+//     last tile, un-rotates by H^T and normalises.
 #include "kvarn_common.cuh"
 #include "kvarn_launch.h"
 
@@ -22,6 +29,12 @@ namespace kvarn {
 namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kWarps = 7;                       // consumer warps per CTA
+constexpr int kStages = 2;                      // bulk-copy stages per warp
+constexpr int kMaxCtas = 1024;                  // upper bound used to size scratch
+constexpr int kPartStride = 132;                // floats per q-head: acc[128], max, sum, pad
+constexpr int kRecFloats = 8 * kPartStride;     // one partial record (8 q-head slots)
+constexpr int kSplitSmem = kWarps * kStages * kRec + kWarps * kStages * 8;
 
 // fp32 pair -> (hi, lo) fp16 pairs with hi + lo ~ x to ~22 bits.
 __device__ __forceinline__ void split2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
@@ -38,8 +51,8 @@ __device__ __forceinline__ float2 h2pair(const uint16_t* p) {
 
 template <uint32_t kMask>
 __device__ __forceinline__ uint32_t lop_magic(uint32_t w) {
-  // (w & kMask) | 0x64006400: places the selected bits in the mantissa of two fp16
-  // values 1024 + field.
+  // (w & kMask) | 0x64006400: the selected bits become the low mantissa bits of two
+  // fp16 values 1024 + field
   uint32_t r;
   asm("lop3.b32 %0, %1, %2, %3, 0xea;" : "=r"(r) : "r"(w), "n"(kMask), "n"(0x64006400u));
   return r;
@@ -51,13 +64,14 @@ __device__ __forceinline__ uint32_t hfma2_u(uint32_t a, uint32_t b, uint32_t c) 
   return r;
 }
 
-// fp16x2 constants
-constexpr uint32_t kH_One = 0x3C003C00u;       // 1.0
+// fp16x2 constants: field = (1024 + scale * code) * (1/scale) - 1024/scale, exact
+constexpr uint32_t kH_One = 0x3C003C00u;       // 1
 constexpr uint32_t kH_M1024 = 0xE400E400u;     // -1024
 constexpr uint32_t kH_Sixteenth = 0x2C002C00u; // 1/16
 constexpr uint32_t kH_M64 = 0xD400D400u;       // -64
 constexpr uint32_t kH_Quarter = 0x34003400u;   // 1/4
 constexpr uint32_t kH_M256 = 0xDC00DC00u;      // -256
+constexpr uint32_t kH_64th = 0x24002400u;      // 1/64
 constexpr uint32_t kH_M16 = 0xCC00CC00u;       // -16
 
 __device__ __forceinline__ void mma16816(float* d, const uint32_t* a, uint32_t b0, uint32_t b1) {
@@ -66,6 +80,12 @@ __device__ __forceinline__ void mma16816(float* d, const uint32_t* a, uint32_t b
       "{%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 __device__ __forceinline__ float quad_sum(float x) {
@@ -84,333 +104,422 @@ struct DecodeArgs {
   const uint8_t* cache;
   const int32_t* block_tables;
   const int32_t* seq_lens;
-  float* part;          // [n_seqs][hkv][n_split][8][132]
+  int64_t* prefix;      // [n_seqs + 1] exclusive prefix of full tiles
+  float* part;          // [records][8][132]
   unsigned* flags;
   int64_t num_blocks;
+  int n_seqs;
   int hkv;
   int group;            // q-heads per kv-head (1..8)
   int max_blocks;
-  int n_split;
-  int tiles_per_split;
+  int n_ctas;           // CTAs of the split kernel
 };
 
-constexpr int kPartStride = 132;  // floats per (split, q-head) partial: acc[128], max, sum, 2 pad (16-byte rows)
+__device__ __forceinline__ int full_tiles(const DecodeArgs& a, int s) {
+  const int L = max(a.seq_lens[s], 0);
+  return min(L / kB, a.max_blocks);
+}
 
-template <int kWarps, int kStages>
-struct SplitSmem {
-  static constexpr int kOffStage = 0;
-  static constexpr int kOffQ = kWarps * kStages * kRec;          // fp32 [8][128]
-  static constexpr int kOffBar = kOffQ + 8 * 128 * 4;            // [kWarps][kStages] mbarriers
-  static constexpr int kBytes = kOffBar + kWarps * kStages * 8;
-  static_assert(kWarps * 8 * kPartStride * 4 <= kWarps * kStages * kRec, "merge area fits in stages");
-};
+// Range [beg, end) of global tiles owned by warp `wg` of the split kernel.
+__device__ __forceinline__ void warp_range(int64_t total, int n_ctas, int64_t wg, int64_t& beg, int64_t& end) {
+  const int64_t b = wg / kWarps, w = wg % kWarps;
+  const int64_t c0 = b * total / n_ctas, c1 = (b + 1) * total / n_ctas;
+  beg = c0 + w * (c1 - c0) / kWarps;
+  end = c0 + (w + 1) * (c1 - c0) / kWarps;
+}
 
-template <int kWarps, int kStages>
-__global__ void __launch_bounds__(kWarps * 32)
-    decode_split_kernel(DecodeArgs args) {
-  using S = SplitSmem<kWarps, kStages>;
-  extern __shared__ __align__(128) uint8_t smem[];
-  const int tid = threadIdx.x;
-  const int warp = tid >> 5, lane = tid & 31;
-  const int g = lane >> 2, c = lane & 3;
-  const int sp = blockIdx.x, h = blockIdx.y;
-  const int64_t s = blockIdx.z;
-
-  int L = args.seq_lens[s];
-  if (L < 0) L = 0;
-  int n_full = L / kB;
-  if (n_full > args.max_blocks) n_full = args.max_blocks;
-  const int t_begin = sp * args.tiles_per_split;
-  const int t_end = min(t_begin + args.tiles_per_split, n_full);
-  if (t_begin >= t_end) return;
-
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::kOffBar);
-  float* qs = reinterpret_cast<float*>(smem + S::kOffQ);
-  const int32_t* btab = args.block_tables + s * args.max_blocks;
-
-  if (tid < kWarps * kStages) mbar_init(&bars[tid], 1);
-  fence_mbar_init();
-  __syncthreads();
-
-  // ---- issue the first kStages loads of this warp's tiles
-  // warp `warp` takes tiles t_begin + warp + kWarps * k, k = 0, 1, ...
-  uint32_t valid_mask = 0;  // bit k%kStages: stage holds a valid tile
-  if (lane == 0) {
-    for (int k = 0; k < kStages; ++k) {
-      const int t = t_begin + warp + kWarps * k;
-      if (t >= t_end) break;
-      const int64_t blk = btab[t];
-      if (blk < 0 || blk >= args.num_blocks) {
-        raise_flag(args.flags, KVARN_FLAG_BAD_BLOCK);
-        continue;
-      }
-      uint64_t* bar = &bars[warp * kStages + k];
-      mbar_arrive_expect_tx(bar, kRec);
-      bulk_g2s(smem + S::kOffStage + (warp * kStages + k) * kRec,
-               args.cache + (blk * args.hkv + h) * static_cast<int64_t>(kRec), kRec, bar);
-      valid_mask |= 1u << k;
-    }
+// ------------------------------------------------------------------ scan
+__global__ void __launch_bounds__(1024) decode_scan_kernel(DecodeArgs a) {
+  __shared__ int64_t part_sums[1024];
+  const int t = threadIdx.x;
+  const int per = (a.n_seqs + 1023) / 1024;
+  const int s0 = min(t * per, a.n_seqs), s1 = min(s0 + per, a.n_seqs);
+  int64_t sum = 0;
+  bool clipped = false;
+  for (int s = s0; s < s1; ++s) {
+    sum += full_tiles(a, s);
+    clipped |= max(a.seq_lens[s], 0) / kB > a.max_blocks;
   }
-  valid_mask = __shfl_sync(0xffffffffu, valid_mask, 0);
-
-  // ---- q of the group, rotated: q_r2 = FWHT(q) * log2(e) / 128 (= H q * log2(e)/sqrt(128))
-  for (int idx = tid; idx < 8 * 128; idx += kWarps * 32) {
-    const int gg = idx >> 7, ch = idx & 127;
-    float v = 0.f;
-    if (gg < args.group)
-      v = h2f_bits(args.q[(s * args.hkv * args.group + static_cast<int64_t>(h) * args.group + gg) * kD + ch]);
-    qs[idx] = v;
-  }
+  if (clipped) raise_flag(a.flags, KVARN_FLAG_BAD_LENGTH);
+  part_sums[t] = sum;
   __syncthreads();
-  for (int st = 1; st < 128; st <<= 1) {
-    for (int idx = tid; idx < 8 * 64; idx += kWarps * 32) {
-      const int gg = idx >> 6, pr = idx & 63;
-      const int lo = ((pr / st) * 2 * st) + (pr % st);
-      const float u = qs[gg * 128 + lo], w = qs[gg * 128 + lo + st];
-      qs[gg * 128 + lo] = u + w;
-      qs[gg * 128 + lo + st] = u - w;
-    }
+  for (int off = 1; off < 1024; off <<= 1) {   // inclusive scan of the chunk sums
+    const int64_t v = t >= off ? part_sums[t - off] : 0;
+    __syncthreads();
+    part_sums[t] += v;
     __syncthreads();
   }
-  float qv[8][4];
+  int64_t run = t > 0 ? part_sums[t - 1] : 0;
+  for (int s = s0; s < s1; ++s) {
+    a.prefix[s] = run;
+    run += full_tiles(a, s);
+  }
+  if (t == 1023) a.prefix[a.n_seqs] = part_sums[1023];
+}
+
+// ------------------------------------------------------------------ tile cursor
+struct Cursor {
+  int s, h, ti, nf;
+};
+
+// sequence s holding global tile g (prefix[s]*hkv <= g < prefix[s+1]*hkv)
+__device__ __forceinline__ Cursor locate(const DecodeArgs& a, int64_t g) {
+  int lo = 0, hi = a.n_seqs - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (a.prefix[mid] * a.hkv <= g) lo = mid; else hi = mid - 1;
+  }
+  Cursor c;
+  c.s = lo;
+  c.nf = static_cast<int>(a.prefix[lo + 1] - a.prefix[lo]);
+  const int64_t off = g - a.prefix[lo] * a.hkv;
+  c.h = static_cast<int>(off / c.nf);
+  c.ti = static_cast<int>(off - static_cast<int64_t>(c.h) * c.nf);
+  return c;
+}
+
+__device__ __forceinline__ void advance(const DecodeArgs& a, Cursor& c) {
+  if (++c.ti < c.nf) return;
+  c.ti = 0;
+  if (++c.h < a.hkv) return;
+  c.h = 0;
+  do {
+    ++c.s;
+    c.nf = c.s < a.n_seqs ? static_cast<int>(a.prefix[c.s + 1] - a.prefix[c.s]) : 1;
+  } while (c.nf == 0);
+}
+
+// Lane 0: start the copy of the tile at cursor `c` into `stage`; a block index
+// outside [0, num_blocks) completes the barrier phase without data and returns false.
+__device__ __forceinline__ bool issue_tile(const DecodeArgs& a, const Cursor& c, uint8_t* stage, uint64_t* bar) {
+  const int64_t blk = a.block_tables[static_cast<int64_t>(c.s) * a.max_blocks + c.ti];
+  if (blk < 0 || blk >= a.num_blocks) {
+    raise_flag(a.flags, KVARN_FLAG_BAD_BLOCK);
+    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+    return false;
+  }
+  mbar_arrive_expect_tx(bar, kRec);
+  bulk_g2s(stage, a.cache + (blk * a.hkv + c.h) * static_cast<int64_t>(kRec), kRec, bar);
+  return true;
+}
+
+// q_r2 of this thread's 32 channels for (sequence s, kv-head h): H q * log2(e)/sqrt(128),
+// computed as FWHT(q) * log2(e) / 128. Thread (g, c) holds head g, channels
+// 16ks + 2c + {0, 1, 8, 9}; channel bits 1-2 live across the quad (lanes ^1, ^2).
+__device__ __forceinline__ void load_q(const DecodeArgs& a, int s, int h, int g, int c, float (&qv)[8][4]) {
+  const int hq = a.hkv * a.group;
+  if (g < a.group) {
+    const uint16_t* row = a.q + (static_cast<int64_t>(s) * hq + static_cast<int64_t>(h) * a.group + g) * kD;
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      const float2 p0 = h2pair(row + 16 * ks + 2 * c), p1 = h2pair(row + 16 * ks + 2 * c + 8);
+      qv[ks][0] = p0.x; qv[ks][1] = p0.y; qv[ks][2] = p1.x; qv[ks][3] = p1.y;
+    }
+  } else {
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) qv[ks][0] = qv[ks][1] = qv[ks][2] = qv[ks][3] = 0.f;
+  }
+#pragma unroll
+  for (int ks = 0; ks < 8; ++ks) {       // channel bits 0 and 3: inside the thread
+    const float u0 = qv[ks][0] + qv[ks][1], u1 = qv[ks][0] - qv[ks][1];
+    const float u2 = qv[ks][2] + qv[ks][3], u3 = qv[ks][2] - qv[ks][3];
+    qv[ks][0] = u0 + u2; qv[ks][2] = u0 - u2; qv[ks][1] = u1 + u3; qv[ks][3] = u1 - u3;
+  }
+#pragma unroll
+  for (int bit = 1; bit <= 2; bit <<= 1) {   // channel bits 1 and 2: across the quad
+    const bool upper = (c & bit) != 0;
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks)
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const float o = __shfl_xor_sync(0xffffffffu, qv[ks][t], bit);
+        qv[ks][t] = upper ? (o - qv[ks][t]) : (qv[ks][t] + o);
+      }
+  }
+#pragma unroll
+  for (int bit = 1; bit < 8; bit <<= 1)      // channel bits 4-6: the ks index
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks)
+      if ((ks & bit) == 0)
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const float u = qv[ks][t], w = qv[ks | bit][t];
+          qv[ks][t] = u + w;
+          qv[ks | bit][t] = u - w;
+        }
+#pragma unroll
+  for (int ks = 0; ks < 8; ++ks)
+#pragma unroll
+    for (int t = 0; t < 4; ++t) qv[ks][t] *= kLog2e / 128.0f;
+}
+
+// One packed tile: update the running (max, sum, acc) of head g.
+__device__ __forceinline__ void attend_tile(const uint8_t* rec, const float (&qv)[8][4], int g, int c, float& m_run,
+                                            float& l_run, float (&acc)[16][2]) {
+  const uint16_t* km = reinterpret_cast<const uint16_t*>(rec + kKMetaOff);
+  const uint16_t* vm = reinterpret_cast<const uint16_t*>(rec + kVMetaOff);
+
+  // q' fragments (hi rows g, lo rows g + 8) and beta
+  uint32_t A[8][4];
+  float beta = 0.f;
 #pragma unroll
   for (int ks = 0; ks < 8; ++ks) {
     const int ch0 = 16 * ks + 2 * c;
-    qv[ks][0] = qs[g * 128 + ch0] * (kLog2e / 128.0f);
-    qv[ks][1] = qs[g * 128 + ch0 + 1] * (kLog2e / 128.0f);
-    qv[ks][2] = qs[g * 128 + ch0 + 8] * (kLog2e / 128.0f);
-    qv[ks][3] = qs[g * 128 + ch0 + 9] * (kLog2e / 128.0f);
+    const float2 r0 = h2pair(km + ch0), r1 = h2pair(km + ch0 + 8);
+    const float2 s0 = h2pair(km + 256 + ch0), s1 = h2pair(km + 256 + ch0 + 8);
+    const float2 z0 = h2pair(km + 384 + ch0), z1 = h2pair(km + 384 + ch0 + 8);
+    split2(qv[ks][0] * (r0.x * s0.x), qv[ks][1] * (r0.y * s0.y), A[ks][0], A[ks][1]);
+    split2(qv[ks][2] * (r1.x * s1.x), qv[ks][3] * (r1.y * s1.y), A[ks][2], A[ks][3]);
+    beta = fmaf(qv[ks][0], r0.x * z0.x, beta);
+    beta = fmaf(qv[ks][1], r0.y * z0.y, beta);
+    beta = fmaf(qv[ks][2], r1.x * z1.x, beta);
+    beta = fmaf(qv[ks][3], r1.y * z1.y, beta);
   }
+  beta = quad_sum(beta);
 
-  float m_run = -INFINITY, l_run = 0.f;
-  float acc[16][2];
+  // scores of tokens 8nt + 2c + {0, 1}, four n-tiles at a time (independent chains)
+  float sc[16][2];
 #pragma unroll
-  for (int n = 0; n < 16; ++n) acc[n][0] = acc[n][1] = 0.f;
-
-  int k = 0;
-  uint32_t phase_bits = 0;  // per stage: parity of the next phase to wait for
-  for (int t = t_begin + warp; t < t_end; t += kWarps, ++k) {
-    const int stg = k % kStages;
-    if ((valid_mask >> stg) & 1u) {
-      const bool ok = __all_sync(0xffffffffu, mbar_wait(&bars[warp * kStages + stg], (phase_bits >> stg) & 1u,
-                                                        args.flags));
-      phase_bits ^= 1u << stg;
-      if (!ok) break;  // a copy never arrived: stop this warp (flag raised)
-      {
-        const uint8_t* rec = smem + S::kOffStage + (warp * kStages + stg) * kRec;
-        const uint16_t* km = reinterpret_cast<const uint16_t*>(rec + kKMetaOff);
-        const uint16_t* vm = reinterpret_cast<const uint16_t*>(rec + kVMetaOff);
-
-        // -- q' fragments (hi/lo rows) and beta
-        uint32_t A[8][4];
-        float beta = 0.f;
+  for (int ntg = 0; ntg < 4; ++ntg) {
+    uint32_t kw[4][4];
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-          const int ch0 = 16 * ks + 2 * c;
-          const float2 r0 = h2pair(km + ch0), r1 = h2pair(km + ch0 + 8);
-          const float2 s0 = h2pair(km + 256 + ch0), s1 = h2pair(km + 256 + ch0 + 8);
-          const float2 z0 = h2pair(km + 384 + ch0), z1 = h2pair(km + 384 + ch0 + 8);
-          split2(qv[ks][0] * (r0.x * s0.x), qv[ks][1] * (r0.y * s0.y), A[ks][0], A[ks][1]);
-          split2(qv[ks][2] * (r1.x * s1.x), qv[ks][3] * (r1.y * s1.y), A[ks][2], A[ks][3]);
-          beta = fmaf(qv[ks][0], r0.x * z0.x, beta);
-          beta = fmaf(qv[ks][1], r0.y * z0.y, beta);
-          beta = fmaf(qv[ks][2], r1.x * z1.x, beta);
-          beta = fmaf(qv[ks][3], r1.y * z1.y, beta);
-        }
-        beta = quad_sum(beta);
-
-        // -- scores for tokens 8nt + 2c + {0,1}
-        float sc[16][2];
+    for (int j = 0; j < 4; ++j) {
+      const uint4 v = *reinterpret_cast<const uint4*>(rec + kKCodeOff + (8 * (4 * ntg + j) + g) * 64 + c * 16);
+      kw[j][0] = v.x; kw[j][1] = v.y; kw[j][2] = v.z; kw[j][3] = v.w;
+    }
+    float d[4][4];
 #pragma unroll
-        for (int nt = 0; nt < 16; ++nt) {
-          const uint4 kw = *reinterpret_cast<const uint4*>(rec + kKCodeOff + (8 * nt + g) * 64 + c * 16);
-          const uint32_t words[4] = {kw.x, kw.y, kw.z, kw.w};
-          float d[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int j = 0; j < 4; ++j) d[j][0] = d[j][1] = d[j][2] = d[j][3] = 0.f;
 #pragma unroll
-          for (int m = 0; m < 4; ++m) {
-            const uint32_t w0 = words[m], w8 = words[m] >> 8;
-            const uint32_t b00 = hfma2_u(lop_magic<0x000F000Fu>(w0), kH_One, kH_M1024);
-            const uint32_t b01 = hfma2_u(lop_magic<0x00F000F0u>(w0), kH_Sixteenth, kH_M64);
-            mma16816(d, A[2 * m], b00, b01);
-            const uint32_t b10 = hfma2_u(lop_magic<0x000F000Fu>(w8), kH_One, kH_M1024);
-            const uint32_t b11 = hfma2_u(lop_magic<0x00F000F0u>(w8), kH_Sixteenth, kH_M64);
-            mma16816(d, A[2 * m + 1], b10, b11);
-          }
-          const float2 ck = h2pair(km + 128 + 8 * nt + 2 * c);
-          sc[nt][0] = ck.x * ((d[0] + d[2]) + beta);
-          sc[nt][1] = ck.y * ((d[1] + d[3]) + beta);
-        }
-
-        // -- online softmax (log2 domain), head g
-        float tmax = -INFINITY;
+    for (int m = 0; m < 4; ++m)
 #pragma unroll
-        for (int nt = 0; nt < 16; ++nt) tmax = fmaxf(tmax, fmaxf(sc[nt][0], sc[nt][1]));
-        tmax = quad_max(tmax);
-        const float m_new = fmaxf(m_run, tmax);
-        const float corr = exp2f(m_run - m_new);
-        m_run = m_new;
-        float lsum = 0.f;
-#pragma unroll
-        for (int nt = 0; nt < 16; ++nt) {
-          sc[nt][0] = exp2f(sc[nt][0] - m_new);
-          sc[nt][1] = exp2f(sc[nt][1] - m_new);
-          lsum += sc[nt][0] + sc[nt][1];
-        }
-        l_run = fmaf(l_run, corr, lsum);
-#pragma unroll
-        for (int n = 0; n < 16; ++n) {
-          acc[n][0] *= corr;
-          acc[n][1] *= corr;
-        }
-
-        // -- p' fragments and gamma; tokens 16ks + 2c + {0,1} (nt = 2ks), +8 (nt = 2ks+1)
-        float gamma = 0.f;
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-          const int t0 = 16 * ks + 2 * c;
-          const float2 c0 = h2pair(vm + 128 + t0), c1 = h2pair(vm + 128 + t0 + 8);
-          const float2 s0 = h2pair(vm + 256 + t0), s1 = h2pair(vm + 256 + t0 + 8);
-          const float2 z0 = h2pair(vm + 384 + t0), z1 = h2pair(vm + 384 + t0 + 8);
-          const float p0 = sc[2 * ks][0], p1 = sc[2 * ks][1], p2 = sc[2 * ks + 1][0], p3 = sc[2 * ks + 1][1];
-          split2(p0 * (c0.x * s0.x), p1 * (c0.y * s0.y), A[ks][0], A[ks][1]);
-          split2(p2 * (c1.x * s1.x), p3 * (c1.y * s1.y), A[ks][2], A[ks][3]);
-          gamma = fmaf(p0, c0.x * z0.x, gamma);
-          gamma = fmaf(p1, c0.y * z0.y, gamma);
-          gamma = fmaf(p2, c1.x * z1.x, gamma);
-          gamma = fmaf(p3, c1.y * z1.y, gamma);
-        }
-        gamma = quad_sum(gamma);
-
-        // -- PV over channel n-tiles 8*nt2 + {0..7}; one 16-byte cell serves nt2 = 2np, 2np+1
-#pragma unroll
-        for (int np = 0; np < 8; ++np) {
-          const uint4 vw = *reinterpret_cast<const uint4*>(rec + kVCodeOff + np * 512 + (g * 4 + c) * 16);
-          const uint32_t words[2][2] = {{vw.x, vw.y}, {vw.z, vw.w}};
-#pragma unroll
-          for (int which = 0; which < 2; ++which) {
-            float d[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-#pragma unroll
-              for (int sg = 0; sg < 2; ++sg) {
-                const uint32_t w = sg ? (words[which][u] >> 8) : words[which][u];
-                // crumb q = 2*(ks&1) + type at shift sg; ks = 4u + 2sg + (q>>1)
-                const uint32_t q0 = hfma2_u(lop_magic<0x00030003u>(w), kH_One, kH_M1024);
-                const uint32_t q1 = hfma2_u(lop_magic<0x000C000Cu>(w), kH_Quarter, kH_M256);
-                const uint32_t q2 = hfma2_u(lop_magic<0x00300030u>(w), kH_Sixteenth, kH_M64);
-                const uint32_t q3 = hfma2_u(lop_magic<0x00C000C0u>(w), 0x24002400u /*1/64*/, kH_M16);
-                mma16816(d, A[4 * u + 2 * sg + 0], q0, q1);
-                mma16816(d, A[4 * u + 2 * sg + 1], q2, q3);
-              }
-            }
-            const int nt2 = 2 * np + which;
-            const float2 rv = h2pair(vm + 8 * nt2 + 2 * c);
-            acc[nt2][0] = fmaf(rv.x, (d[0] + d[2]) + gamma, acc[nt2][0]);
-            acc[nt2][1] = fmaf(rv.y, (d[1] + d[3]) + gamma, acc[nt2][1]);
-          }
-        }
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t w0 = kw[j][m], w8 = kw[j][m] >> 8;
+        mma16816(d[j], A[2 * m], hfma2_u(lop_magic<0x000F000Fu>(w0), kH_One, kH_M1024),
+                 hfma2_u(lop_magic<0x00F000F0u>(w0), kH_Sixteenth, kH_M64));
+        mma16816(d[j], A[2 * m + 1], hfma2_u(lop_magic<0x000F000Fu>(w8), kH_One, kH_M1024),
+                 hfma2_u(lop_magic<0x00F000F0u>(w8), kH_Sixteenth, kH_M64));
       }
-    }
-    __syncwarp();
-    // refill this stage with the warp's tile k + kStages
-    const int tn = t + kWarps * kStages;
-    if (tn < t_end) {
-      bool issued = false;
-      if (lane == 0) {
-        const int64_t blk = btab[tn];
-        if (blk < 0 || blk >= args.num_blocks) {
-          raise_flag(args.flags, KVARN_FLAG_BAD_BLOCK);
-        } else {
-          uint64_t* bar = &bars[warp * kStages + stg];
-          mbar_arrive_expect_tx(bar, kRec);
-          bulk_g2s(smem + S::kOffStage + (warp * kStages + stg) * kRec,
-                   args.cache + (blk * args.hkv + h) * static_cast<int64_t>(kRec), kRec, bar);
-          issued = true;
-        }
-      }
-      issued = __shfl_sync(0xffffffffu, issued, 0);
-      if (issued) valid_mask |= 1u << stg; else valid_mask &= ~(1u << stg);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int nt = 4 * ntg + j;
+      const float2 ck = h2pair(km + 128 + 8 * nt + 2 * c);
+      sc[nt][0] = ck.x * ((d[j][0] + d[j][2]) + beta);
+      sc[nt][1] = ck.y * ((d[j][1] + d[j][3]) + beta);
     }
   }
 
-  // ---- merge the warps of this CTA through shared memory, write the split partial
-  l_run = quad_sum(l_run);
-  __syncthreads();  // every warp has consumed all of its stages
-  float* mrg = reinterpret_cast<float*>(smem + S::kOffStage);
-  {
-    float* mw = mrg + (warp * 8 + g) * kPartStride;
+  // online softmax (log2 domain)
+  float tmax = -INFINITY;
 #pragma unroll
-    for (int n = 0; n < 16; ++n) {
-      mw[8 * n + 2 * c] = acc[n][0];
-      mw[8 * n + 2 * c + 1] = acc[n][1];
-    }
-    if (c == 0) {
-      mw[128] = m_run;
-      mw[129] = l_run;
-    }
+  for (int nt = 0; nt < 16; ++nt) tmax = fmaxf(tmax, fmaxf(sc[nt][0], sc[nt][1]));
+  tmax = quad_max(tmax);
+  const float m_new = fmaxf(m_run, tmax);
+  const float corr = ex2(m_run - m_new);
+  m_run = m_new;
+  float lsum = 0.f;
+#pragma unroll
+  for (int nt = 0; nt < 16; ++nt) {
+    sc[nt][0] = ex2(sc[nt][0] - m_new);
+    sc[nt][1] = ex2(sc[nt][1] - m_new);
+    lsum += sc[nt][0] + sc[nt][1];
   }
-  __syncthreads();
-  float* out = args.part + ((s * args.hkv + h) * args.n_split + sp) * (8 * kPartStride);
-  for (int idx = tid; idx < args.group * 128; idx += kWarps * 32) {
-    const int gg = idx >> 7, ch = idx & 127;
-    float M = -INFINITY;
+  l_run = fmaf(l_run, corr, lsum);
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, mrg[(w * 8 + gg) * kPartStride + 128]);
-    float a = 0.f, l = 0.f;
+  for (int n = 0; n < 16; ++n) {
+    acc[n][0] *= corr;
+    acc[n][1] *= corr;
+  }
+
+  // p' fragments and gamma; tokens 16ks + 2c + {0,1} (nt = 2ks) and + {8,9} (nt = 2ks+1)
+  float gamma = 0.f;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
-      const float mw = mrg[(w * 8 + gg) * kPartStride + 128];
-      const float f = (mw == -INFINITY) ? 0.f : exp2f(mw - M);
-      a = fmaf(mrg[(w * 8 + gg) * kPartStride + ch], f, a);
-      l = fmaf(mrg[(w * 8 + gg) * kPartStride + 129], f, l);
+  for (int ks = 0; ks < 8; ++ks) {
+    const int t0 = 16 * ks + 2 * c;
+    const float2 c0 = h2pair(vm + 128 + t0), c1 = h2pair(vm + 128 + t0 + 8);
+    const float2 s0 = h2pair(vm + 256 + t0), s1 = h2pair(vm + 256 + t0 + 8);
+    const float2 z0 = h2pair(vm + 384 + t0), z1 = h2pair(vm + 384 + t0 + 8);
+    const float p0 = sc[2 * ks][0], p1 = sc[2 * ks][1], p2 = sc[2 * ks + 1][0], p3 = sc[2 * ks + 1][1];
+    split2(p0 * (c0.x * s0.x), p1 * (c0.y * s0.y), A[ks][0], A[ks][1]);
+    split2(p2 * (c1.x * s1.x), p3 * (c1.y * s1.y), A[ks][2], A[ks][3]);
+    gamma = fmaf(p0, c0.x * z0.x, gamma);
+    gamma = fmaf(p1, c0.y * z0.y, gamma);
+    gamma = fmaf(p2, c1.x * z1.x, gamma);
+    gamma = fmaf(p3, c1.y * z1.y, gamma);
+  }
+  gamma = quad_sum(gamma);
+
+  // PV: channel n-tile nt2 = 2np + which; cell (g, c) of panel np serves both `which`;
+  // two panels at a time -> four independent chains
+#pragma unroll
+  for (int npg = 0; npg < 4; ++npg) {
+    uint32_t vw[2][4];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const uint4 v = *reinterpret_cast<const uint4*>(rec + kVCodeOff + (2 * npg + i) * 512 + (g * 4 + c) * 16);
+      vw[i][0] = v.x; vw[i][1] = v.y; vw[i][2] = v.z; vw[i][3] = v.w;   // [which*2 + u]
     }
-    out[gg * kPartStride + ch] = a;
-    if (ch == 0) {
-      out[gg * kPartStride + 128] = M;
-      out[gg * kPartStride + 129] = l;
+    float d[4][4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) d[j][0] = d[j][1] = d[j][2] = d[j][3] = 0.f;
+#pragma unroll
+    for (int u = 0; u < 2; ++u)
+#pragma unroll
+      for (int sg = 0; sg < 2; ++sg)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int i = j >> 1, which = j & 1;
+          const uint32_t w = sg ? (vw[i][which * 2 + u] >> 8) : vw[i][which * 2 + u];
+          // crumb q = 2*(ks&1) + type at shift sg; ks = 4u + 2sg + (q >> 1)
+          mma16816(d[j], A[4 * u + 2 * sg], hfma2_u(lop_magic<0x00030003u>(w), kH_One, kH_M1024),
+                   hfma2_u(lop_magic<0x000C000Cu>(w), kH_Quarter, kH_M256));
+          mma16816(d[j], A[4 * u + 2 * sg + 1], hfma2_u(lop_magic<0x00300030u>(w), kH_Sixteenth, kH_M64),
+                   hfma2_u(lop_magic<0x00C000C0u>(w), kH_64th, kH_M16));
+        }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int nt2 = 2 * (2 * npg + (j >> 1)) + (j & 1);
+      const float2 rv = h2pair(vm + 8 * nt2 + 2 * c);
+      acc[nt2][0] = fmaf(rv.x, (d[j][0] + d[j][2]) + gamma, acc[nt2][0]);
+      acc[nt2][1] = fmaf(rv.y, (d[j][1] + d[j][3]) + gamma, acc[nt2][1]);
     }
   }
 }
 
+// Partial record of one (sequence, kv-head) over the tiles this warp attended.
+__device__ __forceinline__ void flush_record(const DecodeArgs& a, int64_t rec_idx, int g, int c, float m_run,
+                                             float l_run, const float (&acc)[16][2]) {
+  const float l = quad_sum(l_run);
+  if (g >= a.group) return;
+  float* out = a.part + rec_idx * kRecFloats + g * kPartStride;
+#pragma unroll
+  for (int n = 0; n < 16; ++n) *reinterpret_cast<float2*>(out + 8 * n + 2 * c) = make_float2(acc[n][0], acc[n][1]);
+  if (c == 0) *reinterpret_cast<float2*>(out + 128) = make_float2(m_run, l);
+}
+
+__global__ void __launch_bounds__(kWarps * 32, 1) decode_split_kernel(DecodeArgs a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, c = lane & 3;
+  const int64_t wg = static_cast<int64_t>(blockIdx.x) * kWarps + warp;
+  const int64_t total = a.prefix[a.n_seqs] * a.hkv;
+  int64_t gb, ge;
+  warp_range(total, a.n_ctas, wg, gb, ge);
+  if (gb >= ge) return;   // warps are independent: no CTA-wide barrier below
+
+  uint8_t* stages = smem + warp * kStages * kRec;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kWarps * kStages * kRec) + warp * kStages;
+  if (lane == 0) {
+    for (int k = 0; k < kStages; ++k) mbar_init(&bars[k], 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+
+  // load cursor (tiles being copied) runs kStages tiles ahead of the compute cursor
+  Cursor lc = locate(a, gb);
+  Cursor cc = lc;
+  uint32_t valid = 0;
+  for (int k = 0; k < kStages && gb + k < ge; ++k) {
+    if (k > 0) advance(a, lc);
+    bool ok = false;
+    if (lane == 0) ok = issue_tile(a, lc, stages + k * kRec, &bars[k]);
+    if (__shfl_sync(0xffffffffu, ok, 0)) valid |= 1u << k;
+  }
+
+  float qv[8][4];
+  float acc[16][2];
+  float m_run = -INFINITY, l_run = 0.f;
+  int64_t unit = -1;
+  uint32_t phase = 0;
+  for (int64_t k = 0; gb + k < ge; ++k) {
+    const int stg = static_cast<int>(k % kStages);
+    const int64_t u = static_cast<int64_t>(cc.s) * a.hkv + cc.h;
+    if (u != unit) {
+      if (unit >= 0) flush_record(a, wg + unit, g, c, m_run, l_run, acc);
+      unit = u;
+      load_q(a, cc.s, cc.h, g, c, qv);
+      m_run = -INFINITY;
+      l_run = 0.f;
+#pragma unroll
+      for (int n = 0; n < 16; ++n) acc[n][0] = acc[n][1] = 0.f;
+    }
+    const bool ok = __all_sync(0xffffffffu, mbar_wait(&bars[stg], (phase >> stg) & 1u, a.flags));
+    phase ^= 1u << stg;
+    if (!ok) break;   // a copy never arrived (flag raised): stop this warp
+    if ((valid >> stg) & 1u) attend_tile(stages + stg * kRec, qv, g, c, m_run, l_run, acc);
+    __syncwarp();
+    if (gb + k + kStages < ge) {     // refill this stage with the tile kStages ahead
+      advance(a, lc);
+      bool issued = false;
+      if (lane == 0) issued = issue_tile(a, lc, stages + stg * kRec, &bars[stg]);
+      if (__shfl_sync(0xffffffffu, issued, 0)) valid |= 1u << stg; else valid &= ~(1u << stg);
+    }
+    advance(a, cc);
+  }
+  if (unit >= 0) flush_record(a, wg + unit, g, c, m_run, l_run, acc);
+}
+
+// ------------------------------------------------------------------ merge
 // One CTA per (kv-head, sequence), one warp per q-head of the group; lane l owns
 // channels 4l..4l+3.
-__global__ void __launch_bounds__(256) decode_merge_kernel(DecodeArgs args, const uint16_t* __restrict__ ws,
+__global__ void __launch_bounds__(256) decode_merge_kernel(DecodeArgs a, const uint16_t* __restrict__ ws,
                                                            uint16_t* __restrict__ out) {
   __shared__ float sc[8][128];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = blockIdx.x;
-  const int64_t s = blockIdx.y;
+  const int s = blockIdx.y;
   const int gg = warp;
-  int L = args.seq_lens[s];
-  if (L < 0) L = 0;
-  int n_full = L / kB;
-  if (n_full > args.max_blocks) {
-    n_full = args.max_blocks;
-    if (threadIdx.x == 0 && h == 0) raise_flag(args.flags, KVARN_FLAG_BAD_LENGTH);
-  }
+  if (gg >= a.group) return;
+  const int L = max(a.seq_lens[s], 0);
+  const int nf = full_tiles(a, s);
   int n_ws = L % kB;
   if (n_ws > 0 && ws == nullptr) {  // tail tokens without a workspace: attend the tiles only
     n_ws = 0;
-    if (threadIdx.x == 0) raise_flag(args.flags, KVARN_FLAG_BAD_LENGTH);
+    if (lane == 0) raise_flag(a.flags, KVARN_FLAG_BAD_LENGTH);
   }
-  const int n_sp = (n_full + args.tiles_per_split - 1) / args.tiles_per_split;
-  if (gg >= args.group) return;
-  const int64_t qrow = (s * args.hkv * args.group + static_cast<int64_t>(h) * args.group + gg) * kD;
+  const int64_t qrow = (static_cast<int64_t>(s) * a.hkv * a.group + static_cast<int64_t>(h) * a.group + gg) * kD;
+  const int64_t u = static_cast<int64_t>(s) * a.hkv + h;
+  const int64_t n_warps = static_cast<int64_t>(a.n_ctas) * kWarps;
 
-  const float* part = args.part + ((s * args.hkv + h) * args.n_split) * (8 * kPartStride) + gg * kPartStride;
+  // warps whose ranges cover this unit's tiles [t0, t1)
+  int64_t wlo = 0, whi = 0;
+  const int64_t total = a.prefix[a.n_seqs] * a.hkv;
+  const int64_t t0 = a.prefix[s] * a.hkv + static_cast<int64_t>(h) * nf, t1 = t0 + nf;
+  if (nf > 0) {
+    int64_t lo = 0, hi = n_warps - 1;   // first warp with end > t0
+    while (lo < hi) {
+      const int64_t mid = (lo + hi) >> 1;
+      int64_t b, e;
+      warp_range(total, a.n_ctas, mid, b, e);
+      if (e > t0) hi = mid; else lo = mid + 1;
+    }
+    wlo = lo;
+    whi = lo;
+    while (whi < n_warps) {   // warps whose ranges start before t1
+      int64_t b, e;
+      warp_range(total, a.n_ctas, whi, b, e);
+      if (b >= t1) break;
+      ++whi;
+    }
+  }
+
   float M = -INFINITY;
-  for (int p = 0; p < n_sp; ++p) M = fmaxf(M, part[p * 8 * kPartStride + 128]);
-
+  for (int64_t w = wlo; w < whi; ++w) {
+    int64_t b, e;
+    warp_range(total, a.n_ctas, w, b, e);
+    if (b < e) M = fmaxf(M, a.part[(w + u) * kRecFloats + gg * kPartStride + 128]);
+  }
   // workspace tokens: exact fp16 K/V, unrotated
-  const uint16_t* wk = ws ? ws + ((s * args.hkv + h) * 2 + 0) * static_cast<int64_t>(kB * kD) : nullptr;
-  const uint16_t* wv = ws ? ws + ((s * args.hkv + h) * 2 + 1) * static_cast<int64_t>(kB * kD) : nullptr;
+  const int64_t wbase = (static_cast<int64_t>(s) * a.hkv + h) * 2 * static_cast<int64_t>(kB * kD);
+  const uint16_t* wk = ws ? ws + wbase : nullptr;
+  const uint16_t* wv = ws ? ws + wbase + kB * kD : nullptr;
   float qf[4];
 #pragma unroll
-  for (int u = 0; u < 4; ++u) qf[u] = h2f_bits(args.q[qrow + 4 * lane + u]) * (kLog2e * kInvSqrt128);
+  for (int k = 0; k < 4; ++k) qf[k] = h2f_bits(a.q[qrow + 4 * lane + k]) * (kLog2e * kInvSqrt128);
   for (int t = 0; t < n_ws; ++t) {
     float d = 0.f;
 #pragma unroll
-    for (int u = 0; u < 4; ++u) d = fmaf(qf[u], h2f_bits(wk[t * kD + 4 * lane + u]), d);
+    for (int k = 0; k < 4; ++k) d = fmaf(qf[k], h2f_bits(wk[t * kD + 4 * lane + k]), d);
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
     if (lane == 0) sc[gg][t] = d;
@@ -420,26 +529,29 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(DecodeArgs args, cons
 
   float acc[4] = {0.f, 0.f, 0.f, 0.f}, wacc[4] = {0.f, 0.f, 0.f, 0.f};
   float l = 0.f;
-  for (int p = 0; p < n_sp; ++p) {
-    const float* pp = part + p * 8 * kPartStride;
+  for (int64_t w = wlo; w < whi; ++w) {
+    int64_t b, e;
+    warp_range(total, a.n_ctas, w, b, e);
+    if (b >= e) continue;
+    const float* pp = a.part + (w + u) * kRecFloats + gg * kPartStride;
     const float mp = pp[128];
     const float f = (mp == -INFINITY) ? 0.f : exp2f(mp - M);
     l = fmaf(pp[129], f, l);
-    const float4 a = *reinterpret_cast<const float4*>(pp + 4 * lane);
-    acc[0] = fmaf(a.x, f, acc[0]);
-    acc[1] = fmaf(a.y, f, acc[1]);
-    acc[2] = fmaf(a.z, f, acc[2]);
-    acc[3] = fmaf(a.w, f, acc[3]);
+    const float4 v = *reinterpret_cast<const float4*>(pp + 4 * lane);
+    acc[0] = fmaf(v.x, f, acc[0]);
+    acc[1] = fmaf(v.y, f, acc[1]);
+    acc[2] = fmaf(v.z, f, acc[2]);
+    acc[3] = fmaf(v.w, f, acc[3]);
   }
   for (int t = 0; t < n_ws; ++t) {
     const float pw = exp2f(sc[gg][t] - M);
     l += pw;
 #pragma unroll
-    for (int u = 0; u < 4; ++u) wacc[u] = fmaf(pw, h2f_bits(wv[t * kD + 4 * lane + u]), wacc[u]);
+    for (int k = 0; k < 4; ++k) wacc[k] = fmaf(pw, h2f_bits(wv[t * kD + 4 * lane + k]), wacc[k]);
   }
   // un-rotate: FWHT over the 128 channels (4 per lane), then scale by 1/sqrt(128)
   {
-    float a0 = acc[0] + acc[1], a1 = acc[0] - acc[1], a2 = acc[2] + acc[3], a3 = acc[2] - acc[3];
+    const float a0 = acc[0] + acc[1], a1 = acc[0] - acc[1], a2 = acc[2] + acc[3], a3 = acc[2] - acc[3];
     acc[0] = a0 + a2;
     acc[1] = a1 + a3;
     acc[2] = a0 - a2;
@@ -448,61 +560,58 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(DecodeArgs args, cons
     for (int o = 1; o < 32; o <<= 1) {
       const bool upper = (lane & o) != 0;
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const float other = __shfl_xor_sync(0xffffffffu, acc[u], o);
-        acc[u] = upper ? (other - acc[u]) : (acc[u] + other);
+      for (int k = 0; k < 4; ++k) {
+        const float other = __shfl_xor_sync(0xffffffffu, acc[k], o);
+        acc[k] = upper ? (other - acc[k]) : (acc[k] + other);
       }
     }
   }
   const float inv_l = (l > 0.f) ? 1.0f / l : 0.f;
   uint16_t res[4];
 #pragma unroll
-  for (int u = 0; u < 4; ++u) res[u] = f2h_bits(fmaf(acc[u], kInvSqrt128, wacc[u]) * inv_l);
+  for (int k = 0; k < 4; ++k) res[k] = f2h_bits(fmaf(acc[k], kInvSqrt128, wacc[k]) * inv_l);
   *reinterpret_cast<uint2*>(out + qrow + 4 * lane) =
       make_uint2(res[0] | (static_cast<uint32_t>(res[1]) << 16), res[2] | (static_cast<uint32_t>(res[3]) << 16));
 }
 
+size_t prefix_bytes(int n_seqs) { return ((static_cast<size_t>(n_seqs) + 1) * sizeof(int64_t) + 255) & ~size_t(255); }
+
 }  // namespace
 
-int decode_tiles_per_split(int max_blocks) {
-  (void)max_blocks;
-  return 16;
-}
-
-int decode_num_splits(int max_blocks) {
-  const int c = decode_tiles_per_split(max_blocks);
-  return max_blocks <= 0 ? 1 : (max_blocks + c - 1) / c;
-}
-
 size_t decode_part_bytes(int n_seqs, int hkv, int max_blocks) {
-  return static_cast<size_t>(n_seqs) * hkv * decode_num_splits(max_blocks) * 8 * kPartStride * sizeof(float);
+  (void)max_blocks;
+  const size_t records = static_cast<size_t>(kMaxCtas) * kWarps + static_cast<size_t>(n_seqs) * hkv;
+  return prefix_bytes(n_seqs) + records * kRecFloats * sizeof(float);
 }
 
 cudaError_t launch_decode(const uint16_t* q, const uint8_t* cache, const uint16_t* ws, const int32_t* block_tables,
                           const int32_t* seq_lens, int n_seqs, int hkv, int group, int max_blocks, int64_t num_blocks,
                           uint16_t* out, void* scratch, unsigned* flags, cudaStream_t stream) {
   if (n_seqs <= 0) return cudaSuccess;
-  constexpr int kW = 4, kS = 1;
-  using S = SplitSmem<kW, kS>;
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   DecodeArgs a;
   a.q = q;
   a.cache = cache;
   a.block_tables = block_tables;
   a.seq_lens = seq_lens;
-  a.part = static_cast<float*>(scratch);
+  a.prefix = static_cast<int64_t*>(scratch);
+  a.part = reinterpret_cast<float*>(static_cast<uint8_t*>(scratch) + prefix_bytes(n_seqs));
   a.flags = flags;
   a.num_blocks = num_blocks;
+  a.n_seqs = n_seqs;
   a.hkv = hkv;
   a.group = group;
   a.max_blocks = max_blocks;
-  a.n_split = decode_num_splits(max_blocks);
-  a.tiles_per_split = decode_tiles_per_split(max_blocks);
-  cudaError_t err =
-      cudaFuncSetAttribute(decode_split_kernel<kW, kS>, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kBytes);
+  a.n_ctas = sms > 0 ? (sms < kMaxCtas ? sms : kMaxCtas) : 1;
+  decode_scan_kernel<<<1, 1024, 0, stream>>>(a);
+  cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   if (max_blocks > 0) {
-    dim3 grid(a.n_split, hkv, n_seqs);
-    decode_split_kernel<kW, kS><<<grid, kW * 32, S::kBytes, stream>>>(a);
+    err = cudaFuncSetAttribute(decode_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSplitSmem);
+    if (err != cudaSuccess) return err;
+    decode_split_kernel<<<a.n_ctas, kWarps * 32, kSplitSmem, stream>>>(a);
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
   }

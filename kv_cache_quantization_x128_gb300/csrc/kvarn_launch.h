@@ -19,7 +19,7 @@ cudaError_t launch_decode(const uint16_t* q, const uint8_t* cache, const uint16_
                           const int32_t* seq_lens, int n_seqs, int hkv, int group, int max_blocks, int64_t num_blocks,
                           uint16_t* out, void* scratch, unsigned* flags, cudaStream_t stream);
 
-int decode_num_splits(int max_blocks);
+// Device scratch of launch_decode: tile prefix per sequence + partial records.
 size_t decode_part_bytes(int n_seqs, int hkv, int max_blocks);
 
 }  // namespace kvarn
