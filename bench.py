@@ -35,6 +35,33 @@ PREFILL = dict(n_seqs=16, seq_len=16384, n_kv_heads=8, seed=1)
 DECODE = dict(n_seqs=64, seq_len=16384, n_kv_heads=8, n_q_heads=64, seed=2)
 RECORD = 14336
 WORKLOAD = "prefill_quantize_16x16k + decode_attn_64x16k_gqa64/8"
+# Reduced shapes for profiler captures (`--case small`): still larger than L2, a
+# few hundred MB on the device. Not a bench line.
+SMALL = dict(prefill=dict(n_seqs=4, seq_len=16384, n_kv_heads=8, seed=1),
+             decode=dict(n_seqs=16, seq_len=16384, n_kv_heads=8, n_q_heads=64, seed=2),
+             workload="profiling case: prefill_quantize_4x16k + decode_attn_16x16k_gqa64/8")
+
+
+def reduce_max(values, world: int):
+    """Max over ranks of per-rank timings (gloo all-reduce on CPU tensors)."""
+    if world <= 1:
+        return [float(v) for v in values]
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t]
+
+
+# fp32 flops the method needs per fp16 element on the quantize path (the Hadamard
+# runs on tensor cores and is not counted): 4 iterations x 2 passes x (deviation FMA
+# 2 + running sum 1 + square FMA 2) = 40, plus y, group extremes and the code (10).
+Q_FLOP_PER_ELEMENT = 50
+
+
+def fp32_peak_tflops():
+    # 152 SMs x 128 fp32 lanes x 2 flop per FMA x 2.07 GHz maximum SM clock
+    return round(152 * 128 * 2 * 2.07e9 / 1e12, 2)
 
 
 def hbm_peak():
@@ -234,10 +261,7 @@ def run_gpu(args):
     d2h = S["out_h"].numel() * 2
 
     # max over ranks
-    if world > 1:
-        t = torch.tensor([total_ms, e2e_ms, max(q_ms), max(d_ms)], dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms, e2e_ms = float(t[0]), float(t[1])
+    total_ms, e2e_ms = reduce_max([total_ms, e2e_ms], world)
 
     p, d = PREFILL, DECODE
     q_bytes = p["n_seqs"] * p["seq_len"] * p["n_kv_heads"] * 128 * 2 * 2
@@ -247,10 +271,17 @@ def run_gpu(args):
     peak, peak_kind = hbm_peak()
     qm, dm = float(np.median(q_ms)), float(np.median(d_ms))
     q_gbs, d_gbs = q_bytes / (qm * 1e-3) / 1e9, d_bytes / (dm * 1e-3) / 1e9
-    # dominant kernel roofline (time share): both kernels are reported, the larger share leads
-    kq = dict(bound="hbm", achieved=round(q_gbs, 1), peak=peak, unit="GB/s", frac=round(q_gbs / peak, 4),
-              traffic=profiled_traffic("quantize_kernel"), kernel="quantize_kernel",
-              algorithmic_bytes_per_launch=q_bytes, peak_kind=peak_kind)
+    # dominant kernel roofline (time share): both kernels are reported, the larger share leads.
+    # Quantize is bound by fp32 arithmetic by construction (~50 flop per fp16 element
+    # against 2 bytes of HBM traffic); its roofline is the fp32 pipe, with the HBM
+    # fraction reported beside it.
+    q_tflops = Q_FLOP_PER_ELEMENT * (q_bytes // 2) / (qm * 1e-3) / 1e12
+    fp32_peak = fp32_peak_tflops()
+    kq = dict(bound="alu", achieved=round(q_tflops, 2), peak=fp32_peak, unit="TFLOP/s",
+              frac=round(q_tflops / fp32_peak, 4), traffic=profiled_traffic("quantize_kernel"),
+              kernel="quantize_kernel", algorithmic_flops_per_launch=Q_FLOP_PER_ELEMENT * (q_bytes // 2),
+              hbm_gbs=round(q_gbs, 1), hbm_frac=round(q_gbs / peak, 4),
+              peak_kind="derived: 152 SMs x 128 fp32 lanes x 2 flop x 2.07 GHz")
     kd = dict(bound="hbm", achieved=round(d_gbs, 1), peak=peak, unit="GB/s", frac=round(d_gbs / peak, 4),
               traffic=profiled_traffic("decode_split_kernel"), kernel="decode_split_kernel+decode_merge_kernel",
               algorithmic_bytes_per_launch=d_bytes, peak_kind=peak_kind)
@@ -283,7 +314,7 @@ def run_gpu(args):
         "roofline_kernels": [kq, kd],
         "e2e": {"value": round(world * step_bytes / (e2e_ms / args.steps * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
-        "gpu_launches": args.steps * 3,
+        "gpu_launches": args.steps * 4,
         "clocks": clk.summary(),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -399,7 +430,13 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--case", default="full", choices=["full", "small"],
+                    help="small: reduced shapes for profiler captures (not a bench line)")
     args = ap.parse_args()
+    if args.case == "small":
+        global PREFILL, DECODE, WORKLOAD
+        PREFILL, DECODE, WORKLOAD = SMALL["prefill"], SMALL["decode"], SMALL["workload"]
+        args.no_cpu_baseline = True
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":

@@ -105,6 +105,7 @@ struct DecodeArgs {
   const int32_t* block_tables;
   const int32_t* seq_lens;
   int64_t* prefix;      // [n_seqs + 1] exclusive prefix of full tiles
+  int64_t* ranges;      // [n_ctas * kWarps][2] tile range of each split-kernel warp
   float* part;          // [records][8][132]
   unsigned* flags;
   int64_t num_blocks;
@@ -405,6 +406,10 @@ __global__ void __launch_bounds__(kWarps * 32, 1) decode_split_kernel(DecodeArgs
   const int64_t total = a.prefix[a.n_seqs] * a.hkv;
   int64_t gb, ge;
   warp_range(total, a.n_ctas, wg, gb, ge);
+  if (lane == 0) {
+    a.ranges[2 * wg] = gb;
+    a.ranges[2 * wg + 1] = ge;
+  }
   if (gb >= ge) return;   // warps are independent: no CTA-wide barrier below
 
   uint8_t* stages = smem + warp * kStages * kRec;
@@ -481,34 +486,24 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(DecodeArgs a, const u
   const int64_t u = static_cast<int64_t>(s) * a.hkv + h;
   const int64_t n_warps = static_cast<int64_t>(a.n_ctas) * kWarps;
 
-  // warps whose ranges cover this unit's tiles [t0, t1)
+  // warps whose ranges cover this unit's tiles [t0, t1) (ranges are contiguous and
+  // ordered; empty ranges are skipped)
   int64_t wlo = 0, whi = 0;
-  const int64_t total = a.prefix[a.n_seqs] * a.hkv;
   const int64_t t0 = a.prefix[s] * a.hkv + static_cast<int64_t>(h) * nf, t1 = t0 + nf;
   if (nf > 0) {
     int64_t lo = 0, hi = n_warps - 1;   // first warp with end > t0
     while (lo < hi) {
       const int64_t mid = (lo + hi) >> 1;
-      int64_t b, e;
-      warp_range(total, a.n_ctas, mid, b, e);
-      if (e > t0) hi = mid; else lo = mid + 1;
+      if (a.ranges[2 * mid + 1] > t0) hi = mid; else lo = mid + 1;
     }
     wlo = lo;
     whi = lo;
-    while (whi < n_warps) {   // warps whose ranges start before t1
-      int64_t b, e;
-      warp_range(total, a.n_ctas, whi, b, e);
-      if (b >= t1) break;
-      ++whi;
-    }
+    while (whi < n_warps && a.ranges[2 * whi] < t1) ++whi;
   }
 
   float M = -INFINITY;
-  for (int64_t w = wlo; w < whi; ++w) {
-    int64_t b, e;
-    warp_range(total, a.n_ctas, w, b, e);
-    if (b < e) M = fmaxf(M, a.part[(w + u) * kRecFloats + gg * kPartStride + 128]);
-  }
+  for (int64_t w = wlo; w < whi; ++w)
+    if (a.ranges[2 * w] < a.ranges[2 * w + 1]) M = fmaxf(M, a.part[(w + u) * kRecFloats + gg * kPartStride + 128]);
   // workspace tokens: exact fp16 K/V, unrotated
   const int64_t wbase = (static_cast<int64_t>(s) * a.hkv + h) * 2 * static_cast<int64_t>(kB * kD);
   const uint16_t* wk = ws ? ws + wbase : nullptr;
@@ -530,9 +525,7 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(DecodeArgs a, const u
   float acc[4] = {0.f, 0.f, 0.f, 0.f}, wacc[4] = {0.f, 0.f, 0.f, 0.f};
   float l = 0.f;
   for (int64_t w = wlo; w < whi; ++w) {
-    int64_t b, e;
-    warp_range(total, a.n_ctas, w, b, e);
-    if (b >= e) continue;
+    if (a.ranges[2 * w] >= a.ranges[2 * w + 1]) continue;
     const float* pp = a.part + (w + u) * kRecFloats + gg * kPartStride;
     const float mp = pp[128];
     const float f = (mp == -INFINITY) ? 0.f : exp2f(mp - M);
@@ -575,13 +568,14 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(DecodeArgs a, const u
 }
 
 size_t prefix_bytes(int n_seqs) { return ((static_cast<size_t>(n_seqs) + 1) * sizeof(int64_t) + 255) & ~size_t(255); }
+constexpr size_t kRangeBytes = static_cast<size_t>(kMaxCtas) * kWarps * 2 * sizeof(int64_t);
 
 }  // namespace
 
 size_t decode_part_bytes(int n_seqs, int hkv, int max_blocks) {
   (void)max_blocks;
   const size_t records = static_cast<size_t>(kMaxCtas) * kWarps + static_cast<size_t>(n_seqs) * hkv;
-  return prefix_bytes(n_seqs) + records * kRecFloats * sizeof(float);
+  return prefix_bytes(n_seqs) + kRangeBytes + records * kRecFloats * sizeof(float);
 }
 
 cudaError_t launch_decode(const uint16_t* q, const uint8_t* cache, const uint16_t* ws, const int32_t* block_tables,
@@ -597,7 +591,8 @@ cudaError_t launch_decode(const uint16_t* q, const uint8_t* cache, const uint16_
   a.block_tables = block_tables;
   a.seq_lens = seq_lens;
   a.prefix = static_cast<int64_t*>(scratch);
-  a.part = reinterpret_cast<float*>(static_cast<uint8_t*>(scratch) + prefix_bytes(n_seqs));
+  a.ranges = reinterpret_cast<int64_t*>(static_cast<uint8_t*>(scratch) + prefix_bytes(n_seqs));
+  a.part = reinterpret_cast<float*>(static_cast<uint8_t*>(scratch) + prefix_bytes(n_seqs) + kRangeBytes);
   a.flags = flags;
   a.num_blocks = num_blocks;
   a.n_seqs = n_seqs;
