@@ -188,6 +188,29 @@ KVARN_API kvarn_status kvarn_decode_attention(const uint16_t* q, const uint8_t* 
                                     void* scratch, size_t scratch_bytes,
                                     const kvarn_meta* meta, void* stream);
 
+/*
+ * Decode attention that allocates nothing and needs no scratch from the caller.
+ * This entry point has no counterpart in the KVarN paper or README; it exists for
+ * callers that cannot allocate device memory: e.g. a serving engine whose free
+ * device memory is all pre-reserved for its KV-cache pool and handed out only by
+ * its own allocator, or a plain-C host with no device allocator for temporaries.
+ * Same arguments and results as kvarn_decode_attention minus scratch: the scratch
+ * is a fixed 16 MiB array of device memory inside the library (held by every GPU
+ * that loads the library until the process exits), shared by all calls on a device.
+ *   - Sizes: returns KVARN_ESCRATCH, without launching, when the scratch needed for
+ *     n_seqs * num_kv_heads (sequence, kv-head) pairs exceeds 16 MiB (about 3000
+ *     pairs on a 152-SM GB300).
+ *   - The first call on a device (with that device current) looks up the array's
+ *     device address; make that first call before any stream capture.
+ *   - Calls whose work overlaps on the GPU (different streams, not ordered) race on
+ *     the shared array; order them. Nothing in the array needs to start at zero.
+ *   - Calls no cudaMalloc, cudaFree or allocating library routine.
+ */
+KVARN_API kvarn_status kvarn_decode_attention_static(const uint16_t* q, const uint8_t* cache,
+                                                     const uint16_t* workspace, const int32_t* block_tables,
+                                                     const int32_t* seq_lens, int32_t n_seqs, uint16_t* out,
+                                                     const kvarn_meta* meta, void* stream);
+
 /* Copies the device flag word of the current device to *flags (host pointer)
  * after synchronising `stream`, then clears it. */
 KVARN_API kvarn_status kvarn_device_flags(uint32_t* flags, void* stream);

@@ -35,6 +35,9 @@ _SIGS = {
     "kvarn_decode_attention": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                               ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p,
                                               ctypes.c_size_t, ctypes.c_void_p, ctypes.c_void_p]),
+    "kvarn_decode_attention_static": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                                     ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
+                                                     ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
     "kvarn_device_flags": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32), ctypes.c_void_p]),
     "kvarn_last_error": (ctypes.c_char_p, []),
 }
@@ -166,6 +169,20 @@ def kvarn_decode_attention(q, cache, workspace, block_tables, seq_lens, out, scr
                                        _ptr(seq_lens, "seq_lens", torch.int32, n), n,
                                        _ptr(out, "out", torch.float16), _ptr(scratch, "scratch"), nbytes,
                                        ctypes.byref(meta), _stream(stream)))
+
+
+def kvarn_decode_attention_static(q, cache, workspace, block_tables, seq_lens, out, meta: KvarnMeta, stream=None):
+    """kvarn_decode_attention without a scratch argument, for callers that cannot
+    allocate device memory: the library's built-in 16 MiB device array is used
+    instead (shared by all calls on a device; calls overlapping on the GPU race).
+    The first call on a device looks up that array's address."""
+    import torch
+    n = int(q.shape[0])
+    _check(_lib.kvarn_decode_attention_static(_ptr(q, "q", torch.float16), _ptr(cache, "cache", torch.uint8),
+                                              _ptr(workspace, "workspace", torch.float16),
+                                              _ptr(block_tables, "block_tables", torch.int32),
+                                              _ptr(seq_lens, "seq_lens", torch.int32, n), n,
+                                              _ptr(out, "out", torch.float16), ctypes.byref(meta), _stream(stream)))
 
 
 def kvarn_device_flags(stream=None) -> int:

@@ -190,3 +190,23 @@ kvarn_status kvarn_device_flags(uint32_t* flags, void* stream) {
 const char* kvarn_last_error(void) { return g_err; }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------- internal accessors
+// Used by other translation units of the library (not part of the C ABI).
+namespace kvarn {
+
+cudaError_t flags_device_ptr(unsigned** out) {
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_device_flags);
+  if (e == cudaSuccess) *out = static_cast<unsigned*>(p);
+  return e;
+}
+
+kvarn_status set_error(kvarn_status st, const char* msg) {
+  snprintf(g_err, sizeof(g_err), "%s", msg);
+  return st;
+}
+
+void clear_error() { g_err[0] = 0; }
+
+}  // namespace kvarn

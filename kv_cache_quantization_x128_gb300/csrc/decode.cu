@@ -578,6 +578,18 @@ size_t decode_part_bytes(int n_seqs, int hkv, int max_blocks) {
   return prefix_bytes(n_seqs) + kRangeBytes + records * kRecFloats * sizeof(float);
 }
 
+size_t decode_scratch_bytes_for_ctas(int n_seqs, int hkv, int n_ctas) {
+  const size_t records = static_cast<size_t>(n_ctas) * kWarps + static_cast<size_t>(n_seqs) * hkv;
+  return prefix_bytes(n_seqs) + kRangeBytes + records * kRecFloats * sizeof(float);
+}
+
+int decode_num_ctas() {
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  return sms > 0 ? (sms < kMaxCtas ? sms : kMaxCtas) : 1;
+}
+
 cudaError_t launch_decode(const uint16_t* q, const uint8_t* cache, const uint16_t* ws, const int32_t* block_tables,
                           const int32_t* seq_lens, int n_seqs, int hkv, int group, int max_blocks, int64_t num_blocks,
                           uint16_t* out, void* scratch, unsigned* flags, cudaStream_t stream) {

@@ -4,6 +4,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "../../include/kvarn.h"
+
 namespace kvarn {
 
 cudaError_t launch_quantize_prefill(const uint16_t* k, const uint16_t* v, const int64_t* slot, int64_t n_tokens,
@@ -21,5 +23,14 @@ cudaError_t launch_decode(const uint16_t* q, const uint8_t* cache, const uint16_
 
 // Device scratch of launch_decode: tile prefix per sequence + partial records.
 size_t decode_part_bytes(int n_seqs, int hkv, int max_blocks);
+// Scratch launch_decode touches when the split kernel runs `n_ctas` CTAs (the
+// device's SM count, at most 1024).
+size_t decode_scratch_bytes_for_ctas(int n_seqs, int hkv, int n_ctas);
+int decode_num_ctas();
+
+// api.cu: device flag word, per-thread error message
+cudaError_t flags_device_ptr(unsigned** out);
+kvarn_status set_error(kvarn_status st, const char* msg);
+void clear_error();
 
 }  // namespace kvarn
