@@ -126,15 +126,29 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------------------- traffic from profiles
+# sources a kernel's profile summary was captured from (hashed together, in order)
+PROFILE_SOURCES = {
+    "quantize": ["quantize.cu", "kvarn_tc.cuh", "kvarn_common.cuh"],
+    "decode": ["decode.cu", "kvarn_common.cuh"],
+}
+
+
+def source_sha16(kernel: str) -> str:
+    """First 16 hex digits of the sha256 of the kernel's sources, concatenated."""
+    h = hashlib.sha256()
+    for name in PROFILE_SOURCES["quantize" if kernel.startswith("quantize") else "decode"]:
+        with open(os.path.join(ROOT, "kv_cache_quantization_x128_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
 def profiled_traffic(kernel: str):
     """DRAM bytes per launch recorded in profiles/<kernel>.md for the current source
     (null when the kernel source changed since the capture)."""
     path = os.path.join(ROOT, "profiles", f"{kernel}.md")
-    src = os.path.join(ROOT, "kv_cache_quantization_x128_gb300", "csrc",
-                       "quantize.cu" if kernel.startswith("quantize") else "decode.cu")
     try:
         text = open(path).read()
-        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        sha = source_sha16(kernel)
     except OSError:
         return None
     m = re.search(r"dram_bytes_per_full_launch:\s*([0-9.eE+]+)", text)

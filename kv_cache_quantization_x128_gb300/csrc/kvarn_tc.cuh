@@ -24,20 +24,29 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-// Shared-memory matrix descriptor, K-major, no swizzle. Canonical layout of an
-// operand with rows r and reduction index k (16-bit elements):
-//   byte(r, k) = (r/8)*2048 + (k/8)*128 + (r%8)*16 + (k%8)*2
-// i.e. 8x8 core matrices of 128 contiguous bytes, 128 B apart along K (leading
-// byte offset) and 2048 B apart along rows (stride byte offset), for K = 128.
-__device__ __forceinline__ uint32_t canon_offset(int r, int k) {
-  return static_cast<uint32_t>((r >> 3) * 2048 + (k >> 3) * 128 + (r & 7) * 16 + (k & 7) * 2);
+// Operands of 128 rows x 128 fp16 along K are stored as two K-major halves of 64
+// (16 KB each) in the 128-byte swizzled layout that a 2-D TMA box of 64 x 128
+// fp16 writes: row r at (r/8)*1024 + (r%8)*128, its 16-byte chunk c at chunk
+// position c ^ (r%8). The halves must be 1024-byte aligned.
+__host__ __device__ constexpr uint32_t sw_offset(int r, int k) {
+  return static_cast<uint32_t>((k >> 6) * 16384 + (r >> 3) * 1024 + (r & 7) * 128 +
+                               ((((k & 63) >> 3) ^ (r & 7)) << 4) + (k & 7) * 2);
 }
-__device__ __forceinline__ uint64_t smem_desc_kmajor(uint32_t saddr) {
+// Shared-memory matrix descriptor of that layout: 8-row groups 1024 B apart
+// (stride byte offset), 128-byte swizzle (mode 2 in bits [61, 64)); the leading
+// byte offset is unused when the K extent of one MMA lies inside the swizzle row.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
   uint64_t d = static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
-  d |= static_cast<uint64_t>(128u >> 4) << 16;    // leading byte offset (along K)
-  d |= static_cast<uint64_t>(2048u >> 4) << 32;   // stride byte offset (along rows)
+  d |= static_cast<uint64_t>(1) << 16;            // leading byte offset (unused)
+  d |= static_cast<uint64_t>(1024u >> 4) << 32;   // stride byte offset
   d |= static_cast<uint64_t>(1) << 46;            // descriptor version for sm_100 family
-  return d;                                        // base offset 0, no swizzle
+  d |= static_cast<uint64_t>(2) << 61;            // 128-byte swizzle
+  return d;
+}
+// Start address of K step s (16 elements) of such an operand at `base`: 32 B
+// further along the swizzle row, the second half 16 KB on.
+__device__ __forceinline__ uint32_t sw_kstep(uint32_t base, int s) {
+  return base + (s >> 2) * 16384 + (s & 3) * 32;
 }
 // Instruction descriptor, kind::f16: fp32 accumulator, fp16 A and B, both K-major.
 __host__ __device__ constexpr uint32_t idesc_f16_f32(uint32_t m, uint32_t n) {
@@ -59,30 +68,12 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
                : "memory");
 }
 
-// 16 lanes x 128 fp32 columns per warp: thread t gets lane base + (t>>2) + 8(t&1),
-// columns ((t>>1)&1) + 2k for k = 0..63 (register k).
-__device__ __forceinline__ void tmem_ld_16x64b_x64(uint32_t taddr, float (&v)[64]) {
-  uint32_t* r = reinterpret_cast<uint32_t*>(v);
-  asm volatile(
-      "tcgen05.ld.sync.aligned.16x64b.x64.b32 "
-      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,"
-      "%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
-      "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]),
-        "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]),
-        "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]),
-        "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]),
-        "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-
-// Same mapping, 64 columns (register k -> column ((t>>1)&1) + 2k).
-__device__ __forceinline__ void tmem_ld_16x64b_x32(uint32_t taddr, float* v) {
+// 16 lanes x 64 fp32 columns per warp: thread t gets lane base + (t>>2) + 8(t&1),
+// columns ((t>>1)&1) + 2k for k = 0..31 (register k). The registers are valid
+// only after tmem_wait_x32 on the same array: the wait names them as operands,
+// so no use of them moves above it, while independent loads and arithmetic can
+// move across both.
+__device__ __forceinline__ void tmem_ld_16x64b_x32_nowait(uint32_t taddr, float* v) {
   uint32_t* r = reinterpret_cast<uint32_t*>(v);
   asm volatile(
       "tcgen05.ld.sync.aligned.16x64b.x32.b32 "
@@ -93,17 +84,21 @@ __device__ __forceinline__ void tmem_ld_16x64b_x32(uint32_t taddr, float* v) {
         "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
         "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
       : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_wait_x32(float* v) {
+  uint32_t* r = reinterpret_cast<uint32_t*>(v);
+  asm volatile("tcgen05.wait::ld.sync.aligned;" : "+r"(r[0]),"+r"(r[1]),"+r"(r[2]),"+r"(r[3]),"+r"(r[4]),"+r"(r[5]),"+r"(r[6]),"+r"(r[7]),"+r"(r[8]),"+r"(r[9]),"+r"(r[10]),"+r"(r[11]),"+r"(r[12]),"+r"(r[13]),"+r"(r[14]),"+r"(r[15]),"+r"(r[16]),"+r"(r[17]),"+r"(r[18]),"+r"(r[19]),"+r"(r[20]),"+r"(r[21]),"+r"(r[22]),"+r"(r[23]),"+r"(r[24]),"+r"(r[25]),"+r"(r[26]),"+r"(r[27]),"+r"(r[28]),"+r"(r[29]),"+r"(r[30]),"+r"(r[31]));
 }
 
-// ---------------------------------------------------------------- cp.async (16 B)
-__device__ __forceinline__ void cp_async16(void* dst_smem, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst_smem)), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+// ---------------------------------------------------------------- TMA (2-D tiles)
+// Box of the tensor map at coordinates (x, y) into shared memory, completion
+// counted on `bar`; x times the element size must be a multiple of 16 bytes.
+__device__ __forceinline__ void tma_load_2d(void* dst, const void* tensor_map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+      "[%4];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(tensor_map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
 }
 
 // ---------------------------------------------------------------- named barriers

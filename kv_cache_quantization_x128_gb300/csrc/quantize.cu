@@ -6,10 +6,11 @@
 // One persistent CTA per SM, 512 threads in two independent 8-warp groups: group 0
 // quantizes the K tile and group 1 the V tile of each (block, kv-head) work item.
 // Per item and group:
-//   1. cp.async copies the next item's 128 token rows (fp16) into the group's spare
-//      shared-memory buffer, in the no-swizzle K-major canonical UMMA layout;
-//   2. one thread issues tcgen05.mma twice over K = 128: D1 = H X^T (TMEM lanes =
-//      channels, columns = tokens) and D2 = X H (lanes = tokens, columns =
+//   1. one thread starts two 2-D TMA copies (64 channels x 128 tokens each) of the
+//      next item's tile into the group's spare buffer, in the 128-byte swizzled
+//      K-major layout, completing on an mbarrier;
+//   2. the same thread issues tcgen05.mma twice over K = 128: D1 = H X^T (TMEM
+//      lanes = channels, columns = tokens) and D2 = X H (lanes = tokens, columns =
 //      channels), with H the +-1 Sylvester matrix (exact in fp16) and fp32
 //      accumulation; the 1/sqrt(128) factor is folded into the statistics;
 //   3. each column pass reads D2 and each row pass reads D1 straight from TMEM
@@ -19,6 +20,11 @@
 //      the group's part of the record.
 // The groups share only the Hadamard operand and the TMEM allocation (256 columns
 // each), so one group's MMA latency and barriers overlap the other's arithmetic.
+// The slot check of an item is agreed on at the barrier that ends the previous one.
+#include <cuda.h>
+
+#include <mutex>
+
 #include "kvarn_common.cuh"
 #include "kvarn_launch.h"
 #include "kvarn_tc.cuh"
@@ -39,8 +45,8 @@ constexpr int kOffIn = kOffH + kTileOp;                        // [group][buf] o
 constexpr int kOffStageK = kOffIn + 4 * kTileOp;               // [buf]
 constexpr int kOffStageV = kOffStageK + 2 * kStageK;           // [buf]
 constexpr int kOffVec = kOffStageV + 2 * kStageV;              // [group][vector][kVec] fp32
-constexpr int kOffBar = kOffVec + 2 * kNumVec * kVec * 4;      // mma barriers [group]
-constexpr int kOffTmem = kOffBar + 16;
+constexpr int kOffBar = kOffVec + 2 * kNumVec * kVec * 4;      // mma barriers [group], load barriers [group][buf]
+constexpr int kOffTmem = kOffBar + 48;
 constexpr int kSmemBytes = kOffTmem + 16;
 static_assert(kSmemBytes <= 232448, "quantize shared memory");
 static_assert(kOffIn % 1024 == 0 && kOffStageK % 16 == 0 && kOffStageV % 16 == 0 && kOffVec % 16 == 0, "align");
@@ -50,53 +56,63 @@ enum { kVA = 0, kVB = 1, kVG = 2, kVHc = 3, kVW = 4, kVC0 = 5, kVMc = 6, kVMr = 
 // position of entry e in a parity-split vector
 __device__ __forceinline__ int ps(int e) { return (e & 1) * 68 + (e >> 1); }
 
-constexpr float kVarScale = 1.0f / 128.0f;   // (2^-3.5)^2: statistics of the +-1 transform
+constexpr float kVarScale = 1.0f / 128.0f;
+
+__device__ __forceinline__ float fmin3(float a, float b, float c) {
+  float r;
+  asm("min.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+__device__ __forceinline__ float fma_sat(float a, float b, float c) {
+  float r;
+  asm("fma.rn.sat.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}   // (2^-3.5)^2: statistics of the +-1 transform
 
 // ------------------------------------------------------------------ work sources
+// A work item w is a (tile, kv-head) pair; both sources keep w below 2^31.
 struct PrefillSource {
-  const uint16_t* k;
-  const uint16_t* v;
+  CUtensorMap map[2];   // K, V as [n_tokens rows][hkv * 128 channels] fp16
   const int64_t* slot;
   int64_t n_items;      // (n_tokens / 128) * hkv
   int hkv;
   int64_t num_blocks;
 
-  // Row 0 of tensor `g` (0 = K, 1 = V) of item w and the row stride (elements);
-  // false if the item needs no copy.
-  __device__ bool rows(int64_t w, int g, const uint16_t*& base, int64_t& stride) const {
-    const int64_t chunk = w / hkv;
-    const int h = static_cast<int>(w - chunk * hkv);
-    stride = static_cast<int64_t>(hkv) * kD;
-    base = (g ? v : k) + chunk * kB * stride + static_cast<int64_t>(h) * kD;
-    return true;
+  __device__ bool needs_load(int64_t) const { return true; }
+  // TMA coordinates (channel, token) of the item's 128 x 128 tile of tensor g
+  __device__ void coords(int64_t w, int, int& x, int& y) const {
+    const uint32_t chunk = static_cast<uint32_t>(w) / static_cast<uint32_t>(hkv);
+    x = static_cast<int>(static_cast<uint32_t>(w) - chunk * hkv) * kD;
+    y = static_cast<int>(chunk) * kB;
   }
-  // Slot entries this thread checks for item w, loaded one item ahead of use.
   struct Check {
     int64_t base = -1, mine = -1;
   };
+  // Slot entries this thread checks for item w, loaded one item ahead of use.
   __device__ Check prepare(int64_t w, int gt) const {
-    const int64_t t0 = (w / hkv) * kB;
+    const int64_t t0 = static_cast<int64_t>(static_cast<uint32_t>(w) / static_cast<uint32_t>(hkv)) * kB;
     Check c;
     c.base = slot[t0];
-    c.mine = gt < kB ? slot[t0 + gt] : c.base + gt;
+    c.mine = slot[t0 + (gt & (kB - 1))];
     return c;
   }
-  // Group-wide (all 256 threads, barrier `bar_id`): record index of item w or -1.
-  __device__ int64_t resolve(int64_t w, const Check& c, int gt, int bar_id, unsigned* flags) const {
-    const int64_t chunk = w / hkv;
-    const int h = static_cast<int>(w - chunk * hkv);
-    bool ok = c.base >= 0 && (c.base % kB) == 0 && c.base / kB < num_blocks && c.mine == c.base + gt;
-    ok = named_bar_and(bar_id, kGroupThreads, ok);
-    if (!ok) {
-      if (gt == 0) raise_flag(flags, KVARN_FLAG_BAD_SLOTS);
-      return -1;
-    }
-    return (c.base / kB) * hkv + h;
+  __device__ bool check_ok(const Check& c, int gt) const {
+    return c.base >= 0 && (c.base % kB) == 0 && c.base / kB < num_blocks && c.mine == c.base + (gt & (kB - 1));
+  }
+  // Record index of item w once the group agreed its slots are valid.
+  __device__ int64_t target(int64_t w, const Check& c, int, unsigned*) const {
+    const uint32_t chunk = static_cast<uint32_t>(w) / static_cast<uint32_t>(hkv);
+    return (c.base / kB) * hkv + (static_cast<uint32_t>(w) - chunk * hkv);
   }
 };
 
 struct AppendSource {
-  const uint16_t* ws;           // [n_seqs][hkv][2][128][128]
+  CUtensorMap map;              // workspace as [n_seqs * hkv * 2 * 128 rows][128 channels] fp16
   const int32_t* seq_lens;      // lengths before the append
   const int32_t* block_tables;  // [n_seqs][max_blocks]
   int64_t n_items;              // n_seqs * hkv
@@ -104,31 +120,27 @@ struct AppendSource {
   int max_blocks;
   int64_t num_blocks;
 
-  __device__ bool completes(int64_t w) const {
-    const int L = seq_lens[w / hkv];
+  __device__ bool needs_load(int64_t w) const {
+    const int L = seq_lens[static_cast<uint32_t>(w) / static_cast<uint32_t>(hkv)];
     return L >= 0 && (L % kB) == kB - 1;
   }
-  __device__ bool rows(int64_t w, int g, const uint16_t*& base, int64_t& stride) const {
-    if (!completes(w)) return false;
-    const int64_t s = w / hkv;
-    const int h = static_cast<int>(w - s * hkv);
-    stride = kD;
-    base = ws + ((s * hkv + h) * 2 + g) * static_cast<int64_t>(kB * kD);
-    return true;
+  __device__ void coords(int64_t w, int g, int& x, int& y) const {
+    x = 0;
+    y = (static_cast<int>(w) * 2 + g) * kB;
   }
   struct Check {};
   __device__ Check prepare(int64_t, int) const { return Check{}; }
-  __device__ int64_t resolve(int64_t w, const Check&, int gt, int bar_id, unsigned* flags) const {
-    named_bar(bar_id, kGroupThreads);   // copies of the item are visible to the group
-    if (!completes(w)) return -1;
-    const int64_t s = w / hkv;
-    const int h = static_cast<int>(w - s * hkv);
+  __device__ bool check_ok(const Check&, int) const { return true; }
+  __device__ int64_t target(int64_t w, const Check&, int gt, unsigned* flags) const {
+    if (!needs_load(w)) return -1;
+    const uint32_t s = static_cast<uint32_t>(w) / static_cast<uint32_t>(hkv);
+    const uint32_t h = static_cast<uint32_t>(w) - s * hkv;
     const int bi = seq_lens[s] / kB;
     if (bi >= max_blocks) {
       if (gt == 0) raise_flag(flags, KVARN_FLAG_BAD_LENGTH);
       return -1;
     }
-    const int64_t blk = block_tables[s * max_blocks + bi];
+    const int64_t blk = block_tables[static_cast<int64_t>(s) * max_blocks + bi];
     if (blk < 0 || blk >= num_blocks) {
       if (gt == 0) raise_flag(flags, KVARN_FLAG_BAD_BLOCK);
       return -1;
@@ -137,20 +149,19 @@ struct AppendSource {
   }
 };
 
-// Group `g` copies the 128 rows of its tensor for item w into `dst` (canonical layout).
+__device__ __forceinline__ const CUtensorMap* tensor_map(const PrefillSource& s, int g) { return &s.map[g]; }
+__device__ __forceinline__ const CUtensorMap* tensor_map(const AppendSource& s, int) { return &s.map; }
+
+// Thread gt == 0 of group g starts the two TMA copies (64 channels each) of item
+// w's tile into `dst`, completing on `bar`.
 template <class Src>
-__device__ __forceinline__ void load_tile(const Src& src, int64_t w, int g, int gt, uint8_t* dst) {
-  const uint16_t* base;
-  int64_t stride;
-  if (!src.rows(w, g, base, stride)) return;
-  const int gw = gt >> 5, t = gt & 31;
-#pragma unroll
-  for (int m = 0; m < 8; ++m) {
-    const int combo = gw + 8 * m;                // 0..63
-    const int j = 8 * (combo & 15) + (t & 7);    // token (row)
-    const int c8 = 4 * (combo >> 4) + (t >> 3);  // 16-byte chunk along channels
-    cp_async16(dst + canon_offset(j, 8 * c8), base + j * stride + 8 * c8);
-  }
+__device__ __forceinline__ void issue_tile(const Src& src, int64_t w, int g, uint8_t* dst, uint64_t* bar) {
+  int x, y;
+  src.coords(w, g, x, y);
+  const CUtensorMap* map = tensor_map(src, g);
+  mbar_arrive_expect_tx(bar, kTileOp);
+  tma_load_2d(dst, map, x, y, bar);
+  tma_load_2d(dst + kTileOp / 2, map, x + 64, y, bar);
 }
 
 // Population variance and mean over the pair's 128 values of w_e * x_e, where the
@@ -163,22 +174,34 @@ __device__ __forceinline__ void load_tile(const Src& src, int64_t w, int g, int 
 // variance.
 __device__ __forceinline__ float pair_moments(uint32_t taddr, const float* wv, int p, float shift, float& mean) {
   const float2 nsh = make_float2(-shift, -shift);
-  float2 s0 = make_float2(0.f, 0.f), s1 = s0, q0 = s0, q1 = s0;
+  float2 s0 = make_float2(0.f, 0.f), s1 = s0, s2 = s0, s3 = s0, q0 = s0, q1 = s0, q2 = s0, q3 = s0;
 #pragma unroll 1
   for (int hh = 0; hh < 2; ++hh) {
     float x[32];
-    tmem_ld_16x64b_x32(taddr + 64 * hh, x);
+    tmem_ld_16x64b_x32_nowait(taddr + 64 * hh, x);
+    tmem_wait_x32(x);
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
+    for (int q = 0; q < 8; q += 2) {
       const float4 w = reinterpret_cast<const float4*>(wv + p * 68)[8 * hh + q];
+      const float4 v = reinterpret_cast<const float4*>(wv + p * 68)[8 * hh + q + 1];
       const float2 d0 = __ffma2_rn(make_float2(w.x, w.y), make_float2(x[4 * q], x[4 * q + 1]), nsh);
       const float2 d1 = __ffma2_rn(make_float2(w.z, w.w), make_float2(x[4 * q + 2], x[4 * q + 3]), nsh);
+      const float2 d2 = __ffma2_rn(make_float2(v.x, v.y), make_float2(x[4 * q + 4], x[4 * q + 5]), nsh);
+      const float2 d3 = __ffma2_rn(make_float2(v.z, v.w), make_float2(x[4 * q + 6], x[4 * q + 7]), nsh);
       s0 = __fadd2_rn(s0, d0);
       s1 = __fadd2_rn(s1, d1);
+      s2 = __fadd2_rn(s2, d2);
+      s3 = __fadd2_rn(s3, d3);
       q0 = __ffma2_rn(d0, d0, q0);
       q1 = __ffma2_rn(d1, d1, q1);
+      q2 = __ffma2_rn(d2, d2, q2);
+      q3 = __ffma2_rn(d3, d3, q3);
     }
   }
+  s0 = __fadd2_rn(s0, s2);
+  s1 = __fadd2_rn(s1, s3);
+  q0 = __fadd2_rn(q0, q2);
+  q1 = __fadd2_rn(q1, q3);
   float s = (s0.x + s0.y) + (s1.x + s1.y), m2 = (q0.x + q0.y) + (q1.x + q1.y);
   s += __shfl_xor_sync(0xffffffffu, s, 2);
   m2 += __shfl_xor_sync(0xffffffffu, m2, 2);
@@ -195,7 +218,8 @@ __device__ __forceinline__ float pair_moments(uint32_t taddr, const float* wv, i
 #pragma unroll 1
     for (int hh = 0; hh < 2; ++hh) {
       float x[32];
-      tmem_ld_16x64b_x32(taddr + 64 * hh, x);
+      tmem_ld_16x64b_x32_nowait(taddr + 64 * hh, x);
+    tmem_wait_x32(x);
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
         const float4 w = reinterpret_cast<const float4*>(wv + p * 68)[8 * hh + q];
@@ -231,8 +255,9 @@ __device__ __forceinline__ float div_sqrt(float v, float u) {
 // (canonical layout), `line`/`p` locate the thread's half line, `ta1`/`ta2` are
 // its TMEM addresses of D1 and D2.
 template <int kKind>
-__device__ __forceinline__ void quantize_group(float* vec, uint8_t* stage, const uint8_t* tile, uint32_t ta1,
-                                               uint32_t ta2, int line, int p, int n_iters, float eps, int bar_id) {
+__device__ __forceinline__ bool quantize_group(float* vec, uint8_t* stage, const uint8_t* tile, uint32_t ta1,
+                                               uint32_t ta2, int line, int p, int n_iters, float eps, int bar_id,
+                                               bool ok) {
   float* va = vec + kVA * kVec;
   float* vb = vec + kVB * kVec;
   float* vg = vec + kVG * kVec;
@@ -245,7 +270,8 @@ __device__ __forceinline__ void quantize_group(float* vec, uint8_t* stage, const
     va[pl] = 1.0f;
     vb[pl] = 1.0f;
   }
-  named_bar(bar_id, kGroupThreads);
+  // every thread saw its copies and the tensor core finish, or the group stops
+  if (!named_bar_and(bar_id, kGroupThreads, ok)) return false;
 
   float* vmc = vec + kVMc * kVec;
   float* vmr = vec + kVMr * kVec;
@@ -254,7 +280,7 @@ __device__ __forceinline__ void quantize_group(float* vec, uint8_t* stage, const
     // shift is exact: with a = 1 the mean of a +-1 Hadamard column is the token's
     // channel-0 input value
     {
-      const float shift = it == 0 ? __half2float(*reinterpret_cast<const __half*>(tile + canon_offset(line, 0)))
+      const float shift = it == 0 ? __half2float(*reinterpret_cast<const __half*>(tile + sw_offset(line, 0)))
                                   : vmc[pl];
       float mean;
       const float var = pair_moments(ta2, va, p, shift, mean) * kVarScale;
@@ -297,7 +323,8 @@ __device__ __forceinline__ void quantize_group(float* vec, uint8_t* stage, const
 #pragma unroll 1
     for (int hh = 0; hh < 2; ++hh) {
       float xh[32];
-      tmem_ld_16x64b_x32((kKind == 0 ? ta1 : ta2) + 64 * hh, xh);
+      tmem_ld_16x64b_x32_nowait((kKind == 0 ? ta1 : ta2) + 64 * hh, xh);
+    tmem_wait_x32(xh);
       // y = (x * hc_j) * g_i; the factor that is constant along the thread's line is
       // positive, so it multiplies the extremes afterwards (same rounding as per element)
       const float* vv = kKind == 0 ? vh : vg;
@@ -306,8 +333,8 @@ __device__ __forceinline__ void quantize_group(float* vec, uint8_t* stage, const
         const float4 w = reinterpret_cast<const float4*>(vv + p * 68)[8 * hh + q];
         const float2 y0 = __fmul2_rn(make_float2(xh[4 * q], xh[4 * q + 1]), make_float2(w.x, w.y));
         const float2 y1 = __fmul2_rn(make_float2(xh[4 * q + 2], xh[4 * q + 3]), make_float2(w.z, w.w));
-        mn = fminf(fminf(mn, y0.x), fminf(y0.y, fminf(y1.x, y1.y)));
-        mx = fmaxf(fmaxf(mx, y0.x), fmaxf(y0.y, fmaxf(y1.x, y1.y)));
+        mn = fmin3(fmin3(mn, y0.x, y0.y), y1.x, y1.y);
+        mx = fmax3(fmax3(mx, y0.x, y0.y), y1.x, y1.y);
       }
     }
     const float line_factor = kKind == 0 ? vg[pl] : vh[pl];
@@ -320,8 +347,8 @@ __device__ __forceinline__ void quantize_group(float* vec, uint8_t* stage, const
       const float inv_s = 1.0f / h2f_bits(sbits);
       meta[2 * 128 + line] = sbits;
       meta[3 * 128 + line] = zb;
-      vw[pl] = (kKind == 0 ? vg[pl] : vh[pl]) * inv_s;
-      vc0[pl] = fmaf(-z, inv_s, 0.5f);
+      vw[pl] = (kKind == 0 ? vg[pl] : vh[pl]) * inv_s * (1.0f / kLevels);
+      vc0[pl] = fmaf(-z, inv_s, 0.5f) * (1.0f / kLevels);
     }
   }
   named_bar(bar_id, kGroupThreads);
@@ -334,7 +361,8 @@ __device__ __forceinline__ void quantize_group(float* vec, uint8_t* stage, const
 #pragma unroll 1
   for (int hh = 0; hh < 2; ++hh) {
     float xh[32];
-    tmem_ld_16x64b_x32((kKind == 0 ? ta2 : ta1) + 64 * hh, xh);
+    tmem_ld_16x64b_x32_nowait((kKind == 0 ? ta2 : ta1) + 64 * hh, xh);
+    tmem_wait_x32(xh);
     // v = (x * own) * w_e + c0_e = (y - z) / s + 1/2, clamped to [0, levels]; the
     // round-down add of 2^23 leaves 0x4B000000 + floor(v) in the bits, and each
     // word accumulates (bits << shift) with the 0x4B000000 terms removed at the end
@@ -343,14 +371,14 @@ __device__ __forceinline__ void quantize_group(float* vec, uint8_t* stage, const
     for (int q = 0; q < 8; ++q) {
       const float4 w = reinterpret_cast<const float4*>(vw + p * 68)[8 * hh + q];
       const float4 c = reinterpret_cast<const float4*>(vc0 + p * 68)[8 * hh + q];
-      const float2 v0 = __ffma2_rn(__fmul2_rn(make_float2(xh[4 * q], xh[4 * q + 1]), own2), make_float2(w.x, w.y),
-                                   make_float2(c.x, c.y));
-      const float2 v1 = __ffma2_rn(__fmul2_rn(make_float2(xh[4 * q + 2], xh[4 * q + 3]), own2),
-                                   make_float2(w.z, w.w), make_float2(c.z, c.w));
-      const float2 lo = make_float2(fminf(fmaxf(v0.x, 0.f), kLevels), fminf(fmaxf(v0.y, 0.f), kLevels));
-      const float2 hi = make_float2(fminf(fmaxf(v1.x, 0.f), kLevels), fminf(fmaxf(v1.y, 0.f), kLevels));
-      const float2 f0 = __fadd2_rd(lo, make_float2(8388608.0f, 8388608.0f));
-      const float2 f1 = __fadd2_rd(hi, make_float2(8388608.0f, 8388608.0f));
+      const float2 t0 = __fmul2_rn(make_float2(xh[4 * q], xh[4 * q + 1]), own2);
+      const float2 t1 = __fmul2_rn(make_float2(xh[4 * q + 2], xh[4 * q + 3]), own2);
+      // u = clamp(v / levels, 0, 1); floor(u * levels) is the clamped code
+      const float2 u0 = make_float2(fma_sat(t0.x, w.x, c.x), fma_sat(t0.y, w.y, c.y));
+      const float2 u1 = make_float2(fma_sat(t1.x, w.z, c.z), fma_sat(t1.y, w.w, c.w));
+      const float2 lv = make_float2(kLevels, kLevels), mg = make_float2(8388608.0f, 8388608.0f);
+      const float2 f0 = __ffma2_rd(u0, lv, mg);
+      const float2 f1 = __ffma2_rd(u1, lv, mg);
       const uint32_t bits[4] = {__float_as_uint(f0.x), __float_as_uint(f0.y), __float_as_uint(f1.x),
                                 __float_as_uint(f1.y)};
 #pragma unroll
@@ -394,28 +422,32 @@ __device__ __forceinline__ void quantize_group(float* vec, uint8_t* stage, const
       }
     }
   }
+  return true;
 }
 
+// 96 registers a thread (the 512 threads could hold 128): measured faster on the
+// prefill workload than the larger allocation, with a few bytes of spill.
 template <class Src>
-__global__ void __launch_bounds__(kThreads, 1)
-    quantize_kernel(Src src, uint8_t* __restrict__ cache, int n_iters, float eps, unsigned* flags) {
+__global__ void __maxnreg__(96)
+    quantize_kernel(const __grid_constant__ Src src, uint8_t* __restrict__ cache, int n_iters, float eps,
+                    unsigned* flags) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const int tid = threadIdx.x;
   const int grp = tid / kGroupThreads;     // 0 = K, 1 = V
   const int gt = tid % kGroupThreads;
   const int bar_id = 1 + grp;
   uint64_t* mma_bar = reinterpret_cast<uint64_t*>(smem + kOffBar);
+  uint64_t* load_bar = mma_bar + 2 + 2 * grp;   // this group's [buf]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffTmem);
   if (static_cast<int64_t>(blockIdx.x) >= src.n_items) return;
 
-  // Sylvester +-1 Hadamard operand (H[i][k] = (-1)^popcount(i & k)), canonical layout
+  // Sylvester +-1 Hadamard operand (H[i][k] = (-1)^popcount(i & k)), swizzled layout
   for (int e = tid; e < kD * kD; e += kThreads) {
     const int i = e >> 7, kk = e & 127;
-    *reinterpret_cast<uint16_t*>(smem + kOffH + canon_offset(i, kk)) = (__popc(i & kk) & 1) ? 0xBC00u : 0x3C00u;
+    *reinterpret_cast<uint16_t*>(smem + kOffH + sw_offset(i, kk)) = (__popc(i & kk) & 1) ? 0xBC00u : 0x3C00u;
   }
   if (tid == 0) {
-    mbar_init(&mma_bar[0], 1);
-    mbar_init(&mma_bar[1], 1);
+    for (int b = 0; b < 6; ++b) mbar_init(&mma_bar[b], 1);
     fence_mbar_init();
   }
   if (tid < 32) tmem_alloc(tmem_slot, 512);
@@ -436,59 +468,85 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t ta2 = ta1 + 128;
   float* vec = reinterpret_cast<float*>(smem + kOffVec) + grp * kNumVec * kVec;
   const uint32_t sh = smem_u32(smem + kOffH);
+  uint8_t* tiles = smem + kOffIn + grp * 2 * kTileOp;   // this group's [buf]
   constexpr uint32_t kIdesc = idesc_f16_f32(128, 128);
 
+  // The copy of item w's tile is started one item ahead; the slot check of the
+  // next item is agreed on at the barrier that ends the current one.
   int64_t item = blockIdx.x;
-  load_tile(src, item, grp, gt, smem + kOffIn + (grp * 2 + 0) * kTileOp);
-  cp_async_commit();
+  uint32_t pend = 0;               // bit b: a copy into buffer b has not been waited for
+  uint32_t load_parity = 0;        // bit b: phase parity of buffer b's barrier
+  if (src.needs_load(item)) {
+    if (gt == 0) issue_tile(src, item, grp, tiles, &load_bar[0]);
+    pend = 1;
+  }
   typename Src::Check check = src.prepare(item, gt);
+  int64_t dst = -1;
+  if (named_bar_and(bar_id, kGroupThreads, src.check_ok(check, gt)))
+    dst = src.target(item, check, gt, flags);
+  else if (gt == 0)
+    raise_flag(flags, KVARN_FLAG_BAD_SLOTS);
   uint32_t mma_parity = 0;
-  bool alive = true;
+  bool mma_inflight = false;       // thread gt == 0: an issued MMA not yet seen complete
   for (int k = 0; item < src.n_items; ++k, item += gridDim.x) {
     const int buf = k & 1;
     const int64_t next = item + gridDim.x;
+    const bool has_next = next < src.n_items;
     typename Src::Check check_next{};
-    if (next < src.n_items) {
-      load_tile(src, next, grp, gt, smem + kOffIn + (grp * 2 + (buf ^ 1)) * kTileOp);
+    if (has_next) {
+      if (src.needs_load(next)) {   // buffer buf ^ 1 was last read by the previous item
+        if (gt == 0) issue_tile(src, next, grp, tiles + (buf ^ 1) * kTileOp, &load_bar[buf ^ 1]);
+        pend |= 2u >> buf;
+      }
       check_next = src.prepare(next, gt);
     }
-    cp_async_commit();
-    cp_async_wait<1>();               // this item's copies (all but the newest group)
-    fence_proxy_async_smem();         // ... visible to the tensor core
-    tc_fence_before();
-    const int64_t dst = src.resolve(item, check, gt, bar_id, flags);   // includes a group barrier
-    check = check_next;
-    tc_fence_after();
-    if (dst < 0 || !alive) continue;
-    uint8_t* stage = smem + (grp == 0 ? kOffStageK + buf * kStageK : kOffStageV + buf * kStageV);
-    if (gt == 0) {
-      const uint32_t sx = smem_u32(smem + kOffIn + (grp * 2 + buf) * kTileOp);
-#pragma unroll
-      for (int s = 0; s < 8; ++s) {
-        const uint64_t dh = smem_desc_kmajor(sh + 256 * s);
-        const uint64_t dx = smem_desc_kmajor(sx + 256 * s);
-        umma_f16(d1, dh, dx, kIdesc, s > 0);   // D1[i][j] = sum_k H[i][k] X[j][k]
-        umma_f16(d2, dx, dh, kIdesc, s > 0);   // D2[j][i] = sum_k X[j][k] H[i][k]
+    bool ok = true;
+    if ((pend >> buf) & 1u) {
+      ok = mbar_wait(&load_bar[buf], (load_parity >> buf) & 1u, flags);
+      if (ok) {
+        load_parity ^= 1u << buf;
+        pend &= ~(1u << buf);
       }
-      umma_commit(&mma_bar[grp]);
-      bulk_wait_read<1>();              // the stage written two items ago has been stored
     }
-    const bool ok = mbar_wait(&mma_bar[grp], mma_parity, flags);
-    mma_parity ^= 1;
+    if (dst >= 0) {
+      uint8_t* stage = smem + (grp == 0 ? kOffStageK + buf * kStageK : kOffStageV + buf * kStageV);
+      if (gt == 0) {
+        if (ok) {
+          const uint32_t sx = smem_u32(tiles + buf * kTileOp);
+#pragma unroll
+          for (int s = 0; s < 8; ++s) {
+            const uint64_t dh = smem_desc_sw128(sw_kstep(sh, s));
+            const uint64_t dx = smem_desc_sw128(sw_kstep(sx, s));
+            umma_f16(d1, dh, dx, kIdesc, s > 0);   // D1[i][j] = sum_k H[i][k] X[j][k]
+            umma_f16(d2, dx, dh, kIdesc, s > 0);   // D2[j][i] = sum_k X[j][k] H[i][k]
+          }
+          umma_commit(&mma_bar[grp]);
+          mma_inflight = true;
+        }
+        bulk_wait_read<1>();              // the stage written two items ago has been stored
+      }
+      if (ok) {
+        ok = mbar_wait(&mma_bar[grp], mma_parity, flags);
+        if (ok) {
+          mma_parity ^= 1;
+          mma_inflight = false;
+        }
+      }
+      tc_fence_after();
+      const uint8_t* tile = tiles + buf * kTileOp;
+      if (grp == 0)
+        ok = quantize_group<0>(vec, stage, tile, ta1, ta2, line, p, n_iters, eps, bar_id, ok);
+      else
+        ok = quantize_group<1>(vec, stage, tile, ta1, ta2, line, p, n_iters, eps, bar_id, ok);
+      if (!ok) break;                     // a copy or the tensor core never signalled (flag raised)
+      fence_proxy_async_smem();
+      tc_fence_before();
+    }
+    // end of the item: its stage is complete, and the group agrees on the next item's slots
+    const bool next_ok = named_bar_and(bar_id, kGroupThreads, !has_next || src.check_ok(check_next, gt));
     tc_fence_after();
-    if (!named_bar_and(bar_id, kGroupThreads, ok)) {
-      alive = false;                    // the tensor core never signalled: stop (flag raised)
-      continue;
-    }
-    const uint8_t* tile = smem + kOffIn + (grp * 2 + buf) * kTileOp;
-    if (grp == 0)
-      quantize_group<0>(vec, stage, tile, ta1, ta2, line, p, n_iters, eps, bar_id);
-    else
-      quantize_group<1>(vec, stage, tile, ta1, ta2, line, p, n_iters, eps, bar_id);
-    fence_proxy_async_smem();
-    tc_fence_before();
-    named_bar(bar_id, kGroupThreads);
-    if (gt == 0) {
+    if (dst >= 0 && gt == 0) {
+      uint8_t* stage = smem + (grp == 0 ? kOffStageK + buf * kStageK : kOffStageV + buf * kStageV);
       uint8_t* rec = cache + dst * static_cast<int64_t>(kRec);
       if (grp == 0) {
         bulk_s2g(rec + kKCodeOff, stage, 8192);
@@ -499,9 +557,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       bulk_commit();
     }
+    if (has_next) {
+      dst = -1;
+      if (next_ok)
+        dst = src.target(next, check_next, gt, flags);
+      else if (gt == 0)
+        raise_flag(flags, KVARN_FLAG_BAD_SLOTS);
+    }
   }
-  cp_async_wait<0>();
-  if (gt == 0) bulk_wait_all();
+  if (gt == 0) {
+    // after a timeout: let copies and MMAs still in flight finish (bounded) before
+    // the shared memory and TMEM are released
+    for (int b = 0; b < 2; ++b)
+      if ((pend >> b) & 1u) mbar_wait(&load_bar[b], (load_parity >> b) & 1u, flags);
+    if (mma_inflight) mbar_wait(&mma_bar[grp], mma_parity, flags);
+    bulk_wait_all();
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -519,6 +590,7 @@ template <class Src>
 cudaError_t launch_quantize(const Src& src, uint8_t* cache, int n_iters, float eps, unsigned* flags,
                             cudaStream_t stream, int max_ctas) {
   if (src.n_items <= 0) return cudaSuccess;
+  if (src.n_items > INT32_MAX) return cudaErrorInvalidValue;
   cudaError_t err = cudaFuncSetAttribute(quantize_kernel<Src>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (err != cudaSuccess) return err;
   int64_t grid = sm_count();
@@ -547,12 +619,54 @@ __global__ void append_scatter_kernel(const uint16_t* __restrict__ k_new, const 
   if (h == 0 && t == 0 && seq_lens_out != nullptr) seq_lens_out[s] = L + 1;
 }
 
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled() {
+  static std::once_flag once;
+  static EncodeTiledFn fn = nullptr;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+// TMA map of an fp16 matrix [rows][row_elems] read in boxes of 64 channels x 128
+// rows with the 128-byte swizzle (row_elems a multiple of 64, base 16-byte aligned).
+cudaError_t tile_map(CUtensorMap* m, const void* base, uint64_t row_elems, uint64_t rows) {
+  const EncodeTiledFn fn = encode_tiled();
+  if (fn == nullptr) return cudaErrorNotSupported;
+  if (rows > (1ull << 32) || row_elems > (1ull << 32)) return cudaErrorInvalidValue;
+  const cuuint64_t dims[2] = {row_elems, rows};
+  const cuuint64_t strides[1] = {row_elems * 2};
+  const cuuint32_t box[2] = {64, 128};
+  const cuuint32_t elem_strides[2] = {1, 1};
+  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+                        elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 }  // namespace
 
 cudaError_t launch_quantize_prefill(const uint16_t* k, const uint16_t* v, const int64_t* slot, int64_t n_tokens,
                                     int hkv, int64_t num_blocks, uint8_t* cache, int n_iters, float eps,
                                     unsigned* flags, cudaStream_t stream, int max_ctas) {
-  PrefillSource src{k, v, slot, (n_tokens / kB) * hkv, hkv, num_blocks};
+  PrefillSource src{};
+  cudaError_t err = tile_map(&src.map[0], k, static_cast<uint64_t>(hkv) * kD, static_cast<uint64_t>(n_tokens));
+  if (err == cudaSuccess)
+    err = tile_map(&src.map[1], v, static_cast<uint64_t>(hkv) * kD, static_cast<uint64_t>(n_tokens));
+  if (err != cudaSuccess) return err;
+  src.slot = slot;
+  src.n_items = (n_tokens / kB) * hkv;
+  src.hkv = hkv;
+  src.num_blocks = num_blocks;
   return launch_quantize(src, cache, n_iters, eps, flags, stream, max_ctas);
 }
 
@@ -565,7 +679,16 @@ cudaError_t launch_append(const uint16_t* k_new, const uint16_t* v_new, const in
       k_new, v_new, seq_lens, seq_lens_out, ws, n_seqs, hkv);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
-  AppendSource src{ws, seq_lens, block_tables, static_cast<int64_t>(n_seqs) * hkv, hkv, max_blocks, num_blocks};
+  if (static_cast<int64_t>(n_seqs) * hkv * 2 * kB > INT32_MAX) return cudaErrorInvalidValue;
+  AppendSource src{};
+  err = tile_map(&src.map, ws, kD, static_cast<uint64_t>(n_seqs) * hkv * 2 * kB);
+  if (err != cudaSuccess) return err;
+  src.seq_lens = seq_lens;
+  src.block_tables = block_tables;
+  src.n_items = static_cast<int64_t>(n_seqs) * hkv;
+  src.hkv = hkv;
+  src.max_blocks = max_blocks;
+  src.num_blocks = num_blocks;
   return launch_quantize(src, cache, n_iters, eps, flags, stream, 0);
 }
 
