@@ -15,7 +15,9 @@
 //      accumulation; the 1/sqrt(128) factor is folded into the statistics;
 //   3. each column pass reads D2 and each row pass reads D1 straight from TMEM
 //      (tcgen05.ld 16x64b: two threads per line, 64 values each), so both passes
-//      are thread-local loops plus one shuffle with the partner thread;
+//      are thread-local loops plus one shuffle with the partner thread; the first
+//      half of every sweep is loaded at the end of the sweep before it, so its
+//      latency overlaps the reduction, the scale update and the barrier;
 //   4. fp16 scales, RTN, packing into a shared-memory stage, and two bulk stores of
 //      the group's part of the record.
 // The groups share only the Hadamard operand and the TMEM allocation (256 columns
@@ -172,13 +174,13 @@ __device__ __forceinline__ void issue_tile(const Src& src, int64_t w, int g, uin
 // variance, or a non-positive variance), a second sweep recomputes the moments
 // about the exact mean, so the result keeps the accuracy of a centred two-pass
 // variance.
-__device__ __forceinline__ float pair_moments(uint32_t taddr, const float* wv, int p, float shift, float& mean) {
+__device__ __forceinline__ float pair_moments(float (&x)[32], uint32_t taddr, const float* wv, int p, float shift,
+                                             float& mean, uint32_t next_taddr) {
   const float2 nsh = make_float2(-shift, -shift);
   float2 s0 = make_float2(0.f, 0.f), s1 = s0, s2 = s0, s3 = s0, q0 = s0, q1 = s0, q2 = s0, q3 = s0;
 #pragma unroll 1
   for (int hh = 0; hh < 2; ++hh) {
-    float x[32];
-    tmem_ld_16x64b_x32_nowait(taddr + 64 * hh, x);
+    if (hh == 1) tmem_ld_16x64b_x32_nowait(taddr + 64, x);   // the first half was started earlier
     tmem_wait_x32(x);
 #pragma unroll
     for (int q = 0; q < 8; q += 2) {
@@ -217,9 +219,8 @@ __device__ __forceinline__ float pair_moments(uint32_t taddr, const float* wv, i
     float2 r0 = make_float2(0.f, 0.f), r1 = r0;
 #pragma unroll 1
     for (int hh = 0; hh < 2; ++hh) {
-      float x[32];
       tmem_ld_16x64b_x32_nowait(taddr + 64 * hh, x);
-    tmem_wait_x32(x);
+      tmem_wait_x32(x);
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
         const float4 w = reinterpret_cast<const float4*>(wv + p * 68)[8 * hh + q];
@@ -237,6 +238,7 @@ __device__ __forceinline__ float pair_moments(uint32_t taddr, const float* wv, i
       d = 0.f;
     }
   }
+  tmem_ld_16x64b_x32_nowait(next_taddr, x);   // first half of the next sweep, waited there
   mean = shift + d;
   return fmaxf(var, 0.0f);
 }
@@ -266,12 +268,16 @@ __device__ __forceinline__ bool quantize_group(float* vec, uint8_t* stage, const
   float* vc0 = vec + kVC0 * kVec;
   uint16_t* meta = reinterpret_cast<uint16_t*>(stage + (kKind == 0 ? 8192 : 4096));
   const int pl = ps(line);
+
   if (p == 0) {
     va[pl] = 1.0f;
     vb[pl] = 1.0f;
   }
   // every thread saw its copies and the tensor core finish, or the group stops
   if (!named_bar_and(bar_id, kGroupThreads, ok)) return false;
+  // TMEM sweeps: the first half of every sweep is loaded at the end of the one before
+  float x[32];
+  tmem_ld_16x64b_x32_nowait(ta2, x);
 
   float* vmc = vec + kVMc * kVec;
   float* vmr = vec + kVMr * kVec;
@@ -283,7 +289,7 @@ __device__ __forceinline__ bool quantize_group(float* vec, uint8_t* stage, const
       const float shift = it == 0 ? __half2float(*reinterpret_cast<const __half*>(tile + sw_offset(line, 0)))
                                   : vmc[pl];
       float mean;
-      const float var = pair_moments(ta2, va, p, shift, mean) * kVarScale;
+      const float var = pair_moments(x, ta2, va, p, shift, mean, ta1) * kVarScale;
       if (p == 0) {
         const float b = vb[pl];
         vb[pl] = div_sqrt(b, fmaf(b * b, var, eps));
@@ -294,7 +300,8 @@ __device__ __forceinline__ bool quantize_group(float* vec, uint8_t* stage, const
     // row pass: channel i = line, tokens e = p + 2k (D1), weights b
     {
       float mean;
-      const float var = pair_moments(ta1, vb, p, it == 0 ? 0.0f : vmr[pl], mean) * kVarScale;
+      const uint32_t next = it + 1 < n_iters ? ta2 : (kKind == 0 ? ta1 : ta2);   // next column pass or extremes
+      const float var = pair_moments(x, ta1, vb, p, it == 0 ? 0.0f : vmr[pl], mean, next) * kVarScale;
       if (p == 0) {
         const float a = va[pl];
         va[pl] = div_sqrt(a, fmaf(a * a, var, eps));
@@ -322,9 +329,9 @@ __device__ __forceinline__ bool quantize_group(float* vec, uint8_t* stage, const
     float mn = INFINITY, mx = -INFINITY;
 #pragma unroll 1
     for (int hh = 0; hh < 2; ++hh) {
-      float xh[32];
-      tmem_ld_16x64b_x32_nowait((kKind == 0 ? ta1 : ta2) + 64 * hh, xh);
-    tmem_wait_x32(xh);
+      float* xh = x;
+      if (hh == 1) tmem_ld_16x64b_x32_nowait((kKind == 0 ? ta1 : ta2) + 64, xh);
+      tmem_wait_x32(xh);
       // y = (x * hc_j) * g_i; the factor that is constant along the thread's line is
       // positive, so it multiplies the extremes afterwards (same rounding as per element)
       const float* vv = kKind == 0 ? vh : vg;
@@ -337,6 +344,7 @@ __device__ __forceinline__ bool quantize_group(float* vec, uint8_t* stage, const
         mx = fmax3(fmax3(mx, y0.x, y0.y), y1.x, y1.y);
       }
     }
+    tmem_ld_16x64b_x32_nowait(kKind == 0 ? ta2 : ta1, x);   // first half of the codes sweep
     const float line_factor = kKind == 0 ? vg[pl] : vh[pl];
     mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, 2)) * line_factor;
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2)) * line_factor;
@@ -360,8 +368,8 @@ __device__ __forceinline__ bool quantize_group(float* vec, uint8_t* stage, const
   const float2 own2 = make_float2(own, own);
 #pragma unroll 1
   for (int hh = 0; hh < 2; ++hh) {
-    float xh[32];
-    tmem_ld_16x64b_x32_nowait((kKind == 0 ? ta2 : ta1) + 64 * hh, xh);
+    float* xh = x;
+    if (hh == 1) tmem_ld_16x64b_x32_nowait((kKind == 0 ? ta2 : ta1) + 64, xh);
     tmem_wait_x32(xh);
     // v = (x * own) * w_e + c0_e = (y - z) / s + 1/2, clamped to [0, levels]; the
     // round-down add of 2^23 leaves 0x4B000000 + floor(v) in the bits, and each
@@ -425,10 +433,10 @@ __device__ __forceinline__ bool quantize_group(float* vec, uint8_t* stage, const
   return true;
 }
 
-// 96 registers a thread (the 512 threads could hold 128): measured faster on the
-// prefill workload than the larger allocation, with a few bytes of spill.
+// 104 registers a thread (the 512 threads could hold 128): measured faster on the
+// prefill workload than 88, 96 or 128.
 template <class Src>
-__global__ void __maxnreg__(96)
+__global__ void __maxnreg__(104)
     quantize_kernel(const __grid_constant__ Src src, uint8_t* __restrict__ cache, int n_iters, float eps,
                     unsigned* flags) {
   extern __shared__ __align__(1024) uint8_t smem[];
