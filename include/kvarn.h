@@ -67,8 +67,14 @@
  *     whole blocks, a sequence longer than its block table) make the kernels
  *     skip the affected tile and set a bit in a device flag word, read and
  *     cleared by kvarn_device_flags().
- *   - The calls keep no host state besides the per-thread error message; the
- *     device flag word is shared by every call on a device.
+ *   - The calls keep no host state besides the per-thread error message, the
+ *     device flag word's address and which kernels had their shared-memory
+ *     limit raised (both looked up once per device); the flag word is shared by
+ *     every call on a device.
+ *   - kvarn_quantize_tiles, kvarn_append_decode and kvarn_decode_attention only
+ *     queue kernels on `stream` (no allocation, no host synchronisation), so once
+ *     each has been called on a device, a serving step made of them can be
+ *     captured into a CUDA graph and replayed.
  */
 #ifndef KVARN_H
 #define KVARN_H
@@ -156,7 +162,9 @@ KVARN_API kvarn_status kvarn_quantize_tiles(const uint16_t* k, const uint16_t* v
  * Decode-step write. For each sequence s with L = seq_lens[s] stored tokens,
  * writes the new token into workspace[s][h][*][L % 128][*]; when that completes
  * the partial tile (L % 128 == 127) the tile is quantized into block
- * block_tables[s][L / 128] for every kv-head.
+ * block_tables[s][L / 128] for every kv-head. One kernel launch: the
+ * quantize kernel writes each (sequence, kv-head)'s token before it copies
+ * that item's tile.
  *   k_new, v_new  fp16 [n_seqs][num_kv_heads][128].
  *   seq_lens      int32 [n_seqs], lengths before the append, >= 0.
  *   seq_lens_out  int32 [n_seqs] or NULL: receives seq_lens[s] + 1. Must not

@@ -5,6 +5,7 @@
 #include <stdio.h>
 
 #include <cstring>
+#include <mutex>
 
 #include "../../include/kvarn.h"
 #include "kvarn_launch.h"
@@ -56,10 +57,8 @@ kvarn_status need_ptr(const void* p, const char* name) {
 }
 
 kvarn_status flags_ptr(unsigned** out) {
-  void* p = nullptr;
-  cudaError_t e = cudaGetSymbolAddress(&p, g_device_flags);
-  if (e != cudaSuccess) return fail(KVARN_ECUDA, "cudaGetSymbolAddress(flags): %s", cudaGetErrorString(e));
-  *out = static_cast<unsigned*>(p);
+  const cudaError_t e = kvarn::flags_device_ptr(out);
+  if (e != cudaSuccess) return fail(KVARN_ECUDA, "device flag word: %s", cudaGetErrorString(e));
   return KVARN_OK;
 }
 
@@ -195,11 +194,26 @@ const char* kvarn_last_error(void) { return g_err; }
 // Used by other translation units of the library (not part of the C ABI).
 namespace kvarn {
 
+// The flag word's address on the current device, looked up on the first call per
+// device and kept (later calls, e.g. inside a CUDA-graph capture, make no lookup).
 cudaError_t flags_device_ptr(unsigned** out) {
+  static std::mutex mu;
+  static void* known[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const bool cacheable = dev >= 0 && dev < 64;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cacheable && known[dev] != nullptr) {
+    *out = static_cast<unsigned*>(known[dev]);
+    return cudaSuccess;
+  }
   void* p = nullptr;
-  const cudaError_t e = cudaGetSymbolAddress(&p, g_device_flags);
-  if (e == cudaSuccess) *out = static_cast<unsigned*>(p);
-  return e;
+  e = cudaGetSymbolAddress(&p, g_device_flags);
+  if (e != cudaSuccess) return e;
+  if (cacheable) known[dev] = p;
+  *out = static_cast<unsigned*>(p);
+  return cudaSuccess;
 }
 
 kvarn_status set_error(kvarn_status st, const char* msg) {

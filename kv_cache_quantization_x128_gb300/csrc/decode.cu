@@ -616,7 +616,8 @@ cudaError_t launch_decode(const uint16_t* q, const uint8_t* cache, const uint16_
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   if (max_blocks > 0) {
-    err = cudaFuncSetAttribute(decode_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSplitSmem);
+    static std::atomic<unsigned long long> smem_set{0};
+    err = set_smem_once(decode_split_kernel, kSplitSmem, smem_set);
     if (err != cudaSuccess) return err;
     decode_split_kernel<<<a.n_ctas, kWarps * 32, kSplitSmem, stream>>>(a);
     err = cudaGetLastError();

@@ -4,9 +4,25 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "../../include/kvarn.h"
 
 namespace kvarn {
+
+// Sets a kernel's dynamic shared-memory limit once per device (bit d of `done`);
+// later launches, e.g. inside a CUDA-graph capture, make no runtime call for it.
+template <class Kernel>
+inline cudaError_t set_smem_once(Kernel* kernel, int bytes, std::atomic<unsigned long long>& done) {
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  const bool cacheable = dev >= 0 && dev < 64;
+  if (cacheable && ((done.load(std::memory_order_acquire) >> dev) & 1ull)) return cudaSuccess;
+  err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (err == cudaSuccess && cacheable) done.fetch_or(1ull << dev, std::memory_order_acq_rel);
+  return err;
+}
 
 cudaError_t launch_quantize_prefill(const uint16_t* k, const uint16_t* v, const int64_t* slot, int64_t n_tokens,
                                     int hkv, int64_t num_blocks, uint8_t* cache, int n_iters, float eps,

@@ -86,6 +86,7 @@ struct PrefillSource {
   int64_t num_blocks;
 
   __device__ bool needs_load(int64_t) const { return true; }
+  __device__ void scatter(int64_t, int, int) const {}
   // TMA coordinates (channel, token) of the item's 128 x 128 tile of tensor g
   __device__ void coords(int64_t w, int, int& x, int& y) const {
     const uint32_t chunk = static_cast<uint32_t>(w) / static_cast<uint32_t>(hkv);
@@ -115,6 +116,10 @@ struct PrefillSource {
 
 struct AppendSource {
   CUtensorMap map;              // workspace as [n_seqs * hkv * 2 * 128 rows][128 channels] fp16
+  const uint16_t* k_new;        // [n_seqs][hkv][128] fp16: the token appended to each sequence
+  const uint16_t* v_new;
+  uint16_t* ws;                 // the workspace the map describes
+  int32_t* seq_lens_out;        // lengths after the append (may be NULL)
   const int32_t* seq_lens;      // lengths before the append
   const int32_t* block_tables;  // [n_seqs][max_blocks]
   int64_t n_items;              // n_seqs * hkv
@@ -129,6 +134,23 @@ struct AppendSource {
   __device__ void coords(int64_t w, int g, int& x, int& y) const {
     x = 0;
     y = (static_cast<int>(w) * 2 + g) * kB;
+  }
+  // Threads t < 16 of group g copy 16 bytes each of item w's new token (tensor g)
+  // into its workspace row L % 128; thread 0 of the key group also writes the new
+  // length of the item's sequence (kv-head 0). The writers fence the global writes
+  // against the async proxy; a group barrier then orders them before the TMA copy
+  // of the tile.
+  __device__ void scatter(int64_t w, int g, int t) const {
+    if (t < 0 || t >= 16) return;
+    const uint32_t s = static_cast<uint32_t>(w) / static_cast<uint32_t>(hkv);
+    const uint32_t h = static_cast<uint32_t>(w) - s * hkv;
+    const int L = seq_lens[s];
+    if (L < 0) return;
+    const uint16_t* src = (g ? v_new : k_new) + static_cast<int64_t>(w) * kD + t * 8;
+    uint16_t* dst = ws + ((static_cast<int64_t>(w) * 2 + g) * kB + L % kB) * kD + t * 8;
+    *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
+    if (g == 0 && h == 0 && t == 0 && seq_lens_out != nullptr) seq_lens_out[s] = L + 1;
+    asm volatile("fence.proxy.async.global;" ::: "memory");
   }
   struct Check {};
   __device__ Check prepare(int64_t, int) const { return Check{}; }
@@ -484,16 +506,19 @@ __global__ void __maxnreg__(104)
   int64_t item = blockIdx.x;
   uint32_t pend = 0;               // bit b: a copy into buffer b has not been waited for
   uint32_t load_parity = 0;        // bit b: phase parity of buffer b's barrier
-  if (src.needs_load(item)) {
-    if (gt == 0) issue_tile(src, item, grp, tiles, &load_bar[0]);
-    pend = 1;
-  }
+  // appended tokens go into the workspace two items ahead of their tile's copy
+  src.scatter(item, grp, gt);
+  if (item + gridDim.x < src.n_items) src.scatter(item + gridDim.x, grp, gt - 16);
   typename Src::Check check = src.prepare(item, gt);
   int64_t dst = -1;
   if (named_bar_and(bar_id, kGroupThreads, src.check_ok(check, gt)))
     dst = src.target(item, check, gt, flags);
   else if (gt == 0)
     raise_flag(flags, KVARN_FLAG_BAD_SLOTS);
+  if (src.needs_load(item)) {
+    if (gt == 0) issue_tile(src, item, grp, tiles, &load_bar[0]);
+    pend = 1;
+  }
   uint32_t mma_parity = 0;
   bool mma_inflight = false;       // thread gt == 0: an issued MMA not yet seen complete
   for (int k = 0; item < src.n_items; ++k, item += gridDim.x) {
@@ -507,6 +532,7 @@ __global__ void __maxnreg__(104)
         pend |= 2u >> buf;
       }
       check_next = src.prepare(next, gt);
+      if (next + gridDim.x < src.n_items) src.scatter(next + gridDim.x, grp, gt);   // before this item's end barrier
     }
     bool ok = true;
     if ((pend >> buf) & 1u) {
@@ -599,32 +625,14 @@ cudaError_t launch_quantize(const Src& src, uint8_t* cache, int n_iters, float e
                             cudaStream_t stream, int max_ctas) {
   if (src.n_items <= 0) return cudaSuccess;
   if (src.n_items > INT32_MAX) return cudaErrorInvalidValue;
-  cudaError_t err = cudaFuncSetAttribute(quantize_kernel<Src>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  static std::atomic<unsigned long long> smem_set{0};
+  cudaError_t err = set_smem_once(quantize_kernel<Src>, kSmemBytes, smem_set);
   if (err != cudaSuccess) return err;
   int64_t grid = sm_count();
   if (max_ctas > 0 && grid > max_ctas) grid = max_ctas;
   if (grid > src.n_items) grid = src.n_items;
   quantize_kernel<Src><<<static_cast<unsigned>(grid), kThreads, kSmemBytes, stream>>>(src, cache, n_iters, eps, flags);
   return cudaGetLastError();
-}
-
-// New token of each (sequence, kv-head) into its workspace slot; h == 0 also
-// writes the new length.
-__global__ void append_scatter_kernel(const uint16_t* __restrict__ k_new, const uint16_t* __restrict__ v_new,
-                                      const int32_t* __restrict__ seq_lens, int32_t* __restrict__ seq_lens_out,
-                                      uint16_t* __restrict__ ws, int n_seqs, int hkv) {
-  const int64_t pair = blockIdx.x;  // s * hkv + h
-  const int64_t s = pair / hkv;
-  const int h = static_cast<int>(pair - s * hkv);
-  const int L = seq_lens[s];
-  if (L < 0) return;
-  const int pos = L % kB;
-  const int t = threadIdx.x;  // 0..31: 16-byte pieces of K (0..15) and V (16..31)
-  const int which = t >> 4, piece = t & 15;
-  const uint16_t* src = (which ? v_new : k_new) + pair * kD + piece * 8;
-  uint16_t* dst = ws + (((s * hkv + h) * 2 + which) * kB + pos) * static_cast<int64_t>(kD) + piece * 8;
-  *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
-  if (h == 0 && t == 0 && seq_lens_out != nullptr) seq_lens_out[s] = L + 1;
 }
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -683,14 +691,14 @@ cudaError_t launch_append(const uint16_t* k_new, const uint16_t* v_new, const in
                           int64_t num_blocks, uint16_t* ws, uint8_t* cache, int n_iters, float eps,
                           unsigned* flags, cudaStream_t stream) {
   if (n_seqs <= 0) return cudaSuccess;
-  append_scatter_kernel<<<static_cast<unsigned>(static_cast<int64_t>(n_seqs) * hkv), 32, 0, stream>>>(
-      k_new, v_new, seq_lens, seq_lens_out, ws, n_seqs, hkv);
-  cudaError_t err = cudaGetLastError();
-  if (err != cudaSuccess) return err;
   if (static_cast<int64_t>(n_seqs) * hkv * 2 * kB > INT32_MAX) return cudaErrorInvalidValue;
   AppendSource src{};
-  err = tile_map(&src.map, ws, kD, static_cast<uint64_t>(n_seqs) * hkv * 2 * kB);
+  const cudaError_t err = tile_map(&src.map, ws, kD, static_cast<uint64_t>(n_seqs) * hkv * 2 * kB);
   if (err != cudaSuccess) return err;
+  src.k_new = k_new;
+  src.v_new = v_new;
+  src.ws = ws;
+  src.seq_lens_out = seq_lens_out;
   src.seq_lens = seq_lens;
   src.block_tables = block_tables;
   src.n_items = static_cast<int64_t>(n_seqs) * hkv;
