@@ -38,9 +38,11 @@ Readings [R] fixed here (the pages are silent on them):
   mask), and the tokens of a partial last tile are taken exactly from the fp16
   decode workspace (unrotated, unquantised).
 
-The packed record layout (14336 bytes per (block, kv-head)) is documented in the
-C header of the CUDA library and restated by ``k_code_position`` and
-``v_code_position`` below.
+The packed record layout (14336 bytes per (block, kv-head) for the default
+preset) is documented in the C header of the CUDA library and restated by the
+position functions below. Besides the README's preset k4v2, the library offers
+k4v4 and k2v2 (the pages report 2-bit results as well); a record is the key codes,
+then the value codes, then 1024 bytes of key metadata and 1024 of value metadata.
 """
 from __future__ import annotations
 
@@ -60,6 +62,10 @@ V_CODE_OFF, V_CODE_BYTES = 8192, 4096
 K_META_OFF = 12288
 V_META_OFF = 13312
 RECORD_BYTES = 14336
+
+# bit widths (keys, values) of the presets; the default one is the README's
+PRESETS = {"k4v2": (4, 2), "k4v4": (4, 4), "k2v2": (2, 2)}
+DEFAULT_PRESET = "k4v2"
 
 
 # ----------------------------------------------------------------------------------
@@ -133,15 +139,16 @@ def rtn(y: np.ndarray, bits: int, axis: int):
     return codes, s, z, dict(zmin=ymin, zmax=ymax, s_pre=s_pre, pre=pre)
 
 
-def quantize_tensor(x: np.ndarray, kind: str, n_iters: int = N_ITERS, eps: float = EPS):
+def quantize_tensor(x: np.ndarray, kind: str, n_iters: int = N_ITERS, eps: float = EPS, bits: int | None = None):
     """Stages 2-4 for tiles x [..., 128 channels, 128 tokens] (float64 holding fp16
-    values). kind 'K': 4-bit codes, s and z per channel (row); kind 'V': 2-bit
-    codes, s and z per token (column).
+    values). kind 'K': s and z per channel (row); kind 'V': s and z per token
+    (column); `bits` codes (default: 4 for K, 2 for V, the README's preset).
 
     Returns a dict with fp16-valued r [.., 128], c [.., 128], s, z, the codes
     [.., 128 ch, 128 tok] and the pre-rounding values needed to judge ties."""
     assert kind in ("K", "V")
-    bits = K_BITS if kind == "K" else V_BITS
+    if bits is None:
+        bits = K_BITS if kind == "K" else V_BITS
     xr = rotate(np.asarray(x, np.float64))
     lr, lc = normalise(xr, n_iters, eps)
     r_pre, c_pre = np.exp(lr), np.exp(lc)
@@ -149,7 +156,7 @@ def quantize_tensor(x: np.ndarray, kind: str, n_iters: int = N_ITERS, eps: float
     c = fp16_rne(np.clip(c_pre, FP16_MIN_NORMAL, FP16_MAX))
     y = xr / (r[..., :, None] * c[..., None, :])
     codes, s, z, info = rtn(y, bits, axis=-1 if kind == "K" else -2)
-    return dict(kind=kind, codes=codes, r=r, c=c, s=s, z=z, r_pre=r_pre, c_pre=c_pre,
+    return dict(kind=kind, bits=bits, codes=codes, r=r, c=c, s=s, z=z, r_pre=r_pre, c_pre=c_pre,
                 z_pre=info["zmin"], s_pre=info["s_pre"], code_pre=info["pre"], xr=xr, y=y)
 
 
@@ -167,10 +174,11 @@ def dequant_tensor(codes, r, c, s, z, kind: str, rotated: bool = False):
 
 
 # ----------------------------------------------------------------------------------
-# Packed record layout (one (block, kv-head): 14336 bytes)
+# Packed record layout (one (block, kv-head))
 # ----------------------------------------------------------------------------------
-def k_code_position(i: int, t: int):
-    """(byte, bit shift) of the 4-bit key code of channel i, token t.
+def k4_position(i: int, t: int):
+    """(byte, bit shift) of the 4-bit key code of channel i, token t, counted from
+    the start of the key codes.
 
     Token t owns bytes [64 t, 64 t + 64): four 16-byte groups g4 = (i >> 1) & 3,
     each four little-endian 32-bit words w = i >> 5. Within a word, nibble
@@ -178,12 +186,25 @@ def k_code_position(i: int, t: int):
     g4 = (i >> 1) & 3
     w = i >> 5
     p = 4 * (i & 1) + 2 * ((i >> 4) & 1) + ((i >> 3) & 1)
-    byte = K_CODE_OFF + t * 64 + g4 * 16 + w * 4 + p // 2
-    return byte, 4 * (p % 2)
+    return t * 64 + g4 * 16 + w * 4 + p // 2, 4 * (p % 2)
 
 
-def v_code_position(i: int, t: int):
-    """(byte, bit shift) of the 2-bit value code of channel i, token t.
+def k2_position(i: int, t: int):
+    """(byte, bit shift) of the 2-bit key code of channel i, token t, counted from
+    the start of the key codes.
+
+    Token t owns bytes [32 t, 32 t + 32): four 8-byte groups g4 = (i >> 1) & 3,
+    each two little-endian words u = i >> 6. Within a word, crumb
+    p = 8 (i & 1) + 2 ((i >> 4) & 3) + ((i >> 3) & 1), crumb p at bits 2p..2p+1."""
+    g4 = (i >> 1) & 3
+    u = i >> 6
+    p = 8 * (i & 1) + 2 * ((i >> 4) & 3) + ((i >> 3) & 1)
+    return t * 32 + g4 * 8 + u * 4 + p // 4, 2 * (p % 4)
+
+
+def v2_position(i: int, t: int):
+    """(byte, bit shift) of the 2-bit value code of channel i, token t, counted from
+    the start of the value codes.
 
     Channel i lives in 512-byte panel m = i >> 4 (16 channels). Inside a panel,
     16-byte cell (i & 7) * 4 + g4 with g4 = (t >> 1) & 3 holds 8 bytes for channel
@@ -195,28 +216,73 @@ def v_code_position(i: int, t: int):
     which = (i >> 3) & 1
     u = t >> 6
     p = 8 * (t & 1) + 2 * ((t >> 4) & 3) + ((t >> 3) & 1)
-    byte = V_CODE_OFF + m * 512 + cell * 16 + which * 8 + u * 4 + p // 4
-    return byte, 2 * (p % 4)
+    return m * 512 + cell * 16 + which * 8 + u * 4 + p // 4, 2 * (p % 4)
 
 
-def _source_tables():
-    """For each code byte, the flat (i * 128 + t) index of the code held in each of
-    its nibbles (K) / crumbs (V)."""
-    k_src = np.full((K_CODE_BYTES, 2), -1, np.int64)
-    v_src = np.full((V_CODE_BYTES, 4), -1, np.int64)
+def v4_position(i: int, t: int):
+    """(byte, bit shift) of the 4-bit value code of channel i, token t, counted from
+    the start of the value codes: the 4-bit key layout with the roles of channel
+    and token exchanged. Channel i owns bytes [64 i, 64 i + 64): four 16-byte
+    groups g4 = (t >> 1) & 3, each four words w = t >> 5; nibble
+    p = 4 (t & 1) + 2 ((t >> 4) & 1) + ((t >> 3) & 1) at bits 4p..4p+3."""
+    g4 = (t >> 1) & 3
+    w = t >> 5
+    p = 4 * (t & 1) + 2 * ((t >> 4) & 1) + ((t >> 3) & 1)
+    return i * 64 + g4 * 16 + w * 4 + p // 2, 4 * (p % 2)
+
+
+def k_code_position(i: int, t: int):
+    """(byte, bit shift) of the key code of channel i, token t in a k4v2 record."""
+    b, sh = k4_position(i, t)
+    return K_CODE_OFF + b, sh
+
+
+def v_code_position(i: int, t: int):
+    """(byte, bit shift) of the value code of channel i, token t in a k4v2 record."""
+    b, sh = v2_position(i, t)
+    return V_CODE_OFF + b, sh
+
+
+def _source_table(position, bits: int) -> np.ndarray:
+    """For each byte of a code area, the flat (i * 128 + t) index of the code in
+    each of its 8 / bits slots (slot n at bits n*bits..)."""
+    per = 8 // bits
+    nbytes = D * B * bits // 8
+    src = np.full((nbytes, per), -1, np.int64)
     for i in range(D):
         for t in range(B):
-            b, sh = k_code_position(i, t)
-            assert k_src[b - K_CODE_OFF, sh // 4] == -1
-            k_src[b - K_CODE_OFF, sh // 4] = i * B + t
-            b, sh = v_code_position(i, t)
-            assert v_src[b - V_CODE_OFF, sh // 2] == -1
-            v_src[b - V_CODE_OFF, sh // 2] = i * B + t
-    assert (k_src >= 0).all() and (v_src >= 0).all()
-    return k_src, v_src
+            b, sh = position(i, t)
+            assert src[b, sh // bits] == -1
+            src[b, sh // bits] = i * B + t
+    assert (src >= 0).all()
+    return src
 
 
-K_SRC, V_SRC = _source_tables()
+class Layout:
+    """Byte layout of the records of one preset."""
+
+    def __init__(self, name: str):
+        self.name = name
+        self.k_bits, self.v_bits = PRESETS[name]
+        self.k_code_off, self.k_code_bytes = 0, D * B * self.k_bits // 8
+        self.v_code_off, self.v_code_bytes = self.k_code_bytes, D * B * self.v_bits // 8
+        self.k_meta_off = self.v_code_off + self.v_code_bytes
+        self.v_meta_off = self.k_meta_off + 1024
+        self.record_bytes = self.v_meta_off + 1024
+        self.k_src = _source_table(k4_position if self.k_bits == 4 else k2_position, self.k_bits)
+        self.v_src = _source_table(v4_position if self.v_bits == 4 else v2_position, self.v_bits)
+
+
+LAYOUTS = {name: Layout(name) for name in PRESETS}
+K_SRC, V_SRC = LAYOUTS[DEFAULT_PRESET].k_src, LAYOUTS[DEFAULT_PRESET].v_src
+
+
+def layout_of(record_bytes: int) -> Layout:
+    """The preset layout whose records have `record_bytes` bytes."""
+    for lay in LAYOUTS.values():
+        if lay.record_bytes == record_bytes:
+            return lay
+    raise ValueError(f"no preset has {record_bytes}-byte records")
 
 
 def _f16_bytes(vals) -> np.ndarray:
@@ -224,38 +290,48 @@ def _f16_bytes(vals) -> np.ndarray:
     return a.view(np.uint8).reshape(a.shape[:-1] + (a.shape[-1] * 2,))
 
 
-def pack_record(kq: dict, vq: dict) -> np.ndarray:
-    """Records [..., 14336] uint8 from quantize_tensor results for K and V."""
+def _pack_codes(codes: np.ndarray, src: np.ndarray, bits: int) -> np.ndarray:
+    out = np.zeros(codes.shape[:-1] + (src.shape[0],), np.uint8)
+    for n in range(src.shape[1]):
+        out |= (codes[..., src[:, n]] << (bits * n)).astype(np.uint8)
+    return out
+
+
+def _unpack_codes(area: np.ndarray, src: np.ndarray, bits: int) -> np.ndarray:
+    codes = np.zeros(area.shape[:-1] + (D * B,), np.uint8)
+    for n in range(src.shape[1]):
+        codes[..., src[:, n]] = (area >> (bits * n)) & ((1 << bits) - 1)
+    return codes
+
+
+def pack_record(kq: dict, vq: dict, preset: str = DEFAULT_PRESET) -> np.ndarray:
+    """Records [..., record bytes] uint8 from quantize_tensor results for K and V."""
+    lay = LAYOUTS[preset]
+    assert kq.get("bits", lay.k_bits) == lay.k_bits and vq.get("bits", lay.v_bits) == lay.v_bits
     kc = kq["codes"].reshape(kq["codes"].shape[:-2] + (D * B,)).astype(np.uint8)
     vc = vq["codes"].reshape(vq["codes"].shape[:-2] + (D * B,)).astype(np.uint8)
-    lead = kc.shape[:-1]
-    rec = np.zeros(lead + (RECORD_BYTES,), np.uint8)
-    rec[..., K_CODE_OFF:K_CODE_OFF + K_CODE_BYTES] = kc[..., K_SRC[:, 0]] | (kc[..., K_SRC[:, 1]] << 4)
-    rec[..., V_CODE_OFF:V_CODE_OFF + V_CODE_BYTES] = (
-        vc[..., V_SRC[:, 0]] | (vc[..., V_SRC[:, 1]] << 2) | (vc[..., V_SRC[:, 2]] << 4) | (vc[..., V_SRC[:, 3]] << 6))
-    for off, q in ((K_META_OFF, kq), (V_META_OFF, vq)):
+    rec = np.zeros(kc.shape[:-1] + (lay.record_bytes,), np.uint8)
+    rec[..., lay.k_code_off:lay.k_code_off + lay.k_code_bytes] = _pack_codes(kc, lay.k_src, lay.k_bits)
+    rec[..., lay.v_code_off:lay.v_code_off + lay.v_code_bytes] = _pack_codes(vc, lay.v_src, lay.v_bits)
+    for off, q in ((lay.k_meta_off, kq), (lay.v_meta_off, vq)):
         for n, name in enumerate(("r", "c", "s", "z")):
             rec[..., off + 256 * n: off + 256 * (n + 1)] = _f16_bytes(q[name])
     return rec
 
 
 def unpack_record(rec: np.ndarray):
-    """Inverse of pack_record: dicts for K and V with codes [.., 128 ch, 128 tok]
-    and r, c, s, z (float64 holding fp16)."""
+    """Inverse of pack_record (the preset follows from the record size): dicts for
+    K and V with codes [.., 128 ch, 128 tok], bits and r, c, s, z (float64
+    holding fp16)."""
     rec = np.asarray(rec, np.uint8)
+    lay = layout_of(rec.shape[-1])
     lead = rec.shape[:-1]
-    kb = rec[..., K_CODE_OFF:K_CODE_OFF + K_CODE_BYTES]
-    vb = rec[..., V_CODE_OFF:V_CODE_OFF + V_CODE_BYTES]
-    kc = np.zeros(lead + (D * B,), np.uint8)
-    vc = np.zeros(lead + (D * B,), np.uint8)
-    kc[..., K_SRC[:, 0]] = kb & 0xF
-    kc[..., K_SRC[:, 1]] = kb >> 4
-    for n in range(4):
-        vc[..., V_SRC[:, n]] = (vb >> (2 * n)) & 3
+    kc = _unpack_codes(rec[..., lay.k_code_off:lay.k_code_off + lay.k_code_bytes], lay.k_src, lay.k_bits)
+    vc = _unpack_codes(rec[..., lay.v_code_off:lay.v_code_off + lay.v_code_bytes], lay.v_src, lay.v_bits)
     out = []
-    for off, codes, kind in ((K_META_OFF, kc, "K"), (V_META_OFF, vc, "V")):
+    for off, codes, kind, bits in ((lay.k_meta_off, kc, "K", lay.k_bits), (lay.v_meta_off, vc, "V", lay.v_bits)):
         meta = np.ascontiguousarray(rec[..., off:off + 1024]).view("<f2").astype(np.float64)
-        d = dict(kind=kind, codes=codes.reshape(lead + (D, B)))
+        d = dict(kind=kind, bits=bits, codes=codes.reshape(lead + (D, B)))
         for n, name in enumerate(("r", "c", "s", "z")):
             d[name] = meta[..., 128 * n:128 * (n + 1)]
         out.append(d)
@@ -272,21 +348,25 @@ def dequant_record(rec: np.ndarray, rotated: bool = False):
 # ----------------------------------------------------------------------------------
 # Whole-tile and paged-cache operations
 # ----------------------------------------------------------------------------------
-def quantize_tiles(k_tok: np.ndarray, v_tok: np.ndarray, n_iters: int = N_ITERS, eps: float = EPS):
+def quantize_tiles(k_tok: np.ndarray, v_tok: np.ndarray, n_iters: int = N_ITERS, eps: float = EPS,
+                   preset: str = DEFAULT_PRESET):
     """k_tok, v_tok: fp16 tiles [..., 128 tokens, 128 channels] (vLLM row layout).
-    Returns (records [..., 14336], K result, V result)."""
+    Returns (records [..., record bytes], K result, V result)."""
+    kb, vb = PRESETS[preset]
     kx = np.swapaxes(np.asarray(k_tok, np.float64), -1, -2)
     vx = np.swapaxes(np.asarray(v_tok, np.float64), -1, -2)
-    kq = quantize_tensor(kx, "K", n_iters, eps)
-    vq = quantize_tensor(vx, "V", n_iters, eps)
-    return pack_record(kq, vq), kq, vq
+    kq = quantize_tensor(kx, "K", n_iters, eps, bits=kb)
+    vq = quantize_tensor(vx, "V", n_iters, eps, bits=vb)
+    return pack_record(kq, vq, preset), kq, vq
 
 
 def quantize_into_cache(k, v, slot_mapping, cache, tiles=None, batch: int = 32):
     """Prefill write (kvarn_quantize_tiles): every run of 128 tokens [t0, t0+128)
     goes to block slot_mapping[t0] // 128, token t0 + k at offset k. k, v: fp16
-    [n_tokens, Hkv, 128]; cache: uint8 [num_blocks, Hkv, 14336], updated in place.
-    `tiles`, if given, restricts the work to a list of (chunk, head) pairs."""
+    [n_tokens, Hkv, 128]; cache: uint8 [num_blocks, Hkv, record bytes] (the preset
+    follows from the record size), updated in place. `tiles`, if given, restricts
+    the work to a list of (chunk, head) pairs."""
+    preset = layout_of(cache.shape[-1]).name
     n_tokens, hkv, _ = k.shape
     assert n_tokens % B == 0
     work = tiles if tiles is not None else [(ch, h) for ch in range(n_tokens // B) for h in range(hkv)]
@@ -294,7 +374,7 @@ def quantize_into_cache(k, v, slot_mapping, cache, tiles=None, batch: int = 32):
         part = work[b0:b0 + batch]
         kt = np.stack([k[ch * B:(ch + 1) * B, h, :] for ch, h in part])
         vt = np.stack([v[ch * B:(ch + 1) * B, h, :] for ch, h in part])
-        recs, _, _ = quantize_tiles(kt, vt)
+        recs, _, _ = quantize_tiles(kt, vt, preset=preset)
         for (ch, h), rec in zip(part, recs):
             blk = int(slot_mapping[ch * B]) // B
             cache[blk, h] = rec
@@ -314,7 +394,7 @@ def attend(q: np.ndarray, k_tok: np.ndarray, v_tok: np.ndarray) -> np.ndarray:
 def decode_one(q_heads, cache, workspace_sh, block_table, seq_len: int, kv_head: int):
     """Decode attention for the q-heads of one GQA group over one sequence.
 
-    q_heads: [G, 128]; cache: [num_blocks, Hkv, 14336]; workspace_sh: fp16
+    q_heads: [G, 128]; cache: [num_blocks, Hkv, record bytes]; workspace_sh: fp16
     [2, 128 tok, 128 ch] for this (sequence, kv-head) or None; block_table:
     [max_blocks]. Full tiles come from the packed cache (dequantised, un-rotated),
     the last seq_len % 128 tokens from the workspace."""
@@ -355,6 +435,7 @@ def append(k_new, v_new, seq_lens, block_tables, workspace, cache):
     inputs are not modified."""
     ws = np.array(workspace, copy=True)
     cache = np.array(cache, copy=True)
+    preset = layout_of(cache.shape[-1]).name
     n_seqs = k_new.shape[0]
     for s in range(n_seqs):
         L = int(seq_lens[s])
@@ -363,11 +444,11 @@ def append(k_new, v_new, seq_lens, block_tables, workspace, cache):
         ws[s, :, 1, pos] = v_new[s]
         if pos == B - 1:
             blk = int(block_tables[s, L // B])
-            recs, _, _ = quantize_tiles(ws[s, :, 0], ws[s, :, 1])
+            recs, _, _ = quantize_tiles(ws[s, :, 0], ws[s, :, 1], preset=preset)
             cache[blk] = recs
     return ws, cache, np.asarray(seq_lens) + 1
 
 
-def compression_ratio() -> float:
+def compression_ratio(preset: str = DEFAULT_PRESET) -> float:
     """fp16 bytes of one (K, V) tile-head over its packed record."""
-    return (2 * D * B * 2) / RECORD_BYTES
+    return (2 * D * B * 2) / LAYOUTS[preset].record_bytes

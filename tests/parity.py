@@ -46,14 +46,15 @@ def _meta_ok(gpu, ref, pre):
 
 
 def compare_records(gpu_rec: np.ndarray, kq: dict, vq: dict) -> dict:
-    """Check GPU records [N, 14336] against oracle results for the same N tiles.
+    """Check GPU records [N, record bytes] against oracle results for the same N tiles.
     Raises AssertionError with a description on the first violation; returns
     counts of the flips it accepted."""
     gk, gv = o.unpack_record(gpu_rec)
     stats = dict(meta_flips=0, code_flips=0, codes=0, groups_by_property=0)
     for g, r, kind in ((gk, kq, "K"), (gv, vq, "V")):
         n = g["codes"].shape[0]
-        bits = 4 if kind == "K" else 2
+        bits = g["bits"]
+        assert r["bits"] == bits
         gaxis = -1 if kind == "K" else -2      # axis inside a group
         # r, c
         for name, pre in (("r", np.clip(r["r_pre"], o.FP16_MIN_NORMAL, o.FP16_MAX)),

@@ -170,10 +170,11 @@ def _brute_codes(y, s, z, bits, axis):
     return best
 
 
-def test_rtn_is_nearest_grid_point_and_bounded():
+@pytest.mark.parametrize("kbits,vbits", sorted(set(o.PRESETS.values())))
+def test_rtn_is_nearest_grid_point_and_bounded(kbits, vbits):
     kx, vx, _ = _tile(7)
-    for x, kind, bits, axis in ((kx, "K", 4, -1), (vx, "V", 2, -2)):
-        qd = o.quantize_tensor(x, kind)
+    for x, kind, bits, axis in ((kx, "K", kbits, -1), (vx, "V", vbits, -2)):
+        qd = o.quantize_tensor(x, kind, bits=bits)
         codes, s, z, y = qd["codes"], qd["s"], qd["z"], qd["y"]
         assert codes.max() <= 2 ** bits - 1
         assert np.array_equal(codes, _brute_codes(y, s, z, bits, axis))
@@ -363,3 +364,113 @@ def test_append_builds_same_cache_as_prefill():
     assert np.array_equal(cache, ref)
     assert np.array_equal(ws[0, :, 0, :44], k[256:].transpose(1, 0, 2))
     assert np.array_equal(ws[0, :, 1, :44], v[256:].transpose(1, 0, 2))
+
+
+# ----------------------------------------------------------------------------------
+# Other bit presets (k4v4, k2v2): layouts, sizes, and what the bit width leaves alone
+# ----------------------------------------------------------------------------------
+def _random_quantized(rng, n, kbits, vbits):
+    kq = dict(bits=kbits, codes=rng.integers(0, 2 ** kbits, (n, 128, 128)).astype(np.uint8))
+    vq = dict(bits=vbits, codes=rng.integers(0, 2 ** vbits, (n, 128, 128)).astype(np.uint8))
+    for d in (kq, vq):
+        for name in ("r", "c", "s", "z"):
+            d[name] = o.fp16_rne(rng.standard_normal((n, 128)))
+    return kq, vq
+
+
+@pytest.mark.parametrize("preset", sorted(o.PRESETS))
+def test_preset_record_sizes_and_roundtrip(preset):
+    kbits, vbits = o.PRESETS[preset]
+    lay = o.LAYOUTS[preset]
+    # code areas hold 128 x 128 codes at their width, then 2 x 4 x 128 fp16 scales
+    assert lay.record_bytes == 128 * 128 * (kbits + vbits) // 8 + 2 * 4 * 128 * 2
+    assert abs(o.compression_ratio(preset) - 65536 / lay.record_bytes) < 1e-12
+    assert o.layout_of(lay.record_bytes) is lay
+    kq, vq = _random_quantized(np.random.default_rng(17), 2, kbits, vbits)
+    rec = o.pack_record(kq, vq, preset)
+    assert rec.shape == (2, lay.record_bytes)
+    k2, v2 = o.unpack_record(rec)
+    assert k2["bits"] == kbits and v2["bits"] == vbits
+    assert np.array_equal(k2["codes"], kq["codes"]) and np.array_equal(v2["codes"], vq["codes"])
+    for name in ("r", "c", "s", "z"):
+        assert np.array_equal(k2[name], kq[name]) and np.array_equal(v2[name], vq[name])
+
+
+def test_preset_compression_ratios():
+    """fp16 K and V of a tile (65536 bytes) over the record: 4-bit + 2-bit codes
+    (12 KiB) + 2 KiB of scales; 4 + 4 bits (16 KiB + 2 KiB); 2 + 2 bits (8 + 2 KiB)."""
+    assert o.compression_ratio("k4v2") == 65536 / 14336
+    assert o.compression_ratio("k4v4") == 65536 / 18432
+    assert o.compression_ratio("k2v2") == 65536 / 10240 == 6.4
+
+
+def _fragment_codes_k2(rec, t, c, ks):
+    """The four 2-bit key codes a decode thread with column c reads for token t in
+    k-step ks (channels 16 ks + 2c + {0, 1, 8, 9}): word ks >> 2 of its 8-byte group,
+    crumbs 2 (ks & 3) and 2 (ks & 3) + 1 of the low (even channel) and high (odd
+    channel) 16-bit halves."""
+    word = int.from_bytes(bytes(rec[t * 32 + c * 8 + (ks >> 2) * 4: t * 32 + c * 8 + (ks >> 2) * 4 + 4]), "little")
+    out = {}
+    for half8 in (0, 1):
+        for odd in (0, 1):
+            bit = 16 * odd + 2 * (2 * (ks & 3) + half8)
+            out[16 * ks + 2 * c + 8 * half8 + odd] = (word >> bit) & 3
+    return out
+
+
+def _fragment_codes_v4(area, i, c, ks):
+    """The four 4-bit value codes a decode thread with column c reads for channel i
+    in token k-step ks (tokens 16 ks + 2c + {0, 1, 8, 9}): word ks >> 1 of its
+    16-byte group, nibbles 2 (ks & 1) and 2 (ks & 1) + 1 of each 16-bit half."""
+    off = i * 64 + c * 16 + (ks >> 1) * 4
+    word = int.from_bytes(bytes(area[off:off + 4]), "little")
+    out = {}
+    for half8 in (0, 1):
+        for odd in (0, 1):
+            bit = 16 * odd + 4 * (2 * (ks & 1) + half8)
+            out[16 * ks + 2 * c + 8 * half8 + odd] = (word >> bit) & 15
+    return out
+
+
+def test_new_layouts_serve_the_mma_fragments():
+    """The 2-bit key and 4-bit value layouts are read by tensor-core fragments: a
+    thread with column c of an m16n8k16 operand needs rows 2c, 2c+1, 2c+8, 2c+9
+    of each 16-row k-step. Read the way the decode reads them, every (channel,
+    token) code of a packed record comes back exactly once."""
+    rng = np.random.default_rng(23)
+    kq, vq = _random_quantized(rng, 1, 2, 4)
+    lay_k = o.LAYOUTS["k2v2"]
+    rec_k = o.pack_record(kq, dict(vq, bits=2, codes=vq["codes"] & 3), "k2v2")[0]
+    seen = np.zeros((128, 128), int)
+    for t in range(128):
+        for c in range(4):
+            for ks in range(8):
+                for ch, val in _fragment_codes_k2(rec_k[lay_k.k_code_off:], t, c, ks).items():
+                    assert val == kq["codes"][0, ch, t]
+                    seen[ch, t] += 1
+    assert (seen == 1).all()
+    lay_v = o.LAYOUTS["k4v4"]
+    rec_v = o.pack_record(dict(kq, bits=4), vq, "k4v4")[0]
+    area = rec_v[lay_v.v_code_off:lay_v.v_code_off + lay_v.v_code_bytes]
+    seen[:] = 0
+    for i in range(128):
+        for c in range(4):
+            for ks in range(8):
+                for tok, val in _fragment_codes_v4(area, i, c, ks).items():
+                    assert val == vq["codes"][0, i, tok]
+                    seen[i, tok] += 1
+    assert (seen == 1).all()
+
+
+def test_bit_width_changes_only_the_step_and_zero():
+    """Stages 2-3 do not depend on the bit width: the same tile gives the same r and
+    c in every preset; only s, z and the codes change (s shrinks with more levels)."""
+    k, v, _ = synth.single_tile(5)
+    _, k42, v42 = o.quantize_tiles(k, v, preset="k4v2")
+    _, k44, v44 = o.quantize_tiles(k, v, preset="k4v4")
+    _, k22, v22 = o.quantize_tiles(k, v, preset="k2v2")
+    for a, b in ((k42, k44), (k42, k22), (v42, v44), (v42, v22)):
+        assert np.array_equal(a["r"], b["r"]) and np.array_equal(a["c"], b["c"])
+        assert np.array_equal(a["z"], b["z"])           # z is the group minimum in every preset
+    assert (v44["s"] < v42["s"]).all() and (k22["s"] > k42["s"]).all()
+    assert v44["codes"].max() == 15 and k22["codes"].max() == 3
