@@ -9,7 +9,7 @@
  * row-wise std normalisation in log space (Sinkhorn style), keeping the row scale
  * vector r and column scale vector c, and (4) quantized by asymmetric
  * round-to-nearest: keys at 4 bits with (scale, zero) per channel, values at 2
- * bits with (scale, zero) per token. The preset is kvarn_k4v2_g128 with block
+ * bits with (scale, zero) per token. The default preset is kvarn_k4v2_g128 with block
  * size fixed at 128 (one paged block = one tile) and float16 compute (README,
  * quick start and note). Decode attention reads the packed blocks through the
  * block table, re-applies the scales on read (stage 4), rotates q by the same H
@@ -29,8 +29,26 @@
  *   mask (all seq_len tokens are attended).
  *
  * ---------------------------------------------------------------------------
- * Packed record: 14336 bytes per (physical block, kv-head). The cache is
- * uint8 [num_blocks][num_kv_heads][14336], device memory owned by the caller.
+ * Presets. kvarn_meta's (k_bits, v_bits) picks one of: k4v2 (the README's
+ * kvarn_k4v2_g128, the default), k4v4 and k2v2 (the README reports 2-bit
+ * results too). A record holds the key codes, then the value codes, then the key
+ * and the value metadata (1024 bytes each); the layouts below are k4v2's, and
+ * the two others use:
+ *   2-bit K codes, token-major: token t owns bytes [32t, 32t+32) = four 8-byte
+ *     groups g = (i>>1)&3, each two words u = i>>6; channel i sits in crumb
+ *     p = 8(i&1) + 2((i>>4)&3) + ((i>>3)&1) (bits 2p..2p+1) of word u.
+ *   4-bit V codes, channel-major: the 4-bit K layout with channel and token
+ *     exchanged (channel i owns bytes [64i, 64i+64), groups g = (t>>1)&3, words
+ *     w = t>>5, nibble p = 4(t&1) + 2((t>>4)&1) + ((t>>3)&1)).
+ *   k4v4: K codes [0, 8192), V codes [8192, 16384), K meta [16384, 17408), V meta
+ *     [17408, 18432). k2v2: K codes [0, 4096), V codes [4096, 8192), K meta
+ *     [8192, 9216), V meta [9216, 10240).
+ * The decode kernel keeps 7 warps with two record stages each for k4v2 and k2v2,
+ * and 6 warps for k4v4 (its stages would not fit 7 warps' shared memory).
+ *
+ * Packed record (k4v2): 14336 bytes per (physical block, kv-head). The cache is
+ * uint8 [num_blocks][num_kv_heads][record bytes], device memory owned by the
+ * caller.
  *   [    0,  8192)  K codes, 4 bits, token-major: token t owns bytes
  *                   [64t, 64t+64) = four 16-byte groups g = (i>>1)&3, each four
  *                   little-endian 32-bit words w = i>>5; channel i sits in nibble
@@ -117,8 +135,8 @@ typedef struct {
   int32_t num_q_heads;        /* Hq, a multiple of Hkv with Hq/Hkv <= 8           */
   int32_t head_dim;           /* must be 128                                      */
   int32_t block_size;         /* must be 128                                      */
-  int32_t k_bits;             /* must be 4                                        */
-  int32_t v_bits;             /* must be 2                                        */
+  int32_t k_bits;             /* preset: 4 (k4v2, k4v4) or 2 (k2v2)               */
+  int32_t v_bits;             /* preset: 2 (k4v2, k2v2) or 4 (k4v4)               */
   int32_t n_iters;            /* normalisation iterations, 1..16 (preset 4)       */
   float eps;                  /* added to each variance, > 0 (preset 1e-6)        */
   int64_t num_blocks;         /* physical blocks in the cache                     */
@@ -126,11 +144,16 @@ typedef struct {
   int32_t reserved;           /* must be 0                                        */
 } kvarn_meta;
 
-/* Bytes of one (block, kv-head) record: 14336. */
+/* Bytes of one (block, kv-head) record of the default preset k4v2: 14336. */
 KVARN_API size_t kvarn_record_bytes(void);
 
-/* Bytes of the whole paged cache: num_blocks * num_kv_heads * 14336; 0 if meta is
- * invalid. */
+/* Bytes of one (block, kv-head) record of the meta's preset:
+ * 128 * 128 * (k_bits + v_bits) / 8 + 2048 (k4v2 14336, k4v4 18432, k2v2
+ * 10240); 0 if meta is invalid. */
+KVARN_API size_t kvarn_meta_record_bytes(const kvarn_meta* meta);
+
+/* Bytes of the whole paged cache: num_blocks * num_kv_heads *
+ * kvarn_meta_record_bytes(meta); 0 if meta is invalid. */
 KVARN_API size_t kvarn_cache_bytes(const kvarn_meta* meta);
 
 /* Bytes of a decode workspace for `max_seqs` sequences:

@@ -24,6 +24,7 @@ FLAG_BAD_SLOTS, FLAG_BAD_BLOCK, FLAG_BAD_LENGTH, FLAG_WAIT_TIMEOUT = 0x1, 0x2, 0
 # exported entry points and their C signatures (include/kvarn.h)
 _SIGS = {
     "kvarn_record_bytes": (ctypes.c_size_t, []),
+    "kvarn_meta_record_bytes": (ctypes.c_size_t, [ctypes.c_void_p]),
     "kvarn_cache_bytes": (ctypes.c_size_t, [ctypes.c_void_p]),
     "kvarn_workspace_bytes": (ctypes.c_size_t, [ctypes.c_void_p, ctypes.c_int32]),
     "kvarn_decode_scratch_bytes": (ctypes.c_size_t, [ctypes.c_void_p, ctypes.c_int32]),
@@ -66,10 +67,16 @@ class KvarnMeta(ctypes.Structure):
     ]
 
 
+# bit widths (keys, values) of the presets; k4v2 is kvarn_k4v2_g128
+PRESETS = {"k4v2": (4, 2), "k4v4": (4, 4), "k2v2": (2, 2)}
+
+
 def make_meta(num_kv_heads: int, num_q_heads: int, num_blocks: int, max_blocks_per_seq: int = 0,
-              n_iters: int = 4, eps: float = 1e-6) -> KvarnMeta:
-    """Preset kvarn_k4v2_g128: head_dim 128, block 128, 4-bit K, 2-bit V."""
-    return KvarnMeta(num_kv_heads, num_q_heads, HEAD_DIM, BLOCK_SIZE, 4, 2, n_iters, eps,
+              n_iters: int = 4, eps: float = 1e-6, preset: str = "k4v2") -> KvarnMeta:
+    """Head_dim 128, block 128; preset k4v2 (4-bit K, 2-bit V: kvarn_k4v2_g128),
+    k4v4 or k2v2."""
+    kb, vb = PRESETS[preset]
+    return KvarnMeta(num_kv_heads, num_q_heads, HEAD_DIM, BLOCK_SIZE, kb, vb, n_iters, eps,
                      num_blocks, max_blocks_per_seq, 0)
 
 
@@ -119,6 +126,11 @@ def record_bytes() -> int:
     return int(_lib.kvarn_record_bytes())
 
 
+def meta_record_bytes(meta: KvarnMeta) -> int:
+    """Bytes of one (block, kv-head) record for the meta's preset."""
+    return int(_lib.kvarn_meta_record_bytes(ctypes.byref(meta)))
+
+
 def cache_bytes(meta: KvarnMeta) -> int:
     return int(_lib.kvarn_cache_bytes(ctypes.byref(meta)))
 
@@ -133,7 +145,7 @@ def decode_scratch_bytes(meta: KvarnMeta, n_seqs: int) -> int:
 
 def kvarn_quantize_tiles(k, v, slot_mapping, cache, meta: KvarnMeta, stream=None):
     """k, v: fp16 [n_tokens, Hkv, 128]; slot_mapping: int64 [n_tokens];
-    cache: uint8 [num_blocks, Hkv, 14336]."""
+    cache: uint8 [num_blocks, Hkv, meta_record_bytes(meta)]."""
     import torch
     n = int(k.shape[0])
     _check(_lib.kvarn_quantize_tiles(_ptr(k, "k", torch.float16), _ptr(v, "v", torch.float16),

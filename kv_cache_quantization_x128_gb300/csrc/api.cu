@@ -32,8 +32,9 @@ kvarn_status check_meta(const kvarn_meta* m) {
   if (m->head_dim != KVARN_HEAD_DIM) return fail(KVARN_EUNSUPPORTED, "head_dim must be 128 (got %lld)", (long long)m->head_dim);
   if (m->block_size != KVARN_BLOCK_SIZE)
     return fail(KVARN_EUNSUPPORTED, "block_size must be 128 (got %lld)", (long long)m->block_size);
-  if (m->k_bits != 4 || m->v_bits != 2)
-    return fail(KVARN_EUNSUPPORTED, "only the k4v2 preset is supported (k_bits=%lld)", (long long)m->k_bits);
+  if (!((m->k_bits == 4 && (m->v_bits == 2 || m->v_bits == 4)) || (m->k_bits == 2 && m->v_bits == 2)))
+    return fail(KVARN_EUNSUPPORTED, "bit widths must be a preset: k4v2, k4v4 or k2v2 (got k%lldv%lld)",
+                (long long)m->k_bits, (long long)m->v_bits);
   if (m->num_kv_heads < 1) return fail(KVARN_EINVAL, "num_kv_heads must be >= 1 (got %lld)", (long long)m->num_kv_heads);
   if (m->num_q_heads < m->num_kv_heads || m->num_q_heads % m->num_kv_heads != 0)
     return fail(KVARN_EINVAL, "num_q_heads must be a positive multiple of num_kv_heads (got %lld)",
@@ -79,9 +80,14 @@ extern "C" {
 
 size_t kvarn_record_bytes(void) { return KVARN_RECORD_BYTES; }
 
+size_t kvarn_meta_record_bytes(const kvarn_meta* meta) {
+  if (check_meta(meta) != KVARN_OK) return 0;
+  return static_cast<size_t>(KVARN_HEAD_DIM) * KVARN_BLOCK_SIZE * (meta->k_bits + meta->v_bits) / 8 + 2048;
+}
+
 size_t kvarn_cache_bytes(const kvarn_meta* meta) {
   if (check_meta(meta) != KVARN_OK) return 0;
-  return static_cast<size_t>(meta->num_blocks) * meta->num_kv_heads * KVARN_RECORD_BYTES;
+  return static_cast<size_t>(meta->num_blocks) * meta->num_kv_heads * kvarn_meta_record_bytes(meta);
 }
 
 size_t kvarn_workspace_bytes(const kvarn_meta* meta, int32_t max_seqs) {
@@ -109,8 +115,8 @@ kvarn_status kvarn_quantize_tiles(const uint16_t* k, const uint16_t* v, const in
   unsigned* fl = nullptr;
   KV_TRY(flags_ptr(&fl));
   return cuda_status(kvarn::launch_quantize_prefill(k, v, slot_mapping, n_tokens, meta->num_kv_heads,
-                                                    meta->num_blocks, cache, meta->n_iters, meta->eps, fl,
-                                                    static_cast<cudaStream_t>(stream), 0),
+                                                    meta->num_blocks, cache, meta->k_bits, meta->v_bits,
+                                                    meta->n_iters, meta->eps, fl, static_cast<cudaStream_t>(stream), 0),
                      "kvarn_quantize_tiles");
 }
 
@@ -134,8 +140,8 @@ kvarn_status kvarn_append_decode(const uint16_t* k_new, const uint16_t* v_new, c
   KV_TRY(flags_ptr(&fl));
   return cuda_status(kvarn::launch_append(k_new, v_new, seq_lens, seq_lens_out, block_tables, n_seqs,
                                           meta->num_kv_heads, meta->max_blocks_per_seq, meta->num_blocks,
-                                          workspace, cache, meta->n_iters, meta->eps, fl,
-                                          static_cast<cudaStream_t>(stream)),
+                                          workspace, cache, meta->k_bits, meta->v_bits, meta->n_iters, meta->eps,
+                                          fl, static_cast<cudaStream_t>(stream)),
                      "kvarn_append_decode");
 }
 
@@ -166,7 +172,8 @@ kvarn_status kvarn_decode_attention(const uint16_t* q, const uint8_t* cache, con
   KV_TRY(flags_ptr(&fl));
   return cuda_status(kvarn::launch_decode(q, cache, workspace, block_tables, seq_lens, n_seqs, meta->num_kv_heads,
                                           meta->num_q_heads / meta->num_kv_heads, meta->max_blocks_per_seq,
-                                          meta->num_blocks, out, scratch, fl, static_cast<cudaStream_t>(stream)),
+                                          meta->num_blocks, meta->k_bits, meta->v_bits, out, scratch, fl,
+                                          static_cast<cudaStream_t>(stream)),
                      "kvarn_decode_attention");
 }
 

@@ -95,7 +95,8 @@ KVARN_API kvarn_status kvarn_decode_attention_static(const uint16_t* q, const ui
     return kvarn::set_error(KVARN_ECUDA, "kvarn_decode_attention_static: device flag word unavailable");
   const cudaError_t e = kvarn::launch_decode(q, cache, workspace, block_tables, seq_lens, n_seqs, meta->num_kv_heads,
                                              meta->num_q_heads / meta->num_kv_heads, meta->max_blocks_per_seq,
-                                             meta->num_blocks, out, scratch, flags, static_cast<cudaStream_t>(stream));
+                                             meta->num_blocks, 4, 2, out, scratch, flags,
+                                             static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return kvarn::set_error(KVARN_ECUDA, cudaGetErrorString(e));
   return KVARN_OK;
 }

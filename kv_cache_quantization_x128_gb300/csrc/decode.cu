@@ -29,12 +29,21 @@ namespace kvarn {
 namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr int kWarps = 7;                       // consumer warps per CTA
+constexpr int kMaxWarps = 7;                    // consumer warps per CTA (at most)
 constexpr int kStages = 2;                      // bulk-copy stages per warp
 constexpr int kMaxCtas = 1024;                  // upper bound used to size scratch
 constexpr int kPartStride = 132;                // floats per q-head: acc[128], max, sum, pad
 constexpr int kRecFloats = 8 * kPartStride;     // one partial record (8 q-head slots)
-constexpr int kSplitSmem = kWarps * kStages * kRec + kWarps * kStages * 8;
+
+// Split kernel shape for KB-bit keys and VB-bit values: 7 warps, or 6 when two
+// records per warp would not fit in shared memory (k4v4's 18432-byte records).
+template <int KB, int VB>
+struct SplitCfg {
+  using L = RecordLayout<KB, VB>;
+  static constexpr int kWarps = 7 * kStages * L::kBytes + 7 * kStages * 8 <= 232448 ? 7 : 6;
+  static constexpr int kSmem = kWarps * kStages * L::kBytes + kWarps * kStages * 8;
+  static_assert(kSmem <= 232448, "decode stages");
+};
 
 // fp32 pair -> (hi, lo) fp16 pairs with hi + lo ~ x to ~22 bits.
 __device__ __forceinline__ void split2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
@@ -114,6 +123,7 @@ struct DecodeArgs {
   int group;            // q-heads per kv-head (1..8)
   int max_blocks;
   int n_ctas;           // CTAs of the split kernel
+  int warps;            // warps per CTA of the split kernel
 };
 
 __device__ __forceinline__ int full_tiles(const DecodeArgs& a, int s) {
@@ -122,6 +132,7 @@ __device__ __forceinline__ int full_tiles(const DecodeArgs& a, int s) {
 }
 
 // Range [beg, end) of global tiles owned by warp `wg` of the split kernel.
+template <int kWarps>
 __device__ __forceinline__ void warp_range(int64_t total, int n_ctas, int64_t wg, int64_t& beg, int64_t& end) {
   const int64_t b = wg / kWarps, w = wg % kWarps;
   const int64_t c0 = b * total / n_ctas, c1 = (b + 1) * total / n_ctas;
@@ -192,6 +203,7 @@ __device__ __forceinline__ void advance(const DecodeArgs& a, Cursor& c) {
 
 // Lane 0: start the copy of the tile at cursor `c` into `stage`; a block index
 // outside [0, num_blocks) completes the barrier phase without data and returns false.
+template <int kRecBytes>
 __device__ __forceinline__ bool issue_tile(const DecodeArgs& a, const Cursor& c, uint8_t* stage, uint64_t* bar) {
   const int64_t blk = a.block_tables[static_cast<int64_t>(c.s) * a.max_blocks + c.ti];
   if (blk < 0 || blk >= a.num_blocks) {
@@ -199,8 +211,8 @@ __device__ __forceinline__ bool issue_tile(const DecodeArgs& a, const Cursor& c,
     asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
     return false;
   }
-  mbar_arrive_expect_tx(bar, kRec);
-  bulk_g2s(stage, a.cache + (blk * a.hkv + c.h) * static_cast<int64_t>(kRec), kRec, bar);
+  mbar_arrive_expect_tx(bar, kRecBytes);
+  bulk_g2s(stage, a.cache + (blk * a.hkv + c.h) * static_cast<int64_t>(kRecBytes), kRecBytes, bar);
   return true;
 }
 
@@ -255,10 +267,12 @@ __device__ __forceinline__ void load_q(const DecodeArgs& a, int s, int h, int g,
 }
 
 // One packed tile: update the running (max, sum, acc) of head g.
+template <int KB, int VB>
 __device__ __forceinline__ void attend_tile(const uint8_t* rec, const float (&qv)[8][4], int g, int c, float& m_run,
                                             float& l_run, float (&acc)[16][2]) {
-  const uint16_t* km = reinterpret_cast<const uint16_t*>(rec + kKMetaOff);
-  const uint16_t* vm = reinterpret_cast<const uint16_t*>(rec + kVMetaOff);
+  using L = RecordLayout<KB, VB>;
+  const uint16_t* km = reinterpret_cast<const uint16_t*>(rec + L::kKMetaOff);
+  const uint16_t* vm = reinterpret_cast<const uint16_t*>(rec + L::kVMetaOff);
 
   // q' fragments (hi rows g, lo rows g + 8) and beta
   uint32_t A[8][4];
@@ -282,25 +296,50 @@ __device__ __forceinline__ void attend_tile(const uint8_t* rec, const float (&qv
   float sc[16][2];
 #pragma unroll
   for (int ntg = 0; ntg < 4; ++ntg) {
-    uint32_t kw[4][4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const uint4 v = *reinterpret_cast<const uint4*>(rec + kKCodeOff + (8 * (4 * ntg + j) + g) * 64 + c * 16);
-      kw[j][0] = v.x; kw[j][1] = v.y; kw[j][2] = v.z; kw[j][3] = v.w;
-    }
     float d[4][4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) d[j][0] = d[j][1] = d[j][2] = d[j][3] = 0.f;
-#pragma unroll
-    for (int m = 0; m < 4; ++m)
+    if (KB == 4) {
+      // token row of 64 bytes, this thread's 16: word m holds k-steps 2m (low byte
+      // of each half) and 2m + 1 (high byte)
+      uint32_t kw[4][4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const uint32_t w0 = kw[j][m], w8 = kw[j][m] >> 8;
-        mma16816(d[j], A[2 * m], hfma2_u(lop_magic<0x000F000Fu>(w0), kH_One, kH_M1024),
-                 hfma2_u(lop_magic<0x00F000F0u>(w0), kH_Sixteenth, kH_M64));
-        mma16816(d[j], A[2 * m + 1], hfma2_u(lop_magic<0x000F000Fu>(w8), kH_One, kH_M1024),
-                 hfma2_u(lop_magic<0x00F000F0u>(w8), kH_Sixteenth, kH_M64));
+        const uint4 v = *reinterpret_cast<const uint4*>(rec + L::kKCodeOff + (8 * (4 * ntg + j) + g) * 64 + c * 16);
+        kw[j][0] = v.x; kw[j][1] = v.y; kw[j][2] = v.z; kw[j][3] = v.w;
       }
+#pragma unroll
+      for (int m = 0; m < 4; ++m)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t w0 = kw[j][m], w8 = kw[j][m] >> 8;
+          mma16816(d[j], A[2 * m], hfma2_u(lop_magic<0x000F000Fu>(w0), kH_One, kH_M1024),
+                   hfma2_u(lop_magic<0x00F000F0u>(w0), kH_Sixteenth, kH_M64));
+          mma16816(d[j], A[2 * m + 1], hfma2_u(lop_magic<0x000F000Fu>(w8), kH_One, kH_M1024),
+                   hfma2_u(lop_magic<0x00F000F0u>(w8), kH_Sixteenth, kH_M64));
+        }
+    } else {
+      // token row of 32 bytes, this thread's 8: word u holds k-steps 4u + 2sg + {0, 1}
+      // in byte sg of each half (crumbs 0-1 and 2-3 of the byte)
+      uint32_t kw[4][2];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint2 v = *reinterpret_cast<const uint2*>(rec + L::kKCodeOff + (8 * (4 * ntg + j) + g) * 32 + c * 8);
+        kw[j][0] = v.x; kw[j][1] = v.y;
+      }
+#pragma unroll
+      for (int u = 0; u < 2; ++u)
+#pragma unroll
+        for (int sg = 0; sg < 2; ++sg)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint32_t w = sg ? (kw[j][u] >> 8) : kw[j][u];
+            mma16816(d[j], A[4 * u + 2 * sg], hfma2_u(lop_magic<0x00030003u>(w), kH_One, kH_M1024),
+                     hfma2_u(lop_magic<0x000C000Cu>(w), kH_Quarter, kH_M256));
+            mma16816(d[j], A[4 * u + 2 * sg + 1], hfma2_u(lop_magic<0x00300030u>(w), kH_Sixteenth, kH_M64),
+                     hfma2_u(lop_magic<0x00C000C0u>(w), kH_64th, kH_M16));
+          }
+    }
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int nt = 4 * ntg + j;
@@ -350,39 +389,74 @@ __device__ __forceinline__ void attend_tile(const uint8_t* rec, const float (&qv
   }
   gamma = quad_sum(gamma);
 
-  // PV: channel n-tile nt2 = 2np + which; cell (g, c) of panel np serves both `which`;
-  // two panels at a time -> four independent chains
-#pragma unroll
-  for (int npg = 0; npg < 4; ++npg) {
-    uint32_t vw[2][4];
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const uint4 v = *reinterpret_cast<const uint4*>(rec + kVCodeOff + (2 * npg + i) * 512 + (g * 4 + c) * 16);
-      vw[i][0] = v.x; vw[i][1] = v.y; vw[i][2] = v.z; vw[i][3] = v.w;   // [which*2 + u]
+  if (VB == 2) {
+    // PV with 2-bit values: channel n-tile nt2 = 2np + which; cell (g, c) of panel np serves both `which`;
+    // two panels at a time -> four independent chains
+  #pragma unroll
+    for (int npg = 0; npg < 4; ++npg) {
+      uint32_t vw[2][4];
+  #pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const uint4 v = *reinterpret_cast<const uint4*>(rec + L::kVCodeOff + (2 * npg + i) * 512 + (g * 4 + c) * 16);
+        vw[i][0] = v.x; vw[i][1] = v.y; vw[i][2] = v.z; vw[i][3] = v.w;   // [which*2 + u]
+      }
+      float d[4][4];
+  #pragma unroll
+      for (int j = 0; j < 4; ++j) d[j][0] = d[j][1] = d[j][2] = d[j][3] = 0.f;
+  #pragma unroll
+      for (int u = 0; u < 2; ++u)
+  #pragma unroll
+        for (int sg = 0; sg < 2; ++sg)
+  #pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int i = j >> 1, which = j & 1;
+            const uint32_t w = sg ? (vw[i][which * 2 + u] >> 8) : vw[i][which * 2 + u];
+            // crumb q = 2*(ks&1) + type at shift sg; ks = 4u + 2sg + (q >> 1)
+            mma16816(d[j], A[4 * u + 2 * sg], hfma2_u(lop_magic<0x00030003u>(w), kH_One, kH_M1024),
+                     hfma2_u(lop_magic<0x000C000Cu>(w), kH_Quarter, kH_M256));
+            mma16816(d[j], A[4 * u + 2 * sg + 1], hfma2_u(lop_magic<0x00300030u>(w), kH_Sixteenth, kH_M64),
+                     hfma2_u(lop_magic<0x00C000C0u>(w), kH_64th, kH_M16));
+          }
+  #pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int nt2 = 2 * (2 * npg + (j >> 1)) + (j & 1);
+        const float2 rv = h2pair(vm + 8 * nt2 + 2 * c);
+        acc[nt2][0] = fmaf(rv.x, (d[j][0] + d[j][2]) + gamma, acc[nt2][0]);
+        acc[nt2][1] = fmaf(rv.y, (d[j][1] + d[j][3]) + gamma, acc[nt2][1]);
+      }
     }
-    float d[4][4];
+  } else {
+    // PV with 4-bit values: channel row of 64 bytes, this thread's 16; word m holds
+    // token k-steps 2m and 2m + 1 (low and high byte of each half); four channel
+    // n-tiles at a time -> four independent chains
 #pragma unroll
-    for (int j = 0; j < 4; ++j) d[j][0] = d[j][1] = d[j][2] = d[j][3] = 0.f;
+    for (int npg = 0; npg < 4; ++npg) {
+      uint32_t vw[4][4];
 #pragma unroll
-    for (int u = 0; u < 2; ++u)
+      for (int j = 0; j < 4; ++j) {
+        const uint4 v = *reinterpret_cast<const uint4*>(rec + L::kVCodeOff + (8 * (4 * npg + j) + g) * 64 + c * 16);
+        vw[j][0] = v.x; vw[j][1] = v.y; vw[j][2] = v.z; vw[j][3] = v.w;
+      }
+      float d[4][4];
 #pragma unroll
-      for (int sg = 0; sg < 2; ++sg)
+      for (int j = 0; j < 4; ++j) d[j][0] = d[j][1] = d[j][2] = d[j][3] = 0.f;
+#pragma unroll
+      for (int m = 0; m < 4; ++m)
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          const int i = j >> 1, which = j & 1;
-          const uint32_t w = sg ? (vw[i][which * 2 + u] >> 8) : vw[i][which * 2 + u];
-          // crumb q = 2*(ks&1) + type at shift sg; ks = 4u + 2sg + (q >> 1)
-          mma16816(d[j], A[4 * u + 2 * sg], hfma2_u(lop_magic<0x00030003u>(w), kH_One, kH_M1024),
-                   hfma2_u(lop_magic<0x000C000Cu>(w), kH_Quarter, kH_M256));
-          mma16816(d[j], A[4 * u + 2 * sg + 1], hfma2_u(lop_magic<0x00300030u>(w), kH_Sixteenth, kH_M64),
-                   hfma2_u(lop_magic<0x00C000C0u>(w), kH_64th, kH_M16));
+          const uint32_t w0 = vw[j][m], w8 = vw[j][m] >> 8;
+          mma16816(d[j], A[2 * m], hfma2_u(lop_magic<0x000F000Fu>(w0), kH_One, kH_M1024),
+                   hfma2_u(lop_magic<0x00F000F0u>(w0), kH_Sixteenth, kH_M64));
+          mma16816(d[j], A[2 * m + 1], hfma2_u(lop_magic<0x000F000Fu>(w8), kH_One, kH_M1024),
+                   hfma2_u(lop_magic<0x00F000F0u>(w8), kH_Sixteenth, kH_M64));
         }
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int nt2 = 2 * (2 * npg + (j >> 1)) + (j & 1);
-      const float2 rv = h2pair(vm + 8 * nt2 + 2 * c);
-      acc[nt2][0] = fmaf(rv.x, (d[j][0] + d[j][2]) + gamma, acc[nt2][0]);
-      acc[nt2][1] = fmaf(rv.y, (d[j][1] + d[j][3]) + gamma, acc[nt2][1]);
+      for (int j = 0; j < 4; ++j) {
+        const int nt2 = 4 * npg + j;
+        const float2 rv = h2pair(vm + 8 * nt2 + 2 * c);
+        acc[nt2][0] = fmaf(rv.x, (d[j][0] + d[j][2]) + gamma, acc[nt2][0]);
+        acc[nt2][1] = fmaf(rv.y, (d[j][1] + d[j][3]) + gamma, acc[nt2][1]);
+      }
     }
   }
 }
@@ -398,22 +472,25 @@ __device__ __forceinline__ void flush_record(const DecodeArgs& a, int64_t rec_id
   if (c == 0) *reinterpret_cast<float2*>(out + 128) = make_float2(m_run, l);
 }
 
-__global__ void __launch_bounds__(kWarps * 32, 1) decode_split_kernel(DecodeArgs a) {
+template <int KB, int VB>
+__global__ void __launch_bounds__(SplitCfg<KB, VB>::kWarps * 32, 1) decode_split_kernel(DecodeArgs a) {
+  constexpr int kWarps = SplitCfg<KB, VB>::kWarps;
+  constexpr int kRecBytes = RecordLayout<KB, VB>::kBytes;
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
   const int64_t wg = static_cast<int64_t>(blockIdx.x) * kWarps + warp;
   const int64_t total = a.prefix[a.n_seqs] * a.hkv;
   int64_t gb, ge;
-  warp_range(total, a.n_ctas, wg, gb, ge);
+  warp_range<kWarps>(total, a.n_ctas, wg, gb, ge);
   if (lane == 0) {
     a.ranges[2 * wg] = gb;
     a.ranges[2 * wg + 1] = ge;
   }
   if (gb >= ge) return;   // warps are independent: no CTA-wide barrier below
 
-  uint8_t* stages = smem + warp * kStages * kRec;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kWarps * kStages * kRec) + warp * kStages;
+  uint8_t* stages = smem + warp * kStages * kRecBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kWarps * kStages * kRecBytes) + warp * kStages;
   if (lane == 0) {
     for (int k = 0; k < kStages; ++k) mbar_init(&bars[k], 1);
     fence_mbar_init();
@@ -427,7 +504,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) decode_split_kernel(DecodeArgs
   for (int k = 0; k < kStages && gb + k < ge; ++k) {
     if (k > 0) advance(a, lc);
     bool ok = false;
-    if (lane == 0) ok = issue_tile(a, lc, stages + k * kRec, &bars[k]);
+    if (lane == 0) ok = issue_tile<kRecBytes>(a, lc, stages + k * kRecBytes, &bars[k]);
     if (__shfl_sync(0xffffffffu, ok, 0)) valid |= 1u << k;
   }
 
@@ -451,12 +528,12 @@ __global__ void __launch_bounds__(kWarps * 32, 1) decode_split_kernel(DecodeArgs
     const bool ok = __all_sync(0xffffffffu, mbar_wait(&bars[stg], (phase >> stg) & 1u, a.flags));
     phase ^= 1u << stg;
     if (!ok) break;   // a copy never arrived (flag raised): stop this warp
-    if ((valid >> stg) & 1u) attend_tile(stages + stg * kRec, qv, g, c, m_run, l_run, acc);
+    if ((valid >> stg) & 1u) attend_tile<KB, VB>(stages + stg * kRecBytes, qv, g, c, m_run, l_run, acc);
     __syncwarp();
     if (gb + k + kStages < ge) {     // refill this stage with the tile kStages ahead
       advance(a, lc);
       bool issued = false;
-      if (lane == 0) issued = issue_tile(a, lc, stages + stg * kRec, &bars[stg]);
+      if (lane == 0) issued = issue_tile<kRecBytes>(a, lc, stages + stg * kRecBytes, &bars[stg]);
       if (__shfl_sync(0xffffffffu, issued, 0)) valid |= 1u << stg; else valid &= ~(1u << stg);
     }
     advance(a, cc);
@@ -484,7 +561,7 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(DecodeArgs a, const u
   }
   const int64_t qrow = (static_cast<int64_t>(s) * a.hkv * a.group + static_cast<int64_t>(h) * a.group + gg) * kD;
   const int64_t u = static_cast<int64_t>(s) * a.hkv + h;
-  const int64_t n_warps = static_cast<int64_t>(a.n_ctas) * kWarps;
+  const int64_t n_warps = static_cast<int64_t>(a.n_ctas) * a.warps;
 
   // warps whose ranges cover this unit's tiles [t0, t1) (ranges are contiguous and
   // ordered; empty ranges are skipped)
@@ -568,18 +645,18 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(DecodeArgs a, const u
 }
 
 size_t prefix_bytes(int n_seqs) { return ((static_cast<size_t>(n_seqs) + 1) * sizeof(int64_t) + 255) & ~size_t(255); }
-constexpr size_t kRangeBytes = static_cast<size_t>(kMaxCtas) * kWarps * 2 * sizeof(int64_t);
+constexpr size_t kRangeBytes = static_cast<size_t>(kMaxCtas) * kMaxWarps * 2 * sizeof(int64_t);
 
 }  // namespace
 
 size_t decode_part_bytes(int n_seqs, int hkv, int max_blocks) {
   (void)max_blocks;
-  const size_t records = static_cast<size_t>(kMaxCtas) * kWarps + static_cast<size_t>(n_seqs) * hkv;
+  const size_t records = static_cast<size_t>(kMaxCtas) * kMaxWarps + static_cast<size_t>(n_seqs) * hkv;
   return prefix_bytes(n_seqs) + kRangeBytes + records * kRecFloats * sizeof(float);
 }
 
 size_t decode_scratch_bytes_for_ctas(int n_seqs, int hkv, int n_ctas) {
-  const size_t records = static_cast<size_t>(n_ctas) * kWarps + static_cast<size_t>(n_seqs) * hkv;
+  const size_t records = static_cast<size_t>(n_ctas) * kMaxWarps + static_cast<size_t>(n_seqs) * hkv;
   return prefix_bytes(n_seqs) + kRangeBytes + records * kRecFloats * sizeof(float);
 }
 
@@ -590,9 +667,18 @@ int decode_num_ctas() {
   return sms > 0 ? (sms < kMaxCtas ? sms : kMaxCtas) : 1;
 }
 
+template <int KB, int VB>
+cudaError_t launch_split(const DecodeArgs& a, cudaStream_t stream) {
+  static std::atomic<unsigned long long> smem_set{0};
+  cudaError_t err = set_smem_once(decode_split_kernel<KB, VB>, SplitCfg<KB, VB>::kSmem, smem_set);
+  if (err != cudaSuccess) return err;
+  decode_split_kernel<KB, VB><<<a.n_ctas, SplitCfg<KB, VB>::kWarps * 32, SplitCfg<KB, VB>::kSmem, stream>>>(a);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_decode(const uint16_t* q, const uint8_t* cache, const uint16_t* ws, const int32_t* block_tables,
                           const int32_t* seq_lens, int n_seqs, int hkv, int group, int max_blocks, int64_t num_blocks,
-                          uint16_t* out, void* scratch, unsigned* flags, cudaStream_t stream) {
+                          int k_bits, int v_bits, uint16_t* out, void* scratch, unsigned* flags, cudaStream_t stream) {
   if (n_seqs <= 0) return cudaSuccess;
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
@@ -612,15 +698,15 @@ cudaError_t launch_decode(const uint16_t* q, const uint8_t* cache, const uint16_
   a.group = group;
   a.max_blocks = max_blocks;
   a.n_ctas = sms > 0 ? (sms < kMaxCtas ? sms : kMaxCtas) : 1;
+  a.warps = k_bits == 4 && v_bits == 4 ? SplitCfg<4, 4>::kWarps
+            : k_bits == 2 ? SplitCfg<2, 2>::kWarps : SplitCfg<4, 2>::kWarps;
+  if (!((k_bits == 4 && (v_bits == 2 || v_bits == 4)) || (k_bits == 2 && v_bits == 2))) return cudaErrorInvalidValue;
   decode_scan_kernel<<<1, 1024, 0, stream>>>(a);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   if (max_blocks > 0) {
-    static std::atomic<unsigned long long> smem_set{0};
-    err = set_smem_once(decode_split_kernel, kSplitSmem, smem_set);
-    if (err != cudaSuccess) return err;
-    decode_split_kernel<<<a.n_ctas, kWarps * 32, kSplitSmem, stream>>>(a);
-    err = cudaGetLastError();
+    err = k_bits == 2 ? launch_split<2, 2>(a, stream)
+          : v_bits == 4 ? launch_split<4, 4>(a, stream) : launch_split<4, 2>(a, stream);
     if (err != cudaSuccess) return err;
   }
   dim3 mgrid(hkv, n_seqs);

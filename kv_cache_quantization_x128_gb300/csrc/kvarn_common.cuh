@@ -18,6 +18,21 @@ constexpr float kFp16MinNormal = 6.103515625e-05f;   // 2^-14
 constexpr float kFp16Max = 65504.0f;
 constexpr float kInvSqrt128 = 0.088388347648318440f; // 2^-3.5
 
+// Record of one (block, kv-head) for KB-bit keys and VB-bit values: key codes,
+// value codes, key metadata (fp16 r, c, s, z x 128), value metadata.
+template <int KB, int VB>
+struct RecordLayout {
+  static constexpr int kKBits = KB, kVBits = VB;
+  static constexpr int kKCodeBytes = kD * kB * KB / 8;
+  static constexpr int kVCodeBytes = kD * kB * VB / 8;
+  static constexpr int kKCodeOff = 0;
+  static constexpr int kVCodeOff = kKCodeBytes;
+  static constexpr int kKMetaOff = kKCodeBytes + kVCodeBytes;
+  static constexpr int kVMetaOff = kKMetaOff + 1024;
+  static constexpr int kBytes = kVMetaOff + 1024;
+};
+static_assert(RecordLayout<4, 2>::kBytes == kRec && RecordLayout<4, 2>::kVMetaOff == kVMetaOff, "k4v2 record");
+
 // Kernels report data errors by OR-ing KVARN_FLAG_* bits into a device flag word
 // whose address the host passes in.
 __device__ __forceinline__ void raise_flag(unsigned int* flags, unsigned int bit) { atomicOr(flags, bit); }

@@ -37,16 +37,15 @@ namespace {
 constexpr int kGroupThreads = 256;
 constexpr int kThreads = 2 * kGroupThreads;
 constexpr int kTileOp = kB * kD * 2;              // 32768 B: one fp16 128x128 operand
-constexpr int kStageK = 8192 + 1024;              // K codes + K metadata
-constexpr int kStageV = 4096 + 1024;              // V codes + V metadata
+constexpr int kStage = 8192 + 1024;               // codes (at most 4-bit) + metadata of one tensor
 constexpr int kVec = 136;                         // parity-split vector (even at 0, odd at 68)
 constexpr int kNumVec = 8;                        // a, b, g (2^-3.5/r), hc (1/c), w, c0, mc, mr
 
 constexpr int kOffH = 0;
 constexpr int kOffIn = kOffH + kTileOp;                        // [group][buf] operands
 constexpr int kOffStageK = kOffIn + 4 * kTileOp;               // [buf]
-constexpr int kOffStageV = kOffStageK + 2 * kStageK;           // [buf]
-constexpr int kOffVec = kOffStageV + 2 * kStageV;              // [group][vector][kVec] fp32
+constexpr int kOffStageV = kOffStageK + 2 * kStage;            // [buf]
+constexpr int kOffVec = kOffStageV + 2 * kStage;               // [group][vector][kVec] fp32
 constexpr int kOffBar = kOffVec + 2 * kNumVec * kVec * 4;      // mma barriers [group], load barriers [group][buf]
 constexpr int kOffTmem = kOffBar + 48;
 constexpr int kSmemBytes = kOffTmem + 16;
@@ -278,7 +277,7 @@ __device__ __forceinline__ float div_sqrt(float v, float u) {
 // writes the group's stage (codes + metadata). `tile` is the item's fp16 operand
 // (canonical layout), `line`/`p` locate the thread's half line, `ta1`/`ta2` are
 // its TMEM addresses of D1 and D2.
-template <int kKind>
+template <int kKind, int kBits>
 __device__ __forceinline__ bool quantize_group(float* vec, uint8_t* stage, const uint8_t* tile, uint32_t ta1,
                                                uint32_t ta2, int line, int p, int n_iters, float eps, int bar_id,
                                                bool ok) {
@@ -288,7 +287,7 @@ __device__ __forceinline__ bool quantize_group(float* vec, uint8_t* stage, const
   float* vh = vec + kVHc * kVec;
   float* vw = vec + kVW * kVec;
   float* vc0 = vec + kVC0 * kVec;
-  uint16_t* meta = reinterpret_cast<uint16_t*>(stage + (kKind == 0 ? 8192 : 4096));
+  uint16_t* meta = reinterpret_cast<uint16_t*>(stage + kD * kB * kBits / 8);   // after the codes
   const int pl = ps(line);
 
   if (p == 0) {
@@ -344,7 +343,7 @@ __device__ __forceinline__ bool quantize_group(float* vec, uint8_t* stage, const
   }
   named_bar(bar_id, kGroupThreads);
 
-  constexpr float kLevels = kKind == 0 ? 15.0f : 3.0f;
+  constexpr float kLevels = static_cast<float>((1 << kBits) - 1);
   // group extremes of y = (x * hc_j) * g_i: keys per channel (D1 rows), values per
   // token (D2 rows); two halves of 64 columns (registers k = 32 hh + kl)
   {
@@ -385,7 +384,8 @@ __device__ __forceinline__ bool quantize_group(float* vec, uint8_t* stage, const
 
   // codes: keys token-major (D2 rows: token = line, channels e = p + 2k), values
   // channel-major (D1 rows: channel = line, tokens e = p + 2k); half hh holds
-  // k = 32 hh + kl, i.e. key words w = 2hh, 2hh + 1 and value word u = hh
+  // k = 32 hh + kl. 4-bit codes (keys or values) fill line rows of 64 bytes, words
+  // w = 2hh, 2hh + 1 of each 16-byte group; 2-bit codes fill word u = hh
   const float own = kKind == 0 ? vh[pl] : vg[pl];
   const float2 own2 = make_float2(own, own);
 #pragma unroll 1
@@ -414,18 +414,18 @@ __device__ __forceinline__ bool quantize_group(float* vec, uint8_t* stage, const
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int kl = 4 * q + u;
-        if (kKind == 0) {
-          // channel e = 32w + 16a + 8b + 2g4 + p -> k = 16w + 8a + 4b + g4, nibble 4p + 2a + b of word w
+        if (kBits == 4) {
+          // element e = 32w + 16a + 8b + 2g4 + p -> k = 16w + 8a + 4b + g4, nibble 4p + 2a + b of word w
           const int wl = kl >> 4, a = (kl >> 3) & 1, b = (kl >> 2) & 1, g4 = kl & 3;
           part[wl][g4] += bits[u] << (4 * (2 * a + b) + 16 * p);
         } else {
-          // token e = 64u + 16k2 + 8b + 2g4 + p -> k = 32u + 8k2 + 4b + g4, crumb 8p + 2k2 + b of word u
+          // element e = 64u + 16k2 + 8b + 2g4 + p -> k = 32u + 8k2 + 4b + g4, crumb 8p + 2k2 + b of word u
           const int k2 = (kl >> 3) & 3, b = (kl >> 2) & 1, g4 = kl & 3;
           part[0][g4] += bits[u] << (2 * (2 * k2 + b) + 16 * p);
         }
       }
     }
-    if (kKind == 0) {
+    if (kBits == 4) {
       // each word got 4 nibbles (a, b) from this thread: remove their 0x4B000000 terms
       const uint32_t bias = 0x4B000000u * ((1u << (16 * p)) * (1u + (1u << 4) + (1u << 8) + (1u << 12)));
       uint8_t* row = stage + line * 64;
@@ -443,12 +443,15 @@ __device__ __forceinline__ bool quantize_group(float* vec, uint8_t* stage, const
       for (int j = 0; j < 8; ++j) geo += 1u << (2 * j);
       const uint32_t bias = 0x4B000000u * ((1u << (16 * p)) * geo);
       const int i = line;
-      uint8_t* panel = stage + (i >> 4) * 512 + ((i >> 3) & 1) * 8;
+      // keys: token row of 32 bytes, 8-byte group g4, word hh; values: 512-byte
+      // panel of 16 channels, 16-byte cell of the channel pair, word hh
+      uint8_t* base = kKind == 0 ? stage + i * 32 + hh * 4 : stage + (i >> 4) * 512 + ((i >> 3) & 1) * 8 + hh * 4;
 #pragma unroll
       for (int g4 = 0; g4 < 4; ++g4) {
         const uint32_t m = part[0][g4] - bias;
         const uint32_t f = m | __shfl_xor_sync(0xffffffffu, m, 2);
-        if (p == hh) *reinterpret_cast<uint32_t*>(panel + ((i & 7) * 4 + g4) * 16 + hh * 4) = f;
+        const int off = kKind == 0 ? g4 * 8 : ((i & 7) * 4 + g4) * 16;
+        if (p == hh) *reinterpret_cast<uint32_t*>(base + off) = f;
       }
     }
   }
@@ -457,7 +460,7 @@ __device__ __forceinline__ bool quantize_group(float* vec, uint8_t* stage, const
 
 // 104 registers a thread (the 512 threads could hold 128): measured faster on the
 // prefill workload than 88, 96 or 128.
-template <class Src>
+template <class Src, int KB, int VB>
 __global__ void __maxnreg__(104)
     quantize_kernel(const __grid_constant__ Src src, uint8_t* __restrict__ cache, int n_iters, float eps,
                     unsigned* flags) {
@@ -543,7 +546,7 @@ __global__ void __maxnreg__(104)
       }
     }
     if (dst >= 0) {
-      uint8_t* stage = smem + (grp == 0 ? kOffStageK + buf * kStageK : kOffStageV + buf * kStageV);
+      uint8_t* stage = smem + (grp == 0 ? kOffStageK : kOffStageV) + buf * kStage;
       if (gt == 0) {
         if (ok) {
           const uint32_t sx = smem_u32(tiles + buf * kTileOp);
@@ -569,9 +572,9 @@ __global__ void __maxnreg__(104)
       tc_fence_after();
       const uint8_t* tile = tiles + buf * kTileOp;
       if (grp == 0)
-        ok = quantize_group<0>(vec, stage, tile, ta1, ta2, line, p, n_iters, eps, bar_id, ok);
+        ok = quantize_group<0, KB>(vec, stage, tile, ta1, ta2, line, p, n_iters, eps, bar_id, ok);
       else
-        ok = quantize_group<1>(vec, stage, tile, ta1, ta2, line, p, n_iters, eps, bar_id, ok);
+        ok = quantize_group<1, VB>(vec, stage, tile, ta1, ta2, line, p, n_iters, eps, bar_id, ok);
       if (!ok) break;                     // a copy or the tensor core never signalled (flag raised)
       fence_proxy_async_smem();
       tc_fence_before();
@@ -580,14 +583,15 @@ __global__ void __maxnreg__(104)
     const bool next_ok = named_bar_and(bar_id, kGroupThreads, !has_next || src.check_ok(check_next, gt));
     tc_fence_after();
     if (dst >= 0 && gt == 0) {
-      uint8_t* stage = smem + (grp == 0 ? kOffStageK + buf * kStageK : kOffStageV + buf * kStageV);
-      uint8_t* rec = cache + dst * static_cast<int64_t>(kRec);
+      using L = RecordLayout<KB, VB>;
+      uint8_t* stage = smem + (grp == 0 ? kOffStageK : kOffStageV) + buf * kStage;
+      uint8_t* rec = cache + dst * static_cast<int64_t>(L::kBytes);
       if (grp == 0) {
-        bulk_s2g(rec + kKCodeOff, stage, 8192);
-        bulk_s2g(rec + kKMetaOff, stage + 8192, 1024);
+        bulk_s2g(rec + L::kKCodeOff, stage, L::kKCodeBytes);
+        bulk_s2g(rec + L::kKMetaOff, stage + L::kKCodeBytes, 1024);
       } else {
-        bulk_s2g(rec + kVCodeOff, stage, 4096);
-        bulk_s2g(rec + kVMetaOff, stage + 4096, 1024);
+        bulk_s2g(rec + L::kVCodeOff, stage, L::kVCodeBytes);
+        bulk_s2g(rec + L::kVMetaOff, stage + L::kVCodeBytes, 1024);
       }
       bulk_commit();
     }
@@ -620,19 +624,30 @@ int sm_count() {
   return n > 0 ? n : 1;
 }
 
-template <class Src>
-cudaError_t launch_quantize(const Src& src, uint8_t* cache, int n_iters, float eps, unsigned* flags,
+template <class Src, int KB, int VB>
+cudaError_t launch_quantize_bits(const Src& src, uint8_t* cache, int n_iters, float eps, unsigned* flags,
                             cudaStream_t stream, int max_ctas) {
   if (src.n_items <= 0) return cudaSuccess;
   if (src.n_items > INT32_MAX) return cudaErrorInvalidValue;
   static std::atomic<unsigned long long> smem_set{0};
-  cudaError_t err = set_smem_once(quantize_kernel<Src>, kSmemBytes, smem_set);
+  cudaError_t err = set_smem_once(quantize_kernel<Src, KB, VB>, kSmemBytes, smem_set);
   if (err != cudaSuccess) return err;
   int64_t grid = sm_count();
   if (max_ctas > 0 && grid > max_ctas) grid = max_ctas;
   if (grid > src.n_items) grid = src.n_items;
-  quantize_kernel<Src><<<static_cast<unsigned>(grid), kThreads, kSmemBytes, stream>>>(src, cache, n_iters, eps, flags);
+  quantize_kernel<Src, KB, VB><<<static_cast<unsigned>(grid), kThreads, kSmemBytes, stream>>>(src, cache, n_iters, eps,
+                                                                                             flags);
   return cudaGetLastError();
+}
+
+// The kernel instance of a preset (k4v2, k4v4, k2v2).
+template <class Src>
+cudaError_t launch_quantize(const Src& src, uint8_t* cache, int k_bits, int v_bits, int n_iters, float eps,
+                            unsigned* flags, cudaStream_t stream, int max_ctas) {
+  if (k_bits == 4 && v_bits == 2) return launch_quantize_bits<Src, 4, 2>(src, cache, n_iters, eps, flags, stream, max_ctas);
+  if (k_bits == 4 && v_bits == 4) return launch_quantize_bits<Src, 4, 4>(src, cache, n_iters, eps, flags, stream, max_ctas);
+  if (k_bits == 2 && v_bits == 2) return launch_quantize_bits<Src, 2, 2>(src, cache, n_iters, eps, flags, stream, max_ctas);
+  return cudaErrorInvalidValue;
 }
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -672,8 +687,8 @@ cudaError_t tile_map(CUtensorMap* m, const void* base, uint64_t row_elems, uint6
 }  // namespace
 
 cudaError_t launch_quantize_prefill(const uint16_t* k, const uint16_t* v, const int64_t* slot, int64_t n_tokens,
-                                    int hkv, int64_t num_blocks, uint8_t* cache, int n_iters, float eps,
-                                    unsigned* flags, cudaStream_t stream, int max_ctas) {
+                                    int hkv, int64_t num_blocks, uint8_t* cache, int k_bits, int v_bits, int n_iters,
+                                    float eps, unsigned* flags, cudaStream_t stream, int max_ctas) {
   PrefillSource src{};
   cudaError_t err = tile_map(&src.map[0], k, static_cast<uint64_t>(hkv) * kD, static_cast<uint64_t>(n_tokens));
   if (err == cudaSuccess)
@@ -683,13 +698,13 @@ cudaError_t launch_quantize_prefill(const uint16_t* k, const uint16_t* v, const 
   src.n_items = (n_tokens / kB) * hkv;
   src.hkv = hkv;
   src.num_blocks = num_blocks;
-  return launch_quantize(src, cache, n_iters, eps, flags, stream, max_ctas);
+  return launch_quantize(src, cache, k_bits, v_bits, n_iters, eps, flags, stream, max_ctas);
 }
 
 cudaError_t launch_append(const uint16_t* k_new, const uint16_t* v_new, const int32_t* seq_lens,
                           int32_t* seq_lens_out, const int32_t* block_tables, int n_seqs, int hkv, int max_blocks,
-                          int64_t num_blocks, uint16_t* ws, uint8_t* cache, int n_iters, float eps,
-                          unsigned* flags, cudaStream_t stream) {
+                          int64_t num_blocks, uint16_t* ws, uint8_t* cache, int k_bits, int v_bits, int n_iters,
+                          float eps, unsigned* flags, cudaStream_t stream) {
   if (n_seqs <= 0) return cudaSuccess;
   if (static_cast<int64_t>(n_seqs) * hkv * 2 * kB > INT32_MAX) return cudaErrorInvalidValue;
   AppendSource src{};
@@ -705,7 +720,7 @@ cudaError_t launch_append(const uint16_t* k_new, const uint16_t* v_new, const in
   src.hkv = hkv;
   src.max_blocks = max_blocks;
   src.num_blocks = num_blocks;
-  return launch_quantize(src, cache, n_iters, eps, flags, stream, 0);
+  return launch_quantize(src, cache, k_bits, v_bits, n_iters, eps, flags, stream, 0);
 }
 
 }  // namespace kvarn

@@ -68,7 +68,7 @@ MIS = ctypes.c_void_p(0x10008)        # not 16-byte aligned
 
 
 @pytest.mark.parametrize("field,value,status", [
-    ("head_dim", 64, 2), ("block_size", 16, 2), ("k_bits", 2, 2), ("v_bits", 4, 2),
+    ("head_dim", 64, 2), ("block_size", 16, 2), ("k_bits", 3, 2), ("v_bits", 3, 2), ("v_bits", 8, 2),
     ("num_q_heads", 12, 1), ("n_iters", 0, 1), ("n_iters", 17, 1), ("num_kv_heads", 0, 1),
     ("reserved", 1, 1),
 ])
@@ -113,3 +113,14 @@ def test_decode_rejects_small_scratch(kv):
     assert dec(A, A, A, A, A, 4, A, A, need - 16, ctypes.byref(m), None) == 4
     assert dec(A, A, A, A, A, 4, A, None, need, ctypes.byref(m), None) == 1     # NULL scratch
     assert dec(A, A, A, A, A, 4, None, A, need, ctypes.byref(m), None) == 1     # NULL out
+
+
+def test_presets_are_accepted_and_sized(kv):
+    for preset, (kb, vb), rec in (("k4v2", (4, 2), 14336), ("k4v4", (4, 4), 18432), ("k2v2", (2, 2), 10240)):
+        meta = kv.make_meta(8, 64, 10, preset=preset)
+        assert (meta.k_bits, meta.v_bits) == (kb, vb)
+        assert kv.meta_record_bytes(meta) == rec
+        assert kv.cache_bytes(meta) == 10 * 8 * rec
+    meta = kv.make_meta(8, 64, 10)
+    meta.k_bits, meta.v_bits = 2, 4            # not a preset
+    assert kv.meta_record_bytes(meta) == 0 and kv.cache_bytes(meta) == 0
