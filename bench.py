@@ -34,6 +34,8 @@ sys.path.insert(0, ROOT)
 PREFILL = dict(n_seqs=16, seq_len=16384, n_kv_heads=8, seed=1)
 DECODE = dict(n_seqs=64, seq_len=16384, n_kv_heads=8, n_q_heads=64, seed=2)
 RECORD = 14336
+PRESET = "k4v2"             # `--preset`: k4v2 (the headline), k4v4 or k2v2
+PRESET_RECORD = {"k4v2": 14336, "k4v4": 18432, "k2v2": 10240}
 WORKLOAD = "prefill_quantize_16x16k + decode_attn_64x16k_gqa64/8"
 # Reduced shapes for profiler captures (`--case small`): still larger than L2, a
 # few hundred MB on the device. Not a bench line.
@@ -172,7 +174,7 @@ def setup_gpu(torch, kv, synth, dev):
     max_blocks = d["seq_len"] // 128
     perm = synth.block_permutation(n_blocks, d["seed"])
     cache = torch.zeros(n_blocks, hkv, RECORD, dtype=torch.uint8, device=dev)
-    meta = kv.make_meta(hkv, d["n_q_heads"], n_blocks, max_blocks_per_seq=max_blocks)
+    meta = kv.make_meta(hkv, d["n_q_heads"], n_blocks, max_blocks_per_seq=max_blocks, preset=PRESET)
     # fill the whole cache by quantizing the prefill batch into 4 disjoint block sets
     per = n_tok // 128
     slot_sets = []
@@ -292,12 +294,14 @@ def run_gpu(args):
     q_tflops = Q_FLOP_PER_ELEMENT * (q_bytes // 2) / (qm * 1e-3) / 1e12
     fp32_peak = fp32_peak_tflops()
     kq = dict(bound="alu", achieved=round(q_tflops, 2), peak=fp32_peak, unit="TFLOP/s",
-              frac=round(q_tflops / fp32_peak, 4), traffic=profiled_traffic("quantize_kernel"),
+              frac=round(q_tflops / fp32_peak, 4),
+              traffic=profiled_traffic("quantize_kernel") if PRESET == "k4v2" else None,
               kernel="quantize_kernel", algorithmic_flops_per_launch=Q_FLOP_PER_ELEMENT * (q_bytes // 2),
               hbm_gbs=round(q_gbs, 1), hbm_frac=round(q_gbs / peak, 4),
               peak_kind="derived: 152 SMs x 128 fp32 lanes x 2 flop x 2.07 GHz")
     kd = dict(bound="hbm", achieved=round(d_gbs, 1), peak=peak, unit="GB/s", frac=round(d_gbs / peak, 4),
-              traffic=profiled_traffic("decode_split_kernel"), kernel="decode_split_kernel+decode_merge_kernel",
+              traffic=profiled_traffic("decode_split_kernel") if PRESET == "k4v2" else None,
+              kernel="decode_split_kernel+decode_merge_kernel",
               algorithmic_bytes_per_launch=d_bytes, peak_kind=peak_kind)
     dominant = kq if qm >= dm else kd
     res = {
@@ -313,7 +317,7 @@ def run_gpu(args):
         "vs_baseline": None,
         "dtype": "f32",
         "data": "synthetic",
-        "config": {"workload": WORKLOAD, "quantize": PREFILL, "decode": DECODE, "preset": "kvarn_k4v2_g128",
+        "config": {"workload": WORKLOAD, "quantize": PREFILL, "decode": DECODE, "preset": f"kvarn_{PRESET}_g128",
                    "n_iters": 4, "l2": "every input > L2 (129 MB); no flush",
                    "parallelism": f"replicas x{world}"},
         "quantize_gbs": round(q_gbs, 1),
@@ -446,10 +450,16 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--case", default="full", choices=["full", "small"],
                     help="small: reduced shapes for profiler captures (not a bench line)")
+    ap.add_argument("--preset", default="k4v2", choices=sorted(PRESET_RECORD),
+                    help="bit preset of the gb300 arm; the default k4v2 is the headline workload")
     args = ap.parse_args()
+    global PRESET, RECORD, PREFILL, DECODE, WORKLOAD
+    PRESET, RECORD = args.preset, PRESET_RECORD[args.preset]
     if args.case == "small":
-        global PREFILL, DECODE, WORKLOAD
         PREFILL, DECODE, WORKLOAD = SMALL["prefill"], SMALL["decode"], SMALL["workload"]
+        args.no_cpu_baseline = True
+    if PRESET != "k4v2":
+        WORKLOAD = f"{WORKLOAD} (preset {PRESET})"
         args.no_cpu_baseline = True
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
