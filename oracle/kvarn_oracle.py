@@ -64,8 +64,13 @@ V_META_OFF = 13312
 RECORD_BYTES = 14336
 
 # bit widths (keys, values) of the presets; the default one is the README's
-PRESETS = {"k4v2": (4, 2), "k4v4": (4, 4), "k2v2": (2, 2)}
+PRESETS = {"k4v2": (4, 2), "k4v4": (4, 4), "k2v2": (2, 2), "k4v2l": (4, 2)}
 DEFAULT_PRESET = "k4v2"
+# Presets with lean metadata [R]: a key group is one channel, so the channel's
+# row scale r_i is one constant inside it and folds into the group's (s, z); a
+# value group is one token, so c_j folds into the value (s, z). Such records store
+# (c, s, z) for keys and (r, s, z) for values: 768 bytes each instead of 1024.
+LEAN = {"k4v2l"}
 
 
 # ----------------------------------------------------------------------------------
@@ -139,10 +144,16 @@ def rtn(y: np.ndarray, bits: int, axis: int):
     return codes, s, z, dict(zmin=ymin, zmax=ymax, s_pre=s_pre, pre=pre)
 
 
-def quantize_tensor(x: np.ndarray, kind: str, n_iters: int = N_ITERS, eps: float = EPS, bits: int | None = None):
+def quantize_tensor(x: np.ndarray, kind: str, n_iters: int = N_ITERS, eps: float = EPS, bits: int | None = None,
+                    lean: bool = False):
     """Stages 2-4 for tiles x [..., 128 channels, 128 tokens] (float64 holding fp16
     values). kind 'K': s and z per channel (row); kind 'V': s and z per token
     (column); `bits` codes (default: 4 for K, 2 for V, the README's preset).
+
+    With `lean`, the scale that is constant inside a group is folded into the
+    group's (s, z): keys are quantized from X_r / c_j (groups are channels) and
+    values from X_r / r_i (groups are tokens); the result's `stored` names the
+    scale vectors a lean record keeps.
 
     Returns a dict with fp16-valued r [.., 128], c [.., 128], s, z, the codes
     [.., 128 ch, 128 tok] and the pre-rounding values needed to judge ties."""
@@ -154,10 +165,18 @@ def quantize_tensor(x: np.ndarray, kind: str, n_iters: int = N_ITERS, eps: float
     r_pre, c_pre = np.exp(lr), np.exp(lc)
     r = fp16_rne(np.clip(r_pre, FP16_MIN_NORMAL, FP16_MAX))
     c = fp16_rne(np.clip(c_pre, FP16_MIN_NORMAL, FP16_MAX))
-    y = xr / (r[..., :, None] * c[..., None, :])
+    if not lean:
+        y = xr / (r[..., :, None] * c[..., None, :])
+        stored = ("r", "c", "s", "z")
+    elif kind == "K":
+        y = xr / c[..., None, :]
+        stored = ("c", "s", "z")
+    else:
+        y = xr / r[..., :, None]
+        stored = ("r", "s", "z")
     codes, s, z, info = rtn(y, bits, axis=-1 if kind == "K" else -2)
     return dict(kind=kind, bits=bits, codes=codes, r=r, c=c, s=s, z=z, r_pre=r_pre, c_pre=c_pre,
-                z_pre=info["zmin"], s_pre=info["s_pre"], code_pre=info["pre"], xr=xr, y=y)
+                z_pre=info["zmin"], s_pre=info["s_pre"], code_pre=info["pre"], xr=xr, y=y, stored=stored)
 
 
 def dequant_tensor(codes, r, c, s, z, kind: str, rotated: bool = False):
@@ -264,11 +283,15 @@ class Layout:
     def __init__(self, name: str):
         self.name = name
         self.k_bits, self.v_bits = PRESETS[name]
+        self.lean = name in LEAN
+        # scale vectors kept per tensor, in record order (fp16 x 128 each)
+        self.k_meta = ("c", "s", "z") if self.lean else ("r", "c", "s", "z")
+        self.v_meta = ("r", "s", "z") if self.lean else ("r", "c", "s", "z")
         self.k_code_off, self.k_code_bytes = 0, D * B * self.k_bits // 8
         self.v_code_off, self.v_code_bytes = self.k_code_bytes, D * B * self.v_bits // 8
         self.k_meta_off = self.v_code_off + self.v_code_bytes
-        self.v_meta_off = self.k_meta_off + 1024
-        self.record_bytes = self.v_meta_off + 1024
+        self.v_meta_off = self.k_meta_off + 256 * len(self.k_meta)
+        self.record_bytes = self.v_meta_off + 256 * len(self.v_meta)
         self.k_src = _source_table(k4_position if self.k_bits == 4 else k2_position, self.k_bits)
         self.v_src = _source_table(v4_position if self.v_bits == 4 else v2_position, self.v_bits)
 
@@ -308,13 +331,14 @@ def pack_record(kq: dict, vq: dict, preset: str = DEFAULT_PRESET) -> np.ndarray:
     """Records [..., record bytes] uint8 from quantize_tensor results for K and V."""
     lay = LAYOUTS[preset]
     assert kq.get("bits", lay.k_bits) == lay.k_bits and vq.get("bits", lay.v_bits) == lay.v_bits
+    assert kq.get("stored", lay.k_meta) == lay.k_meta and vq.get("stored", lay.v_meta) == lay.v_meta
     kc = kq["codes"].reshape(kq["codes"].shape[:-2] + (D * B,)).astype(np.uint8)
     vc = vq["codes"].reshape(vq["codes"].shape[:-2] + (D * B,)).astype(np.uint8)
     rec = np.zeros(kc.shape[:-1] + (lay.record_bytes,), np.uint8)
     rec[..., lay.k_code_off:lay.k_code_off + lay.k_code_bytes] = _pack_codes(kc, lay.k_src, lay.k_bits)
     rec[..., lay.v_code_off:lay.v_code_off + lay.v_code_bytes] = _pack_codes(vc, lay.v_src, lay.v_bits)
-    for off, q in ((lay.k_meta_off, kq), (lay.v_meta_off, vq)):
-        for n, name in enumerate(("r", "c", "s", "z")):
+    for off, q, names in ((lay.k_meta_off, kq, lay.k_meta), (lay.v_meta_off, vq, lay.v_meta)):
+        for n, name in enumerate(names):
             rec[..., off + 256 * n: off + 256 * (n + 1)] = _f16_bytes(q[name])
     return rec
 
@@ -322,17 +346,21 @@ def pack_record(kq: dict, vq: dict, preset: str = DEFAULT_PRESET) -> np.ndarray:
 def unpack_record(rec: np.ndarray):
     """Inverse of pack_record (the preset follows from the record size): dicts for
     K and V with codes [.., 128 ch, 128 tok], bits and r, c, s, z (float64
-    holding fp16)."""
+    holding fp16); a scale a lean record does not keep is returned as ones, which
+    is what it was folded against, and `stored` names the kept ones."""
     rec = np.asarray(rec, np.uint8)
     lay = layout_of(rec.shape[-1])
     lead = rec.shape[:-1]
     kc = _unpack_codes(rec[..., lay.k_code_off:lay.k_code_off + lay.k_code_bytes], lay.k_src, lay.k_bits)
     vc = _unpack_codes(rec[..., lay.v_code_off:lay.v_code_off + lay.v_code_bytes], lay.v_src, lay.v_bits)
     out = []
-    for off, codes, kind, bits in ((lay.k_meta_off, kc, "K", lay.k_bits), (lay.v_meta_off, vc, "V", lay.v_bits)):
-        meta = np.ascontiguousarray(rec[..., off:off + 1024]).view("<f2").astype(np.float64)
-        d = dict(kind=kind, bits=bits, codes=codes.reshape(lead + (D, B)))
-        for n, name in enumerate(("r", "c", "s", "z")):
+    for off, codes, kind, bits, names in ((lay.k_meta_off, kc, "K", lay.k_bits, lay.k_meta),
+                                          (lay.v_meta_off, vc, "V", lay.v_bits, lay.v_meta)):
+        meta = np.ascontiguousarray(rec[..., off:off + 256 * len(names)]).view("<f2").astype(np.float64)
+        d = dict(kind=kind, bits=bits, codes=codes.reshape(lead + (D, B)), stored=names)
+        for name in ("r", "c"):
+            d[name] = np.ones(lead + (D,))
+        for n, name in enumerate(names):
             d[name] = meta[..., 128 * n:128 * (n + 1)]
         out.append(d)
     return out[0], out[1]
@@ -353,10 +381,11 @@ def quantize_tiles(k_tok: np.ndarray, v_tok: np.ndarray, n_iters: int = N_ITERS,
     """k_tok, v_tok: fp16 tiles [..., 128 tokens, 128 channels] (vLLM row layout).
     Returns (records [..., record bytes], K result, V result)."""
     kb, vb = PRESETS[preset]
+    lean = preset in LEAN
     kx = np.swapaxes(np.asarray(k_tok, np.float64), -1, -2)
     vx = np.swapaxes(np.asarray(v_tok, np.float64), -1, -2)
-    kq = quantize_tensor(kx, "K", n_iters, eps, bits=kb)
-    vq = quantize_tensor(vx, "V", n_iters, eps, bits=vb)
+    kq = quantize_tensor(kx, "K", n_iters, eps, bits=kb, lean=lean)
+    vq = quantize_tensor(vx, "V", n_iters, eps, bits=vb, lean=lean)
     return pack_record(kq, vq, preset), kq, vq
 
 

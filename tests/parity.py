@@ -57,12 +57,17 @@ def compare_records(gpu_rec: np.ndarray, kq: dict, vq: dict) -> dict:
         assert r["bits"] == bits
         gaxis = -1 if kind == "K" else -2      # axis inside a group
         # r, c
+        stored = g["stored"]                   # a lean record keeps one of r, c
+        assert tuple(r.get("stored", stored)) == tuple(stored)
+        tile_rc_flip = np.zeros(g["codes"].shape[0], bool)
         for name, pre in (("r", np.clip(r["r_pre"], o.FP16_MIN_NORMAL, o.FP16_MAX)),
                           ("c", np.clip(r["c_pre"], o.FP16_MIN_NORMAL, o.FP16_MAX))):
+            if name not in stored:
+                continue
             ok = _meta_ok(g[name], r[name], pre)
             assert ok.all(), f"{kind}.{name}: {np.count_nonzero(~ok)} values outside tolerance"
             stats["meta_flips"] += int(np.count_nonzero(g[name] != r[name]))
-        tile_rc_flip = (g["r"] != r["r"]).any(axis=-1) | (g["c"] != r["c"]).any(axis=-1)   # [N]
+            tile_rc_flip |= (g[name] != r[name]).any(axis=-1)                 # [N]
         # s, z (only meaningful where r, c agree)
         z_pre = np.clip(r["z_pre"], -o.FP16_MAX, o.FP16_MAX)
         s_pre = np.clip(r["s_pre"], o.FP16_MIN_NORMAL, o.FP16_MAX)
@@ -105,8 +110,10 @@ def compare_records(gpu_rec: np.ndarray, kq: dict, vq: dict) -> dict:
     # dequantised tiles (rotated domain; elements whose codes flipped are covered by
     # the code-flip budget above, a single 2-bit flip alone moves a tile by ~1e-2)
     for g, r, kind in ((gk, kq, "K"), (gv, vq, "V")):
+        # the scales a record does not keep are ones on both sides (they were folded)
+        rr = {n: (r[n] if n in g["stored"] else np.ones_like(r[n])) for n in ("r", "c")}
         a = o.dequant_tensor(g["codes"], g["r"], g["c"], g["s"], g["z"], kind, rotated=True)
-        b = o.dequant_tensor(r["codes"], r["r"], r["c"], r["s"], r["z"], kind, rotated=True)
+        b = o.dequant_tensor(r["codes"], rr["r"], rr["c"], r["s"], r["z"], kind, rotated=True)
         keep = g["codes"] == r["codes"]
         num = np.sqrt(((a - b) ** 2 * keep).reshape(a.shape[0], -1).sum(axis=1))
         den = np.maximum(np.sqrt((b ** 2 * keep).reshape(b.shape[0], -1).sum(axis=1)), 1e-30)

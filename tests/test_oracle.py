@@ -382,11 +382,16 @@ def _random_quantized(rng, n, kbits, vbits):
 def test_preset_record_sizes_and_roundtrip(preset):
     kbits, vbits = o.PRESETS[preset]
     lay = o.LAYOUTS[preset]
-    # code areas hold 128 x 128 codes at their width, then 2 x 4 x 128 fp16 scales
-    assert lay.record_bytes == 128 * 128 * (kbits + vbits) // 8 + 2 * 4 * 128 * 2
+    # code areas hold 128 x 128 codes at their width, then 4 (lean: 3) vectors of 128
+    # fp16 scales per tensor
+    n_vec = 3 if preset in o.LEAN else 4
+    assert lay.record_bytes == 128 * 128 * (kbits + vbits) // 8 + 2 * n_vec * 128 * 2
     assert abs(o.compression_ratio(preset) - 65536 / lay.record_bytes) < 1e-12
     assert o.layout_of(lay.record_bytes) is lay
     kq, vq = _random_quantized(np.random.default_rng(17), 2, kbits, vbits)
+    if preset in o.LEAN:                      # the folded scales are ones after unpacking
+        kq["r"] = np.ones_like(kq["r"])
+        vq["c"] = np.ones_like(vq["c"])
     rec = o.pack_record(kq, vq, preset)
     assert rec.shape == (2, lay.record_bytes)
     k2, v2 = o.unpack_record(rec)
@@ -474,3 +479,30 @@ def test_bit_width_changes_only_the_step_and_zero():
         assert np.array_equal(a["z"], b["z"])           # z is the group minimum in every preset
     assert (v44["s"] < v42["s"]).all() and (k22["s"] > k42["s"]).all()
     assert v44["codes"].max() == 15 and k22["codes"].max() == 3
+
+
+def test_lean_preset_folds_the_in_group_scale():
+    """Lean metadata: keys are quantized from X_r / c (the channel's r is constant in
+    a key group), values from X_r / r (the token's c is constant in a value group).
+    Recomputed from the full-format quantization's y = X_r / (r c): multiplying a
+    key row by r_i (a value column by c_j) and rounding gives the lean result."""
+    k, v, _ = synth.single_tile(9)
+    rec, kq, vq = o.quantize_tiles(k, v, preset="k4v2l")
+    _, kf, vf = o.quantize_tiles(k, v, preset="k4v2")
+    assert rec.shape[-1] == 13824 and abs(o.compression_ratio("k4v2l") - 65536 / 13824) < 1e-12
+    assert abs(o.compression_ratio("k4v2l") - 4.74) < 0.005            # 2048 -> 1536 bytes of scales
+    assert np.array_equal(kq["c"], kf["c"]) and np.array_equal(vq["r"], vf["r"])
+    for lq, f, kind, axis, bits in ((kq, kf, "K", -1, 4), (vq, vf, "V", -2, 2)):
+        y = f["y"] * (f["r"][:, None] if kind == "K" else f["c"][None, :])
+        assert np.allclose(y, lq["y"], rtol=1e-14, atol=0)
+        assert np.array_equal(lq["codes"], _brute_codes(lq["y"], lq["s"], lq["z"], bits, axis))
+        assert np.array_equal(lq["z"], o.fp16_rne(np.clip(y.min(axis=axis), -o.FP16_MAX, o.FP16_MAX)))
+    k2, v2 = o.unpack_record(rec)
+    assert k2["stored"] == ("c", "s", "z") and v2["stored"] == ("r", "s", "z")
+    assert (k2["r"] == 1).all() and (v2["c"] == 1).all()
+    # both formats dequantize to nearly the same tile (each within its own step)
+    kl, vl = o.dequant_record(rec)
+    kfull, vfull = o.dequant_record(o.pack_record(kf, vf))
+    for a, b in ((kl, kfull), (vl, vfull)):
+        rel = np.linalg.norm(a - b) / np.linalg.norm(b)
+        assert rel < 0.05, rel
