@@ -34,8 +34,8 @@ sys.path.insert(0, ROOT)
 PREFILL = dict(n_seqs=16, seq_len=16384, n_kv_heads=8, seed=1)
 DECODE = dict(n_seqs=64, seq_len=16384, n_kv_heads=8, n_q_heads=64, seed=2)
 RECORD = 14336
-PRESET = "k4v2"             # `--preset`: k4v2 (the headline), k4v4 or k2v2
-PRESET_RECORD = {"k4v2": 14336, "k4v4": 18432, "k2v2": 10240}
+PRESET = "k4v2"             # `--preset`: k4v2 (the headline), k4v4, k2v2 or k4v2l
+PRESET_RECORD = {"k4v2": 14336, "k4v4": 18432, "k2v2": 10240, "k4v2l": 13824}
 WORKLOAD = "prefill_quantize_16x16k + decode_attn_64x16k_gqa64/8"
 # Reduced shapes for profiler captures (`--case small`): still larger than L2, a
 # few hundred MB on the device. Not a bench line.

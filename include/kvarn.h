@@ -43,6 +43,11 @@
  *   k4v4: K codes [0, 8192), V codes [8192, 16384), K meta [16384, 17408), V meta
  *     [17408, 18432). k2v2: K codes [0, 4096), V codes [4096, 8192), K meta
  *     [8192, 9216), V meta [9216, 10240).
+ *   k4v2l (k4v2 with layout = KVARN_LAYOUT_LEAN): lean metadata. A key group is
+ *     one channel, so the channel's r is constant inside it and is folded into
+ *     its s and z (keys are quantized from X_r / c); a value group is one token,
+ *     so c is folded likewise (values from X_r / r). K meta [12288, 13056) is fp16
+ *     c, s, z x 128; V meta [13056, 13824) is r, s, z; 13824 bytes in all.
  * The decode kernel keeps 7 warps with two record stages each for k4v2 and k2v2,
  * and 6 warps for k4v4 (its stages would not fit 7 warps' shared memory).
  *
@@ -114,6 +119,7 @@ extern "C" {
 #define KVARN_BLOCK_SIZE 128
 #define KVARN_RECORD_BYTES 14336
 #define KVARN_MAX_GQA_GROUP 8
+#define KVARN_LAYOUT_LEAN 1  /* kvarn_meta.layout: lean metadata (see presets)    */
 
 typedef enum {
   KVARN_OK = 0,
@@ -141,7 +147,7 @@ typedef struct {
   float eps;                  /* added to each variance, > 0 (preset 1e-6)        */
   int64_t num_blocks;         /* physical blocks in the cache                     */
   int32_t max_blocks_per_seq; /* row length of block_tables                       */
-  int32_t reserved;           /* must be 0                                        */
+  int32_t layout;             /* 0, or KVARN_LAYOUT_LEAN with k4v2 (preset k4v2l) */
 } kvarn_meta;
 
 /* Bytes of one (block, kv-head) record of the default preset k4v2: 14336. */

@@ -63,21 +63,23 @@ class KvarnMeta(ctypes.Structure):
         ("eps", ctypes.c_float),
         ("num_blocks", ctypes.c_int64),
         ("max_blocks_per_seq", ctypes.c_int32),
-        ("reserved", ctypes.c_int32),
+        ("layout", ctypes.c_int32),
     ]
 
 
-# bit widths (keys, values) of the presets; k4v2 is kvarn_k4v2_g128
-PRESETS = {"k4v2": (4, 2), "k4v4": (4, 4), "k2v2": (2, 2)}
+# bit widths (keys, values) and metadata layout of the presets; k4v2 is
+# kvarn_k4v2_g128, k4v2l the same with lean metadata (KVARN_LAYOUT_LEAN)
+PRESETS = {"k4v2": (4, 2, 0), "k4v4": (4, 4, 0), "k2v2": (2, 2, 0), "k4v2l": (4, 2, 1)}
+KVARN_LAYOUT_LEAN = 1
 
 
 def make_meta(num_kv_heads: int, num_q_heads: int, num_blocks: int, max_blocks_per_seq: int = 0,
               n_iters: int = 4, eps: float = 1e-6, preset: str = "k4v2") -> KvarnMeta:
     """Head_dim 128, block 128; preset k4v2 (4-bit K, 2-bit V: kvarn_k4v2_g128),
-    k4v4 or k2v2."""
-    kb, vb = PRESETS[preset]
+    k4v4, k2v2, or k4v2l (k4v2 with lean metadata)."""
+    kb, vb, layout = PRESETS[preset]
     return KvarnMeta(num_kv_heads, num_q_heads, HEAD_DIM, BLOCK_SIZE, kb, vb, n_iters, eps,
-                     num_blocks, max_blocks_per_seq, 0)
+                     num_blocks, max_blocks_per_seq, layout)
 
 
 def load_library(path: str = LIB_PATH) -> ctypes.CDLL:

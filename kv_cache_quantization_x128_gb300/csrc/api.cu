@@ -47,7 +47,10 @@ kvarn_status check_meta(const kvarn_meta* m) {
   if (m->num_blocks < 0) return fail(KVARN_EINVAL, "num_blocks must be >= 0 (got %lld)", (long long)m->num_blocks);
   if (m->max_blocks_per_seq < 0)
     return fail(KVARN_EINVAL, "max_blocks_per_seq must be >= 0 (got %lld)", (long long)m->max_blocks_per_seq);
-  if (m->reserved != 0) return fail(KVARN_EINVAL, "reserved must be 0");
+  if (m->layout != 0 && m->layout != KVARN_LAYOUT_LEAN)
+    return fail(KVARN_EINVAL, "layout must be 0 or KVARN_LAYOUT_LEAN (got %lld)", (long long)m->layout);
+  if (m->layout == KVARN_LAYOUT_LEAN && !(m->k_bits == 4 && m->v_bits == 2))
+    return fail(KVARN_EUNSUPPORTED, "lean metadata is offered with k4v2 only");
   return KVARN_OK;
 }
 
@@ -82,7 +85,8 @@ size_t kvarn_record_bytes(void) { return KVARN_RECORD_BYTES; }
 
 size_t kvarn_meta_record_bytes(const kvarn_meta* meta) {
   if (check_meta(meta) != KVARN_OK) return 0;
-  return static_cast<size_t>(KVARN_HEAD_DIM) * KVARN_BLOCK_SIZE * (meta->k_bits + meta->v_bits) / 8 + 2048;
+  return static_cast<size_t>(KVARN_HEAD_DIM) * KVARN_BLOCK_SIZE * (meta->k_bits + meta->v_bits) / 8 +
+         (meta->layout == KVARN_LAYOUT_LEAN ? 1536 : 2048);
 }
 
 size_t kvarn_cache_bytes(const kvarn_meta* meta) {
@@ -116,7 +120,8 @@ kvarn_status kvarn_quantize_tiles(const uint16_t* k, const uint16_t* v, const in
   KV_TRY(flags_ptr(&fl));
   return cuda_status(kvarn::launch_quantize_prefill(k, v, slot_mapping, n_tokens, meta->num_kv_heads,
                                                     meta->num_blocks, cache, meta->k_bits, meta->v_bits,
-                                                    meta->n_iters, meta->eps, fl, static_cast<cudaStream_t>(stream), 0),
+                                                    meta->layout == KVARN_LAYOUT_LEAN, meta->n_iters, meta->eps, fl,
+                                                    static_cast<cudaStream_t>(stream), 0),
                      "kvarn_quantize_tiles");
 }
 
@@ -140,8 +145,9 @@ kvarn_status kvarn_append_decode(const uint16_t* k_new, const uint16_t* v_new, c
   KV_TRY(flags_ptr(&fl));
   return cuda_status(kvarn::launch_append(k_new, v_new, seq_lens, seq_lens_out, block_tables, n_seqs,
                                           meta->num_kv_heads, meta->max_blocks_per_seq, meta->num_blocks,
-                                          workspace, cache, meta->k_bits, meta->v_bits, meta->n_iters, meta->eps,
-                                          fl, static_cast<cudaStream_t>(stream)),
+                                          workspace, cache, meta->k_bits, meta->v_bits,
+                                          meta->layout == KVARN_LAYOUT_LEAN, meta->n_iters, meta->eps, fl,
+                                          static_cast<cudaStream_t>(stream)),
                      "kvarn_append_decode");
 }
 
@@ -172,7 +178,8 @@ kvarn_status kvarn_decode_attention(const uint16_t* q, const uint8_t* cache, con
   KV_TRY(flags_ptr(&fl));
   return cuda_status(kvarn::launch_decode(q, cache, workspace, block_tables, seq_lens, n_seqs, meta->num_kv_heads,
                                           meta->num_q_heads / meta->num_kv_heads, meta->max_blocks_per_seq,
-                                          meta->num_blocks, meta->k_bits, meta->v_bits, out, scratch, fl,
+                                          meta->num_blocks, meta->k_bits, meta->v_bits,
+                                          meta->layout == KVARN_LAYOUT_LEAN, out, scratch, fl,
                                           static_cast<cudaStream_t>(stream)),
                      "kvarn_decode_attention");
 }

@@ -67,7 +67,7 @@ KVARN_API kvarn_status kvarn_decode_attention_static(const uint16_t* q, const ui
     return kvarn::set_error(KVARN_EUNSUPPORTED, "only the kvarn_k4v2_g128 preset (head_dim 128, block 128) is supported");
   if (meta->num_kv_heads < 1 || meta->num_q_heads < meta->num_kv_heads ||
       meta->num_q_heads % meta->num_kv_heads != 0 || meta->num_blocks < 0 || meta->max_blocks_per_seq < 0 ||
-      meta->reserved != 0 || meta->n_iters < 1 || meta->n_iters > 16 || !(meta->eps > 0.0f) || !(meta->eps < 1.0f))
+      meta->layout != 0 || meta->n_iters < 1 || meta->n_iters > 16 || !(meta->eps > 0.0f) || !(meta->eps < 1.0f))
     return kvarn::set_error(KVARN_EINVAL, "invalid kvarn_meta");
   if (meta->num_q_heads / meta->num_kv_heads > KVARN_MAX_GQA_GROUP)
     return kvarn::set_error(KVARN_EUNSUPPORTED, "GQA group (Hq/Hkv) must be <= 8");
@@ -95,7 +95,7 @@ KVARN_API kvarn_status kvarn_decode_attention_static(const uint16_t* q, const ui
     return kvarn::set_error(KVARN_ECUDA, "kvarn_decode_attention_static: device flag word unavailable");
   const cudaError_t e = kvarn::launch_decode(q, cache, workspace, block_tables, seq_lens, n_seqs, meta->num_kv_heads,
                                              meta->num_q_heads / meta->num_kv_heads, meta->max_blocks_per_seq,
-                                             meta->num_blocks, 4, 2, out, scratch, flags,
+                                             meta->num_blocks, 4, 2, false, out, scratch, flags,
                                              static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return kvarn::set_error(KVARN_ECUDA, cudaGetErrorString(e));
   return KVARN_OK;

@@ -37,9 +37,9 @@ constexpr int kRecFloats = 8 * kPartStride;     // one partial record (8 q-head 
 
 // Split kernel shape for KB-bit keys and VB-bit values: 7 warps, or 6 when two
 // records per warp would not fit in shared memory (k4v4's 18432-byte records).
-template <int KB, int VB>
+template <int KB, int VB, bool kLean = false>
 struct SplitCfg {
-  using L = RecordLayout<KB, VB>;
+  using L = RecordLayout<KB, VB, kLean>;
   static constexpr int kWarps = 7 * kStages * L::kBytes + 7 * kStages * 8 <= 232448 ? 7 : 6;
   static constexpr int kSmem = kWarps * kStages * L::kBytes + kWarps * kStages * 8;
   static_assert(kSmem <= 232448, "decode stages");
@@ -267,10 +267,10 @@ __device__ __forceinline__ void load_q(const DecodeArgs& a, int s, int h, int g,
 }
 
 // One packed tile: update the running (max, sum, acc) of head g.
-template <int KB, int VB>
+template <int KB, int VB, bool kLean>
 __device__ __forceinline__ void attend_tile(const uint8_t* rec, const float (&qv)[8][4], int g, int c, float& m_run,
                                             float& l_run, float (&acc)[16][2]) {
-  using L = RecordLayout<KB, VB>;
+  using L = RecordLayout<KB, VB, kLean>;
   const uint16_t* km = reinterpret_cast<const uint16_t*>(rec + L::kKMetaOff);
   const uint16_t* vm = reinterpret_cast<const uint16_t*>(rec + L::kVMetaOff);
 
@@ -280,9 +280,11 @@ __device__ __forceinline__ void attend_tile(const uint8_t* rec, const float (&qv
 #pragma unroll
   for (int ks = 0; ks < 8; ++ks) {
     const int ch0 = 16 * ks + 2 * c;
-    const float2 r0 = h2pair(km + ch0), r1 = h2pair(km + ch0 + 8);
-    const float2 s0 = h2pair(km + 256 + ch0), s1 = h2pair(km + 256 + ch0 + 8);
-    const float2 z0 = h2pair(km + 384 + ch0), z1 = h2pair(km + 384 + ch0 + 8);
+    // lean records fold the key row scale r into s and z
+    const float2 r0 = kLean ? make_float2(1.f, 1.f) : h2pair(km + L::kKr + ch0);
+    const float2 r1 = kLean ? make_float2(1.f, 1.f) : h2pair(km + L::kKr + ch0 + 8);
+    const float2 s0 = h2pair(km + L::kKs + ch0), s1 = h2pair(km + L::kKs + ch0 + 8);
+    const float2 z0 = h2pair(km + L::kKz + ch0), z1 = h2pair(km + L::kKz + ch0 + 8);
     split2(qv[ks][0] * (r0.x * s0.x), qv[ks][1] * (r0.y * s0.y), A[ks][0], A[ks][1]);
     split2(qv[ks][2] * (r1.x * s1.x), qv[ks][3] * (r1.y * s1.y), A[ks][2], A[ks][3]);
     beta = fmaf(qv[ks][0], r0.x * z0.x, beta);
@@ -343,7 +345,7 @@ __device__ __forceinline__ void attend_tile(const uint8_t* rec, const float (&qv
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int nt = 4 * ntg + j;
-      const float2 ck = h2pair(km + 128 + 8 * nt + 2 * c);
+      const float2 ck = h2pair(km + L::kKc + 8 * nt + 2 * c);
       sc[nt][0] = ck.x * ((d[j][0] + d[j][2]) + beta);
       sc[nt][1] = ck.y * ((d[j][1] + d[j][3]) + beta);
     }
@@ -376,9 +378,11 @@ __device__ __forceinline__ void attend_tile(const uint8_t* rec, const float (&qv
 #pragma unroll
   for (int ks = 0; ks < 8; ++ks) {
     const int t0 = 16 * ks + 2 * c;
-    const float2 c0 = h2pair(vm + 128 + t0), c1 = h2pair(vm + 128 + t0 + 8);
-    const float2 s0 = h2pair(vm + 256 + t0), s1 = h2pair(vm + 256 + t0 + 8);
-    const float2 z0 = h2pair(vm + 384 + t0), z1 = h2pair(vm + 384 + t0 + 8);
+    // lean records fold the value column scale c into s and z
+    const float2 c0 = kLean ? make_float2(1.f, 1.f) : h2pair(vm + L::kVc + t0);
+    const float2 c1 = kLean ? make_float2(1.f, 1.f) : h2pair(vm + L::kVc + t0 + 8);
+    const float2 s0 = h2pair(vm + L::kVs + t0), s1 = h2pair(vm + L::kVs + t0 + 8);
+    const float2 z0 = h2pair(vm + L::kVz + t0), z1 = h2pair(vm + L::kVz + t0 + 8);
     const float p0 = sc[2 * ks][0], p1 = sc[2 * ks][1], p2 = sc[2 * ks + 1][0], p3 = sc[2 * ks + 1][1];
     split2(p0 * (c0.x * s0.x), p1 * (c0.y * s0.y), A[ks][0], A[ks][1]);
     split2(p2 * (c1.x * s1.x), p3 * (c1.y * s1.y), A[ks][2], A[ks][3]);
@@ -420,7 +424,7 @@ __device__ __forceinline__ void attend_tile(const uint8_t* rec, const float (&qv
   #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int nt2 = 2 * (2 * npg + (j >> 1)) + (j & 1);
-        const float2 rv = h2pair(vm + 8 * nt2 + 2 * c);
+        const float2 rv = h2pair(vm + L::kVr + 8 * nt2 + 2 * c);
         acc[nt2][0] = fmaf(rv.x, (d[j][0] + d[j][2]) + gamma, acc[nt2][0]);
         acc[nt2][1] = fmaf(rv.y, (d[j][1] + d[j][3]) + gamma, acc[nt2][1]);
       }
@@ -453,7 +457,7 @@ __device__ __forceinline__ void attend_tile(const uint8_t* rec, const float (&qv
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int nt2 = 4 * npg + j;
-        const float2 rv = h2pair(vm + 8 * nt2 + 2 * c);
+        const float2 rv = h2pair(vm + L::kVr + 8 * nt2 + 2 * c);
         acc[nt2][0] = fmaf(rv.x, (d[j][0] + d[j][2]) + gamma, acc[nt2][0]);
         acc[nt2][1] = fmaf(rv.y, (d[j][1] + d[j][3]) + gamma, acc[nt2][1]);
       }
@@ -472,10 +476,10 @@ __device__ __forceinline__ void flush_record(const DecodeArgs& a, int64_t rec_id
   if (c == 0) *reinterpret_cast<float2*>(out + 128) = make_float2(m_run, l);
 }
 
-template <int KB, int VB>
-__global__ void __launch_bounds__(SplitCfg<KB, VB>::kWarps * 32, 1) decode_split_kernel(DecodeArgs a) {
-  constexpr int kWarps = SplitCfg<KB, VB>::kWarps;
-  constexpr int kRecBytes = RecordLayout<KB, VB>::kBytes;
+template <int KB, int VB, bool kLean>
+__global__ void __launch_bounds__(SplitCfg<KB, VB, kLean>::kWarps * 32, 1) decode_split_kernel(DecodeArgs a) {
+  constexpr int kWarps = SplitCfg<KB, VB, kLean>::kWarps;
+  constexpr int kRecBytes = RecordLayout<KB, VB, kLean>::kBytes;
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
@@ -528,7 +532,7 @@ __global__ void __launch_bounds__(SplitCfg<KB, VB>::kWarps * 32, 1) decode_split
     const bool ok = __all_sync(0xffffffffu, mbar_wait(&bars[stg], (phase >> stg) & 1u, a.flags));
     phase ^= 1u << stg;
     if (!ok) break;   // a copy never arrived (flag raised): stop this warp
-    if ((valid >> stg) & 1u) attend_tile<KB, VB>(stages + stg * kRecBytes, qv, g, c, m_run, l_run, acc);
+    if ((valid >> stg) & 1u) attend_tile<KB, VB, kLean>(stages + stg * kRecBytes, qv, g, c, m_run, l_run, acc);
     __syncwarp();
     if (gb + k + kStages < ge) {     // refill this stage with the tile kStages ahead
       advance(a, lc);
@@ -667,18 +671,20 @@ int decode_num_ctas() {
   return sms > 0 ? (sms < kMaxCtas ? sms : kMaxCtas) : 1;
 }
 
-template <int KB, int VB>
+template <int KB, int VB, bool kLean>
 cudaError_t launch_split(const DecodeArgs& a, cudaStream_t stream) {
+  using C = SplitCfg<KB, VB, kLean>;
   static std::atomic<unsigned long long> smem_set{0};
-  cudaError_t err = set_smem_once(decode_split_kernel<KB, VB>, SplitCfg<KB, VB>::kSmem, smem_set);
+  cudaError_t err = set_smem_once(decode_split_kernel<KB, VB, kLean>, C::kSmem, smem_set);
   if (err != cudaSuccess) return err;
-  decode_split_kernel<KB, VB><<<a.n_ctas, SplitCfg<KB, VB>::kWarps * 32, SplitCfg<KB, VB>::kSmem, stream>>>(a);
+  decode_split_kernel<KB, VB, kLean><<<a.n_ctas, C::kWarps * 32, C::kSmem, stream>>>(a);
   return cudaGetLastError();
 }
 
 cudaError_t launch_decode(const uint16_t* q, const uint8_t* cache, const uint16_t* ws, const int32_t* block_tables,
                           const int32_t* seq_lens, int n_seqs, int hkv, int group, int max_blocks, int64_t num_blocks,
-                          int k_bits, int v_bits, uint16_t* out, void* scratch, unsigned* flags, cudaStream_t stream) {
+                          int k_bits, int v_bits, bool lean, uint16_t* out, void* scratch, unsigned* flags,
+                          cudaStream_t stream) {
   if (n_seqs <= 0) return cudaSuccess;
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
@@ -698,15 +704,17 @@ cudaError_t launch_decode(const uint16_t* q, const uint8_t* cache, const uint16_
   a.group = group;
   a.max_blocks = max_blocks;
   a.n_ctas = sms > 0 ? (sms < kMaxCtas ? sms : kMaxCtas) : 1;
-  a.warps = k_bits == 4 && v_bits == 4 ? SplitCfg<4, 4>::kWarps
-            : k_bits == 2 ? SplitCfg<2, 2>::kWarps : SplitCfg<4, 2>::kWarps;
-  if (!((k_bits == 4 && (v_bits == 2 || v_bits == 4)) || (k_bits == 2 && v_bits == 2))) return cudaErrorInvalidValue;
+  const bool k4v2 = k_bits == 4 && v_bits == 2, k4v4 = k_bits == 4 && v_bits == 4, k2v2 = k_bits == 2 && v_bits == 2;
+  if (!(k4v2 || ((k4v4 || k2v2) && !lean))) return cudaErrorInvalidValue;
+  a.warps = k4v4 ? SplitCfg<4, 4>::kWarps : k2v2 ? SplitCfg<2, 2>::kWarps
+            : lean ? SplitCfg<4, 2, true>::kWarps : SplitCfg<4, 2>::kWarps;
   decode_scan_kernel<<<1, 1024, 0, stream>>>(a);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   if (max_blocks > 0) {
-    err = k_bits == 2 ? launch_split<2, 2>(a, stream)
-          : v_bits == 4 ? launch_split<4, 4>(a, stream) : launch_split<4, 2>(a, stream);
+    err = k2v2 ? launch_split<2, 2, false>(a, stream)
+          : k4v4 ? launch_split<4, 4, false>(a, stream)
+          : lean ? launch_split<4, 2, true>(a, stream) : launch_split<4, 2, false>(a, stream);
     if (err != cudaSuccess) return err;
   }
   dim3 mgrid(hkv, n_seqs);

@@ -19,19 +19,26 @@ constexpr float kFp16Max = 65504.0f;
 constexpr float kInvSqrt128 = 0.088388347648318440f; // 2^-3.5
 
 // Record of one (block, kv-head) for KB-bit keys and VB-bit values: key codes,
-// value codes, key metadata (fp16 r, c, s, z x 128), value metadata.
-template <int KB, int VB>
+// value codes, key metadata, value metadata. Full metadata is fp16 (r, c, s, z) x
+// 128 per tensor; lean metadata keeps (c, s, z) for keys and (r, s, z) for values
+// (the scale constant inside a quantization group is folded into its s and z).
+template <int KB, int VB, bool kLean = false>
 struct RecordLayout {
   static constexpr int kKBits = KB, kVBits = VB;
+  static constexpr int kMetaBytes = kLean ? 768 : 1024;   // per tensor
   static constexpr int kKCodeBytes = kD * kB * KB / 8;
   static constexpr int kVCodeBytes = kD * kB * VB / 8;
   static constexpr int kKCodeOff = 0;
   static constexpr int kVCodeOff = kKCodeBytes;
   static constexpr int kKMetaOff = kKCodeBytes + kVCodeBytes;
-  static constexpr int kVMetaOff = kKMetaOff + 1024;
-  static constexpr int kBytes = kVMetaOff + 1024;
+  static constexpr int kVMetaOff = kKMetaOff + kMetaBytes;
+  static constexpr int kBytes = kVMetaOff + kMetaBytes;
+  // fp16 offsets of the vectors inside a tensor's metadata (-1: not stored)
+  static constexpr int kKr = kLean ? -1 : 0, kKc = kLean ? 0 : 128, kKs = kLean ? 128 : 256, kKz = kLean ? 256 : 384;
+  static constexpr int kVr = 0, kVc = kLean ? -1 : 128, kVs = kLean ? 128 : 256, kVz = kLean ? 256 : 384;
 };
 static_assert(RecordLayout<4, 2>::kBytes == kRec && RecordLayout<4, 2>::kVMetaOff == kVMetaOff, "k4v2 record");
+static_assert(RecordLayout<4, 2, true>::kBytes == 13824, "k4v2 lean record");
 
 // Kernels report data errors by OR-ing KVARN_FLAG_* bits into a device flag word
 // whose address the host passes in.

@@ -24,19 +24,20 @@ inline cudaError_t set_smem_once(Kernel* kernel, int bytes, std::atomic<unsigned
   return err;
 }
 
-// k_bits / v_bits: a preset of kvarn.h (4/2, 4/4 or 2/2), checked by the caller.
+// k_bits / v_bits / lean: a preset of kvarn.h (4/2, 4/4, 2/2; lean with 4/2 only),
+// checked by the caller.
 cudaError_t launch_quantize_prefill(const uint16_t* k, const uint16_t* v, const int64_t* slot, int64_t n_tokens,
-                                    int hkv, int64_t num_blocks, uint8_t* cache, int k_bits, int v_bits, int n_iters,
-                                    float eps, unsigned* flags, cudaStream_t stream, int max_ctas);
+                                    int hkv, int64_t num_blocks, uint8_t* cache, int k_bits, int v_bits, bool lean,
+                                    int n_iters, float eps, unsigned* flags, cudaStream_t stream, int max_ctas);
 
 cudaError_t launch_append(const uint16_t* k_new, const uint16_t* v_new, const int32_t* seq_lens,
                           int32_t* seq_lens_out, const int32_t* block_tables, int n_seqs, int hkv, int max_blocks,
-                          int64_t num_blocks, uint16_t* ws, uint8_t* cache, int k_bits, int v_bits, int n_iters,
-                          float eps, unsigned* flags, cudaStream_t stream);
+                          int64_t num_blocks, uint16_t* ws, uint8_t* cache, int k_bits, int v_bits, bool lean,
+                          int n_iters, float eps, unsigned* flags, cudaStream_t stream);
 
 cudaError_t launch_decode(const uint16_t* q, const uint8_t* cache, const uint16_t* ws, const int32_t* block_tables,
                           const int32_t* seq_lens, int n_seqs, int hkv, int group, int max_blocks, int64_t num_blocks,
-                          int k_bits, int v_bits, uint16_t* out, void* scratch, unsigned* flags,
+                          int k_bits, int v_bits, bool lean, uint16_t* out, void* scratch, unsigned* flags,
                           cudaStream_t stream);
 
 // Device scratch of launch_decode: tile prefix per sequence + partial records.

@@ -286,7 +286,7 @@ __device__ __forceinline__ float div_sqrt(float v, float u) {
 // writes the group's stage (codes + metadata). `tile` is the item's fp16 operand
 // (canonical layout), `line`/`p` locate the thread's half line, `ta1`/`ta2` are
 // its TMEM addresses of D1 and D2.
-template <int kKind, int kBits>
+template <int kKind, int kBits, bool kLean>
 __device__ __forceinline__ bool quantize_group(float* vec, uint8_t* stage, const uint8_t* tile, uint32_t ta1,
                                                uint32_t ta2, int line, int p, int n_iters, float eps, int bar_id,
                                                bool ok) {
@@ -345,10 +345,16 @@ __device__ __forceinline__ bool quantize_group(float* vec, uint8_t* stage, const
   if (p == 0) {
     const uint16_t rb = f2h_bits(clampf(1.0f / va[pl], kFp16MinNormal, kFp16Max));
     const uint16_t cb = f2h_bits(clampf(1.0f / vb[pl], kFp16MinNormal, kFp16Max));
-    meta[0 * 128 + line] = rb;
-    meta[1 * 128 + line] = cb;
-    vg[pl] = kInvSqrt128 / h2f_bits(rb);   // the +-1 transform's 2^-3.5 is folded here
-    vh[pl] = 1.0f / h2f_bits(cb);
+    // the +-1 transform's 2^-3.5 is folded into g; lean metadata keeps c for keys and r
+    // for values, and the other scale (constant in each group) is folded into s, z
+    if (!kLean) {
+      meta[0 * 128 + line] = rb;
+      meta[1 * 128 + line] = cb;
+    } else {
+      meta[line] = kKind == 0 ? cb : rb;
+    }
+    vg[pl] = (kLean && kKind == 0) ? kInvSqrt128 : kInvSqrt128 / h2f_bits(rb);
+    vh[pl] = (kLean && kKind == 1) ? 1.0f : 1.0f / h2f_bits(cb);
   }
   named_bar(bar_id, kGroupThreads);
 
@@ -383,8 +389,8 @@ __device__ __forceinline__ bool quantize_group(float* vec, uint8_t* stage, const
       const float z = h2f_bits(zb);
       const uint16_t sbits = f2h_bits(clampf(fmaxf(mx - z, 0.0f) / kLevels, kFp16MinNormal, kFp16Max));
       const float inv_s = 1.0f / h2f_bits(sbits);
-      meta[2 * 128 + line] = sbits;
-      meta[3 * 128 + line] = zb;
+      meta[(kLean ? 1 : 2) * 128 + line] = sbits;
+      meta[(kLean ? 2 : 3) * 128 + line] = zb;
       vw[pl] = (kKind == 0 ? vg[pl] : vh[pl]) * inv_s * (1.0f / kLevels);
       vc0[pl] = fmaf(-z, inv_s, 0.5f) * (1.0f / kLevels);
     }
@@ -469,7 +475,7 @@ __device__ __forceinline__ bool quantize_group(float* vec, uint8_t* stage, const
 
 // 104 registers a thread (the 512 threads could hold 128): measured faster on the
 // prefill workload than 88, 96 or 128.
-template <class Src, int KB, int VB>
+template <class Src, int KB, int VB, bool kLean>
 __global__ void __maxnreg__(104)
     quantize_kernel(const __grid_constant__ Src src, uint8_t* __restrict__ cache, int n_iters, float eps,
                     unsigned* flags) {
@@ -582,9 +588,9 @@ __global__ void __maxnreg__(104)
       tc_fence_after();
       const uint8_t* tile = tiles + buf * kTileOp;
       if (grp == 0)
-        ok = quantize_group<0, KB>(vec, stage, tile, ta1, ta2, line, p, n_iters, eps, bar_id, ok);
+        ok = quantize_group<0, KB, kLean>(vec, stage, tile, ta1, ta2, line, p, n_iters, eps, bar_id, ok);
       else
-        ok = quantize_group<1, VB>(vec, stage, tile, ta1, ta2, line, p, n_iters, eps, bar_id, ok);
+        ok = quantize_group<1, VB, kLean>(vec, stage, tile, ta1, ta2, line, p, n_iters, eps, bar_id, ok);
       if (!ok) break;                     // a copy or the tensor core never signalled (flag raised)
       fence_proxy_async_smem();
       tc_fence_before();
@@ -593,15 +599,15 @@ __global__ void __maxnreg__(104)
     const bool next_ok = named_bar_and(bar_id, kGroupThreads, !has_next || src.check_ok(check_next, gt));
     tc_fence_after();
     if (dst >= 0 && gt == 0) {
-      using L = RecordLayout<KB, VB>;
+      using L = RecordLayout<KB, VB, kLean>;
       uint8_t* stage = smem + (grp == 0 ? S::kOffStageK + buf * S::kStageK : S::kOffStageV + buf * S::kStageV);
       uint8_t* rec = cache + dst * static_cast<int64_t>(L::kBytes);
       if (grp == 0) {
         bulk_s2g(rec + L::kKCodeOff, stage, L::kKCodeBytes);
-        bulk_s2g(rec + L::kKMetaOff, stage + L::kKCodeBytes, 1024);
+        bulk_s2g(rec + L::kKMetaOff, stage + L::kKCodeBytes, L::kMetaBytes);
       } else {
         bulk_s2g(rec + L::kVCodeOff, stage, L::kVCodeBytes);
-        bulk_s2g(rec + L::kVMetaOff, stage + L::kVCodeBytes, 1024);
+        bulk_s2g(rec + L::kVMetaOff, stage + L::kVCodeBytes, L::kMetaBytes);
       }
       bulk_commit();
     }
@@ -634,29 +640,34 @@ int sm_count() {
   return n > 0 ? n : 1;
 }
 
-template <class Src, int KB, int VB>
+template <class Src, int KB, int VB, bool kLean>
 cudaError_t launch_quantize_bits(const Src& src, uint8_t* cache, int n_iters, float eps, unsigned* flags,
                             cudaStream_t stream, int max_ctas) {
   if (src.n_items <= 0) return cudaSuccess;
   if (src.n_items > INT32_MAX) return cudaErrorInvalidValue;
   static std::atomic<unsigned long long> smem_set{0};
-  cudaError_t err = set_smem_once(quantize_kernel<Src, KB, VB>, QSmem<KB, VB>::kBytes, smem_set);
+  cudaError_t err = set_smem_once(quantize_kernel<Src, KB, VB, kLean>, QSmem<KB, VB>::kBytes, smem_set);
   if (err != cudaSuccess) return err;
   int64_t grid = sm_count();
   if (max_ctas > 0 && grid > max_ctas) grid = max_ctas;
   if (grid > src.n_items) grid = src.n_items;
-  quantize_kernel<Src, KB, VB><<<static_cast<unsigned>(grid), kThreads, QSmem<KB, VB>::kBytes, stream>>>(src, cache, n_iters, eps,
+  quantize_kernel<Src, KB, VB, kLean><<<static_cast<unsigned>(grid), kThreads, QSmem<KB, VB>::kBytes, stream>>>(src, cache, n_iters, eps,
                                                                                              flags);
   return cudaGetLastError();
 }
 
-// The kernel instance of a preset (k4v2, k4v4, k2v2).
+// The kernel instance of a preset (k4v2, k4v4, k2v2; k4v2 with lean metadata).
 template <class Src>
-cudaError_t launch_quantize(const Src& src, uint8_t* cache, int k_bits, int v_bits, int n_iters, float eps,
+cudaError_t launch_quantize(const Src& src, uint8_t* cache, int k_bits, int v_bits, bool lean, int n_iters, float eps,
                             unsigned* flags, cudaStream_t stream, int max_ctas) {
-  if (k_bits == 4 && v_bits == 2) return launch_quantize_bits<Src, 4, 2>(src, cache, n_iters, eps, flags, stream, max_ctas);
-  if (k_bits == 4 && v_bits == 4) return launch_quantize_bits<Src, 4, 4>(src, cache, n_iters, eps, flags, stream, max_ctas);
-  if (k_bits == 2 && v_bits == 2) return launch_quantize_bits<Src, 2, 2>(src, cache, n_iters, eps, flags, stream, max_ctas);
+  if (k_bits == 4 && v_bits == 2 && !lean)
+    return launch_quantize_bits<Src, 4, 2, false>(src, cache, n_iters, eps, flags, stream, max_ctas);
+  if (k_bits == 4 && v_bits == 2 && lean)
+    return launch_quantize_bits<Src, 4, 2, true>(src, cache, n_iters, eps, flags, stream, max_ctas);
+  if (k_bits == 4 && v_bits == 4 && !lean)
+    return launch_quantize_bits<Src, 4, 4, false>(src, cache, n_iters, eps, flags, stream, max_ctas);
+  if (k_bits == 2 && v_bits == 2 && !lean)
+    return launch_quantize_bits<Src, 2, 2, false>(src, cache, n_iters, eps, flags, stream, max_ctas);
   return cudaErrorInvalidValue;
 }
 
@@ -697,8 +708,8 @@ cudaError_t tile_map(CUtensorMap* m, const void* base, uint64_t row_elems, uint6
 }  // namespace
 
 cudaError_t launch_quantize_prefill(const uint16_t* k, const uint16_t* v, const int64_t* slot, int64_t n_tokens,
-                                    int hkv, int64_t num_blocks, uint8_t* cache, int k_bits, int v_bits, int n_iters,
-                                    float eps, unsigned* flags, cudaStream_t stream, int max_ctas) {
+                                    int hkv, int64_t num_blocks, uint8_t* cache, int k_bits, int v_bits, bool lean,
+                                    int n_iters, float eps, unsigned* flags, cudaStream_t stream, int max_ctas) {
   PrefillSource src{};
   cudaError_t err = tile_map(&src.map[0], k, static_cast<uint64_t>(hkv) * kD, static_cast<uint64_t>(n_tokens));
   if (err == cudaSuccess)
@@ -708,13 +719,13 @@ cudaError_t launch_quantize_prefill(const uint16_t* k, const uint16_t* v, const 
   src.n_items = (n_tokens / kB) * hkv;
   src.hkv = hkv;
   src.num_blocks = num_blocks;
-  return launch_quantize(src, cache, k_bits, v_bits, n_iters, eps, flags, stream, max_ctas);
+  return launch_quantize(src, cache, k_bits, v_bits, lean, n_iters, eps, flags, stream, max_ctas);
 }
 
 cudaError_t launch_append(const uint16_t* k_new, const uint16_t* v_new, const int32_t* seq_lens,
                           int32_t* seq_lens_out, const int32_t* block_tables, int n_seqs, int hkv, int max_blocks,
-                          int64_t num_blocks, uint16_t* ws, uint8_t* cache, int k_bits, int v_bits, int n_iters,
-                          float eps, unsigned* flags, cudaStream_t stream) {
+                          int64_t num_blocks, uint16_t* ws, uint8_t* cache, int k_bits, int v_bits, bool lean,
+                          int n_iters, float eps, unsigned* flags, cudaStream_t stream) {
   if (n_seqs <= 0) return cudaSuccess;
   if (static_cast<int64_t>(n_seqs) * hkv * 2 * kB > INT32_MAX) return cudaErrorInvalidValue;
   AppendSource src{};
@@ -730,7 +741,7 @@ cudaError_t launch_append(const uint16_t* k_new, const uint16_t* v_new, const in
   src.hkv = hkv;
   src.max_blocks = max_blocks;
   src.num_blocks = num_blocks;
-  return launch_quantize(src, cache, k_bits, v_bits, n_iters, eps, flags, stream, 0);
+  return launch_quantize(src, cache, k_bits, v_bits, lean, n_iters, eps, flags, stream, 0);
 }
 
 }  // namespace kvarn

@@ -70,7 +70,7 @@ MIS = ctypes.c_void_p(0x10008)        # not 16-byte aligned
 @pytest.mark.parametrize("field,value,status", [
     ("head_dim", 64, 2), ("block_size", 16, 2), ("k_bits", 3, 2), ("v_bits", 3, 2), ("v_bits", 8, 2),
     ("num_q_heads", 12, 1), ("n_iters", 0, 1), ("n_iters", 17, 1), ("num_kv_heads", 0, 1),
-    ("reserved", 1, 1),
+    ("layout", 2, 1),
 ])
 def test_quantize_rejects_bad_meta(kv, field, value, status):
     m = kv.make_meta(8, 64, 16)
@@ -116,7 +116,8 @@ def test_decode_rejects_small_scratch(kv):
 
 
 def test_presets_are_accepted_and_sized(kv):
-    for preset, (kb, vb), rec in (("k4v2", (4, 2), 14336), ("k4v4", (4, 4), 18432), ("k2v2", (2, 2), 10240)):
+    for preset, (kb, vb), rec in (("k4v2", (4, 2), 14336), ("k4v4", (4, 4), 18432), ("k2v2", (2, 2), 10240),
+                                  ("k4v2l", (4, 2), 13824)):
         meta = kv.make_meta(8, 64, 10, preset=preset)
         assert (meta.k_bits, meta.v_bits) == (kb, vb)
         assert kv.meta_record_bytes(meta) == rec
@@ -124,3 +125,11 @@ def test_presets_are_accepted_and_sized(kv):
     meta = kv.make_meta(8, 64, 10)
     meta.k_bits, meta.v_bits = 2, 4            # not a preset
     assert kv.meta_record_bytes(meta) == 0 and kv.cache_bytes(meta) == 0
+
+
+def test_lean_layout_only_with_k4v2(kv):
+    meta = kv.make_meta(2, 2, 4, preset="k4v4")
+    meta.layout = kv.KVARN_LAYOUT_LEAN
+    assert kv.meta_record_bytes(meta) == 0
+    st = _raw(kv, "kvarn_quantize_tiles")(None, None, None, 0, None, ctypes.byref(meta), None)
+    assert st == 2                      # KVARN_EUNSUPPORTED

@@ -1,4 +1,4 @@
-"""Parity of the k4v4 and k2v2 presets (quantize, decode, append; CUDA through the
+"""Parity of the k4v4, k2v2 and k4v2l presets (quantize, decode, append; CUDA through the
 C ABI) with the CPU oracle, under the same tolerances as the default preset."""
 import numpy as np
 import pytest
@@ -9,7 +9,7 @@ from tests.parity import assert_decode_close, compare_records
 
 pytestmark = pytest.mark.gpu
 
-PRESETS = ["k4v4", "k2v2"]
+PRESETS = ["k4v4", "k2v2", "k4v2l"]
 
 
 @pytest.fixture(scope="module")
