@@ -456,6 +456,46 @@ def decode(q, cache, workspace, block_tables, seq_lens, pairs=None):
     return out
 
 
+def prefill_attention(q, k_new, v_new, cu_tokens, seq_lens, block_tables, workspace, cache, tokens=None):
+    """Chunked-prefill attention (kvarn_prefill_attention) [R]: sequence s has
+    L0 = seq_lens[s] tokens in the cache (floor(L0/128) packed tiles read through
+    its block table, then L0 % 128 tokens in its fp16 workspace) and appends the
+    chunk of fresh fp16 tokens cu_tokens[s] .. cu_tokens[s+1] - 1 of k_new, v_new
+    [n_tokens, Hkv, 128]. Chunk token p (0-based) attends the L0 cached tokens and
+    chunk tokens 0..p (causal), with the decode's softmax scale and GQA mapping.
+
+    q: [n_tokens, Hq, 128]; returns float64 [n_tokens, Hq, 128]. `tokens`, if given,
+    restricts the work to a list of (token, kv-head) pairs (other rows are NaN)."""
+    n_tokens, hq, _ = q.shape
+    hkv = k_new.shape[1]
+    g = hq // hkv
+    out = np.full(q.shape, np.nan)
+    seq_of = np.searchsorted(np.asarray(cu_tokens), np.arange(n_tokens), side="right") - 1
+    work = tokens if tokens is not None else [(t, h) for t in range(n_tokens) for h in range(hkv)]
+    ctx = {}
+    for t, h in work:
+        s = int(seq_of[t])
+        if (s, h) not in ctx:                    # cached tokens of (s, h), un-rotated
+            L0 = int(seq_lens[s])
+            n_full, n_ws = L0 // B, L0 % B
+            ks, vs = [np.zeros((0, D))], [np.zeros((0, D))]
+            if n_full:
+                kh, vh = dequant_record(cache[np.asarray(block_tables[s, :n_full], np.int64), h])
+                ks.append(np.swapaxes(kh, -1, -2).reshape(-1, D))
+                vs.append(np.swapaxes(vh, -1, -2).reshape(-1, D))
+            if n_ws:
+                ks.append(np.asarray(workspace[s, h, 0, :n_ws], np.float64))
+                vs.append(np.asarray(workspace[s, h, 1, :n_ws], np.float64))
+            ctx[(s, h)] = (np.concatenate(ks), np.concatenate(vs))
+        kc, vc = ctx[(s, h)]
+        t0 = int(cu_tokens[s])
+        kf = np.asarray(k_new[t0:t + 1, h], np.float64)
+        vf = np.asarray(v_new[t0:t + 1, h], np.float64)
+        out[t, h * g:(h + 1) * g] = attend(np.asarray(q[t, h * g:(h + 1) * g], np.float64),
+                                           np.concatenate([kc, kf]), np.concatenate([vc, vf]))
+    return out
+
+
 def append(k_new, v_new, seq_lens, block_tables, workspace, cache):
     """Decode-step write (kvarn_append_decode): for each sequence s with L =
     seq_lens[s] tokens, store the new token in workspace[s, :, :, L % 128]; when

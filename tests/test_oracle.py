@@ -506,3 +506,68 @@ def test_lean_preset_folds_the_in_group_scale():
     for a, b in ((kl, kfull), (vl, vfull)):
         rel = np.linalg.norm(a - b) / np.linalg.norm(b)
         assert rel < 0.05, rel
+
+
+# ----------------------------------------------------------------------------------
+# Chunked-prefill attention over the packed cache plus the fresh chunk
+# ----------------------------------------------------------------------------------
+def _prefill_case(seed, lens, chunks, hkv=2, g=2, preset="k4v2"):
+    rng = np.random.default_rng(seed)
+    n_seqs = len(lens)
+    max_blocks = max(1, max(L // 128 for L in lens))
+    num_blocks = n_seqs * max_blocks
+    bt = synth.block_tables(n_seqs, max_blocks, num_blocks, seed)
+    cache = np.zeros((num_blocks, hkv, o.LAYOUTS[preset].record_bytes), np.uint8)
+    ws = np.zeros((n_seqs, hkv, 2, 128, 128), np.float16)
+    for s, L in enumerate(lens):
+        k, v = synth.prefill_kv(max(L, 1), hkv, seed=seed * 10 + s)
+        nf = L // 128
+        if nf:
+            slots = np.concatenate([bt[s, b] * 128 + np.arange(128) for b in range(nf)]).astype(np.int64)
+            o.quantize_into_cache(k[:nf * 128], v[:nf * 128], slots, cache)
+        ws[s, :, 0, :L % 128] = k[nf * 128:L].transpose(1, 0, 2)
+        ws[s, :, 1, :L % 128] = v[nf * 128:L].transpose(1, 0, 2)
+    cu = np.concatenate([[0], np.cumsum(chunks)]).astype(np.int32)
+    kn, vn = synth.prefill_kv(int(cu[-1]), hkv, seed=seed + 99)
+    q = rng.standard_normal((int(cu[-1]), hkv * g, 128)).astype(np.float16)
+    return q, kn, vn, cu, np.asarray(lens, np.int32), bt, ws, cache
+
+
+def test_prefill_one_token_chunk_equals_append_then_decode():
+    """A chunk of one token is a decode step: append the token, then decode over
+    L0 + 1 tokens (when L0 % 128 < 127 the token stays in the workspace)."""
+    q, kn, vn, cu, lens, bt, ws, cache = _prefill_case(3, [300, 0, 17], [1, 1, 1])
+    got = o.prefill_attention(q, kn, vn, cu, lens, bt, ws, cache)
+    ws2, cache2, lens2 = o.append(kn, vn, lens, bt, ws, cache)
+    want = o.decode(q.astype(np.float64), cache2, ws2, bt, lens2)
+    assert np.allclose(got, want, rtol=1e-12, atol=1e-12)
+
+
+def test_prefill_on_empty_cache_is_causal_attention():
+    """With nothing cached the chunk attends itself with a causal mask: compare with
+    softmax(Q K^T / sqrt(128) + mask) V written out on the fp16 inputs."""
+    q, kn, vn, cu, lens, bt, ws, cache = _prefill_case(4, [0], [37], hkv=1, g=3)
+    got = o.prefill_attention(q, kn, vn, cu, lens, bt, ws, cache)
+    k = kn[:, 0].astype(np.float64)
+    v = vn[:, 0].astype(np.float64)
+    for h in range(3):
+        qq = q[:, h].astype(np.float64)
+        sc = qq @ k.T / math.sqrt(128) + np.triu(np.full((37, 37), -np.inf), 1)
+        p = np.exp(sc - sc.max(axis=1, keepdims=True))
+        want = (p / p.sum(axis=1, keepdims=True)) @ v
+        assert np.allclose(got[:, h], want, rtol=1e-12, atol=1e-12)
+
+
+def test_prefill_is_causal_and_reads_the_cache():
+    """Changing chunk token p's key and value moves outputs p.. only; a chunk token
+    sees every cached token (changing one cached tile moves the first output)."""
+    q, kn, vn, cu, lens, bt, ws, cache = _prefill_case(5, [256 + 40], [9])
+    base = o.prefill_attention(q, kn, vn, cu, lens, bt, ws, cache)
+    kn2, vn2 = kn.copy(), vn.copy()
+    kn2[4] *= -1
+    vn2[4] += np.float16(1)
+    moved = o.prefill_attention(q, kn2, vn2, cu, lens, bt, ws, cache)
+    assert np.array_equal(moved[:4], base[:4]) and not np.allclose(moved[4:], base[4:])
+    cache2 = cache.copy()
+    cache2[bt[0, 1]] = cache[bt[0, 0]]            # tile 1 := tile 0
+    assert not np.allclose(o.prefill_attention(q, kn, vn, cu, lens, bt, ws, cache2)[0], base[0])
