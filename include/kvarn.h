@@ -248,6 +248,32 @@ KVARN_API kvarn_status kvarn_decode_attention_static(const uint16_t* q, const ui
                                                      const int32_t* seq_lens, int32_t n_seqs, uint16_t* out,
                                                      const kvarn_meta* meta, void* stream);
 
+/*
+ * Chunked-prefill attention, a reading of this library (the pages are silent on
+ * prefill over a quantized cache): each sequence s has L0 = seq_lens[s] tokens
+ * in the cache (floor(L0/128) packed tiles through block_tables, then L0 % 128
+ * workspace tokens) and a chunk of fresh tokens cu_tokens[s] .. cu_tokens[s+1]-1
+ * of k_new / v_new. Chunk token p attends the L0 cached tokens and chunk tokens
+ * 0..p (causal), with the decode's softmax scale and GQA mapping; packed tiles
+ * are read with their scales re-applied and q rotated by H (stage 2), fresh and
+ * workspace tokens exactly. The chunk is not written to the cache (quantize it
+ * with kvarn_quantize_tiles / kvarn_append_decode as it fills tiles).
+ *   q, out        fp16 [n_tokens][num_q_heads][128], n_tokens = cu_tokens[n_seqs].
+ *   k_new, v_new  fp16 [n_tokens][num_kv_heads][128].
+ *   cu_tokens     int32 [n_seqs + 1], non-decreasing, cu_tokens[0] = 0.
+ *   seq_lens      int32 [n_seqs], cached tokens before each chunk.
+ *   n_seqs        0..65535. max_chunk: an upper bound of every chunk length
+ *                 (sets the grid; tokens of a longer chunk are not computed).
+ *   workspace     fp16 workspace or NULL (then L0 % 128 tokens are not attended
+ *                 and KVARN_FLAG_BAD_LENGTH is raised).
+ * One launch; no scratch. Every preset of kvarn_meta is supported.
+ */
+KVARN_API kvarn_status kvarn_prefill_attention(const uint16_t* q, const uint16_t* k_new, const uint16_t* v_new,
+                                     const int32_t* cu_tokens, const int32_t* seq_lens, int32_t n_seqs,
+                                     int32_t max_chunk, const int32_t* block_tables, const uint8_t* cache,
+                                     const uint16_t* workspace, uint16_t* out, const kvarn_meta* meta,
+                                     void* stream);
+
 /* Copies the device flag word of the current device to *flags (host pointer)
  * after synchronising `stream`, then clears it. */
 KVARN_API kvarn_status kvarn_device_flags(uint32_t* flags, void* stream);

@@ -39,6 +39,10 @@ _SIGS = {
     "kvarn_decode_attention_static": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                                      ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
                                                      ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
+    "kvarn_prefill_attention": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                               ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p,
+                                               ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                               ctypes.c_void_p]),
     "kvarn_device_flags": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32), ctypes.c_void_p]),
     "kvarn_last_error": (ctypes.c_char_p, []),
 }
@@ -197,6 +201,22 @@ def kvarn_decode_attention_static(q, cache, workspace, block_tables, seq_lens, o
                                               _ptr(block_tables, "block_tables", torch.int32),
                                               _ptr(seq_lens, "seq_lens", torch.int32, n), n,
                                               _ptr(out, "out", torch.float16), ctypes.byref(meta), _stream(stream)))
+
+
+def kvarn_prefill_attention(q, k_new, v_new, cu_tokens, seq_lens, max_chunk: int, block_tables, cache, workspace,
+                            out, meta: KvarnMeta, stream=None):
+    """Chunked prefill: q, out fp16 [n_tokens, Hq, 128]; k_new, v_new fp16
+    [n_tokens, Hkv, 128]; cu_tokens int32 [n_seqs + 1]; seq_lens int32 [n_seqs]
+    (cached tokens before each chunk); max_chunk >= every chunk length."""
+    import torch
+    n = int(seq_lens.shape[0])
+    _check(_lib.kvarn_prefill_attention(_ptr(q, "q", torch.float16), _ptr(k_new, "k_new", torch.float16),
+                                        _ptr(v_new, "v_new", torch.float16),
+                                        _ptr(cu_tokens, "cu_tokens", torch.int32, n + 1),
+                                        _ptr(seq_lens, "seq_lens", torch.int32, n), n, int(max_chunk),
+                                        _ptr(block_tables, "block_tables", torch.int32),
+                                        _ptr(cache, "cache", torch.uint8), _ptr(workspace, "workspace", torch.float16),
+                                        _ptr(out, "out", torch.float16), ctypes.byref(meta), _stream(stream)))
 
 
 def kvarn_device_flags(stream=None) -> int:

@@ -184,6 +184,38 @@ kvarn_status kvarn_decode_attention(const uint16_t* q, const uint8_t* cache, con
                      "kvarn_decode_attention");
 }
 
+kvarn_status kvarn_prefill_attention(const uint16_t* q, const uint16_t* k_new, const uint16_t* v_new,
+                                     const int32_t* cu_tokens, const int32_t* seq_lens, int32_t n_seqs,
+                                     int32_t max_chunk, const int32_t* block_tables, const uint8_t* cache,
+                                     const uint16_t* workspace, uint16_t* out, const kvarn_meta* meta,
+                                     void* stream) {
+  g_err[0] = 0;
+  KV_TRY(check_meta(meta));
+  if (n_seqs < 0 || n_seqs > 65535) return fail(KVARN_EINVAL, "n_seqs must be in 0..65535 (got %lld)", (long long)n_seqs);
+  if (max_chunk < 0) return fail(KVARN_EINVAL, "max_chunk must be >= 0 (got %lld)", (long long)max_chunk);
+  if (n_seqs == 0 || max_chunk == 0) return KVARN_OK;
+  KV_TRY(need_ptr(q, "q"));
+  KV_TRY(need_ptr(k_new, "k_new"));
+  KV_TRY(need_ptr(v_new, "v_new"));
+  KV_TRY(need_ptr(cu_tokens, "cu_tokens"));
+  KV_TRY(need_ptr(seq_lens, "seq_lens"));
+  KV_TRY(need_ptr(out, "out"));
+  if (meta->max_blocks_per_seq > 0) {
+    KV_TRY(need_ptr(cache, "cache"));
+    KV_TRY(need_ptr(block_tables, "block_tables"));
+  }
+  if (workspace != nullptr) KV_TRY(need_ptr(workspace, "workspace"));
+  unsigned* fl = nullptr;
+  KV_TRY(flags_ptr(&fl));
+  return cuda_status(kvarn::launch_prefill(q, k_new, v_new, cu_tokens, seq_lens, block_tables, cache, workspace,
+                                           n_seqs, max_chunk, meta->num_kv_heads,
+                                           meta->num_q_heads / meta->num_kv_heads, meta->max_blocks_per_seq,
+                                           meta->num_blocks, meta->k_bits, meta->v_bits,
+                                           meta->layout == KVARN_LAYOUT_LEAN, out, fl,
+                                           static_cast<cudaStream_t>(stream)),
+                     "kvarn_prefill_attention");
+}
+
 kvarn_status kvarn_device_flags(uint32_t* flags, void* stream) {
   g_err[0] = 0;
   if (flags == nullptr) return fail(KVARN_EINVAL, "flags is NULL");

@@ -40,6 +40,12 @@ cudaError_t launch_decode(const uint16_t* q, const uint8_t* cache, const uint16_
                           int k_bits, int v_bits, bool lean, uint16_t* out, void* scratch, unsigned* flags,
                           cudaStream_t stream);
 
+cudaError_t launch_prefill(const uint16_t* q, const uint16_t* k_new, const uint16_t* v_new, const int32_t* cu_tokens,
+                           const int32_t* seq_lens, const int32_t* block_tables, const uint8_t* cache,
+                           const uint16_t* ws, int n_seqs, int max_chunk, int hkv, int group, int max_blocks,
+                           int64_t num_blocks, int k_bits, int v_bits, bool lean, uint16_t* out, unsigned* flags,
+                           cudaStream_t stream);
+
 // Device scratch of launch_decode: tile prefix per sequence + partial records.
 size_t decode_part_bytes(int n_seqs, int hkv, int max_blocks);
 // Scratch launch_decode touches when the split kernel runs `n_ctas` CTAs (the
