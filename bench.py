@@ -131,7 +131,7 @@ class ClockSampler:
 # sources a kernel's profile summary was captured from (hashed together, in order)
 PROFILE_SOURCES = {
     "quantize": ["quantize.cu", "kvarn_tc.cuh", "kvarn_common.cuh"],
-    "decode": ["decode.cu", "kvarn_common.cuh"],
+    "decode": ["decode.cu", "kvarn_common.cuh", "kvarn_frag.cuh"],
 }
 
 
