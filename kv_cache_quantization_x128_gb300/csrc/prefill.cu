@@ -30,9 +30,9 @@ constexpr int kTileBytes = 128 * kPitch * 2;
 constexpr int kMaxRec = 18432;                    // largest record (k4v4)
 constexpr int kOffK = 0;                          // fp16 [128][kPitch]
 constexpr int kOffV = kOffK + kTileBytes;         // fp16 [128][kPitch]
-constexpr int kOffRec = kOffV + kTileBytes;       // packed record
-constexpr int kOffScale = kOffRec + kMaxRec;      // fp32 [6][128]
-constexpr int kOffCtl = kOffScale + 6 * 128 * 4;  // mbarrier, tile-valid word
+constexpr int kOffRec = kOffV + kTileBytes;       // packed records [2] (the next one in flight)
+constexpr int kOffScale = kOffRec + 2 * kMaxRec;  // fp32 [6][128]
+constexpr int kOffCtl = kOffScale + 6 * 128 * 4;  // mbarriers [2]
 constexpr int kPSmem = kOffCtl + 16;
 constexpr float kLog2eP = 1.4426950408889634f;
 
@@ -356,7 +356,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(PrefillArgs a) {
   uint16_t* vs = reinterpret_cast<uint16_t*>(smem + kOffV);
   uint8_t* rec = smem + kOffRec;
   float* sc = reinterpret_cast<float*>(smem + kOffScale);
-  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kOffCtl);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kOffCtl);      // [2]
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, c = lane & 3;
   const int h = blockIdx.y, s = blockIdx.z;
@@ -376,7 +376,8 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(PrefillArgs a) {
     if (tid == 0 && blockIdx.x == 0 && h == 0) raise_flag(a.flags, KVARN_FLAG_BAD_LENGTH);
   }
   if (tid == 0) {
-    mbar_init(bar, 1);
+    mbar_init(&bar[0], 1);
+    mbar_init(&bar[1], 1);
     fence_mbar_init();
   }
   __syncthreads();
@@ -391,32 +392,54 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(PrefillArgs a) {
   // packed tiles, rotated domain: q_r = H q * log2(e) / sqrt(128), as FWHT(q) * log2(e) / 128
   load_q_frag(a, tok, h, g, c, kLog2eP / 128.0f, qv);
   fwht_q(qv, c);
-  uint32_t phase = 0;
-  bool alive = true;
-  for (int ti = 0; ti < n_full; ++ti) {
+  // thread 0 starts the copy of packed tile ti into record buffer b; false (and the
+  // flag) for a block index outside the cache. Same answer in every thread.
+  auto prefetch = [&](int ti, int b) {
     const int64_t blk = a.block_tables[static_cast<int64_t>(s) * a.max_blocks + ti];
-    const bool valid = blk >= 0 && blk < a.num_blocks;               // same for every thread
-    if (!valid) {
-      if (tid == 0) raise_flag(a.flags, KVARN_FLAG_BAD_BLOCK);
-      continue;
-    }
+    const bool valid = blk >= 0 && blk < a.num_blocks;
     if (tid == 0) {
-      mbar_arrive_expect_tx(bar, L::kBytes);
-      bulk_g2s(rec, a.cache + (blk * a.hkv + h) * static_cast<int64_t>(L::kBytes), L::kBytes, bar);
+      if (valid) {
+        mbar_arrive_expect_tx(&bar[b], L::kBytes);
+        bulk_g2s(rec + b * kMaxRec, a.cache + (blk * a.hkv + h) * static_cast<int64_t>(L::kBytes), L::kBytes,
+                 &bar[b]);
+      } else {
+        raise_flag(a.flags, KVARN_FLAG_BAD_BLOCK);
+      }
     }
-    const bool ok = mbar_wait(bar, phase, a.flags);
-    phase ^= 1u;
-    if (!__syncthreads_and(ok)) {         // the copy never arrived (flag raised): stop
-      alive = false;
-      break;
+    return valid;
+  };
+  uint32_t phase = 0;                     // bit b: parity of record buffer b's barrier
+  uint32_t pending = 0;                   // bit b: a copy into buffer b not yet waited for
+  bool alive = true;
+  bool cur = n_full > 0 && prefetch(0, 0);
+  if (cur) pending |= 1u;
+  for (int ti = 0; ti < n_full; ++ti) {
+    const int b = ti & 1;
+    // the next tile's copy overlaps this one's work (buffer b ^ 1 was last read by
+    // the unpack of tile ti - 1, before the barrier that followed it)
+    const bool next = ti + 1 < n_full && prefetch(ti + 1, b ^ 1);
+    if (next) pending |= 2u >> b;
+    if (cur) {
+      const bool ok = mbar_wait(&bar[b], (phase >> b) & 1u, a.flags);
+      if (ok) {
+        phase ^= 1u << b;
+        pending &= ~(1u << b);
+      }
+      if (!__syncthreads_and(ok)) {       // the copy never arrived (flag raised): stop
+        alive = false;
+        break;
+      }
+      unpack_tile<KB, VB, kLean>(rec + b * kMaxRec, ks, vs, sc, tid);
+      __syncthreads();
+      if (active) attend_block<true>(ks, vs, sc, qv, g, c, lane, 0, m_run, l_run, acc);
+      __syncthreads();                    // shared tiles and record buffer b are rewritten next
     }
-    unpack_tile<KB, VB, kLean>(rec, ks, vs, sc, tid);
-    __syncthreads();
-    if (active) attend_block<true>(ks, vs, sc, qv, g, c, lane, 0, m_run, l_run, acc);
-    __syncthreads();                      // shared tiles are rewritten next
+    cur = next;
   }
   if (!alive) {
-    if (tid == 0) mbar_wait(bar, phase, a.flags);   // let a late copy land before the CTA exits
+    if (tid == 0)                         // let copies still in flight land before the CTA exits
+      for (int b = 0; b < 2; ++b)
+        if ((pending >> b) & 1u) mbar_wait(&bar[b], (phase >> b) & 1u, a.flags);
     return;
   }
 
