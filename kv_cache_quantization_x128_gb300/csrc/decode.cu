@@ -4,10 +4,11 @@
 //
 // Three launches:
 //   decode_scan_kernel  - exclusive prefix of full tiles per sequence (scratch);
-//   decode_split_kernel - persistent, one CTA per SM, 7 warps. The flattened tile
-//     space (sequence, kv-head, tile) is cut into one contiguous range per warp
-//     (stream-K), so ragged batches balance to a tile. Each warp streams its
-//     range through two private 14336-byte bulk-copy (TMA) stages and runs its
+//   decode_split_kernel - persistent, one CTA per SM, 8 warps (6 for 4-bit
+//     values). The flattened tile space (sequence, kv-head, tile) is cut into
+//     one contiguous range per warp (stream-K), so ragged batches balance to a
+//     tile. Each warp streams its range through two private record-sized
+//     (14336 bytes for k4v2) bulk-copy (TMA) stages and runs its
 //     GQA group (up to 8 q-heads) on m16n8k16 tensor-core MMAs, with an online
 //     softmax in the log2 domain:
 //       QK^T: A = q' = q_r r^K s^K per channel, fp16 hi part in rows 0-7 and fp16
@@ -30,18 +31,19 @@ namespace kvarn {
 namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr int kMaxWarps = 7;                    // consumer warps per CTA (at most)
+constexpr int kMaxWarps = 8;                    // consumer warps per CTA (at most)
 constexpr int kStages = 2;                      // bulk-copy stages per warp
 constexpr int kMaxCtas = 1024;                  // upper bound used to size scratch
 constexpr int kPartStride = 132;                // floats per q-head: acc[128], max, sum, pad
 constexpr int kRecFloats = 8 * kPartStride;     // one partial record (8 q-head slots)
 
-// Split kernel shape for KB-bit keys and VB-bit values: 7 warps, or 6 when two
-// records per warp would not fit in shared memory (k4v4's 18432-byte records).
+// Split kernel shape for KB-bit keys and VB-bit values: the most warps (8 down to
+// 6) whose two records each fit in shared memory; k4v4's 18432-byte records get 6.
 template <int KB, int VB, bool kLean = false>
 struct SplitCfg {
   using L = RecordLayout<KB, VB, kLean>;
-  static constexpr int kWarps = 7 * kStages * L::kBytes + 7 * kStages * 8 <= 232448 ? 7 : 6;
+  static constexpr int fits(int w) { return w * kStages * L::kBytes + w * kStages * 8 <= 232448; }
+  static constexpr int kWarps = fits(8) ? 8 : fits(7) ? 7 : 6;
   static constexpr int kSmem = kWarps * kStages * L::kBytes + kWarps * kStages * 8;
   static_assert(kSmem <= 232448, "decode stages");
 };
