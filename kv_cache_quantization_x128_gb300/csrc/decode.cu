@@ -214,28 +214,34 @@ __device__ __forceinline__ void attend_tile(const uint8_t* rec, const float (&qv
   const uint16_t* km = reinterpret_cast<const uint16_t*>(rec + L::kKMetaOff);
   const uint16_t* vm = reinterpret_cast<const uint16_t*>(rec + L::kVMetaOff);
 
-  // q' fragments (hi rows g, lo rows g + 8) and beta
+  // q' fragments (hi rows g, lo rows g + 8) and beta (fp32 pairs)
   uint32_t A[8][4];
-  float beta = 0.f;
+  float2 beta2 = make_float2(0.f, 0.f);
 #pragma unroll
   for (int ks = 0; ks < 8; ++ks) {
     const int ch0 = 16 * ks + 2 * c;
-    // lean records fold the key row scale r into s and z
-    const float2 r0 = kLean ? make_float2(1.f, 1.f) : h2pair(km + L::kKr + ch0);
-    const float2 r1 = kLean ? make_float2(1.f, 1.f) : h2pair(km + L::kKr + ch0 + 8);
     const float2 s0 = h2pair(km + L::kKs + ch0), s1 = h2pair(km + L::kKs + ch0 + 8);
     const float2 z0 = h2pair(km + L::kKz + ch0), z1 = h2pair(km + L::kKz + ch0 + 8);
-    split2(qv[ks][0] * (r0.x * s0.x), qv[ks][1] * (r0.y * s0.y), A[ks][0], A[ks][1]);
-    split2(qv[ks][2] * (r1.x * s1.x), qv[ks][3] * (r1.y * s1.y), A[ks][2], A[ks][3]);
-    beta = fmaf(qv[ks][0], r0.x * z0.x, beta);
-    beta = fmaf(qv[ks][1], r0.y * z0.y, beta);
-    beta = fmaf(qv[ks][2], r1.x * z1.x, beta);
-    beta = fmaf(qv[ks][3], r1.y * z1.y, beta);
+    // lean records fold the key row scale r into s and z
+    float2 rs0 = s0, rs1 = s1, rz0 = z0, rz1 = z1;
+    if (!kLean) {
+      const float2 r0 = h2pair(km + L::kKr + ch0), r1 = h2pair(km + L::kKr + ch0 + 8);
+      rs0 = __fmul2_rn(r0, s0);
+      rs1 = __fmul2_rn(r1, s1);
+      rz0 = __fmul2_rn(r0, z0);
+      rz1 = __fmul2_rn(r1, z1);
+    }
+    const float2 qa = make_float2(qv[ks][0], qv[ks][1]), qb = make_float2(qv[ks][2], qv[ks][3]);
+    split2p(__fmul2_rn(qa, rs0), A[ks][0], A[ks][1]);
+    split2p(__fmul2_rn(qb, rs1), A[ks][2], A[ks][3]);
+    beta2 = __ffma2_rn(qa, rz0, beta2);
+    beta2 = __ffma2_rn(qb, rz1, beta2);
   }
-  beta = quad_sum(beta);
+  const float beta = quad_sum(beta2.x + beta2.y);
+  const float2 beta_2 = make_float2(beta, beta);
 
   // scores of tokens 8nt + 2c + {0, 1}, four n-tiles at a time (independent chains)
-  float sc[16][2];
+  float2 sc[16];
 #pragma unroll
   for (int ntg = 0; ntg < 4; ++ntg) {
     float d[4][4];
@@ -286,52 +292,59 @@ __device__ __forceinline__ void attend_tile(const uint8_t* rec, const float (&qv
     for (int j = 0; j < 4; ++j) {
       const int nt = 4 * ntg + j;
       const float2 ck = h2pair(km + L::kKc + 8 * nt + 2 * c);
-      sc[nt][0] = ck.x * ((d[j][0] + d[j][2]) + beta);
-      sc[nt][1] = ck.y * ((d[j][1] + d[j][3]) + beta);
+      sc[nt] = __fmul2_rn(ck, __fadd2_rn(__fadd2_rn(make_float2(d[j][0], d[j][1]), make_float2(d[j][2], d[j][3])),
+                                         beta_2));
     }
   }
 
   // online softmax (log2 domain)
   float tmax = -INFINITY;
 #pragma unroll
-  for (int nt = 0; nt < 16; ++nt) tmax = fmaxf(tmax, fmaxf(sc[nt][0], sc[nt][1]));
+  for (int nt = 0; nt < 16; ++nt) tmax = fmax3f(tmax, sc[nt].x, sc[nt].y);
   tmax = quad_max(tmax);
   const float m_new = fmaxf(m_run, tmax);
   const float corr = ex2(m_run - m_new);
   m_run = m_new;
-  float lsum = 0.f;
+  const float2 mneg = make_float2(-m_new, -m_new);
+  float2 lsum2 = make_float2(0.f, 0.f);
 #pragma unroll
   for (int nt = 0; nt < 16; ++nt) {
-    sc[nt][0] = ex2(sc[nt][0] - m_new);
-    sc[nt][1] = ex2(sc[nt][1] - m_new);
-    lsum += sc[nt][0] + sc[nt][1];
+    const float2 e = __fadd2_rn(sc[nt], mneg);
+    sc[nt] = make_float2(ex2(e.x), ex2(e.y));
+    lsum2 = __fadd2_rn(lsum2, sc[nt]);
   }
-  l_run = fmaf(l_run, corr, lsum);
+  l_run = fmaf(l_run, corr, lsum2.x + lsum2.y);
+  const float2 corr2 = make_float2(corr, corr);
 #pragma unroll
   for (int n = 0; n < 16; ++n) {
-    acc[n][0] *= corr;
-    acc[n][1] *= corr;
+    const float2 v = __fmul2_rn(make_float2(acc[n][0], acc[n][1]), corr2);
+    acc[n][0] = v.x;
+    acc[n][1] = v.y;
   }
 
   // p' fragments and gamma; tokens 16ks + 2c + {0,1} (nt = 2ks) and + {8,9} (nt = 2ks+1)
-  float gamma = 0.f;
+  float2 gamma2 = make_float2(0.f, 0.f);
 #pragma unroll
   for (int ks = 0; ks < 8; ++ks) {
     const int t0 = 16 * ks + 2 * c;
-    // lean records fold the value column scale c into s and z
-    const float2 c0 = kLean ? make_float2(1.f, 1.f) : h2pair(vm + L::kVc + t0);
-    const float2 c1 = kLean ? make_float2(1.f, 1.f) : h2pair(vm + L::kVc + t0 + 8);
     const float2 s0 = h2pair(vm + L::kVs + t0), s1 = h2pair(vm + L::kVs + t0 + 8);
     const float2 z0 = h2pair(vm + L::kVz + t0), z1 = h2pair(vm + L::kVz + t0 + 8);
-    const float p0 = sc[2 * ks][0], p1 = sc[2 * ks][1], p2 = sc[2 * ks + 1][0], p3 = sc[2 * ks + 1][1];
-    split2(p0 * (c0.x * s0.x), p1 * (c0.y * s0.y), A[ks][0], A[ks][1]);
-    split2(p2 * (c1.x * s1.x), p3 * (c1.y * s1.y), A[ks][2], A[ks][3]);
-    gamma = fmaf(p0, c0.x * z0.x, gamma);
-    gamma = fmaf(p1, c0.y * z0.y, gamma);
-    gamma = fmaf(p2, c1.x * z1.x, gamma);
-    gamma = fmaf(p3, c1.y * z1.y, gamma);
+    // lean records fold the value column scale c into s and z
+    float2 cs0 = s0, cs1 = s1, cz0 = z0, cz1 = z1;
+    if (!kLean) {
+      const float2 c0 = h2pair(vm + L::kVc + t0), c1 = h2pair(vm + L::kVc + t0 + 8);
+      cs0 = __fmul2_rn(c0, s0);
+      cs1 = __fmul2_rn(c1, s1);
+      cz0 = __fmul2_rn(c0, z0);
+      cz1 = __fmul2_rn(c1, z1);
+    }
+    split2p(__fmul2_rn(sc[2 * ks], cs0), A[ks][0], A[ks][1]);
+    split2p(__fmul2_rn(sc[2 * ks + 1], cs1), A[ks][2], A[ks][3]);
+    gamma2 = __ffma2_rn(sc[2 * ks], cz0, gamma2);
+    gamma2 = __ffma2_rn(sc[2 * ks + 1], cz1, gamma2);
   }
-  gamma = quad_sum(gamma);
+  const float gamma = quad_sum(gamma2.x + gamma2.y);
+  const float2 gamma_2 = make_float2(gamma, gamma);
 
   if (VB == 2) {
     // PV with 2-bit values: channel n-tile nt2 = 2np + which; cell (g, c) of panel np serves both `which`;
@@ -365,8 +378,11 @@ __device__ __forceinline__ void attend_tile(const uint8_t* rec, const float (&qv
       for (int j = 0; j < 4; ++j) {
         const int nt2 = 2 * (2 * npg + (j >> 1)) + (j & 1);
         const float2 rv = h2pair(vm + L::kVr + 8 * nt2 + 2 * c);
-        acc[nt2][0] = fmaf(rv.x, (d[j][0] + d[j][2]) + gamma, acc[nt2][0]);
-        acc[nt2][1] = fmaf(rv.y, (d[j][1] + d[j][3]) + gamma, acc[nt2][1]);
+        const float2 v = __ffma2_rn(
+            rv, __fadd2_rn(__fadd2_rn(make_float2(d[j][0], d[j][1]), make_float2(d[j][2], d[j][3])), gamma_2),
+            make_float2(acc[nt2][0], acc[nt2][1]));
+        acc[nt2][0] = v.x;
+        acc[nt2][1] = v.y;
       }
     }
   } else {
@@ -398,8 +414,11 @@ __device__ __forceinline__ void attend_tile(const uint8_t* rec, const float (&qv
       for (int j = 0; j < 4; ++j) {
         const int nt2 = 4 * npg + j;
         const float2 rv = h2pair(vm + L::kVr + 8 * nt2 + 2 * c);
-        acc[nt2][0] = fmaf(rv.x, (d[j][0] + d[j][2]) + gamma, acc[nt2][0]);
-        acc[nt2][1] = fmaf(rv.y, (d[j][1] + d[j][3]) + gamma, acc[nt2][1]);
+        const float2 v = __ffma2_rn(
+            rv, __fadd2_rn(__fadd2_rn(make_float2(d[j][0], d[j][1]), make_float2(d[j][2], d[j][3])), gamma_2),
+            make_float2(acc[nt2][0], acc[nt2][1]));
+        acc[nt2][0] = v.x;
+        acc[nt2][1] = v.y;
       }
     }
   }

@@ -15,6 +15,21 @@ __device__ __forceinline__ void split2(float x0, float x1, uint32_t& hi, uint32_
   lo = *reinterpret_cast<const uint32_t*>(&l);
 }
 
+// The same split of an fp32 pair; the residual x - hi is one packed fma (exact).
+__device__ __forceinline__ void split2p(float2 x, uint32_t& hi, uint32_t& lo) {
+  const __half2 h = __floats2half2_rn(x.x, x.y);
+  const float2 r = __ffma2_rn(__half22float2(h), make_float2(-1.f, -1.f), x);
+  const __half2 l = __floats2half2_rn(r.x, r.y);
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+
+__device__ __forceinline__ float fmax3f(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
 __device__ __forceinline__ float2 h2pair(const uint16_t* p) {
   return __half22float2(*reinterpret_cast<const __half2*>(p));
 }

@@ -15,11 +15,12 @@
 //      accumulation; the 1/sqrt(128) factor is folded into the statistics;
 //   3. each column pass reads D2 and each row pass reads D1 straight from TMEM
 //      (tcgen05.ld 16x64b: two threads per line, 64 values each), so both passes
-//      are thread-local loops plus one shuffle with the partner thread; the first
-//      half of every sweep is loaded at the end of the sweep before it, so its
-//      latency overlaps the reduction, the scale update and the barrier;
-//   4. fp16 scales, RTN, packing into a shared-memory stage, and two bulk stores of
-//      the group's part of the record.
+//      are thread-local loops plus one shuffle with the partner thread; every
+//      sweep (the thread's 64 values) is loaded at the end of the sweep before it,
+//      so its latency overlaps the reduction, the scale update and the barrier;
+//   4. fp16 scales, group extremes (for keys taken in the last row pass, whose
+//      lines are the key groups), RTN, packing into a shared-memory stage, and two
+//      bulk stores of the group's part of the record.
 // The groups share only the Hadamard operand and the TMEM allocation (256 columns
 // each), so one group's MMA latency and barriers overlap the other's arithmetic.
 // The slot check of an item is agreed on at the barrier that ends the previous one.
@@ -196,6 +197,17 @@ __device__ __forceinline__ void issue_tile(const Src& src, int64_t w, int g, uin
   tma_load_2d(dst + kTileOp / 2, map, x + 64, y, bar);
 }
 
+// A thread's whole half line (64 values, two x32 loads) from TMEM; the registers
+// are valid after tmem_wait_line.
+__device__ __forceinline__ void tmem_ld_line(uint32_t taddr, float (&x)[64]) {
+  tmem_ld_16x64b_x32_nowait(taddr, x);
+  tmem_ld_16x64b_x32_nowait(taddr + 64, x + 32);
+}
+__device__ __forceinline__ void tmem_wait_line(float (&x)[64]) {
+  tmem_wait_x32(x);
+  tmem_wait_x32(x + 32);
+}
+
 // Population variance and mean over the pair's 128 values of w_e * x_e, where the
 // thread's line in TMEM is at `taddr` (entries e = p + 2k, k < 64, streamed in two
 // halves of 32) and w is a parity-split vector. One sweep accumulates the first
@@ -204,22 +216,28 @@ __device__ __forceinline__ void issue_tile(const Src& src, int64_t w, int g, uin
 // variance, or a non-positive variance), a second sweep recomputes the moments
 // about the exact mean, so the result keeps the accuracy of a centred two-pass
 // variance.
-__device__ __forceinline__ float pair_moments(float (&x)[32], uint32_t taddr, const float* wv, int p, float shift,
-                                             float& mean, uint32_t next_taddr) {
+//
+// With kExt, the same sweep also takes the extremes over the pair's values of
+// x_e * h_e (h a second parity-split vector), returned in mn, mx for both threads.
+template <bool kExt = false>
+__device__ __forceinline__ float pair_moments(float (&x)[64], uint32_t taddr, const float* wv, int p, float shift,
+                                             float& mean, uint32_t next_taddr, const float* hv = nullptr,
+                                             float* mn_out = nullptr, float* mx_out = nullptr) {
   const float2 nsh = make_float2(-shift, -shift);
   float2 s0 = make_float2(0.f, 0.f), s1 = s0, s2 = s0, s3 = s0, q0 = s0, q1 = s0, q2 = s0, q3 = s0;
-#pragma unroll 1
+  float mn = INFINITY, mx = -INFINITY;
+  tmem_wait_line(x);   // the whole sweep was started at the end of the one before
+#pragma unroll
   for (int hh = 0; hh < 2; ++hh) {
-    if (hh == 1) tmem_ld_16x64b_x32_nowait(taddr + 64, x);   // the first half was started earlier
-    tmem_wait_x32(x);
+    const float* xh = x + 32 * hh;
 #pragma unroll
     for (int q = 0; q < 8; q += 2) {
       const float4 w = reinterpret_cast<const float4*>(wv + p * 68)[8 * hh + q];
       const float4 v = reinterpret_cast<const float4*>(wv + p * 68)[8 * hh + q + 1];
-      const float2 d0 = __ffma2_rn(make_float2(w.x, w.y), make_float2(x[4 * q], x[4 * q + 1]), nsh);
-      const float2 d1 = __ffma2_rn(make_float2(w.z, w.w), make_float2(x[4 * q + 2], x[4 * q + 3]), nsh);
-      const float2 d2 = __ffma2_rn(make_float2(v.x, v.y), make_float2(x[4 * q + 4], x[4 * q + 5]), nsh);
-      const float2 d3 = __ffma2_rn(make_float2(v.z, v.w), make_float2(x[4 * q + 6], x[4 * q + 7]), nsh);
+      const float2 d0 = __ffma2_rn(make_float2(w.x, w.y), make_float2(xh[4 * q], xh[4 * q + 1]), nsh);
+      const float2 d1 = __ffma2_rn(make_float2(w.z, w.w), make_float2(xh[4 * q + 2], xh[4 * q + 3]), nsh);
+      const float2 d2 = __ffma2_rn(make_float2(v.x, v.y), make_float2(xh[4 * q + 4], xh[4 * q + 5]), nsh);
+      const float2 d3 = __ffma2_rn(make_float2(v.z, v.w), make_float2(xh[4 * q + 6], xh[4 * q + 7]), nsh);
       s0 = __fadd2_rn(s0, d0);
       s1 = __fadd2_rn(s1, d1);
       s2 = __fadd2_rn(s2, d2);
@@ -228,7 +246,21 @@ __device__ __forceinline__ float pair_moments(float (&x)[32], uint32_t taddr, co
       q1 = __ffma2_rn(d1, d1, q1);
       q2 = __ffma2_rn(d2, d2, q2);
       q3 = __ffma2_rn(d3, d3, q3);
+      if (kExt) {
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          const float4 h = reinterpret_cast<const float4*>(hv + p * 68)[8 * hh + q + r];
+          const float2 y0 = __fmul2_rn(make_float2(xh[4 * (q + r)], xh[4 * (q + r) + 1]), make_float2(h.x, h.y));
+          const float2 y1 = __fmul2_rn(make_float2(xh[4 * (q + r) + 2], xh[4 * (q + r) + 3]), make_float2(h.z, h.w));
+          mn = fmin3(fmin3(mn, y0.x, y0.y), y1.x, y1.y);
+          mx = fmax3(fmax3(mx, y0.x, y0.y), y1.x, y1.y);
+        }
+      }
     }
+  }
+  if (kExt) {
+    *mn_out = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, 2));
+    *mx_out = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
   }
   s0 = __fadd2_rn(s0, s2);
   s1 = __fadd2_rn(s1, s3);
@@ -247,15 +279,16 @@ __device__ __forceinline__ float pair_moments(float (&x)[32], uint32_t taddr, co
     const float c = shift + d;
     const float2 nc = make_float2(-c, -c);
     float2 r0 = make_float2(0.f, 0.f), r1 = r0;
-#pragma unroll 1
+    tmem_ld_line(taddr, x);
+    tmem_wait_line(x);
+#pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
-      tmem_ld_16x64b_x32_nowait(taddr + 64 * hh, x);
-      tmem_wait_x32(x);
+      const float* xh = x + 32 * hh;
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
         const float4 w = reinterpret_cast<const float4*>(wv + p * 68)[8 * hh + q];
-        const float2 e0 = __ffma2_rn(make_float2(w.x, w.y), make_float2(x[4 * q], x[4 * q + 1]), nc);
-        const float2 e1 = __ffma2_rn(make_float2(w.z, w.w), make_float2(x[4 * q + 2], x[4 * q + 3]), nc);
+        const float2 e0 = __ffma2_rn(make_float2(w.x, w.y), make_float2(xh[4 * q], xh[4 * q + 1]), nc);
+        const float2 e1 = __ffma2_rn(make_float2(w.z, w.w), make_float2(xh[4 * q + 2], xh[4 * q + 3]), nc);
         r0 = __ffma2_rn(e0, e0, r0);
         r1 = __ffma2_rn(e1, e1, r1);
       }
@@ -268,7 +301,7 @@ __device__ __forceinline__ float pair_moments(float (&x)[32], uint32_t taddr, co
       d = 0.f;
     }
   }
-  tmem_ld_16x64b_x32_nowait(next_taddr, x);   // first half of the next sweep, waited there
+  tmem_ld_line(next_taddr, x);   // the next sweep, waited there
   mean = shift + d;
   return fmaxf(var, 0.0f);
 }
@@ -280,6 +313,33 @@ __device__ __forceinline__ float div_sqrt(float v, float u) {
   const float e = fmaf(-u * y0, y0, 1.0f);
   const float y1 = fmaf(0.5f * y0, e, y0);
   return v * y1;
+}
+
+// Keys, after the last column pass: the fp16 scale c of token `line` (b its final
+// normaliser) into the metadata, and 1/c into the vector the extremes and codes use.
+template <bool kLean>
+__device__ __forceinline__ void key_token_scale(uint16_t* meta, float* vh, int line, int pl, float b) {
+  const uint16_t cb = f2h_bits(clampf(1.0f / b, kFp16MinNormal, kFp16Max));
+  meta[(kLean ? 0 : 1) * 128 + line] = cb;
+  vh[pl] = 1.0f / h2f_bits(cb);
+}
+
+// Zero point and scale of group `line` from its extremes mn, mx of y, in fp16, and
+// the code-pass coefficients: v = (x * own) * w + c0 = ((y - z) / s + 1/2) / levels,
+// where `lf` is the group's own factor of y (the part of 1/(r c) and 2^-3.5 that is
+// constant along the group).
+template <int kBits, bool kLean>
+__device__ __forceinline__ void group_zero_scale(uint16_t* meta, float* vw, float* vc0, int line, int pl, float mn,
+                                                 float mx, float lf) {
+  constexpr float kLevels = static_cast<float>((1 << kBits) - 1);
+  const uint16_t zb = f2h_bits(clampf(mn, -kFp16Max, kFp16Max));
+  const float z = h2f_bits(zb);
+  const uint16_t sbits = f2h_bits(clampf(fmaxf(mx - z, 0.0f) / kLevels, kFp16MinNormal, kFp16Max));
+  const float inv_s = 1.0f / h2f_bits(sbits);
+  meta[(kLean ? 1 : 2) * 128 + line] = sbits;
+  meta[(kLean ? 2 : 3) * 128 + line] = zb;
+  vw[pl] = lf * inv_s * (1.0f / kLevels);
+  vc0[pl] = fmaf(-z, inv_s, 0.5f) * (1.0f / kLevels);
 }
 
 // Quantize the tensor of group g (0 = K, 1 = V) of the current item from TMEM;
@@ -305,9 +365,9 @@ __device__ __forceinline__ bool quantize_group(float* vec, uint8_t* stage, const
   }
   // every thread saw its copies and the tensor core finish, or the group stops
   if (!named_bar_and(bar_id, kGroupThreads, ok)) return false;
-  // TMEM sweeps: the first half of every sweep is loaded at the end of the one before
-  float x[32];
-  tmem_ld_16x64b_x32_nowait(ta2, x);
+  // TMEM sweeps: every sweep is loaded at the end of the one before
+  float x[64];
+  tmem_ld_line(ta2, x);
 
   float* vmc = vec + kVMc * kVec;
   float* vmr = vec + kVMr * kVec;
@@ -322,92 +382,96 @@ __device__ __forceinline__ bool quantize_group(float* vec, uint8_t* stage, const
       const float var = pair_moments(x, ta2, va, p, shift, mean, ta1) * kVarScale;
       if (p == 0) {
         const float b = vb[pl];
-        vb[pl] = div_sqrt(b, fmaf(b * b, var, eps));
+        const float bn = div_sqrt(b, fmaf(b * b, var, eps));
+        vb[pl] = bn;
         vmc[pl] = mean;
+        if (kKind == 0 && it + 1 == n_iters) key_token_scale<kLean>(meta, vh, line, pl, bn);
       }
     }
     named_bar(bar_id, kGroupThreads);
     // row pass: channel i = line, tokens e = p + 2k (D1), weights b
-    {
+    if (kKind == 1 || it + 1 < n_iters) {
       float mean;
-      const uint32_t next = it + 1 < n_iters ? ta2 : (kKind == 0 ? ta1 : ta2);   // next column pass or extremes
-      const float var = pair_moments(x, ta1, vb, p, it == 0 ? 0.0f : vmr[pl], mean, next) * kVarScale;
+      const float var = pair_moments(x, ta1, vb, p, it == 0 ? 0.0f : vmr[pl], mean, ta2) * kVarScale;
       if (p == 0) {
         const float a = va[pl];
         va[pl] = div_sqrt(a, fmaf(a * a, var, eps));
         vmr[pl] = mean;
       }
+    } else {
+      // last row pass of the keys: the same sweep takes each channel's extremes of
+      // x_ij / c_j, so r, s and z of the channel follow without another sweep
+      float mean, mn, mx;
+      const float var =
+          pair_moments<true>(x, ta1, vb, p, it == 0 ? 0.0f : vmr[pl], mean, ta2, vh, &mn, &mx) * kVarScale;
+      if (p == 0) {
+        const float a = va[pl];
+        const float an = div_sqrt(a, fmaf(a * a, var, eps));
+        const uint16_t rb = f2h_bits(clampf(1.0f / an, kFp16MinNormal, kFp16Max));
+        if (!kLean) meta[0 * 128 + line] = rb;
+        const float g = kLean ? kInvSqrt128 : kInvSqrt128 / h2f_bits(rb);
+        group_zero_scale<kBits, kLean>(meta, vw, vc0, line, pl, mn * g, mx * g, g);
+      }
     }
     named_bar(bar_id, kGroupThreads);
   }
 
-  // fp16 scales: r per channel (line as channel), c per token (line as token)
-  if (p == 0) {
-    const uint16_t rb = f2h_bits(clampf(1.0f / va[pl], kFp16MinNormal, kFp16Max));
-    const uint16_t cb = f2h_bits(clampf(1.0f / vb[pl], kFp16MinNormal, kFp16Max));
-    // the +-1 transform's 2^-3.5 is folded into g; lean metadata keeps c for keys and r
-    // for values, and the other scale (constant in each group) is folded into s, z
-    if (!kLean) {
-      meta[0 * 128 + line] = rb;
-      meta[1 * 128 + line] = cb;
-    } else {
-      meta[line] = kKind == 0 ? cb : rb;
+  if (kKind == 1) {
+    // fp16 scales of the values: r per channel (line as channel), c per token (line
+    // as token); the +-1 transform's 2^-3.5 is folded into g; lean metadata keeps r,
+    // and c (constant in each token's group) is folded into s, z
+    if (p == 0) {
+      const uint16_t rb = f2h_bits(clampf(1.0f / va[pl], kFp16MinNormal, kFp16Max));
+      const uint16_t cb = f2h_bits(clampf(1.0f / vb[pl], kFp16MinNormal, kFp16Max));
+      if (!kLean) {
+        meta[0 * 128 + line] = rb;
+        meta[1 * 128 + line] = cb;
+      } else {
+        meta[line] = rb;
+      }
+      vg[pl] = kInvSqrt128 / h2f_bits(rb);
+      vh[pl] = kLean ? 1.0f : 1.0f / h2f_bits(cb);
     }
-    vg[pl] = (kLean && kKind == 0) ? kInvSqrt128 : kInvSqrt128 / h2f_bits(rb);
-    vh[pl] = (kLean && kKind == 1) ? 1.0f : 1.0f / h2f_bits(cb);
-  }
-  named_bar(bar_id, kGroupThreads);
+    named_bar(bar_id, kGroupThreads);
 
-  constexpr float kLevels = static_cast<float>((1 << kBits) - 1);
-  // group extremes of y = (x * hc_j) * g_i: keys per channel (D1 rows), values per
-  // token (D2 rows); two halves of 64 columns (registers k = 32 hh + kl)
-  {
+    // extremes of y = (x * g_i) * hc_j per token (D2 rows); two halves of 64 columns
+    // (registers k = 32 hh + kl); the factor that is constant along the thread's line
+    // is positive, so it multiplies the extremes afterwards (same rounding as per element)
     float mn = INFINITY, mx = -INFINITY;
-#pragma unroll 1
+    tmem_wait_line(x);
+#pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
-      float* xh = x;
-      if (hh == 1) tmem_ld_16x64b_x32_nowait((kKind == 0 ? ta1 : ta2) + 64, xh);
-      tmem_wait_x32(xh);
-      // y = (x * hc_j) * g_i; the factor that is constant along the thread's line is
-      // positive, so it multiplies the extremes afterwards (same rounding as per element)
-      const float* vv = kKind == 0 ? vh : vg;
+      const float* xh = x + 32 * hh;
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
-        const float4 w = reinterpret_cast<const float4*>(vv + p * 68)[8 * hh + q];
+        const float4 w = reinterpret_cast<const float4*>(vg + p * 68)[8 * hh + q];
         const float2 y0 = __fmul2_rn(make_float2(xh[4 * q], xh[4 * q + 1]), make_float2(w.x, w.y));
         const float2 y1 = __fmul2_rn(make_float2(xh[4 * q + 2], xh[4 * q + 3]), make_float2(w.z, w.w));
         mn = fmin3(fmin3(mn, y0.x, y0.y), y1.x, y1.y);
         mx = fmax3(fmax3(mx, y0.x, y0.y), y1.x, y1.y);
       }
     }
-    tmem_ld_16x64b_x32_nowait(kKind == 0 ? ta2 : ta1, x);   // first half of the codes sweep
-    const float line_factor = kKind == 0 ? vg[pl] : vh[pl];
-    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, 2)) * line_factor;
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2)) * line_factor;
+    tmem_ld_line(ta1, x);   // the codes sweep
+    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, 2));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
     if (p == 0) {
-      const uint16_t zb = f2h_bits(clampf(mn, -kFp16Max, kFp16Max));
-      const float z = h2f_bits(zb);
-      const uint16_t sbits = f2h_bits(clampf(fmaxf(mx - z, 0.0f) / kLevels, kFp16MinNormal, kFp16Max));
-      const float inv_s = 1.0f / h2f_bits(sbits);
-      meta[(kLean ? 1 : 2) * 128 + line] = sbits;
-      meta[(kLean ? 2 : 3) * 128 + line] = zb;
-      vw[pl] = (kKind == 0 ? vg[pl] : vh[pl]) * inv_s * (1.0f / kLevels);
-      vc0[pl] = fmaf(-z, inv_s, 0.5f) * (1.0f / kLevels);
+      const float hc = vh[pl];
+      group_zero_scale<kBits, kLean>(meta, vw, vc0, line, pl, mn * hc, mx * hc, hc);
     }
+    named_bar(bar_id, kGroupThreads);
   }
-  named_bar(bar_id, kGroupThreads);
 
   // codes: keys token-major (D2 rows: token = line, channels e = p + 2k), values
   // channel-major (D1 rows: channel = line, tokens e = p + 2k); half hh holds
   // k = 32 hh + kl. 4-bit codes (keys or values) fill line rows of 64 bytes, words
   // w = 2hh, 2hh + 1 of each 16-byte group; 2-bit codes fill word u = hh
+  constexpr float kLevels = static_cast<float>((1 << kBits) - 1);
   const float own = kKind == 0 ? vh[pl] : vg[pl];
   const float2 own2 = make_float2(own, own);
-#pragma unroll 1
+  tmem_wait_line(x);
+#pragma unroll
   for (int hh = 0; hh < 2; ++hh) {
-    float* xh = x;
-    if (hh == 1) tmem_ld_16x64b_x32_nowait((kKind == 0 ? ta2 : ta1) + 64, xh);
-    tmem_wait_x32(xh);
+    const float* xh = x + 32 * hh;
     // v = (x * own) * w_e + c0_e = (y - z) / s + 1/2, clamped to [0, levels]; the
     // round-down add of 2^23 leaves 0x4B000000 + floor(v) in the bits, and each
     // word accumulates (bits << shift) with the 0x4B000000 terms removed at the end
@@ -473,10 +537,10 @@ __device__ __forceinline__ bool quantize_group(float* vec, uint8_t* stage, const
   return true;
 }
 
-// 104 registers a thread (the 512 threads could hold 128): measured faster on the
-// prefill workload than 88, 96 or 128.
+// 128 registers a thread (all that 512 threads can hold): a whole sweep in flight
+// needs 64 of them; 112 spilled and measured 5 % slower.
 template <class Src, int KB, int VB, bool kLean>
-__global__ void __maxnreg__(104)
+__global__ void __maxnreg__(128)
     quantize_kernel(const __grid_constant__ Src src, uint8_t* __restrict__ cache, int n_iters, float eps,
                     unsigned* flags) {
   extern __shared__ __align__(1024) uint8_t smem[];
