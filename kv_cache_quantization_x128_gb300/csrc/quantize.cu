@@ -39,7 +39,7 @@ constexpr int kGroupThreads = 256;
 constexpr int kThreads = 2 * kGroupThreads;
 constexpr int kTileOp = kB * kD * 2;              // 32768 B: one fp16 128x128 operand
 constexpr int kVec = 136;                         // parity-split vector (even at 0, odd at 68)
-constexpr int kNumVec = 8;                        // a, b, g (2^-3.5/r), hc (1/c), w, c0, mc, mr
+constexpr int kNumVec = 6;                        // a, b, g (2^-3.5/r), hc (1/c), w, c0
 
 constexpr int kOffH = 0;
 constexpr int kOffIn = kOffH + kTileOp;                        // [group][buf] operands
@@ -62,7 +62,7 @@ struct QSmem {
   static_assert(kOffStageV % 16 == 0 && kOffVec % 16 == 0, "align");
 };
 
-enum { kVA = 0, kVB = 1, kVG = 2, kVHc = 3, kVW = 4, kVC0 = 5, kVMc = 6, kVMr = 7 };
+enum { kVA = 0, kVB = 1, kVG = 2, kVHc = 3, kVW = 4, kVC0 = 5 };
 
 // position of entry e in a parity-split vector
 __device__ __forceinline__ int ps(int e) { return (e & 1) * 68 + (e >> 1); }
@@ -317,11 +317,16 @@ __device__ __forceinline__ float div_sqrt(float v, float u) {
 
 // Keys, after the last column pass: the fp16 scale c of token `line` (b its final
 // normaliser) into the metadata, and 1/c into the vector the extremes and codes use.
+// Returns 1/c; `store` selects the thread that writes.
 template <bool kLean>
-__device__ __forceinline__ void key_token_scale(uint16_t* meta, float* vh, int line, int pl, float b) {
+__device__ __forceinline__ float key_token_scale(uint16_t* meta, float* vh, int line, int pl, float b, bool store) {
   const uint16_t cb = f2h_bits(clampf(1.0f / b, kFp16MinNormal, kFp16Max));
-  meta[(kLean ? 0 : 1) * 128 + line] = cb;
-  vh[pl] = 1.0f / h2f_bits(cb);
+  const float hc = 1.0f / h2f_bits(cb);
+  if (store) {
+    meta[(kLean ? 0 : 1) * 128 + line] = cb;
+    vh[pl] = hc;
+  }
+  return hc;
 }
 
 // Zero point and scale of group `line` from its extremes mn, mx of y, in fp16, and
@@ -363,50 +368,44 @@ __device__ __forceinline__ bool quantize_group(float* vec, uint8_t* stage, const
     va[pl] = 1.0f;
     vb[pl] = 1.0f;
   }
+  // The thread pair of a line keeps that line's scale and mean in registers (both
+  // threads compute them; thread p = 0 publishes the scale for the other lines).
+  float a_own = 1.0f, b_own = 1.0f, mean_r = 0.0f;
+  // the first column shift is exact: with a = 1 the mean of a +-1 Hadamard column
+  // is the token's channel-0 input value
+  float mean_c = __half2float(*reinterpret_cast<const __half*>(tile + sw_offset(line, 0)));
   // every thread saw its copies and the tensor core finish, or the group stops
   if (!named_bar_and(bar_id, kGroupThreads, ok)) return false;
   // TMEM sweeps: every sweep is loaded at the end of the one before
   float x[64];
   tmem_ld_line(ta2, x);
 
-  float* vmc = vec + kVMc * kVec;
-  float* vmr = vec + kVMr * kVec;
+  float own = 0.0f;   // the line's own factor in the codes pass (keys: 1/c, values: g)
   for (int it = 0; it < n_iters; ++it) {
-    // column pass: token j = line, channels e = p + 2k (D2), weights a; the first
-    // shift is exact: with a = 1 the mean of a +-1 Hadamard column is the token's
-    // channel-0 input value
+    // column pass: token j = line, channels e = p + 2k (D2), weights a
     {
-      const float shift = it == 0 ? __half2float(*reinterpret_cast<const __half*>(tile + sw_offset(line, 0)))
-                                  : vmc[pl];
       float mean;
-      const float var = pair_moments(x, ta2, va, p, shift, mean, ta1) * kVarScale;
-      if (p == 0) {
-        const float b = vb[pl];
-        const float bn = div_sqrt(b, fmaf(b * b, var, eps));
-        vb[pl] = bn;
-        vmc[pl] = mean;
-        if (kKind == 0 && it + 1 == n_iters) key_token_scale<kLean>(meta, vh, line, pl, bn);
-      }
+      const float var = pair_moments(x, ta2, va, p, mean_c, mean, ta1) * kVarScale;
+      b_own = div_sqrt(b_own, fmaf(b_own * b_own, var, eps));
+      mean_c = mean;
+      if (p == 0) vb[pl] = b_own;
+      if (kKind == 0 && it + 1 == n_iters) own = key_token_scale<kLean>(meta, vh, line, pl, b_own, p == 0);
     }
     named_bar(bar_id, kGroupThreads);
     // row pass: channel i = line, tokens e = p + 2k (D1), weights b
     if (kKind == 1 || it + 1 < n_iters) {
       float mean;
-      const float var = pair_moments(x, ta1, vb, p, it == 0 ? 0.0f : vmr[pl], mean, ta2) * kVarScale;
-      if (p == 0) {
-        const float a = va[pl];
-        va[pl] = div_sqrt(a, fmaf(a * a, var, eps));
-        vmr[pl] = mean;
-      }
+      const float var = pair_moments(x, ta1, vb, p, mean_r, mean, ta2) * kVarScale;
+      a_own = div_sqrt(a_own, fmaf(a_own * a_own, var, eps));
+      mean_r = mean;
+      if (p == 0) va[pl] = a_own;
     } else {
       // last row pass of the keys: the same sweep takes each channel's extremes of
       // x_ij / c_j, so r, s and z of the channel follow without another sweep
       float mean, mn, mx;
-      const float var =
-          pair_moments<true>(x, ta1, vb, p, it == 0 ? 0.0f : vmr[pl], mean, ta2, vh, &mn, &mx) * kVarScale;
+      const float var = pair_moments<true>(x, ta1, vb, p, mean_r, mean, ta2, vh, &mn, &mx) * kVarScale;
       if (p == 0) {
-        const float a = va[pl];
-        const float an = div_sqrt(a, fmaf(a * a, var, eps));
+        const float an = div_sqrt(a_own, fmaf(a_own * a_own, var, eps));
         const uint16_t rb = f2h_bits(clampf(1.0f / an, kFp16MinNormal, kFp16Max));
         if (!kLean) meta[0 * 128 + line] = rb;
         const float g = kLean ? kInvSqrt128 : kInvSqrt128 / h2f_bits(rb);
@@ -420,17 +419,18 @@ __device__ __forceinline__ bool quantize_group(float* vec, uint8_t* stage, const
     // fp16 scales of the values: r per channel (line as channel), c per token (line
     // as token); the +-1 transform's 2^-3.5 is folded into g; lean metadata keeps r,
     // and c (constant in each token's group) is folded into s, z
+    const uint16_t rb = f2h_bits(clampf(1.0f / a_own, kFp16MinNormal, kFp16Max));
+    const uint16_t cb = f2h_bits(clampf(1.0f / b_own, kFp16MinNormal, kFp16Max));
+    own = kInvSqrt128 / h2f_bits(rb);
+    const float hc = kLean ? 1.0f : 1.0f / h2f_bits(cb);
     if (p == 0) {
-      const uint16_t rb = f2h_bits(clampf(1.0f / va[pl], kFp16MinNormal, kFp16Max));
-      const uint16_t cb = f2h_bits(clampf(1.0f / vb[pl], kFp16MinNormal, kFp16Max));
       if (!kLean) {
         meta[0 * 128 + line] = rb;
         meta[1 * 128 + line] = cb;
       } else {
         meta[line] = rb;
       }
-      vg[pl] = kInvSqrt128 / h2f_bits(rb);
-      vh[pl] = kLean ? 1.0f : 1.0f / h2f_bits(cb);
+      vg[pl] = own;
     }
     named_bar(bar_id, kGroupThreads);
 
@@ -454,10 +454,7 @@ __device__ __forceinline__ bool quantize_group(float* vec, uint8_t* stage, const
     tmem_ld_line(ta1, x);   // the codes sweep
     mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, 2));
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-    if (p == 0) {
-      const float hc = vh[pl];
-      group_zero_scale<kBits, kLean>(meta, vw, vc0, line, pl, mn * hc, mx * hc, hc);
-    }
+    if (p == 0) group_zero_scale<kBits, kLean>(meta, vw, vc0, line, pl, mn * hc, mx * hc, hc);
     named_bar(bar_id, kGroupThreads);
   }
 
@@ -466,7 +463,6 @@ __device__ __forceinline__ bool quantize_group(float* vec, uint8_t* stage, const
   // k = 32 hh + kl. 4-bit codes (keys or values) fill line rows of 64 bytes, words
   // w = 2hh, 2hh + 1 of each 16-byte group; 2-bit codes fill word u = hh
   constexpr float kLevels = static_cast<float>((1 << kBits) - 1);
-  const float own = kKind == 0 ? vh[pl] : vg[pl];
   const float2 own2 = make_float2(own, own);
   tmem_wait_line(x);
 #pragma unroll
