@@ -220,17 +220,13 @@ __device__ __forceinline__ void attend_tile(const uint8_t* rec, const float (&qv
 #pragma unroll
   for (int ks = 0; ks < 8; ++ks) {
     const int ch0 = 16 * ks + 2 * c;
-    const float2 s0 = h2pair(km + L::kKs + ch0), s1 = h2pair(km + L::kKs + ch0 + 8);
-    const float2 z0 = h2pair(km + L::kKz + ch0), z1 = h2pair(km + L::kKz + ch0 + 8);
-    // lean records fold the key row scale r into s and z
-    float2 rs0 = s0, rs1 = s1, rz0 = z0, rz1 = z1;
-    if (!kLean) {
-      const float2 r0 = h2pair(km + L::kKr + ch0), r1 = h2pair(km + L::kKr + ch0 + 8);
-      rs0 = __fmul2_rn(r0, s0);
-      rs1 = __fmul2_rn(r1, s1);
-      rz0 = __fmul2_rn(r0, z0);
-      rz1 = __fmul2_rn(r1, z1);
-    }
+    // r s and r z in fp32 straight from the fp16 pairs (lean records fold r into s, z)
+    const uint32_t s0 = h2raw(km + L::kKs + ch0), s1 = h2raw(km + L::kKs + ch0 + 8);
+    const uint32_t z0 = h2raw(km + L::kKz + ch0), z1 = h2raw(km + L::kKz + ch0 + 8);
+    const uint32_t r0 = kLean ? kH_One : h2raw(km + L::kKr + ch0);
+    const uint32_t r1 = kLean ? kH_One : h2raw(km + L::kKr + ch0 + 8);
+    const float2 rs0 = mul_h2(r0, s0), rs1 = mul_h2(r1, s1);
+    const float2 rz0 = mul_h2(r0, z0), rz1 = mul_h2(r1, z1);
     const float2 qa = make_float2(qv[ks][0], qv[ks][1]), qb = make_float2(qv[ks][2], qv[ks][3]);
     split2p(__fmul2_rn(qa, rs0), A[ks][0], A[ks][1]);
     split2p(__fmul2_rn(qb, rs1), A[ks][2], A[ks][3]);
@@ -327,17 +323,13 @@ __device__ __forceinline__ void attend_tile(const uint8_t* rec, const float (&qv
 #pragma unroll
   for (int ks = 0; ks < 8; ++ks) {
     const int t0 = 16 * ks + 2 * c;
-    const float2 s0 = h2pair(vm + L::kVs + t0), s1 = h2pair(vm + L::kVs + t0 + 8);
-    const float2 z0 = h2pair(vm + L::kVz + t0), z1 = h2pair(vm + L::kVz + t0 + 8);
-    // lean records fold the value column scale c into s and z
-    float2 cs0 = s0, cs1 = s1, cz0 = z0, cz1 = z1;
-    if (!kLean) {
-      const float2 c0 = h2pair(vm + L::kVc + t0), c1 = h2pair(vm + L::kVc + t0 + 8);
-      cs0 = __fmul2_rn(c0, s0);
-      cs1 = __fmul2_rn(c1, s1);
-      cz0 = __fmul2_rn(c0, z0);
-      cz1 = __fmul2_rn(c1, z1);
-    }
+    // c s and c z in fp32 straight from the fp16 pairs (lean records fold c into s, z)
+    const uint32_t s0 = h2raw(vm + L::kVs + t0), s1 = h2raw(vm + L::kVs + t0 + 8);
+    const uint32_t z0 = h2raw(vm + L::kVz + t0), z1 = h2raw(vm + L::kVz + t0 + 8);
+    const uint32_t c0 = kLean ? kH_One : h2raw(vm + L::kVc + t0);
+    const uint32_t c1 = kLean ? kH_One : h2raw(vm + L::kVc + t0 + 8);
+    const float2 cs0 = mul_h2(c0, s0), cs1 = mul_h2(c1, s1);
+    const float2 cz0 = mul_h2(c0, z0), cz1 = mul_h2(c1, z1);
     split2p(__fmul2_rn(sc[2 * ks], cs0), A[ks][0], A[ks][1]);
     split2p(__fmul2_rn(sc[2 * ks + 1], cs1), A[ks][2], A[ks][3]);
     gamma2 = __ffma2_rn(sc[2 * ks], cz0, gamma2);

@@ -30,6 +30,18 @@ __device__ __forceinline__ float fmax3f(float a, float b, float c) {
   return r;
 }
 
+// Products of two fp16 pairs in fp32 (exact: 11 x 11 significant bits), from the
+// packed halves without converting them first.
+__device__ __forceinline__ float2 mul_h2(uint32_t a, uint32_t b) {
+  float2 r;
+  asm("{\n .reg .f16 a0, a1, b0, b1;\n mov.b32 {a0, a1}, %2;\n mov.b32 {b0, b1}, %3;\n"
+      " fma.rn.f32.f16 %0, a0, b0, 0f00000000;\n fma.rn.f32.f16 %1, a1, b1, 0f00000000;\n}"
+      : "=f"(r.x), "=f"(r.y)
+      : "r"(a), "r"(b));
+  return r;
+}
+__device__ __forceinline__ uint32_t h2raw(const uint16_t* p) { return *reinterpret_cast<const uint32_t*>(p); }
+
 __device__ __forceinline__ float2 h2pair(const uint16_t* p) {
   return __half22float2(*reinterpret_cast<const __half2*>(p));
 }
