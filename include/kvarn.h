@@ -36,10 +36,10 @@
  * the two others use:
  *   2-bit K codes, token-major: token t owns bytes [32t, 32t+32) = four 8-byte
  *     groups g = (i>>1)&3, each two words u = i>>6; channel i sits in crumb
- *     p = 8(i&1) + 2((i>>4)&3) + ((i>>3)&1) (bits 2p..2p+1) of word u.
+ *     p = 4((i>>4)&3) + 2(i&1) + ((i>>3)&1) (bits 2p..2p+1) of word u.
  *   4-bit V codes, channel-major: the 4-bit K layout with channel and token
  *     exchanged (channel i owns bytes [64i, 64i+64), groups g = (t>>1)&3, words
- *     w = t>>5, nibble p = 4(t&1) + 2((t>>4)&1) + ((t>>3)&1)).
+ *     w = t>>5, nibble p = 4((t>>3)&1) + 2(t&1) + ((t>>4)&1)).
  *   k4v4: K codes [0, 8192), V codes [8192, 16384), K meta [16384, 17408), V meta
  *     [17408, 18432). k2v2: K codes [0, 4096), V codes [4096, 8192), K meta
  *     [8192, 9216), V meta [9216, 10240).
@@ -57,13 +57,13 @@
  *   [    0,  8192)  K codes, 4 bits, token-major: token t owns bytes
  *                   [64t, 64t+64) = four 16-byte groups g = (i>>1)&3, each four
  *                   little-endian 32-bit words w = i>>5; channel i sits in nibble
- *                   p = 4(i&1) + 2((i>>4)&1) + ((i>>3)&1) (bits 4p..4p+3) of word w.
+ *                   p = 4((i>>3)&1) + 2(i&1) + ((i>>4)&1) (bits 4p..4p+3) of word w.
  *   [ 8192, 12288)  V codes, 2 bits, channel-major: channel i lives in 512-byte
  *                   panel i>>4; 16-byte cell (i&7)*4 + ((t>>1)&3) of the panel
  *                   holds 8 bytes for the channel with bit 3 clear followed by 8
  *                   bytes for its partner i|8; each 8 bytes are two words
  *                   u = t>>6; token t sits in crumb
- *                   p = 8(t&1) + 2((t>>4)&3) + ((t>>3)&1) (bits 2p..2p+1).
+ *                   p = 4((t>>4)&3) + 2(t&1) + ((t>>3)&1) (bits 2p..2p+1).
  *   [12288, 13312)  K metadata, fp16 [4][128]: r (per channel), c (per token),
  *                   s (per channel), z (per channel).
  *   [13312, 14336)  V metadata, fp16 [4][128]: r (per channel), c (per token),
@@ -72,6 +72,10 @@
  * per channel i for K and per token j for V; the tile is H * X_r.
  * The code orders follow the register fragments of the decode kernel's
  * m16n8k16 tensor-core operands, so a thread's operands are contiguous bytes.
+ * Inside a word, the two codes of one operand register sit in the low nibbles of
+ * the two bytes of a 16-bit half (4-bit) or at bits 0-1 and 4-5 of one byte
+ * (2-bit), so one fp6 (e2m3: value code/8) or fp4 (e2m1: value code/2) conversion
+ * instruction turns them into an fp16 pair.
  *
  * Decode workspace: fp16 [max_seqs][num_kv_heads][2 (K,V)][128 tokens][128 ch],
  * raw (unrotated, unquantised) tokens of each sequence's partial last tile;

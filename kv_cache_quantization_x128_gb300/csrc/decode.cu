@@ -235,6 +235,7 @@ __device__ __forceinline__ void attend_tile(const uint8_t* rec, const float (&qv
   }
   const float beta = quad_sum(beta2.x + beta2.y);
   const float2 beta_2 = make_float2(beta, beta);
+  const float2 kf2 = make_float2(KB == 4 ? 8.f : 2.f, KB == 4 ? 8.f : 2.f);   // codes were converted to c / 8 or c / 2
 
   // scores of tokens 8nt + 2c + {0, 1}, four n-tiles at a time (independent chains)
   float2 sc[16];
@@ -256,11 +257,11 @@ __device__ __forceinline__ void attend_tile(const uint8_t* rec, const float (&qv
       for (int m = 0; m < 4; ++m)
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          const uint32_t w0 = kw[j][m], w8 = kw[j][m] >> 8;
-          mma16816(d[j], A[2 * m], hfma2_u(lop_magic<0x000F000Fu>(w0), kH_One, kH_M1024),
-                   hfma2_u(lop_magic<0x00F000F0u>(w0), kH_Sixteenth, kH_M64));
-          mma16816(d[j], A[2 * m + 1], hfma2_u(lop_magic<0x000F000Fu>(w8), kH_One, kH_M1024),
-                   hfma2_u(lop_magic<0x00F000F0u>(w8), kH_Sixteenth, kH_M64));
+          uint32_t b00, b01, b10, b11;
+          cvt4(kw[j][m] & 0x0F0F0F0Fu, b00, b01);
+          cvt4((kw[j][m] >> 4) & 0x0F0F0F0Fu, b10, b11);
+          mma16816(d[j], A[2 * m], b00, b01);
+          mma16816(d[j], A[2 * m + 1], b10, b11);
         }
     } else {
       // token row of 32 bytes, this thread's 8: word u holds k-steps 4u + 2sg + {0, 1}
@@ -274,22 +275,20 @@ __device__ __forceinline__ void attend_tile(const uint8_t* rec, const float (&qv
 #pragma unroll
       for (int u = 0; u < 2; ++u)
 #pragma unroll
-        for (int sg = 0; sg < 2; ++sg)
+        for (int j = 0; j < 4; ++j) {
+          uint32_t b0[4], b1[4];
+          cvt2(kw[j][u] & 0x33333333u, b0);
+          cvt2((kw[j][u] >> 2) & 0x33333333u, b1);
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const uint32_t w = sg ? (kw[j][u] >> 8) : kw[j][u];
-            mma16816(d[j], A[4 * u + 2 * sg], hfma2_u(lop_magic<0x00030003u>(w), kH_One, kH_M1024),
-                     hfma2_u(lop_magic<0x000C000Cu>(w), kH_Quarter, kH_M256));
-            mma16816(d[j], A[4 * u + 2 * sg + 1], hfma2_u(lop_magic<0x00300030u>(w), kH_Sixteenth, kH_M64),
-                     hfma2_u(lop_magic<0x00C000C0u>(w), kH_64th, kH_M16));
-          }
+          for (int b = 0; b < 4; ++b) mma16816(d[j], A[4 * u + b], b0[b], b1[b]);
+        }
     }
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int nt = 4 * ntg + j;
       const float2 ck = h2pair(km + L::kKc + 8 * nt + 2 * c);
-      sc[nt] = __fmul2_rn(ck, __fadd2_rn(__fadd2_rn(make_float2(d[j][0], d[j][1]), make_float2(d[j][2], d[j][3])),
-                                         beta_2));
+      sc[nt] = __fmul2_rn(ck, __ffma2_rn(__fadd2_rn(make_float2(d[j][0], d[j][1]), make_float2(d[j][2], d[j][3])),
+                                         kf2, beta_2));
     }
   }
 
@@ -337,6 +336,7 @@ __device__ __forceinline__ void attend_tile(const uint8_t* rec, const float (&qv
   }
   const float gamma = quad_sum(gamma2.x + gamma2.y);
   const float2 gamma_2 = make_float2(gamma, gamma);
+  const float2 vf2 = make_float2(VB == 4 ? 8.f : 2.f, VB == 4 ? 8.f : 2.f);
 
   if (VB == 2) {
     // PV with 2-bit values: channel n-tile nt2 = 2np + which; cell (g, c) of panel np serves both `which`;
@@ -355,23 +355,21 @@ __device__ __forceinline__ void attend_tile(const uint8_t* rec, const float (&qv
   #pragma unroll
       for (int u = 0; u < 2; ++u)
   #pragma unroll
-        for (int sg = 0; sg < 2; ++sg)
+        for (int j = 0; j < 4; ++j) {
+          const int i = j >> 1, which = j & 1;
+          const uint32_t w = vw[i][which * 2 + u];
+          uint32_t b0[4], b1[4];
+          cvt2(w & 0x33333333u, b0);
+          cvt2((w >> 2) & 0x33333333u, b1);
   #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int i = j >> 1, which = j & 1;
-            const uint32_t w = sg ? (vw[i][which * 2 + u] >> 8) : vw[i][which * 2 + u];
-            // crumb q = 2*(ks&1) + type at shift sg; ks = 4u + 2sg + (q >> 1)
-            mma16816(d[j], A[4 * u + 2 * sg], hfma2_u(lop_magic<0x00030003u>(w), kH_One, kH_M1024),
-                     hfma2_u(lop_magic<0x000C000Cu>(w), kH_Quarter, kH_M256));
-            mma16816(d[j], A[4 * u + 2 * sg + 1], hfma2_u(lop_magic<0x00300030u>(w), kH_Sixteenth, kH_M64),
-                     hfma2_u(lop_magic<0x00C000C0u>(w), kH_64th, kH_M16));
-          }
+          for (int b = 0; b < 4; ++b) mma16816(d[j], A[4 * u + b], b0[b], b1[b]);
+        }
   #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int nt2 = 2 * (2 * npg + (j >> 1)) + (j & 1);
         const float2 rv = h2pair(vm + L::kVr + 8 * nt2 + 2 * c);
         const float2 v = __ffma2_rn(
-            rv, __fadd2_rn(__fadd2_rn(make_float2(d[j][0], d[j][1]), make_float2(d[j][2], d[j][3])), gamma_2),
+            rv, __ffma2_rn(__fadd2_rn(make_float2(d[j][0], d[j][1]), make_float2(d[j][2], d[j][3])), vf2, gamma_2),
             make_float2(acc[nt2][0], acc[nt2][1]));
         acc[nt2][0] = v.x;
         acc[nt2][1] = v.y;
@@ -396,18 +394,18 @@ __device__ __forceinline__ void attend_tile(const uint8_t* rec, const float (&qv
       for (int m = 0; m < 4; ++m)
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          const uint32_t w0 = vw[j][m], w8 = vw[j][m] >> 8;
-          mma16816(d[j], A[2 * m], hfma2_u(lop_magic<0x000F000Fu>(w0), kH_One, kH_M1024),
-                   hfma2_u(lop_magic<0x00F000F0u>(w0), kH_Sixteenth, kH_M64));
-          mma16816(d[j], A[2 * m + 1], hfma2_u(lop_magic<0x000F000Fu>(w8), kH_One, kH_M1024),
-                   hfma2_u(lop_magic<0x00F000F0u>(w8), kH_Sixteenth, kH_M64));
+          uint32_t b00, b01, b10, b11;
+          cvt4(vw[j][m] & 0x0F0F0F0Fu, b00, b01);
+          cvt4((vw[j][m] >> 4) & 0x0F0F0F0Fu, b10, b11);
+          mma16816(d[j], A[2 * m], b00, b01);
+          mma16816(d[j], A[2 * m + 1], b10, b11);
         }
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int nt2 = 4 * npg + j;
         const float2 rv = h2pair(vm + L::kVr + 8 * nt2 + 2 * c);
         const float2 v = __ffma2_rn(
-            rv, __fadd2_rn(__fadd2_rn(make_float2(d[j][0], d[j][1]), make_float2(d[j][2], d[j][3])), gamma_2),
+            rv, __ffma2_rn(__fadd2_rn(make_float2(d[j][0], d[j][1]), make_float2(d[j][2], d[j][3])), vf2, gamma_2),
             make_float2(acc[nt2][0], acc[nt2][1]));
         acc[nt2][0] = v.x;
         acc[nt2][1] = v.y;

@@ -1,5 +1,6 @@
 // Register-fragment helpers shared by the attention kernels (mma.sync m16n8k16
-// with fp16 operands and fp32 accumulators; fp16 code conversion; quad reductions).
+// with fp16 operands and fp32 accumulators; code conversion by the fp6 / fp4
+// conversion instructions; quad reductions).
 #pragma once
 #include <cuda_fp16.h>
 #include <stdint.h>
@@ -46,30 +47,24 @@ __device__ __forceinline__ float2 h2pair(const uint16_t* p) {
   return __half22float2(*reinterpret_cast<const __half2*>(p));
 }
 
-template <uint32_t kMask>
-__device__ __forceinline__ uint32_t lop_magic(uint32_t w) {
-  // (w & kMask) | 0x64006400: the selected bits become the low mantissa bits of two
-  // fp16 values 1024 + field
-  uint32_t r;
-  asm("lop3.b32 %0, %1, %2, %3, 0xea;" : "=r"(r) : "r"(w), "n"(kMask), "n"(0x64006400u));
-  return r;
+// Four 4-bit codes in the low nibbles of the bytes of m -> two fp16 pairs (code / 8):
+// bytes 0, 1 -> lo, bytes 2, 3 -> hi (fp6 e2m3 patterns 0..15 are the values c / 8).
+__device__ __forceinline__ void cvt4(uint32_t m, uint32_t& lo, uint32_t& hi) {
+  asm("{\n .reg .b16 l, h;\n mov.b32 {l, h}, %2;\n cvt.rn.f16x2.e2m3x2 %0, l;\n cvt.rn.f16x2.e2m3x2 %1, h;\n}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(m));
+}
+// Eight 2-bit codes at bits 8b and 8b + 4 of m -> four fp16 pairs (code / 2), one per
+// byte b (fp4 e2m1 patterns 0..3 are the values c / 2).
+__device__ __forceinline__ void cvt2(uint32_t m, uint32_t (&r)[4]) {
+  asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %4;\n"
+      " cvt.rn.f16x2.e2m1x2 %0, b0;\n cvt.rn.f16x2.e2m1x2 %1, b1;\n"
+      " cvt.rn.f16x2.e2m1x2 %2, b2;\n cvt.rn.f16x2.e2m1x2 %3, b3;\n}"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+      : "r"(m));
 }
 
-__device__ __forceinline__ uint32_t hfma2_u(uint32_t a, uint32_t b, uint32_t c) {
-  uint32_t r;
-  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
-  return r;
-}
-
-// fp16x2 constants: field = (1024 + scale * code) * (1/scale) - 1024/scale, exact
-constexpr uint32_t kH_One = 0x3C003C00u;       // 1
-constexpr uint32_t kH_M1024 = 0xE400E400u;     // -1024
-constexpr uint32_t kH_Sixteenth = 0x2C002C00u; // 1/16
-constexpr uint32_t kH_M64 = 0xD400D400u;       // -64
-constexpr uint32_t kH_Quarter = 0x34003400u;   // 1/4
-constexpr uint32_t kH_M256 = 0xDC00DC00u;      // -256
-constexpr uint32_t kH_64th = 0x24002400u;      // 1/64
-constexpr uint32_t kH_M16 = 0xCC00CC00u;       // -16
+constexpr uint32_t kH_One = 0x3C003C00u;       // fp16x2 (1, 1)
 
 __device__ __forceinline__ void mma16816(float* d, const uint32_t* a, uint32_t b0, uint32_t b1) {
   asm volatile(

@@ -128,27 +128,30 @@ __device__ __forceinline__ void fwht_acc(float (&acc)[16][2], int c) {
         }
 }
 
-// fp16 pair of codes (1024 + field * scale) -> field, stored at `dst`.
+// A pair of fp16 code values stored at `dst`.
 __device__ __forceinline__ void put_pair(uint16_t* dst, uint32_t v) { *reinterpret_cast<uint32_t*>(dst) = v; }
 
-// 4-bit word: four pairs of codes (even, odd index) at index offsets 0, 8, 16, 24
-// from i0 along a shared row: row + i0 + {0, 8, 16, 24}.
+// 4-bit word (codes of indices i0 + {0, 1, 8, 9} of two 16-index steps, low nibbles
+// for the first step, high nibbles for the second): pairs code / 8 at index offsets
+// 0, 8, 16, 24 from i0 along a shared row.
 __device__ __forceinline__ void nibble_word(uint32_t w, uint16_t* row, int i0) {
-  const uint32_t w8 = w >> 8;
-  put_pair(row + i0, hfma2_u(lop_magic<0x000F000Fu>(w), kH_One, kH_M1024));
-  put_pair(row + i0 + 8, hfma2_u(lop_magic<0x00F000F0u>(w), kH_Sixteenth, kH_M64));
-  put_pair(row + i0 + 16, hfma2_u(lop_magic<0x000F000Fu>(w8), kH_One, kH_M1024));
-  put_pair(row + i0 + 24, hfma2_u(lop_magic<0x00F000F0u>(w8), kH_Sixteenth, kH_M64));
+  uint32_t lo, hi;
+  cvt4(w & 0x0F0F0F0Fu, lo, hi);
+  put_pair(row + i0, lo);
+  put_pair(row + i0 + 8, hi);
+  cvt4((w >> 4) & 0x0F0F0F0Fu, lo, hi);
+  put_pair(row + i0 + 16, lo);
+  put_pair(row + i0 + 24, hi);
 }
-// 2-bit word: eight pairs at index offsets 0, 8, ..., 56 from i0.
+// 2-bit word (four 16-index steps, one per byte): pairs code / 2 at index offsets
+// 16k + 8r from i0 (k the byte, r = 0 for bits {0, 4} and 1 for bits {2, 6}).
 __device__ __forceinline__ void crumb_word(uint32_t w, uint16_t* row, int i0) {
 #pragma unroll
-  for (int sg = 0; sg < 2; ++sg) {
-    const uint32_t x = sg ? (w >> 8) : w;
-    put_pair(row + i0 + 32 * sg, hfma2_u(lop_magic<0x00030003u>(x), kH_One, kH_M1024));
-    put_pair(row + i0 + 32 * sg + 8, hfma2_u(lop_magic<0x000C000Cu>(x), kH_Quarter, kH_M256));
-    put_pair(row + i0 + 32 * sg + 16, hfma2_u(lop_magic<0x00300030u>(x), kH_Sixteenth, kH_M64));
-    put_pair(row + i0 + 32 * sg + 24, hfma2_u(lop_magic<0x00C000C0u>(x), kH_64th, kH_M16));
+  for (int r = 0; r < 2; ++r) {
+    uint32_t v[4];
+    cvt2((w >> (2 * r)) & 0x33333333u, v);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) put_pair(row + i0 + 16 * k + 8 * r, v[k]);
   }
 }
 
@@ -188,10 +191,13 @@ __device__ __forceinline__ void unpack_tile(const uint8_t* rec, uint16_t* ks, ui
     const uint16_t* vm = reinterpret_cast<const uint16_t*>(rec + L::kVMetaOff);
     const float kr = kLean ? 1.0f : h2f_bits(km[L::kKr + tid]);
     const float vc = kLean ? 1.0f : h2f_bits(vm[L::kVc + tid]);
-    sc[0 * 128 + tid] = kr * h2f_bits(km[L::kKs + tid]);   // per channel: r s (keys)
+    // the fp16 codes in shared memory are code / 8 (4-bit) or code / 2 (2-bit): the
+    // step vectors carry the factor back (a power of two: exact)
+    constexpr float kKf = KB == 4 ? 8.0f : 2.0f, kVf = VB == 4 ? 8.0f : 2.0f;
+    sc[0 * 128 + tid] = kKf * kr * h2f_bits(km[L::kKs + tid]);   // per channel: r s (keys)
     sc[1 * 128 + tid] = kr * h2f_bits(km[L::kKz + tid]);   // per channel: r z
     sc[2 * 128 + tid] = h2f_bits(km[L::kKc + tid]);        // per token: c
-    sc[3 * 128 + tid] = vc * h2f_bits(vm[L::kVs + tid]);   // per token: c s (values)
+    sc[3 * 128 + tid] = kVf * vc * h2f_bits(vm[L::kVs + tid]);   // per token: c s (values)
     sc[4 * 128 + tid] = vc * h2f_bits(vm[L::kVz + tid]);   // per token: c z
     sc[5 * 128 + tid] = h2f_bits(vm[L::kVr + tid]);        // per channel: r
   }

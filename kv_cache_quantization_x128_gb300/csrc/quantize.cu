@@ -471,8 +471,9 @@ __device__ __forceinline__ bool quantize_group(float* vec, uint8_t* stage, const
     // v = (x * own) * w_e + c0_e = (y - z) / s + 1/2, clamped to [0, levels]; the
     // round-down add of 2^23 leaves 0x4B000000 + floor(v) in the bits, and each
     // word accumulates (bits << shift) with the 0x4B000000 terms removed at the end.
-    // The shifts are constants (the thread's half-word offset 16p is applied once,
-    // after the bias is removed): a runtime shift per code cost 5 % of the kernel.
+    // The shifts are constants (the thread's offset, 8p for nibbles and 4p for
+    // crumbs, is applied once after the bias is removed): a runtime shift per code
+    // cost 5 % of the kernel.
     uint32_t part[2][4] = {{0, 0, 0, 0}, {0, 0, 0, 0}};
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
@@ -492,40 +493,37 @@ __device__ __forceinline__ bool quantize_group(float* vec, uint8_t* stage, const
       for (int u = 0; u < 4; ++u) {
         const int kl = 4 * q + u;
         if (kBits == 4) {
-          // element e = 32w + 16a + 8b + 2g4 + p -> k = 16w + 8a + 4b + g4, nibble 4p + 2a + b of word w
+          // element e = 32w + 16a + 8b + 2g4 + p -> k = 16w + 8a + 4b + g4, nibble 4b + 2p + a of word w
           const int wl = kl >> 4, a = (kl >> 3) & 1, b = (kl >> 2) & 1, g4 = kl & 3;
-          part[wl][g4] += bits[u] << (4 * (2 * a + b));
+          part[wl][g4] += bits[u] << (16 * b + 4 * a);
         } else {
-          // element e = 64u + 16k2 + 8b + 2g4 + p -> k = 32u + 8k2 + 4b + g4, crumb 8p + 2k2 + b of word u
+          // element e = 64u + 16k2 + 8b + 2g4 + p -> k = 32u + 8k2 + 4b + g4, crumb 4k2 + 2p + b of word u
           const int k2 = (kl >> 3) & 3, b = (kl >> 2) & 1, g4 = kl & 3;
-          part[0][g4] += bits[u] << (2 * (2 * k2 + b));
+          part[0][g4] += bits[u] << (8 * k2 + 2 * b);
         }
       }
     }
     if (kBits == 4) {
       // each word got 4 nibbles (a, b) from this thread: remove their 0x4B000000 terms
-      const uint32_t bias = 0x4B000000u * (1u + (1u << 4) + (1u << 8) + (1u << 12));
+      const uint32_t bias = 0x4B000000u * (1u + (1u << 4) + (1u << 16) + (1u << 20));
       uint8_t* row = stage + line * 64;
 #pragma unroll
       for (int g4 = 0; g4 < 4; ++g4) {
-        const uint32_t m0 = (part[0][g4] - bias) << (16 * p), m1 = (part[1][g4] - bias) << (16 * p);
+        const uint32_t m0 = (part[0][g4] - bias) << (8 * p), m1 = (part[1][g4] - bias) << (8 * p);
         const uint32_t f0 = m0 | __shfl_xor_sync(0xffffffffu, m0, 2);
         const uint32_t f1 = m1 | __shfl_xor_sync(0xffffffffu, m1, 2);
         if (p == hh) *reinterpret_cast<uint2*>(row + g4 * 16 + hh * 8) = make_uint2(f0, f1);
       }
     } else {
-      // each word got 8 crumbs (k2, b) from this thread
-      uint32_t geo = 0;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) geo += 1u << (2 * j);
-      const uint32_t bias = 0x4B000000u * geo;
+      // each word got 8 crumbs (k2, b) from this thread, at bits 8k2 + 2b
+      const uint32_t bias = 0x4B000000u * 0x05050505u;
       const int i = line;
       // keys: token row of 32 bytes, 8-byte group g4, word hh; values: 512-byte
       // panel of 16 channels, 16-byte cell of the channel pair, word hh
       uint8_t* base = kKind == 0 ? stage + i * 32 + hh * 4 : stage + (i >> 4) * 512 + ((i >> 3) & 1) * 8 + hh * 4;
 #pragma unroll
       for (int g4 = 0; g4 < 4; ++g4) {
-        const uint32_t m = (part[0][g4] - bias) << (16 * p);
+        const uint32_t m = (part[0][g4] - bias) << (4 * p);
         const uint32_t f = m | __shfl_xor_sync(0xffffffffu, m, 2);
         const int off = kKind == 0 ? g4 * 8 : ((i & 7) * 4 + g4) * 16;
         if (p == hh) *reinterpret_cast<uint32_t*>(base + off) = f;

@@ -201,10 +201,14 @@ def k4_position(i: int, t: int):
 
     Token t owns bytes [64 t, 64 t + 64): four 16-byte groups g4 = (i >> 1) & 3,
     each four little-endian 32-bit words w = i >> 5. Within a word, nibble
-    p = 4 (i & 1) + 2 ((i >> 4) & 1) + ((i >> 3) & 1), nibble p at bits 4p..4p+3."""
+    p = 4 ((i >> 3) & 1) + 2 (i & 1) + ((i >> 4) & 1), nibble p at bits 4p..4p+3:
+    the low nibbles of bytes (0, 1) and (2, 3) hold channels 2c + {0, 1} and
+    2c + {8, 9} of the word's first 16 channels, the high nibbles those of its last 16
+    (c = g4), so one 16-bit half of the word masked to low nibbles is a pair of
+    fp6 (e2m3) values code / 8."""
     g4 = (i >> 1) & 3
     w = i >> 5
-    p = 4 * (i & 1) + 2 * ((i >> 4) & 1) + ((i >> 3) & 1)
+    p = 4 * ((i >> 3) & 1) + 2 * (i & 1) + ((i >> 4) & 1)
     return t * 64 + g4 * 16 + w * 4 + p // 2, 4 * (p % 2)
 
 
@@ -214,10 +218,13 @@ def k2_position(i: int, t: int):
 
     Token t owns bytes [32 t, 32 t + 32): four 8-byte groups g4 = (i >> 1) & 3,
     each two little-endian words u = i >> 6. Within a word, crumb
-    p = 8 (i & 1) + 2 ((i >> 4) & 3) + ((i >> 3) & 1), crumb p at bits 2p..2p+1."""
+    p = 4 ((i >> 4) & 3) + 2 (i & 1) + ((i >> 3) & 1), crumb p at bits 2p..2p+1:
+    byte k of the word holds the 16-channel step k, channels 2c + {0, 1} at bits
+    {0, 4} and 2c + {8, 9} at bits {2, 6} of the byte (c = g4), so a byte masked to
+    bits {0, 1, 4, 5} is a pair of fp4 (e2m1) values code / 2."""
     g4 = (i >> 1) & 3
     u = i >> 6
-    p = 8 * (i & 1) + 2 * ((i >> 4) & 3) + ((i >> 3) & 1)
+    p = 4 * ((i >> 4) & 3) + 2 * (i & 1) + ((i >> 3) & 1)
     return t * 32 + g4 * 8 + u * 4 + p // 4, 2 * (p % 4)
 
 
@@ -229,12 +236,13 @@ def v2_position(i: int, t: int):
     16-byte cell (i & 7) * 4 + g4 with g4 = (t >> 1) & 3 holds 8 bytes for channel
     i with (i >> 3) & 1 == 0 followed by 8 bytes for its partner i + 8; each 8
     bytes are two little-endian words u = t >> 6. Within a word, crumb
-    p = 8 (t & 1) + 2 ((t >> 4) & 3) + ((t >> 3) & 1), crumb p at bits 2p..2p+1."""
+    p = 4 ((t >> 4) & 3) + 2 (t & 1) + ((t >> 3) & 1), crumb p at bits 2p..2p+1
+    (the 2-bit key order with the token in the channel's place)."""
     m = i >> 4
     cell = (i & 7) * 4 + ((t >> 1) & 3)
     which = (i >> 3) & 1
     u = t >> 6
-    p = 8 * (t & 1) + 2 * ((t >> 4) & 3) + ((t >> 3) & 1)
+    p = 4 * ((t >> 4) & 3) + 2 * (t & 1) + ((t >> 3) & 1)
     return m * 512 + cell * 16 + which * 8 + u * 4 + p // 4, 2 * (p % 4)
 
 
@@ -243,10 +251,10 @@ def v4_position(i: int, t: int):
     the start of the value codes: the 4-bit key layout with the roles of channel
     and token exchanged. Channel i owns bytes [64 i, 64 i + 64): four 16-byte
     groups g4 = (t >> 1) & 3, each four words w = t >> 5; nibble
-    p = 4 (t & 1) + 2 ((t >> 4) & 1) + ((t >> 3) & 1) at bits 4p..4p+3."""
+    p = 4 ((t >> 3) & 1) + 2 (t & 1) + ((t >> 4) & 1) at bits 4p..4p+3."""
     g4 = (t >> 1) & 3
     w = t >> 5
-    p = 4 * (t & 1) + 2 * ((t >> 4) & 1) + ((t >> 3) & 1)
+    p = 4 * ((t >> 3) & 1) + 2 * (t & 1) + ((t >> 4) & 1)
     return i * 64 + g4 * 16 + w * 4 + p // 2, 4 * (p % 2)
 
 

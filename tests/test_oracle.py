@@ -409,62 +409,76 @@ def test_preset_compression_ratios():
     assert o.compression_ratio("k2v2") == 65536 / 10240 == 6.4
 
 
-def _fragment_codes_k2(rec, t, c, ks):
-    """The four 2-bit key codes a decode thread with column c reads for token t in
-    k-step ks (channels 16 ks + 2c + {0, 1, 8, 9}): word ks >> 2 of its 8-byte group,
-    crumbs 2 (ks & 3) and 2 (ks & 3) + 1 of the low (even channel) and high (odd
-    channel) 16-bit halves."""
-    word = int.from_bytes(bytes(rec[t * 32 + c * 8 + (ks >> 2) * 4: t * 32 + c * 8 + (ks >> 2) * 4 + 4]), "little")
+def _word(area, off):
+    return int.from_bytes(bytes(area[off:off + 4]), "little")
+
+
+def _fragment_codes_4bit(word, c, m):
+    """The eight 4-bit codes a decode thread with column c of an m16n8k16 operand
+    takes from word m of its 16-byte group (k-steps 2m and 2m + 1): the word shifted
+    by 4h and masked to the low nibble of each byte gives k-step 2m + h, byte b
+    holding row 2c + (b & 1) + 8 (b >> 1); returns {16 ks + row: code}."""
     out = {}
-    for half8 in (0, 1):
-        for odd in (0, 1):
-            bit = 16 * odd + 2 * (2 * (ks & 3) + half8)
-            out[16 * ks + 2 * c + 8 * half8 + odd] = (word >> bit) & 3
+    for h in (0, 1):
+        masked = (word >> (4 * h)) & 0x0F0F0F0F
+        for b in range(4):
+            out[16 * (2 * m + h) + 2 * c + (b & 1) + 8 * (b >> 1)] = (masked >> (8 * b)) & 15
     return out
 
 
-def _fragment_codes_v4(area, i, c, ks):
-    """The four 4-bit value codes a decode thread with column c reads for channel i
-    in token k-step ks (tokens 16 ks + 2c + {0, 1, 8, 9}): word ks >> 1 of its
-    16-byte group, nibbles 2 (ks & 1) and 2 (ks & 1) + 1 of each 16-bit half."""
-    off = i * 64 + c * 16 + (ks >> 1) * 4
-    word = int.from_bytes(bytes(area[off:off + 4]), "little")
+def _fragment_codes_2bit(word, c, u):
+    """The sixteen 2-bit codes a decode thread with column c takes from word u of
+    its 8-byte group (k-steps 4u..4u + 3): the word shifted by 2r and masked to bits
+    {0, 1, 4, 5} of each byte gives, in byte k, rows 2c + 8r (low nibble) and
+    2c + 8r + 1 (high nibble) of k-step 4u + k; returns {16 ks + row: code}."""
     out = {}
-    for half8 in (0, 1):
-        for odd in (0, 1):
-            bit = 16 * odd + 4 * (2 * (ks & 1) + half8)
-            out[16 * ks + 2 * c + 8 * half8 + odd] = (word >> bit) & 15
+    for r in (0, 1):
+        masked = (word >> (2 * r)) & 0x33333333
+        for k in range(4):
+            byte = (masked >> (8 * k)) & 0xFF
+            out[16 * (4 * u + k) + 2 * c + 8 * r] = byte & 3
+            out[16 * (4 * u + k) + 2 * c + 8 * r + 1] = byte >> 4
     return out
 
 
-def test_new_layouts_serve_the_mma_fragments():
-    """The 2-bit key and 4-bit value layouts are read by tensor-core fragments: a
-    thread with column c of an m16n8k16 operand needs rows 2c, 2c+1, 2c+8, 2c+9
-    of each 16-row k-step. Read the way the decode reads them, every (channel,
-    token) code of a packed record comes back exactly once."""
-    rng = np.random.default_rng(23)
-    kq, vq = _random_quantized(rng, 1, 2, 4)
-    lay_k = o.LAYOUTS["k2v2"]
-    rec_k = o.pack_record(kq, dict(vq, bits=2, codes=vq["codes"] & 3), "k2v2")[0]
+def _check_fragment_reads(area, codes, offsets, bits):
+    """Every (line, element) code comes back exactly once through the fragment reads
+    listed in `offsets`: (line, c, word index, byte offset of the word)."""
     seen = np.zeros((128, 128), int)
-    for t in range(128):
-        for c in range(4):
-            for ks in range(8):
-                for ch, val in _fragment_codes_k2(rec_k[lay_k.k_code_off:], t, c, ks).items():
-                    assert val == kq["codes"][0, ch, t]
-                    seen[ch, t] += 1
+    for line, c, wi, off in offsets:
+        read = _fragment_codes_4bit if bits == 4 else _fragment_codes_2bit
+        for e, val in read(_word(area, off), c, wi).items():
+            assert val == codes[line, e], (line, e)
+            seen[line, e] += 1
     assert (seen == 1).all()
-    lay_v = o.LAYOUTS["k4v4"]
-    rec_v = o.pack_record(dict(kq, bits=4), vq, "k4v4")[0]
-    area = rec_v[lay_v.v_code_off:lay_v.v_code_off + lay_v.v_code_bytes]
-    seen[:] = 0
-    for i in range(128):
-        for c in range(4):
-            for ks in range(8):
-                for tok, val in _fragment_codes_v4(area, i, c, ks).items():
-                    assert val == vq["codes"][0, i, tok]
-                    seen[i, tok] += 1
-    assert (seen == 1).all()
+
+
+def test_code_layouts_serve_the_mma_fragments():
+    """Every code layout is read by tensor-core fragments: a thread with column c of
+    an m16n8k16 operand needs rows 2c, 2c+1, 2c+8, 2c+9 of each 16-row k-step, and
+    converts each register's pair of codes with one fp6 (4-bit) or fp4 (2-bit)
+    conversion. Read that way, every (channel, token) code of a packed record comes
+    back exactly once: keys by token line (elements = channels), values by channel
+    line (elements = tokens)."""
+    rng = np.random.default_rng(23)
+    k4q, v4q = _random_quantized(rng, 1, 4, 4)
+    k2q, v2q = dict(k4q, bits=2, codes=k4q["codes"] & 3), dict(v4q, bits=2, codes=v4q["codes"] & 3)
+    for preset, kk, vv in (("k4v2", k4q, v2q), ("k2v2", k2q, v2q), ("k4v4", k4q, v4q)):
+        lay = o.LAYOUTS[preset]
+        rec = o.pack_record(kk, vv, preset)[0]
+        karea = rec[lay.k_code_off:lay.k_code_off + lay.k_code_bytes]
+        varea = rec[lay.v_code_off:lay.v_code_off + lay.v_code_bytes]
+        if lay.k_bits == 4:   # token row of 64 bytes: group c, words m
+            offs = [(t, c, m, t * 64 + c * 16 + m * 4) for t in range(128) for c in range(4) for m in range(4)]
+        else:                 # token row of 32 bytes: group c, words u
+            offs = [(t, c, u, t * 32 + c * 8 + u * 4) for t in range(128) for c in range(4) for u in range(2)]
+        _check_fragment_reads(karea, kk["codes"][0].T, offs, lay.k_bits)
+        if lay.v_bits == 4:   # channel row of 64 bytes
+            offs = [(i, c, m, i * 64 + c * 16 + m * 4) for i in range(128) for c in range(4) for m in range(4)]
+        else:                 # 512-byte panel of 16 channels, 16-byte cell (i & 7, c), partner half, words u
+            offs = [(i, c, u, (i >> 4) * 512 + ((i & 7) * 4 + c) * 16 + ((i >> 3) & 1) * 8 + u * 4)
+                    for i in range(128) for c in range(4) for u in range(2)]
+        _check_fragment_reads(varea, vv["codes"][0], offs, lay.v_bits)
 
 
 def test_bit_width_changes_only_the_step_and_zero():
