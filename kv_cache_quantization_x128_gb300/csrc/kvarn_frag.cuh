@@ -16,12 +16,17 @@ __device__ __forceinline__ void split2(float x0, float x1, uint32_t& hi, uint32_
   lo = *reinterpret_cast<const uint32_t*>(&l);
 }
 
-// The same split of an fp32 pair; the residual x - hi is one packed fma (exact).
+// The same split of an fp32 pair; each residual x - hi is one mixed-precision fma
+// of the fp16 half with -1 (exact).
 __device__ __forceinline__ void split2p(float2 x, uint32_t& hi, uint32_t& lo) {
   const __half2 h = __floats2half2_rn(x.x, x.y);
-  const float2 r = __ffma2_rn(__half22float2(h), make_float2(-1.f, -1.f), x);
-  const __half2 l = __floats2half2_rn(r.x, r.y);
   hi = *reinterpret_cast<const uint32_t*>(&h);
+  float r0, r1;
+  asm("{\n .reg .f16 h0, h1, m;\n mov.b32 {h0, h1}, %2;\n mov.b16 m, 0xBC00;\n"
+      " fma.rn.f32.f16 %0, h0, m, %3;\n fma.rn.f32.f16 %1, h1, m, %4;\n}"
+      : "=f"(r0), "=f"(r1)
+      : "r"(hi), "f"(x.x), "f"(x.y));
+  const __half2 l = __floats2half2_rn(r0, r1);
   lo = *reinterpret_cast<const uint32_t*>(&l);
 }
 
