@@ -131,8 +131,8 @@ class ClockSampler:
 # ----------------------------------------------------------------------------- traffic from profiles
 # sources a kernel's profile summary was captured from (hashed together, in order)
 PROFILE_SOURCES = {
-    "quantize": ["quantize.cu", "kvarn_tc.cuh", "kvarn_common.cuh"],
-    "decode": ["decode.cu", "kvarn_common.cuh", "kvarn_frag.cuh"],
+    "quantize": ["quantize.cu", "quantize_group.cuh", "kvarn_tc.cuh", "kvarn_common.cuh"],
+    "decode": ["decode.cu", "decode_tile.cuh", "kvarn_common.cuh", "kvarn_frag.cuh"],
 }
 
 

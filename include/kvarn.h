@@ -230,6 +230,32 @@ KVARN_API kvarn_status kvarn_decode_attention(const uint16_t* q, const uint8_t* 
                                     const kvarn_meta* meta, void* stream);
 
 /*
+ * One serving step in one launch: kvarn_append_decode (the new token of every
+ * sequence into the workspace; tiles it completes quantized into their blocks),
+ * then kvarn_decode_attention over the lengths after the append, with the same
+ * results as those two calls in order. A cooperative launch of one CTA per SM
+ * whose phases (append and tile quantization; attention over the tiles; merge
+ * with the workspace tokens) meet at grid-wide barriers; every wait is bounded
+ * and reports KVARN_FLAG_WAIT_TIMEOUT instead of hanging. Capturable in a CUDA graph.
+ *   q             fp16 [n_seqs][num_q_heads][128], the new query of each sequence.
+ *   k_new, v_new  fp16 [n_seqs][num_kv_heads][128].
+ *   seq_lens      int32 [n_seqs], lengths before the append, >= 0.
+ *   seq_lens_out  int32 [n_seqs] (required): receives seq_lens[s] + 1, the lengths
+ *                 the attention uses. Must not alias seq_lens.
+ *   block_tables  int32 [n_seqs][max_blocks_per_seq].
+ *   workspace     fp16 workspace (required).
+ *   n_seqs        0..65535.
+ *   out           fp16 [n_seqs][num_q_heads][128].
+ *   scratch       device buffer of >= kvarn_decode_scratch_bytes(meta, n_seqs).
+ * Returns KVARN_ECUDA if the device cannot hold the grid co-resident.
+ */
+KVARN_API kvarn_status kvarn_serve_step(const uint16_t* q, const uint16_t* k_new, const uint16_t* v_new,
+                                        const int32_t* seq_lens, int32_t* seq_lens_out,
+                                        const int32_t* block_tables, int32_t n_seqs, uint16_t* workspace,
+                                        uint8_t* cache, uint16_t* out, void* scratch, size_t scratch_bytes,
+                                        const kvarn_meta* meta, void* stream);
+
+/*
  * Decode attention that allocates nothing and needs no scratch from the caller.
  * This entry point has no counterpart in the KVarN paper or README; it exists for
  * callers that cannot allocate device memory: e.g. a serving engine whose free

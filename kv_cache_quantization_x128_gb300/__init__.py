@@ -39,6 +39,10 @@ _SIGS = {
     "kvarn_decode_attention_static": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                                      ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
                                                      ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
+    "kvarn_serve_step": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p,
+                                        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t,
+                                        ctypes.c_void_p, ctypes.c_void_p]),
     "kvarn_prefill_attention": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                                ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p,
                                                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
@@ -187,6 +191,24 @@ def kvarn_decode_attention(q, cache, workspace, block_tables, seq_lens, out, scr
                                        _ptr(seq_lens, "seq_lens", torch.int32, n), n,
                                        _ptr(out, "out", torch.float16), _ptr(scratch, "scratch"), nbytes,
                                        ctypes.byref(meta), _stream(stream)))
+
+
+def kvarn_serve_step(q, k_new, v_new, seq_lens, seq_lens_out, block_tables, workspace, cache, out, scratch,
+                     meta: KvarnMeta, stream=None):
+    """One serving step in one launch: kvarn_append_decode then
+    kvarn_decode_attention over seq_lens_out. q, out: fp16 [n_seqs, Hq, 128];
+    k_new, v_new: fp16 [n_seqs, Hkv, 128]; seq_lens / seq_lens_out: int32 [n_seqs];
+    scratch: at least decode_scratch_bytes(meta, n_seqs) bytes."""
+    import torch
+    n = int(q.shape[0])
+    nbytes = 0 if scratch is None else scratch.numel() * scratch.element_size()
+    _check(_lib.kvarn_serve_step(_ptr(q, "q", torch.float16), _ptr(k_new, "k_new", torch.float16),
+                                 _ptr(v_new, "v_new", torch.float16), _ptr(seq_lens, "seq_lens", torch.int32, n),
+                                 _ptr(seq_lens_out, "seq_lens_out", torch.int32, n),
+                                 _ptr(block_tables, "block_tables", torch.int32), n,
+                                 _ptr(workspace, "workspace", torch.float16), _ptr(cache, "cache", torch.uint8),
+                                 _ptr(out, "out", torch.float16), _ptr(scratch, "scratch"), nbytes,
+                                 ctypes.byref(meta), _stream(stream)))
 
 
 def kvarn_decode_attention_static(q, cache, workspace, block_tables, seq_lens, out, meta: KvarnMeta, stream=None):

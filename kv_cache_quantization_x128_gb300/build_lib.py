@@ -15,7 +15,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libkvarn.so")
-SOURCES = ["api.cu", "api_static.cu", "quantize.cu", "decode.cu", "prefill.cu"]
+SOURCES = ["api.cu", "api_static.cu", "quantize.cu", "decode.cu", "prefill.cu", "serve.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-fvisibility=hidden", "-Xptxas", "-v"]
 

@@ -184,6 +184,40 @@ kvarn_status kvarn_decode_attention(const uint16_t* q, const uint8_t* cache, con
                      "kvarn_decode_attention");
 }
 
+kvarn_status kvarn_serve_step(const uint16_t* q, const uint16_t* k_new, const uint16_t* v_new,
+                              const int32_t* seq_lens, int32_t* seq_lens_out, const int32_t* block_tables,
+                              int32_t n_seqs, uint16_t* workspace, uint8_t* cache, uint16_t* out, void* scratch,
+                              size_t scratch_bytes, const kvarn_meta* meta, void* stream) {
+  g_err[0] = 0;
+  KV_TRY(check_meta(meta));
+  if (n_seqs < 0 || n_seqs > 65535) return fail(KVARN_EINVAL, "n_seqs must be in 0..65535 (got %lld)", (long long)n_seqs);
+  if (n_seqs == 0) return KVARN_OK;
+  KV_TRY(need_ptr(q, "q"));
+  KV_TRY(need_ptr(k_new, "k_new"));
+  KV_TRY(need_ptr(v_new, "v_new"));
+  KV_TRY(need_ptr(seq_lens, "seq_lens"));
+  KV_TRY(need_ptr(seq_lens_out, "seq_lens_out"));
+  if (seq_lens_out == seq_lens) return fail(KVARN_EINVAL, "seq_lens_out must not alias seq_lens");
+  KV_TRY(need_ptr(block_tables, "block_tables"));
+  KV_TRY(need_ptr(workspace, "workspace"));
+  KV_TRY(need_ptr(cache, "cache"));
+  KV_TRY(need_ptr(out, "out"));
+  if (meta->max_blocks_per_seq < 1) return fail(KVARN_EINVAL, "max_blocks_per_seq must be >= 1");
+  const size_t need = kvarn::decode_part_bytes(n_seqs, meta->num_kv_heads, meta->max_blocks_per_seq);
+  KV_TRY(need_ptr(scratch, "scratch"));
+  if (scratch_bytes < need)
+    return fail(KVARN_ESCRATCH, "scratch too small: need %lld bytes", static_cast<long long>(need));
+  unsigned* fl = nullptr;
+  KV_TRY(flags_ptr(&fl));
+  return cuda_status(kvarn::launch_serve_step(q, k_new, v_new, seq_lens, seq_lens_out, block_tables, workspace,
+                                              cache, n_seqs, meta->num_kv_heads,
+                                              meta->num_q_heads / meta->num_kv_heads, meta->max_blocks_per_seq,
+                                              meta->num_blocks, meta->k_bits, meta->v_bits,
+                                              meta->layout == KVARN_LAYOUT_LEAN, meta->n_iters, meta->eps, out,
+                                              scratch, fl, static_cast<cudaStream_t>(stream)),
+                     "kvarn_serve_step");
+}
+
 kvarn_status kvarn_prefill_attention(const uint16_t* q, const uint16_t* k_new, const uint16_t* v_new,
                                      const int32_t* cu_tokens, const int32_t* seq_lens, int32_t n_seqs,
                                      int32_t max_chunk, const int32_t* block_tables, const uint8_t* cache,

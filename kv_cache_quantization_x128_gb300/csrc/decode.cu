@@ -23,62 +23,12 @@
 //   decode_merge_kernel - per (sequence, kv-head): merges the partial records of
 //     the warps that covered it with the fp16 workspace tokens of the partial
 //     last tile, un-rotates by H^T and normalises.
+#include "decode_tile.cuh"
 #include "kvarn_common.cuh"
-#include "kvarn_frag.cuh"
 #include "kvarn_launch.h"
 
 namespace kvarn {
 namespace {
-
-constexpr float kLog2e = 1.4426950408889634f;
-constexpr int kMaxWarps = 8;                    // consumer warps per CTA (at most)
-constexpr int kStages = 2;                      // bulk-copy stages per warp
-constexpr int kMaxCtas = 1024;                  // upper bound used to size scratch
-constexpr int kPartStride = 132;                // floats per q-head: acc[128], max, sum, pad
-constexpr int kRecFloats = 8 * kPartStride;     // one partial record (8 q-head slots)
-
-// Split kernel shape for KB-bit keys and VB-bit values: the most warps (8 down to
-// 6) whose two records each fit in shared memory; k4v4's 18432-byte records get 6.
-template <int KB, int VB, bool kLean = false>
-struct SplitCfg {
-  using L = RecordLayout<KB, VB, kLean>;
-  static constexpr int fits(int w) { return w * kStages * L::kBytes + w * kStages * 8 <= 232448; }
-  static constexpr int kWarps = fits(8) ? 8 : fits(7) ? 7 : 6;
-  static constexpr int kSmem = kWarps * kStages * L::kBytes + kWarps * kStages * 8;
-  static_assert(kSmem <= 232448, "decode stages");
-};
-
-struct DecodeArgs {
-  const uint16_t* q;
-  const uint8_t* cache;
-  const int32_t* block_tables;
-  const int32_t* seq_lens;
-  int64_t* prefix;      // [n_seqs + 1] exclusive prefix of full tiles
-  int64_t* ranges;      // [n_ctas * kWarps][2] tile range of each split-kernel warp
-  float* part;          // [records][8][132]
-  unsigned* flags;
-  int64_t num_blocks;
-  int n_seqs;
-  int hkv;
-  int group;            // q-heads per kv-head (1..8)
-  int max_blocks;
-  int n_ctas;           // CTAs of the split kernel
-  int warps;            // warps per CTA of the split kernel
-};
-
-__device__ __forceinline__ int full_tiles(const DecodeArgs& a, int s) {
-  const int L = max(a.seq_lens[s], 0);
-  return min(L / kB, a.max_blocks);
-}
-
-// Range [beg, end) of global tiles owned by warp `wg` of the split kernel.
-template <int kWarps>
-__device__ __forceinline__ void warp_range(int64_t total, int n_ctas, int64_t wg, int64_t& beg, int64_t& end) {
-  const int64_t b = wg / kWarps, w = wg % kWarps;
-  const int64_t c0 = b * total / n_ctas, c1 = (b + 1) * total / n_ctas;
-  beg = c0 + w * (c1 - c0) / kWarps;
-  end = c0 + (w + 1) * (c1 - c0) / kWarps;
-}
 
 // ------------------------------------------------------------------ scan
 __global__ void __launch_bounds__(1024) decode_scan_kernel(DecodeArgs a) {
@@ -109,496 +59,18 @@ __global__ void __launch_bounds__(1024) decode_scan_kernel(DecodeArgs a) {
   if (t == 1023) a.prefix[a.n_seqs] = part_sums[1023];
 }
 
-// ------------------------------------------------------------------ tile cursor
-struct Cursor {
-  int s, h, ti, nf;
-};
-
-// sequence s holding global tile g (prefix[s]*hkv <= g < prefix[s+1]*hkv)
-__device__ __forceinline__ Cursor locate(const DecodeArgs& a, int64_t g) {
-  int lo = 0, hi = a.n_seqs - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (a.prefix[mid] * a.hkv <= g) lo = mid; else hi = mid - 1;
-  }
-  Cursor c;
-  c.s = lo;
-  c.nf = static_cast<int>(a.prefix[lo + 1] - a.prefix[lo]);
-  const int64_t off = g - a.prefix[lo] * a.hkv;
-  c.h = static_cast<int>(off / c.nf);
-  c.ti = static_cast<int>(off - static_cast<int64_t>(c.h) * c.nf);
-  return c;
-}
-
-__device__ __forceinline__ void advance(const DecodeArgs& a, Cursor& c) {
-  if (++c.ti < c.nf) return;
-  c.ti = 0;
-  if (++c.h < a.hkv) return;
-  c.h = 0;
-  do {
-    ++c.s;
-    c.nf = c.s < a.n_seqs ? static_cast<int>(a.prefix[c.s + 1] - a.prefix[c.s]) : 1;
-  } while (c.nf == 0);
-}
-
-// Lane 0: start the copy of the tile at cursor `c` into `stage`; a block index
-// outside [0, num_blocks) completes the barrier phase without data and returns false.
-template <int kRecBytes>
-__device__ __forceinline__ bool issue_tile(const DecodeArgs& a, const Cursor& c, uint8_t* stage, uint64_t* bar) {
-  const int64_t blk = a.block_tables[static_cast<int64_t>(c.s) * a.max_blocks + c.ti];
-  if (blk < 0 || blk >= a.num_blocks) {
-    raise_flag(a.flags, KVARN_FLAG_BAD_BLOCK);
-    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-    return false;
-  }
-  mbar_arrive_expect_tx(bar, kRecBytes);
-  bulk_g2s(stage, a.cache + (blk * a.hkv + c.h) * static_cast<int64_t>(kRecBytes), kRecBytes, bar);
-  return true;
-}
-
-// q_r2 of this thread's 32 channels for (sequence s, kv-head h): H q * log2(e)/sqrt(128),
-// computed as FWHT(q) * log2(e) / 128. Thread (g, c) holds head g, channels
-// 16ks + 2c + {0, 1, 8, 9}; channel bits 1-2 live across the quad (lanes ^1, ^2).
-__device__ __forceinline__ void load_q(const DecodeArgs& a, int s, int h, int g, int c, float (&qv)[8][4]) {
-  const int hq = a.hkv * a.group;
-  if (g < a.group) {
-    const uint16_t* row = a.q + (static_cast<int64_t>(s) * hq + static_cast<int64_t>(h) * a.group + g) * kD;
-#pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-      const float2 p0 = h2pair(row + 16 * ks + 2 * c), p1 = h2pair(row + 16 * ks + 2 * c + 8);
-      qv[ks][0] = p0.x; qv[ks][1] = p0.y; qv[ks][2] = p1.x; qv[ks][3] = p1.y;
-    }
-  } else {
-#pragma unroll
-    for (int ks = 0; ks < 8; ++ks) qv[ks][0] = qv[ks][1] = qv[ks][2] = qv[ks][3] = 0.f;
-  }
-#pragma unroll
-  for (int ks = 0; ks < 8; ++ks) {       // channel bits 0 and 3: inside the thread
-    const float u0 = qv[ks][0] + qv[ks][1], u1 = qv[ks][0] - qv[ks][1];
-    const float u2 = qv[ks][2] + qv[ks][3], u3 = qv[ks][2] - qv[ks][3];
-    qv[ks][0] = u0 + u2; qv[ks][2] = u0 - u2; qv[ks][1] = u1 + u3; qv[ks][3] = u1 - u3;
-  }
-#pragma unroll
-  for (int bit = 1; bit <= 2; bit <<= 1) {   // channel bits 1 and 2: across the quad
-    const bool upper = (c & bit) != 0;
-#pragma unroll
-    for (int ks = 0; ks < 8; ++ks)
-#pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        const float o = __shfl_xor_sync(0xffffffffu, qv[ks][t], bit);
-        qv[ks][t] = upper ? (o - qv[ks][t]) : (qv[ks][t] + o);
-      }
-  }
-#pragma unroll
-  for (int bit = 1; bit < 8; bit <<= 1)      // channel bits 4-6: the ks index
-#pragma unroll
-    for (int ks = 0; ks < 8; ++ks)
-      if ((ks & bit) == 0)
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {
-          const float u = qv[ks][t], w = qv[ks | bit][t];
-          qv[ks][t] = u + w;
-          qv[ks | bit][t] = u - w;
-        }
-#pragma unroll
-  for (int ks = 0; ks < 8; ++ks)
-#pragma unroll
-    for (int t = 0; t < 4; ++t) qv[ks][t] *= kLog2e / 128.0f;
-}
-
-// One packed tile: update the running (max, sum, acc) of head g.
-template <int KB, int VB, bool kLean>
-__device__ __forceinline__ void attend_tile(const uint8_t* rec, const float (&qv)[8][4], int g, int c, float& m_run,
-                                            float& l_run, float (&acc)[16][2]) {
-  using L = RecordLayout<KB, VB, kLean>;
-  const uint16_t* km = reinterpret_cast<const uint16_t*>(rec + L::kKMetaOff);
-  const uint16_t* vm = reinterpret_cast<const uint16_t*>(rec + L::kVMetaOff);
-
-  // q' fragments (hi rows g, lo rows g + 8) and beta (fp32 pairs)
-  uint32_t A[8][4];
-  float2 beta2 = make_float2(0.f, 0.f);
-#pragma unroll
-  for (int ks = 0; ks < 8; ++ks) {
-    const int ch0 = 16 * ks + 2 * c;
-    // r s and r z in fp32 straight from the fp16 pairs (lean records fold r into s, z)
-    const uint32_t s0 = h2raw(km + L::kKs + ch0), s1 = h2raw(km + L::kKs + ch0 + 8);
-    const uint32_t z0 = h2raw(km + L::kKz + ch0), z1 = h2raw(km + L::kKz + ch0 + 8);
-    const uint32_t r0 = kLean ? kH_One : h2raw(km + L::kKr + ch0);
-    const uint32_t r1 = kLean ? kH_One : h2raw(km + L::kKr + ch0 + 8);
-    const float2 rs0 = mul_h2(r0, s0), rs1 = mul_h2(r1, s1);
-    const float2 rz0 = mul_h2(r0, z0), rz1 = mul_h2(r1, z1);
-    const float2 qa = make_float2(qv[ks][0], qv[ks][1]), qb = make_float2(qv[ks][2], qv[ks][3]);
-    split2p(__fmul2_rn(qa, rs0), A[ks][0], A[ks][1]);
-    split2p(__fmul2_rn(qb, rs1), A[ks][2], A[ks][3]);
-    beta2 = __ffma2_rn(qa, rz0, beta2);
-    beta2 = __ffma2_rn(qb, rz1, beta2);
-  }
-  const float beta = quad_sum(beta2.x + beta2.y);
-  const float2 beta_2 = make_float2(beta, beta);
-  const float2 kf2 = make_float2(KB == 4 ? 8.f : 2.f, KB == 4 ? 8.f : 2.f);   // codes were converted to c / 8 or c / 2
-
-  // scores of tokens 8nt + 2c + {0, 1}, four n-tiles at a time (independent chains)
-  float2 sc[16];
-#pragma unroll
-  for (int ntg = 0; ntg < 4; ++ntg) {
-    float d[4][4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) d[j][0] = d[j][1] = d[j][2] = d[j][3] = 0.f;
-    if (KB == 4) {
-      // token row of 64 bytes, this thread's 16: word m holds k-steps 2m (low byte
-      // of each half) and 2m + 1 (high byte)
-      uint32_t kw[4][4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const uint4 v = *reinterpret_cast<const uint4*>(rec + L::kKCodeOff + (8 * (4 * ntg + j) + g) * 64 + c * 16);
-        kw[j][0] = v.x; kw[j][1] = v.y; kw[j][2] = v.z; kw[j][3] = v.w;
-      }
-#pragma unroll
-      for (int m = 0; m < 4; ++m)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          uint32_t b00, b01, b10, b11;
-          cvt4(kw[j][m] & 0x0F0F0F0Fu, b00, b01);
-          cvt4((kw[j][m] >> 4) & 0x0F0F0F0Fu, b10, b11);
-          mma16816(d[j], A[2 * m], b00, b01);
-          mma16816(d[j], A[2 * m + 1], b10, b11);
-        }
-    } else {
-      // token row of 32 bytes, this thread's 8: word u holds k-steps 4u + 2sg + {0, 1}
-      // in byte sg of each half (crumbs 0-1 and 2-3 of the byte)
-      uint32_t kw[4][2];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const uint2 v = *reinterpret_cast<const uint2*>(rec + L::kKCodeOff + (8 * (4 * ntg + j) + g) * 32 + c * 8);
-        kw[j][0] = v.x; kw[j][1] = v.y;
-      }
-#pragma unroll
-      for (int u = 0; u < 2; ++u)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          uint32_t b0[4], b1[4];
-          cvt2(kw[j][u] & 0x33333333u, b0);
-          cvt2((kw[j][u] >> 2) & 0x33333333u, b1);
-#pragma unroll
-          for (int b = 0; b < 4; ++b) mma16816(d[j], A[4 * u + b], b0[b], b1[b]);
-        }
-    }
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int nt = 4 * ntg + j;
-      const float2 ck = h2pair(km + L::kKc + 8 * nt + 2 * c);
-      sc[nt] = __fmul2_rn(ck, __ffma2_rn(__fadd2_rn(make_float2(d[j][0], d[j][1]), make_float2(d[j][2], d[j][3])),
-                                         kf2, beta_2));
-    }
-  }
-
-  // online softmax (log2 domain)
-  float tmax = -INFINITY;
-#pragma unroll
-  for (int nt = 0; nt < 16; ++nt) tmax = fmax3f(tmax, sc[nt].x, sc[nt].y);
-  tmax = quad_max(tmax);
-  const float m_new = fmaxf(m_run, tmax);
-  const float corr = ex2(m_run - m_new);
-  m_run = m_new;
-  const float2 mneg = make_float2(-m_new, -m_new);
-  float2 lsum2 = make_float2(0.f, 0.f);
-#pragma unroll
-  for (int nt = 0; nt < 16; ++nt) {
-    const float2 e = __fadd2_rn(sc[nt], mneg);
-    sc[nt] = make_float2(ex2(e.x), ex2(e.y));
-    lsum2 = __fadd2_rn(lsum2, sc[nt]);
-  }
-  l_run = fmaf(l_run, corr, lsum2.x + lsum2.y);
-  const float2 corr2 = make_float2(corr, corr);
-#pragma unroll
-  for (int n = 0; n < 16; ++n) {
-    const float2 v = __fmul2_rn(make_float2(acc[n][0], acc[n][1]), corr2);
-    acc[n][0] = v.x;
-    acc[n][1] = v.y;
-  }
-
-  // p' fragments and gamma; tokens 16ks + 2c + {0,1} (nt = 2ks) and + {8,9} (nt = 2ks+1)
-  float2 gamma2 = make_float2(0.f, 0.f);
-#pragma unroll
-  for (int ks = 0; ks < 8; ++ks) {
-    const int t0 = 16 * ks + 2 * c;
-    // c s and c z in fp32 straight from the fp16 pairs (lean records fold c into s, z)
-    const uint32_t s0 = h2raw(vm + L::kVs + t0), s1 = h2raw(vm + L::kVs + t0 + 8);
-    const uint32_t z0 = h2raw(vm + L::kVz + t0), z1 = h2raw(vm + L::kVz + t0 + 8);
-    const uint32_t c0 = kLean ? kH_One : h2raw(vm + L::kVc + t0);
-    const uint32_t c1 = kLean ? kH_One : h2raw(vm + L::kVc + t0 + 8);
-    const float2 cs0 = mul_h2(c0, s0), cs1 = mul_h2(c1, s1);
-    const float2 cz0 = mul_h2(c0, z0), cz1 = mul_h2(c1, z1);
-    split2p(__fmul2_rn(sc[2 * ks], cs0), A[ks][0], A[ks][1]);
-    split2p(__fmul2_rn(sc[2 * ks + 1], cs1), A[ks][2], A[ks][3]);
-    gamma2 = __ffma2_rn(sc[2 * ks], cz0, gamma2);
-    gamma2 = __ffma2_rn(sc[2 * ks + 1], cz1, gamma2);
-  }
-  const float gamma = quad_sum(gamma2.x + gamma2.y);
-  const float2 gamma_2 = make_float2(gamma, gamma);
-  const float2 vf2 = make_float2(VB == 4 ? 8.f : 2.f, VB == 4 ? 8.f : 2.f);
-
-  if (VB == 2) {
-    // PV with 2-bit values: channel n-tile nt2 = 2np + which; cell (g, c) of panel np serves both `which`;
-    // two panels at a time -> four independent chains
-  #pragma unroll
-    for (int npg = 0; npg < 4; ++npg) {
-      uint32_t vw[2][4];
-  #pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        const uint4 v = *reinterpret_cast<const uint4*>(rec + L::kVCodeOff + (2 * npg + i) * 512 + (g * 4 + c) * 16);
-        vw[i][0] = v.x; vw[i][1] = v.y; vw[i][2] = v.z; vw[i][3] = v.w;   // [which*2 + u]
-      }
-      float d[4][4];
-  #pragma unroll
-      for (int j = 0; j < 4; ++j) d[j][0] = d[j][1] = d[j][2] = d[j][3] = 0.f;
-  #pragma unroll
-      for (int u = 0; u < 2; ++u)
-  #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int i = j >> 1, which = j & 1;
-          const uint32_t w = vw[i][which * 2 + u];
-          uint32_t b0[4], b1[4];
-          cvt2(w & 0x33333333u, b0);
-          cvt2((w >> 2) & 0x33333333u, b1);
-  #pragma unroll
-          for (int b = 0; b < 4; ++b) mma16816(d[j], A[4 * u + b], b0[b], b1[b]);
-        }
-  #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int nt2 = 2 * (2 * npg + (j >> 1)) + (j & 1);
-        const float2 rv = h2pair(vm + L::kVr + 8 * nt2 + 2 * c);
-        const float2 v = __ffma2_rn(
-            rv, __ffma2_rn(__fadd2_rn(make_float2(d[j][0], d[j][1]), make_float2(d[j][2], d[j][3])), vf2, gamma_2),
-            make_float2(acc[nt2][0], acc[nt2][1]));
-        acc[nt2][0] = v.x;
-        acc[nt2][1] = v.y;
-      }
-    }
-  } else {
-    // PV with 4-bit values: channel row of 64 bytes, this thread's 16; word m holds
-    // token k-steps 2m and 2m + 1 (low and high byte of each half); four channel
-    // n-tiles at a time -> four independent chains
-#pragma unroll
-    for (int npg = 0; npg < 4; ++npg) {
-      uint32_t vw[4][4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const uint4 v = *reinterpret_cast<const uint4*>(rec + L::kVCodeOff + (8 * (4 * npg + j) + g) * 64 + c * 16);
-        vw[j][0] = v.x; vw[j][1] = v.y; vw[j][2] = v.z; vw[j][3] = v.w;
-      }
-      float d[4][4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) d[j][0] = d[j][1] = d[j][2] = d[j][3] = 0.f;
-#pragma unroll
-      for (int m = 0; m < 4; ++m)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          uint32_t b00, b01, b10, b11;
-          cvt4(vw[j][m] & 0x0F0F0F0Fu, b00, b01);
-          cvt4((vw[j][m] >> 4) & 0x0F0F0F0Fu, b10, b11);
-          mma16816(d[j], A[2 * m], b00, b01);
-          mma16816(d[j], A[2 * m + 1], b10, b11);
-        }
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int nt2 = 4 * npg + j;
-        const float2 rv = h2pair(vm + L::kVr + 8 * nt2 + 2 * c);
-        const float2 v = __ffma2_rn(
-            rv, __ffma2_rn(__fadd2_rn(make_float2(d[j][0], d[j][1]), make_float2(d[j][2], d[j][3])), vf2, gamma_2),
-            make_float2(acc[nt2][0], acc[nt2][1]));
-        acc[nt2][0] = v.x;
-        acc[nt2][1] = v.y;
-      }
-    }
-  }
-}
-
-// Partial record of one (sequence, kv-head) over the tiles this warp attended.
-__device__ __forceinline__ void flush_record(const DecodeArgs& a, int64_t rec_idx, int g, int c, float m_run,
-                                             float l_run, const float (&acc)[16][2]) {
-  const float l = quad_sum(l_run);
-  if (g >= a.group) return;
-  float* out = a.part + rec_idx * kRecFloats + g * kPartStride;
-#pragma unroll
-  for (int n = 0; n < 16; ++n) *reinterpret_cast<float2*>(out + 8 * n + 2 * c) = make_float2(acc[n][0], acc[n][1]);
-  if (c == 0) *reinterpret_cast<float2*>(out + 128) = make_float2(m_run, l);
-}
-
 template <int KB, int VB, bool kLean>
 __global__ void __launch_bounds__(SplitCfg<KB, VB, kLean>::kWarps * 32, 1) decode_split_kernel(DecodeArgs a) {
-  constexpr int kWarps = SplitCfg<KB, VB, kLean>::kWarps;
-  constexpr int kRecBytes = RecordLayout<KB, VB, kLean>::kBytes;
   extern __shared__ __align__(128) uint8_t smem[];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g = lane >> 2, c = lane & 3;
-  const int64_t wg = static_cast<int64_t>(blockIdx.x) * kWarps + warp;
-  const int64_t total = a.prefix[a.n_seqs] * a.hkv;
-  int64_t gb, ge;
-  warp_range<kWarps>(total, a.n_ctas, wg, gb, ge);
-  if (lane == 0) {
-    a.ranges[2 * wg] = gb;
-    a.ranges[2 * wg + 1] = ge;
-  }
-  if (gb >= ge) return;   // warps are independent: no CTA-wide barrier below
-
-  uint8_t* stages = smem + warp * kStages * kRecBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kWarps * kStages * kRecBytes) + warp * kStages;
-  if (lane == 0) {
-    for (int k = 0; k < kStages; ++k) mbar_init(&bars[k], 1);
-    fence_mbar_init();
-  }
-  __syncwarp();
-
-  // load cursor (tiles being copied) runs kStages tiles ahead of the compute cursor
-  Cursor lc = locate(a, gb);
-  Cursor cc = lc;
-  uint32_t valid = 0;
-  for (int k = 0; k < kStages && gb + k < ge; ++k) {
-    if (k > 0) advance(a, lc);
-    bool ok = false;
-    if (lane == 0) ok = issue_tile<kRecBytes>(a, lc, stages + k * kRecBytes, &bars[k]);
-    if (__shfl_sync(0xffffffffu, ok, 0)) valid |= 1u << k;
-  }
-
-  float qv[8][4];
-  float acc[16][2];
-  float m_run = -INFINITY, l_run = 0.f;
-  int64_t unit = -1;
-  uint32_t phase = 0;
-  for (int64_t k = 0; gb + k < ge; ++k) {
-    const int stg = static_cast<int>(k % kStages);
-    const int64_t u = static_cast<int64_t>(cc.s) * a.hkv + cc.h;
-    if (u != unit) {
-      if (unit >= 0) flush_record(a, wg + unit, g, c, m_run, l_run, acc);
-      unit = u;
-      load_q(a, cc.s, cc.h, g, c, qv);
-      m_run = -INFINITY;
-      l_run = 0.f;
-#pragma unroll
-      for (int n = 0; n < 16; ++n) acc[n][0] = acc[n][1] = 0.f;
-    }
-    const bool ok = __all_sync(0xffffffffu, mbar_wait(&bars[stg], (phase >> stg) & 1u, a.flags));
-    phase ^= 1u << stg;
-    if (!ok) break;   // a copy never arrived (flag raised): stop this warp
-    if ((valid >> stg) & 1u) attend_tile<KB, VB, kLean>(stages + stg * kRecBytes, qv, g, c, m_run, l_run, acc);
-    __syncwarp();
-    if (gb + k + kStages < ge) {     // refill this stage with the tile kStages ahead
-      advance(a, lc);
-      bool issued = false;
-      if (lane == 0) issued = issue_tile<kRecBytes>(a, lc, stages + stg * kRecBytes, &bars[stg]);
-      if (__shfl_sync(0xffffffffu, issued, 0)) valid |= 1u << stg; else valid &= ~(1u << stg);
-    }
-    advance(a, cc);
-  }
-  if (unit >= 0) flush_record(a, wg + unit, g, c, m_run, l_run, acc);
+  split_body<KB, VB, kLean>(a, smem, blockIdx.x);
 }
 
-// ------------------------------------------------------------------ merge
-// One CTA per (kv-head, sequence), one warp per q-head of the group; lane l owns
-// channels 4l..4l+3.
+// One CTA per (kv-head, sequence).
 __global__ void __launch_bounds__(256) decode_merge_kernel(DecodeArgs a, const uint16_t* __restrict__ ws,
                                                            uint16_t* __restrict__ out) {
   __shared__ float sc[8][128];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int h = blockIdx.x;
-  const int s = blockIdx.y;
-  const int gg = warp;
-  if (gg >= a.group) return;
-  const int L = max(a.seq_lens[s], 0);
-  const int nf = full_tiles(a, s);
-  int n_ws = L % kB;
-  if (n_ws > 0 && ws == nullptr) {  // tail tokens without a workspace: attend the tiles only
-    n_ws = 0;
-    if (lane == 0) raise_flag(a.flags, KVARN_FLAG_BAD_LENGTH);
-  }
-  const int64_t qrow = (static_cast<int64_t>(s) * a.hkv * a.group + static_cast<int64_t>(h) * a.group + gg) * kD;
-  const int64_t u = static_cast<int64_t>(s) * a.hkv + h;
-  const int64_t n_warps = static_cast<int64_t>(a.n_ctas) * a.warps;
-
-  // warps whose ranges cover this unit's tiles [t0, t1) (ranges are contiguous and
-  // ordered; empty ranges are skipped)
-  int64_t wlo = 0, whi = 0;
-  const int64_t t0 = a.prefix[s] * a.hkv + static_cast<int64_t>(h) * nf, t1 = t0 + nf;
-  if (nf > 0) {
-    int64_t lo = 0, hi = n_warps - 1;   // first warp with end > t0
-    while (lo < hi) {
-      const int64_t mid = (lo + hi) >> 1;
-      if (a.ranges[2 * mid + 1] > t0) hi = mid; else lo = mid + 1;
-    }
-    wlo = lo;
-    whi = lo;
-    while (whi < n_warps && a.ranges[2 * whi] < t1) ++whi;
-  }
-
-  float M = -INFINITY;
-  for (int64_t w = wlo; w < whi; ++w)
-    if (a.ranges[2 * w] < a.ranges[2 * w + 1]) M = fmaxf(M, a.part[(w + u) * kRecFloats + gg * kPartStride + 128]);
-  // workspace tokens: exact fp16 K/V, unrotated
-  const int64_t wbase = (static_cast<int64_t>(s) * a.hkv + h) * 2 * static_cast<int64_t>(kB * kD);
-  const uint16_t* wk = ws ? ws + wbase : nullptr;
-  const uint16_t* wv = ws ? ws + wbase + kB * kD : nullptr;
-  float qf[4];
-#pragma unroll
-  for (int k = 0; k < 4; ++k) qf[k] = h2f_bits(a.q[qrow + 4 * lane + k]) * (kLog2e * kInvSqrt128);
-  for (int t = 0; t < n_ws; ++t) {
-    float d = 0.f;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) d = fmaf(qf[k], h2f_bits(wk[t * kD + 4 * lane + k]), d);
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
-    if (lane == 0) sc[gg][t] = d;
-    M = fmaxf(M, d);
-  }
-  __syncwarp();
-
-  float acc[4] = {0.f, 0.f, 0.f, 0.f}, wacc[4] = {0.f, 0.f, 0.f, 0.f};
-  float l = 0.f;
-  for (int64_t w = wlo; w < whi; ++w) {
-    if (a.ranges[2 * w] >= a.ranges[2 * w + 1]) continue;
-    const float* pp = a.part + (w + u) * kRecFloats + gg * kPartStride;
-    const float mp = pp[128];
-    const float f = (mp == -INFINITY) ? 0.f : exp2f(mp - M);
-    l = fmaf(pp[129], f, l);
-    const float4 v = *reinterpret_cast<const float4*>(pp + 4 * lane);
-    acc[0] = fmaf(v.x, f, acc[0]);
-    acc[1] = fmaf(v.y, f, acc[1]);
-    acc[2] = fmaf(v.z, f, acc[2]);
-    acc[3] = fmaf(v.w, f, acc[3]);
-  }
-  for (int t = 0; t < n_ws; ++t) {
-    const float pw = exp2f(sc[gg][t] - M);
-    l += pw;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) wacc[k] = fmaf(pw, h2f_bits(wv[t * kD + 4 * lane + k]), wacc[k]);
-  }
-  // un-rotate: FWHT over the 128 channels (4 per lane), then scale by 1/sqrt(128)
-  {
-    const float a0 = acc[0] + acc[1], a1 = acc[0] - acc[1], a2 = acc[2] + acc[3], a3 = acc[2] - acc[3];
-    acc[0] = a0 + a2;
-    acc[1] = a1 + a3;
-    acc[2] = a0 - a2;
-    acc[3] = a1 - a3;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const bool upper = (lane & o) != 0;
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const float other = __shfl_xor_sync(0xffffffffu, acc[k], o);
-        acc[k] = upper ? (other - acc[k]) : (acc[k] + other);
-      }
-    }
-  }
-  const float inv_l = (l > 0.f) ? 1.0f / l : 0.f;
-  uint16_t res[4];
-#pragma unroll
-  for (int k = 0; k < 4; ++k) res[k] = f2h_bits(fmaf(acc[k], kInvSqrt128, wacc[k]) * inv_l);
-  *reinterpret_cast<uint2*>(out + qrow + 4 * lane) =
-      make_uint2(res[0] | (static_cast<uint32_t>(res[1]) << 16), res[2] | (static_cast<uint32_t>(res[3]) << 16));
+  merge_body(a, ws, out, blockIdx.x, blockIdx.y, sc);
 }
-
-size_t prefix_bytes(int n_seqs) { return ((static_cast<size_t>(n_seqs) + 1) * sizeof(int64_t) + 255) & ~size_t(255); }
-constexpr size_t kRangeBytes = static_cast<size_t>(kMaxCtas) * kMaxWarps * 2 * sizeof(int64_t);
 
 }  // namespace
 

@@ -46,6 +46,11 @@ cudaError_t launch_prefill(const uint16_t* q, const uint16_t* k_new, const uint1
                            int64_t num_blocks, int k_bits, int v_bits, bool lean, uint16_t* out, unsigned* flags,
                            cudaStream_t stream);
 
+cudaError_t launch_serve_step(const uint16_t* q, const uint16_t* k_new, const uint16_t* v_new,
+                              const int32_t* seq_lens, int32_t* seq_lens_out, const int32_t* block_tables,
+                              uint16_t* ws, uint8_t* cache, int n_seqs, int hkv, int group, int max_blocks,
+                              int64_t num_blocks, int k_bits, int v_bits, bool lean, int n_iters, float eps,
+                              uint16_t* out, void* scratch, unsigned* flags, cudaStream_t stream);
 // Device scratch of launch_decode: tile prefix per sequence + partial records.
 size_t decode_part_bytes(int n_seqs, int hkv, int max_blocks);
 // Scratch launch_decode touches when the split kernel runs `n_ctas` CTAs (the

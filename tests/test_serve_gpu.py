@@ -1,0 +1,136 @@
+"""kvarn_serve_step (append + decode attention in one cooperative launch, CUDA
+through the C ABI) against the two calls it fuses, kvarn_append_decode then
+kvarn_decode_attention, on the same inputs: the workspace, the cache, the new
+lengths and the attention output must agree bit for bit (the two paths run the same
+arithmetic; the two calls are checked against the CPU oracle by the append and
+decode parity tests). Also: the step captured in a CUDA graph and replayed."""
+import numpy as np
+import pytest
+
+import kvarn_synth as synth
+from oracle import kvarn_oracle as o
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def env():
+    import torch
+    import kv_cache_quantization_x128_gb300 as kv
+    torch.cuda.set_device(0)
+    kv.kvarn_device_flags()
+    return kv, torch
+
+
+def _case(torch, n_seqs, hkv, group, seed, preset):
+    lay = o.LAYOUTS[preset]
+    lens = synth.ragged_lengths(n_seqs, 1, 5000, seed)
+    lens[::5] = (lens[::5] // 128) * 128 + 127          # these appends complete a tile
+    lens[1] = 0                                          # an empty sequence gets its first token
+    max_blocks = int(max((L + 1 + 127) // 128 for L in lens))
+    total_blocks = int(((lens + 1 + 127) // 128).sum())
+    num_blocks = total_blocks + 8
+    perm = synth.block_permutation(num_blocks, seed)
+    bt = np.full((n_seqs, max_blocks), -1, np.int32)
+    pos = 0
+    for s in range(n_seqs):
+        nb = (lens[s] + 1 + 127) // 128
+        bt[s, :nb] = perm[pos:pos + nb]
+        pos += nb
+    recs = synth.random_records(num_blocks * hkv, seed, lay.record_bytes,
+                                lay.k_code_bytes + lay.v_code_bytes).reshape(num_blocks, hkv, -1)
+    ws = synth.workspace_tokens(n_seqs, hkv, seed)
+    k_new, v_new = synth.prefill_kv(n_seqs, hkv, seed=seed + 1)
+    q = synth.queries(n_seqs, hkv * group, seed)
+    f16 = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.float16).cuda()
+    return dict(lens=torch.from_numpy(lens).cuda(), bt=torch.from_numpy(bt).cuda(),
+                cache=torch.from_numpy(recs).cuda(), ws=f16(ws), k_new=f16(k_new), v_new=f16(v_new), q=f16(q),
+                num_blocks=num_blocks, max_blocks=max_blocks, n_done=int((lens % 128 == 127).sum()))
+
+
+def _meta(kv, c, hkv, group, preset):
+    return kv.make_meta(hkv, hkv * group, c["num_blocks"], max_blocks_per_seq=c["max_blocks"], preset=preset)
+
+
+def _two_calls(kv, torch, c, meta, scratch):
+    ws, cache = c["ws"].clone(), c["cache"].clone()
+    lens_out = torch.full_like(c["lens"], -7)
+    out = torch.full_like(c["q"], float("nan"))
+    kv.kvarn_append_decode(c["k_new"], c["v_new"], c["lens"], lens_out, c["bt"], ws, cache, meta)
+    kv.kvarn_decode_attention(c["q"], cache, ws, c["bt"], lens_out, out, scratch, meta)
+    torch.cuda.synchronize()
+    return ws, cache, lens_out, out
+
+
+@pytest.mark.parametrize("preset", ["k4v2", "k4v4", "k2v2", "k4v2l"])
+def test_serve_step_matches_append_then_decode(env, preset):
+    kv, torch = env
+    n_seqs, hkv, group = 40, 4, 8
+    c = _case(torch, n_seqs, hkv, group, seed=91, preset=preset)
+    assert c["n_done"] >= 8
+    meta = _meta(kv, c, hkv, group, preset)
+    scratch = torch.empty(kv.decode_scratch_bytes(meta, n_seqs), dtype=torch.uint8, device="cuda")
+    want = _two_calls(kv, torch, c, meta, scratch)
+    assert kv.kvarn_device_flags() == 0
+    ws, cache = c["ws"].clone(), c["cache"].clone()
+    lens_out = torch.full_like(c["lens"], -7)
+    out = torch.full_like(c["q"], float("nan"))
+    kv.kvarn_serve_step(c["q"], c["k_new"], c["v_new"], c["lens"], lens_out, c["bt"], ws, cache, out, scratch, meta)
+    torch.cuda.synchronize()
+    assert kv.kvarn_device_flags() == 0
+    assert torch.equal(lens_out, c["lens"] + 1)
+    assert torch.equal(lens_out, want[2])
+    assert torch.equal(ws.view(torch.int16), want[0].view(torch.int16))
+    assert torch.equal(cache, want[1])
+    assert torch.equal(out.view(torch.int16), want[3].view(torch.int16))
+    assert torch.isfinite(out.float()).all()
+
+
+def test_serve_step_graph_replay(env):
+    """The fused step captured in a CUDA graph: two replays from the same state give
+    the eager result bit for bit."""
+    kv, torch = env
+    n_seqs, hkv, group = 24, 2, 8
+    c = _case(torch, n_seqs, hkv, group, seed=92, preset="k4v2")
+    meta = _meta(kv, c, hkv, group, "k4v2")
+    scratch = torch.empty(kv.decode_scratch_bytes(meta, n_seqs), dtype=torch.uint8, device="cuda")
+    init = {k: c[k].clone() for k in ("ws", "cache")}
+    st = {k: c[k].clone() for k in ("ws", "cache")}
+    lens_out = torch.empty_like(c["lens"])
+    out = torch.empty_like(c["q"])
+
+    def step():
+        kv.kvarn_serve_step(c["q"], c["k_new"], c["v_new"], c["lens"], lens_out, c["bt"], st["ws"], st["cache"],
+                            out, scratch, meta)
+
+    def reset():
+        for k in st:
+            st[k].copy_(init[k])
+        lens_out.fill_(-1)
+        out.fill_(float("nan"))
+
+    reset()
+    step()
+    torch.cuda.synchronize()
+    assert kv.kvarn_device_flags() == 0
+    want = {k: v.clone() for k, v in st.items()}
+    want_out = out.clone()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        reset()
+        step()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    for replay in range(2):
+        reset()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert kv.kvarn_device_flags() == 0
+        for k in st:
+            assert torch.equal(st[k], want[k]), (replay, k)
+        assert torch.equal(lens_out, c["lens"] + 1)
+        assert torch.equal(out.view(torch.int16), want_out.view(torch.int16)), replay
