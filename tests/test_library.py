@@ -65,6 +65,7 @@ def _raw(kv, name):
 
 A = ctypes.c_void_p(0x10000)          # aligned fake device address (never dereferenced)
 MIS = ctypes.c_void_p(0x10008)        # not 16-byte aligned
+B = ctypes.c_void_p(0x20000)          # a second aligned fake address
 
 
 @pytest.mark.parametrize("field,value,status", [
@@ -113,6 +114,24 @@ def test_decode_rejects_small_scratch(kv):
     assert dec(A, A, A, A, A, 4, A, A, need - 16, ctypes.byref(m), None) == 4
     assert dec(A, A, A, A, A, 4, A, None, need, ctypes.byref(m), None) == 1     # NULL scratch
     assert dec(A, A, A, A, A, 4, None, A, need, ctypes.byref(m), None) == 1     # NULL out
+
+
+def test_serve_step_rejects_bad_arguments(kv):
+    """kvarn_serve_step: seq_lens_out is required and must not alias seq_lens, the
+    workspace is required, and the scratch must hold the decode's partial records."""
+    m = kv.make_meta(8, 64, 1024, max_blocks_per_seq=128)
+    need = kv.decode_scratch_bytes(m, 4)
+    sv = _raw(kv, "kvarn_serve_step")
+    mm = ctypes.byref(m)
+    #        q  kn vn lens out_lens bt  n  ws cache out scratch bytes meta stream
+    assert sv(A, A, A, A, None, A, 4, A, A, A, A, need, mm, None) == 1       # NULL seq_lens_out
+    assert sv(A, A, A, A, A, A, 4, A, A, A, A, need, mm, None) == 1          # seq_lens_out aliases seq_lens
+    assert sv(A, A, A, A, B, A, 4, None, A, A, A, need, mm, None) == 1       # NULL workspace
+    assert sv(A, A, A, A, B, A, 4, A, A, A, A, need - 16, mm, None) == 4     # scratch too small
+    assert sv(A, A, A, A, B, A, 70000, A, A, A, A, need, mm, None) == 1      # n_seqs > 65535
+    assert sv(A, A, A, A, B, A, 0, A, A, A, A, 0, mm, None) == 0             # nothing to do
+    m0 = kv.make_meta(8, 64, 16, max_blocks_per_seq=0)
+    assert sv(A, A, A, A, B, A, 4, A, A, A, A, need, ctypes.byref(m0), None) == 1
 
 
 def test_presets_are_accepted_and_sized(kv):
