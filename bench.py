@@ -255,17 +255,20 @@ def run_gpu(args):
     # region. The prefill batch moves in E2E_CHUNKS slices on two copy streams; each
     # slice is quantized (one kvarn_quantize_tiles call) as soon as it is resident, so
     # copies overlap the kernels; decode follows, then its output goes back to the host.
+    # A slice's copy for the next step waits only for this step's quantization of that
+    # slice, and the small inputs wait for this step's decode, so the next step's
+    # copies run under this step's decode.
     copy_streams = [torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)]
     n_tok = S["kd"].shape[0]
     piece = n_tok // E2E_CHUNKS
+    prev = {"quant": [None] * E2E_CHUNKS, "decode": None}
 
     def e2e_step():
-        for cs in copy_streams:
-            cs.wait_stream(stream)              # the previous step no longer reads the inputs
         with torch.cuda.stream(copy_streams[0]):
-            for name in ("slots", "qd", "bt", "lens"):
-                S[name].copy_(S[{"slots": "slots_h", "qd": "qh", "bt": "bt_h", "lens": "lens_h"}[name]],
-                              non_blocking=True)
+            if prev["decode"] is not None:
+                copy_streams[0].wait_event(prev["decode"])   # the last decode read these
+            for name in ("qd", "bt", "lens"):
+                S[name].copy_(S[{"qd": "qh", "bt": "bt_h", "lens": "lens_h"}[name]], non_blocking=True)
         small = torch.cuda.Event()
         small.record(copy_streams[0])
         ready = []
@@ -273,17 +276,26 @@ def run_gpu(args):
             cs = copy_streams[i % 2]
             sl = slice(i * piece, (i + 1) * piece)
             with torch.cuda.stream(cs):
+                if prev["quant"][i] is not None:
+                    cs.wait_event(prev["quant"][i])         # the last quantization of this slice
                 S["kd"][sl].copy_(S["kh"][sl], non_blocking=True)
                 S["vd"][sl].copy_(S["vh"][sl], non_blocking=True)
+                S["slots"][sl].copy_(S["slots_h"][sl], non_blocking=True)
             ev = torch.cuda.Event()
             ev.record(cs)
             ready.append(ev)
-        stream.wait_event(small)
         for i in range(E2E_CHUNKS):
             sl = slice(i * piece, (i + 1) * piece)
             stream.wait_event(ready[i])
             kv.kvarn_quantize_tiles(S["kd"][sl], S["vd"][sl], S["slots"][sl], S["cache"], S["meta"])
+            done = torch.cuda.Event()
+            done.record(stream)
+            prev["quant"][i] = done
+        stream.wait_event(small)
         kv.kvarn_decode_attention(S["qd"], S["cache"], None, S["bt"], S["lens"], S["out"], S["scratch"], S["meta"])
+        dec = torch.cuda.Event()
+        dec.record(stream)
+        prev["decode"] = dec
         S["out_h"].copy_(S["out"], non_blocking=True)
     for _ in range(max(1, args.warmup)):
         e2e_step()
@@ -358,7 +370,8 @@ def run_gpu(args):
         "e2e": {"value": round(world * step_bytes / (e2e_ms / args.steps * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
         "gpu_launches": args.steps * 4,
-        "e2e_pipeline": f"{E2E_CHUNKS} slices on 2 copy streams, quantize per slice",
+        "e2e_pipeline": f"{E2E_CHUNKS} slices on 2 copy streams, quantize per slice; the next step's copies "
+                        "overlap this step's decode",
         "clocks": clk.summary(),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
