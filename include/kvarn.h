@@ -49,7 +49,7 @@
  *     so c is folded likewise (values from X_r / r). K meta [12288, 13056) is fp16
  *     c, s, z x 128; V meta [13056, 13824) is r, s, z; 13824 bytes in all.
  * The decode kernel runs 8 warps with two record stages each for k4v2, k4v2l and
- * k2v2, and 6 warps for k4v4 (its stages would not fit 7 warps' shared memory).
+ * k2v2, and 6 warps for k4v4 (two of its 18432-byte records per warp fit only 6).
  *
  * Packed record (k4v2): 14336 bytes per (physical block, kv-head). The cache is
  * uint8 [num_blocks][num_kv_heads][record bytes], device memory owned by the
