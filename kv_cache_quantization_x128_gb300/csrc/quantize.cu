@@ -18,9 +18,10 @@
 //      are thread-local loops plus one shuffle with the partner thread; every
 //      sweep (the thread's 64 values) is loaded at the end of the sweep before it,
 //      so its latency overlaps the reduction, the scale update and the barrier;
-//   4. fp16 scales, group extremes (for keys taken in the last row pass, whose
-//      lines are the key groups), RTN, packing into a shared-memory stage, and two
-//      bulk stores of the group's part of the record.
+//   4. fp16 scales, group extremes (keys: a sweep of D1, whose lines are the key
+//      groups, needing no barrier after the last row pass; values: a sweep of D2),
+//      RTN, packing into a shared-memory stage, and two bulk stores of the group's
+//      part of the record.
 // The groups share only the Hadamard operand and the TMEM allocation (256 columns
 // each), so one group's MMA latency and barriers overlap the other's arithmetic.
 // The slot check of an item is agreed on at the barrier that ends the previous one.

@@ -60,16 +60,10 @@ __device__ __forceinline__ void tmem_wait_line(float (&x)[64]) {
 // variance, or a non-positive variance), a second sweep recomputes the moments
 // about the exact mean, so the result keeps the accuracy of a centred two-pass
 // variance.
-//
-// With kExt, the same sweep also takes the extremes over the pair's values of
-// x_e * h_e (h a second parity-split vector), returned in mn, mx for both threads.
-template <bool kExt = false>
 __device__ __forceinline__ float pair_moments(float (&x)[64], uint32_t taddr, const float* wv, int p, float shift,
-                                             float& mean, uint32_t next_taddr, const float* hv = nullptr,
-                                             float* mn_out = nullptr, float* mx_out = nullptr) {
+                                             float& mean, uint32_t next_taddr) {
   const float2 nsh = make_float2(-shift, -shift);
   float2 s0 = make_float2(0.f, 0.f), s1 = s0, s2 = s0, s3 = s0, q0 = s0, q1 = s0, q2 = s0, q3 = s0;
-  float mn = INFINITY, mx = -INFINITY;
   tmem_wait_line(x);   // the whole sweep was started at the end of the one before
 #pragma unroll
   for (int hh = 0; hh < 2; ++hh) {
@@ -90,21 +84,7 @@ __device__ __forceinline__ float pair_moments(float (&x)[64], uint32_t taddr, co
       q1 = __ffma2_rn(d1, d1, q1);
       q2 = __ffma2_rn(d2, d2, q2);
       q3 = __ffma2_rn(d3, d3, q3);
-      if (kExt) {
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          const float4 h = reinterpret_cast<const float4*>(hv + p * 68)[8 * hh + q + r];
-          const float2 y0 = __fmul2_rn(make_float2(xh[4 * (q + r)], xh[4 * (q + r) + 1]), make_float2(h.x, h.y));
-          const float2 y1 = __fmul2_rn(make_float2(xh[4 * (q + r) + 2], xh[4 * (q + r) + 3]), make_float2(h.z, h.w));
-          mn = fmin3(fmin3(mn, y0.x, y0.y), y1.x, y1.y);
-          mx = fmax3(fmax3(mx, y0.x, y0.y), y1.x, y1.y);
-        }
-      }
     }
-  }
-  if (kExt) {
-    *mn_out = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, 2));
-    *mx_out = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
   }
   s0 = __fadd2_rn(s0, s2);
   s1 = __fadd2_rn(s1, s3);
@@ -236,29 +216,46 @@ __device__ __forceinline__ bool quantize_group(float* vec, uint8_t* stage, const
       if (kKind == 0 && it + 1 == n_iters) own = key_token_scale<kLean>(meta, vh, line, pl, b_own, p == 0);
     }
     named_bar(bar_id, kGroupThreads);
-    // row pass: channel i = line, tokens e = p + 2k (D1), weights b
-    if (kKind == 1 || it + 1 < n_iters) {
+    // row pass: channel i = line, tokens e = p + 2k (D1), weights b; after the keys'
+    // last one their extremes sweep D1 again (the key groups are its lines)
+    {
       float mean;
-      const float var = pair_moments(x, ta1, vb, p, mean_r, mean, ta2) * kVarScale;
+      const uint32_t next = kKind == 0 && it + 1 == n_iters ? ta1 : ta2;
+      const float var = pair_moments(x, ta1, vb, p, mean_r, mean, next) * kVarScale;
       a_own = div_sqrt(a_own, fmaf(a_own * a_own, var, eps));
       mean_r = mean;
       if (p == 0) va[pl] = a_own;
-    } else {
-      // last row pass of the keys: the same sweep takes each channel's extremes of
-      // x_ij / c_j, so r, s and z of the channel follow without another sweep
-      float mean, mn, mx;
-      const float var = pair_moments<true>(x, ta1, vb, p, mean_r, mean, ta2, vh, &mn, &mx) * kVarScale;
-      if (p == 0) {
-        const float an = div_sqrt(a_own, fmaf(a_own * a_own, var, eps));
-        const uint16_t rb = f2h_bits(clampf(1.0f / an, kFp16MinNormal, kFp16Max));
-        if (!kLean) meta[0 * 128 + line] = rb;
-        const float g = kLean ? kInvSqrt128 : kInvSqrt128 / h2f_bits(rb);
-        group_zero_scale<kBits, kLean>(meta, vw, vc0, line, pl, mn * g, mx * g, g);
-      }
     }
     named_bar(bar_id, kGroupThreads);
   }
 
+  if (kKind == 0) {
+    // keys: r of the channel (the line) and the channel's extremes of
+    // y = (x * hc_j) * g_i over D1 (hc published after the last column pass); the
+    // factor g_i constant along the line is positive, so it multiplies the extremes
+    const uint16_t rb = f2h_bits(clampf(1.0f / a_own, kFp16MinNormal, kFp16Max));
+    const float g = kLean ? kInvSqrt128 : kInvSqrt128 / h2f_bits(rb);
+    if (p == 0 && !kLean) meta[0 * 128 + line] = rb;
+    float mn = INFINITY, mx = -INFINITY;
+    tmem_wait_line(x);
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const float* xh = x + 32 * hh;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const float4 w = reinterpret_cast<const float4*>(vh + p * 68)[8 * hh + q];
+        const float2 y0 = __fmul2_rn(make_float2(xh[4 * q], xh[4 * q + 1]), make_float2(w.x, w.y));
+        const float2 y1 = __fmul2_rn(make_float2(xh[4 * q + 2], xh[4 * q + 3]), make_float2(w.z, w.w));
+        mn = fmin3(fmin3(mn, y0.x, y0.y), y1.x, y1.y);
+        mx = fmax3(fmax3(mx, y0.x, y0.y), y1.x, y1.y);
+      }
+    }
+    tmem_ld_line(ta2, x);   // the codes sweep
+    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, 2));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    if (p == 0) group_zero_scale<kBits, kLean>(meta, vw, vc0, line, pl, mn * g, mx * g, g);
+    named_bar(bar_id, kGroupThreads);
+  }
   if (kKind == 1) {
     // fp16 scales of the values: r per channel (line as channel), c per token (line
     // as token); the +-1 transform's 2^-3.5 is folded into g; lean metadata keeps r,

@@ -61,6 +61,29 @@ def test_quantize_single_and_multi_tile(env, preset):
     print(preset, "multi", compare_records(got[blocks, heads], kq, vq))
 
 
+@pytest.mark.parametrize("preset", PRESETS)
+@pytest.mark.parametrize("n_iters", [1, 3])
+def test_quantize_iteration_counts(env, preset, n_iters):
+    """Other iteration counts per preset (with one iteration the keys' token scales
+    are fixed straight after the first column pass)."""
+    kv, torch = env
+    hkv, n_chunks, num_blocks = 2, 6, 8
+    k, v = synth.prefill_kv(n_chunks * 128, hkv, seed=77 + n_iters)
+    slots = synth.prefill_slot_mapping(n_chunks * 128, num_blocks, seed=77)
+    meta = kv.make_meta(hkv, hkv, num_blocks, n_iters=n_iters, preset=preset)
+    cache = torch.zeros(num_blocks, hkv, record_bytes(preset), dtype=torch.uint8, device="cuda")
+    kv.kvarn_quantize_tiles(f16_to_dev(torch, k), f16_to_dev(torch, v), torch.from_numpy(slots).cuda(), cache, meta)
+    assert kv.kvarn_device_flags() == 0
+    pairs = [(c, h) for c in range(n_chunks) for h in range(hkv)]
+    kt = np.stack([k[c * 128:(c + 1) * 128, h] for c, h in pairs])
+    vt = np.stack([v[c * 128:(c + 1) * 128, h] for c, h in pairs])
+    _, kq, vq = o.quantize_tiles(kt, vt, n_iters, preset=preset)
+    got = cache.cpu().numpy()
+    blocks = np.array([slots[c * 128] // 128 for c, _ in pairs])
+    heads = np.array([h for _, h in pairs])
+    print(preset, n_iters, compare_records(got[blocks, heads], kq, vq))
+
+
 def _gpu_decode(env, q, cache, ws, bt, lens, hkv, num_blocks, preset):
     kv, torch = env
     n_seqs, hq, _ = q.shape

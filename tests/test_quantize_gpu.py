@@ -66,7 +66,7 @@ def test_multi_tile_random_slots(env):
     print(stats)
 
 
-@pytest.mark.parametrize("n_iters,eps", [(1, 1e-6), (8, 1e-6), (4, 1e-3)])
+@pytest.mark.parametrize("n_iters,eps", [(1, 1e-6), (8, 1e-6), (16, 1e-6), (4, 1e-3)])
 def test_iteration_count_and_eps(env, n_iters, eps):
     hkv, n_chunks = 2, 4
     k, v = synth.prefill_kv(n_chunks * 128, hkv, seed=22)
