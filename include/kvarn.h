@@ -184,7 +184,10 @@ KVARN_API size_t kvarn_decode_scratch_bytes(const kvarn_meta* meta, int32_t n_se
  *                 A run that does not, or whose block b is outside
  *                 [0, num_blocks), is skipped and flagged.
  *   n_tokens      >= 0 and a multiple of 128 (partial tiles belong in the decode
- *                 workspace, see kvarn_append_decode).
+ *                 workspace, see kvarn_append_decode), below 2^31, with
+ *                 (n_tokens / 128) * num_kv_heads below 2^31 (KVARN_EINVAL otherwise).
+ *                 Byte offsets into k, v and cache are 64-bit: inputs and caches
+ *                 beyond 4 GiB are supported.
  *   cache         uint8 [num_blocks][num_kv_heads][14336]; written records only.
  */
 KVARN_API kvarn_status kvarn_quantize_tiles(const uint16_t* k, const uint16_t* v,

@@ -111,6 +111,9 @@ kvarn_status kvarn_quantize_tiles(const uint16_t* k, const uint16_t* v, const in
   if (n_tokens < 0 || n_tokens % KVARN_BLOCK_SIZE != 0)
     return fail(KVARN_EINVAL, "n_tokens must be a non-negative multiple of 128 (got %lld)", (long long)n_tokens);
   if (n_tokens == 0) return KVARN_OK;
+  if (n_tokens > INT32_MAX || (n_tokens / KVARN_BLOCK_SIZE) * meta->num_kv_heads > INT32_MAX)
+    return fail(KVARN_EINVAL, "n_tokens and (n_tokens / 128) * num_kv_heads must be below 2^31 (got %lld)",
+                (long long)n_tokens);
   KV_TRY(need_ptr(k, "k"));
   KV_TRY(need_ptr(v, "v"));
   KV_TRY(need_ptr(slot_mapping, "slot_mapping"));

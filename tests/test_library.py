@@ -95,6 +95,9 @@ def test_quantize_rejects_partial_tiles_and_nulls(kv):
     assert q(A, MIS, A, 128, A, ctypes.byref(m), None) == 3        # misaligned v
     assert q(A, A, A, 128, A, None, None) == 1                     # NULL meta
     assert q(A, A, A, 0, A, ctypes.byref(m), None) == 0            # nothing to do
+    assert q(A, A, A, 1 << 31, A, ctypes.byref(m), None) == 1      # token index beyond 32 bits
+    m1 = kv.make_meta(512, 512, 16)
+    assert q(A, A, A, 1 << 30, A, ctypes.byref(m1), None) == 1     # 2^23 tiles x 512 kv-heads: items beyond 2^31
 
 
 def test_append_rejects_aliasing_and_nulls(kv):
