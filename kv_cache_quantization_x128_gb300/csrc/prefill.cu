@@ -4,37 +4,48 @@
 // L0 cached tokens attends the L0 cached tokens (floor(L0/128) packed tiles, then
 // the L0 % 128 fp16 workspace tokens) and chunk tokens 0..p.
 //
-// One CTA per (8 chunk tokens, kv-head, sequence), 8 warps; warp w runs chunk
-// token 8 * blockIdx.x + w with its GQA group of q-heads as the rows of m16n8k16
-// MMAs (fp16 hi part in rows 0-7, lo part in rows 8-15, as in decode). Per packed
-// tile the CTA bulk-copies the record once, turns the codes into fp16 in shared
-// memory (keys [token][channel], values [channel][token]) and the scales into
-// fp32 vectors, and every warp reads its B operands with ldmatrix:
-//   QK^T: A = q_r * r^K s^K, B = key codes; score_j = c^K_j (D + beta);
-//   PV:   A = p * c^V s^V,   B = value codes; acc_i += r^V_i (D + gamma).
-// The packed pass runs in the rotated domain (q_r = H q); the accumulator is then
-// rotated back once (H is its own inverse), and the fresh pass (workspace tail and
-// chunk, causal) continues in the input domain with unrotated q and plain fp16
-// K/V, under the same online softmax (log2 domain).
+// One CTA per (16 chunk tokens, kv-head, sequence): its 128 rows are the 16 tokens
+// times 8 GQA head slots (row 8t + g), the M of 128 x N x 16 tcgen05 MMAs with
+// fp32 accumulators in TMEM. B operands are fp16 in shared memory in the 128-byte
+// swizzled K-major layout; every fp32 operand is carried as an fp16 hi + lo pair
+// (three products, hi*hi + hi*lo + lo*hi, keep ~22 bits: fp16 alone moves outputs
+// of keys with outlier channels by up to 3e-2). Per packed tile:
+//   QK^T: A = q_r (hi, lo; shared memory), B = k~ (hi, lo) with k~[j][i] = code *
+//         r^K_i s^K_i and a 129th row r^K z^K, so S[:, 128] = beta;
+//         score_j = c^K_j (S_j + beta);
+//   PV:   A = p' (hi, lo; TMEM, two values per column) with p'_j = p_j c^V_j s^V_j,
+//         B = value codes (exact); acc_i += r^V_i (D_i + gamma),
+//         gamma = sum_j p_j c^V_j z^V_j.
+// Two threads own a row (channels 0-63 and 64-127 of S and of the accumulator,
+// which lives in registers). The packed pass runs in the rotated domain (q_r = H q);
+// the accumulator is then rotated back once (H is its own inverse) and the fresh
+// pass (workspace tail and chunk, causal) continues in the input domain with
+// unrotated q and plain fp16 K/V under the same online softmax (log2 domain).
 #include "kvarn_common.cuh"
 #include "kvarn_frag.cuh"
 #include "kvarn_launch.h"
+#include "kvarn_tc.cuh"
 
 namespace kvarn {
 namespace {
 
-constexpr int kPWarps = 8;                        // chunk tokens per CTA, one per warp
-constexpr int kPThreads = kPWarps * 32;
-constexpr int kPitch = 136;                       // fp16 per shared row: 128 + 8 (rows 272 B apart)
-constexpr int kTileBytes = 128 * kPitch * 2;
+constexpr int kPThreads = 256;                    // 8 warps; two threads per row in the row phases
+constexpr int kPTokens = 16;                      // chunk tokens per CTA (x 8 head slots = 128 rows)
+constexpr uint32_t kHalfB = 18432;                // K-half stride of the keys operand (144 rows)
+constexpr uint32_t kHalfQ = 16384;                // K-half stride of the 128-row operands
 constexpr int kMaxRec = 18432;                    // largest record (k4v4)
-constexpr int kOffK = 0;                          // fp16 [128][kPitch]
-constexpr int kOffV = kOffK + kTileBytes;         // fp16 [128][kPitch]
-constexpr int kOffRec = kOffV + kTileBytes;       // packed records [2] (the next one in flight)
-constexpr int kOffScale = kOffRec + 2 * kMaxRec;  // fp32 [6][128]
-constexpr int kOffCtl = kOffScale + 6 * 128 * 4;  // mbarriers [2]
-constexpr int kPSmem = kOffCtl + 16;
+constexpr int kOffQ = 0;                          // A of QK^T: q hi, q lo (32 KB each)
+constexpr int kOffB = 65536;                      // B of QK^T: k~ hi, lo (36 KB each)
+constexpr int kOffV = kOffB + 4 * kHalfB;         // B of PV: values [channel][token] (32 KB)
+constexpr int kOffRec = kOffV + 2 * kHalfQ;       // packed records [2] (the next one in flight)
+constexpr int kOffSc = kOffRec + 2 * kMaxRec;     // fp32 [5][128]: c^K, c s^V, c z^V, r^V, r s^K
+constexpr int kOffX = kOffSc + 5 * 512;           // fp32 [3][2][128]: row max, gamma and sum of each half
+constexpr int kOffBar = kOffX + 3 * 1024;         // mbarriers: records [2], MMA
+constexpr int kOffSlot = kOffBar + 24;            // TMEM base address
+constexpr int kPSmem = kOffSlot + 8;
+constexpr uint32_t kColS = 0, kColO = 256, kColP = 384;   // TMEM columns: S (144), PV product (128), p' hi, lo (64 + 64)
 constexpr float kLog2eP = 1.4426950408889634f;
+static_assert(kOffV % 1024 == 0 && kOffRec % 16 == 0 && kPSmem <= 232448, "prefill shared memory");
 
 struct PrefillArgs {
   const uint16_t* q;           // [n_tokens][hq][128]
@@ -51,325 +62,279 @@ struct PrefillArgs {
   int hkv, group, max_blocks;
 };
 
-__device__ __forceinline__ void ldsm_x4(const void* p, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(smem_u32(p)));
+// Byte offset of element (row r, K index k) in a 128-byte swizzled K-major operand
+// whose two 64-wide K halves are `half` bytes apart.
+__device__ __forceinline__ uint32_t swo(int r, int k, uint32_t half) {
+  return static_cast<uint32_t>(k >> 6) * half + static_cast<uint32_t>((r >> 3) * 1024 + (r & 7) * 128 +
+                                                                      ((((k & 63) >> 3) ^ (r & 7)) << 4) + (k & 7) * 2);
 }
-__device__ __forceinline__ void ldsm_x4_t(const void* p, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(smem_u32(p)));
+__device__ __forceinline__ uint64_t op_desc(uint32_t base, int s, uint32_t half) {
+  return smem_desc_sw128(base + static_cast<uint32_t>(s >> 2) * half + static_cast<uint32_t>(s & 3) * 32);
 }
 
-// Unnormalised FWHT over the 128 channels of the q fragment layout (thread (g, c)
-// holds channels 16ks + 2c + {0, 1, 8, 9} in qv[ks][0..3]).
-__device__ __forceinline__ void fwht_q(float (&qv)[8][4], int c) {
+// Thread t of the warp: TMEM lane (base lane + t), 32 consecutive columns.
+__device__ __forceinline__ void tld_x32(uint32_t taddr, float* v) {
+  uint32_t* r = reinterpret_cast<uint32_t*>(v);
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tld_x1(uint32_t taddr, float& v) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(*reinterpret_cast<uint32_t*>(&v)) : "r"(taddr));
+}
+__device__ __forceinline__ void tld_wait1(float& v) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" : "+r"(*reinterpret_cast<uint32_t*>(&v)));
+}
+
+// D[tmem] (+)= A[tmem] * B[smem]^T: A's row m in TMEM lane m, its K elements two per
+// 32-bit column (K step k of 16 at column a_tmem + 8 k); issued by one thread.
+__device__ __forceinline__ void umma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Thread t of the warp: 32 consecutive columns of TMEM lane (base lane + t) from v.
+__device__ __forceinline__ void tst_x32(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
+      "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
+      "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+__device__ __forceinline__ void tst_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// 64 fp32 values as fp16 (hi, lo) pairs into 32 TMEM columns each (hi at taddr, lo at
+// taddr + 64), two values per column.
+__device__ __forceinline__ void tmem_split_store(const float (&x)[64], uint32_t taddr) {
+  uint32_t h[32], l[32];
 #pragma unroll
-  for (int ks = 0; ks < 8; ++ks) {
-    const float u0 = qv[ks][0] + qv[ks][1], u1 = qv[ks][0] - qv[ks][1];
-    const float u2 = qv[ks][2] + qv[ks][3], u3 = qv[ks][2] - qv[ks][3];
-    qv[ks][0] = u0 + u2; qv[ks][2] = u0 - u2; qv[ks][1] = u1 + u3; qv[ks][3] = u1 - u3;
-  }
+  for (int e = 0; e < 32; ++e) split2p(make_float2(x[2 * e], x[2 * e + 1]), h[e], l[e]);
+  tst_x32(taddr, h);
+  tst_x32(taddr + 64, l);
+}
+
+// Unnormalised FWHT over 64 values (the butterflies of index bits 0-5).
+__device__ __forceinline__ void fwht64(float (&x)[64]) {
 #pragma unroll
-  for (int bit = 1; bit <= 2; bit <<= 1) {
-    const bool upper = (c & bit) != 0;
+  for (int bit = 1; bit < 64; bit <<= 1)
 #pragma unroll
-    for (int ks = 0; ks < 8; ++ks)
-#pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        const float o = __shfl_xor_sync(0xffffffffu, qv[ks][t], bit);
-        qv[ks][t] = upper ? (o - qv[ks][t]) : (qv[ks][t] + o);
+    for (int i = 0; i < 64; ++i)
+      if ((i & bit) == 0) {
+        const float u = x[i], w = x[i | bit];
+        x[i] = u + w;
+        x[i | bit] = u - w;
       }
-  }
-#pragma unroll
-  for (int bit = 1; bit < 8; bit <<= 1)
-#pragma unroll
-    for (int ks = 0; ks < 8; ++ks)
-      if ((ks & bit) == 0)
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {
-          const float u = qv[ks][t], w = qv[ks | bit][t];
-          qv[ks][t] = u + w;
-          qv[ks | bit][t] = u - w;
-        }
 }
 
-// Unnormalised FWHT over the 128 channels of the accumulator layout (thread (g, c)
-// holds channels 8n + 2c + {0, 1} in acc[n][0..1]).
-__device__ __forceinline__ void fwht_acc(float (&acc)[16][2], int c) {
+// Last butterfly (index bit 6) between the two threads of a row through shared
+// memory `xb` ([2][64][128] fp32, column-major so a warp's lanes hit distinct banks):
+// the lower half becomes own + partner, the upper half partner - own.
+__device__ __forceinline__ void fwht_pair(float (&x)[64], float* xb, int row, int hf) {
 #pragma unroll
-  for (int n = 0; n < 16; ++n) {
-    const float u = acc[n][0], w = acc[n][1];
-    acc[n][0] = u + w;
-    acc[n][1] = u - w;
+  for (int i = 0; i < 64; ++i) xb[(hf * 64 + i) * 128 + row] = x[i];
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < 64; ++i) {
+    const float o = xb[((hf ^ 1) * 64 + i) * 128 + row];
+    x[i] = hf == 0 ? x[i] + o : o - x[i];
   }
-#pragma unroll
-  for (int bit = 1; bit <= 2; bit <<= 1) {
-    const bool upper = (c & bit) != 0;
-#pragma unroll
-    for (int n = 0; n < 16; ++n)
-#pragma unroll
-      for (int t = 0; t < 2; ++t) {
-        const float o = __shfl_xor_sync(0xffffffffu, acc[n][t], bit);
-        acc[n][t] = upper ? (o - acc[n][t]) : (acc[n][t] + o);
-      }
-  }
-#pragma unroll
-  for (int bit = 1; bit < 16; bit <<= 1)
-#pragma unroll
-    for (int n = 0; n < 16; ++n)
-      if ((n & bit) == 0)
-#pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          const float u = acc[n][t], w = acc[n | bit][t];
-          acc[n][t] = u + w;
-          acc[n | bit][t] = u - w;
-        }
+  __syncthreads();
 }
 
-// A pair of fp16 code values stored at `dst`.
-__device__ __forceinline__ void put_pair(uint16_t* dst, uint32_t v) { *reinterpret_cast<uint32_t*>(dst) = v; }
-
-// 4-bit word (codes of indices i0 + {0, 1, 8, 9} of two 16-index steps, low nibbles
-// for the first step, high nibbles for the second): pairs code / 8 at index offsets
-// 0, 8, 16, 24 from i0 along a shared row.
-__device__ __forceinline__ void nibble_word(uint32_t w, uint16_t* row, int i0) {
-  uint32_t lo, hi;
-  cvt4(w & 0x0F0F0F0Fu, lo, hi);
-  put_pair(row + i0, lo);
-  put_pair(row + i0 + 8, hi);
-  cvt4((w >> 4) & 0x0F0F0F0Fu, lo, hi);
-  put_pair(row + i0 + 16, lo);
-  put_pair(row + i0 + 24, hi);
-}
-// 2-bit word (four 16-index steps, one per byte): pairs code / 2 at index offsets
-// 16k + 8r from i0 (k the byte, r = 0 for bits {0, 4} and 1 for bits {2, 6}).
-__device__ __forceinline__ void crumb_word(uint32_t w, uint16_t* row, int i0) {
+// 64 fp32 values of a row (K indices k0 .. k0 + 63) as fp16 hi and lo parts into two
+// swizzled operands, 16 bytes at a time.
+__device__ __forceinline__ void store_split(const float (&x)[64], uint8_t* hi, uint8_t* lo, int row, int k0,
+                                            uint32_t half) {
 #pragma unroll
-  for (int r = 0; r < 2; ++r) {
-    uint32_t v[4];
-    cvt2((w >> (2 * r)) & 0x33333333u, v);
+  for (int q = 0; q < 8; ++q) {
+    uint32_t h[4], l[4];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) put_pair(row + i0 + 16 * k + 8 * r, v[k]);
+    for (int e = 0; e < 4; ++e) split2p(make_float2(x[8 * q + 2 * e], x[8 * q + 2 * e + 1]), h[e], l[e]);
+    const uint32_t off = swo(row, k0 + 8 * q, half);
+    *reinterpret_cast<uint4*>(hi + off) = make_uint4(h[0], h[1], h[2], h[3]);
+    *reinterpret_cast<uint4*>(lo + off) = make_uint4(l[0], l[1], l[2], l[3]);
   }
 }
 
-// The CTA turns the record in shared memory into fp16 key codes [token][channel],
-// fp16 value codes [channel][token] and the six scale vectors (record layouts as
-// in kvarn.h).
+// A pair of key code values (fp16 pair v) times r s^K of their two channels (rsp),
+// as fp16 hi and lo parts at byte offset `off` of the two key operands.
+__device__ __forceinline__ void put_key_pair(uint8_t* bh, uint8_t* bl, uint32_t off, uint32_t v, float2 rsp) {
+  uint32_t h, l;
+  split2p(__fmul2_rn(__half22float2(*reinterpret_cast<const __half2*>(&v)), rsp), h, l);
+  *reinterpret_cast<uint32_t*>(bh + off) = h;
+  *reinterpret_cast<uint32_t*>(bl + off) = l;
+}
+
+// Scale vectors of the record (threads 0-127: index tid) and the 129th key row
+// r^K z^K (hi, lo). Codes in the operands are code / 8 (4-bit) or code / 2 (2-bit);
+// r s^K and c s^V carry the factor back (a power of two: exact).
 template <int KB, int VB, bool kLean>
-__device__ __forceinline__ void unpack_tile(const uint8_t* rec, uint16_t* ks, uint16_t* vs, float* sc, int tid) {
+__device__ __forceinline__ void unpack_scales(const uint8_t* rec, float* sc, uint8_t* bh, uint8_t* bl, int tid) {
+  using L = RecordLayout<KB, VB, kLean>;
+  const uint16_t* km = reinterpret_cast<const uint16_t*>(rec + L::kKMetaOff);
+  const uint16_t* vm = reinterpret_cast<const uint16_t*>(rec + L::kVMetaOff);
+  constexpr float kKf = KB == 4 ? 8.0f : 2.0f, kVf = VB == 4 ? 8.0f : 2.0f;
+  const float kr = kLean ? 1.0f : h2f_bits(km[L::kKr + tid]);
+  const float vc = kLean ? 1.0f : h2f_bits(vm[L::kVc + tid]);
+  sc[0 * 128 + tid] = h2f_bits(km[L::kKc + tid]);                 // per token: c^K
+  sc[1 * 128 + tid] = kVf * vc * h2f_bits(vm[L::kVs + tid]);      // per token: c s^V
+  sc[2 * 128 + tid] = vc * h2f_bits(vm[L::kVz + tid]);            // per token: c z^V
+  sc[3 * 128 + tid] = h2f_bits(vm[L::kVr + tid]);                 // per channel: r^V
+  sc[4 * 128 + tid] = kKf * kr * h2f_bits(km[L::kKs + tid]);      // per channel: r s^K
+  const float rz = kr * h2f_bits(km[L::kKz + tid]);
+  const uint16_t hz = f2h_bits(rz);
+  const uint32_t off = swo(128, tid, kHalfB);
+  *reinterpret_cast<uint16_t*>(bh + off) = hz;
+  *reinterpret_cast<uint16_t*>(bl + off) = f2h_bits(rz - h2f_bits(hz));
+}
+
+// Code words of a record, as the decode fragments lay them out (kvarn.h), go to
+// operand rows and K indices as follows; thread tid handles words tid + 256 k.
+//  * 4-bit (keys [token][channel], values [channel][token]): word wi of row wi >> 4
+//    holds the pairs at K indices c0 + {0, 8} (low nibbles) and c0 + {16, 24} (high
+//    nibbles), c0 = 32 (wi & 3) + 2 ((wi >> 2) & 3).
+//  * 2-bit keys: word wi of token wi >> 3 holds, in bits 2r of byte m, the pair at
+//    channel c0 + 16 m + 8 r, c0 = 64 (wi & 1) + 2 ((wi >> 1) & 3).
+//  * 2-bit values: word wi (panel wi >> 7, cell (wi >> 2) & 31, partner (wi >> 1) & 1,
+//    word wi & 1) of channel 16 panel + 8 partner + cell / 4 holds, like the keys,
+//    the pairs at tokens c0 + 16 m + 8 r, c0 = 64 (wi & 1) + 2 (cell & 3).
+// Per k the row moves by 16 (4-bit) or 32 (2-bit) rows, a whole number of 8-row
+// swizzle groups, so each thread's byte offsets are computed once and advance by
+// 2048 or 4096 bytes.
+template <int KB, int VB, bool kLean>
+__device__ __forceinline__ void unpack_values(const uint8_t* rec, uint8_t* vb, int tid) {
+  using L = RecordLayout<KB, VB, kLean>;
+  const uint32_t* vw = reinterpret_cast<const uint32_t*>(rec + L::kVCodeOff);
+  if (VB == 4) {
+    const int r0 = tid >> 4, c0 = 32 * (tid & 3) + 2 * ((tid >> 2) & 3);
+    uint32_t off[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) off[q] = swo(r0, c0 + 8 * q, kHalfQ);
+#pragma unroll 2
+    for (int k = 0; k < 8; ++k) {
+      const uint32_t w = vw[tid + 256 * k];
+      uint32_t v[4];
+      cvt4(w & 0x0F0F0F0Fu, v[0], v[1]);
+      cvt4((w >> 4) & 0x0F0F0F0Fu, v[2], v[3]);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) *reinterpret_cast<uint32_t*>(vb + off[q] + 2048 * k) = v[q];
+    }
+  } else {
+    const int r0 = 16 * (tid >> 7) + 8 * ((tid >> 1) & 1) + ((tid >> 4) & 7);
+    const int c0 = 64 * (tid & 1) + 2 * ((tid >> 2) & 3);
+    uint32_t off[2][4];
+#pragma unroll
+    for (int r = 0; r < 2; ++r)
+#pragma unroll
+      for (int m = 0; m < 4; ++m) off[r][m] = swo(r0, c0 + 16 * m + 8 * r, kHalfQ);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint32_t w = vw[tid + 256 * k];
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        uint32_t v[4];
+        cvt2((w >> (2 * r)) & 0x33333333u, v);
+#pragma unroll
+        for (int m = 0; m < 4; ++m) *reinterpret_cast<uint32_t*>(vb + off[r][m] + 4096 * k) = v[m];
+      }
+    }
+  }
+}
+
+// Key codes of the record, times r s^K per channel, into the QK^T operand
+// [token][channel] (hi, lo).
+template <int KB, int VB, bool kLean>
+__device__ __forceinline__ void unpack_keys(const uint8_t* rec, const float* rs, uint8_t* bh, uint8_t* bl, int tid) {
   using L = RecordLayout<KB, VB, kLean>;
   const uint32_t* kw = reinterpret_cast<const uint32_t*>(rec + L::kKCodeOff);
-  const uint32_t* vw = reinterpret_cast<const uint32_t*>(rec + L::kVCodeOff);
   if (KB == 4) {
-    for (int wi = tid; wi < 2048; wi += kPThreads) {     // token t: 16 words, group (wi>>2)&3, word wi&3
-      const int t = wi >> 4;
-      nibble_word(kw[wi], ks + t * kPitch, 32 * (wi & 3) + 2 * ((wi >> 2) & 3));
+    const int r0 = tid >> 4, c0 = 32 * (tid & 3) + 2 * ((tid >> 2) & 3);
+    uint32_t off[4];
+    float2 f[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      off[q] = swo(r0, c0 + 8 * q, kHalfB);
+      f[q] = *reinterpret_cast<const float2*>(rs + c0 + 8 * q);
+    }
+#pragma unroll 2
+    for (int k = 0; k < 8; ++k) {
+      const uint32_t w = kw[tid + 256 * k];
+      uint32_t v[4];
+      cvt4(w & 0x0F0F0F0Fu, v[0], v[1]);
+      cvt4((w >> 4) & 0x0F0F0F0Fu, v[2], v[3]);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) put_key_pair(bh, bl, off[q] + 2048 * k, v[q], f[q]);
     }
   } else {
-    for (int wi = tid; wi < 1024; wi += kPThreads) {     // token t: 8 words, group (wi>>1)&3, word wi&1
-      const int t = wi >> 3;
-      crumb_word(kw[wi], ks + t * kPitch, 64 * (wi & 1) + 2 * ((wi >> 1) & 3));
-    }
-  }
-  if (VB == 4) {
-    for (int wi = tid; wi < 2048; wi += kPThreads) {     // channel i: 16 words
-      const int i = wi >> 4;
-      nibble_word(vw[wi], vs + i * kPitch, 32 * (wi & 3) + 2 * ((wi >> 2) & 3));
-    }
-  } else {
-    for (int wi = tid; wi < 1024; wi += kPThreads) {     // panel m, cell, partner `which`, word u
-      const int m = wi >> 7, cell = (wi >> 2) & 31, which = (wi >> 1) & 1, u = wi & 1;
-      const int i = 16 * m + 8 * which + (cell >> 2);
-      crumb_word(vw[wi], vs + i * kPitch, 64 * u + 2 * (cell & 3));
-    }
-  }
-  if (tid < 128) {
-    const uint16_t* km = reinterpret_cast<const uint16_t*>(rec + L::kKMetaOff);
-    const uint16_t* vm = reinterpret_cast<const uint16_t*>(rec + L::kVMetaOff);
-    const float kr = kLean ? 1.0f : h2f_bits(km[L::kKr + tid]);
-    const float vc = kLean ? 1.0f : h2f_bits(vm[L::kVc + tid]);
-    // the fp16 codes in shared memory are code / 8 (4-bit) or code / 2 (2-bit): the
-    // step vectors carry the factor back (a power of two: exact)
-    constexpr float kKf = KB == 4 ? 8.0f : 2.0f, kVf = VB == 4 ? 8.0f : 2.0f;
-    sc[0 * 128 + tid] = kKf * kr * h2f_bits(km[L::kKs + tid]);   // per channel: r s (keys)
-    sc[1 * 128 + tid] = kr * h2f_bits(km[L::kKz + tid]);   // per channel: r z
-    sc[2 * 128 + tid] = h2f_bits(km[L::kKc + tid]);        // per token: c
-    sc[3 * 128 + tid] = kVf * vc * h2f_bits(vm[L::kVs + tid]);   // per token: c s (values)
-    sc[4 * 128 + tid] = vc * h2f_bits(vm[L::kVz + tid]);   // per token: c z
-    sc[5 * 128 + tid] = h2f_bits(vm[L::kVr + tid]);        // per channel: r
-  }
-}
-
-// One 128-token block for warp (g, c): keys ks [token][channel] fp16, values vs
-// ([channel][token] if kPacked, else [token][channel]), scales sc (packed only),
-// tokens with index > limit masked (fresh only).
-template <bool kPacked>
-__device__ __forceinline__ void attend_block(const uint16_t* ks, const uint16_t* vs, const float* sc,
-                                             const float (&qv)[8][4], int g, int c, int lane, int limit,
-                                             float& m_run, float& l_run, float (&acc)[16][2]) {
-  uint32_t A[8][4];
-  float beta = 0.f;
+    const int r0 = tid >> 3, c0 = 64 * (tid & 1) + 2 * ((tid >> 1) & 3);
+    uint32_t off[2][4];
+    float2 f[2][4];
 #pragma unroll
-  for (int ks8 = 0; ks8 < 8; ++ks8) {
-    const int ch0 = 16 * ks8 + 2 * c;
-    float s0 = 1.f, s1 = 1.f, s2 = 1.f, s3 = 1.f;
-    if (kPacked) {
-      s0 = sc[ch0]; s1 = sc[ch0 + 1]; s2 = sc[ch0 + 8]; s3 = sc[ch0 + 9];
-      beta = fmaf(qv[ks8][0], sc[128 + ch0], beta);
-      beta = fmaf(qv[ks8][1], sc[128 + ch0 + 1], beta);
-      beta = fmaf(qv[ks8][2], sc[128 + ch0 + 8], beta);
-      beta = fmaf(qv[ks8][3], sc[128 + ch0 + 9], beta);
-    }
-    split2(qv[ks8][0] * s0, qv[ks8][1] * s1, A[ks8][0], A[ks8][1]);
-    split2(qv[ks8][2] * s2, qv[ks8][3] * s3, A[ks8][2], A[ks8][3]);
-  }
-  if (kPacked) beta = quad_sum(beta);
-
-  // scores of tokens 8nt + 2c + {0, 1}; ldmatrix x4 gives the B fragments of two k-steps
-  float sc2[16][2];
+    for (int r = 0; r < 2; ++r)
 #pragma unroll
-  for (int ntg = 0; ntg < 4; ++ntg) {
-    float d[4][4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) d[j][0] = d[j][1] = d[j][2] = d[j][3] = 0.f;
-#pragma unroll
-    for (int kp = 0; kp < 4; ++kp)
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int nt = 4 * ntg + j;
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(ks + (8 * nt + (lane & 7)) * kPitch + 32 * kp + 8 * (lane >> 3), b0, b1, b2, b3);
-        mma16816(d[j], A[2 * kp], b0, b1);
-        mma16816(d[j], A[2 * kp + 1], b2, b3);
+      for (int m = 0; m < 4; ++m) {
+        off[r][m] = swo(r0, c0 + 16 * m + 8 * r, kHalfB);
+        f[r][m] = *reinterpret_cast<const float2*>(rs + c0 + 16 * m + 8 * r);
       }
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int nt = 4 * ntg + j;
-      const int t0 = 8 * nt + 2 * c;
-      float v0 = d[j][0] + d[j][2], v1 = d[j][1] + d[j][3];
-      if (kPacked) {
-        v0 = sc[256 + t0] * (v0 + beta);
-        v1 = sc[256 + t0 + 1] * (v1 + beta);
-      } else {
-        if (t0 > limit) v0 = -INFINITY;
-        if (t0 + 1 > limit) v1 = -INFINITY;
-      }
-      sc2[nt][0] = v0;
-      sc2[nt][1] = v1;
-    }
-  }
-
-  // online softmax (log2 domain)
-  float tmax = -INFINITY;
+    for (int k = 0; k < 4; ++k) {
+      const uint32_t w = kw[tid + 256 * k];
 #pragma unroll
-  for (int nt = 0; nt < 16; ++nt) tmax = fmaxf(tmax, fmaxf(sc2[nt][0], sc2[nt][1]));
-  tmax = quad_max(tmax);
-  const float m_new = fmaxf(m_run, tmax);
-  if (m_new == -INFINITY) return;           // every token of the block masked
-  const float corr = ex2(m_run - m_new);
-  m_run = m_new;
-  float lsum = 0.f;
+      for (int r = 0; r < 2; ++r) {
+        uint32_t v[4];
+        cvt2((w >> (2 * r)) & 0x33333333u, v);
 #pragma unroll
-  for (int nt = 0; nt < 16; ++nt) {
-    sc2[nt][0] = ex2(sc2[nt][0] - m_new);
-    sc2[nt][1] = ex2(sc2[nt][1] - m_new);
-    lsum += sc2[nt][0] + sc2[nt][1];
-  }
-  l_run = fmaf(l_run, corr, lsum);
-#pragma unroll
-  for (int n = 0; n < 16; ++n) {
-    acc[n][0] *= corr;
-    acc[n][1] *= corr;
-  }
-
-  // p' fragments and gamma; tokens 16ks + 2c + {0, 1} (nt = 2ks) and + {8, 9}
-  float gamma = 0.f;
-#pragma unroll
-  for (int ks8 = 0; ks8 < 8; ++ks8) {
-    const int t0 = 16 * ks8 + 2 * c;
-    const float p0 = sc2[2 * ks8][0], p1 = sc2[2 * ks8][1], p2 = sc2[2 * ks8 + 1][0], p3 = sc2[2 * ks8 + 1][1];
-    float s0 = 1.f, s1 = 1.f, s2 = 1.f, s3 = 1.f;
-    if (kPacked) {
-      s0 = sc[384 + t0]; s1 = sc[384 + t0 + 1]; s2 = sc[384 + t0 + 8]; s3 = sc[384 + t0 + 9];
-      gamma = fmaf(p0, sc[512 + t0], gamma);
-      gamma = fmaf(p1, sc[512 + t0 + 1], gamma);
-      gamma = fmaf(p2, sc[512 + t0 + 8], gamma);
-      gamma = fmaf(p3, sc[512 + t0 + 9], gamma);
-    }
-    split2(p0 * s0, p1 * s1, A[ks8][0], A[ks8][1]);
-    split2(p2 * s2, p3 * s3, A[ks8][2], A[ks8][3]);
-  }
-  if (kPacked) gamma = quad_sum(gamma);
-
-  // PV: channel n-tiles n2 = 4 n2g + j
-#pragma unroll
-  for (int n2g = 0; n2g < 4; ++n2g) {
-    float d[4][4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) d[j][0] = d[j][1] = d[j][2] = d[j][3] = 0.f;
-#pragma unroll
-    for (int kp = 0; kp < 4; ++kp)
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int n2 = 4 * n2g + j;
-        uint32_t b0, b1, b2, b3;
-        if (kPacked)    // values [channel][token]
-          ldsm_x4(vs + (8 * n2 + (lane & 7)) * kPitch + 32 * kp + 8 * (lane >> 3), b0, b1, b2, b3);
-        else            // values [token][channel]
-          ldsm_x4_t(vs + (32 * kp + 8 * (lane >> 3) + (lane & 7)) * kPitch + 8 * n2, b0, b1, b2, b3);
-        mma16816(d[j], A[2 * kp], b0, b1);
-        mma16816(d[j], A[2 * kp + 1], b2, b3);
-      }
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int n2 = 4 * n2g + j;
-      const int ch = 8 * n2 + 2 * c;
-      const float v0 = d[j][0] + d[j][2], v1 = d[j][1] + d[j][3];
-      if (kPacked) {
-        acc[n2][0] = fmaf(sc[640 + ch], v0 + gamma, acc[n2][0]);
-        acc[n2][1] = fmaf(sc[640 + ch + 1], v1 + gamma, acc[n2][1]);
-      } else {
-        acc[n2][0] += v0;
-        acc[n2][1] += v1;
+        for (int m = 0; m < 4; ++m) put_key_pair(bh, bl, off[r][m] + 4096 * k, v[m], f[r][m]);
       }
     }
   }
 }
 
-// q of head g (< group) of chunk token `tok`, channels of the fragment layout,
-// times `scale`; zeros for rows beyond the group.
-__device__ __forceinline__ void load_q_frag(const PrefillArgs& a, int64_t tok, int h, int g, int c, float scale,
-                                            float (&qv)[8][4]) {
-#pragma unroll
-  for (int ks = 0; ks < 8; ++ks) qv[ks][0] = qv[ks][1] = qv[ks][2] = qv[ks][3] = 0.f;
-  if (g >= a.group) return;
-  const uint16_t* row = a.q + (tok * a.hkv * a.group + static_cast<int64_t>(h) * a.group + g) * kD;
-#pragma unroll
-  for (int ks = 0; ks < 8; ++ks) {
-    const float2 p0 = h2pair(row + 16 * ks + 2 * c), p1 = h2pair(row + 16 * ks + 2 * c + 8);
-    qv[ks][0] = p0.x * scale; qv[ks][1] = p0.y * scale; qv[ks][2] = p1.x * scale; qv[ks][3] = p1.y * scale;
-  }
+// Generic-proxy shared-memory writes -> visible to the tensor core, all threads
+// past the barrier, then thread 0 may issue MMAs.
+__device__ __forceinline__ void sync_for_mma() {
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
 }
 
 template <int KB, int VB, bool kLean>
 __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(PrefillArgs a) {
-  extern __shared__ __align__(128) uint8_t smem[];
+  extern __shared__ __align__(1024) uint8_t smem[];
   using L = RecordLayout<KB, VB, kLean>;
-  uint16_t* ks = reinterpret_cast<uint16_t*>(smem + kOffK);
-  uint16_t* vs = reinterpret_cast<uint16_t*>(smem + kOffV);
+  uint8_t* opq = smem + kOffQ;                    // q hi at +0, lo at +32 KB
+  uint8_t* opb = smem + kOffB;                    // k~ / p' hi at +0, lo at +2 * kHalfB
+  uint8_t* opv = smem + kOffV;
   uint8_t* rec = smem + kOffRec;
-  float* sc = reinterpret_cast<float*>(smem + kOffScale);
-  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kOffCtl);      // [2]
+  float* sc = reinterpret_cast<float*>(smem + kOffSc);
+  float* xch = reinterpret_cast<float*>(smem + kOffX);
+  float* xb = reinterpret_cast<float*>(smem + kOffB);   // FWHT exchange ([2][64][128] fp32) when opb is free
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kOffBar);   // records [2], MMA
+  uint32_t* slot = reinterpret_cast<uint32_t*>(smem + kOffSlot);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int g = lane >> 2, c = lane & 3;
   const int h = blockIdx.y, s = blockIdx.z;
   const int t0 = a.cu[s], chunk = a.cu[s + 1] - t0;
-  if (static_cast<int>(blockIdx.x) * kPWarps >= chunk) return;        // whole CTA: nothing to do
-  const int p = blockIdx.x * kPWarps + warp;                           // this warp's chunk token
-  const bool active = p < chunk;
+  if (static_cast<int>(blockIdx.x) * kPTokens >= chunk) return;      // whole CTA: nothing to do
+  // row phases: thread (row, hf) owns columns / channels 64 hf .. 64 hf + 63 of row `row`
+  const int sub = warp & 3, hf = warp >> 2;
+  const int row = 32 * sub + lane;
+  const int p = static_cast<int>(blockIdx.x) * kPTokens + (row >> 3), gh = row & 7;
+  const bool active = p < chunk && gh < a.group;
+  const int64_t qrow = (static_cast<int64_t>(t0) + p) * a.hkv * a.group + static_cast<int64_t>(h) * a.group + gh;
   const int L0 = max(a.seq_lens[s], 0);
   int n_full = L0 / kB;
   if (n_full > a.max_blocks) {
@@ -381,115 +346,367 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(PrefillArgs a) {
     n_ws = 0;
     if (tid == 0 && blockIdx.x == 0 && h == 0) raise_flag(a.flags, KVARN_FLAG_BAD_LENGTH);
   }
+
   if (tid == 0) {
-    mbar_init(&bar[0], 1);
-    mbar_init(&bar[1], 1);
+    for (int b = 0; b < 3; ++b) mbar_init(&bar[b], 1);
     fence_mbar_init();
   }
+  if (warp == 0) tmem_alloc(slot, 512);
+  tc_fence_before();
   __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *slot;
+  const uint32_t trow = tmem_addr(tmem, 32 * sub, 0);          // this warp's lanes
+  const uint32_t s_tm = tmem + kColS, o_tm = tmem + kColO;
+  const uint32_t q_hi = smem_u32(opq), q_lo = q_hi + 2 * kHalfQ;
+  const uint32_t b_hi = smem_u32(opb), b_lo = b_hi + 2 * kHalfB;
+  const uint32_t v_op = smem_u32(opv);
+  constexpr uint32_t kId144 = idesc_f16_f32(128, 144), kId128 = idesc_f16_f32(128, 128);
 
-  float acc[16][2];
+  float acc[64];
 #pragma unroll
-  for (int n = 0; n < 16; ++n) acc[n][0] = acc[n][1] = 0.f;
+  for (int i = 0; i < 64; ++i) acc[i] = 0.f;
   float m_run = -INFINITY, l_run = 0.f;
-  float qv[8][4];
-  const int64_t tok = static_cast<int64_t>(t0) + (active ? p : 0);
-
-  // packed tiles, rotated domain: q_r = H q * log2(e) / sqrt(128), as FWHT(q) * log2(e) / 128
-  load_q_frag(a, tok, h, g, c, kLog2eP / 128.0f, qv);
-  fwht_q(qv, c);
-  // thread 0 starts the copy of packed tile ti into record buffer b; false (and the
-  // flag) for a block index outside the cache. Same answer in every thread.
-  auto prefetch = [&](int ti, int b) {
-    const int64_t blk = a.block_tables[static_cast<int64_t>(s) * a.max_blocks + ti];
-    const bool valid = blk >= 0 && blk < a.num_blocks;
-    if (tid == 0) {
-      if (valid) {
-        mbar_arrive_expect_tx(&bar[b], L::kBytes);
-        bulk_g2s(rec + b * kMaxRec, a.cache + (blk * a.hkv + h) * static_cast<int64_t>(L::kBytes), L::kBytes,
-                 &bar[b]);
-      } else {
-        raise_flag(a.flags, KVARN_FLAG_BAD_BLOCK);
-      }
-    }
-    return valid;
-  };
-  uint32_t phase = 0;                     // bit b: parity of record buffer b's barrier
-  uint32_t pending = 0;                   // bit b: a copy into buffer b not yet waited for
+  uint32_t mma_parity = 0;
+  bool mma_pending = false;                       // thread 0: a commit not yet waited for
   bool alive = true;
-  bool cur = n_full > 0 && prefetch(0, 0);
-  if (cur) pending |= 1u;
-  for (int ti = 0; ti < n_full; ++ti) {
-    const int b = ti & 1;
-    // the next tile's copy overlaps this one's work (buffer b ^ 1 was last read by
-    // the unpack of tile ti - 1, before the barrier that followed it)
-    const bool next = ti + 1 < n_full && prefetch(ti + 1, b ^ 1);
-    if (next) pending |= 2u >> b;
-    if (cur) {
-      const bool ok = mbar_wait(&bar[b], (phase >> b) & 1u, a.flags);
-      if (ok) {
-        phase ^= 1u << b;
-        pending &= ~(1u << b);
+
+  // waits for the MMAs committed last; every thread, bounded
+  auto wait_mma = [&]() {
+    bool ok = mbar_wait(&bar[2], mma_parity, a.flags);
+    if (ok) {
+      mma_parity ^= 1u;
+      if (tid == 0) mma_pending = false;
+    }
+    tc_fence_after();
+    return ok;
+  };
+
+  // softmax of this thread's 64 scores x (log2 domain, -inf = masked) against the row
+  // max over both halves; x becomes p; returns the correction of the old state
+  auto softmax = [&](float (&x)[64]) {
+    float mx = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < 64; j += 2) mx = fmax3f(mx, x[j], x[j + 1]);
+    xch[hf * 128 + row] = mx;
+    named_bar(1, kPThreads);
+    mx = fmaxf(mx, xch[(hf ^ 1) * 128 + row]);
+    const float m_new = fmaxf(m_run, mx);
+    float corr = 1.f;
+    if (m_new == -INFINITY) {                     // every token so far masked
+#pragma unroll
+      for (int j = 0; j < 64; ++j) x[j] = 0.f;
+    } else {
+      corr = ex2(m_run - m_new);
+      m_run = m_new;
+      const float2 nm = make_float2(-m_new, -m_new);
+      float2 ls = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int j = 0; j < 64; j += 2) {
+        const float2 e = __fadd2_rn(make_float2(x[j], x[j + 1]), nm);
+        x[j] = ex2(e.x);
+        x[j + 1] = ex2(e.y);
+        ls = __fadd2_rn(ls, make_float2(x[j], x[j + 1]));
       }
-      if (!__syncthreads_and(ok)) {       // the copy never arrived (flag raised): stop
-        alive = false;
-        break;
+      l_run = fmaf(l_run, corr, ls.x + ls.y);
+    }
+    const float2 c2 = make_float2(corr, corr);
+#pragma unroll
+    for (int i = 0; i < 64; i += 2) {
+      const float2 v = __fmul2_rn(make_float2(acc[i], acc[i + 1]), c2);
+      acc[i] = v.x;
+      acc[i + 1] = v.y;
+    }
+  };
+
+  // ---------------------------------------------------------------- packed tiles
+  if (n_full > 0) {
+    // q_r = H q * log2(e) / sqrt(128), as FWHT(q) * log2(e) / 128, into the A operand
+    {
+      float x[64];
+      const uint16_t* qp = a.q + qrow * kD + 64 * hf;
+#pragma unroll
+      for (int i = 0; i < 64; i += 2) {
+        const float2 f = active ? h2pair(qp + i) : make_float2(0.f, 0.f);
+        x[i] = f.x;
+        x[i + 1] = f.y;
       }
-      unpack_tile<KB, VB, kLean>(rec + b * kMaxRec, ks, vs, sc, tid);
+      fwht64(x);
+      fwht_pair(x, xb, row, hf);
+#pragma unroll
+      for (int i = 0; i < 64; ++i) x[i] *= kLog2eP / 128.0f;
+      store_split(x, opq, opq + 2 * kHalfQ, row, 64 * hf, kHalfQ);
+    }
+    // rows 129-143 of the keys operand stay zero (row 128 is rewritten per tile; the
+    // exchange above used this space)
+    for (int e = tid; e < 2 * 2 * 15 * 8; e += kPThreads) {   // [hi/lo][K half][row 129..143][16-byte chunk]
+      const int part = e / 240, rem = e % 240, k0 = 64 * (rem / 120), r = 129 + (rem % 120) / 8, c = rem % 8;
+      *reinterpret_cast<uint4*>(opb + part * 2 * kHalfB + swo(r, k0 + 8 * c, kHalfB)) = make_uint4(0, 0, 0, 0);
+    }
+    // thread 0 starts the copy of packed tile ti into record buffer b; false (and the
+    // flag) for a block index outside the cache. Same answer in every thread.
+    auto prefetch = [&](int ti, int b) {
+      const int64_t blk = a.block_tables[static_cast<int64_t>(s) * a.max_blocks + ti];
+      const bool valid = blk >= 0 && blk < a.num_blocks;
+      if (tid == 0) {
+        if (valid) {
+          mbar_arrive_expect_tx(&bar[b], L::kBytes);
+          bulk_g2s(rec + b * kMaxRec, a.cache + (blk * a.hkv + h) * static_cast<int64_t>(L::kBytes), L::kBytes,
+                   &bar[b]);
+        } else {
+          raise_flag(a.flags, KVARN_FLAG_BAD_BLOCK);
+        }
+      }
+      return valid;
+    };
+    uint32_t phase = 0;                   // bit b: parity of record buffer b's barrier
+    uint32_t pending = 0;                 // bit b: a copy into buffer b not yet waited for
+    bool cur = prefetch(0, 0);
+    if (cur) pending |= 1u;
+    for (int ti = 0; ti < n_full; ++ti) {
+      const int b = ti & 1;
+      const bool next = ti + 1 < n_full && prefetch(ti + 1, b ^ 1);
+      if (next) pending |= 2u >> b;
+      if (cur) {
+        bool ok = mbar_wait(&bar[b], (phase >> b) & 1u, a.flags);
+        if (ok) {
+          phase ^= 1u << b;
+          pending &= ~(1u << b);
+        }
+        if (!__syncthreads_and(ok)) {
+          alive = false;
+          break;
+        }
+        const uint8_t* r = rec + b * kMaxRec;
+        if (tid < 128) unpack_scales<KB, VB, kLean>(r, sc, opb, opb + 2 * kHalfB, tid);
+        __syncthreads();
+        unpack_keys<KB, VB, kLean>(r, sc + 4 * 128, opb, opb + 2 * kHalfB, tid);
+        sync_for_mma();
+        if (tid == 0) {
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const uint64_t ah = op_desc(q_hi, k, kHalfQ), al = op_desc(q_lo, k, kHalfQ);
+            const uint64_t bh = op_desc(b_hi, k, kHalfB), bl = op_desc(b_lo, k, kHalfB);
+            umma_f16(s_tm, ah, bh, kId144, k > 0);
+            umma_f16(s_tm, ah, bl, kId144, 1);
+            umma_f16(s_tm, al, bh, kId144, 1);
+          }
+          umma_commit(&bar[2]);
+          mma_pending = true;
+        }
+        // the value operand (read by the previous tile's finished PV) fills while
+        // the tensor core computes the scores
+        unpack_values<KB, VB, kLean>(r, opv, tid);
+        ok = wait_mma();
+        float x[64], beta;
+        tld_x32(trow + kColS + 64 * hf, x);
+        tld_x32(trow + kColS + 64 * hf + 32, x + 32);
+        tld_x1(trow + kColS + 128, beta);
+        tmem_wait_x32(x);
+        tmem_wait_x32(x + 32);
+        tld_wait1(beta);
+        {
+          const float2 b2 = make_float2(beta, beta);
+          const float4* ck = reinterpret_cast<const float4*>(sc + 64 * hf);
+#pragma unroll
+          for (int j = 0; j < 64; j += 4) {
+            const float4 c = ck[j >> 2];
+            const float2 u = __fmul2_rn(__fadd2_rn(make_float2(x[j], x[j + 1]), b2), make_float2(c.x, c.y));
+            const float2 w = __fmul2_rn(__fadd2_rn(make_float2(x[j + 2], x[j + 3]), b2), make_float2(c.z, c.w));
+            x[j] = u.x; x[j + 1] = u.y; x[j + 2] = w.x; x[j + 3] = w.y;
+          }
+        }
+        softmax(x);
+        float gam;
+        {
+          float2 g2 = make_float2(0.f, 0.f);
+          const float4* cs = reinterpret_cast<const float4*>(sc + 1 * 128 + 64 * hf);
+          const float4* cz = reinterpret_cast<const float4*>(sc + 2 * 128 + 64 * hf);
+#pragma unroll
+          for (int j = 0; j < 64; j += 4) {
+            const float4 z = cz[j >> 2], c = cs[j >> 2];
+            const float2 p0 = make_float2(x[j], x[j + 1]), p1 = make_float2(x[j + 2], x[j + 3]);
+            g2 = __ffma2_rn(p0, make_float2(z.x, z.y), g2);
+            g2 = __ffma2_rn(p1, make_float2(z.z, z.w), g2);
+            const float2 u = __fmul2_rn(p0, make_float2(c.x, c.y)), w = __fmul2_rn(p1, make_float2(c.z, c.w));
+            x[j] = u.x; x[j + 1] = u.y; x[j + 2] = w.x; x[j + 3] = w.y;
+          }
+          gam = g2.x + g2.y;
+        }
+        tmem_split_store(x, trow + kColP + 32 * hf);
+        xch[256 + hf * 128 + row] = gam;
+        tst_wait();
+        sync_for_mma();
+        if (!__syncthreads_and(ok)) {
+          alive = false;
+          break;
+        }
+        if (tid == 0) {
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const uint64_t bv = op_desc(v_op, k, kHalfQ);
+            umma_f16_ts(o_tm, tmem + kColP + 8 * k, bv, kId128, k > 0);
+            umma_f16_ts(o_tm, tmem + kColP + 64 + 8 * k, bv, kId128, 1);
+          }
+          umma_commit(&bar[2]);
+          mma_pending = true;
+        }
+        gam += xch[256 + (hf ^ 1) * 128 + row];
+        ok = wait_mma();
+        tld_x32(trow + kColO + 64 * hf, x);
+        tld_x32(trow + kColO + 64 * hf + 32, x + 32);
+        tmem_wait_x32(x);
+        tmem_wait_x32(x + 32);
+        {
+          const float2 g2 = make_float2(gam, gam);
+          const float4* rv = reinterpret_cast<const float4*>(sc + 3 * 128 + 64 * hf);
+#pragma unroll
+          for (int i = 0; i < 64; i += 4) {
+            const float4 v = rv[i >> 2];
+            const float2 u = __ffma2_rn(make_float2(v.x, v.y), __fadd2_rn(make_float2(x[i], x[i + 1]), g2),
+                                        make_float2(acc[i], acc[i + 1]));
+            const float2 w = __ffma2_rn(make_float2(v.z, v.w), __fadd2_rn(make_float2(x[i + 2], x[i + 3]), g2),
+                                        make_float2(acc[i + 2], acc[i + 3]));
+            acc[i] = u.x; acc[i + 1] = u.y; acc[i + 2] = w.x; acc[i + 3] = w.y;
+          }
+        }
+        tc_fence_before();
+        if (!__syncthreads_and(ok)) {     // operands and TMEM are rewritten next
+          alive = false;
+          break;
+        }
+      }
+      cur = next;
+    }
+    if (!alive) {
+      if (tid == 0) {                     // copies and MMAs in flight finish before the CTA exits
+        for (int b = 0; b < 2; ++b)
+          if ((pending >> b) & 1u) mbar_wait(&bar[b], (phase >> b) & 1u, a.flags);
+        if (mma_pending) mbar_wait(&bar[2], mma_parity, a.flags);
+      }
+      tc_fence_before();
       __syncthreads();
-      if (active) attend_block<true>(ks, vs, sc, qv, g, c, lane, 0, m_run, l_run, acc);
-      __syncthreads();                    // shared tiles and record buffer b are rewritten next
+      tc_fence_after();
+      if (warp == 0) tmem_dealloc(tmem, 512);
+      return;
     }
-    cur = next;
-  }
-  if (!alive) {
-    if (tid == 0)                         // let copies still in flight land before the CTA exits
-      for (int b = 0; b < 2; ++b)
-        if ((pending >> b) & 1u) mbar_wait(&bar[b], (phase >> b) & 1u, a.flags);
-    return;
+    // back to the input domain: acc_u = H acc_r = FWHT(acc_r) / sqrt(128)
+    fwht64(acc);
+    fwht_pair(acc, xb, row, hf);
+#pragma unroll
+    for (int i = 0; i < 64; ++i) acc[i] *= kInvSqrt128;
   }
 
-  // back to the input domain: acc_u = H acc_r (orthonormal H), then the fresh tokens
-  fwht_acc(acc, c);
+  // ---------------------------------------------------------------- fresh tokens
+  // q * log2(e) / sqrt(128), unrotated, into the A operand (the packed pass is done)
+  {
+    float x[64];
+    const uint16_t* qp = a.q + qrow * kD + 64 * hf;
 #pragma unroll
-  for (int n = 0; n < 16; ++n) {
-    acc[n][0] *= kInvSqrt128;
-    acc[n][1] *= kInvSqrt128;
+    for (int i = 0; i < 64; i += 2) {
+      const float2 f = active ? h2pair(qp + i) : make_float2(0.f, 0.f);
+      x[i] = f.x * (kLog2eP * kInvSqrt128);
+      x[i + 1] = f.y * (kLog2eP * kInvSqrt128);
+    }
+    store_split(x, opq, opq + 2 * kHalfQ, row, 64 * hf, kHalfQ);
   }
-  load_q_frag(a, tok, h, g, c, kLog2eP * kInvSqrt128, qv);
-  // fresh token f: workspace token f (f < n_ws) or chunk token f - n_ws; this CTA's
-  // last token attends f <= n_ws + p_last
-  const int p_last = min(chunk - 1, static_cast<int>(blockIdx.x) * kPWarps + kPWarps - 1);
+  // fresh token f: workspace token f (f < n_ws) or chunk token f - n_ws; row `row`
+  // attends f <= n_ws + p; this CTA's last token attends f < n_fresh
+  const int p_last = min(chunk - 1, static_cast<int>(blockIdx.x) * kPTokens + kPTokens - 1);
   const int n_fresh = n_ws + p_last + 1;
-  for (int fb = 0; fb * kB < n_fresh; ++fb) {
-    // rows f = 128 fb + r; 16-byte pieces: K and V, 128 rows x 16 pieces each
-    for (int e = tid; e < 2 * 128 * 16; e += kPThreads) {
-      const int which = e >> 11, r = (e >> 4) & 127, piece = e & 15;
-      const int f = fb * kB + r;
+  const int lim = min(n_ws + p, n_fresh - 1);
+  auto fresh_src = [&](int f, int which) -> const uint16_t* {
+    if (f < n_ws) return a.ws + (((static_cast<int64_t>(s) * a.hkv + h) * 2 + which) * kB + f) * kD;
+    return (which ? a.v_new : a.k_new) + ((static_cast<int64_t>(t0) + f - n_ws) * a.hkv + h) * kD;
+  };
+  bool ok = true;
+  for (int fb = 0; fb * kB < n_fresh && ok; ++fb) {
+    // keys [token][channel] into the B operand of QK^T (hi part only: fp16 exact)
+    for (int e = tid; e < 128 * 16; e += kPThreads) {
+      const int jj = e >> 4, c8 = e & 15, f = fb * kB + jj;
       uint4 v = make_uint4(0, 0, 0, 0);
-      if (f < n_fresh) {
-        const uint16_t* src;
-        if (f < n_ws)
-          src = a.ws + (((static_cast<int64_t>(s) * a.hkv + h) * 2 + which) * kB + f) * kD;
-        else
-          src = (which ? a.v_new : a.k_new) + ((static_cast<int64_t>(t0) + f - n_ws) * a.hkv + h) * kD;
-        v = *reinterpret_cast<const uint4*>(src + piece * 8);
-      }
-      *reinterpret_cast<uint4*>((which ? vs : ks) + r * kPitch + piece * 8) = v;
+      if (f < n_fresh) v = *reinterpret_cast<const uint4*>(fresh_src(f, 0) + 8 * c8);
+      *reinterpret_cast<uint4*>(opb + swo(jj, 8 * c8, kHalfB)) = v;
     }
-    __syncthreads();
-    if (active) attend_block<false>(ks, vs, nullptr, qv, g, c, lane, n_ws + p - fb * kB, m_run, l_run, acc);
-    __syncthreads();
+    // values transposed to [channel][token]: lane = token, so each 2-byte store of a
+    // warp fills 64 contiguous bytes of one channel row
+    for (int e = tid; e < 128 * 16; e += kPThreads) {
+      const int c8 = e >> 7, jj = e & 127, f = fb * kB + jj;
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (f < n_fresh) v = *reinterpret_cast<const uint4*>(fresh_src(f, 1) + 8 * c8);
+      const uint16_t* u = reinterpret_cast<const uint16_t*>(&v);
+#pragma unroll
+      for (int e2 = 0; e2 < 8; ++e2) *reinterpret_cast<uint16_t*>(opv + swo(8 * c8 + e2, jj, kHalfQ)) = u[e2];
+    }
+    sync_for_mma();
+    if (tid == 0) {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const uint64_t bk = op_desc(b_hi, k, kHalfB);
+        umma_f16(s_tm, op_desc(q_hi, k, kHalfQ), bk, kId128, k > 0);
+        umma_f16(s_tm, op_desc(q_lo, k, kHalfQ), bk, kId128, 1);
+      }
+      umma_commit(&bar[2]);
+      mma_pending = true;
+    }
+    ok = wait_mma();
+    float x[64];
+    tld_x32(trow + kColS + 64 * hf, x);
+    tld_x32(trow + kColS + 64 * hf + 32, x + 32);
+    tmem_wait_x32(x);
+    tmem_wait_x32(x + 32);
+#pragma unroll
+    for (int j = 0; j < 64; ++j)
+      if (fb * kB + 64 * hf + j > lim) x[j] = -INFINITY;
+    softmax(x);
+    tmem_split_store(x, trow + kColP + 32 * hf);
+    tst_wait();
+    sync_for_mma();
+    if (!__syncthreads_and(ok)) break;
+    if (tid == 0) {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const uint64_t bv = op_desc(v_op, k, kHalfQ);
+        umma_f16_ts(o_tm, tmem + kColP + 8 * k, bv, kId128, k > 0);
+        umma_f16_ts(o_tm, tmem + kColP + 64 + 8 * k, bv, kId128, 1);
+      }
+      umma_commit(&bar[2]);
+      mma_pending = true;
+    }
+    ok = wait_mma();
+    tld_x32(trow + kColO + 64 * hf, x);
+    tld_x32(trow + kColO + 64 * hf + 32, x + 32);
+    tmem_wait_x32(x);
+    tmem_wait_x32(x + 32);
+#pragma unroll
+    for (int i = 0; i < 64; i += 2) {
+      const float2 u = __fadd2_rn(make_float2(acc[i], acc[i + 1]), make_float2(x[i], x[i + 1]));
+      acc[i] = u.x;
+      acc[i + 1] = u.y;
+    }
+    tc_fence_before();
+    ok = __syncthreads_and(ok);
   }
 
-  if (!active || g >= a.group) return;
-  const float l = quad_sum(l_run);
+  // output: acc / l over both halves
+  xch[512 + hf * 128 + row] = l_run;
+  if (tid == 0 && mma_pending) mbar_wait(&bar[2], mma_parity, a.flags);   // only after a timeout
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(tmem, 512);
+  if (!ok || !active) return;
+  const float l = l_run + xch[512 + (hf ^ 1) * 128 + row];
   const float inv_l = l > 0.f ? 1.0f / l : 0.f;
-  uint16_t* orow = a.out + (tok * a.hkv * a.group + static_cast<int64_t>(h) * a.group + g) * kD;
+  uint16_t* orow = a.out + qrow * kD + 64 * hf;
 #pragma unroll
-  for (int n = 0; n < 16; ++n) {
-    const uint32_t lo = f2h_bits(acc[n][0] * inv_l), hi = f2h_bits(acc[n][1] * inv_l);
-    *reinterpret_cast<uint32_t*>(orow + 8 * n + 2 * c) = lo | (hi << 16);
+  for (int q = 0; q < 8; ++q) {
+    uint32_t w[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      w[e] = static_cast<uint32_t>(f2h_bits(acc[8 * q + 2 * e] * inv_l)) |
+             (static_cast<uint32_t>(f2h_bits(acc[8 * q + 2 * e + 1] * inv_l)) << 16);
+    *reinterpret_cast<uint4*>(orow + 8 * q) = make_uint4(w[0], w[1], w[2], w[3]);
   }
 }
 
@@ -498,7 +715,7 @@ cudaError_t launch_prefill_kernel(const PrefillArgs& a, int n_seqs, int max_chun
   static std::atomic<unsigned long long> smem_set{0};
   cudaError_t err = set_smem_once(prefill_kernel<KB, VB, kLean>, kPSmem, smem_set);
   if (err != cudaSuccess) return err;
-  const dim3 grid((max_chunk + kPWarps - 1) / kPWarps, a.hkv, n_seqs);
+  const dim3 grid((max_chunk + kPTokens - 1) / kPTokens, a.hkv, n_seqs);
   prefill_kernel<KB, VB, kLean><<<grid, kPThreads, kPSmem, stream>>>(a);
   return cudaGetLastError();
 }
