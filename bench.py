@@ -479,6 +479,60 @@ def run_reference(args):
     print(json.dumps(res), flush=True)
 
 
+# `--case prefill_attn`: the chunked-prefill attention kernel alone (not the headline
+# line): 16 sequences x (4096 cached tokens in 32 packed k4v2 tiles + a 512-token
+# chunk), 64 q-heads over 8 kv-heads, random valid records; flops 4 x 128 per (q-head,
+# attended token). L2 is flushed before every timed call.
+PREFILL_ATTN = dict(n_seqs=16, cached=4096, chunk=512, n_kv_heads=8, group=8, seed=5)
+
+
+def run_prefill_attn(args):
+    import numpy as np
+    import torch
+    import kvarn_synth as synth
+    import kv_cache_quantization_x128_gb300 as kv
+    torch.cuda.set_device(0)
+    c = PREFILL_ATTN
+    n_seqs, hkv, group = c["n_seqs"], c["n_kv_heads"], c["group"]
+    mb = c["cached"] // 128
+    nb = n_seqs * mb
+    f16 = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.float16).cuda()
+    rec = torch.from_numpy(synth.random_records(nb * hkv, c["seed"], 14336, 12288)).cuda().reshape(nb, hkv, 14336)
+    bt = torch.from_numpy(synth.block_tables(n_seqs, mb, nb, c["seed"])).cuda()
+    lens = torch.full((n_seqs,), c["cached"], dtype=torch.int32, device="cuda")
+    cu = torch.arange(0, (n_seqs + 1) * c["chunk"], c["chunk"], dtype=torch.int32, device="cuda")
+    n = n_seqs * c["chunk"]
+    k, v = synth.prefill_kv(n, hkv, seed=c["seed"] + 1)
+    q = f16(synth.queries(n, hkv * group, c["seed"]))
+    kd, vd = f16(k), f16(v)
+    out = torch.empty_like(q)
+    meta = kv.make_meta(hkv, hkv * group, nb, max_blocks_per_seq=mb)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    call = lambda: kv.kvarn_prefill_attention(q, kd, vd, cu, lens, c["chunk"], bt, rec, None, out, meta)
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(args.steps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        call()
+        e1.record()
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1))
+    if kv.kvarn_device_flags() != 0:
+        raise SystemExit("prefill attention raised a device flag")
+    ms = float(np.median(times))
+    pairs = n_seqs * sum(c["cached"] + p + 1 for p in range(c["chunk"]))    # (query, key) pairs per q-head
+    flops = 4.0 * 128 * hkv * group * pairs
+    print(json.dumps({"metric": "chunked_prefill_attention_tflops", "value": round(flops / (ms * 1e-3) / 1e12, 1),
+                      "unit": "TFLOP/s", "ms_per_call": round(ms, 4), "steps": args.steps, "warmup": args.warmup,
+                      "higher_is_better": True, "dtype": "f16 operands (hi + lo pairs), f32 accumulate",
+                      "data": "synthetic", "config": {"workload": "prefill_attn_16x(4096+512)_gqa64/8", "l2": "flushed"},
+                      "prefill_tokens_per_s": round(n / (ms * 1e-3))}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -487,8 +541,9 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--case", default="full", choices=["full", "small"],
-                    help="small: reduced shapes for profiler captures (not a bench line)")
+    ap.add_argument("--case", default="full", choices=["full", "small", "prefill_attn"],
+                    help="small: reduced shapes for profiler captures (not a bench line); "
+                         "prefill_attn: the chunked-prefill attention kernel alone")
     ap.add_argument("--preset", default="k4v2", choices=sorted(PRESET_RECORD),
                     help="bit preset of the gb300 arm; the default k4v2 is the headline workload")
     args = ap.parse_args()
@@ -502,7 +557,9 @@ def main():
         args.no_cpu_baseline = True
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    if args.impl == "reference":
+    if args.case == "prefill_attn":
+        run_prefill_attn(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_gpu(args)
