@@ -17,7 +17,14 @@
 //         B = value codes (exact); acc_i += r^V_i (D_i + gamma),
 //         gamma = sum_j p_j c^V_j z^V_j.
 // Two threads own a row (channels 0-63 and 64-127 of S and of the accumulator,
-// which lives in registers). The packed pass runs in the rotated domain (q_r = H q);
+// which lives in registers). Warps 0-7 do all the per-tile thread work (code
+// unpacking, softmax, accumulator); the first warp of a third warpgroup only issues
+// the UMMAs and starts the record copies, so no row warp waits in an issue (a thread
+// issuing a tile's UMMAs was measured to stay there for most of their run). setmaxnreg
+// moves the registers to the row warps (232 each, 40 for the issuing warpgroup).
+// Per tile t the row warps take S(t), the softmax and p'(t), then unpack tile t + 1's
+// keys while PV(t) runs, so its QK^T is queued as soon as they are ready.
+// The packed pass runs in the rotated domain (q_r = H q);
 // the accumulator is then rotated back once (H is its own inverse) and the fresh
 // pass (workspace tail and chunk, causal) continues in the input domain with
 // unrotated q and plain fp16 K/V under the same online softmax (log2 domain).
@@ -29,7 +36,11 @@
 namespace kvarn {
 namespace {
 
-constexpr int kPThreads = 256;                    // 8 warps; two threads per row in the row phases
+constexpr int kRowThreads = 256;                  // 8 row warps: two threads per row in the row phases
+constexpr int kPThreads = kRowThreads + 128;      // + one warpgroup whose first warp issues the UMMAs
+// Registers after the split (setmaxnreg): 2 x 128 x 232 + 128 x 40 = 384 x 168, the
+// launch's allocation at 168 a thread.
+constexpr int kRowRegs = 232, kIssueRegs = 40;
 constexpr int kPTokens = 16;                      // chunk tokens per CTA (x 8 head slots = 128 rows)
 constexpr uint32_t kHalfB = 18432;                // K-half stride of the keys operand (144 rows)
 constexpr uint32_t kHalfQ = 16384;                // K-half stride of the 128-row operands
@@ -38,10 +49,11 @@ constexpr int kOffQ = 0;                          // A of QK^T: q hi, q lo (32 K
 constexpr int kOffB = 65536;                      // B of QK^T: k~ hi, lo (36 KB each)
 constexpr int kOffV = kOffB + 4 * kHalfB;         // B of PV: values [channel][token] (32 KB)
 constexpr int kOffRec = kOffV + 2 * kHalfQ;       // packed records [2] (the next one in flight)
-constexpr int kOffSc = kOffRec + 2 * kMaxRec;     // fp32 [5][128]: c^K, c s^V, c z^V, r^V, r s^K
-constexpr int kOffX = kOffSc + 5 * 512;           // fp32 [3][2][128]: row max, gamma and sum of each half
-constexpr int kOffBar = kOffX + 3 * 1024;         // mbarriers: records [2], MMA
-constexpr int kOffSlot = kOffBar + 24;            // TMEM base address
+constexpr int kScN = 5 * 128;                     // scale floats of one tile
+constexpr int kOffSc = kOffRec + 2 * kMaxRec;     // fp32 [2][5][128]: c^K, c s^V, c z^V, r^V, r s^K
+constexpr int kOffX = kOffSc + 2 * kScN * 4;      // fp32 [3][2][128]: row max, gamma and sum of each half
+constexpr int kOffBar = kOffX + 3 * 1024;         // mbarriers: records [2], QK^T, PV
+constexpr int kOffSlot = kOffBar + 32;            // TMEM base address
 constexpr int kPSmem = kOffSlot + 8;
 constexpr uint32_t kColS = 0, kColO = 256, kColP = 384;   // TMEM columns: S (144), PV product (128), p' hi, lo (64 + 64)
 constexpr float kLog2eP = 1.4426950408889634f;
@@ -114,7 +126,6 @@ __device__ __forceinline__ void tst_x32(uint32_t taddr, const uint32_t* r) {
       "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
       : "memory");
 }
-__device__ __forceinline__ void tst_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // 64 fp32 values as fp16 (hi, lo) pairs into 32 TMEM columns each (hi at taddr, lo at
 // taddr + 64), two values per column.
@@ -145,13 +156,13 @@ __device__ __forceinline__ void fwht64(float (&x)[64]) {
 __device__ __forceinline__ void fwht_pair(float (&x)[64], float* xb, int row, int hf) {
 #pragma unroll
   for (int i = 0; i < 64; ++i) xb[(hf * 64 + i) * 128 + row] = x[i];
-  __syncthreads();
+  named_bar(2, kRowThreads);
 #pragma unroll
   for (int i = 0; i < 64; ++i) {
     const float o = xb[((hf ^ 1) * 64 + i) * 128 + row];
     x[i] = hf == 0 ? x[i] + o : o - x[i];
   }
-  __syncthreads();
+  named_bar(2, kRowThreads);
 }
 
 // 64 fp32 values of a row (K indices k0 .. k0 + 63) as fp16 hi and lo parts into two
@@ -303,13 +314,27 @@ __device__ __forceinline__ void unpack_keys(const uint8_t* rec, const float* rs,
   }
 }
 
-// Generic-proxy shared-memory writes -> visible to the tensor core, all threads
-// past the barrier, then thread 0 may issue MMAs.
-__device__ __forceinline__ void sync_for_mma() {
+// Named barriers: 0 (__syncthreads) at the start and the end only; 1 the row max
+// exchange and 2 the other row-only points (256 threads); 3 "p' (and the tile's values)
+// ready" and 4 "keys ready": the row threads arrive, the issuing warp waits (288).
+__device__ __forceinline__ void bar_arrive(int id, int n) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+template <int N>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+// A row thread's operand writes (shared memory, TMEM) visible to the tensor core,
+// then its arrival on producer barrier `id`.
+__device__ __forceinline__ void rows_ready(int id) {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
   fence_proxy_async_smem();
   tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
+  bar_arrive(id, kRowThreads + 32);
 }
 
 template <int KB, int VB, bool kLean>
@@ -317,24 +342,18 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(PrefillArgs a) {
   extern __shared__ __align__(1024) uint8_t smem[];
   using L = RecordLayout<KB, VB, kLean>;
   uint8_t* opq = smem + kOffQ;                    // q hi at +0, lo at +32 KB
-  uint8_t* opb = smem + kOffB;                    // k~ / p' hi at +0, lo at +2 * kHalfB
+  uint8_t* opb = smem + kOffB;                    // k~ hi at +0, lo at +2 * kHalfB
   uint8_t* opv = smem + kOffV;
   uint8_t* rec = smem + kOffRec;
-  float* sc = reinterpret_cast<float*>(smem + kOffSc);
+  float* scb = reinterpret_cast<float*>(smem + kOffSc);   // [2][kScN]
   float* xch = reinterpret_cast<float*>(smem + kOffX);
-  float* xb = reinterpret_cast<float*>(smem + kOffB);   // FWHT exchange ([2][64][128] fp32) when opb is free
-  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kOffBar);   // records [2], MMA
+  float* xb = reinterpret_cast<float*>(smem + kOffB);     // FWHT exchange ([2][64][128] fp32) when opb is free
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kOffBar);   // records [2], QK^T, PV
   uint32_t* slot = reinterpret_cast<uint32_t*>(smem + kOffSlot);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int h = blockIdx.y, s = blockIdx.z;
   const int t0 = a.cu[s], chunk = a.cu[s + 1] - t0;
   if (static_cast<int>(blockIdx.x) * kPTokens >= chunk) return;      // whole CTA: nothing to do
-  // row phases: thread (row, hf) owns columns / channels 64 hf .. 64 hf + 63 of row `row`
-  const int sub = warp & 3, hf = warp >> 2;
-  const int row = 32 * sub + lane;
-  const int p = static_cast<int>(blockIdx.x) * kPTokens + (row >> 3), gh = row & 7;
-  const bool active = p < chunk && gh < a.group;
-  const int64_t qrow = (static_cast<int64_t>(t0) + p) * a.hkv * a.group + static_cast<int64_t>(h) * a.group + gh;
   const int L0 = max(a.seq_lens[s], 0);
   int n_full = L0 / kB;
   if (n_full > a.max_blocks) {
@@ -346,9 +365,20 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(PrefillArgs a) {
     n_ws = 0;
     if (tid == 0 && blockIdx.x == 0 && h == 0) raise_flag(a.flags, KVARN_FLAG_BAD_LENGTH);
   }
+  // fresh token f: workspace token f (f < n_ws) or chunk token f - n_ws; this CTA's
+  // last token attends f < n_fresh
+  const int p_last = min(chunk - 1, static_cast<int>(blockIdx.x) * kPTokens + kPTokens - 1);
+  const int n_fresh = n_ws + p_last + 1;
+  const int n_fb = (n_fresh + kB - 1) / kB;
+  // tile ti's block index is inside the cache (same answer in every thread); a tile
+  // outside attends nothing
+  auto valid_tile = [&](int ti) {
+    const int64_t blk = a.block_tables[static_cast<int64_t>(s) * a.max_blocks + ti];
+    return blk >= 0 && blk < a.num_blocks;
+  };
 
   if (tid == 0) {
-    for (int b = 0; b < 3; ++b) mbar_init(&bar[b], 1);
+    for (int b = 0; b < 4; ++b) mbar_init(&bar[b], 1);
     fence_mbar_init();
   }
   if (warp == 0) tmem_alloc(slot, 512);
@@ -356,148 +386,220 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(PrefillArgs a) {
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *slot;
-  const uint32_t trow = tmem_addr(tmem, 32 * sub, 0);          // this warp's lanes
   const uint32_t s_tm = tmem + kColS, o_tm = tmem + kColO;
   const uint32_t q_hi = smem_u32(opq), q_lo = q_hi + 2 * kHalfQ;
   const uint32_t b_hi = smem_u32(opb), b_lo = b_hi + 2 * kHalfB;
   const uint32_t v_op = smem_u32(opv);
   constexpr uint32_t kId144 = idesc_f16_f32(128, 144), kId128 = idesc_f16_f32(128, 128);
 
-  float acc[64];
-#pragma unroll
-  for (int i = 0; i < 64; ++i) acc[i] = 0.f;
-  float m_run = -INFINITY, l_run = 0.f;
-  uint32_t mma_parity = 0;
-  bool mma_pending = false;                       // thread 0: a commit not yet waited for
-  bool alive = true;
+  const bool rower = warp < kRowThreads / 32;
+  const int sub = warp & 3, hf = (warp >> 2) & 1;
+  const int row = 32 * sub + lane;
+  const int p = static_cast<int>(blockIdx.x) * kPTokens + (row >> 3), gh = row & 7;
+  const bool active = rower && p < chunk && gh < a.group;
+  const int64_t qrow = (static_cast<int64_t>(t0) + p) * a.hkv * a.group + static_cast<int64_t>(h) * a.group + gh;
 
-  // waits for the MMAs committed last; every thread, bounded
-  auto wait_mma = [&]() {
-    bool ok = mbar_wait(&bar[2], mma_parity, a.flags);
-    if (ok) {
-      mma_parity ^= 1u;
-      if (tid == 0) mma_pending = false;
-    }
-    tc_fence_after();
-    return ok;
-  };
-
-  // softmax of this thread's 64 scores x (log2 domain, -inf = masked) against the row
-  // max over both halves; x becomes p; returns the correction of the old state
-  auto softmax = [&](float (&x)[64]) {
-    float mx = -INFINITY;
-#pragma unroll
-    for (int j = 0; j < 64; j += 2) mx = fmax3f(mx, x[j], x[j + 1]);
-    xch[hf * 128 + row] = mx;
-    named_bar(1, kPThreads);
-    mx = fmaxf(mx, xch[(hf ^ 1) * 128 + row]);
-    const float m_new = fmaxf(m_run, mx);
-    float corr = 1.f;
-    if (m_new == -INFINITY) {                     // every token so far masked
-#pragma unroll
-      for (int j = 0; j < 64; ++j) x[j] = 0.f;
-    } else {
-      corr = ex2(m_run - m_new);
-      m_run = m_new;
-      const float2 nm = make_float2(-m_new, -m_new);
-      float2 ls = make_float2(0.f, 0.f);
-#pragma unroll
-      for (int j = 0; j < 64; j += 2) {
-        const float2 e = __fadd2_rn(make_float2(x[j], x[j + 1]), nm);
-        x[j] = ex2(e.x);
-        x[j + 1] = ex2(e.y);
-        ls = __fadd2_rn(ls, make_float2(x[j], x[j + 1]));
-      }
-      l_run = fmaf(l_run, corr, ls.x + ls.y);
-    }
-    const float2 c2 = make_float2(corr, corr);
-#pragma unroll
-    for (int i = 0; i < 64; i += 2) {
-      const float2 v = __fmul2_rn(make_float2(acc[i], acc[i + 1]), c2);
-      acc[i] = v.x;
-      acc[i + 1] = v.y;
-    }
-  };
-
-  // ---------------------------------------------------------------- packed tiles
-  if (n_full > 0) {
-    // q_r = H q * log2(e) / sqrt(128), as FWHT(q) * log2(e) / 128, into the A operand
-    {
-      float x[64];
-      const uint16_t* qp = a.q + qrow * kD + 64 * hf;
-#pragma unroll
-      for (int i = 0; i < 64; i += 2) {
-        const float2 f = active ? h2pair(qp + i) : make_float2(0.f, 0.f);
-        x[i] = f.x;
-        x[i + 1] = f.y;
-      }
-      fwht64(x);
-      fwht_pair(x, xb, row, hf);
-#pragma unroll
-      for (int i = 0; i < 64; ++i) x[i] *= kLog2eP / 128.0f;
-      store_split(x, opq, opq + 2 * kHalfQ, row, 64 * hf, kHalfQ);
-    }
-    // rows 129-143 of the keys operand stay zero (row 128 is rewritten per tile; the
-    // exchange above used this space)
-    for (int e = tid; e < 2 * 2 * 15 * 8; e += kPThreads) {   // [hi/lo][K half][row 129..143][16-byte chunk]
-      const int part = e / 240, rem = e % 240, k0 = 64 * (rem / 120), r = 129 + (rem % 120) / 8, c = rem % 8;
-      *reinterpret_cast<uint4*>(opb + part * 2 * kHalfB + swo(r, k0 + 8 * c, kHalfB)) = make_uint4(0, 0, 0, 0);
-    }
-    // thread 0 starts the copy of packed tile ti into record buffer b; false (and the
-    // flag) for a block index outside the cache. Same answer in every thread.
-    auto prefetch = [&](int ti, int b) {
-      const int64_t blk = a.block_tables[static_cast<int64_t>(s) * a.max_blocks + ti];
-      const bool valid = blk >= 0 && blk < a.num_blocks;
-      if (tid == 0) {
-        if (valid) {
+  if (!rower) {
+    // ------------------------------------------------------------ issuing warpgroup
+    regs_dec<kIssueRegs>();
+    if (warp == kRowThreads / 32) {
+      const bool leader = lane == 0;
+      uint32_t n_qk = 0, n_pv = 0;        // commits on the QK^T and PV barriers
+      auto prefetch = [&](int ti) {       // record of tile ti into buffer ti & 1
+        if (ti >= n_full) return;
+        const int64_t blk = a.block_tables[static_cast<int64_t>(s) * a.max_blocks + ti];
+        const int b = ti & 1;
+        if (blk >= 0 && blk < a.num_blocks) {
           mbar_arrive_expect_tx(&bar[b], L::kBytes);
           bulk_g2s(rec + b * kMaxRec, a.cache + (blk * a.hkv + h) * static_cast<int64_t>(L::kBytes), L::kBytes,
                    &bar[b]);
         } else {
           raise_flag(a.flags, KVARN_FLAG_BAD_BLOCK);
         }
-      }
-      return valid;
-    };
-    uint32_t phase = 0;                   // bit b: parity of record buffer b's barrier
-    uint32_t pending = 0;                 // bit b: a copy into buffer b not yet waited for
-    bool cur = prefetch(0, 0);
-    if (cur) pending |= 1u;
-    for (int ti = 0; ti < n_full; ++ti) {
-      const int b = ti & 1;
-      const bool next = ti + 1 < n_full && prefetch(ti + 1, b ^ 1);
-      if (next) pending |= 2u >> b;
-      if (cur) {
-        bool ok = mbar_wait(&bar[b], (phase >> b) & 1u, a.flags);
-        if (ok) {
-          phase ^= 1u << b;
-          pending &= ~(1u << b);
-        }
-        if (!__syncthreads_and(ok)) {
-          alive = false;
-          break;
-        }
-        const uint8_t* r = rec + b * kMaxRec;
-        if (tid < 128) unpack_scales<KB, VB, kLean>(r, sc, opb, opb + 2 * kHalfB, tid);
-        __syncthreads();
-        unpack_keys<KB, VB, kLean>(r, sc + 4 * 128, opb, opb + 2 * kHalfB, tid);
-        sync_for_mma();
-        if (tid == 0) {
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const uint64_t ah = op_desc(q_hi, k, kHalfQ), al = op_desc(q_lo, k, kHalfQ);
-            const uint64_t bh = op_desc(b_hi, k, kHalfB), bl = op_desc(b_lo, k, kHalfB);
+      };
+      auto issue_qk = [&](bool packed) {  // S = q (hi, lo) x keys (hi, lo: three products, or hi)
+#pragma unroll 1
+        for (int k = 0; k < 8; ++k) {
+          const uint64_t ah = op_desc(q_hi, k, kHalfQ), al = op_desc(q_lo, k, kHalfQ);
+          const uint64_t bh = op_desc(b_hi, k, kHalfB);
+          if (packed) {
             umma_f16(s_tm, ah, bh, kId144, k > 0);
-            umma_f16(s_tm, ah, bl, kId144, 1);
+            umma_f16(s_tm, ah, op_desc(b_lo, k, kHalfB), kId144, 1);
             umma_f16(s_tm, al, bh, kId144, 1);
+          } else {
+            umma_f16(s_tm, ah, bh, kId128, k > 0);
+            umma_f16(s_tm, al, bh, kId128, 1);
           }
-          umma_commit(&bar[2]);
-          mma_pending = true;
         }
-        // the value operand (read by the previous tile's finished PV) fills while
-        // the tensor core computes the scores
-        unpack_values<KB, VB, kLean>(r, opv, tid);
-        ok = wait_mma();
+        umma_commit(&bar[2]);
+        ++n_qk;
+      };
+      auto issue_pv = [&]() {             // D = p' (TMEM, hi and lo) x values
+#pragma unroll 1
+        for (int k = 0; k < 8; ++k) {
+          const uint64_t bv = op_desc(v_op, k, kHalfQ);
+          umma_f16_ts(o_tm, tmem + kColP + 8 * k, bv, kId128, k > 0);
+          umma_f16_ts(o_tm, tmem + kColP + 64 + 8 * k, bv, kId128, 1);
+        }
+        umma_commit(&bar[3]);
+        ++n_pv;
+      };
+      if (n_full > 0) {
+        if (leader) {
+          prefetch(0);
+          prefetch(1);
+        }
+        named_bar(4, kRowThreads + 32);   // keys and values of tile 0
+        tc_fence_after();
+        if (leader) issue_qk(true);
+        for (int t = 0; t < n_full; ++t) {
+          named_bar(3, kRowThreads + 32); // p'(t); record t + 2's buffer is free
+          tc_fence_after();
+          if (leader) {
+            prefetch(t + 2);
+            issue_pv();
+          }
+          if (t + 1 < n_full) {
+            named_bar(4, kRowThreads + 32);   // keys of tile t + 1
+            tc_fence_after();
+            if (leader) issue_qk(true);
+          }
+        }
+      }
+      for (int fb = 0; fb < n_fb; ++fb) {
+        named_bar(4, kRowThreads + 32);
+        tc_fence_after();
+        if (leader) issue_qk(false);
+        named_bar(3, kRowThreads + 32);
+        tc_fence_after();
+        if (leader) issue_pv();
+      }
+      // the last products are done before TMEM is released (bounded waits)
+      if (leader) {
+        if (n_qk) mbar_wait(&bar[2], (n_qk - 1) & 1u, a.flags);
+        if (n_pv) mbar_wait(&bar[3], (n_pv - 1) & 1u, a.flags);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ row warpgroups
+    regs_inc<kRowRegs>();
+    const uint32_t trow = tmem_addr(tmem, 32 * sub, 0);          // this warp's lanes
+    bool ok = true;
+    float acc[64];
+#pragma unroll
+    for (int i = 0; i < 64; ++i) acc[i] = 0.f;
+    float m_run = -INFINITY, l_run = 0.f;
+    uint32_t qk_par = 0, pv_par = 0, rpar = 0;
+    auto wait_qk = [&]() {
+      const bool r = mbar_wait(&bar[2], qk_par, a.flags);
+      if (r) qk_par ^= 1u;
+      tc_fence_after();
+      return r;
+    };
+    auto wait_pv = [&]() {
+      const bool r = mbar_wait(&bar[3], pv_par, a.flags);
+      if (r) pv_par ^= 1u;
+      tc_fence_after();
+      return r;
+    };
+    // softmax of this thread's 64 scores x (log2 domain, -inf = masked) against the
+    // row max over both halves; x becomes p, the accumulator is rescaled
+    auto softmax = [&](float (&x)[64]) {
+      float mx = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < 64; j += 2) mx = fmax3f(mx, x[j], x[j + 1]);
+      xch[hf * 128 + row] = mx;
+      named_bar(1, kRowThreads);
+      mx = fmaxf(mx, xch[(hf ^ 1) * 128 + row]);
+      const float m_new = fmaxf(m_run, mx);
+      float corr = 1.f;
+      if (m_new == -INFINITY) {                   // every token so far masked
+#pragma unroll
+        for (int j = 0; j < 64; ++j) x[j] = 0.f;
+      } else {
+        corr = ex2(m_run - m_new);
+        m_run = m_new;
+        const float2 nm = make_float2(-m_new, -m_new);
+        float2 ls = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int j = 0; j < 64; j += 2) {
+          const float2 e = __fadd2_rn(make_float2(x[j], x[j + 1]), nm);
+          x[j] = ex2(e.x);
+          x[j + 1] = ex2(e.y);
+          ls = __fadd2_rn(ls, make_float2(x[j], x[j + 1]));
+        }
+        l_run = fmaf(l_run, corr, ls.x + ls.y);
+      }
+      const float2 c2 = make_float2(corr, corr);
+#pragma unroll
+      for (int i = 0; i < 64; i += 2) {
+        const float2 v = __fmul2_rn(make_float2(acc[i], acc[i + 1]), c2);
+        acc[i] = v.x;
+        acc[i + 1] = v.y;
+      }
+    };
+
+    // -------------------------------------------------------------- packed tiles
+    if (n_full > 0) {
+      // q_r = H q * log2(e) / sqrt(128), as FWHT(q) * log2(e) / 128, into the A operand
+      {
+        float x[64];
+        const uint16_t* qp = a.q + qrow * kD + 64 * hf;
+#pragma unroll
+        for (int i = 0; i < 64; i += 2) {
+          const float2 f = active ? h2pair(qp + i) : make_float2(0.f, 0.f);
+          x[i] = f.x;
+          x[i + 1] = f.y;
+        }
+        fwht64(x);
+        fwht_pair(x, xb, row, hf);
+#pragma unroll
+        for (int i = 0; i < 64; ++i) x[i] *= kLog2eP / 128.0f;
+        store_split(x, opq, opq + 2 * kHalfQ, row, 64 * hf, kHalfQ);
+      }
+      // rows 129-143 of the keys operand stay zero (row 128 is rewritten per tile; the
+      // exchange above used this space)
+      for (int e = tid; e < 2 * 2 * 15 * 8; e += kRowThreads) {   // [hi/lo][K half][row 129..143][chunk]
+        const int part = e / 240, rem = e % 240, k0 = 64 * (rem / 120), r = 129 + (rem % 120) / 8, c = rem % 8;
+        *reinterpret_cast<uint4*>(opb + part * 2 * kHalfB + swo(r, k0 + 8 * c, kHalfB)) = make_uint4(0, 0, 0, 0);
+      }
+      auto wait_rec = [&](int ti) {
+        if (!valid_tile(ti)) return true;
+        const int b = ti & 1;
+        const bool r = mbar_wait(&bar[b], (rpar >> b) & 1u, a.flags);
+        if (r) rpar ^= 1u << b;
+        return r;
+      };
+      // tile ti's scales (buffer ti & 1) and keys; a masked tile gets zero scales, which
+      // keep its PV term zero
+      auto stage_keys = [&](int ti) {
+        float* sct = scb + (ti & 1) * kScN;
+        if (valid_tile(ti)) {
+          const uint8_t* r = rec + (ti & 1) * kMaxRec;
+          if (tid < 128) unpack_scales<KB, VB, kLean>(r, sct, opb, opb + 2 * kHalfB, tid);
+          named_bar(2, kRowThreads);
+          unpack_keys<KB, VB, kLean>(r, sct + 4 * 128, opb, opb + 2 * kHalfB, tid);
+        } else {
+          for (int e = tid; e < kScN; e += kRowThreads) sct[e] = 0.f;
+          named_bar(2, kRowThreads);
+        }
+      };
+      auto stage_values = [&](int ti) {
+        if (valid_tile(ti)) {
+          unpack_values<KB, VB, kLean>(rec + (ti & 1) * kMaxRec, opv, tid);
+        } else {
+          for (int e = tid; e < static_cast<int>(2 * kHalfQ / 16); e += kRowThreads)
+            reinterpret_cast<uint4*>(opv)[e] = make_uint4(0, 0, 0, 0);
+        }
+      };
+
+      ok = wait_rec(0) && ok;
+      stage_keys(0);
+      stage_values(0);
+      rows_ready(4);
+      for (int t = 0; t < n_full; ++t) {
+        const float* sct = scb + (t & 1) * kScN;
+        ok = wait_qk() && ok;
         float x[64], beta;
         tld_x32(trow + kColS + 64 * hf, x);
         tld_x32(trow + kColS + 64 * hf + 32, x + 32);
@@ -505,9 +607,9 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(PrefillArgs a) {
         tmem_wait_x32(x);
         tmem_wait_x32(x + 32);
         tld_wait1(beta);
-        {
+        if (valid_tile(t)) {
           const float2 b2 = make_float2(beta, beta);
-          const float4* ck = reinterpret_cast<const float4*>(sc + 64 * hf);
+          const float4* ck = reinterpret_cast<const float4*>(sct + 64 * hf);
 #pragma unroll
           for (int j = 0; j < 64; j += 4) {
             const float4 c = ck[j >> 2];
@@ -515,13 +617,16 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(PrefillArgs a) {
             const float2 w = __fmul2_rn(__fadd2_rn(make_float2(x[j + 2], x[j + 3]), b2), make_float2(c.z, c.w));
             x[j] = u.x; x[j + 1] = u.y; x[j + 2] = w.x; x[j + 3] = w.y;
           }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 64; ++j) x[j] = -INFINITY;
         }
         softmax(x);
         float gam;
         {
           float2 g2 = make_float2(0.f, 0.f);
-          const float4* cs = reinterpret_cast<const float4*>(sc + 1 * 128 + 64 * hf);
-          const float4* cz = reinterpret_cast<const float4*>(sc + 2 * 128 + 64 * hf);
+          const float4* cs = reinterpret_cast<const float4*>(sct + 1 * 128 + 64 * hf);
+          const float4* cz = reinterpret_cast<const float4*>(sct + 2 * 128 + 64 * hf);
 #pragma unroll
           for (int j = 0; j < 64; j += 4) {
             const float4 z = cz[j >> 2], c = cs[j >> 2];
@@ -535,31 +640,23 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(PrefillArgs a) {
         }
         tmem_split_store(x, trow + kColP + 32 * hf);
         xch[256 + hf * 128 + row] = gam;
-        tst_wait();
-        sync_for_mma();
-        if (!__syncthreads_and(ok)) {
-          alive = false;
-          break;
-        }
-        if (tid == 0) {
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const uint64_t bv = op_desc(v_op, k, kHalfQ);
-            umma_f16_ts(o_tm, tmem + kColP + 8 * k, bv, kId128, k > 0);
-            umma_f16_ts(o_tm, tmem + kColP + 64 + 8 * k, bv, kId128, 1);
-          }
-          umma_commit(&bar[2]);
-          mma_pending = true;
+        rows_ready(3);                    // p'(t): the issuer starts PV(t)
+        if (t + 1 < n_full) {             // keys of tile t + 1 while PV(t) runs
+          ok = wait_rec(t + 1) && ok;
+          stage_keys(t + 1);
+          rows_ready(4);
+        } else {
+          named_bar(2, kRowThreads);      // gamma's other half is written
         }
         gam += xch[256 + (hf ^ 1) * 128 + row];
-        ok = wait_mma();
+        ok = wait_pv() && ok;
         tld_x32(trow + kColO + 64 * hf, x);
         tld_x32(trow + kColO + 64 * hf + 32, x + 32);
         tmem_wait_x32(x);
         tmem_wait_x32(x + 32);
         {
           const float2 g2 = make_float2(gam, gam);
-          const float4* rv = reinterpret_cast<const float4*>(sc + 3 * 128 + 64 * hf);
+          const float4* rv = reinterpret_cast<const float4*>(sct + 3 * 128 + 64 * hf);
 #pragma unroll
           for (int i = 0; i < 64; i += 4) {
             const float4 v = rv[i >> 2];
@@ -570,144 +667,103 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(PrefillArgs a) {
             acc[i] = u.x; acc[i + 1] = u.y; acc[i + 2] = w.x; acc[i + 3] = w.y;
           }
         }
-        tc_fence_before();
-        if (!__syncthreads_and(ok)) {     // operands and TMEM are rewritten next
-          alive = false;
-          break;
-        }
+        if (t + 1 < n_full) stage_values(t + 1);   // PV(t) has read the values operand
+        named_bar(2, kRowThreads);        // gamma, scales and operands are rewritten next
       }
-      cur = next;
-    }
-    if (!alive) {
-      if (tid == 0) {                     // copies and MMAs in flight finish before the CTA exits
-        for (int b = 0; b < 2; ++b)
-          if ((pending >> b) & 1u) mbar_wait(&bar[b], (phase >> b) & 1u, a.flags);
-        if (mma_pending) mbar_wait(&bar[2], mma_parity, a.flags);
-      }
-      tc_fence_before();
-      __syncthreads();
-      tc_fence_after();
-      if (warp == 0) tmem_dealloc(tmem, 512);
-      return;
-    }
-    // back to the input domain: acc_u = H acc_r = FWHT(acc_r) / sqrt(128)
-    fwht64(acc);
-    fwht_pair(acc, xb, row, hf);
+      // back to the input domain: acc_u = H acc_r = FWHT(acc_r) / sqrt(128)
+      fwht64(acc);
+      fwht_pair(acc, xb, row, hf);
 #pragma unroll
-    for (int i = 0; i < 64; ++i) acc[i] *= kInvSqrt128;
+      for (int i = 0; i < 64; ++i) acc[i] *= kInvSqrt128;
+    }
+
+    // -------------------------------------------------------------- fresh tokens
+    // q * log2(e) / sqrt(128), unrotated, into the A operand (the packed pass is done)
+    {
+      float x[64];
+      const uint16_t* qp = a.q + qrow * kD + 64 * hf;
+#pragma unroll
+      for (int i = 0; i < 64; i += 2) {
+        const float2 f = active ? h2pair(qp + i) : make_float2(0.f, 0.f);
+        x[i] = f.x * (kLog2eP * kInvSqrt128);
+        x[i + 1] = f.y * (kLog2eP * kInvSqrt128);
+      }
+      store_split(x, opq, opq + 2 * kHalfQ, row, 64 * hf, kHalfQ);
+    }
+    // row `row` attends f <= n_ws + p
+    const int lim = min(n_ws + p, n_fresh - 1);
+    auto fresh_src = [&](int f, int which) -> const uint16_t* {
+      if (f < n_ws) return a.ws + (((static_cast<int64_t>(s) * a.hkv + h) * 2 + which) * kB + f) * kD;
+      return (which ? a.v_new : a.k_new) + ((static_cast<int64_t>(t0) + f - n_ws) * a.hkv + h) * kD;
+    };
+    for (int fb = 0; fb < n_fb; ++fb) {
+      // keys [token][channel] into the B operand of QK^T (hi part only: fp16 exact)
+      for (int e = tid; e < 128 * 16; e += kRowThreads) {
+        const int jj = e >> 4, c8 = e & 15, f = fb * kB + jj;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (f < n_fresh) v = *reinterpret_cast<const uint4*>(fresh_src(f, 0) + 8 * c8);
+        *reinterpret_cast<uint4*>(opb + swo(jj, 8 * c8, kHalfB)) = v;
+      }
+      // values transposed to [channel][token]: lane = token, so each 2-byte store of a
+      // warp fills 64 contiguous bytes of one channel row
+      for (int e = tid; e < 128 * 16; e += kRowThreads) {
+        const int c8 = e >> 7, jj = e & 127, f = fb * kB + jj;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (f < n_fresh) v = *reinterpret_cast<const uint4*>(fresh_src(f, 1) + 8 * c8);
+        const uint16_t* u = reinterpret_cast<const uint16_t*>(&v);
+#pragma unroll
+        for (int e2 = 0; e2 < 8; ++e2) *reinterpret_cast<uint16_t*>(opv + swo(8 * c8 + e2, jj, kHalfQ)) = u[e2];
+      }
+      rows_ready(4);
+      ok = wait_qk() && ok;
+      float x[64];
+      tld_x32(trow + kColS + 64 * hf, x);
+      tld_x32(trow + kColS + 64 * hf + 32, x + 32);
+      tmem_wait_x32(x);
+      tmem_wait_x32(x + 32);
+#pragma unroll
+      for (int j = 0; j < 64; ++j)
+        if (fb * kB + 64 * hf + j > lim) x[j] = -INFINITY;
+      softmax(x);
+      tmem_split_store(x, trow + kColP + 32 * hf);
+      rows_ready(3);
+      ok = wait_pv() && ok;
+      tld_x32(trow + kColO + 64 * hf, x);
+      tld_x32(trow + kColO + 64 * hf + 32, x + 32);
+      tmem_wait_x32(x);
+      tmem_wait_x32(x + 32);
+#pragma unroll
+      for (int i = 0; i < 64; i += 2) {
+        const float2 u = __fadd2_rn(make_float2(acc[i], acc[i + 1]), make_float2(x[i], x[i + 1]));
+        acc[i] = u.x;
+        acc[i + 1] = u.y;
+      }
+      named_bar(2, kRowThreads);          // the operands are rewritten next
+    }
+    // output: acc / l over both halves (nothing is written after a timeout)
+    xch[512 + hf * 128 + row] = l_run;
+    ok = named_bar_and(2, kRowThreads, ok);
+    if (ok && active) {
+      const float l = xch[512 + row] + xch[512 + 128 + row];
+      const float inv_l = l > 0.f ? 1.0f / l : 0.f;
+      uint16_t* orow = a.out + qrow * kD + 64 * hf;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          w[e] = static_cast<uint32_t>(f2h_bits(acc[8 * q + 2 * e] * inv_l)) |
+                 (static_cast<uint32_t>(f2h_bits(acc[8 * q + 2 * e + 1] * inv_l)) << 16);
+        *reinterpret_cast<uint4*>(orow + 8 * q) = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+    }
   }
 
-  // ---------------------------------------------------------------- fresh tokens
-  // q * log2(e) / sqrt(128), unrotated, into the A operand (the packed pass is done)
-  {
-    float x[64];
-    const uint16_t* qp = a.q + qrow * kD + 64 * hf;
-#pragma unroll
-    for (int i = 0; i < 64; i += 2) {
-      const float2 f = active ? h2pair(qp + i) : make_float2(0.f, 0.f);
-      x[i] = f.x * (kLog2eP * kInvSqrt128);
-      x[i + 1] = f.y * (kLog2eP * kInvSqrt128);
-    }
-    store_split(x, opq, opq + 2 * kHalfQ, row, 64 * hf, kHalfQ);
-  }
-  // fresh token f: workspace token f (f < n_ws) or chunk token f - n_ws; row `row`
-  // attends f <= n_ws + p; this CTA's last token attends f < n_fresh
-  const int p_last = min(chunk - 1, static_cast<int>(blockIdx.x) * kPTokens + kPTokens - 1);
-  const int n_fresh = n_ws + p_last + 1;
-  const int lim = min(n_ws + p, n_fresh - 1);
-  auto fresh_src = [&](int f, int which) -> const uint16_t* {
-    if (f < n_ws) return a.ws + (((static_cast<int64_t>(s) * a.hkv + h) * 2 + which) * kB + f) * kD;
-    return (which ? a.v_new : a.k_new) + ((static_cast<int64_t>(t0) + f - n_ws) * a.hkv + h) * kD;
-  };
-  bool ok = true;
-  for (int fb = 0; fb * kB < n_fresh && ok; ++fb) {
-    // keys [token][channel] into the B operand of QK^T (hi part only: fp16 exact)
-    for (int e = tid; e < 128 * 16; e += kPThreads) {
-      const int jj = e >> 4, c8 = e & 15, f = fb * kB + jj;
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (f < n_fresh) v = *reinterpret_cast<const uint4*>(fresh_src(f, 0) + 8 * c8);
-      *reinterpret_cast<uint4*>(opb + swo(jj, 8 * c8, kHalfB)) = v;
-    }
-    // values transposed to [channel][token]: lane = token, so each 2-byte store of a
-    // warp fills 64 contiguous bytes of one channel row
-    for (int e = tid; e < 128 * 16; e += kPThreads) {
-      const int c8 = e >> 7, jj = e & 127, f = fb * kB + jj;
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (f < n_fresh) v = *reinterpret_cast<const uint4*>(fresh_src(f, 1) + 8 * c8);
-      const uint16_t* u = reinterpret_cast<const uint16_t*>(&v);
-#pragma unroll
-      for (int e2 = 0; e2 < 8; ++e2) *reinterpret_cast<uint16_t*>(opv + swo(8 * c8 + e2, jj, kHalfQ)) = u[e2];
-    }
-    sync_for_mma();
-    if (tid == 0) {
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const uint64_t bk = op_desc(b_hi, k, kHalfB);
-        umma_f16(s_tm, op_desc(q_hi, k, kHalfQ), bk, kId128, k > 0);
-        umma_f16(s_tm, op_desc(q_lo, k, kHalfQ), bk, kId128, 1);
-      }
-      umma_commit(&bar[2]);
-      mma_pending = true;
-    }
-    ok = wait_mma();
-    float x[64];
-    tld_x32(trow + kColS + 64 * hf, x);
-    tld_x32(trow + kColS + 64 * hf + 32, x + 32);
-    tmem_wait_x32(x);
-    tmem_wait_x32(x + 32);
-#pragma unroll
-    for (int j = 0; j < 64; ++j)
-      if (fb * kB + 64 * hf + j > lim) x[j] = -INFINITY;
-    softmax(x);
-    tmem_split_store(x, trow + kColP + 32 * hf);
-    tst_wait();
-    sync_for_mma();
-    if (!__syncthreads_and(ok)) break;
-    if (tid == 0) {
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const uint64_t bv = op_desc(v_op, k, kHalfQ);
-        umma_f16_ts(o_tm, tmem + kColP + 8 * k, bv, kId128, k > 0);
-        umma_f16_ts(o_tm, tmem + kColP + 64 + 8 * k, bv, kId128, 1);
-      }
-      umma_commit(&bar[2]);
-      mma_pending = true;
-    }
-    ok = wait_mma();
-    tld_x32(trow + kColO + 64 * hf, x);
-    tld_x32(trow + kColO + 64 * hf + 32, x + 32);
-    tmem_wait_x32(x);
-    tmem_wait_x32(x + 32);
-#pragma unroll
-    for (int i = 0; i < 64; i += 2) {
-      const float2 u = __fadd2_rn(make_float2(acc[i], acc[i + 1]), make_float2(x[i], x[i + 1]));
-      acc[i] = u.x;
-      acc[i + 1] = u.y;
-    }
-    tc_fence_before();
-    ok = __syncthreads_and(ok);
-  }
-
-  // output: acc / l over both halves
-  xch[512 + hf * 128 + row] = l_run;
-  if (tid == 0 && mma_pending) mbar_wait(&bar[2], mma_parity, a.flags);   // only after a timeout
+  // ---------------------------------------------------------------- end (all warps)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   if (warp == 0) tmem_dealloc(tmem, 512);
-  if (!ok || !active) return;
-  const float l = l_run + xch[512 + (hf ^ 1) * 128 + row];
-  const float inv_l = l > 0.f ? 1.0f / l : 0.f;
-  uint16_t* orow = a.out + qrow * kD + 64 * hf;
-#pragma unroll
-  for (int q = 0; q < 8; ++q) {
-    uint32_t w[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e)
-      w[e] = static_cast<uint32_t>(f2h_bits(acc[8 * q + 2 * e] * inv_l)) |
-             (static_cast<uint32_t>(f2h_bits(acc[8 * q + 2 * e + 1] * inv_l)) << 16);
-    *reinterpret_cast<uint4*>(orow + 8 * q) = make_uint4(w[0], w[1], w[2], w[3]);
-  }
 }
 
 template <int KB, int VB, bool kLean>
