@@ -1,0 +1,38 @@
+"""bench.py prints one JSON line with the keys its consumers read: the profiling
+case of the headline workload and the prefill-attention case, each run briefly."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+pytestmark = pytest.mark.gpu
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _run(*args):
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), *args], cwd=ROOT, capture_output=True,
+                       text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1, r.stdout[-2000:]
+    return json.loads(lines[0])
+
+
+def test_bench_small_case_line():
+    d = _run("--case", "small", "--steps", "2", "--warmup", "3", "--no-cpu-baseline")
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "dtype", "data", "config", "roofline", "e2e", "gpu_launches", "clocks"):
+        assert key in d, key
+    assert d["n_gpus"] == 1 and d["steps"] == 2 and d["warmup"] == 3
+    assert d["value"] > 0 and d["ms_per_step"] > 0 and d["gpu_launches"] > 0
+    assert d["roofline"]["bound"] in ("alu", "hbm", "tensor") and 0 < d["roofline"]["frac"] < 2
+    assert d["e2e"]["value"] > 0 and d["e2e"]["h2d_bytes_per_step"] > 0
+
+
+def test_bench_prefill_attention_line():
+    d = _run("--case", "prefill_attn", "--steps", "2", "--warmup", "3")
+    assert d["metric"] == "chunked_prefill_attention_tflops" and d["unit"] == "TFLOP/s"
+    assert d["value"] > 0 and d["ms_per_call"] > 0 and d["prefill_tokens_per_s"] > 0
