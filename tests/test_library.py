@@ -137,6 +137,29 @@ def test_serve_step_rejects_bad_arguments(kv):
     assert sv(A, A, A, A, B, A, 4, A, A, A, A, need, ctypes.byref(m0), None) == 1
 
 
+def test_prefill_rejects_bad_arguments(kv):
+    """kvarn_prefill_attention: sequence count and chunk bound are checked, empty work
+    returns before any pointer is looked at, pointers must be non-NULL and 16-byte
+    aligned (cache and block tables only when the meta allows cached blocks, the
+    workspace only when given)."""
+    m = kv.make_meta(8, 64, 1024, max_blocks_per_seq=128)
+    pf = _raw(kv, "kvarn_prefill_attention")
+    mm = ctypes.byref(m)
+    #        q  kn vn cu lens  n  max  bt cache ws  out meta stream
+    assert pf(A, A, A, A, A, -1, 16, A, A, A, A, mm, None) == 1           # n_seqs < 0
+    assert pf(A, A, A, A, A, 65536, 16, A, A, A, A, mm, None) == 1        # n_seqs > 65535
+    assert pf(A, A, A, A, A, 4, -1, A, A, A, A, mm, None) == 1            # max_chunk < 0
+    assert pf(None, None, None, None, None, 0, 16, None, None, None, None, mm, None) == 0   # no sequences
+    assert pf(None, None, None, None, None, 4, 0, None, None, None, None, mm, None) == 0    # empty chunks
+    assert pf(None, A, A, A, A, 4, 16, A, A, A, A, mm, None) == 1         # NULL q
+    assert pf(A, MIS, A, A, A, 4, 16, A, A, A, A, mm, None) == 3          # misaligned k_new
+    assert pf(A, A, A, A, A, 4, 16, A, None, A, A, mm, None) == 1         # NULL cache with cached blocks
+    assert pf(A, A, A, A, A, 4, 16, A, A, MIS, A, mm, None) == 3          # misaligned workspace
+    assert pf(A, A, A, A, A, 4, 16, A, A, A, None, mm, None) == 1         # NULL out
+    assert pf(A, A, A, A, A, 4, 16, A, A, A, A, None, None) == 1          # NULL meta
+    assert kv._lib.kvarn_last_error().decode()
+
+
 def test_presets_are_accepted_and_sized(kv):
     for preset, (kb, vb), rec in (("k4v2", (4, 2), 14336), ("k4v4", (4, 4), 18432), ("k2v2", (2, 2), 10240),
                                   ("k4v2l", (4, 2), 13824)):
