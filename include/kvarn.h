@@ -264,7 +264,8 @@ KVARN_API kvarn_status kvarn_serve_step(const uint16_t* q, const uint16_t* k_new
  * callers that cannot allocate device memory: e.g. a serving engine whose free
  * device memory is all pre-reserved for its KV-cache pool and handed out only by
  * its own allocator, or a plain-C host with no device allocator for temporaries.
- * Same arguments and results as kvarn_decode_attention minus scratch: the scratch
+ * Same arguments, argument checks (every preset, KVARN_EALIGN for a misaligned
+ * pointer) and results as kvarn_decode_attention minus scratch: the scratch
  * is a fixed 16 MiB array of device memory inside the library (held by every GPU
  * that loads the library until the process exits), shared by all calls on a device.
  *   - Sizes: returns KVARN_ESCRATCH, without launching, when the scratch needed for

@@ -306,4 +306,8 @@ kvarn_status set_error(kvarn_status st, const char* msg) {
 
 void clear_error() { g_err[0] = 0; }
 
+kvarn_status check_meta_status(const kvarn_meta* meta) { return check_meta(meta); }
+
+kvarn_status check_device_ptr(const void* p, const char* name) { return need_ptr(p, name); }
+
 }  // namespace kvarn

@@ -50,8 +50,6 @@ kvarn_status static_scratch(void** out) {
   return KVARN_OK;
 }
 
-bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
 }  // namespace
 
 extern "C" {
@@ -61,26 +59,22 @@ KVARN_API kvarn_status kvarn_decode_attention_static(const uint16_t* q, const ui
                                                      const int32_t* seq_lens, int32_t n_seqs, uint16_t* out,
                                                      const kvarn_meta* meta, void* stream) {
   kvarn::clear_error();
-  if (meta == nullptr) return kvarn::set_error(KVARN_EINVAL, "meta is NULL");
-  if (meta->head_dim != KVARN_HEAD_DIM || meta->block_size != KVARN_BLOCK_SIZE || meta->k_bits != 4 ||
-      meta->v_bits != 2)
-    return kvarn::set_error(KVARN_EUNSUPPORTED, "only the kvarn_k4v2_g128 preset (head_dim 128, block 128) is supported");
-  if (meta->num_kv_heads < 1 || meta->num_q_heads < meta->num_kv_heads ||
-      meta->num_q_heads % meta->num_kv_heads != 0 || meta->num_blocks < 0 || meta->max_blocks_per_seq < 0 ||
-      meta->layout != 0 || meta->n_iters < 1 || meta->n_iters > 16 || !(meta->eps > 0.0f) || !(meta->eps < 1.0f))
-    return kvarn::set_error(KVARN_EINVAL, "invalid kvarn_meta");
-  if (meta->num_q_heads / meta->num_kv_heads > KVARN_MAX_GQA_GROUP)
-    return kvarn::set_error(KVARN_EUNSUPPORTED, "GQA group (Hq/Hkv) must be <= 8");
+  // the same checks as kvarn_decode_attention: every preset of kvarn.h is served
+  kvarn_status st = kvarn::check_meta_status(meta);
+  if (st != KVARN_OK) return st;
   if (n_seqs < 0 || n_seqs > 65535) return kvarn::set_error(KVARN_EINVAL, "n_seqs must be in 0..65535");
   if (n_seqs == 0) return KVARN_OK;
-  const void* need_aligned[] = {q, seq_lens, out};
-  for (const void* p : need_aligned)
-    if (p == nullptr || !aligned16(p)) return kvarn::set_error(KVARN_EINVAL, "q, seq_lens and out must be non-NULL, 16-byte aligned");
-  if (meta->max_blocks_per_seq > 0 && (cache == nullptr || !aligned16(cache) || block_tables == nullptr ||
-                                       !aligned16(block_tables)))
-    return kvarn::set_error(KVARN_EINVAL, "cache and block_tables must be non-NULL, 16-byte aligned");
-  if (workspace != nullptr && !aligned16(workspace))
-    return kvarn::set_error(KVARN_EALIGN, "workspace is not 16-byte aligned");
+  const struct {
+    const void* p;
+    const char* name;
+  } need_aligned[] = {{q, "q"}, {seq_lens, "seq_lens"}, {out, "out"}};
+  for (const auto& a : need_aligned)
+    if ((st = kvarn::check_device_ptr(a.p, a.name)) != KVARN_OK) return st;
+  if (meta->max_blocks_per_seq > 0) {
+    if ((st = kvarn::check_device_ptr(cache, "cache")) != KVARN_OK) return st;
+    if ((st = kvarn::check_device_ptr(block_tables, "block_tables")) != KVARN_OK) return st;
+  }
+  if (workspace != nullptr && (st = kvarn::check_device_ptr(workspace, "workspace")) != KVARN_OK) return st;
 
   const size_t need = kvarn::decode_scratch_bytes_for_ctas(n_seqs, meta->num_kv_heads, kvarn::decode_num_ctas());
   if (need > kStaticScratchBytes)
@@ -88,14 +82,15 @@ KVARN_API kvarn_status kvarn_decode_attention_static(const uint16_t* q, const ui
                             "kvarn_decode_attention_static: n_seqs * num_kv_heads exceeds the 16 MiB built-in "
                             "scratch; use kvarn_decode_attention with a caller buffer");
   void* scratch = nullptr;
-  kvarn_status st = static_scratch(&scratch);
+  st = static_scratch(&scratch);
   if (st != KVARN_OK) return st;
   unsigned* flags = nullptr;
   if (kvarn::flags_device_ptr(&flags) != cudaSuccess)
     return kvarn::set_error(KVARN_ECUDA, "kvarn_decode_attention_static: device flag word unavailable");
   const cudaError_t e = kvarn::launch_decode(q, cache, workspace, block_tables, seq_lens, n_seqs, meta->num_kv_heads,
                                              meta->num_q_heads / meta->num_kv_heads, meta->max_blocks_per_seq,
-                                             meta->num_blocks, 4, 2, false, out, scratch, flags,
+                                             meta->num_blocks, meta->k_bits, meta->v_bits,
+                                             meta->layout == KVARN_LAYOUT_LEAN, out, scratch, flags,
                                              static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return kvarn::set_error(KVARN_ECUDA, cudaGetErrorString(e));
   return KVARN_OK;

@@ -62,5 +62,11 @@ int decode_num_ctas();
 cudaError_t flags_device_ptr(unsigned** out);
 kvarn_status set_error(kvarn_status st, const char* msg);
 void clear_error();
+// The entry points' shared argument checks: a kvarn_meta that names a preset and
+// valid sizes (KVARN_EINVAL / KVARN_EUNSUPPORTED), and a device pointer that is
+// non-NULL (KVARN_EINVAL) and 16-byte aligned (KVARN_EALIGN). Both set the
+// thread's error message.
+kvarn_status check_meta_status(const kvarn_meta* meta);
+kvarn_status check_device_ptr(const void* p, const char* name);
 
 }  // namespace kvarn

@@ -178,3 +178,25 @@ def test_lean_layout_only_with_k4v2(kv):
     assert kv.meta_record_bytes(meta) == 0
     st = _raw(kv, "kvarn_quantize_tiles")(None, None, None, 0, None, ctypes.byref(meta), None)
     assert st == 2                      # KVARN_EUNSUPPORTED
+
+
+def test_static_decode_checks_like_the_scratch_decode(kv):
+    """kvarn_decode_attention_static takes the same argument checks as
+    kvarn_decode_attention: a misaligned pointer is KVARN_EALIGN, a NULL one
+    KVARN_EINVAL, and every preset passes the meta check (these calls return
+    before touching a device)."""
+    st = _raw(kv, "kvarn_decode_attention_static")
+    for preset in ("k4v2", "k4v4", "k2v2", "k4v2l"):
+        m = kv.make_meta(8, 64, 1024, max_blocks_per_seq=128, preset=preset)
+        mm = ctypes.byref(m)
+        #          q    cache ws  bt  lens n  out  meta stream
+        assert st(MIS, A, None, A, A, 4, A, mm, None) == 3, preset        # misaligned q
+        assert st(A, A, None, A, MIS, 4, A, mm, None) == 3, preset        # misaligned seq_lens
+        assert st(A, A, None, A, A, 4, MIS, mm, None) == 3, preset        # misaligned out
+        assert st(A, MIS, None, A, A, 4, A, mm, None) == 3, preset        # misaligned cache
+        assert st(A, A, MIS, A, A, 4, A, mm, None) == 3, preset           # misaligned workspace
+        assert st(None, A, None, A, A, 4, A, mm, None) == 1, preset       # NULL q
+        assert st(A, A, None, A, A, 0, A, mm, None) == 0, preset          # nothing to do
+    bad = kv.make_meta(8, 64, 1024, max_blocks_per_seq=128)
+    bad.k_bits = 3
+    assert st(A, A, None, A, A, 4, A, ctypes.byref(bad), None) == 2     # not a preset

@@ -26,7 +26,7 @@ def env():
     return kv, torch
 
 
-def _case(torch, n_seqs, hkv, group, seed):
+def _case(torch, n_seqs, hkv, group, seed, preset="k4v2"):
     """Ragged lengths with partial tiles, random valid records, fp16 workspace."""
     rng = np.random.default_rng(seed)
     lens = rng.integers(1, 40 * 128, n_seqs).astype(np.int32)
@@ -34,18 +34,20 @@ def _case(torch, n_seqs, hkv, group, seed):
     max_blocks = int(lens.max()) // 128 + 1
     num_blocks = n_seqs * max_blocks
     bt = synth.block_tables(n_seqs, max_blocks, num_blocks, seed)
-    recs = synth.random_records(num_blocks * hkv, seed, o.RECORD_BYTES, 12288).reshape(num_blocks, hkv, -1)
+    lay = o.LAYOUTS[preset]
+    recs = synth.random_records(num_blocks * hkv, seed, lay.record_bytes, lay.k_code_bytes + lay.v_code_bytes)
+    recs = recs.reshape(num_blocks, hkv, -1)
     ws = synth.workspace_tokens(n_seqs, hkv, seed)
     q = synth.queries(n_seqs, hkv * group, seed)
     f16 = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.float16).cuda()
     return dict(q=f16(q), cache=torch.from_numpy(recs).cuda(), ws=f16(ws), bt=torch.from_numpy(bt).cuda(),
-                lens=torch.from_numpy(lens).cuda(), num_blocks=num_blocks, max_blocks=max_blocks)
+                lens=torch.from_numpy(lens).cuda(), num_blocks=num_blocks, max_blocks=max_blocks, preset=preset)
 
 
 def _both(env, c, hkv, group):
     kv, torch = env
     n_seqs = c["q"].shape[0]
-    meta = kv.make_meta(hkv, hkv * group, c["num_blocks"], max_blocks_per_seq=c["max_blocks"])
+    meta = kv.make_meta(hkv, hkv * group, c["num_blocks"], max_blocks_per_seq=c["max_blocks"], preset=c["preset"])
     out_ref = torch.empty_like(c["q"])
     scratch = torch.empty(kv.decode_scratch_bytes(meta, n_seqs), dtype=torch.uint8, device="cuda")
     kv.kvarn_decode_attention(c["q"], c["cache"], c["ws"], c["bt"], c["lens"], out_ref, scratch, meta)
@@ -68,6 +70,18 @@ def test_static_scratch_matches_caller_scratch_twice(env):
     got, want = _both(env, c2, 2, 4)
     assert np.isfinite(got).all()
     assert_decode_close(got, want, "second call")
+
+
+@pytest.mark.parametrize("preset", ["k4v4", "k2v2", "k4v2l"])
+def test_static_scratch_serves_every_preset(env, preset):
+    """The other presets go through the same kernels as with a caller buffer: two
+    calls in a row match kvarn_decode_attention."""
+    kv, torch = env
+    for seed, (n_seqs, hkv, group) in ((61, (10, 2, 8)), (62, (5, 4, 2))):
+        c = _case(torch, n_seqs, hkv, group, seed=seed, preset=preset)
+        got, want = _both(env, c, hkv, group)
+        assert np.isfinite(got).all()
+        assert_decode_close(got, want, f"{preset} seed {seed}")
 
 
 def test_static_scratch_rejects_sizes_beyond_its_limit(env):
