@@ -239,7 +239,15 @@ KVARN_API kvarn_status kvarn_decode_attention(const uint16_t* q, const uint8_t* 
  * results as those two calls in order. A cooperative launch of one CTA per SM
  * whose phases (append and tile quantization; attention over the tiles; merge
  * with the workspace tokens) meet at grid-wide barriers; every wait is bounded
- * and reports KVARN_FLAG_WAIT_TIMEOUT instead of hanging. Capturable in a CUDA graph.
+ * and reports KVARN_FLAG_WAIT_TIMEOUT instead of hanging (a CTA whose barrier wait
+ * runs out stops there, so the outputs of such a call are not valid). The barrier
+ * words are the last 256 bytes of `scratch`, zeroed on `stream` before each launch:
+ * calls that overlap on the GPU must not share a scratch buffer (nor, as for the
+ * two calls it fuses, a workspace or cache region). Capturable in a CUDA graph.
+ * Measured on GB300 this one launch is slower than kvarn_append_decode followed by
+ * kvarn_decode_attention (its merge phase runs at the split phase's 8 warps per SM),
+ * so those two calls, captured in a CUDA graph, are the recommended serving step;
+ * this entry point is kept for callers that want a single launch.
  *   q             fp16 [n_seqs][num_q_heads][128], the new query of each sequence.
  *   k_new, v_new  fp16 [n_seqs][num_kv_heads][128].
  *   seq_lens      int32 [n_seqs], lengths before the append, >= 0.
@@ -297,7 +305,9 @@ KVARN_API kvarn_status kvarn_decode_attention_static(const uint16_t* q, const ui
  *   cu_tokens     int32 [n_seqs + 1], non-decreasing, cu_tokens[0] = 0.
  *   seq_lens      int32 [n_seqs], cached tokens before each chunk.
  *   n_seqs        0..65535. max_chunk: an upper bound of every chunk length
- *                 (sets the grid; tokens of a longer chunk are not computed).
+ *                 (sets the grid; the tokens of a longer chunk beyond max_chunk
+ *                 rounded up to 16 are not computed, their out rows are left as
+ *                 they were, and KVARN_FLAG_BAD_LENGTH is raised).
  *   workspace     fp16 workspace or NULL (then L0 % 128 tokens are not attended
  *                 and KVARN_FLAG_BAD_LENGTH is raised).
  * One launch; no scratch. Every preset of kvarn_meta is supported.
@@ -307,6 +317,30 @@ KVARN_API kvarn_status kvarn_prefill_attention(const uint16_t* q, const uint16_t
                                      int32_t max_chunk, const int32_t* block_tables, const uint8_t* cache,
                                      const uint16_t* workspace, uint16_t* out, const kvarn_meta* meta,
                                      void* stream);
+
+/*
+ * Self-test of the give-up path of the library's bounded waits (failure
+ * detection): every wait of the kernels on a copy, a tensor-core commit or a grid
+ * barrier gives up after a time limit (2 s in the kernels), raises
+ * KVARN_FLAG_WAIT_TIMEOUT in the device flag word and returns instead of hanging.
+ * This call runs the same device wait code against conditions that never complete,
+ * with a limit of `limit_us` microseconds (1..1000000), so a caller can check on its
+ * own device that a wait that runs out is reported and leaves the device usable:
+ *   which = KVARN_WAIT_MBARRIER: one warp waits on an mbarrier phase that expects
+ *           16 bytes no copy delivers;
+ *   which = KVARN_WAIT_GRID: a cooperative grid of one CTA per SM waits at a grid
+ *           barrier that expects one CTA more than were launched; its barrier
+ *           words are the first 8 bytes of `scratch` (device memory, 16-byte
+ *           aligned, scratch_bytes >= 8; ignored for KVARN_WAIT_MBARRIER).
+ * Nothing is copied or multiplied while the waits run. Asynchronous on `stream`;
+ * read the flag with kvarn_device_flags. The serving step keeps its own barrier
+ * words in its scratch and zeroes them on the stream before each launch, so a
+ * timed-out barrier of one call never affects another.
+ */
+#define KVARN_WAIT_MBARRIER 0
+#define KVARN_WAIT_GRID 1
+KVARN_API kvarn_status kvarn_check_bounded_waits(int32_t which, uint32_t limit_us, void* scratch,
+                                                 size_t scratch_bytes, void* stream);
 
 /* Copies the device flag word of the current device to *flags (host pointer)
  * after synchronising `stream`, then clears it. */

@@ -20,6 +20,7 @@ BLOCK_SIZE = 128
 
 KVARN_OK, KVARN_EINVAL, KVARN_EUNSUPPORTED, KVARN_EALIGN, KVARN_ESCRATCH, KVARN_ECUDA = range(6)
 FLAG_BAD_SLOTS, FLAG_BAD_BLOCK, FLAG_BAD_LENGTH, FLAG_WAIT_TIMEOUT = 0x1, 0x2, 0x4, 0x8
+KVARN_WAIT_MBARRIER, KVARN_WAIT_GRID = 0, 1
 
 # exported entry points and their C signatures (include/kvarn.h)
 _SIGS = {
@@ -47,6 +48,8 @@ _SIGS = {
                                                ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p,
                                                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                                ctypes.c_void_p]),
+    "kvarn_check_bounded_waits": (ctypes.c_int, [ctypes.c_int32, ctypes.c_uint32, ctypes.c_void_p, ctypes.c_size_t,
+                                                 ctypes.c_void_p]),
     "kvarn_device_flags": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32), ctypes.c_void_p]),
     "kvarn_last_error": (ctypes.c_char_p, []),
 }
@@ -239,6 +242,16 @@ def kvarn_prefill_attention(q, k_new, v_new, cu_tokens, seq_lens, max_chunk: int
                                         _ptr(block_tables, "block_tables", torch.int32),
                                         _ptr(cache, "cache", torch.uint8), _ptr(workspace, "workspace", torch.float16),
                                         _ptr(out, "out", torch.float16), ctypes.byref(meta), _stream(stream)))
+
+
+def kvarn_check_bounded_waits(which: int, limit_us: int, scratch=None, stream=None):
+    """Runs the library's bounded-wait code against a wait that never completes
+    (KVARN_WAIT_MBARRIER or KVARN_WAIT_GRID), giving up after limit_us; the
+    timeout shows as FLAG_WAIT_TIMEOUT in kvarn_device_flags(). scratch: a device
+    buffer of at least 8 bytes for the grid barrier's words."""
+    nbytes = 0 if scratch is None else scratch.numel() * scratch.element_size()
+    _check(_lib.kvarn_check_bounded_waits(int(which), int(limit_us), _ptr(scratch, "scratch"), nbytes,
+                                          _stream(stream)))
 
 
 def kvarn_device_flags(stream=None) -> int:

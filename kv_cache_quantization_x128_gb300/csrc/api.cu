@@ -253,6 +253,24 @@ kvarn_status kvarn_prefill_attention(const uint16_t* q, const uint16_t* k_new, c
                      "kvarn_prefill_attention");
 }
 
+kvarn_status kvarn_check_bounded_waits(int32_t which, uint32_t limit_us, void* scratch, size_t scratch_bytes,
+                                       void* stream) {
+  g_err[0] = 0;
+  if (which != KVARN_WAIT_MBARRIER && which != KVARN_WAIT_GRID)
+    return fail(KVARN_EINVAL, "which must be KVARN_WAIT_MBARRIER or KVARN_WAIT_GRID (got %lld)", (long long)which);
+  if (limit_us < 1 || limit_us > 1000000)
+    return fail(KVARN_EINVAL, "limit_us must be in 1..1000000 (got %llu)", (unsigned long long)limit_us);
+  if (which == KVARN_WAIT_GRID) {
+    KV_TRY(need_ptr(scratch, "scratch"));
+    if (scratch_bytes < 8) return fail(KVARN_ESCRATCH, "scratch too small: need 8 bytes");
+  }
+  unsigned* fl = nullptr;
+  KV_TRY(flags_ptr(&fl));
+  return cuda_status(kvarn::launch_wait_selftest(which, 1000ull * limit_us, scratch, fl,
+                                                 static_cast<cudaStream_t>(stream)),
+                     "kvarn_check_bounded_waits");
+}
+
 kvarn_status kvarn_device_flags(uint32_t* flags, void* stream) {
   g_err[0] = 0;
   if (flags == nullptr) return fail(KVARN_EINVAL, "flags is NULL");

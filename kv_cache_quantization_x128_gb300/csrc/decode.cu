@@ -77,7 +77,7 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(DecodeArgs a, const u
 size_t decode_part_bytes(int n_seqs, int hkv, int max_blocks) {
   (void)max_blocks;
   const size_t records = static_cast<size_t>(kMaxCtas) * kMaxWarps + static_cast<size_t>(n_seqs) * hkv;
-  return prefix_bytes(n_seqs) + kRangeBytes + records * kRecFloats * sizeof(float);
+  return prefix_bytes(n_seqs) + kRangeBytes + records * kRecFloats * sizeof(float) + kServeBarrierBytes;
 }
 
 size_t decode_scratch_bytes_for_ctas(int n_seqs, int hkv, int n_ctas) {

@@ -74,8 +74,10 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                : "memory");
 }
 // Bounded wait for the phase with parity `parity` to complete. Returns false (and
-// raises KVARN_FLAG_WAIT_TIMEOUT) if it did not complete within kWaitNs.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned int* flags) {
+// raises KVARN_FLAG_WAIT_TIMEOUT) if it did not complete within `limit_ns` of the
+// global timer (kWaitNs unless a self-test asks for less).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned int* flags,
+                                          unsigned long long limit_ns = kWaitNs) {
   const uint32_t addr = smem_u32(bar);
   unsigned long long t0 = 0;
   for (unsigned int n = 0;; ++n) {
@@ -90,7 +92,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsign
     if (done) return true;
     if (n == 0) {
       t0 = global_ns();
-    } else if ((n & 63) == 0 && global_ns() - t0 > kWaitNs) {
+    } else if ((n & 63) == 0 && global_ns() - t0 > limit_ns) {
       raise_flag(flags, KVARN_FLAG_WAIT_TIMEOUT);
       return false;
     }

@@ -51,8 +51,15 @@ cudaError_t launch_serve_step(const uint16_t* q, const uint16_t* k_new, const ui
                               uint16_t* ws, uint8_t* cache, int n_seqs, int hkv, int group, int max_blocks,
                               int64_t num_blocks, int k_bits, int v_bits, bool lean, int n_iters, float eps,
                               uint16_t* out, void* scratch, unsigned* flags, cudaStream_t stream);
-// Device scratch of launch_decode: tile prefix per sequence + partial records.
+// Device scratch of launch_decode: tile prefix per sequence + partial records, and
+// at its end kServeBarrierBytes for the serving step's grid barrier words.
+constexpr size_t kServeBarrierBytes = 256;
 size_t decode_part_bytes(int n_seqs, int hkv, int max_blocks);
+size_t serve_barrier_offset(int n_seqs, int hkv, int max_blocks);
+unsigned* serve_barrier_words(void* scratch, int n_seqs, int hkv, int max_blocks);
+// Bounded-wait self-test (serve.cu): which = 0 mbarrier wait, 1 grid barrier.
+cudaError_t launch_wait_selftest(int which, unsigned long long limit_ns, void* barrier_words, unsigned* flags,
+                                 cudaStream_t stream);
 // Scratch launch_decode touches when the split kernel runs `n_ctas` CTAs (the
 // device's SM count, at most 1024).
 size_t decode_scratch_bytes_for_ctas(int n_seqs, int hkv, int n_ctas);

@@ -353,6 +353,10 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(PrefillArgs a) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int h = blockIdx.y, s = blockIdx.z;
   const int t0 = a.cu[s], chunk = a.cu[s + 1] - t0;
+  // a chunk longer than the grid covers (max_chunk too small): its tail tokens get
+  // no CTA and their output rows are not written, so the last CTA of the row says so
+  if (tid == 0 && h == 0 && blockIdx.x == gridDim.x - 1 && chunk > static_cast<int>(gridDim.x) * kPTokens)
+    raise_flag(a.flags, KVARN_FLAG_BAD_LENGTH);
   if (static_cast<int>(blockIdx.x) * kPTokens >= chunk) return;      // whole CTA: nothing to do
   const int L0 = max(a.seq_lens[s], 0);
   int n_full = L0 / kB;

@@ -31,16 +31,14 @@
 namespace kvarn {
 namespace {
 
-// Grid barrier state: arrivals and generation. Every completed launch leaves the
-// arrival count at zero.
-__device__ unsigned g_serve_barrier[2];
-
 constexpr int kServeThreads = 256;
 constexpr int kListCap = 16384;           // items whose tile completes, per CTA (at most)
 constexpr int kOpBytes = kB * kD * 2;   // one fp16 128 x 128 operand (32 KB)
 
 struct ServeArgs {
   DecodeArgs a;                // decode view; a.seq_lens = the lengths after the append
+  unsigned* barrier;           // grid barrier words [arrivals, generation] in the caller's
+                               // scratch, zeroed on the stream before every launch
   const uint16_t* k_new;       // [n_seqs][hkv][128] fp16
   const uint16_t* v_new;
   const int32_t* seq_lens_in;  // lengths before the append
@@ -75,23 +73,30 @@ struct ServeSmem {
   static_assert(kOffStage % 1024 == 0 && kOffVec % 16 == 0 && kOffBar % 8 == 0 && kOffScan % 8 == 0, "align");
 };
 
-// All CTAs of the grid meet here; a CTA that waits longer than kWaitNs raises
-// KVARN_FLAG_WAIT_TIMEOUT and goes on.
-__device__ void grid_sync(unsigned n_ctas, unsigned* flags) {
+// All CTAs of the grid meet here. `barrier` = [arrivals, generation], zero before the
+// launch's first barrier; the last CTA to arrive resets the arrivals and advances the
+// generation. A CTA that waits longer than `limit_ns` raises KVARN_FLAG_WAIT_TIMEOUT
+// and gets false: it must not start the next phase (its inputs may not be ready), so
+// the caller returns. The words live in the call's own scratch, so a timeout in one
+// call cannot disturb the barriers of another.
+__device__ bool grid_sync(unsigned* barrier, unsigned n_ctas, unsigned* flags,
+                          unsigned long long limit_ns = kWaitNs) {
+  bool ok = true;
   __syncthreads();
   if (threadIdx.x == 0) {
-    volatile unsigned* gen = &g_serve_barrier[1];
+    volatile unsigned* gen = &barrier[1];
     const unsigned g0 = *gen;   // read before arriving: it cannot advance without this CTA
     __threadfence();
-    if (atomicAdd(&g_serve_barrier[0], 1u) + 1u == n_ctas) {
-      atomicExch(&g_serve_barrier[0], 0u);
+    if (atomicAdd(&barrier[0], 1u) + 1u == n_ctas) {
+      atomicExch(&barrier[0], 0u);
       __threadfence();
-      atomicAdd(&g_serve_barrier[1], 1u);
+      atomicAdd(&barrier[1], 1u);
     } else {
       const unsigned long long t0 = global_ns();
       while (*gen == g0) {
-        if (global_ns() - t0 > kWaitNs) {
+        if (global_ns() - t0 > limit_ns) {
           raise_flag(flags, KVARN_FLAG_WAIT_TIMEOUT);
+          ok = false;
           break;
         }
         __nanosleep(100);
@@ -99,7 +104,7 @@ __device__ void grid_sync(unsigned n_ctas, unsigned* flags) {
     }
     __threadfence();
   }
-  __syncthreads();
+  return __syncthreads_and(ok) != 0;   // thread 0's verdict, for the whole CTA
 }
 
 // Length of sequence s after the append (a negative length is left as it is).
@@ -303,11 +308,11 @@ template <int KB, int VB, bool kLean>
 __global__ void __launch_bounds__(kServeThreads, 1) serve_step_kernel(const ServeArgs sa) {
   extern __shared__ __align__(1024) uint8_t smem[];
   serve_append<KB, VB, kLean>(sa, smem);
-  grid_sync(gridDim.x, sa.a.flags);
+  if (!grid_sync(sa.barrier, gridDim.x, sa.a.flags)) return;   // timed out (flag raised)
   // records written through the async proxy by other CTAs are read the same way
   asm volatile("fence.proxy.async.global;" ::: "memory");
   if (sa.a.max_blocks > 0) split_body<KB, VB, kLean>(sa.a, smem, blockIdx.x);
-  grid_sync(gridDim.x, sa.a.flags);
+  if (!grid_sync(sa.barrier, gridDim.x, sa.a.flags)) return;
   // merge: every warp takes (sequence, kv-head, q-head) items on its own; the split
   // warps' ranges are copied to shared memory for the searches
   float* scw = reinterpret_cast<float*>(smem) + (threadIdx.x >> 5) * 128;
@@ -346,7 +351,62 @@ cudaError_t launch_serve_bits(const ServeArgs& sa, int grid, cudaStream_t stream
   return cudaLaunchKernelEx(&cfg, serve_step_kernel<KB, VB, kLean>, sa);
 }
 
+// Self-test of the bounded waits: waits that can never complete, each with a
+// `limit_ns` limit. which = 0: every thread waits on an mbarrier whose phase expects
+// 16 bytes that no copy delivers. which = 1: a cooperative grid whose barrier
+// expects one CTA more than were launched. Either way each wait gives up, raises
+// KVARN_FLAG_WAIT_TIMEOUT and the kernel returns; no copy or MMA is in flight.
+__global__ void __launch_bounds__(32) wait_selftest_mbar_kernel(unsigned* flags, unsigned long long limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_arrive_expect_tx(&bar, 16);
+  __syncwarp();
+  mbar_wait(&bar, 0, flags, limit_ns);
+}
+
+__global__ void __launch_bounds__(32) wait_selftest_grid_kernel(unsigned* barrier, unsigned* flags,
+                                                                unsigned long long limit_ns) {
+  grid_sync(barrier, gridDim.x + 1, flags, limit_ns);
+}
+
 }  // namespace
+
+size_t serve_barrier_offset(int n_seqs, int hkv, int max_blocks) {
+  return decode_part_bytes(n_seqs, hkv, max_blocks) - kServeBarrierBytes;
+}
+
+unsigned* serve_barrier_words(void* scratch, int n_seqs, int hkv, int max_blocks) {
+  return reinterpret_cast<unsigned*>(static_cast<uint8_t*>(scratch) + serve_barrier_offset(n_seqs, hkv, max_blocks));
+}
+
+cudaError_t launch_wait_selftest(int which, unsigned long long limit_ns, void* barrier_words, unsigned* flags,
+                                 cudaStream_t stream) {
+  if (which == 0) {
+    wait_selftest_mbar_kernel<<<1, 32, 0, stream>>>(flags, limit_ns);
+    return cudaGetLastError();
+  }
+  if (which != 1) return cudaErrorInvalidValue;
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  cudaError_t err = cudaMemsetAsync(barrier_words, 0, 2 * sizeof(unsigned), stream);
+  if (err != cudaSuccess) return err;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(sms > 0 ? sms : 1));
+  cfg.blockDim = dim3(32);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  unsigned* words = static_cast<unsigned*>(barrier_words);
+  return cudaLaunchKernelEx(&cfg, wait_selftest_grid_kernel, words, flags, limit_ns);
+}
 
 cudaError_t launch_serve_step(const uint16_t* q, const uint16_t* k_new, const uint16_t* v_new,
                               const int32_t* seq_lens, int32_t* seq_lens_out, const int32_t* block_tables,
@@ -384,6 +444,9 @@ cudaError_t launch_serve_step(const uint16_t* q, const uint16_t* k_new, const ui
   sa.out = out;
   sa.n_iters = n_iters;
   sa.eps = eps;
+  sa.barrier = serve_barrier_words(scratch, n_seqs, hkv, max_blocks);
+  const cudaError_t zero = cudaMemsetAsync(sa.barrier, 0, 2 * sizeof(unsigned), stream);
+  if (zero != cudaSuccess) return zero;
   if (k_bits == 4 && v_bits == 2 && !lean) {
     a.warps = SplitCfg<4, 2>::kWarps;
     return launch_serve_bits<4, 2, false>(sa, grid, stream);

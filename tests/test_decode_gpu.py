@@ -1,6 +1,7 @@
 """Parity of kvarn_decode_attention (CUDA, through the C ABI) with the CPU oracle.
-The packed caches are made by the oracle's quantizer (small cases) or drawn as
-random valid records (full sizes), never by the CUDA quantizer."""
+The packed caches are made by the oracle's quantizer (small cases, and every block
+of the sampled pairs at full sizes; random valid records fill the rest of a
+full-size cache), never by the CUDA quantizer."""
 import numpy as np
 import pytest
 
@@ -84,33 +85,50 @@ def test_ragged_lengths_and_groups(env, group):
     assert_decode_close(out, ref, f"group {group}")
 
 
-def _random_cache_case(env, n_seqs, seq_len, hkv, hq, seed, n_pairs):
+def _config_case(env, n_seqs, seq_len, hkv, hq, seed, n_pairs):
+    """A full-size decode workload whose sampled (sequence, kv-head) pairs hold K/V
+    drawn like the prefill batch (outlier key channels x10-x50) and quantized by the
+    oracle into every block of the pair; random valid records fill the rest of the
+    cache. The oracle's decode of each sampled pair runs over exactly those records
+    (in worker processes, tests/oracle_pool.py)."""
+    from tests.oracle_pool import run_pairs
     kv, torch = env
     max_blocks = seq_len // 128
     num_blocks = n_seqs * max_blocks
     bt = synth.block_tables(n_seqs, max_blocks, num_blocks, seed)
     recs = synth.random_records(num_blocks * hkv, seed, o.RECORD_BYTES, 12288).reshape(num_blocks, hkv, -1)
     q = synth.queries(n_seqs, hq, seed)
+    g = hq // hkv
+    rng = np.random.default_rng(seed)
+    all_pairs = [(s, h) for s in range(n_seqs) for h in range(hkv)]
+    pick = rng.choice(len(all_pairs), size=min(n_pairs, len(all_pairs)), replace=False)
+    pairs = sorted(all_pairs[int(i)] for i in pick)
+    jobs = [(1_000_003 * seed + 64 * s + h, seq_len, q[s, h * g:(h + 1) * g], "k4v2") for s, h in pairs]
+    res = run_pairs(jobs)
+    for (s, h), (r, _, _) in zip(pairs, res):
+        recs[bt[s], h] = r
     lens = np.full(n_seqs, seq_len, np.int32)
     out, flags = gpu_decode(env, q, torch.from_numpy(recs).cuda(), None, bt, lens, hkv, num_blocks)
     assert flags == 0
-    rng = np.random.default_rng(seed)
-    pairs = sorted({(int(s), int(h)) for s, h in zip(rng.integers(0, n_seqs, n_pairs), rng.integers(0, hkv, n_pairs))})
-    ref = o.decode(q.astype(np.float64), recs, None, bt, lens, pairs=pairs)
-    g = hq // hkv
-    for s, h in pairs:
-        assert_decode_close(out[s, h * g:(h + 1) * g], ref[s, h * g:(h + 1) * g], f"seq {s} head {h}")
+    worst = 0.0
+    for (s, h), (_, _, ref) in zip(pairs, res):
+        worst = max(worst, assert_decode_close(out[s, h * g:(h + 1) * g], ref, f"seq {s} head {h}"))
     assert np.isfinite(out).all()
+    print(f"{len(pairs)} oracle-quantized pairs, max |err| {worst:.2e}")
 
 
 def test_decode_64x16k_sampled(env):
-    """Full decode workload: 64 sequences x 16384 tokens, 64 q-heads over 8 kv-heads."""
-    _random_cache_case(env, 64, 16384, 8, 64, seed=2, n_pairs=12)
+    """Full decode workload: 64 sequences x 16384 tokens, 64 q-heads over 8 kv-heads;
+    64 sampled (sequence, kv-head) pairs hold oracle-quantized K/V of the prefill
+    distribution."""
+    _config_case(env, 64, 16384, 8, 64, seed=2, n_pairs=64)
 
 
 def test_decode_4x128k_sampled(env):
-    """Long-context workload: 4 sequences x 131072 tokens, split-K over 64 splits."""
-    _random_cache_case(env, 4, 131072, 8, 64, seed=3, n_pairs=6)
+    """Long-context workload: 4 sequences x 131072 tokens, split-K; every one of the
+    32 (sequence, kv-head) pairs holds oracle-quantized K/V of the prefill
+    distribution."""
+    _config_case(env, 4, 131072, 8, 64, seed=3, n_pairs=32)
 
 
 def test_bad_block_is_skipped_and_flagged(env):

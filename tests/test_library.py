@@ -200,3 +200,13 @@ def test_static_decode_checks_like_the_scratch_decode(kv):
     bad = kv.make_meta(8, 64, 1024, max_blocks_per_seq=128)
     bad.k_bits = 3
     assert st(A, A, None, A, A, 4, A, ctypes.byref(bad), None) == 2     # not a preset
+
+
+def test_bounded_wait_check_rejects_bad_arguments(kv):
+    chk = _raw(kv, "kvarn_check_bounded_waits")
+    assert chk(2, 1000, A, 256, None) == 1              # unknown wait kind
+    assert chk(0, 0, None, 0, None) == 1                # limit below 1 us
+    assert chk(0, 2000000, None, 0, None) == 1          # limit above 1 s
+    assert chk(1, 1000, None, 0, None) == 1             # grid barrier needs scratch
+    assert chk(1, 1000, MIS, 256, None) == 3            # misaligned scratch
+    assert chk(1, 1000, A, 4, None) == 4                # scratch smaller than the barrier words

@@ -251,6 +251,31 @@ def test_layout_spots_match_hand_computed_table():
         assert f(int(ch), int(tok)) == (int(byte), int(shift)), (tensor, ch, tok)
 
 
+def test_k2_and_v4_layout_spots_match_hand_computed_table():
+    """The 2-bit key layout (k2v2) and the 4-bit value layout (k4v4) at hand-computed
+    spots: the position function and the packer (a single code written alone lands
+    at exactly those bits of a whole record) both agree with the table."""
+    zero = {n: np.zeros(128) for n in ("r", "c", "s", "z")}
+    for preset, tensor, ch, tok, byte, shift in _golden_rows("record_layout_spots_k2_v4.txt"):
+        ch, tok, byte, shift = int(ch), int(tok), int(byte), int(shift)
+        lay = o.LAYOUTS[preset]
+        if tensor == "K":
+            b, sh = o.k2_position(ch, tok)
+            b += lay.k_code_off
+        else:
+            b, sh = o.v4_position(ch, tok)
+            b += lay.v_code_off
+        assert (b, sh) == (byte, shift), (preset, tensor, ch, tok)
+        bits = lay.k_bits if tensor == "K" else lay.v_bits
+        val = (1 << bits) - 1
+        kc = np.zeros((128, 128), np.uint8)
+        vc = np.zeros((128, 128), np.uint8)
+        (kc if tensor == "K" else vc)[ch, tok] = val
+        rec = o.pack_record(dict(codes=kc, bits=lay.k_bits, **zero), dict(codes=vc, bits=lay.v_bits, **zero), preset)
+        codes = rec[:lay.k_meta_off]
+        assert codes[byte] == val << shift and np.count_nonzero(codes) == 1, (preset, tensor, ch, tok)
+
+
 def test_pack_roundtrip_and_single_code_positions():
     rng = np.random.default_rng(13)
     kq = dict(codes=rng.integers(0, 16, (3, 128, 128)).astype(np.uint8))
@@ -520,6 +545,47 @@ def test_lean_preset_folds_the_in_group_scale():
     for a, b in ((kl, kfull), (vl, vfull)):
         rel = np.linalg.norm(a - b) / np.linalg.norm(b)
         assert rel < 0.05, rel
+
+
+def _fwht_rows(x):
+    """Orthonormal Walsh-Hadamard transform along axis 0 by the butterfly recursion
+    (independent of the oracle's dense H)."""
+    x = np.array(x, np.float64)
+    h = 1
+    while h < x.shape[0]:
+        for i in range(0, x.shape[0], 2 * h):
+            a, b = x[i:i + h].copy(), x[i + h:i + 2 * h].copy()
+            x[i:i + h], x[i + h:i + 2 * h] = a + b, a - b
+        h *= 2
+    return x / np.sqrt(x.shape[0])
+
+
+def test_lean_groups_quantize_the_rotated_tile_over_the_other_scale():
+    """Lean metadata against the tile itself: with X_r from an independent butterfly
+    transform, a lean key group (channel i) holds X_r[i, :] / c within half a step of
+    its (s_i, z_i) grid, and a lean value group (token j) holds X_r[:, j] / r likewise;
+    the group extremes land on the end codes. Dropping the division, dividing by the
+    wrong scale or grouping along the wrong axis breaks the bound."""
+    k, v, _ = synth.single_tile(10)
+    rec, kq, vq = o.quantize_tiles(k, v, preset="k4v2l")
+    k2, v2 = o.unpack_record(rec)
+    ulp = lambda a: np.spacing(np.abs(a).astype(np.float16)).astype(np.float64)
+    for x, g, kind, bits in ((k, k2, "K", 4), (v, v2, "V", 2)):
+        xr = _fwht_rows(np.asarray(x, np.float64).T)             # [channel, token]
+        if kind == "K":
+            y = xr / g["c"][None, :]
+            axis = 1
+        else:
+            y = xr / g["r"][:, None]
+            axis = 0
+        s, z, codes = g["s"], g["z"], g["codes"]
+        deq = np.expand_dims(z, axis) + codes * np.expand_dims(s, axis)
+        bound = np.expand_dims(s / 2 + ulp(z) / 2 + (2 ** bits - 1) * ulp(s) / 2, axis)
+        assert (np.abs(y - deq) <= bound * (1 + 1e-9) + 1e-12).all(), kind
+        assert (np.take_along_axis(codes, np.expand_dims(y.argmin(axis), axis), axis) == 0).all(), kind
+        assert (np.take_along_axis(codes, np.expand_dims(y.argmax(axis), axis), axis) == 2 ** bits - 1).all(), kind
+        # z is the fp16 group minimum of exactly this y
+        assert np.array_equal(z, o.fp16_rne(y.min(axis=axis))), kind
 
 
 # ----------------------------------------------------------------------------------

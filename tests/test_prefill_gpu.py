@@ -57,7 +57,7 @@ def _case(lens, chunks, hkv, group, seed, preset="k4v2", random_cache=False):
                 num_blocks=num_blocks, max_blocks=max_blocks, hkv=hkv, group=group, preset=preset)
 
 
-def _gpu(env, c, use_ws=True):
+def _gpu(env, c, use_ws=True, max_chunk=None):
     kv, torch = env
     meta = kv.make_meta(c["hkv"], c["hkv"] * c["group"], c["num_blocks"], max_blocks_per_seq=c["max_blocks"],
                         preset=c["preset"])
@@ -66,7 +66,8 @@ def _gpu(env, c, use_ws=True):
     chunks = np.diff(c["cu"])
     kv.kvarn_prefill_attention(q, f16_to_dev(torch, c["kn"]), f16_to_dev(torch, c["vn"]),
                                torch.from_numpy(c["cu"]).cuda(), torch.from_numpy(c["lens"]).cuda(),
-                               int(chunks.max()) if len(chunks) else 0, torch.from_numpy(c["bt"]).cuda(),
+                               max_chunk if max_chunk is not None else int(chunks.max()) if len(chunks) else 0,
+                               torch.from_numpy(c["bt"]).cuda(),
                                torch.from_numpy(c["cache"]).cuda(), f16_to_dev(torch, c["ws"]) if use_ws else None,
                                out, meta)
     flags = kv.kvarn_device_flags()
@@ -112,3 +113,18 @@ def test_prefill_without_workspace_and_empty_chunk(env):
     c = _case([200], [3], hkv=1, group=2, seed=84)
     _, flags = _gpu(env, c, use_ws=False)
     assert flags == 0x4                          # KVARN_FLAG_BAD_LENGTH
+
+
+def test_prefill_chunk_longer_than_max_chunk_is_flagged(env):
+    """A chunk longer than max_chunk (rounded up to 16 tokens) leaves its tail
+    tokens uncomputed: the call raises KVARN_FLAG_BAD_LENGTH, the covered tokens
+    still match the oracle and the rows past the grid stay untouched."""
+    c = _case([300, 130], [40, 9], hkv=2, group=4, seed=85)
+    out, flags = _gpu(env, c, max_chunk=20)          # grid: 2 CTAs x 16 tokens = 32 < 40
+    assert flags == 0x4                              # KVARN_FLAG_BAD_LENGTH
+    ref = o.prefill_attention(c["q"], c["kn"], c["vn"], c["cu"], c["lens"], c["bt"], c["ws"], c["cache"])
+    assert_decode_close(out[:32], ref[:32], "covered tokens of the long chunk")
+    assert np.isnan(out[32:40]).all()                # never written
+    assert_decode_close(out[40:49], ref[40:49], "the short chunk")
+    out, flags = _gpu(env, c, max_chunk=40)          # the bound is met: no flag
+    assert flags == 0

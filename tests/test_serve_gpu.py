@@ -134,3 +134,76 @@ def test_serve_step_graph_replay(env):
             assert torch.equal(st[k], want[k]), (replay, k)
         assert torch.equal(lens_out, c["lens"] + 1)
         assert torch.equal(out.view(torch.int16), want_out.view(torch.int16)), replay
+
+
+def test_serve_step_256_ragged_against_oracle(env):
+    """The mixed serving step at its full shape through the one-launch entry point,
+    against the oracle: 256 sequences with lengths log-uniform in [1024, 32768] (every
+    8th forced to L % 128 == 127, so the append completes its tile), 64 q-heads over
+    8 kv-heads. 32 sampled (sequence, kv-head) pairs hold K/V drawn like the prefill
+    batch and quantized by the oracle (all their full tiles, their workspace tail);
+    random valid records and workspace tokens fill the rest. Checked against
+    oracle.append + oracle.decode: the whole workspace and the new lengths bit for
+    bit, every completed tile within the record tolerances, every other record
+    untouched, and the attention of the sampled pairs within the decode tolerance."""
+    from tests.oracle_pool import run_pairs
+    from tests.parity import assert_decode_close, compare_records
+    kv, torch = env
+    cfg = synth.WORKLOADS["serve_256_ragged"]
+    n_seqs, hkv, hq, seed = cfg["n_seqs"], cfg["n_kv_heads"], cfg["n_q_heads"], cfg["seed"]
+    g = hq // hkv
+    lens = synth.ragged_lengths(n_seqs, cfg["lo"], cfg["hi"], seed)
+    lens[::8] = (lens[::8] // 128) * 128 + 127
+    max_blocks = int(max((L + 1 + 127) // 128 for L in lens))
+    num_blocks = int(((lens + 1 + 127) // 128).sum()) + 16
+    perm = synth.block_permutation(num_blocks, seed)
+    bt = np.full((n_seqs, max_blocks), -1, np.int32)
+    pos = 0
+    for s in range(n_seqs):
+        nb = (lens[s] + 1 + 127) // 128
+        bt[s, :nb] = perm[pos:pos + nb]
+        pos += nb
+    recs = synth.random_records(num_blocks * hkv, seed, o.RECORD_BYTES, 12288).reshape(num_blocks, hkv, -1)
+    ws = synth.workspace_tokens(n_seqs, hkv, seed)
+    rng = np.random.default_rng(seed)
+    done = [s for s in range(n_seqs) if lens[s] % 128 == 127]
+    seqs = sorted(set(rng.choice(n_seqs, 24, replace=False).tolist()) | set(done[::4]))
+    pairs = [(s, int(rng.integers(0, hkv))) for s in seqs]
+    res = run_pairs([(7_000_001 + 64 * s + h, int(lens[s]), None, "k4v2") for s, h in pairs])
+    for (s, h), (r, tail, _) in zip(pairs, res):
+        recs[bt[s, :lens[s] // 128], h] = r
+        ws[s, h] = tail
+    k_new, v_new = synth.prefill_kv(n_seqs, hkv, seed=seed + 1)
+    q = synth.queries(n_seqs, hq, seed)
+    f16 = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.float16).cuda()
+    meta = kv.make_meta(hkv, hq, num_blocks, max_blocks_per_seq=max_blocks)
+    ws_d, cache_d = f16(ws), torch.from_numpy(recs).cuda()
+    lens_out = torch.full((n_seqs,), -7, dtype=torch.int32, device="cuda")
+    out = torch.full((n_seqs, hq, 128), float("nan"), dtype=torch.float16, device="cuda")
+    scratch = torch.empty(kv.decode_scratch_bytes(meta, n_seqs), dtype=torch.uint8, device="cuda")
+    kv.kvarn_serve_step(f16(q), f16(k_new), f16(v_new), torch.from_numpy(lens).cuda(), lens_out,
+                        torch.from_numpy(bt).cuda(), ws_d, cache_d, out, scratch, meta)
+    torch.cuda.synchronize()
+    assert kv.kvarn_device_flags() == 0
+    ws_ref, cache_ref, lens_ref = o.append(k_new, v_new, lens, bt, ws, recs)
+    assert np.array_equal(lens_out.cpu().numpy(), lens_ref)
+    ws_g = ws_d.view(torch.int16).cpu().numpy().view(np.float16)
+    assert np.array_equal(ws_g.view(np.int16), ws_ref.view(np.int16))
+    cache_g = cache_d.cpu().numpy()
+    blocks = np.array([bt[s, lens[s] // 128] for s in done]).repeat(hkv)
+    heads = np.tile(np.arange(hkv), len(done))
+    _, kq, vq = o.quantize_tiles(np.stack([ws_ref[s, :, 0] for s in done]).reshape(-1, 128, 128),
+                                 np.stack([ws_ref[s, :, 1] for s in done]).reshape(-1, 128, 128))
+    print("completed tiles", compare_records(cache_g[blocks, heads], kq, vq))
+    untouched = np.ones(cache_g.shape[:2], bool)
+    untouched[blocks, heads] = False
+    assert np.array_equal(cache_g[untouched], cache_ref[untouched])
+    ref = o.decode(q.astype(np.float64), cache_ref, ws_ref, bt, lens_ref, pairs=pairs)
+    out = out.float().cpu().numpy().astype(np.float64)
+    assert np.isfinite(out).all()
+    worst = 0.0
+    for s, h in pairs:
+        worst = max(worst, assert_decode_close(out[s, h * g:(h + 1) * g], ref[s, h * g:(h + 1) * g],
+                                               f"seq {s} head {h}"))
+    print(f"{len(pairs)} sampled pairs ({sum(s in done for s, _ in pairs)} with a completed tile), "
+          f"max |err| {worst:.2e}")
