@@ -15,7 +15,8 @@ it. Every input is larger than L2 (129 MB), so no flush is needed between steps.
 Under torchrun (N > 1) each rank runs the same per-GPU workload on its own GPU
 (weak scaling, no data-path collective); timing is the max over ranks.
 --impl reference times the CPU oracle (float64 NumPy restatement of the method)
-on a bounded sample of the same workload on this host's cores.
+in a process pool over all of this host's cores; each of its steps is a bounded,
+scaled-down copy of the GPU step with the same quantize/decode mix.
 """
 from __future__ import annotations
 
@@ -56,15 +57,25 @@ def reduce_max(values, world: int):
     return [float(x) for x in t]
 
 
-# fp32 flops the method needs per fp16 element on the quantize path (the Hadamard
-# runs on tensor cores and is not counted): 4 iterations x 2 passes x (deviation FMA
-# 2 + running sum 1 + square FMA 2) = 40, plus y, group extremes and the code (10).
+# The quantize kernel's work counted as fp32 operations per fp16 element by this
+# implementation's scheme (a secondary view of the roofline, derived, not measured):
+# 4 iterations x 2 passes x (deviation FMA 2 + running sum 1 + square FMA 2) = 40,
+# plus y, group extremes and the code (10). The Hadamard runs on tensor cores.
 Q_FLOP_PER_ELEMENT = 50
+# Algorithmic HBM bytes of the quantize kernel per token per kv-head: K and V fp16
+# read (2 x 128 x 2) and the packed record written (14336 / 128 = 112 for k4v2).
+Q_BYTES_READ_PER_TOKEN_HEAD = 512
 
 
 def fp32_peak_tflops():
     # 152 SMs x 128 fp32 lanes x 2 flop per FMA x 2.07 GHz maximum SM clock
     return round(152 * 128 * 2 * 2.07e9 / 1e12, 2)
+
+
+def step_config(world: int):
+    """The `config` object of both arms' JSON lines (the same workload)."""
+    return {"workload": WORKLOAD, "quantize": PREFILL, "decode": DECODE, "preset": f"kvarn_{PRESET}_g128",
+            "n_iters": 4, "l2": "every input > L2 (129 MB); no flush", "parallelism": f"replicas x{world}"}
 
 
 def hbm_peak():
@@ -251,6 +262,17 @@ def run_gpu(args):
     d_ms = [e[1].elapsed_time(e[2]) for e in evs]
     assert kv.kvarn_device_flags() == 0
 
+    # the host link on this machine: the prefill batch's K (pinned) copied to the device alone
+    h2d_ms = []
+    for _ in range(4):
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        c0.record(stream)
+        S["kd"].copy_(S["kh"], non_blocking=True)
+        c1.record(stream)
+        torch.cuda.synchronize()
+        h2d_ms.append(c0.elapsed_time(c1))
+    h2d_gbs = S["kh"].numel() * 2 / (min(h2d_ms[1:]) * 1e-3) / 1e9
+
     # end to end through the C ABI with host buffers: inputs H2D, result D2H inside the
     # region. The prefill batch moves in E2E_CHUNKS slices on two copy streams; each
     # slice is quantized (one kvarn_quantize_tiles call) as soon as it is resident, so
@@ -318,28 +340,38 @@ def run_gpu(args):
 
     p, d = PREFILL, DECODE
     q_bytes = p["n_seqs"] * p["seq_len"] * p["n_kv_heads"] * 128 * 2 * 2
+    q_out_bytes = p["n_seqs"] * p["seq_len"] // 128 * p["n_kv_heads"] * RECORD
     d_bytes = d["n_seqs"] * (d["seq_len"] // 128) * d["n_kv_heads"] * RECORD
     step_bytes = q_bytes + d_bytes
     ms = total_ms / args.steps
     peak, peak_kind = hbm_peak()
     qm, dm = float(np.median(q_ms)), float(np.median(d_ms))
+    q_avg, d_avg = float(np.mean(q_ms)), float(np.mean(d_ms))
     q_gbs, d_gbs = q_bytes / (qm * 1e-3) / 1e9, d_bytes / (dm * 1e-3) / 1e9
-    # dominant kernel roofline (time share): both kernels are reported, the larger share leads.
-    # Quantize is bound by fp32 arithmetic by construction (~50 flop per fp16 element
-    # against 2 bytes of HBM traffic); its roofline is the fp32 pipe, with the HBM
-    # fraction reported beside it.
-    q_tflops = Q_FLOP_PER_ELEMENT * (q_bytes // 2) / (qm * 1e-3) / 1e12
+    # Roofline of each kernel on HBM bandwidth: algorithmic bytes per launch (quantize:
+    # fp16 K+V read + records written; decode: records read) over the kernel's average
+    # launch time in the timed region, against the measured copy bandwidth. The
+    # quantize kernel's fp32-ALU view is reported beside it (derived peak).
+    q_alg = q_bytes + q_out_bytes
+    q_tflops = Q_FLOP_PER_ELEMENT * (q_bytes // 2) / (q_avg * 1e-3) / 1e12
     fp32_peak = fp32_peak_tflops()
-    kq = dict(bound="alu", achieved=round(q_tflops, 2), peak=fp32_peak, unit="TFLOP/s",
-              frac=round(q_tflops / fp32_peak, 4),
+    q_hbm = q_alg / (q_avg * 1e-3) / 1e9
+    kq = dict(bound="hbm", achieved=round(q_hbm, 1), peak=peak, unit="GB/s", frac=round(q_hbm / peak, 4),
               traffic=profiled_traffic("quantize_kernel") if PRESET == "k4v2" else None,
-              kernel="quantize_kernel", algorithmic_flops_per_launch=Q_FLOP_PER_ELEMENT * (q_bytes // 2),
-              hbm_gbs=round(q_gbs, 1), hbm_frac=round(q_gbs / peak, 4),
-              peak_kind="derived: 152 SMs x 128 fp32 lanes x 2 flop x 2.07 GHz")
-    kd = dict(bound="hbm", achieved=round(d_gbs, 1), peak=peak, unit="GB/s", frac=round(d_gbs / peak, 4),
+              kernel="quantize_kernel", algorithmic_bytes_per_launch=q_alg,
+              algorithmic_bytes_per_unit="512 B read + 112 B written per token per kv-head",
+              launch_ms=round(q_avg, 4), peak_kind=peak_kind,
+              alu_view=dict(achieved=round(q_tflops, 2), peak=fp32_peak, unit="TFLOP/s",
+                            frac=round(q_tflops / fp32_peak, 4),
+                            flops_per_launch=Q_FLOP_PER_ELEMENT * (q_bytes // 2),
+                            peak_kind="derived: 152 SMs x 128 fp32 lanes x 2 flop x 2.07 GHz; flops counted "
+                                      "by this implementation's scheme (50 per fp16 element)"))
+    d_hbm = d_bytes / (d_avg * 1e-3) / 1e9
+    kd = dict(bound="hbm", achieved=round(d_hbm, 1), peak=peak, unit="GB/s", frac=round(d_hbm / peak, 4),
               traffic=profiled_traffic("decode_split_kernel") if PRESET == "k4v2" else None,
               kernel="decode_split_kernel+decode_merge_kernel",
-              algorithmic_bytes_per_launch=d_bytes, peak_kind=peak_kind)
+              algorithmic_bytes_per_launch=d_bytes, algorithmic_bytes_per_unit="112 B per cached token per kv-head",
+              launch_ms=round(d_avg, 4), peak_kind=peak_kind)
     dominant = kq if qm >= dm else kd
     res = {
         "metric": "quantize GB/s (fp16 KV in) + paged decode-attn GB/s, % of GB300 HBM peak",
@@ -354,9 +386,7 @@ def run_gpu(args):
         "vs_baseline": None,
         "dtype": "f32",
         "data": "synthetic",
-        "config": {"workload": WORKLOAD, "quantize": PREFILL, "decode": DECODE, "preset": f"kvarn_{PRESET}_g128",
-                   "n_iters": 4, "l2": "every input > L2 (129 MB); no flush",
-                   "parallelism": f"replicas x{world}"},
+        "config": step_config(world),
         "quantize_gbs": round(q_gbs, 1),
         "quantize_frac_hbm": round(q_gbs / peak, 4),
         "decode_gbs": round(d_gbs, 1),
@@ -368,7 +398,12 @@ def run_gpu(args):
         "roofline": dominant,
         "roofline_kernels": [kq, kd],
         "e2e": {"value": round(world * step_bytes / (e2e_ms / args.steps * 1e-3) / 1e9, 2), "unit": "GB/s",
-                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                "h2d_gbs": round(h2d_gbs, 1),
+                "h2d_bound": round(world * step_bytes / (h2d / (h2d_gbs * 1e9)) / 1e9, 1),
+                "h2d_note": "h2d_gbs: a pinned-host to device copy of the prefill batch's K (512 MiB) timed "
+                            "alone on this box; h2d_bound: the metric if the step took only its "
+                            "host-to-device copies at that rate"},
         "gpu_launches": args.steps * 4,
         "e2e_pipeline": f"{E2E_CHUNKS} slices on 2 copy streams, quantize per slice; the next step's copies "
                         "overlap this step's decode",
@@ -383,68 +418,117 @@ def run_gpu(args):
 
 
 # ----------------------------------------------------------------------------- CPU oracle arms
-_ORACLE_SNIPPET = r"""
-import json, os, sys, time
-sys.path.insert(0, {root!r})
-import numpy as np
-import kvarn_synth as synth
-from oracle import kvarn_oracle as o
-budget = {budget}
-p, d = {p!r}, {d!r}
-# quantize sample: consecutive tiles of the prefill batch
-n_tiles = {n_q_tiles}
-k, v = synth.prefill_kv(n_tiles // p["n_kv_heads"] * 128, p["n_kv_heads"], seed=p["seed"])
-pairs = [(c, h) for c in range(n_tiles // p["n_kv_heads"]) for h in range(p["n_kv_heads"])]
-t0 = time.perf_counter()
-done_q = 0
-for b0 in range(0, len(pairs), 32):
-    part = pairs[b0:b0 + 32]
-    kt = np.stack([k[c * 128:(c + 1) * 128, h] for c, h in part])
-    vt = np.stack([v[c * 128:(c + 1) * 128, h] for c, h in part])
-    o.quantize_tiles(kt, vt)
-    done_q += len(part)
-    if time.perf_counter() - t0 > budget / 2:
-        break
-tq = time.perf_counter() - t0
-# decode sample: (sequence, kv-head) pairs over full 16384-token contexts of random records
-max_blocks = d["seq_len"] // 128
-recs = synth.random_records(max_blocks, d["seed"], 14336, 12288).reshape(max_blocks, 1, -1)
-q = synth.queries(1, d["n_q_heads"], d["seed"]).astype(np.float64)
-g = d["n_q_heads"] // d["n_kv_heads"]
-t0 = time.perf_counter()
-done_d = 0
-while time.perf_counter() - t0 < budget / 2 or done_d == 0:
-    o.decode_one(q[0, :g], recs, None, np.arange(max_blocks), d["seq_len"], 0)
-    done_d += 1
-td = time.perf_counter() - t0
-print(json.dumps(dict(tq=tq, nq=done_q, td=td, nd=done_d)))
-"""
+# The oracle (float64 NumPy, one tile at a time, as it stands) on this host's cores.
+# A step of the oracle arm is a scaled-down copy of the GPU step with the same mix:
+# every worker process quantizes ORACLE_TILES_PER_UNIT tile-heads of the prefill
+# batch and decodes one (sequence, kv-head) pair over 16384 tokens, per unit, and
+# the workload has PREFILL tile-heads / DECODE pairs = 16384 / 512 = 32 tile-heads
+# per decode pair, so a unit is 1/512 of the full step's bytes.
+ORACLE_TILES_PER_UNIT = 32
+_ORACLE_STATE = {}
 
 
-def _oracle_sample(seconds: float):
-    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
-    code = _ORACLE_SNIPPET.format(root=ROOT, budget=seconds, p=PREFILL, d=DECODE, n_q_tiles=4096)
-    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env)
-    if r.returncode != 0:
-        raise RuntimeError(r.stderr[-2000:])
-    return json.loads(r.stdout.strip().splitlines()[-1])
+def _oracle_worker(job):
+    """One worker's share of an oracle step: `units` units (see above). Runs in a
+    spawned process with single-threaded BLAS; returns (seconds, tile-heads, pairs)."""
+    wid, units = job
+    import numpy as np
+    if not _ORACLE_STATE:
+        import kvarn_synth as synth
+        from oracle import kvarn_oracle as o
+        p, d = PREFILL, DECODE
+        heads = p["n_kv_heads"]
+        chunks = ORACLE_TILES_PER_UNIT // heads
+        k, v = synth.prefill_kv((wid + 1) * chunks * 128, heads, seed=p["seed"])
+        k, v = k[wid * chunks * 128:], v[wid * chunks * 128:]
+        kt = np.stack([k[c * 128:(c + 1) * 128, h] for c in range(chunks) for h in range(heads)])
+        vt = np.stack([v[c * 128:(c + 1) * 128, h] for c in range(chunks) for h in range(heads)])
+        max_blocks = d["seq_len"] // 128
+        recs = synth.random_records(max_blocks, d["seed"] + wid, 14336, 12288).reshape(max_blocks, 1, -1)
+        g = d["n_q_heads"] // d["n_kv_heads"]
+        q = synth.queries(1, d["n_q_heads"], d["seed"]).astype(np.float64)[0, :g]
+        _ORACLE_STATE.update(o=o, kt=kt, vt=vt, recs=recs, q=q, max_blocks=max_blocks)
+    st = _ORACLE_STATE
+    t0 = time.perf_counter()
+    for _ in range(units):
+        st["o"].quantize_tiles(st["kt"], st["vt"])
+        st["o"].decode_one(st["q"], st["recs"], None, np.arange(st["max_blocks"]), DECODE["seq_len"], 0)
+    return time.perf_counter() - t0, units * ORACLE_TILES_PER_UNIT, units
+
+
+class OraclePool:
+    """Persistent spawned worker processes (one per host core unless told otherwise),
+    BLAS limited to one thread each."""
+
+    def __init__(self, workers: int):
+        import multiprocessing as mp
+        from concurrent.futures import ProcessPoolExecutor
+        for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+            os.environ[k] = "1"
+        self.workers = workers
+        self.ex = ProcessPoolExecutor(max_workers=workers, mp_context=mp.get_context("spawn"))
+
+    def step(self, units_per_worker: int):
+        """Wall seconds of one step (every worker runs its units) and the units done."""
+        t0 = time.perf_counter()
+        res = list(self.ex.map(_oracle_worker, [(w, units_per_worker) for w in range(self.workers)]))
+        wall = time.perf_counter() - t0
+        return wall, sum(r[1] for r in res), sum(r[2] for r in res)
+
+    def close(self):
+        self.ex.shutdown()
+
+
+def _unit_bytes():
+    """Bytes of the metric one unit stands for: its tile-heads' fp16 K+V and its
+    decode pair's packed records."""
+    return ORACLE_TILES_PER_UNIT * 2 * 128 * 128 * 2 + (DECODE["seq_len"] // 128) * RECORD
+
+
+def _full_step_units():
+    n_pairs = DECODE["n_seqs"] * DECODE["n_kv_heads"]
+    n_tiles = PREFILL["n_seqs"] * PREFILL["seq_len"] // 128 * PREFILL["n_kv_heads"]
+    assert n_tiles == ORACLE_TILES_PER_UNIT * n_pairs
+    return n_pairs
+
+
+def oracle_rate(workers: int, units_per_worker: int, steps: int, warmup: int = 1):
+    """Oracle GB/s of the metric on `workers` host cores: median over `steps` timed
+    steps after `warmup` untimed ones (which also start the workers and draw their
+    inputs). Returns (GB/s, per-step walls, units per step)."""
+    pool = OraclePool(workers)
+    try:
+        for _ in range(warmup):
+            pool.step(1)
+        walls, units = [], 0
+        for _ in range(steps):
+            w, _, u = pool.step(units_per_worker)
+            walls.append(w)
+            units = u
+    finally:
+        pool.close()
+    walls.sort()
+    med = walls[len(walls) // 2]
+    return units * _unit_bytes() / med / 1e9, walls, units
 
 
 def cpu_baseline(seconds: float):
-    s = _oracle_sample(seconds)
-    q_bytes_per_tile = 2 * 128 * 128 * 2
-    d_bytes_per_pair = (DECODE["seq_len"] // 128) * RECORD
-    # the step's time on the oracle, extrapolated from the measured per-unit rates
-    n_q_units = PREFILL["n_seqs"] * PREFILL["seq_len"] // 128 * PREFILL["n_kv_heads"]
-    n_d_units = DECODE["n_seqs"] * DECODE["n_kv_heads"]
-    t_step = n_q_units * s["tq"] / s["nq"] + n_d_units * s["td"] / s["nd"]
-    step_bytes = n_q_units * q_bytes_per_tile + n_d_units * d_bytes_per_pair
-    return {"value": round(step_bytes / t_step / 1e9, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": (f"{s['nq']} tile-heads quantized ({s['tq']:.1f} s) and {s['nd']} (sequence, kv-head) "
-                       f"decodes at 16384 tokens ({s['td']:.1f} s) on 1 host core, float64 NumPy; the step "
-                       f"time is extrapolated from these per-unit rates"),
-            "quantize_gbs": round(s["nq"] * q_bytes_per_tile / s["tq"] / 1e9, 6),
-            "decode_gbs": round(s["nd"] * d_bytes_per_pair / s["td"] / 1e9, 6)}
+    """The oracle on all host cores (process pool) and on one core, each on a bounded
+    sample of the step's workload with the step's mix."""
+    cores = os.cpu_count() or 1
+    per = max(1, int(seconds / 2 / 0.1 / 3))       # a unit is ~0.1 s of one core; 3 timed steps
+    gbs_all, walls_all, units_all = oracle_rate(cores, max(1, per // 4), steps=3)
+    gbs_one, walls_one, units_one = oracle_rate(1, per, steps=3)
+    full = _full_step_units()
+    return {"value": round(gbs_all, 6), "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": (f"float64 NumPy oracle in a process pool of {cores} workers (one per host core, "
+                       f"single-threaded BLAS); each timed step {units_all} units of {ORACLE_TILES_PER_UNIT} "
+                       f"tile-heads quantized plus one (sequence, kv-head) decode over 16384 tokens, i.e. "
+                       f"{units_all}/{full} of the full step with its mix; median of 3 steps"),
+            "step_s": round(walls_all[len(walls_all) // 2], 3),
+            "single_core": {"value": round(gbs_one, 6), "unit": "GB/s", "cores": 1,
+                            "sample": f"the same oracle in one worker, {units_one} units per timed step, median of 3",
+                            "step_s": round(walls_one[len(walls_one) // 2], 3)}}
 
 
 def run_reference(args):
@@ -452,28 +536,39 @@ def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    per_step = max(2.0, args.cpu_seconds / max(1, args.steps))
-    for _ in range(args.warmup):
-        _oracle_sample(1.0)
-    vals = []
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        vals.append(cpu_baseline(per_step))
-    wall = time.perf_counter() - t0
-    import statistics
-    value = statistics.median(v["value"] for v in vals)
-    step_bytes = (PREFILL["n_seqs"] * PREFILL["seq_len"] * PREFILL["n_kv_heads"] * 128 * 4
-                  + DECODE["n_seqs"] * (DECODE["seq_len"] // 128) * DECODE["n_kv_heads"] * RECORD)
+    cores = os.cpu_count() or 1
+    units_per_worker = 4
+    pool = OraclePool(cores)
+    try:
+        for _ in range(args.warmup):
+            pool.step(1)
+        t0 = time.perf_counter()
+        walls, units = [], 0
+        for _ in range(args.steps):
+            w, _, units = pool.step(units_per_worker)
+            walls.append(w)
+        wall = time.perf_counter() - t0
+    finally:
+        pool.close()
+    step_bytes = units * _unit_bytes()
+    ms = 1e3 * sum(walls) / len(walls)
+    value = step_bytes / (ms * 1e-3) / 1e9
+    full = _full_step_units()
+    sample = (f"float64 NumPy oracle in a process pool of {cores} workers (one per host core, single-threaded "
+              f"BLAS); a step is {units} units of {ORACLE_TILES_PER_UNIT} tile-heads quantized plus one "
+              f"(sequence, kv-head) decode over 16384 tokens: {units}/{full} of the GPU step, same mix")
     res = {
         "impl": "reference",
         "metric": "quantize GB/s (fp16 KV in) + paged decode-attn GB/s, % of GB300 HBM peak",
-        "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": round(step_bytes / (value * 1e9) * 1e3, 3), "higher_is_better": True,
+        "value": round(value, 6), "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "quantize": PREFILL, "decode": DECODE, "preset": "kvarn_k4v2_g128"},
-        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": vals[0]["sample"]},
-        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "config": step_config(world),
+        "step_fraction_of_gpu_step": f"{units}/{full}",
+        "extrapolated_full_step_ms": round(ms * full / units, 1),
+        "cpu_baseline": {"value": round(value, 6), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "wall_s": round(wall, 1),
     }
     print(json.dumps(res), flush=True)
