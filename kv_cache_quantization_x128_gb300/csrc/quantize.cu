@@ -233,8 +233,13 @@ __global__ void __maxnreg__(128)
     dst = src.target(item, check, gt, flags);
   else if (gt == 0)
     raise_flag(flags, KVARN_FLAG_BAD_SLOTS);
+  // Async work is spread over three threads of the group so that it overlaps:
+  // gt == 0 issues the Hadamard products, gt == kTmaThread the tile copies and
+  // gt == kStoreThread the record stores (bulk groups belong to the thread that
+  // commits them, so it also waits for them).
+  constexpr int kTmaThread = 64, kStoreThread = 32;
   if (src.needs_load(item)) {
-    if (gt == 0) issue_tile(src, item, grp, tiles, &load_bar[0]);
+    if (gt == kTmaThread) issue_tile(src, item, grp, tiles, &load_bar[0]);
     pend = 1;
   }
   uint32_t mma_parity = 0;
@@ -246,7 +251,7 @@ __global__ void __maxnreg__(128)
     typename Src::Check check_next{};
     if (has_next) {
       if (src.needs_load(next)) {   // buffer buf ^ 1 was last read by the previous item
-        if (gt == 0) issue_tile(src, next, grp, tiles + (buf ^ 1) * kTileOp, &load_bar[buf ^ 1]);
+        if (gt == kTmaThread) issue_tile(src, next, grp, tiles + (buf ^ 1) * kTileOp, &load_bar[buf ^ 1]);
         pend |= 2u >> buf;
       }
       check_next = src.prepare(next, gt);
@@ -275,8 +280,8 @@ __global__ void __maxnreg__(128)
           umma_commit(&mma_bar[grp]);
           mma_inflight = true;
         }
-        bulk_wait_read<1>();              // the stage written two items ago has been stored
       }
+      if (gt == kStoreThread) bulk_wait_read<1>();   // the stage written two items ago has been stored
       if (ok) {
         ok = mbar_wait(&mma_bar[grp], mma_parity, flags);
         if (ok) {
@@ -297,7 +302,7 @@ __global__ void __maxnreg__(128)
     // end of the item: its stage is complete, and the group agrees on the next item's slots
     const bool next_ok = named_bar_and(bar_id, kGroupThreads, !has_next || src.check_ok(check_next, gt));
     tc_fence_after();
-    if (dst >= 0 && gt == 0) {
+    if (dst >= 0 && gt == kStoreThread) {
       using L = RecordLayout<KB, VB, kLean>;
       uint8_t* stage = smem + (grp == 0 ? S::kOffStageK + buf * S::kStageK : S::kOffStageV + buf * S::kStageV);
       uint8_t* rec = cache + dst * static_cast<int64_t>(L::kBytes);
@@ -318,14 +323,13 @@ __global__ void __maxnreg__(128)
         raise_flag(flags, KVARN_FLAG_BAD_SLOTS);
     }
   }
-  if (gt == 0) {
-    // after a timeout: let copies and MMAs still in flight finish (bounded) before
-    // the shared memory and TMEM are released
+  // after a timeout: let copies and MMAs still in flight finish (bounded) before the
+  // shared memory and TMEM are released
+  if (gt == kTmaThread)
     for (int b = 0; b < 2; ++b)
       if ((pend >> b) & 1u) mbar_wait(&load_bar[b], (load_parity >> b) & 1u, flags);
-    if (mma_inflight) mbar_wait(&mma_bar[grp], mma_parity, flags);
-    bulk_wait_all();
-  }
+  if (gt == 0 && mma_inflight) mbar_wait(&mma_bar[grp], mma_parity, flags);
+  if (gt == kStoreThread) bulk_wait_all();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
