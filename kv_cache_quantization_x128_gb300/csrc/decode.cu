@@ -23,6 +23,12 @@
 //   decode_merge_kernel - per (sequence, kv-head): merges the partial records of
 //     the warps that covered it with the fp16 workspace tokens of the partial
 //     last tile, un-rotates by H^T and normalises.
+// decode_tc_kernel (decode_tc.cuh) is the split phase on tcgen05 for k4v2, chosen
+// with KVARN_DECODE_SPLIT=tc; it writes the same partial records.
+#include <cstdlib>
+#include <cstring>
+
+#include "decode_tc.cuh"
 #include "decode_tile.cuh"
 #include "kvarn_common.cuh"
 #include "kvarn_launch.h"
@@ -61,7 +67,7 @@ __global__ void __launch_bounds__(1024) decode_scan_kernel(DecodeArgs a) {
 
 template <int KB, int VB, bool kLean>
 __global__ void __launch_bounds__(SplitCfg<KB, VB, kLean>::kWarps * 32, 1) decode_split_kernel(DecodeArgs a) {
-  extern __shared__ __align__(128) uint8_t smem[];
+  extern __shared__ __align__(1024) uint8_t smem[];
   split_body<KB, VB, kLean>(a, smem, blockIdx.x);
 }
 
@@ -102,6 +108,24 @@ cudaError_t launch_split(const DecodeArgs& a, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+template <bool kLean>
+cudaError_t launch_split_tc(const DecodeArgs& a, cudaStream_t stream) {
+  using C = TcCfg<kLean>;
+  static std::atomic<unsigned long long> smem_set{0};
+  cudaError_t err = set_smem_once(decode_tc_kernel<kLean>, C::kSmem, smem_set);
+  if (err != cudaSuccess) return err;
+  decode_tc_kernel<kLean><<<a.n_ctas, kTcThreads, C::kSmem, stream>>>(a);
+  return cudaGetLastError();
+}
+
+// The warp-level split kernel serves every preset; KVARN_DECODE_SPLIT=tc selects the
+// tcgen05 one for k4v2 (measured slower: 0.51 against 0.25 ms on 64 x 16384
+// tokens). Read on every call, so one process can run both.
+bool use_tc_split() {
+  const char* e = std::getenv("KVARN_DECODE_SPLIT");
+  return e != nullptr && std::strcmp(e, "tc") == 0;
+}
+
 cudaError_t launch_decode(const uint16_t* q, const uint8_t* cache, const uint16_t* ws, const int32_t* block_tables,
                           const int32_t* seq_lens, int n_seqs, int hkv, int group, int max_blocks, int64_t num_blocks,
                           int k_bits, int v_bits, bool lean, uint16_t* out, void* scratch, unsigned* flags,
@@ -127,13 +151,16 @@ cudaError_t launch_decode(const uint16_t* q, const uint8_t* cache, const uint16_
   a.n_ctas = sms > 0 ? (sms < kMaxCtas ? sms : kMaxCtas) : 1;
   const bool k4v2 = k_bits == 4 && v_bits == 2, k4v4 = k_bits == 4 && v_bits == 4, k2v2 = k_bits == 2 && v_bits == 2;
   if (!(k4v2 || ((k4v4 || k2v2) && !lean))) return cudaErrorInvalidValue;
-  a.warps = k4v4 ? SplitCfg<4, 4>::kWarps : k2v2 ? SplitCfg<2, 2>::kWarps
+  const bool tc = k4v2 && use_tc_split();
+  a.warps = tc ? kTcTeams
+            : k4v4 ? SplitCfg<4, 4>::kWarps : k2v2 ? SplitCfg<2, 2>::kWarps
             : lean ? SplitCfg<4, 2, true>::kWarps : SplitCfg<4, 2>::kWarps;
   decode_scan_kernel<<<1, 1024, 0, stream>>>(a);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   if (max_blocks > 0) {
-    err = k2v2 ? launch_split<2, 2, false>(a, stream)
+    err = tc ? (lean ? launch_split_tc<true>(a, stream) : launch_split_tc<false>(a, stream))
+          : k2v2 ? launch_split<2, 2, false>(a, stream)
           : k4v4 ? launch_split<4, 4, false>(a, stream)
           : lean ? launch_split<4, 2, true>(a, stream) : launch_split<4, 2, false>(a, stream);
     if (err != cudaSuccess) return err;

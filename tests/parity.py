@@ -12,7 +12,8 @@ Tolerances (stated once, used by every parity test):
   the elements whose codes agree (a permitted flip of one 2-bit code alone moves a
   128 x 128 tile by ~1e-2 relative; flips are bounded by the code budget instead).
 * decode outputs (fp16): |gpu - oracle| <= 2e-3 + half an fp16 ulp of the oracle
-  value (the output's own rounding).
+  value (the output's own rounding). Two GPU paths that each hold that bound are
+  compared with each other at twice the absolute part plus one ulp.
 """
 from __future__ import annotations
 
@@ -130,4 +131,19 @@ def assert_decode_close(gpu_out: np.ndarray, ref: np.ndarray, what: str = ""):
     tol = DECODE_ATOL + ulp_half
     bad = ~(err <= tol)
     assert not bad.any(), f"{what}: {np.count_nonzero(bad)} outputs off, max err {err.max():.3e}"
+    return float(err.max())
+
+
+def assert_paths_close(a, b, what: str = ""):
+    """Two GPU decode outputs of the same inputs computed by different kernels (the
+    tensor-core split phase of kvarn_decode_attention and the warp-level one of the
+    fused serving step): each is within DECODE_ATOL + half an ulp of the oracle, so
+    they differ by at most 2 * DECODE_ATOL + one fp16 ulp."""
+    a = np.asarray(a, np.float64)
+    b = np.asarray(b, np.float64)
+    assert np.isfinite(a).all() and np.isfinite(b).all(), f"{what}: non-finite outputs"
+    ulp = np.spacing(np.abs(b).astype(np.float16)).astype(np.float64)
+    err = np.abs(a - b)
+    bad = ~(err <= 2 * DECODE_ATOL + ulp)
+    assert not bad.any(), f"{what}: {np.count_nonzero(bad)} outputs apart, max {err.max():.3e}"
     return float(err.max())

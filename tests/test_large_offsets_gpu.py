@@ -11,7 +11,7 @@ import pytest
 
 import kvarn_synth as synth
 from oracle import kvarn_oracle as o
-from tests.parity import assert_decode_close, compare_records
+from tests.parity import assert_decode_close, assert_paths_close, compare_records
 
 pytestmark = pytest.mark.gpu
 
@@ -194,7 +194,9 @@ def test_append_and_serve_step_past_4gb(env, state):
     ref = o.decode(c_q, c_cache, c_ws, st["c_bt"], c_lens)
     for i, s in enumerate(seqs):
         assert_decode_close(got[s], ref[i], f"sequence {s} after the append")
-    # the same step in one launch: bit for bit the two calls
+    # the same step in one launch: the two calls' workspace, cache and lengths bit for
+    # bit; its output (the warp-level split kernel) within the decode tolerance of the
+    # two calls' (the tensor-core one) and of the oracle
     ws1, cache1 = st["ws"].clone(), st["cache"].clone()
     lens1 = torch.full_like(lens_d, -7)
     out1 = torch.full_like(q, float("nan"))
@@ -204,7 +206,10 @@ def test_append_and_serve_step_past_4gb(env, state):
     assert torch.equal(lens1, lens2)
     assert torch.equal(ws1.view(torch.int16), ws2.view(torch.int16))
     assert torch.equal(cache1, cache2)
-    assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
+    got1 = out1.float().cpu().numpy().astype(np.float64)
+    assert_paths_close(got1, got, "serve step vs two calls")
+    for i, s in enumerate(seqs):
+        assert_decode_close(got1[s], ref[i], f"sequence {s}, serve step")
 
 
 def test_prefill_past_4gb(env, state):

@@ -62,16 +62,16 @@ def test_grid_barrier_gives_up_and_later_steps_are_exact(env):
     """A grid barrier that expects one CTA more than were launched runs out; its
     words are left in the last 256 bytes of a scratch buffer, exactly where a
     serving step keeps its own. A serving step on that same scratch right after
-    still matches kvarn_append_decode + kvarn_decode_attention bit for bit: the
-    step zeroes its barrier words before it starts."""
+    still matches the same step run before the timeout bit for bit: the step zeroes
+    its barrier words before it starts."""
     kv, torch = env
-    from tests.test_serve_gpu import _case, _meta, _two_calls
+    from tests.test_serve_gpu import _case, _meta, _serve
     n_seqs, hkv, group = 24, 2, 8
     c = _case(torch, n_seqs, hkv, group, seed=96, preset="k4v2")
     meta = _meta(kv, c, hkv, group, "k4v2")
     need = kv.decode_scratch_bytes(meta, n_seqs)
     scratch = torch.empty(need, dtype=torch.uint8, device="cuda")
-    want = _two_calls(kv, torch, c, meta, scratch)
+    want = _serve(kv, torch, c, meta, scratch)
     assert kv.kvarn_device_flags() == 0
     kv.kvarn_check_bounded_waits(kv.KVARN_WAIT_GRID, LIMIT_US, scratch[need - 256:])
     assert kv.kvarn_device_flags() == kv.FLAG_WAIT_TIMEOUT
