@@ -335,6 +335,34 @@ def run_gpu(args):
     h2d = sum(S[n].numel() * S[n].element_size() for n in ("kh", "vh", "slots_h", "qh", "bt_h", "lens_h"))
     d2h = S["out_h"].numel() * 2
 
+    # the decode with its tcgen05 split kernel (KVARN_DECODE_SPLIT=tc) on the same batch,
+    # outside the timed step, beside the default warp-level split kernel
+    tc_ms = None
+    if PRESET == "k4v2":
+        saved = os.environ.get("KVARN_DECODE_SPLIT")
+        os.environ["KVARN_DECODE_SPLIT"] = "tc"
+        try:
+            call = lambda: kv.kvarn_decode_attention(S["qd"], S["cache"], None, S["bt"], S["lens"], S["out"],
+                                                     S["scratch"], S["meta"])
+            for _ in range(3):
+                call()
+            torch.cuda.synchronize()
+            ts = []
+            for _ in range(10):
+                a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a0.record(stream)
+                call()
+                a1.record(stream)
+                torch.cuda.synchronize()
+                ts.append(a0.elapsed_time(a1))
+            tc_ms = float(np.median(ts))
+        finally:
+            if saved is None:
+                del os.environ["KVARN_DECODE_SPLIT"]
+            else:
+                os.environ["KVARN_DECODE_SPLIT"] = saved
+        assert kv.kvarn_device_flags() == 0
+
     # max over ranks
     total_ms, e2e_ms = reduce_max([total_ms, e2e_ms], world)
 
@@ -404,6 +432,12 @@ def run_gpu(args):
                 "h2d_note": "h2d_gbs: a pinned-host to device copy of the prefill batch's K (512 MiB) timed "
                             "alone on this box; h2d_bound: the metric if the step took only its "
                             "host-to-device copies at that rate"},
+        "decode_variants": None if tc_ms is None else {
+            "tcgen05_split_ms": round(tc_ms, 4),
+            "tcgen05_split_gbs": round(d_bytes / (tc_ms * 1e-3) / 1e9, 1),
+            "note": "the same decode with KVARN_DECODE_SPLIT=tc (tcgen05 split kernel, then the same merge), "
+                    "timed after the step (median of 10, inputs > L2); decode_ms is the default "
+                    "warp-level split kernel"},
         "gpu_launches": args.steps * 4,
         "e2e_pipeline": f"{E2E_CHUNKS} slices on 2 copy streams, quantize per slice; the next step's copies "
                         "overlap this step's decode",
