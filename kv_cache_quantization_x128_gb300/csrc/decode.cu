@@ -23,8 +23,10 @@
 //   decode_merge_kernel - per (sequence, kv-head): merges the partial records of
 //     the warps that covered it with the fp16 workspace tokens of the partial
 //     last tile, un-rotates by H^T and normalises.
-// decode_tc_kernel (decode_tc.cuh) is the split phase on tcgen05 for k4v2, chosen
-// with KVARN_DECODE_SPLIT=tc; it writes the same partial records.
+// decode_tc_split_kernel (decode_tc.cuh) is the split phase on tcgen05 for k4v2,
+// chosen with KVARN_DECODE_SPLIT=tc; it writes the same partial records. The split
+// and merge kernels are launched as programmatic dependents of the kernel before
+// them, so their launch overlaps its tail.
 #include <cstdlib>
 #include <cstring>
 
@@ -36,10 +38,22 @@
 namespace kvarn {
 namespace {
 
+// Programmatic dependent launch: a kernel launched with the attribute may start
+// while its predecessor in the stream runs; it waits for the predecessor's
+// completion (and memory) before touching its outputs. Without the attribute both
+// instructions do nothing.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ scan
+// Exclusive prefix of full tiles per sequence: each thread a contiguous chunk of
+// sequences, then a warp-shuffle scan and a scan of the 32 warp totals.
 __global__ void __launch_bounds__(1024) decode_scan_kernel(DecodeArgs a) {
-  __shared__ int64_t part_sums[1024];
-  const int t = threadIdx.x;
+  griddep_launch_dependents();          // the split kernel waits for this grid itself
+  __shared__ int64_t warp_sums[32];
+  const int t = threadIdx.x, lane = t & 31, w = t >> 5;
   const int per = (a.n_seqs + 1023) / 1024;
   const int s0 = min(t * per, a.n_seqs), s1 = min(s0 + per, a.n_seqs);
   int64_t sum = 0;
@@ -49,33 +63,70 @@ __global__ void __launch_bounds__(1024) decode_scan_kernel(DecodeArgs a) {
     clipped |= max(a.seq_lens[s], 0) / kB > a.max_blocks;
   }
   if (clipped) raise_flag(a.flags, KVARN_FLAG_BAD_LENGTH);
-  part_sums[t] = sum;
-  __syncthreads();
-  for (int off = 1; off < 1024; off <<= 1) {   // inclusive scan of the chunk sums
-    const int64_t v = t >= off ? part_sums[t - off] : 0;
-    __syncthreads();
-    part_sums[t] += v;
-    __syncthreads();
+  int64_t incl = sum;                   // inclusive scan inside the warp
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int64_t v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
   }
-  int64_t run = t > 0 ? part_sums[t - 1] : 0;
+  if (lane == 31) warp_sums[w] = incl;
+  __syncthreads();
+  if (w == 0) {                         // inclusive scan of the warp totals
+    int64_t v = warp_sums[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int64_t u = __shfl_up_sync(0xffffffffu, v, o);
+      if (lane >= o) v += u;
+    }
+    warp_sums[lane] = v;
+  }
+  __syncthreads();
+  int64_t run = incl - sum + (w > 0 ? warp_sums[w - 1] : 0);
   for (int s = s0; s < s1; ++s) {
     a.prefix[s] = run;
     run += full_tiles(a, s);
   }
-  if (t == 1023) a.prefix[a.n_seqs] = part_sums[1023];
+  if (t == 1023) a.prefix[a.n_seqs] = warp_sums[31];
 }
 
 template <int KB, int VB, bool kLean>
 __global__ void __launch_bounds__(SplitCfg<KB, VB, kLean>::kWarps * 32, 1) decode_split_kernel(DecodeArgs a) {
   extern __shared__ __align__(1024) uint8_t smem[];
+  griddep_launch_dependents();          // the merge kernel waits for this grid itself
+  griddep_wait();                       // the scan's prefix
   split_body<KB, VB, kLean>(a, smem, blockIdx.x);
+}
+
+template <bool kLean>
+__global__ void __launch_bounds__(kTcThreads, 1) decode_tc_split_kernel(DecodeArgs a) {
+  griddep_launch_dependents();
+  griddep_wait();
+  decode_tc_body<kLean>(a);
 }
 
 // One CTA per (kv-head, sequence).
 __global__ void __launch_bounds__(256) decode_merge_kernel(DecodeArgs a, const uint16_t* __restrict__ ws,
                                                            uint16_t* __restrict__ out) {
   __shared__ float sc[8][128];
+  griddep_wait();                       // the split kernel's ranges and partial records
   merge_body(a, ws, out, blockIdx.x, blockIdx.y, sc);
+}
+
+// Launch with programmatic stream serialization (see griddep_wait).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_after(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                         Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
 }  // namespace
@@ -104,18 +155,16 @@ cudaError_t launch_split(const DecodeArgs& a, cudaStream_t stream) {
   static std::atomic<unsigned long long> smem_set{0};
   cudaError_t err = set_smem_once(decode_split_kernel<KB, VB, kLean>, C::kSmem, smem_set);
   if (err != cudaSuccess) return err;
-  decode_split_kernel<KB, VB, kLean><<<a.n_ctas, C::kWarps * 32, C::kSmem, stream>>>(a);
-  return cudaGetLastError();
+  return launch_after(decode_split_kernel<KB, VB, kLean>, dim3(a.n_ctas), dim3(C::kWarps * 32), C::kSmem, stream, a);
 }
 
 template <bool kLean>
 cudaError_t launch_split_tc(const DecodeArgs& a, cudaStream_t stream) {
   using C = TcCfg<kLean>;
   static std::atomic<unsigned long long> smem_set{0};
-  cudaError_t err = set_smem_once(decode_tc_kernel<kLean>, C::kSmem, smem_set);
+  cudaError_t err = set_smem_once(decode_tc_split_kernel<kLean>, C::kSmem, smem_set);
   if (err != cudaSuccess) return err;
-  decode_tc_kernel<kLean><<<a.n_ctas, kTcThreads, C::kSmem, stream>>>(a);
-  return cudaGetLastError();
+  return launch_after(decode_tc_split_kernel<kLean>, dim3(a.n_ctas), dim3(kTcThreads), C::kSmem, stream, a);
 }
 
 // The warp-level split kernel serves every preset; KVARN_DECODE_SPLIT=tc selects the
@@ -165,9 +214,7 @@ cudaError_t launch_decode(const uint16_t* q, const uint8_t* cache, const uint16_
           : lean ? launch_split<4, 2, true>(a, stream) : launch_split<4, 2, false>(a, stream);
     if (err != cudaSuccess) return err;
   }
-  dim3 mgrid(hkv, n_seqs);
-  decode_merge_kernel<<<mgrid, 256, 0, stream>>>(a, ws, out);
-  return cudaGetLastError();
+  return launch_after(decode_merge_kernel, dim3(hkv, n_seqs), dim3(256), 0, stream, a, ws, out);
 }
 
 }  // namespace kvarn

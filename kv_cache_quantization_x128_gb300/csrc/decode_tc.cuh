@@ -545,8 +545,10 @@ __device__ __forceinline__ void tc_issue(const DecodeArgs& a, uint8_t* smem, uin
   mbar_wait(fin, 0, a.flags);
 }
 
+// The kernel body (one CTA per SM, kTcThreads threads, TcCfg<kLean>::kSmem bytes of
+// dynamic shared memory).
 template <bool kLean>
-__global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(DecodeArgs a) {
+__device__ __forceinline__ void decode_tc_body(const DecodeArgs& a) {
   extern __shared__ __align__(1024) uint8_t smem[];
   using C = TcCfg<kLean>;
   uint32_t* slot = reinterpret_cast<uint32_t*>(smem + C::kOffSlot);

@@ -63,6 +63,20 @@ __device__ __forceinline__ void warp_range(int64_t total, int n_ctas, int64_t wg
   end = c0 + (w + 1) * (c1 - c0) / kWarps;
 }
 
+// First split warp whose range (warp_range, kw warps per CTA) ends after global
+// tile t0 (0 <= t0 < total): the inverse of warp_range by integer arithmetic,
+// corrected by at most a step or two each way.
+__device__ __forceinline__ int64_t first_covering_warp(int64_t t0, int64_t total, int64_t n_ctas, int64_t kw) {
+  int64_t b = t0 * n_ctas / total;
+  while (b > 0 && b * total / n_ctas > t0) --b;
+  while ((b + 1) * total / n_ctas <= t0) ++b;
+  const int64_t c0 = b * total / n_ctas, n = (b + 1) * total / n_ctas - c0;   // c0 <= t0 < c0 + n
+  int64_t w = (t0 - c0) * kw / n;
+  while (w > 0 && w * n / kw > t0 - c0) --w;
+  while ((w + 1) * n / kw <= t0 - c0) ++w;
+  return b * kw + w;
+}
+
 // ------------------------------------------------------------------ tile cursor
 struct Cursor {
   int s, h, ti, nf;
@@ -477,17 +491,13 @@ __device__ __forceinline__ void merge_warp(const DecodeArgs& a, const uint16_t* 
   const int64_t n_warps = static_cast<int64_t>(a.n_ctas) * a.warps;
 
   // warps whose ranges cover this unit's tiles [t0, t1) (ranges are contiguous and
-  // ordered; empty ranges are skipped)
+  // ordered; empty ranges are skipped): the first from the range formula, the rest
+  // from the published ranges
   int64_t wlo = 0, whi = 0;
   const int64_t t0 = a.prefix[s] * a.hkv + static_cast<int64_t>(h) * nf, t1 = t0 + nf;
   if (nf > 0) {
-    int64_t lo = 0, hi = n_warps - 1;   // first warp with end > t0
-    while (lo < hi) {
-      const int64_t mid = (lo + hi) >> 1;
-      if (rg[2 * mid + 1] > t0) hi = mid; else lo = mid + 1;
-    }
-    wlo = lo;
-    whi = lo;
+    wlo = first_covering_warp(t0, a.prefix[a.n_seqs] * a.hkv, a.n_ctas, a.warps);
+    whi = wlo;
     while (whi < n_warps && rg[2 * whi] < t1) ++whi;
   }
 
