@@ -62,18 +62,38 @@ struct QSmem {
 
 // ------------------------------------------------------------------ work sources
 // A work item w is a (tile, kv-head) pair; both sources keep w below 2^31.
+// w / d for 0 <= w < 2^31 by a multiply-high (the round-up method of Granlund and
+// Montgomery, "Division by invariant integers using multiplication"):
+// q = (umulhi(m, w) + w) >> l, l = ceil(log2 d), m = floor(2^32 (2^l - d) / d) + 1.
+// Item indices split into (chunk or sequence, kv-head) without a division routine on
+// the path to the next item's products.
+struct ItemDiv {
+  uint32_t d, m, l;
+  __device__ __forceinline__ uint32_t div(int64_t w) const {
+    const uint32_t x = static_cast<uint32_t>(w);
+    return (__umulhi(m, x) + x) >> l;
+  }
+};
+inline ItemDiv make_item_div(uint32_t d) {
+  uint32_t l = 0;
+  while ((1u << l) < d) ++l;
+  const uint64_t m = ((uint64_t(1) << 32) * ((uint64_t(1) << l) - d)) / d + 1;
+  return ItemDiv{d, static_cast<uint32_t>(m), l};
+}
+
 struct PrefillSource {
   CUtensorMap map[2];   // K, V as [n_tokens rows][hkv * 128 channels] fp16
   const int64_t* slot;
   int64_t n_items;      // (n_tokens / 128) * hkv
   int hkv;
+  ItemDiv hd;           // division by hkv
   int64_t num_blocks;
 
   __device__ bool needs_load(int64_t) const { return true; }
   __device__ void scatter(int64_t, int, int) const {}
   // TMA coordinates (channel, token) of the item's 128 x 128 tile of tensor g
   __device__ void coords(int64_t w, int, int& x, int& y) const {
-    const uint32_t chunk = static_cast<uint32_t>(w) / static_cast<uint32_t>(hkv);
+    const uint32_t chunk = hd.div(w);
     x = static_cast<int>(static_cast<uint32_t>(w) - chunk * hkv) * kD;
     y = static_cast<int>(chunk) * kB;
   }
@@ -82,7 +102,7 @@ struct PrefillSource {
   };
   // Slot entries this thread checks for item w, loaded one item ahead of use.
   __device__ Check prepare(int64_t w, int gt) const {
-    const int64_t t0 = static_cast<int64_t>(static_cast<uint32_t>(w) / static_cast<uint32_t>(hkv)) * kB;
+    const int64_t t0 = static_cast<int64_t>(hd.div(w)) * kB;
     Check c;
     c.base = slot[t0];
     c.mine = slot[t0 + (gt & (kB - 1))];
@@ -93,7 +113,7 @@ struct PrefillSource {
   }
   // Record index of item w once the group agreed its slots are valid.
   __device__ int64_t target(int64_t w, const Check& c, int, unsigned*) const {
-    const uint32_t chunk = static_cast<uint32_t>(w) / static_cast<uint32_t>(hkv);
+    const uint32_t chunk = hd.div(w);
     return (c.base / kB) * hkv + (static_cast<uint32_t>(w) - chunk * hkv);
   }
 };
@@ -108,11 +128,12 @@ struct AppendSource {
   const int32_t* block_tables;  // [n_seqs][max_blocks]
   int64_t n_items;              // n_seqs * hkv
   int hkv;
+  ItemDiv hd;                   // division by hkv
   int max_blocks;
   int64_t num_blocks;
 
   __device__ bool needs_load(int64_t w) const {
-    const int L = seq_lens[static_cast<uint32_t>(w) / static_cast<uint32_t>(hkv)];
+    const int L = seq_lens[hd.div(w)];
     return L >= 0 && (L % kB) == kB - 1;
   }
   __device__ void coords(int64_t w, int g, int& x, int& y) const {
@@ -126,7 +147,7 @@ struct AppendSource {
   // of the tile.
   __device__ void scatter(int64_t w, int g, int t) const {
     if (t < 0 || t >= 16) return;
-    const uint32_t s = static_cast<uint32_t>(w) / static_cast<uint32_t>(hkv);
+    const uint32_t s = hd.div(w);
     const uint32_t h = static_cast<uint32_t>(w) - s * hkv;
     const int L = seq_lens[s];
     if (L < 0) return;
@@ -141,7 +162,7 @@ struct AppendSource {
   __device__ bool check_ok(const Check&, int) const { return true; }
   __device__ int64_t target(int64_t w, const Check&, int gt, unsigned* flags) const {
     if (!needs_load(w)) return -1;
-    const uint32_t s = static_cast<uint32_t>(w) / static_cast<uint32_t>(hkv);
+    const uint32_t s = hd.div(w);
     const uint32_t h = static_cast<uint32_t>(w) - s * hkv;
     const int bi = seq_lens[s] / kB;
     if (bi >= max_blocks) {
@@ -248,6 +269,28 @@ __global__ void __maxnreg__(128)
     const int buf = k & 1;
     const int64_t next = item + gridDim.x;
     const bool has_next = next < src.n_items;
+    bool ok = true;
+    if ((pend >> buf) & 1u) {
+      ok = mbar_wait(&load_bar[buf], (load_parity >> buf) & 1u, flags);
+      if (ok) {
+        load_parity ^= 1u << buf;
+        pend &= ~(1u << buf);
+      }
+    }
+    // the item's Hadamard products first, so the next item's bookkeeping below
+    // (slot loads, the next tile copy) runs under them
+    if (dst >= 0 && gt == 0 && ok) {
+      const uint32_t sx = smem_u32(tiles + buf * kTileOp);
+#pragma unroll
+      for (int s = 0; s < 8; ++s) {
+        const uint64_t dh = smem_desc_sw128(sw_kstep(sh, s));
+        const uint64_t dx = smem_desc_sw128(sw_kstep(sx, s));
+        umma_f16(d1, dh, dx, kIdesc, s > 0);   // D1[i][j] = sum_k H[i][k] X[j][k]
+        umma_f16(d2, dx, dh, kIdesc, s > 0);   // D2[j][i] = sum_k X[j][k] H[i][k]
+      }
+      umma_commit(&mma_bar[grp]);
+      mma_inflight = true;
+    }
     typename Src::Check check_next{};
     if (has_next) {
       if (src.needs_load(next)) {   // buffer buf ^ 1 was last read by the previous item
@@ -257,30 +300,8 @@ __global__ void __maxnreg__(128)
       check_next = src.prepare(next, gt);
       if (next + gridDim.x < src.n_items) src.scatter(next + gridDim.x, grp, gt);   // before this item's end barrier
     }
-    bool ok = true;
-    if ((pend >> buf) & 1u) {
-      ok = mbar_wait(&load_bar[buf], (load_parity >> buf) & 1u, flags);
-      if (ok) {
-        load_parity ^= 1u << buf;
-        pend &= ~(1u << buf);
-      }
-    }
     if (dst >= 0) {
       uint8_t* stage = smem + (grp == 0 ? S::kOffStageK + buf * S::kStageK : S::kOffStageV + buf * S::kStageV);
-      if (gt == 0) {
-        if (ok) {
-          const uint32_t sx = smem_u32(tiles + buf * kTileOp);
-#pragma unroll
-          for (int s = 0; s < 8; ++s) {
-            const uint64_t dh = smem_desc_sw128(sw_kstep(sh, s));
-            const uint64_t dx = smem_desc_sw128(sw_kstep(sx, s));
-            umma_f16(d1, dh, dx, kIdesc, s > 0);   // D1[i][j] = sum_k H[i][k] X[j][k]
-            umma_f16(d2, dx, dh, kIdesc, s > 0);   // D2[j][i] = sum_k X[j][k] H[i][k]
-          }
-          umma_commit(&mma_bar[grp]);
-          mma_inflight = true;
-        }
-      }
       if (gt == kStoreThread) bulk_wait_read<1>();   // the stage written two items ago has been stored
       if (ok) {
         ok = mbar_wait(&mma_bar[grp], mma_parity, flags);
@@ -421,6 +442,7 @@ cudaError_t launch_quantize_prefill(const uint16_t* k, const uint16_t* v, const 
   src.slot = slot;
   src.n_items = (n_tokens / kB) * hkv;
   src.hkv = hkv;
+  src.hd = make_item_div(static_cast<uint32_t>(hkv));
   src.num_blocks = num_blocks;
   return launch_quantize(src, cache, k_bits, v_bits, lean, n_iters, eps, flags, stream, max_ctas);
 }
@@ -442,6 +464,7 @@ cudaError_t launch_append(const uint16_t* k_new, const uint16_t* v_new, const in
   src.block_tables = block_tables;
   src.n_items = static_cast<int64_t>(n_seqs) * hkv;
   src.hkv = hkv;
+  src.hd = make_item_div(static_cast<uint32_t>(hkv));
   src.max_blocks = max_blocks;
   src.num_blocks = num_blocks;
   return launch_quantize(src, cache, k_bits, v_bits, lean, n_iters, eps, flags, stream, 0);
