@@ -225,6 +225,11 @@ KVARN_API kvarn_status kvarn_append_decode(const uint16_t* k_new, const uint16_t
  *                 KVARN_FLAG_BAD_LENGTH is set).
  *   out           fp16 [n_seqs][num_q_heads][128]; a sequence with L == 0 gets 0.
  *   scratch       device buffer of >= kvarn_decode_scratch_bytes(meta, n_seqs).
+ * Three kernels on the stream (a scan, the split phase, the merge); the last two
+ * are programmatic dependent launches of the kernel before them. With the
+ * environment variable KVARN_DECODE_SPLIT=tc (read on every call) the k4v2
+ * presets run their split phase on the tcgen05 kernel instead of the warp-level
+ * one (same results within the decode tolerance; measured slower).
  */
 KVARN_API kvarn_status kvarn_decode_attention(const uint16_t* q, const uint8_t* cache,
                                     const uint16_t* workspace, const int32_t* block_tables,
