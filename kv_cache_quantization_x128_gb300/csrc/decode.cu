@@ -87,6 +87,9 @@ __global__ void __launch_bounds__(1024) decode_scan_kernel(DecodeArgs a) {
     run += full_tiles(a, s);
   }
   if (t == 1023) a.prefix[a.n_seqs] = warp_sums[31];
+  // no unit has a first or last split warp yet (the split kernel marks them)
+  const int64_t n_cover = 2 * static_cast<int64_t>(a.n_seqs) * a.hkv;
+  for (int64_t i = t; i < n_cover; i += 1024) a.cover[i] = -1;
 }
 
 template <int KB, int VB, bool kLean>
@@ -134,12 +137,13 @@ cudaError_t launch_after(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t
 size_t decode_part_bytes(int n_seqs, int hkv, int max_blocks) {
   (void)max_blocks;
   const size_t records = static_cast<size_t>(kMaxCtas) * kMaxWarps + static_cast<size_t>(n_seqs) * hkv;
-  return prefix_bytes(n_seqs) + kRangeBytes + records * kRecFloats * sizeof(float) + kServeBarrierBytes;
+  return prefix_bytes(n_seqs) + kRangeBytes + records * kRecFloats * sizeof(float) + cover_bytes(n_seqs, hkv) +
+         kServeBarrierBytes;
 }
 
 size_t decode_scratch_bytes_for_ctas(int n_seqs, int hkv, int n_ctas) {
   const size_t records = static_cast<size_t>(n_ctas) * kMaxWarps + static_cast<size_t>(n_seqs) * hkv;
-  return prefix_bytes(n_seqs) + kRangeBytes + records * kRecFloats * sizeof(float);
+  return prefix_bytes(n_seqs) + kRangeBytes + records * kRecFloats * sizeof(float) + cover_bytes(n_seqs, hkv);
 }
 
 int decode_num_ctas() {
@@ -198,6 +202,7 @@ cudaError_t launch_decode(const uint16_t* q, const uint8_t* cache, const uint16_
   a.group = group;
   a.max_blocks = max_blocks;
   a.n_ctas = sms > 0 ? (sms < kMaxCtas ? sms : kMaxCtas) : 1;
+  a.cover = cover_ptr(a.part, n_seqs, hkv, a.n_ctas);
   const bool k4v2 = k_bits == 4 && v_bits == 2, k4v4 = k_bits == 4 && v_bits == 4, k2v2 = k_bits == 2 && v_bits == 2;
   if (!(k4v2 || ((k4v4 || k2v2) && !lean))) return cudaErrorInvalidValue;
   const bool tc = k4v2 && use_tc_split();

@@ -346,6 +346,7 @@ __device__ __forceinline__ void tc_team(const DecodeArgs& a, uint8_t* tsm, uint3
     if (u != unit) {
       if (unit >= 0) tc_flush(a, wg + unit, t, hh, jj, bar_id, pz, acc, lsum, mrun);
       unit = u;
+      if (t == 0 && cc.ti == 0) a.cover[2 * u] = static_cast<int32_t>(wg);   // the unit's first split team
       tc_load_q(a, cc.s, cc.h, hh, jj, qr);
 #pragma unroll
       for (int h = 0; h < 8; ++h) {
@@ -354,6 +355,7 @@ __device__ __forceinline__ void tc_team(const DecodeArgs& a, uint8_t* tsm, uint3
         mrun[h] = -INFINITY;
       }
     }
+    if (t == 0 && cc.ti == cc.nf - 1) a.cover[2 * u + 1] = static_cast<int32_t>(wg);   // and its last
     const int64_t blk = a.block_tables[static_cast<int64_t>(cc.s) * a.max_blocks + cc.ti];
     const bool valid = blk >= 0 && blk < a.num_blocks;
     ok = mbar_wait(&bars[kTcBarRec + stg], (rph >> stg) & 1u, a.flags) && ok;

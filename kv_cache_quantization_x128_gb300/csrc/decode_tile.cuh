@@ -39,6 +39,7 @@ struct DecodeArgs {
   int64_t* prefix;      // [n_seqs + 1] exclusive prefix of full tiles
   int64_t* ranges;      // [n_ctas * kWarps][2] tile range of each split-kernel warp
   float* part;          // [records][8][132]
+  int32_t* cover;       // [n_seqs * hkv][2]: first and last split warp of each unit (-1: none)
   unsigned* flags;
   int64_t num_blocks;
   int n_seqs;
@@ -61,20 +62,6 @@ __device__ __forceinline__ void warp_range(int64_t total, int n_ctas, int64_t wg
   const int64_t c0 = b * total / n_ctas, c1 = (b + 1) * total / n_ctas;
   beg = c0 + w * (c1 - c0) / kWarps;
   end = c0 + (w + 1) * (c1 - c0) / kWarps;
-}
-
-// First split warp whose range (warp_range, kw warps per CTA) ends after global
-// tile t0 (0 <= t0 < total): the inverse of warp_range by integer arithmetic,
-// corrected by at most a step or two each way.
-__device__ __forceinline__ int64_t first_covering_warp(int64_t t0, int64_t total, int64_t n_ctas, int64_t kw) {
-  int64_t b = t0 * n_ctas / total;
-  while (b > 0 && b * total / n_ctas > t0) --b;
-  while ((b + 1) * total / n_ctas <= t0) ++b;
-  const int64_t c0 = b * total / n_ctas, n = (b + 1) * total / n_ctas - c0;   // c0 <= t0 < c0 + n
-  int64_t w = (t0 - c0) * kw / n;
-  while (w > 0 && w * n / kw > t0 - c0) --w;
-  while ((w + 1) * n / kw <= t0 - c0) ++w;
-  return b * kw + w;
 }
 
 // ------------------------------------------------------------------ tile cursor
@@ -443,6 +430,7 @@ __device__ __forceinline__ void split_body(const DecodeArgs& a, uint8_t* smem, i
     if (u != unit) {
       if (unit >= 0) flush_record(a, wg + unit, g, c, m_run, l_run, acc);
       unit = u;
+      if (lane == 0 && cc.ti == 0) a.cover[2 * u] = static_cast<int32_t>(wg);   // the unit's first split warp
       load_q(a, cc.s, cc.h, g, c, qv);
       m_run = -INFINITY;
       l_run = 0.f;
@@ -455,6 +443,7 @@ __device__ __forceinline__ void split_body(const DecodeArgs& a, uint8_t* smem, i
       clean = false;
       break;
     }
+    if (lane == 0 && cc.ti == cc.nf - 1) a.cover[2 * u + 1] = static_cast<int32_t>(wg);   // and its last
     if ((valid >> stg) & 1u) attend_tile<KB, VB, kLean>(stages + stg * kRecBytes, qv, g, c, m_run, l_run, acc);
     __syncwarp();
     if (gb + k + kStages < ge) {     // refill this stage with the tile kStages ahead
@@ -490,20 +479,25 @@ __device__ __forceinline__ void merge_warp(const DecodeArgs& a, const uint16_t* 
   const int64_t u = static_cast<int64_t>(s) * a.hkv + h;
   const int64_t n_warps = static_cast<int64_t>(a.n_ctas) * a.warps;
 
-  // warps whose ranges cover this unit's tiles [t0, t1) (ranges are contiguous and
-  // ordered; empty ranges are skipped): the first from the range formula, the rest
-  // from the published ranges
+  // split warps whose ranges cover this unit's tiles: from the warp that took its
+  // first tile to the one that took its last, as the split phase recorded them
+  // (ranges are contiguous and ordered; an empty range in between left no record;
+  // a unit without both marks, after a timed-out split warp, merges no records)
   int64_t wlo = 0, whi = 0;
-  const int64_t t0 = a.prefix[s] * a.hkv + static_cast<int64_t>(h) * nf, t1 = t0 + nf;
   if (nf > 0) {
-    wlo = first_covering_warp(t0, a.prefix[a.n_seqs] * a.hkv, a.n_ctas, a.warps);
-    whi = wlo;
-    while (whi < n_warps && rg[2 * whi] < t1) ++whi;
+    const int2 cv = *reinterpret_cast<const int2*>(a.cover + 2 * u);
+    if (cv.x >= 0 && cv.y >= cv.x && cv.y < n_warps) {
+      wlo = cv.x;
+      whi = static_cast<int64_t>(cv.y) + 1;
+    }
   }
 
+  // the records' running maxima, lane i taking records wlo + i, wlo + i + 32, ...
   float M = -INFINITY;
-  for (int64_t w = wlo; w < whi; ++w)
+  for (int64_t w = wlo + lane; w < whi; w += 32)
     if (rg[2 * w] < rg[2 * w + 1]) M = fmaxf(M, a.part[(w + u) * kRecFloats + gg * kPartStride + 128]);
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
   // workspace tokens: exact fp16 K/V, unrotated
   const int64_t wbase = (static_cast<int64_t>(s) * a.hkv + h) * 2 * static_cast<int64_t>(kB * kD);
   const uint16_t* wk = ws ? ws + wbase : nullptr;
@@ -537,20 +531,45 @@ __device__ __forceinline__ void merge_warp(const DecodeArgs& a, const uint16_t* 
   }
   __syncwarp();
 
+  // records 32 at a time: lane i finds record w0 + i's weight f = 2^(max - M) and its
+  // share of the sum; then every lane adds each record's 4 channels times its f
+  // (records unrolled so that their loads are in flight together)
   float acc[4] = {0.f, 0.f, 0.f, 0.f}, wacc[4] = {0.f, 0.f, 0.f, 0.f};
   float l = 0.f;
-  for (int64_t w = wlo; w < whi; ++w) {
-    if (rg[2 * w] >= rg[2 * w + 1]) continue;
-    const float* pp = a.part + (w + u) * kRecFloats + gg * kPartStride;
-    const float mp = pp[128];
-    const float f = (mp == -INFINITY) ? 0.f : exp2f(mp - M);
-    l = fmaf(pp[129], f, l);
-    const float4 v = *reinterpret_cast<const float4*>(pp + 4 * lane);
-    acc[0] = fmaf(v.x, f, acc[0]);
-    acc[1] = fmaf(v.y, f, acc[1]);
-    acc[2] = fmaf(v.z, f, acc[2]);
-    acc[3] = fmaf(v.w, f, acc[3]);
+  for (int64_t w0 = wlo; w0 < whi; w0 += 32) {
+    const int64_t w = w0 + lane;
+    float f = 0.f;
+    if (w < whi && rg[2 * w] < rg[2 * w + 1]) {
+      const float* pp = a.part + (w + u) * kRecFloats + gg * kPartStride;
+      const float mp = pp[128];
+      f = (mp == -INFINITY) ? 0.f : exp2f(mp - M);
+      l = fmaf(pp[129], f, l);
+    }
+    const int cnt = static_cast<int>(min(static_cast<int64_t>(32), whi - w0));
+    for (int i0 = 0; i0 < cnt; i0 += 8) {
+      // eight records' loads first (an index past cnt reads record w0 again, inside
+      // the scratch; its weight is 0), then the sums; a record without data has
+      // weight 0 and is selected away, never multiplied
+      float4 v[8];
+      float fi[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        fi[j] = __shfl_sync(0xffffffffu, f, (i0 + j) & 31);
+        const int64_t wr = i0 + j < cnt ? w0 + i0 + j : w0;
+        v[j] = *reinterpret_cast<const float4*>(a.part + (wr + u) * kRecFloats + gg * kPartStride + 4 * lane);
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const bool use = i0 + j < cnt && fi[j] != 0.f;
+        acc[0] = fmaf(use ? v[j].x : 0.f, fi[j], acc[0]);
+        acc[1] = fmaf(use ? v[j].y : 0.f, fi[j], acc[1]);
+        acc[2] = fmaf(use ? v[j].z : 0.f, fi[j], acc[2]);
+        acc[3] = fmaf(use ? v[j].w : 0.f, fi[j], acc[3]);
+      }
+    }
   }
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
   // eight tokens at a time: their value rows and scores are loaded before the sums
   for (int tb = 0; tb < n_ws; tb += 8) {
     uint2 vv[8];
@@ -609,6 +628,12 @@ __device__ __forceinline__ void merge_body(const DecodeArgs& a, const uint16_t* 
 
 size_t prefix_bytes(int n_seqs) { return ((static_cast<size_t>(n_seqs) + 1) * sizeof(int64_t) + 255) & ~size_t(255); }
 constexpr size_t kRangeBytes = static_cast<size_t>(kMaxCtas) * kMaxWarps * 2 * sizeof(int64_t);
+// The units' first and last split warps, after the records of n_ctas CTAs.
+size_t cover_bytes(int n_seqs, int hkv) { return (static_cast<size_t>(n_seqs) * hkv * 2 * sizeof(int32_t) + 255) & ~size_t(255); }
+int32_t* cover_ptr(float* part, int n_seqs, int hkv, int n_ctas) {
+  const size_t records = static_cast<size_t>(n_ctas) * kMaxWarps + static_cast<size_t>(n_seqs) * hkv;
+  return reinterpret_cast<int32_t*>(part + records * kRecFloats);
+}
 
 }  // namespace
 }  // namespace kvarn

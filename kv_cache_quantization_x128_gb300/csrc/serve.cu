@@ -142,6 +142,9 @@ __device__ void serve_scan(const ServeArgs& sa, int64_t* part_sums) {
     run += min(max(len_after(sa, s), 0) / kB, a.max_blocks);
   }
   if (t == kServeThreads - 1) a.prefix[a.n_seqs] = part_sums[kServeThreads - 1];
+  // no unit has a first or last split warp yet (the split phase marks them)
+  const int64_t n_cover = 2 * static_cast<int64_t>(a.n_seqs) * a.hkv;
+  for (int64_t i = t; i < n_cover; i += kServeThreads) a.cover[i] = -1;
 }
 
 // Phase A for the items of this CTA.
@@ -435,6 +438,7 @@ cudaError_t launch_serve_step(const uint16_t* q, const uint16_t* k_new, const ui
   a.group = group;
   a.max_blocks = max_blocks;
   a.n_ctas = grid;
+  a.cover = cover_ptr(a.part, n_seqs, hkv, grid);
   sa.k_new = k_new;
   sa.v_new = v_new;
   sa.seq_lens_in = seq_lens;
