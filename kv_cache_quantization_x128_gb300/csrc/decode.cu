@@ -3,7 +3,8 @@
 // attention scores, so q is rotated by the same H and the output un-rotated).
 //
 // Three launches:
-//   decode_scan_kernel  - exclusive prefix of full tiles per sequence (scratch);
+//   decode_scan_kernel  - exclusive prefix of full tiles per sequence (scratch),
+//     and every unit's first / last split-warp marks reset to -1;
 //   decode_split_kernel - persistent, one CTA per SM, 8 warps (6 for 4-bit
 //     values). The flattened tile space (sequence, kv-head, tile) is cut into
 //     one contiguous range per warp (stream-K), so ragged batches balance to a
@@ -19,9 +20,10 @@
 //             acc_i += r^V_i (D_hi + D_lo + gamma), gamma = sum_j p_j c^V_j z^V_j.
 //     Four independent accumulator chains keep the MMA pipe busy. When a warp's
 //     range crosses into a new (sequence, kv-head) it writes a partial record
-//     (acc, running max, running sum) for the one it leaves;
+//     (acc, running max, running sum) for the one it leaves; the warp that takes a
+//     unit's first tile and the one that takes its last mark themselves;
 //   decode_merge_kernel - per (sequence, kv-head): merges the partial records of
-//     the warps that covered it with the fp16 workspace tokens of the partial
+//     the warps between those marks with the fp16 workspace tokens of the partial
 //     last tile, un-rotates by H^T and normalises.
 // decode_tc_split_kernel (decode_tc.cuh) is the split phase on tcgen05 for k4v2,
 // chosen with KVARN_DECODE_SPLIT=tc; it writes the same partial records. The split
