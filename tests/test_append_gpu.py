@@ -41,8 +41,9 @@ def gpu_append(env, k_new, v_new, lens, bt, ws, cache, num_blocks):
     return ws_d, cache_d, lens_out.cpu().numpy(), flags
 
 
-def test_append_small(env):
-    hkv, n_seqs, max_blocks = 2, 6, 4
+@pytest.mark.parametrize("hkv", [2, 3])
+def test_append_small(env, hkv):
+    n_seqs, max_blocks = 6, 4
     lens = np.array([0, 5, 126, 127, 255, 383], np.int32)
     num_blocks = n_seqs * max_blocks
     bt = synth.block_tables(n_seqs, max_blocks, num_blocks, seed=40)

@@ -71,9 +71,8 @@ def test_single_tile_decode(env):
     assert_decode_close(out, ref, "single tile")
 
 
-@pytest.mark.parametrize("group", [1, 2, 4, 8])
-def test_ragged_lengths_and_groups(env, group):
-    hkv = 2
+@pytest.mark.parametrize("group,hkv", [(1, 2), (2, 2), (4, 2), (8, 2), (8, 3), (3, 5)])
+def test_ragged_lengths_and_groups(env, group, hkv):
     lens = np.array([1, 127, 128, 129, 300, 640, 1000, 2047, 2300, 0], np.int32)
     cache, bt, ws, nb = oracle_cache(hkv, lens, seed=30 + group, max_blocks=19)
     q = synth.queries(len(lens), hkv * group, seed=31)

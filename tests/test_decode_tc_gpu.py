@@ -24,9 +24,9 @@ def test_single_tile(env, tc):
     D.test_single_tile_decode(env)
 
 
-@pytest.mark.parametrize("group", [1, 2, 4, 8])
-def test_ragged_lengths_and_groups(env, tc, group):
-    D.test_ragged_lengths_and_groups(env, group)
+@pytest.mark.parametrize("group,hkv", [(1, 2), (2, 2), (4, 2), (8, 2), (8, 3), (3, 5)])
+def test_ragged_lengths_and_groups(env, tc, group, hkv):
+    D.test_ragged_lengths_and_groups(env, group, hkv)
 
 
 def test_64x16k_sampled(env, tc):

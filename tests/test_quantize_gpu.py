@@ -48,8 +48,11 @@ def test_single_tile(env):
     assert not cache[0].any()
 
 
-def test_multi_tile_random_slots(env):
-    hkv, n_chunks, num_blocks = 8, 40, 48
+@pytest.mark.parametrize("hkv", [8, 3, 5])
+def test_multi_tile_random_slots(env, hkv):
+    """40 chunks into 48 blocks in random order; 3 and 5 kv-heads split the item
+    index by a divisor that is not a power of two."""
+    n_chunks, num_blocks = 40, 48
     k, v = synth.prefill_kv(n_chunks * 128, hkv, seed=21)
     slots = synth.prefill_slot_mapping(n_chunks * 128, num_blocks, seed=21)
     cache, flags = run_prefill(env, k, v, slots, num_blocks)
