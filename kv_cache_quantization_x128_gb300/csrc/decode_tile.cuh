@@ -461,6 +461,20 @@ __device__ __forceinline__ void split_body(const DecodeArgs& a, uint8_t* smem, i
 }
 
 // ------------------------------------------------------------------ merge
+// One level of a transposed warp reduction: lanes whose bit `o` is clear keep sums
+// d[0, kHalf) and those whose bit is set keep d[kHalf, 2 kHalf) (moved to d[0, kHalf)),
+// each adding the partner lane's share of the sums it keeps.
+template <int kHalf>
+__device__ __forceinline__ void transpose_sum(float (&d)[16], int lane, int o) {
+  const bool upper = (lane & o) != 0;
+#pragma unroll
+  for (int i = 0; i < kHalf; ++i) {
+    const float send = upper ? d[i] : d[i + kHalf];
+    const float keep = upper ? d[i + kHalf] : d[i];
+    d[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+  }
+}
+
 // Q-head gg of unit (kv-head h, sequence s), one warp: lane l owns channels
 // 4l..4l+3; scw is the warp's 128 floats of shared memory for workspace scores; rg
 // the split warps' tile ranges (a.ranges, or a copy of it in shared memory).
@@ -518,17 +532,23 @@ __device__ __forceinline__ void merge_warp(const DecodeArgs& a, const uint16_t* 
         d[j] = fmaf(qf[3], k23.y, fmaf(qf[2], k23.x, fmaf(qf[1], k01.y, qf[0] * k01.x)));
       }
     }
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1)
-#pragma unroll
-      for (int j = 0; j < 16; ++j) d[j] += __shfl_xor_sync(0xffffffffu, d[j], o);
-#pragma unroll
-    for (int j = 0; j < 16; ++j)
-      if (tb + j < n_ws) {
-        if (lane == 0) scw[tb + j] = d[j];
-        M = fmaxf(M, d[j]);
-      }
+    // transposed reduction over the warp: at each level a lane keeps half of its
+    // sums (the half its lane bit selects) and adds its partner's share of them, so
+    // 16 sums take 16 shuffles instead of 80; lanes l and l ^ 1 end with the sum of
+    // token 8 b4 + 4 b3 + 2 b2 + b1 (b = bits of l)
+    transpose_sum<8>(d, lane, 16);
+    transpose_sum<4>(d, lane, 8);
+    transpose_sum<2>(d, lane, 4);
+    transpose_sum<1>(d, lane, 2);
+    d[0] += __shfl_xor_sync(0xffffffffu, d[0], 1);
+    const int tok = tb + ((lane >> 1) & 15);
+    if (tok < n_ws) {
+      if ((lane & 1) == 0) scw[tok] = d[0];
+      M = fmaxf(M, d[0]);
+    }
   }
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
   __syncwarp();
 
   // records 32 at a time: lane i finds record w0 + i's weight f = 2^(max - M) and its
