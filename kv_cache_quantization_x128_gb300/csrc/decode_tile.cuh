@@ -519,18 +519,20 @@ __device__ __forceinline__ void merge_warp(const DecodeArgs& a, const uint16_t* 
   float qf[4];
 #pragma unroll
   for (int k = 0; k < 4; ++k) qf[k] = h2f_bits(a.q[qrow + 4 * lane + k]) * (kLog2e * kInvSqrt128);
-  // sixteen tokens at a time: independent dot products and shuffle trees in flight
+  // sixteen tokens at a time: their rows are loaded together (rows past n_ws, still
+  // inside the unit's 128 workspace rows, are read and not used), then independent
+  // dot products and one transposed reduction
   for (int tb = 0; tb < n_ws; tb += 16) {
+    uint2 kw[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) kw[j] = *reinterpret_cast<const uint2*>(wk + (tb + j) * kD + 4 * lane);
     float d[16];
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
-      d[j] = 0.f;
-      if (tb + j < n_ws) {
-        const uint2 kw = *reinterpret_cast<const uint2*>(wk + (tb + j) * kD + 4 * lane);
-        const float2 k01 = h2pair(reinterpret_cast<const uint16_t*>(&kw.x));
-        const float2 k23 = h2pair(reinterpret_cast<const uint16_t*>(&kw.y));
-        d[j] = fmaf(qf[3], k23.y, fmaf(qf[2], k23.x, fmaf(qf[1], k01.y, qf[0] * k01.x)));
-      }
+      const float2 k01 = h2pair(reinterpret_cast<const uint16_t*>(&kw[j].x));
+      const float2 k23 = h2pair(reinterpret_cast<const uint16_t*>(&kw[j].y));
+      const float dj = fmaf(qf[3], k23.y, fmaf(qf[2], k23.x, fmaf(qf[1], k01.y, qf[0] * k01.x)));
+      d[j] = tb + j < n_ws ? dj : 0.f;
     }
     // transposed reduction over the warp: at each level a lane keeps half of its
     // sums (the half its lane bit selects) and adds its partner's share of them, so
@@ -551,6 +553,12 @@ __device__ __forceinline__ void merge_warp(const DecodeArgs& a, const uint16_t* 
   for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
   __syncwarp();
 
+  // the first sixteen value rows start loading under the records' merge
+  uint2 vv[16];
+  if (n_ws > 0) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) vv[j] = *reinterpret_cast<const uint2*>(wv + j * kD + 4 * lane);
+  }
   // records 32 at a time: lane i finds record w0 + i's weight f = 2^(max - M) and its
   // share of the sum; then every lane adds each record's 4 channels times its f
   // (records unrolled so that their loads are in flight together)
@@ -590,20 +598,17 @@ __device__ __forceinline__ void merge_warp(const DecodeArgs& a, const uint16_t* 
   }
 #pragma unroll
   for (int o = 16; o >= 1; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
-  // eight tokens at a time: their value rows and scores are loaded before the sums
-  for (int tb = 0; tb < n_ws; tb += 8) {
-    uint2 vv[8];
-    float sv[8];
+  // sixteen value rows at a time (the first batch already loaded; rows past n_ws
+  // inside the unit's 128 are read and not used)
+  for (int tb = 0; tb < n_ws; tb += 16) {
+    if (tb > 0) {
 #pragma unroll
-    for (int j = 0; j < 8; ++j)
-      if (tb + j < n_ws) {
-        vv[j] = *reinterpret_cast<const uint2*>(wv + (tb + j) * kD + 4 * lane);
-        sv[j] = scw[tb + j];
-      }
+      for (int j = 0; j < 16; ++j) vv[j] = *reinterpret_cast<const uint2*>(wv + (tb + j) * kD + 4 * lane);
+    }
 #pragma unroll
-    for (int j = 0; j < 8; ++j)
+    for (int j = 0; j < 16; ++j)
       if (tb + j < n_ws) {
-        const float pw = exp2f(sv[j] - M);
+        const float pw = exp2f(scw[tb + j] - M);
         l += pw;
         const float2 v01 = h2pair(reinterpret_cast<const uint16_t*>(&vv[j].x));
         const float2 v23 = h2pair(reinterpret_cast<const uint16_t*>(&vv[j].y));
