@@ -662,6 +662,103 @@ def run_prefill_attn(args):
                       "prefill_tokens_per_s": round(n / (ms * 1e-3))}), flush=True)
 
 
+# `--case serve`: the mixed serving step (not the headline line): 256 sequences with
+# lengths log-uniform in [1024, 32768] and a partial last tile each (every 8th at
+# L % 128 == 127, so that the append completes 33 tiles), 64 q-heads over 8 kv-heads,
+# k4v2, random valid records in the cache and fp16 tokens in the workspace. One step
+# appends a token to every sequence and decodes over the result; the append is
+# idempotent on the same inputs, so steps repeat without a reset. L2 is flushed
+# before every timed call.
+SERVE = "serve_256_ragged"
+
+
+def run_serve(args):
+    import numpy as np
+    import torch
+    import kvarn_synth as synth
+    import kv_cache_quantization_x128_gb300 as kv
+    torch.cuda.set_device(0)
+    cfg = synth.WORKLOADS[SERVE]
+    n_seqs, hkv, hq, seed = cfg["n_seqs"], cfg["n_kv_heads"], cfg["n_q_heads"], cfg["seed"]
+    lens = synth.ragged_lengths(n_seqs, cfg["lo"], cfg["hi"], seed)
+    lens[::8] = (lens[::8] // 128) * 128 + 127
+    max_blocks = int(max((L + 1 + 127) // 128 for L in lens))
+    num_blocks = int(((lens + 1 + 127) // 128).sum()) + 16
+    perm = synth.block_permutation(num_blocks, seed)
+    bt = np.full((n_seqs, max_blocks), -1, np.int32)
+    pos = 0
+    for i in range(n_seqs):
+        nb = (lens[i] + 1 + 127) // 128
+        bt[i, :nb] = perm[pos:pos + nb]
+        pos += nb
+    recs = synth.random_records(num_blocks * hkv, seed, RECORD, 12288).reshape(num_blocks, hkv, -1)
+    f16 = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.float16).cuda()
+    k_new, v_new = synth.prefill_kv(n_seqs, hkv, seed=seed + 1)
+    ws, cache = f16(synth.workspace_tokens(n_seqs, hkv, seed)), torch.from_numpy(recs).cuda()
+    lens_d, bt_d = torch.from_numpy(lens).cuda(), torch.from_numpy(bt).cuda()
+    q, kn, vn = f16(synth.queries(n_seqs, hq, seed)), f16(k_new), f16(v_new)
+    lens_out = torch.empty((n_seqs,), dtype=torch.int32, device="cuda")
+    out = torch.empty((n_seqs, hq, 128), dtype=torch.float16, device="cuda")
+    meta = kv.make_meta(hkv, hq, num_blocks, max_blocks_per_seq=max_blocks)
+    scratch = torch.empty(kv.decode_scratch_bytes(meta, n_seqs), dtype=torch.uint8, device="cuda")
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+
+    def append():
+        kv.kvarn_append_decode(kn, vn, lens_d, lens_out, bt_d, ws, cache, meta)
+
+    def decode():
+        kv.kvarn_decode_attention(q, cache, ws, bt_d, lens_out, out, scratch, meta)
+
+    def two():
+        append()
+        decode()
+
+    def fused():
+        kv.kvarn_serve_step(q, kn, vn, lens_d, lens_out, bt_d, ws, cache, out, scratch, meta)
+
+    def timed(fn):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(args.steps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        return float(np.median(ts))
+
+    two()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        two()
+    res = {"graph": timed(graph.replay), "two_calls": timed(two), "append": timed(append),
+           "decode": timed(decode), "fused": timed(fused)}
+    if kv.kvarn_device_flags() != 0:
+        raise SystemExit("the serving step raised a device flag")
+    peak, peak_kind = hbm_peak()
+    tiles = int(sum((L + 1) // 128 for L in lens)) * hkv          # full tiles the decode reads
+    decode_gbs = tiles * RECORD / (res["decode"] * 1e-3) / 1e9
+    ms = res["graph"]
+    print(json.dumps({"metric": "serving_step_sequences_per_s", "value": round(n_seqs / (ms * 1e-3)),
+                      "unit": "sequences/s", "ms_per_step": round(ms, 4), "steps": args.steps,
+                      "warmup": args.warmup, "higher_is_better": True,
+                      "dtype": "f32 statistics and accumulation on fp16 inputs", "data": "synthetic",
+                      "config": {"workload": f"{SERVE}: 256 sequences, lengths log-uniform 1024-32768, "
+                                             "gqa64/8, one token appended and decoded",
+                                 "preset": "kvarn_k4v2_g128", "l2": "flushed", "step": "append + decode "
+                                 "captured in one CUDA graph"},
+                      "append_us": round(res["append"] * 1e3, 1), "decode_us": round(res["decode"] * 1e3, 1),
+                      "two_calls_eager_us": round(res["two_calls"] * 1e3, 1),
+                      "graph_us": round(res["graph"] * 1e3, 1), "serve_step_one_launch_us": round(res["fused"] * 1e3, 1),
+                      "decode_gbs": round(decode_gbs, 1), "decode_frac_hbm": round(decode_gbs / peak, 4),
+                      "peak_kind": peak_kind, "decode_bytes": tiles * RECORD}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -670,9 +767,10 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--case", default="full", choices=["full", "small", "prefill_attn"],
+    ap.add_argument("--case", default="full", choices=["full", "small", "prefill_attn", "serve"],
                     help="small: reduced shapes for profiler captures (not a bench line); "
-                         "prefill_attn: the chunked-prefill attention kernel alone")
+                         "prefill_attn: the chunked-prefill attention kernel alone; "
+                         "serve: the 256-sequence serving step (append + decode)")
     ap.add_argument("--preset", default="k4v2", choices=sorted(PRESET_RECORD),
                     help="bit preset of the gb300 arm; the default k4v2 is the headline workload")
     args = ap.parse_args()
@@ -688,6 +786,8 @@ def main():
         ap.error("--warmup must be >= 3")
     if args.case == "prefill_attn":
         run_prefill_attn(args)
+    elif args.case == "serve":
+        run_serve(args)
     elif args.impl == "reference":
         run_reference(args)
     else:

@@ -112,9 +112,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_split_kernel(DecodeAr
 // One CTA per (kv-head, sequence).
 __global__ void __launch_bounds__(256) decode_merge_kernel(DecodeArgs a, const uint16_t* __restrict__ ws,
                                                            uint16_t* __restrict__ out) {
-  __shared__ float sc[8][128];
+  __shared__ WsPart sm;
   griddep_wait();                       // the split kernel's ranges and partial records
-  merge_body(a, ws, out, blockIdx.x, blockIdx.y, sc);
+  merge_body(a, ws, out, blockIdx.x, blockIdx.y, sm, a.ranges);
 }
 
 // Launch with programmatic stream serialization (see griddep_wait).

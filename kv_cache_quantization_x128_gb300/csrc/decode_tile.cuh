@@ -461,34 +461,143 @@ __device__ __forceinline__ void split_body(const DecodeArgs& a, uint8_t* smem, i
 }
 
 // ------------------------------------------------------------------ merge
-// One level of a transposed warp reduction: lanes whose bit `o` is clear keep sums
-// d[0, kHalf) and those whose bit is set keep d[kHalf, 2 kHalf) (moved to d[0, kHalf)),
-// each adding the partner lane's share of the sums it keeps.
-template <int kHalf>
-__device__ __forceinline__ void transpose_sum(float (&d)[16], int lane, int o) {
-  const bool upper = (lane & o) != 0;
+// The fp16 workspace tokens of a unit (exact, unrotated K and V rows of its partial
+// last tile) are attended by the unit's 8 warps together, warp w taking tokens
+// 16w .. 16w + 15 for all q-heads of the group at once with m16n8k16 MMAs; each
+// warp leaves per head its running max, sum and 128-channel output in shared
+// memory, and the records' merge then folds them in.
+struct WsPart {
+  float o[8][8][128];   // [warp][q-head][channel]
+  float m[8][8];        // [warp][q-head] max of the warp's scores (log2 domain)
+  float l[8][8];        // [warp][q-head] sum of 2^(score - max)
+};
+
+// Workspace tokens of sequence s: L % 128, or none (flag raised) without a workspace.
+__device__ __forceinline__ int ws_tokens(const DecodeArgs& a, const uint16_t* ws, int s, bool report) {
+  const int n_ws = max(a.seq_lens[s], 0) % kB;
+  if (n_ws > 0 && ws == nullptr) {   // tail tokens without a workspace: attend the tiles only
+    if (report) raise_flag(a.flags, KVARN_FLAG_BAD_LENGTH);
+    return 0;
+  }
+  return n_ws;
+}
+
+// Warp w's share of the workspace tokens of unit (kv-head h, sequence s). Thread
+// (g, c) = (lane / 4, lane % 4). The MMAs' K index is permuted the same way in both
+// operands so that every load is 16 bytes: in k-step ks the fragment's positions
+// 2c, 2c+1 carry channels 32c + 4ks + {0, 1} and 2c+8, 2c+9 channels 32c + 4ks + {2, 3}.
+// S = q K^T: A = q (rows 0-7 the group's heads, exact fp16; rows 8-15 zero), B = the
+// K rows of tokens 16w + 8nt + g. PV: A = p as fp16 hi (rows 0-7) and lo (rows 8-15),
+// K index = the warp's 16 tokens in the S accumulators' order; B = the V rows, n-tile
+// j's column g being channel 16g + j, so each thread loads 32 contiguous bytes of
+// each of its four tokens.
+__device__ __forceinline__ void merge_ws_part(const DecodeArgs& a, const uint16_t* __restrict__ ws, int h, int s,
+                                              int n_ws, int w, WsPart& sm) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
+  const int t0 = 16 * w;
+  if (t0 >= n_ws) return;
+  const int64_t wbase = (static_cast<int64_t>(s) * a.hkv + h) * 2 * static_cast<int64_t>(kB * kD);
+  const uint16_t* wk = ws + wbase;
+  const uint16_t* wv = ws + wbase + kB * kD;
+
+  // q fragments of head g (zero for heads past the group)
+  uint32_t qa[8][2];
+  if (g < a.group) {
+    const uint4* qr = reinterpret_cast<const uint4*>(
+        a.q + ((static_cast<int64_t>(s) * a.hkv + h) * a.group + g) * kD + 32 * c);
 #pragma unroll
-  for (int i = 0; i < kHalf; ++i) {
-    const float send = upper ? d[i] : d[i + kHalf];
-    const float keep = upper ? d[i + kHalf] : d[i];
-    d[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+    for (int j = 0; j < 4; ++j) {
+      const uint4 v = qr[j];
+      qa[2 * j][0] = v.x; qa[2 * j][1] = v.y; qa[2 * j + 1][0] = v.z; qa[2 * j + 1][1] = v.w;
+    }
+  } else {
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) qa[ks][0] = qa[ks][1] = 0u;
+  }
+  // scores: tokens t0 + 8nt + 2c + {0, 1} of head g (rows past n_ws, still inside the
+  // unit's 128 workspace rows, are read and masked out)
+  float d[2][4];
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt) {
+    const uint4* kr = reinterpret_cast<const uint4*>(wk + (t0 + 8 * nt + g) * kD + 32 * c);
+    uint4 kv4[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) kv4[j] = kr[j];
+    d[nt][0] = d[nt][1] = d[nt][2] = d[nt][3] = 0.f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t a0[4] = {qa[2 * j][0], 0u, qa[2 * j][1], 0u};
+      const uint32_t a1[4] = {qa[2 * j + 1][0], 0u, qa[2 * j + 1][1], 0u};
+      mma16816(d[nt], a0, kv4[j].x, kv4[j].y);
+      mma16816(d[nt], a1, kv4[j].z, kv4[j].w);
+    }
+  }
+  constexpr float kScale = kLog2e * kInvSqrt128;
+  float sc[2][2];
+  float mx = -INFINITY;
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      sc[nt][e] = (t0 + 8 * nt + 2 * c + e < n_ws) ? d[nt][e] * kScale : -INFINITY;
+      mx = fmaxf(mx, sc[nt][e]);
+    }
+  mx = quad_max(mx);   // finite: token t0 is valid
+  float lsum = 0.f;
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      sc[nt][e] = exp2f(sc[nt][e] - mx);   // 0 for the masked tokens
+      lsum += sc[nt][e];
+    }
+  lsum = quad_sum(lsum);
+  uint32_t pa[4];
+  split2p(make_float2(sc[0][0], sc[0][1]), pa[0], pa[1]);
+  split2p(make_float2(sc[1][0], sc[1][1]), pa[2], pa[3]);
+
+  // PV in two halves of eight n-tiles (channels 16g + 8hf .. 16g + 8hf + 7)
+  const int tk[4] = {t0 + 2 * c, t0 + 2 * c + 1, t0 + 2 * c + 8, t0 + 2 * c + 9};
+  float* orow = &sm.o[w][g][0];
+#pragma unroll
+  for (int hf = 0; hf < 2; ++hf) {
+    uint4 vr[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)   // masked tokens contribute zero (their rows are never multiplied)
+      vr[i] = tk[i] < n_ws ? *reinterpret_cast<const uint4*>(wv + tk[i] * kD + 16 * g + 8 * hf)
+                           : make_uint4(0u, 0u, 0u, 0u);
+    float o[8][4];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const uint32_t w01 = (&vr[0].x)[j >> 1], w1 = (&vr[1].x)[j >> 1];
+      const uint32_t w8 = (&vr[2].x)[j >> 1], w9 = (&vr[3].x)[j >> 1];
+      const uint32_t sel = (j & 1) ? 0x7632u : 0x5410u;   // high or low halves of both words
+      const uint32_t b0 = __byte_perm(w01, w1, sel), b1 = __byte_perm(w8, w9, sel);
+      o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+      mma16816(o[j], pa, b0, b1);
+    }
+    // column 2c of n-tile j is channel 16(2c) + 8hf + j, column 2c + 1 channel 16(2c+1) + 8hf + j;
+    // rows g (hi) and g + 8 (lo) add up to head g
+    float4* o0 = reinterpret_cast<float4*>(orow + 32 * c + 8 * hf);
+    float4* o1 = reinterpret_cast<float4*>(orow + 32 * c + 16 + 8 * hf);
+    o0[0] = make_float4(o[0][0] + o[0][2], o[1][0] + o[1][2], o[2][0] + o[2][2], o[3][0] + o[3][2]);
+    o0[1] = make_float4(o[4][0] + o[4][2], o[5][0] + o[5][2], o[6][0] + o[6][2], o[7][0] + o[7][2]);
+    o1[0] = make_float4(o[0][1] + o[0][3], o[1][1] + o[1][3], o[2][1] + o[2][3], o[3][1] + o[3][3]);
+    o1[1] = make_float4(o[4][1] + o[4][3], o[5][1] + o[5][3], o[6][1] + o[6][3], o[7][1] + o[7][3]);
+  }
+  if (c == 0) {
+    sm.m[w][g] = mx;
+    sm.l[w][g] = lsum;
   }
 }
 
-// Q-head gg of unit (kv-head h, sequence s), one warp: lane l owns channels
-// 4l..4l+3; scw is the warp's 128 floats of shared memory for workspace scores; rg
-// the split warps' tile ranges (a.ranges, or a copy of it in shared memory).
-__device__ __forceinline__ void merge_warp(const DecodeArgs& a, const uint16_t* __restrict__ ws,
-                                           uint16_t* __restrict__ out, int h, int s, int gg, float* scw,
-                                           const int64_t* rg) {
+// Q-head gg of unit (kv-head h, sequence s), one warp, after merge_ws_part of the
+// unit's warps: lane l owns channels 4l..4l+3; rg the split warps' tile ranges
+// (a.ranges, or a copy of it in shared memory).
+__device__ __forceinline__ void merge_warp(const DecodeArgs& a, uint16_t* __restrict__ out, int h, int s, int gg,
+                                           int n_ws, const WsPart& sm, const int64_t* rg) {
   const int lane = threadIdx.x & 31;
-  const int L = max(a.seq_lens[s], 0);
   const int nf = full_tiles(a, s);
-  int n_ws = L % kB;
-  if (n_ws > 0 && ws == nullptr) {  // tail tokens without a workspace: attend the tiles only
-    n_ws = 0;
-    if (lane == 0) raise_flag(a.flags, KVARN_FLAG_BAD_LENGTH);
-  }
   const int64_t qrow = (static_cast<int64_t>(s) * a.hkv * a.group + static_cast<int64_t>(h) * a.group + gg) * kD;
   const int64_t u = static_cast<int64_t>(s) * a.hkv + h;
   const int64_t n_warps = static_cast<int64_t>(a.n_ctas) * a.warps;
@@ -506,64 +615,31 @@ __device__ __forceinline__ void merge_warp(const DecodeArgs& a, const uint16_t* 
     }
   }
 
-  // the records' running maxima, lane i taking records wlo + i, wlo + i + 32, ...
-  float M = -INFINITY;
+  // the records' running maxima, lane i taking records wlo + i, wlo + i + 32, ...,
+  // and the workspace warps' maxima
+  const int n_wsw = (n_ws + 15) >> 4;
+  float M = lane < n_wsw ? sm.m[lane][gg] : -INFINITY;
   for (int64_t w = wlo + lane; w < whi; w += 32)
     if (rg[2 * w] < rg[2 * w + 1]) M = fmaxf(M, a.part[(w + u) * kRecFloats + gg * kPartStride + 128]);
 #pragma unroll
   for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-  // workspace tokens: exact fp16 K/V, unrotated
-  const int64_t wbase = (static_cast<int64_t>(s) * a.hkv + h) * 2 * static_cast<int64_t>(kB * kD);
-  const uint16_t* wk = ws ? ws + wbase : nullptr;
-  const uint16_t* wv = ws ? ws + wbase + kB * kD : nullptr;
-  float qf[4];
-#pragma unroll
-  for (int k = 0; k < 4; ++k) qf[k] = h2f_bits(a.q[qrow + 4 * lane + k]) * (kLog2e * kInvSqrt128);
-  // sixteen tokens at a time: their rows are loaded together (rows past n_ws, still
-  // inside the unit's 128 workspace rows, are read and not used), then independent
-  // dot products and one transposed reduction
-  for (int tb = 0; tb < n_ws; tb += 16) {
-    uint2 kw[16];
-#pragma unroll
-    for (int j = 0; j < 16; ++j) kw[j] = *reinterpret_cast<const uint2*>(wk + (tb + j) * kD + 4 * lane);
-    float d[16];
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const float2 k01 = h2pair(reinterpret_cast<const uint16_t*>(&kw[j].x));
-      const float2 k23 = h2pair(reinterpret_cast<const uint16_t*>(&kw[j].y));
-      const float dj = fmaf(qf[3], k23.y, fmaf(qf[2], k23.x, fmaf(qf[1], k01.y, qf[0] * k01.x)));
-      d[j] = tb + j < n_ws ? dj : 0.f;
-    }
-    // transposed reduction over the warp: at each level a lane keeps half of its
-    // sums (the half its lane bit selects) and adds its partner's share of them, so
-    // 16 sums take 16 shuffles instead of 80; lanes l and l ^ 1 end with the sum of
-    // token 8 b4 + 4 b3 + 2 b2 + b1 (b = bits of l)
-    transpose_sum<8>(d, lane, 16);
-    transpose_sum<4>(d, lane, 8);
-    transpose_sum<2>(d, lane, 4);
-    transpose_sum<1>(d, lane, 2);
-    d[0] += __shfl_xor_sync(0xffffffffu, d[0], 1);
-    const int tok = tb + ((lane >> 1) & 15);
-    if (tok < n_ws) {
-      if ((lane & 1) == 0) scw[tok] = d[0];
-      M = fmaxf(M, d[0]);
-    }
-  }
-#pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-  __syncwarp();
 
-  // the first sixteen value rows start loading under the records' merge
-  uint2 vv[16];
-  if (n_ws > 0) {
-#pragma unroll
-    for (int j = 0; j < 16; ++j) vv[j] = *reinterpret_cast<const uint2*>(wv + j * kD + 4 * lane);
+  // workspace warps' outputs (unrotated) with their weights 2^(max - M)
+  float wacc[4] = {0.f, 0.f, 0.f, 0.f};
+  float l = 0.f;
+  for (int w = 0; w < n_wsw; ++w) {
+    const float f = exp2f(sm.m[w][gg] - M);
+    const float4 v = *reinterpret_cast<const float4*>(&sm.o[w][gg][4 * lane]);
+    wacc[0] = fmaf(v.x, f, wacc[0]);
+    wacc[1] = fmaf(v.y, f, wacc[1]);
+    wacc[2] = fmaf(v.z, f, wacc[2]);
+    wacc[3] = fmaf(v.w, f, wacc[3]);
+    if (lane == 0) l = fmaf(sm.l[w][gg], f, l);
   }
   // records 32 at a time: lane i finds record w0 + i's weight f = 2^(max - M) and its
   // share of the sum; then every lane adds each record's 4 channels times its f
   // (records unrolled so that their loads are in flight together)
-  float acc[4] = {0.f, 0.f, 0.f, 0.f}, wacc[4] = {0.f, 0.f, 0.f, 0.f};
-  float l = 0.f;
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
   for (int64_t w0 = wlo; w0 < whi; w0 += 32) {
     const int64_t w = w0 + lane;
     float f = 0.f;
@@ -598,26 +674,6 @@ __device__ __forceinline__ void merge_warp(const DecodeArgs& a, const uint16_t* 
   }
 #pragma unroll
   for (int o = 16; o >= 1; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
-  // sixteen value rows at a time (the first batch already loaded; rows past n_ws
-  // inside the unit's 128 are read and not used)
-  for (int tb = 0; tb < n_ws; tb += 16) {
-    if (tb > 0) {
-#pragma unroll
-      for (int j = 0; j < 16; ++j) vv[j] = *reinterpret_cast<const uint2*>(wv + (tb + j) * kD + 4 * lane);
-    }
-#pragma unroll
-    for (int j = 0; j < 16; ++j)
-      if (tb + j < n_ws) {
-        const float pw = exp2f(scw[tb + j] - M);
-        l += pw;
-        const float2 v01 = h2pair(reinterpret_cast<const uint16_t*>(&vv[j].x));
-        const float2 v23 = h2pair(reinterpret_cast<const uint16_t*>(&vv[j].y));
-        wacc[0] = fmaf(pw, v01.x, wacc[0]);
-        wacc[1] = fmaf(pw, v01.y, wacc[1]);
-        wacc[2] = fmaf(pw, v23.x, wacc[2]);
-        wacc[3] = fmaf(pw, v23.y, wacc[3]);
-      }
-  }
   // un-rotate: FWHT over the 128 channels (4 per lane), then scale by 1/sqrt(128)
   {
     const float a0 = acc[0] + acc[1], a1 = acc[0] - acc[1], a2 = acc[2] + acc[3], a3 = acc[2] - acc[3];
@@ -643,12 +699,16 @@ __device__ __forceinline__ void merge_warp(const DecodeArgs& a, const uint16_t* 
       make_uint2(res[0] | (static_cast<uint32_t>(res[1]) << 16), res[2] | (static_cast<uint32_t>(res[3]) << 16));
 }
 
-// Unit (kv-head h, sequence s) with 8 warps, one per q-head of the group; sc is
-// [8][128] floats of shared memory.
+// Unit (kv-head h, sequence s) with the block's 8 warps: the workspace part, then one
+// warp per q-head of the group; sm is the block's shared WsPart.
 __device__ __forceinline__ void merge_body(const DecodeArgs& a, const uint16_t* __restrict__ ws,
-                                           uint16_t* __restrict__ out, int h, int s, float (*sc)[128]) {
+                                           uint16_t* __restrict__ out, int h, int s, WsPart& sm,
+                                           const int64_t* rg) {
   const int warp = threadIdx.x >> 5;
-  if (warp < a.group) merge_warp(a, ws, out, h, s, warp, sc[warp], a.ranges);
+  const int n_ws = ws_tokens(a, ws, s, threadIdx.x == 0);
+  merge_ws_part(a, ws, h, s, n_ws, warp, sm);
+  __syncthreads();
+  if (warp < a.group) merge_warp(a, out, h, s, warp, n_ws, sm, rg);
 }
 
 size_t prefix_bytes(int n_seqs) { return ((static_cast<size_t>(n_seqs) + 1) * sizeof(int64_t) + 255) & ~size_t(255); }

@@ -66,7 +66,7 @@ struct ServeSmem {
   static constexpr int kOffList = kOffListN + 16;                   // int32 [kListCap] item indices
   static constexpr int kAppendBytes = kOffList + kListCap * 4;
   static constexpr int kSplitBytes = SplitCfg<KB, VB, kLean>::kSmem;
-  static constexpr int kMergeBytes = 8 * 128 * 4 + kMaxCtas * kMaxWarps * 2 * 8;   // scores, range copy
+  static constexpr int kMergeBytes = static_cast<int>(sizeof(WsPart)) + kMaxCtas * kMaxWarps * 2 * 8;   // workspace part, range copy
   static constexpr int kBytes = kAppendBytes > kSplitBytes ? (kAppendBytes > kMergeBytes ? kAppendBytes : kMergeBytes)
                                                            : (kSplitBytes > kMergeBytes ? kSplitBytes : kMergeBytes);
   static_assert(kBytes <= 232448, "serving-step shared memory");
@@ -316,22 +316,18 @@ __global__ void __launch_bounds__(kServeThreads, 1) serve_step_kernel(const Serv
   asm volatile("fence.proxy.async.global;" ::: "memory");
   if (sa.a.max_blocks > 0) split_body<KB, VB, kLean>(sa.a, smem, blockIdx.x);
   if (!grid_sync(sa.barrier, gridDim.x, sa.a.flags)) return;
-  // merge: every warp takes (sequence, kv-head, q-head) items on its own; the split
-  // warps' ranges are copied to shared memory for the searches
-  float* scw = reinterpret_cast<float*>(smem) + (threadIdx.x >> 5) * 128;
-  int64_t* rg = reinterpret_cast<int64_t*>(smem + 8 * 128 * 4);
+  // merge: the block takes (sequence, kv-head) units in turn with its 8 warps; the
+  // split warps' ranges are copied to shared memory for the record lookups
+  WsPart& wsp = *reinterpret_cast<WsPart*>(smem);
+  int64_t* rg = reinterpret_cast<int64_t*>(smem + sizeof(WsPart));
   const int n_range = 2 * sa.a.n_ctas * sa.a.warps;
   for (int i = threadIdx.x; i < n_range; i += kServeThreads) rg[i] = sa.a.ranges[i];
   __syncthreads();
-  const int64_t n_items = static_cast<int64_t>(sa.a.n_seqs) * sa.a.hkv * sa.a.group;
-  const int64_t n_warps = static_cast<int64_t>(gridDim.x) * (kServeThreads / 32);
-  for (int64_t it = static_cast<int64_t>(blockIdx.x) * (kServeThreads / 32) + (threadIdx.x >> 5); it < n_items;
-       it += n_warps) {
-    const int64_t u = it / sa.a.group;
-    const int gg = static_cast<int>(it - u * sa.a.group);
+  const int64_t n_units = static_cast<int64_t>(sa.a.n_seqs) * sa.a.hkv;
+  for (int64_t u = blockIdx.x; u < n_units; u += gridDim.x) {
     const int s = static_cast<int>(u / sa.a.hkv), h = static_cast<int>(u - static_cast<int64_t>(s) * sa.a.hkv);
-    merge_warp(sa.a, sa.ws, sa.out, h, s, gg, scw, rg);
-    __syncwarp();
+    merge_body(sa.a, sa.ws, sa.out, h, s, wsp, rg);
+    __syncthreads();   // the next unit's workspace part reuses wsp
   }
 }
 
