@@ -759,6 +759,60 @@ def run_serve(args):
                       "peak_kind": peak_kind, "decode_bytes": tiles * RECORD}), flush=True)
 
 
+# `--case decode_long`: long-context decode alone (not the headline line): 4 sequences
+# x 131072 tokens, 64 q-heads over 8 kv-heads, k4v2, random valid records (decode time
+# does not depend on the code values), stream-K over 32 (sequence, kv-head) units.
+# L2 is flushed before every timed call.
+DECODE_LONG = "decode_4x128k"
+
+
+def run_decode_long(args):
+    import numpy as np
+    import torch
+    import kvarn_synth as synth
+    import kv_cache_quantization_x128_gb300 as kv
+    torch.cuda.set_device(0)
+    cfg = synth.WORKLOADS[DECODE_LONG]
+    n_seqs, L, hkv, hq, seed = cfg["n_seqs"], cfg["seq_len"], cfg["n_kv_heads"], cfg["n_q_heads"], cfg["seed"]
+    mb = L // 128
+    nb = n_seqs * mb
+    recs = torch.from_numpy(synth.random_records(nb * hkv, seed, RECORD, 12288)).cuda().reshape(nb, hkv, RECORD)
+    bt = torch.from_numpy(synth.block_tables(n_seqs, mb, nb, seed)).cuda()
+    lens = torch.full((n_seqs,), L, dtype=torch.int32, device="cuda")
+    q = torch.from_numpy(synth.queries(n_seqs, hq, seed).view(np.int16)).view(torch.float16).cuda()
+    out = torch.empty_like(q)
+    meta = kv.make_meta(hkv, hq, nb, max_blocks_per_seq=mb)
+    scratch = torch.empty(kv.decode_scratch_bytes(meta, n_seqs), dtype=torch.uint8, device="cuda")
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    call = lambda: kv.kvarn_decode_attention(q, recs, None, bt, lens, out, scratch, meta)
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(args.steps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        call()
+        e1.record()
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1))
+    if kv.kvarn_device_flags() != 0:
+        raise SystemExit("the decode raised a device flag")
+    ms = float(np.median(times))
+    peak, peak_kind = hbm_peak()
+    nbytes = nb * hkv * RECORD
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    print(json.dumps({"metric": "decode_attention_gbs", "value": round(gbs, 1), "unit": "GB/s",
+                      "ms_per_call": round(ms, 4), "steps": args.steps, "warmup": args.warmup,
+                      "higher_is_better": True, "dtype": "f32 accumulation on fp16 operands (hi + lo q', p')",
+                      "data": "synthetic (random valid records)",
+                      "config": {"workload": f"{DECODE_LONG}: 4 sequences x 131072 tokens, gqa64/8",
+                                 "preset": "kvarn_k4v2_g128", "l2": "flushed"},
+                      "frac_hbm": round(gbs / peak, 4), "peak_kind": peak_kind, "bytes": nbytes,
+                      "tokens_per_s": round(n_seqs / (ms * 1e-3), 1)}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -767,10 +821,11 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--case", default="full", choices=["full", "small", "prefill_attn", "serve"],
+    ap.add_argument("--case", default="full", choices=["full", "small", "prefill_attn", "serve", "decode_long"],
                     help="small: reduced shapes for profiler captures (not a bench line); "
                          "prefill_attn: the chunked-prefill attention kernel alone; "
-                         "serve: the 256-sequence serving step (append + decode)")
+                         "serve: the 256-sequence serving step (append + decode); "
+                         "decode_long: the 4 x 131072-token decode alone")
     ap.add_argument("--preset", default="k4v2", choices=sorted(PRESET_RECORD),
                     help="bit preset of the gb300 arm; the default k4v2 is the headline workload")
     args = ap.parse_args()
@@ -788,6 +843,8 @@ def main():
         run_prefill_attn(args)
     elif args.case == "serve":
         run_serve(args)
+    elif args.case == "decode_long":
+        run_decode_long(args)
     elif args.impl == "reference":
         run_reference(args)
     else:

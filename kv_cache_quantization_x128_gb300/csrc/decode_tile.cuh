@@ -594,6 +594,7 @@ __device__ __forceinline__ void merge_ws_part(const DecodeArgs& a, const uint16_
 // Q-head gg of unit (kv-head h, sequence s), one warp, after merge_ws_part of the
 // unit's warps: lane l owns channels 4l..4l+3; rg the split warps' tile ranges
 // (a.ranges, or a copy of it in shared memory).
+template <int kBatch>
 __device__ __forceinline__ void merge_warp(const DecodeArgs& a, uint16_t* __restrict__ out, int h, int s, int gg,
                                            int n_ws, const WsPart& sm, const int64_t* rg) {
   const int lane = threadIdx.x & 31;
@@ -615,16 +616,11 @@ __device__ __forceinline__ void merge_warp(const DecodeArgs& a, uint16_t* __rest
     }
   }
 
-  // the records' running maxima, lane i taking records wlo + i, wlo + i + 32, ...,
-  // and the workspace warps' maxima
+  // the workspace warps first: M their common max, wacc their outputs (unrotated) and
+  // l their sums, each weighted by 2^(max - M)
   const int n_wsw = (n_ws + 15) >> 4;
-  float M = lane < n_wsw ? sm.m[lane][gg] : -INFINITY;
-  for (int64_t w = wlo + lane; w < whi; w += 32)
-    if (rg[2 * w] < rg[2 * w + 1]) M = fmaxf(M, a.part[(w + u) * kRecFloats + gg * kPartStride + 128]);
-#pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-
-  // workspace warps' outputs (unrotated) with their weights 2^(max - M)
+  float M = -INFINITY;
+  for (int w = 0; w < n_wsw; ++w) M = fmaxf(M, sm.m[w][gg]);
   float wacc[4] = {0.f, 0.f, 0.f, 0.f};
   float l = 0.f;
   for (int w = 0; w < n_wsw; ++w) {
@@ -634,46 +630,53 @@ __device__ __forceinline__ void merge_warp(const DecodeArgs& a, uint16_t* __rest
     wacc[1] = fmaf(v.y, f, wacc[1]);
     wacc[2] = fmaf(v.z, f, wacc[2]);
     wacc[3] = fmaf(v.w, f, wacc[3]);
-    if (lane == 0) l = fmaf(sm.l[w][gg], f, l);
+    l = fmaf(sm.l[w][gg], f, l);
   }
-  // records 32 at a time: lane i finds record w0 + i's weight f = 2^(max - M) and its
-  // share of the sum; then every lane adds each record's 4 channels times its f
-  // (records unrolled so that their loads are in flight together)
+  // then the records, kBatch at a time and merged online: all of a batch's loads (each
+  // record's range check, max and sum, and the lane's 4 channels) are in flight
+  // together; the running max then moves to the batch's and the sums are rescaled.
+  // Every lane reads the same maxima, so M, l and the rescale are warp-uniform. A
+  // record without data (an empty split range, or an index past whi, which reads the
+  // last record again) gets weight 0 and is selected away, never multiplied.
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
-  for (int64_t w0 = wlo; w0 < whi; w0 += 32) {
-    const int64_t w = w0 + lane;
-    float f = 0.f;
-    if (w < whi && rg[2 * w] < rg[2 * w + 1]) {
-      const float* pp = a.part + (w + u) * kRecFloats + gg * kPartStride;
-      const float mp = pp[128];
-      f = (mp == -INFINITY) ? 0.f : exp2f(mp - M);
-      l = fmaf(pp[129], f, l);
+  for (int64_t w0 = wlo; w0 < whi; w0 += kBatch) {
+    float4 v[kBatch];
+    float2 ml[kBatch];
+    bool ok[kBatch];
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const int64_t wr = min(w0 + j, whi - 1);
+      const longlong2 r = *reinterpret_cast<const longlong2*>(rg + 2 * wr);
+      const float* pp = a.part + (wr + u) * kRecFloats + gg * kPartStride;
+      ml[j] = *reinterpret_cast<const float2*>(pp + 128);
+      v[j] = *reinterpret_cast<const float4*>(pp + 4 * lane);
+      ok[j] = w0 + j < whi && r.x < r.y;
     }
-    const int cnt = static_cast<int>(min(static_cast<int64_t>(32), whi - w0));
-    for (int i0 = 0; i0 < cnt; i0 += 8) {
-      // eight records' loads first (an index past cnt reads record w0 again, inside
-      // the scratch; its weight is 0), then the sums; a record without data has
-      // weight 0 and is selected away, never multiplied
-      float4 v[8];
-      float fi[8];
+    float mb = M;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        fi[j] = __shfl_sync(0xffffffffu, f, (i0 + j) & 31);
-        const int64_t wr = i0 + j < cnt ? w0 + i0 + j : w0;
-        v[j] = *reinterpret_cast<const float4*>(a.part + (wr + u) * kRecFloats + gg * kPartStride + 4 * lane);
-      }
+    for (int j = 0; j < kBatch; ++j)
+      if (ok[j]) mb = fmaxf(mb, ml[j].x);
+    if (mb > M) {
+      const float sc = exp2f(M - mb);   // 0 while M is -inf (nothing summed yet)
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const bool use = i0 + j < cnt && fi[j] != 0.f;
-        acc[0] = fmaf(use ? v[j].x : 0.f, fi[j], acc[0]);
-        acc[1] = fmaf(use ? v[j].y : 0.f, fi[j], acc[1]);
-        acc[2] = fmaf(use ? v[j].z : 0.f, fi[j], acc[2]);
-        acc[3] = fmaf(use ? v[j].w : 0.f, fi[j], acc[3]);
+      for (int k = 0; k < 4; ++k) {
+        acc[k] *= sc;
+        wacc[k] *= sc;
       }
+      l *= sc;
+      M = mb;
+    }
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const bool use = ok[j] && ml[j].x != -INFINITY;
+      const float f = use ? exp2f(ml[j].x - M) : 0.f;
+      acc[0] = fmaf(use ? v[j].x : 0.f, f, acc[0]);
+      acc[1] = fmaf(use ? v[j].y : 0.f, f, acc[1]);
+      acc[2] = fmaf(use ? v[j].z : 0.f, f, acc[2]);
+      acc[3] = fmaf(use ? v[j].w : 0.f, f, acc[3]);
+      l = fmaf(use ? ml[j].y : 0.f, f, l);
     }
   }
-#pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
   // un-rotate: FWHT over the 128 channels (4 per lane), then scale by 1/sqrt(128)
   {
     const float a0 = acc[0] + acc[1], a1 = acc[0] - acc[1], a2 = acc[2] + acc[3], a3 = acc[2] - acc[3];
@@ -700,7 +703,9 @@ __device__ __forceinline__ void merge_warp(const DecodeArgs& a, uint16_t* __rest
 }
 
 // Unit (kv-head h, sequence s) with the block's 8 warps: the workspace part, then one
-// warp per q-head of the group; sm is the block's shared WsPart.
+// warp per q-head of the group, taking the partial records kBatch at a time; sm is
+// the block's shared WsPart.
+template <int kBatch = 8>
 __device__ __forceinline__ void merge_body(const DecodeArgs& a, const uint16_t* __restrict__ ws,
                                            uint16_t* __restrict__ out, int h, int s, WsPart& sm,
                                            const int64_t* rg) {
@@ -708,7 +713,7 @@ __device__ __forceinline__ void merge_body(const DecodeArgs& a, const uint16_t* 
   const int n_ws = ws_tokens(a, ws, s, threadIdx.x == 0);
   merge_ws_part(a, ws, h, s, n_ws, warp, sm);
   __syncthreads();
-  if (warp < a.group) merge_warp(a, out, h, s, warp, n_ws, sm, rg);
+  if (warp < a.group) merge_warp<kBatch>(a, out, h, s, warp, n_ws, sm, rg);
 }
 
 size_t prefix_bytes(int n_seqs) { return ((static_cast<size_t>(n_seqs) + 1) * sizeof(int64_t) + 255) & ~size_t(255); }

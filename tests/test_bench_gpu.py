@@ -1,5 +1,6 @@
 """bench.py prints one JSON line with the keys its consumers read: the profiling
-case of the headline workload and the prefill-attention case, each run briefly."""
+case of the headline workload, and the prefill-attention, serving-step and
+long-context decode cases, each run briefly."""
 import json
 import os
 import subprocess
@@ -36,3 +37,17 @@ def test_bench_prefill_attention_line():
     d = _run("--case", "prefill_attn", "--steps", "2", "--warmup", "3")
     assert d["metric"] == "chunked_prefill_attention_tflops" and d["unit"] == "TFLOP/s"
     assert d["value"] > 0 and d["ms_per_call"] > 0 and d["prefill_tokens_per_s"] > 0
+
+
+def test_bench_serve_line():
+    d = _run("--case", "serve", "--steps", "2", "--warmup", "3")
+    assert d["metric"] == "serving_step_sequences_per_s" and d["value"] > 0 and d["ms_per_step"] > 0
+    for key in ("append_us", "decode_us", "two_calls_eager_us", "graph_us", "serve_step_one_launch_us"):
+        assert d[key] > 0, key
+    assert 0 < d["decode_frac_hbm"] < 2
+
+
+def test_bench_decode_long_line():
+    d = _run("--case", "decode_long", "--steps", "2", "--warmup", "3")
+    assert d["metric"] == "decode_attention_gbs" and d["unit"] == "GB/s"
+    assert d["value"] > 0 and d["ms_per_call"] > 0 and 0 < d["frac_hbm"] < 2
