@@ -250,9 +250,10 @@ KVARN_API kvarn_status kvarn_decode_attention(const uint16_t* q, const uint8_t* 
  * calls that overlap on the GPU must not share a scratch buffer (nor, as for the
  * two calls it fuses, a workspace or cache region). Capturable in a CUDA graph.
  * Measured on GB300 this one launch is slower than kvarn_append_decode followed by
- * kvarn_decode_attention (its merge phase runs at the split phase's 8 warps per SM),
- * so those two calls, captured in a CUDA graph, are the recommended serving step;
- * this entry point is kept for callers that want a single launch.
+ * kvarn_decode_attention (the grid-wide barriers between its phases, and its merge
+ * phase at the split phase's one CTA per SM), so those two calls, captured in a CUDA
+ * graph, are the recommended serving step; this entry point is kept for callers that
+ * want a single launch.
  *   q             fp16 [n_seqs][num_q_heads][128], the new query of each sequence.
  *   k_new, v_new  fp16 [n_seqs][num_kv_heads][128].
  *   seq_lens      int32 [n_seqs], lengths before the append, >= 0.

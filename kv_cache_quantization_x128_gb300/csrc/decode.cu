@@ -22,9 +22,10 @@
 //     range crosses into a new (sequence, kv-head) it writes a partial record
 //     (acc, running max, running sum) for the one it leaves; the warp that takes a
 //     unit's first tile and the one that takes its last mark themselves;
-//   decode_merge_kernel - per (sequence, kv-head): merges the partial records of
-//     the warps between those marks with the fp16 workspace tokens of the partial
-//     last tile, un-rotates by H^T and normalises.
+//   decode_merge_kernel - per (sequence, kv-head): attends the fp16 workspace
+//     tokens of the partial last tile (m16n8k16 MMAs over all q-heads of the
+//     group), merges them online with the partial records of the warps between
+//     those marks, un-rotates the records' part by H^T and normalises.
 // decode_tc_split_kernel (decode_tc.cuh) is the split phase on tcgen05 for k4v2,
 // chosen with KVARN_DECODE_SPLIT=tc; it writes the same partial records. The split
 // and merge kernels are launched as programmatic dependents of the kernel before
