@@ -175,3 +175,61 @@ def test_append_completes_tiles(env, preset):
     blocks = np.array([bt[s, lens[s] // 128] for s in done]).repeat(hkv)
     heads = np.tile(np.arange(hkv), len(done))
     print(preset, "append", compare_records(got[blocks, heads], kq, vq))
+
+
+@pytest.mark.parametrize("preset", PRESETS)
+def test_decode_64x16k_oracle_pairs(env, preset):
+    """The full decode workload (64 sequences x 16384 tokens, 64 q-heads over 8
+    kv-heads) in each preset's layout: 16 sampled (sequence, kv-head) pairs hold K/V
+    drawn like the prefill batch (outlier key channels x10-x50), quantized by the
+    oracle into every block of the pair; random valid records fill the rest. The
+    oracle's decode of each sampled pair runs over exactly those records."""
+    from tests.oracle_pool import run_pairs
+    kv, torch = env
+    n_seqs, seq_len, hkv, hq, seed = 64, 16384, 8, 64, 78
+    max_blocks = seq_len // 128
+    num_blocks = n_seqs * max_blocks
+    lay = o.LAYOUTS[preset]
+    bt = synth.block_tables(n_seqs, max_blocks, num_blocks, seed)
+    recs = synth.random_records(num_blocks * hkv, seed, lay.record_bytes, lay.k_code_bytes + lay.v_code_bytes)
+    recs = recs.reshape(num_blocks, hkv, -1)
+    q = synth.queries(n_seqs, hq, seed)
+    g = hq // hkv
+    rng = np.random.default_rng(seed)
+    all_pairs = [(s, h) for s in range(n_seqs) for h in range(hkv)]
+    pairs = sorted(all_pairs[int(i)] for i in rng.choice(len(all_pairs), size=16, replace=False))
+    res = run_pairs([(1_000_003 * seed + 64 * s + h, seq_len, q[s, h * g:(h + 1) * g], preset) for s, h in pairs])
+    for (s, h), (r, _, _) in zip(pairs, res):
+        recs[bt[s], h] = r
+    lens = np.full(n_seqs, seq_len, np.int32)
+    out, flags = _gpu_decode(env, q, torch.from_numpy(recs).cuda(), None, bt, lens, hkv, num_blocks, preset)
+    assert flags == 0 and np.isfinite(out).all()
+    worst = 0.0
+    for (s, h), (_, _, ref) in zip(pairs, res):
+        worst = max(worst, assert_decode_close(out[s, h * g:(h + 1) * g], ref, f"{preset} seq {s} head {h}"))
+    print(preset, f"{len(pairs)} oracle-quantized pairs at 64 x 16384, max |err| {worst:.2e}")
+
+
+@pytest.mark.parametrize("preset", PRESETS)
+def test_quantize_16x16k_sampled(env, preset):
+    """The full prefill workload (16 sequences x 16384 tokens, 8 kv-heads) in each
+    preset's layout, in the benchmark's launch configuration; 64 sampled tile-heads
+    against the oracle."""
+    kv, torch = env
+    n_tokens, hkv = 16 * 16384, 8
+    num_blocks = n_tokens // 128
+    k, v = synth.prefill_kv(n_tokens, hkv, seed=1)
+    slots = synth.prefill_slot_mapping(n_tokens, num_blocks, seed=1)
+    meta = kv.make_meta(hkv, hkv, num_blocks, preset=preset)
+    cache = torch.zeros(num_blocks, hkv, record_bytes(preset), dtype=torch.uint8, device="cuda")
+    kv.kvarn_quantize_tiles(f16_to_dev(torch, k), f16_to_dev(torch, v), torch.from_numpy(slots).cuda(), cache, meta)
+    assert kv.kvarn_device_flags() == 0
+    rng = np.random.default_rng(79)
+    pairs = [(int(c), int(h)) for c, h in zip(rng.integers(0, num_blocks, 64), rng.integers(0, hkv, 64))]
+    kt = np.stack([k[c * 128:(c + 1) * 128, h] for c, h in pairs])
+    vt = np.stack([v[c * 128:(c + 1) * 128, h] for c, h in pairs])
+    _, kq, vq = o.quantize_tiles(kt, vt, preset=preset)
+    got = cache.cpu().numpy()
+    blocks = np.array([slots[c * 128] // 128 for c, _ in pairs])
+    heads = np.array([h for _, h in pairs])
+    print(preset, "16 x 16384", compare_records(got[blocks, heads], kq, vq))
