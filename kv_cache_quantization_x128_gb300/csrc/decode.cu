@@ -110,16 +110,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_split_kernel(DecodeAr
   decode_tc_body<kLean>(a);
 }
 
-// One CTA per (kv-head, sequence). kMinBlocks 4 keeps it at 64 registers, so that 4
-// CTAs share an SM, for batches of many short units (a few records each); 1 lets
-// the compiler keep more of the record batches' loads in flight, for a few long units
-// with tens of records each.
-template <int kMinBlocks, int kBatch>
-__global__ void __launch_bounds__(256, kMinBlocks) decode_merge_kernel(DecodeArgs a, const uint16_t* __restrict__ ws,
-                                                                      uint16_t* __restrict__ out) {
+// One CTA of 8 kParts warps per (kv-head, sequence). For batches of many short units
+// (a few partial records each): kParts 1 and kMinBlocks 4, so that 4 CTAs (at 64
+// registers) share an SM. For a few long units (tens of records each): kParts 4, the
+// records of a q-head split between 4 warps.
+template <int kMinBlocks, int kParts>
+__global__ void __launch_bounds__(256 * kParts, kMinBlocks) decode_merge_kernel(DecodeArgs a,
+                                                                               const uint16_t* __restrict__ ws,
+                                                                               uint16_t* __restrict__ out) {
   __shared__ WsPart sm;
+  __shared__ RecShares<kParts> rs;
   griddep_wait();                       // the split kernel's ranges and partial records
-  merge_body<kBatch>(a, ws, out, blockIdx.x, blockIdx.y, sm, a.ranges);
+  merge_body<8, kParts>(a, ws, out, blockIdx.x, blockIdx.y, sm, &rs, a.ranges);
 }
 
 // Launch with programmatic stream serialization (see griddep_wait).
@@ -226,11 +228,11 @@ cudaError_t launch_decode(const uint16_t* q, const uint8_t* cache, const uint16_
           : lean ? launch_split<4, 2, true>(a, stream) : launch_split<4, 2, false>(a, stream);
     if (err != cudaSuccess) return err;
   }
-  // units with 8 or more partial records on average: the unconstrained merge
+  // units with 8 or more partial records on average: the records of a q-head split 4 ways
   const int64_t units = static_cast<int64_t>(n_seqs) * hkv;
   const bool long_units = static_cast<int64_t>(a.n_ctas) * a.warps >= 8 * units;
-  return long_units ? launch_after(decode_merge_kernel<1, 8>, dim3(hkv, n_seqs), dim3(256), 0, stream, a, ws, out)
-                    : launch_after(decode_merge_kernel<4, 8>, dim3(hkv, n_seqs), dim3(256), 0, stream, a, ws, out);
+  return long_units ? launch_after(decode_merge_kernel<1, 4>, dim3(hkv, n_seqs), dim3(1024), 0, stream, a, ws, out)
+                    : launch_after(decode_merge_kernel<4, 1>, dim3(hkv, n_seqs), dim3(256), 0, stream, a, ws, out);
 }
 
 }  // namespace kvarn

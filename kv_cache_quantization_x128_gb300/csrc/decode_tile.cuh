@@ -591,66 +591,46 @@ __device__ __forceinline__ void merge_ws_part(const DecodeArgs& a, const uint16_
   }
 }
 
-// Q-head gg of unit (kv-head h, sequence s), one warp, after merge_ws_part of the
-// unit's warps: lane l owns channels 4l..4l+3; rg the split warps' tile ranges
-// (a.ranges, or a copy of it in shared memory).
-template <int kBatch>
-__device__ __forceinline__ void merge_warp(const DecodeArgs& a, uint16_t* __restrict__ out, int h, int s, int gg,
-                                           int n_ws, const WsPart& sm, const int64_t* rg) {
-  const int lane = threadIdx.x & 31;
-  const int nf = full_tiles(a, s);
-  const int64_t qrow = (static_cast<int64_t>(s) * a.hkv * a.group + static_cast<int64_t>(h) * a.group + gg) * kD;
-  const int64_t u = static_cast<int64_t>(s) * a.hkv + h;
-  const int64_t n_warps = static_cast<int64_t>(a.n_ctas) * a.warps;
-
-  // split warps whose ranges cover this unit's tiles: from the warp that took its
-  // first tile to the one that took its last, as the split phase recorded them
-  // (ranges are contiguous and ordered; an empty range in between left no record;
-  // a unit without both marks, after a timed-out split warp, merges no records)
-  int64_t wlo = 0, whi = 0;
-  if (nf > 0) {
+// The split warps whose ranges cover unit u's tiles, [wlo, whi): from the warp that
+// took its first tile to the one that took its last, as the split phase marked them
+// (ranges are contiguous and ordered; an empty range in between left no record; a
+// unit without both marks, after a timed-out split warp, merges no records).
+__device__ __forceinline__ void covering_warps(const DecodeArgs& a, int s, int64_t u, int64_t& wlo, int64_t& whi) {
+  wlo = whi = 0;
+  if (full_tiles(a, s) > 0) {
     const int2 cv = *reinterpret_cast<const int2*>(a.cover + 2 * u);
-    if (cv.x >= 0 && cv.y >= cv.x && cv.y < n_warps) {
+    if (cv.x >= 0 && cv.y >= cv.x && cv.y < static_cast<int64_t>(a.n_ctas) * a.warps) {
       wlo = cv.x;
       whi = static_cast<int64_t>(cv.y) + 1;
     }
   }
+}
 
-  // the workspace warps first: M their common max, wacc their outputs (unrotated) and
-  // l their sums, each weighted by 2^(max - M)
-  const int n_wsw = (n_ws + 15) >> 4;
-  float M = -INFINITY;
-  for (int w = 0; w < n_wsw; ++w) M = fmaxf(M, sm.m[w][gg]);
-  float wacc[4] = {0.f, 0.f, 0.f, 0.f};
-  float l = 0.f;
-  for (int w = 0; w < n_wsw; ++w) {
-    const float f = exp2f(sm.m[w][gg] - M);
-    const float4 v = *reinterpret_cast<const float4*>(&sm.o[w][gg][4 * lane]);
-    wacc[0] = fmaf(v.x, f, wacc[0]);
-    wacc[1] = fmaf(v.y, f, wacc[1]);
-    wacc[2] = fmaf(v.z, f, wacc[2]);
-    wacc[3] = fmaf(v.w, f, wacc[3]);
-    l = fmaf(sm.l[w][gg], f, l);
-  }
-  // then the records, kBatch at a time and merged online: all of a batch's loads (each
-  // record's range check, max and sum, and the lane's 4 channels) are in flight
-  // together; the running max then moves to the batch's and the sums are rescaled.
-  // Every lane reads the same maxima, so M, l and the rescale are warp-uniform. A
-  // record without data (an empty split range, or an index past whi, which reads the
-  // last record again) gets weight 0 and is selected away, never multiplied.
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
-  for (int64_t w0 = wlo; w0 < whi; w0 += kBatch) {
+// Q-head gg's partial records w = wlo + first, wlo + first + kStride, ... below whi,
+// merged online kBatch at a time into (M, l, acc): all of a batch's loads (each
+// record's range check, max and sum, and the lane's 4 channels, 4l..4l+3) are in
+// flight together; the running max then moves to the batch's and the sums are
+// rescaled. Every lane reads the same maxima, so M, l and the rescale are
+// warp-uniform. A record without data (an empty split range, or an index past whi,
+// which reads the unit's last record again) gets weight 0 and is selected away,
+// never multiplied.
+template <int kBatch, int kStride>
+__device__ __forceinline__ void merge_records(const DecodeArgs& a, const int64_t* rg, int64_t u, int gg, int64_t wlo,
+                                              int64_t whi, int first, float& M, float& l, float (&acc)[4]) {
+  const int lane = threadIdx.x & 31;
+  for (int64_t w0 = wlo + first; w0 < whi; w0 += kBatch * kStride) {
     float4 v[kBatch];
     float2 ml[kBatch];
     bool ok[kBatch];
 #pragma unroll
     for (int j = 0; j < kBatch; ++j) {
-      const int64_t wr = min(w0 + j, whi - 1);
+      const int64_t wj = w0 + j * kStride;
+      const int64_t wr = min(wj, whi - 1);
       const longlong2 r = *reinterpret_cast<const longlong2*>(rg + 2 * wr);
       const float* pp = a.part + (wr + u) * kRecFloats + gg * kPartStride;
       ml[j] = *reinterpret_cast<const float2*>(pp + 128);
       v[j] = *reinterpret_cast<const float4*>(pp + 4 * lane);
-      ok[j] = w0 + j < whi && r.x < r.y;
+      ok[j] = wj < whi && r.x < r.y;
     }
     float mb = M;
 #pragma unroll
@@ -659,10 +639,7 @@ __device__ __forceinline__ void merge_warp(const DecodeArgs& a, uint16_t* __rest
     if (mb > M) {
       const float sc = exp2f(M - mb);   // 0 while M is -inf (nothing summed yet)
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        acc[k] *= sc;
-        wacc[k] *= sc;
-      }
+      for (int k = 0; k < 4; ++k) acc[k] *= sc;
       l *= sc;
       M = mb;
     }
@@ -676,6 +653,58 @@ __device__ __forceinline__ void merge_warp(const DecodeArgs& a, uint16_t* __rest
       acc[3] = fmaf(use ? v[j].w : 0.f, f, acc[3]);
       l = fmaf(use ? ml[j].y : 0.f, f, l);
     }
+  }
+}
+
+// Partial records' state of the warps that merged a share of a unit's records for
+// q-head g: [share - 1][g] = acc[128], max, sum (kPartStride floats).
+template <int kParts>
+struct RecShares {
+  float v[kParts > 1 ? kParts - 1 : 1][8][kPartStride];
+};
+
+// Q-head gg of unit (kv-head h, sequence s), one warp: the records' state (M, l, acc:
+// lane l owns channels 4l..4l+3, rotated domain) is combined with the other shares'
+// (`shares` of them in rs) and with the workspace warps' outputs (sm), un-rotated by
+// a 128-point FWHT, normalised and stored as fp16.
+template <int kParts>
+__device__ __forceinline__ void merge_finish(const DecodeArgs& a, uint16_t* __restrict__ out, int h, int s, int gg,
+                                             int n_ws, const WsPart& sm, const RecShares<kParts>* rs, float M,
+                                             float l, float (&acc)[4]) {
+  const int lane = threadIdx.x & 31;
+  const int64_t qrow = (static_cast<int64_t>(s) * a.hkv * a.group + static_cast<int64_t>(h) * a.group + gg) * kD;
+  // the other shares of the records, then the workspace warps, against the common max
+  const int n_wsw = (n_ws + 15) >> 4;
+  float Mt = M;
+#pragma unroll
+  for (int p = 0; p < kParts - 1; ++p) Mt = fmaxf(Mt, rs->v[p][gg][128]);
+  for (int w = 0; w < n_wsw; ++w) Mt = fmaxf(Mt, sm.m[w][gg]);
+  {
+    const float sc = M == -INFINITY ? 0.f : exp2f(M - Mt);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) acc[k] *= sc;
+    l *= sc;
+  }
+#pragma unroll
+  for (int p = 0; p < kParts - 1; ++p) {
+    const float mp = rs->v[p][gg][128];
+    const float f = mp == -INFINITY ? 0.f : exp2f(mp - Mt);
+    const float4 v = *reinterpret_cast<const float4*>(&rs->v[p][gg][4 * lane]);
+    acc[0] = fmaf(f != 0.f ? v.x : 0.f, f, acc[0]);
+    acc[1] = fmaf(f != 0.f ? v.y : 0.f, f, acc[1]);
+    acc[2] = fmaf(f != 0.f ? v.z : 0.f, f, acc[2]);
+    acc[3] = fmaf(f != 0.f ? v.w : 0.f, f, acc[3]);
+    l = fmaf(f != 0.f ? rs->v[p][gg][129] : 0.f, f, l);
+  }
+  float wacc[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int w = 0; w < n_wsw; ++w) {
+    const float f = exp2f(sm.m[w][gg] - Mt);
+    const float4 v = *reinterpret_cast<const float4*>(&sm.o[w][gg][4 * lane]);
+    wacc[0] = fmaf(v.x, f, wacc[0]);
+    wacc[1] = fmaf(v.y, f, wacc[1]);
+    wacc[2] = fmaf(v.z, f, wacc[2]);
+    wacc[3] = fmaf(v.w, f, wacc[3]);
+    l = fmaf(sm.l[w][gg], f, l);
   }
   // un-rotate: FWHT over the 128 channels (4 per lane), then scale by 1/sqrt(128)
   {
@@ -702,18 +731,33 @@ __device__ __forceinline__ void merge_warp(const DecodeArgs& a, uint16_t* __rest
       make_uint2(res[0] | (static_cast<uint32_t>(res[1]) << 16), res[2] | (static_cast<uint32_t>(res[3]) << 16));
 }
 
-// Unit (kv-head h, sequence s) with the block's 8 warps: the workspace part, then one
-// warp per q-head of the group, taking the partial records kBatch at a time; sm is
-// the block's shared WsPart.
-template <int kBatch = 8>
+// Unit (kv-head h, sequence s) with the block's 8 kParts warps: warps 0-7 attend the
+// workspace tokens (merge_ws_part); warp w takes share w / 8 of the partial records
+// for q-head w % 8 (every kParts-th record); after one block barrier the warps of
+// share 0 combine the shares with the workspace part and finish their q-heads. sm and
+// rs are the block's shared memory (rs unused when kParts is 1).
+template <int kBatch = 8, int kParts = 1>
 __device__ __forceinline__ void merge_body(const DecodeArgs& a, const uint16_t* __restrict__ ws,
                                            uint16_t* __restrict__ out, int h, int s, WsPart& sm,
-                                           const int64_t* rg) {
-  const int warp = threadIdx.x >> 5;
+                                           RecShares<kParts>* rs, const int64_t* rg) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gg = warp & 7, share = warp >> 3;
   const int n_ws = ws_tokens(a, ws, s, threadIdx.x == 0);
-  merge_ws_part(a, ws, h, s, n_ws, warp, sm);
+  if (warp < 8) merge_ws_part(a, ws, h, s, n_ws, warp, sm);
+  const int64_t u = static_cast<int64_t>(s) * a.hkv + h;
+  float M = -INFINITY, l = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
+  if (gg < a.group) {
+    int64_t wlo, whi;
+    covering_warps(a, s, u, wlo, whi);
+    merge_records<kBatch, kParts>(a, rg, u, gg, wlo, whi, share, M, l, acc);
+    if (kParts > 1 && share > 0) {
+      float* dst = rs->v[share - 1][gg];
+      *reinterpret_cast<float4*>(dst + 4 * lane) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      if (lane == 0) *reinterpret_cast<float2*>(dst + 128) = make_float2(M, l);
+    }
+  }
   __syncthreads();
-  if (warp < a.group) merge_warp<kBatch>(a, out, h, s, warp, n_ws, sm, rg);
+  if (share == 0 && gg < a.group) merge_finish<kParts>(a, out, h, s, gg, n_ws, sm, rs, M, l, acc);
 }
 
 size_t prefix_bytes(int n_seqs) { return ((static_cast<size_t>(n_seqs) + 1) * sizeof(int64_t) + 255) & ~size_t(255); }

@@ -326,7 +326,7 @@ __global__ void __launch_bounds__(kServeThreads, 1) serve_step_kernel(const Serv
   const int64_t n_units = static_cast<int64_t>(sa.a.n_seqs) * sa.a.hkv;
   for (int64_t u = blockIdx.x; u < n_units; u += gridDim.x) {
     const int s = static_cast<int>(u / sa.a.hkv), h = static_cast<int>(u - static_cast<int64_t>(s) * sa.a.hkv);
-    merge_body(sa.a, sa.ws, sa.out, h, s, wsp, rg);
+    merge_body<8, 1>(sa.a, sa.ws, sa.out, h, s, wsp, nullptr, rg);
     __syncthreads();   // the next unit's workspace part reuses wsp
   }
 }
