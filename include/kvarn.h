@@ -283,7 +283,7 @@ KVARN_API kvarn_status kvarn_serve_step(const uint16_t* q, const uint16_t* k_new
  * is a fixed 16 MiB array of device memory inside the library (held by every GPU
  * that loads the library until the process exits), shared by all calls on a device.
  *   - Sizes: returns KVARN_ESCRATCH, without launching, when the scratch needed for
- *     n_seqs * num_kv_heads (sequence, kv-head) pairs exceeds 16 MiB (about 3000
+ *     n_seqs * num_kv_heads (sequence, kv-head) pairs exceeds 16 MiB (about 2100
  *     pairs on a 152-SM GB300).
  *   - The first call on a device (with that device current) looks up the array's
  *     device address; make that first call before any stream capture.

@@ -95,12 +95,12 @@ __global__ void __launch_bounds__(1024) decode_scan_kernel(DecodeArgs a) {
   for (int64_t i = t; i < n_cover; i += 1024) a.cover[i] = -1;
 }
 
-template <int KB, int VB, bool kLean>
-__global__ void __launch_bounds__(SplitCfg<KB, VB, kLean>::kWarps * 32, 1) decode_split_kernel(DecodeArgs a) {
+template <int KB, int VB, bool kLean, class Cfg>
+__global__ void __launch_bounds__(Cfg::kWarps * 32, 1) decode_split_kernel(DecodeArgs a) {
   extern __shared__ __align__(1024) uint8_t smem[];
   griddep_launch_dependents();          // the merge kernel waits for this grid itself
   griddep_wait();                       // the scan's prefix
-  split_body<KB, VB, kLean>(a, smem, blockIdx.x);
+  split_body<KB, VB, kLean, Cfg>(a, smem, blockIdx.x);
 }
 
 template <bool kLean>
@@ -162,13 +162,25 @@ int decode_num_ctas() {
   return sms > 0 ? (sms < kMaxCtas ? sms : kMaxCtas) : 1;
 }
 
-template <int KB, int VB, bool kLean>
-cudaError_t launch_split(const DecodeArgs& a, cudaStream_t stream) {
-  using C = SplitCfg<KB, VB, kLean>;
+template <int KB, int VB, bool kLean, class C>
+cudaError_t launch_split_cfg(const DecodeArgs& a, cudaStream_t stream) {
   static std::atomic<unsigned long long> smem_set{0};
-  cudaError_t err = set_smem_once(decode_split_kernel<KB, VB, kLean>, C::kSmem, smem_set);
+  cudaError_t err = set_smem_once(decode_split_kernel<KB, VB, kLean, C>, C::kSmem, smem_set);
   if (err != cudaSuccess) return err;
-  return launch_after(decode_split_kernel<KB, VB, kLean>, dim3(a.n_ctas), dim3(C::kWarps * 32), C::kSmem, stream, a);
+  return launch_after(decode_split_kernel<KB, VB, kLean, C>, dim3(a.n_ctas), dim3(C::kWarps * 32), C::kSmem, stream,
+                      a);
+}
+
+// The split kernel in the shape a.warps was set for (SplitCfg, or SplitCfg2 for few units).
+template <int KB, int VB, bool kLean>
+cudaError_t launch_split(const DecodeArgs& a, bool few_units, cudaStream_t stream) {
+  return few_units ? launch_split_cfg<KB, VB, kLean, SplitCfg2<KB, VB, kLean>>(a, stream)
+                   : launch_split_cfg<KB, VB, kLean, SplitCfg<KB, VB, kLean>>(a, stream);
+}
+
+template <int KB, int VB, bool kLean>
+int split_warps(bool few_units) {
+  return few_units ? SplitCfg2<KB, VB, kLean>::kWarps : SplitCfg<KB, VB, kLean>::kWarps;
 }
 
 template <bool kLean>
@@ -215,21 +227,24 @@ cudaError_t launch_decode(const uint16_t* q, const uint8_t* cache, const uint16_
   const bool k4v2 = k_bits == 4 && v_bits == 2, k4v4 = k_bits == 4 && v_bits == 4, k2v2 = k_bits == 2 && v_bits == 2;
   if (!(k4v2 || ((k4v4 || k2v2) && !lean))) return cudaErrorInvalidValue;
   const bool tc = k4v2 && use_tc_split();
+  // at most as many (sequence, kv-head) units as CTAs: 8 or more partial records per
+  // unit with 8 split warps per CTA
+  const int64_t units = static_cast<int64_t>(n_seqs) * hkv;
+  const bool few_units = units <= a.n_ctas;
   a.warps = tc ? kTcTeams
-            : k4v4 ? SplitCfg<4, 4>::kWarps : k2v2 ? SplitCfg<2, 2>::kWarps
-            : lean ? SplitCfg<4, 2, true>::kWarps : SplitCfg<4, 2>::kWarps;
+            : k4v4 ? split_warps<4, 4, false>(few_units) : k2v2 ? split_warps<2, 2, false>(few_units)
+            : lean ? split_warps<4, 2, true>(few_units) : split_warps<4, 2, false>(few_units);
   decode_scan_kernel<<<1, 1024, 0, stream>>>(a);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   if (max_blocks > 0) {
     err = tc ? (lean ? launch_split_tc<true>(a, stream) : launch_split_tc<false>(a, stream))
-          : k2v2 ? launch_split<2, 2, false>(a, stream)
-          : k4v4 ? launch_split<4, 4, false>(a, stream)
-          : lean ? launch_split<4, 2, true>(a, stream) : launch_split<4, 2, false>(a, stream);
+          : k2v2 ? launch_split<2, 2, false>(a, few_units, stream)
+          : k4v4 ? launch_split<4, 4, false>(a, few_units, stream)
+          : lean ? launch_split<4, 2, true>(a, few_units, stream) : launch_split<4, 2, false>(a, few_units, stream);
     if (err != cudaSuccess) return err;
   }
   // units with 8 or more partial records on average: the records of a q-head split 4 ways
-  const int64_t units = static_cast<int64_t>(n_seqs) * hkv;
   const bool long_units = static_cast<int64_t>(a.n_ctas) * a.warps >= 8 * units;
   return long_units ? launch_after(decode_merge_kernel<1, 4>, dim3(hkv, n_seqs), dim3(1024), 0, stream, a, ws, out)
                     : launch_after(decode_merge_kernel<4, 1>, dim3(hkv, n_seqs), dim3(256), 0, stream, a, ws, out);

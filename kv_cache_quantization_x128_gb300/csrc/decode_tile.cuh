@@ -14,20 +14,40 @@ namespace kvarn {
 namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr int kMaxWarps = 8;                    // consumer warps per CTA (at most)
-constexpr int kStages = 2;                      // bulk-copy stages per warp
+constexpr int kMaxWarps = 12;                   // split warps per CTA (at most)
 constexpr int kMaxCtas = 1024;                  // upper bound used to size scratch
 constexpr int kPartStride = 132;                // floats per q-head: acc[128], max, sum, pad
 constexpr int kRecFloats = 8 * kPartStride;     // one partial record (8 q-head slots)
 
-// Split kernel shape for KB-bit keys and VB-bit values: the most warps (8 down to
-// 6) whose two records each fit in shared memory; k4v4's 18432-byte records get 6.
+// Split-phase shapes for KB-bit keys and VB-bit values.
+// SplitCfg: up to 12 warps (3 per scheduler), each with one record stage, q_r in
+// shared memory so that 168 registers hold the rest, and the tile after the next one
+// prefetched into L2: 12 warps for the 10-14 KB records, 10 for k4v4's 18 KB. The
+// split kernel's shape for batches of many (sequence, kv-head) units.
 template <int KB, int VB, bool kLean = false>
 struct SplitCfg {
   using L = RecordLayout<KB, VB, kLean>;
-  static constexpr int fits(int w) { return w * kStages * L::kBytes + w * kStages * 8 <= 232448; }
+  static constexpr int fits(int w) { return w * (L::kBytes + 8 + 4096) <= 232448; }
+  static constexpr int kWarps = fits(12) ? 12 : fits(10) ? 10 : 8;
+  static constexpr int kStages = 1;
+  static constexpr bool kQSmem = true;
+  static constexpr int kQOff = kWarps * kStages * (L::kBytes + 8);   // q_r: [warp][ks][lane] float4
+  static constexpr int kSmem = kQOff + kWarps * 4096;
+  static_assert(kSmem <= 232448 && kQOff % 16 == 0 && kWarps <= kMaxWarps, "decode stages");
+};
+// SplitCfg2: the most warps (8 down to 6) whose two record stages each fit in shared
+// memory, q_r in registers. The split kernel's shape for a few long units (a third
+// fewer warps, so a third fewer partial records to merge per unit), and the serving
+// step's (its blocks have 8 warps).
+template <int KB, int VB, bool kLean = false>
+struct SplitCfg2 {
+  using L = RecordLayout<KB, VB, kLean>;
+  static constexpr int fits(int w) { return w * 2 * (L::kBytes + 8) <= 232448; }
   static constexpr int kWarps = fits(8) ? 8 : fits(7) ? 7 : 6;
-  static constexpr int kSmem = kWarps * kStages * L::kBytes + kWarps * kStages * 8;
+  static constexpr int kStages = 2;
+  static constexpr bool kQSmem = false;
+  static constexpr int kQOff = 0;
+  static constexpr int kSmem = kWarps * kStages * (L::kBytes + 8);
   static_assert(kSmem <= 232448, "decode stages");
 };
 
@@ -111,6 +131,17 @@ __device__ __forceinline__ bool issue_tile(const DecodeArgs& a, const Cursor& c,
   return true;
 }
 
+// Lane 0: prefetch the record of the tile at cursor `c` into L2 (nothing for a block
+// index outside [0, num_blocks); its copy will raise the flag).
+template <int kRecBytes>
+__device__ __forceinline__ void prefetch_tile(const DecodeArgs& a, const Cursor& c) {
+  const int64_t blk = a.block_tables[static_cast<int64_t>(c.s) * a.max_blocks + c.ti];
+  if (blk < 0 || blk >= a.num_blocks) return;
+  const uint8_t* src = a.cache + (blk * a.hkv + c.h) * static_cast<int64_t>(kRecBytes);
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(static_cast<uint32_t>(kRecBytes))
+               : "memory");
+}
+
 // q_r2 of this thread's 32 channels for (sequence s, kv-head h): H q * log2(e)/sqrt(128),
 // computed as FWHT(q) * log2(e) / 128. Thread (g, c) holds head g, channels
 // 16ks + 2c + {0, 1, 8, 9}; channel bits 1-2 live across the quad (lanes ^1, ^2).
@@ -162,9 +193,11 @@ __device__ __forceinline__ void load_q(const DecodeArgs& a, int s, int h, int g,
 }
 
 // One packed tile: update the running (max, sum, acc) of head g.
-template <int KB, int VB, bool kLean>
-__device__ __forceinline__ void attend_tile(const uint8_t* rec, const float (&qv)[8][4], int g, int c, float& m_run,
-                                            float& l_run, float (&acc)[16][2]) {
+// q_r comes from qv, or from shared memory (qsm[32 ks], this thread's float4 of k-step
+// ks) when kQSmem.
+template <int KB, int VB, bool kLean, bool kQSmem>
+__device__ __forceinline__ void attend_tile(const uint8_t* rec, const float (&qv)[8][4], const float4* qsm, int g,
+                                            int c, float& m_run, float& l_run, float (&acc)[16][2]) {
   using L = RecordLayout<KB, VB, kLean>;
   const uint16_t* km = reinterpret_cast<const uint16_t*>(rec + L::kKMetaOff);
   const uint16_t* vm = reinterpret_cast<const uint16_t*>(rec + L::kVMetaOff);
@@ -182,7 +215,8 @@ __device__ __forceinline__ void attend_tile(const uint8_t* rec, const float (&qv
     const uint32_t r1 = kLean ? kH_One : h2raw(km + L::kKr + ch0 + 8);
     const float2 rs0 = mul_h2(r0, s0), rs1 = mul_h2(r1, s1);
     const float2 rz0 = mul_h2(r0, z0), rz1 = mul_h2(r1, z1);
-    const float2 qa = make_float2(qv[ks][0], qv[ks][1]), qb = make_float2(qv[ks][2], qv[ks][3]);
+    const float4 qq = kQSmem ? qsm[32 * ks] : make_float4(qv[ks][0], qv[ks][1], qv[ks][2], qv[ks][3]);
+    const float2 qa = make_float2(qq.x, qq.y), qb = make_float2(qq.z, qq.w);
     split2p(__fmul2_rn(qa, rs0), A[ks][0], A[ks][1]);
     split2p(__fmul2_rn(qb, rs1), A[ks][2], A[ks][3]);
     beta2 = __ffma2_rn(qa, rz0, beta2);
@@ -380,11 +414,12 @@ __device__ __forceinline__ void flush_record(const DecodeArgs& a, int64_t rec_id
   if (c == 0) *reinterpret_cast<float2*>(out + 128) = make_float2(m_run, l);
 }
 
-// The split phase of CTA `cta`: warp w < kWarps attends its range of tiles
-// (warps beyond kWarps, in a larger block, have none); `smem` holds the stages.
-template <int KB, int VB, bool kLean>
+// The split phase of CTA `cta` in shape Cfg: warp w < kWarps attends its range of
+// tiles (warps beyond kWarps, in a larger block, have none); `smem` holds the stages
+// (and q_r when Cfg::kQSmem).
+template <int KB, int VB, bool kLean, class Cfg = SplitCfg<KB, VB, kLean>>
 __device__ __forceinline__ void split_body(const DecodeArgs& a, uint8_t* smem, int cta) {
-  constexpr int kWarps = SplitCfg<KB, VB, kLean>::kWarps;
+  constexpr int kWarps = Cfg::kWarps, kStages = Cfg::kStages;
   constexpr int kRecBytes = RecordLayout<KB, VB, kLean>::kBytes;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (warp >= kWarps) return;
@@ -399,6 +434,7 @@ __device__ __forceinline__ void split_body(const DecodeArgs& a, uint8_t* smem, i
   }
   if (gb >= ge) return;   // warps are independent: no CTA-wide barrier below
 
+  float4* qsm = reinterpret_cast<float4*>(smem + Cfg::kQOff) + warp * 256 + lane;   // used when Cfg::kQSmem
   uint8_t* stages = smem + warp * kStages * kRecBytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kWarps * kStages * kRecBytes) + warp * kStages;
   if (lane == 0) {
@@ -418,6 +454,11 @@ __device__ __forceinline__ void split_body(const DecodeArgs& a, uint8_t* smem, i
     if (__shfl_sync(0xffffffffu, ok, 0)) valid |= 1u << k;
   }
 
+  Cursor pc = lc;   // one stage: the tile after the one being copied, prefetched into L2
+  if (kStages == 1 && gb + 1 < ge) {
+    advance(a, pc);
+    if (lane == 0) prefetch_tile<kRecBytes>(a, pc);
+  }
   float qv[8][4];
   float acc[16][2];
   float m_run = -INFINITY, l_run = 0.f;
@@ -432,6 +473,10 @@ __device__ __forceinline__ void split_body(const DecodeArgs& a, uint8_t* smem, i
       unit = u;
       if (lane == 0 && cc.ti == 0) a.cover[2 * u] = static_cast<int32_t>(wg);   // the unit's first split warp
       load_q(a, cc.s, cc.h, g, c, qv);
+      if (Cfg::kQSmem) {
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) qsm[32 * ks] = make_float4(qv[ks][0], qv[ks][1], qv[ks][2], qv[ks][3]);
+      }
       m_run = -INFINITY;
       l_run = 0.f;
 #pragma unroll
@@ -444,13 +489,18 @@ __device__ __forceinline__ void split_body(const DecodeArgs& a, uint8_t* smem, i
       break;
     }
     if (lane == 0 && cc.ti == cc.nf - 1) a.cover[2 * u + 1] = static_cast<int32_t>(wg);   // and its last
-    if ((valid >> stg) & 1u) attend_tile<KB, VB, kLean>(stages + stg * kRecBytes, qv, g, c, m_run, l_run, acc);
+    if ((valid >> stg) & 1u)
+      attend_tile<KB, VB, kLean, Cfg::kQSmem>(stages + stg * kRecBytes, qv, qsm, g, c, m_run, l_run, acc);
     __syncwarp();
     if (gb + k + kStages < ge) {     // refill this stage with the tile kStages ahead
       advance(a, lc);
       bool issued = false;
       if (lane == 0) issued = issue_tile<kRecBytes>(a, lc, stages + stg * kRecBytes, &bars[stg]);
       if (__shfl_sync(0xffffffffu, issued, 0)) valid |= 1u << stg; else valid &= ~(1u << stg);
+      if (kStages == 1 && gb + k + 2 < ge) {
+        advance(a, pc);
+        if (lane == 0) prefetch_tile<kRecBytes>(a, pc);
+      }
     }
     advance(a, cc);
   }

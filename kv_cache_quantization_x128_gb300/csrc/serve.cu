@@ -65,7 +65,7 @@ struct ServeSmem {
   static constexpr int kOffListN = kOffScan + kServeThreads * 8;    // int32: completed tiles listed
   static constexpr int kOffList = kOffListN + 16;                   // int32 [kListCap] item indices
   static constexpr int kAppendBytes = kOffList + kListCap * 4;
-  static constexpr int kSplitBytes = SplitCfg<KB, VB, kLean>::kSmem;
+  static constexpr int kSplitBytes = SplitCfg2<KB, VB, kLean>::kSmem;
   static constexpr int kMergeBytes = static_cast<int>(sizeof(WsPart)) + kMaxCtas * kMaxWarps * 2 * 8;   // workspace part, range copy
   static constexpr int kBytes = kAppendBytes > kSplitBytes ? (kAppendBytes > kMergeBytes ? kAppendBytes : kMergeBytes)
                                                            : (kSplitBytes > kMergeBytes ? kSplitBytes : kMergeBytes);
@@ -314,7 +314,7 @@ __global__ void __launch_bounds__(kServeThreads, 1) serve_step_kernel(const Serv
   if (!grid_sync(sa.barrier, gridDim.x, sa.a.flags)) return;   // timed out (flag raised)
   // records written through the async proxy by other CTAs are read the same way
   asm volatile("fence.proxy.async.global;" ::: "memory");
-  if (sa.a.max_blocks > 0) split_body<KB, VB, kLean>(sa.a, smem, blockIdx.x);
+  if (sa.a.max_blocks > 0) split_body<KB, VB, kLean, SplitCfg2<KB, VB, kLean>>(sa.a, smem, blockIdx.x);
   if (!grid_sync(sa.barrier, gridDim.x, sa.a.flags)) return;
   // merge: the block takes (sequence, kv-head) units in turn with its 8 warps; the
   // split warps' ranges are copied to shared memory for the record lookups
@@ -448,19 +448,19 @@ cudaError_t launch_serve_step(const uint16_t* q, const uint16_t* k_new, const ui
   const cudaError_t zero = cudaMemsetAsync(sa.barrier, 0, 2 * sizeof(unsigned), stream);
   if (zero != cudaSuccess) return zero;
   if (k_bits == 4 && v_bits == 2 && !lean) {
-    a.warps = SplitCfg<4, 2>::kWarps;
+    a.warps = SplitCfg2<4, 2>::kWarps;
     return launch_serve_bits<4, 2, false>(sa, grid, stream);
   }
   if (k_bits == 4 && v_bits == 2 && lean) {
-    a.warps = SplitCfg<4, 2, true>::kWarps;
+    a.warps = SplitCfg2<4, 2, true>::kWarps;
     return launch_serve_bits<4, 2, true>(sa, grid, stream);
   }
   if (k_bits == 4 && v_bits == 4 && !lean) {
-    a.warps = SplitCfg<4, 4>::kWarps;
+    a.warps = SplitCfg2<4, 4>::kWarps;
     return launch_serve_bits<4, 4, false>(sa, grid, stream);
   }
   if (k_bits == 2 && v_bits == 2 && !lean) {
-    a.warps = SplitCfg<2, 2>::kWarps;
+    a.warps = SplitCfg2<2, 2>::kWarps;
     return launch_serve_bits<2, 2, false>(sa, grid, stream);
   }
   return cudaErrorInvalidValue;

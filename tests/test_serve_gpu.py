@@ -1,13 +1,12 @@
 """kvarn_serve_step (append + decode attention in one cooperative launch, CUDA
 through the C ABI) against the two calls it fuses, kvarn_append_decode then
 kvarn_decode_attention, on the same inputs: the workspace, the cache and the new
-lengths must agree bit for bit, and so must the attention output (both run the same
-split and merge code), except when KVARN_DECODE_SPLIT=tc sends the decode call's k4v2
-split phase to the tensor-core kernel: the outputs are then compared within the
-decode tolerance (each is checked against the CPU oracle: the decode parity tests,
-and the oracle test of the step below). Also: the step captured in a CUDA graph and
-replayed."""
-import os
+lengths must agree bit for bit. The attention outputs are compared within the decode
+tolerance: the step's split phase runs 8 warps per SM with two record stages each,
+the decode call's up to 12 with one (and its merge may split a unit's records between
+warps), so the two sum the same terms in another order; each is checked against the
+CPU oracle (the decode parity tests, and the oracle test of the step below). Also:
+the step captured in a CUDA graph and replayed."""
 import numpy as np
 import pytest
 
@@ -96,10 +95,7 @@ def test_serve_step_matches_append_then_decode(env, preset):
     assert torch.equal(lens_out, want[2])
     assert torch.equal(ws.view(torch.int16), want[0].view(torch.int16))
     assert torch.equal(cache, want[1])
-    if preset.startswith("k4v2") and os.environ.get("KVARN_DECODE_SPLIT") == "tc":
-        assert_paths_close(out.float().cpu().numpy(), want[3].float().cpu().numpy(), preset)
-    else:
-        assert torch.equal(out.view(torch.int16), want[3].view(torch.int16))
+    assert_paths_close(out.float().cpu().numpy(), want[3].float().cpu().numpy(), preset)
     assert torch.isfinite(out.float()).all()
 
 
