@@ -40,10 +40,11 @@ PRESET_RECORD = {"k4v2": 14336, "k4v4": 18432, "k2v2": 10240, "k4v2l": 13824}
 WORKLOAD = "prefill_quantize_16x16k + decode_attn_64x16k_gqa64/8"
 E2E_CHUNKS = 8             # slices of the prefill batch in the end-to-end leg
 # Reduced shapes for profiler captures (`--case small`): still larger than L2, a
-# few hundred MB on the device. Not a bench line.
+# few hundred MB on the device, and more (sequence, kv-head) units than SMs so that
+# the decode runs the split kernel in the full bench's shape. Not a bench line.
 SMALL = dict(prefill=dict(n_seqs=4, seq_len=16384, n_kv_heads=8, seed=1),
-             decode=dict(n_seqs=16, seq_len=16384, n_kv_heads=8, n_q_heads=64, seed=2),
-             workload="profiling case: prefill_quantize_4x16k + decode_attn_16x16k_gqa64/8")
+             decode=dict(n_seqs=20, seq_len=16384, n_kv_heads=8, n_q_heads=64, seed=2),
+             workload="profiling case: prefill_quantize_4x16k + decode_attn_20x16k_gqa64/8")
 
 
 def reduce_max(values, world: int):
