@@ -5,13 +5,14 @@
 // Three launches:
 //   decode_scan_kernel  - exclusive prefix of full tiles per sequence (scratch),
 //     and every unit's first / last split-warp marks reset to -1;
-//   decode_split_kernel - persistent, one CTA per SM, 8 warps (6 for 4-bit
-//     values). The flattened tile space (sequence, kv-head, tile) is cut into
-//     one contiguous range per warp (stream-K), so ragged batches balance to a
-//     tile. Each warp streams its range through two private record-sized
-//     (14336 bytes for k4v2) bulk-copy (TMA) stages and runs its
-//     GQA group (up to 8 q-heads) on m16n8k16 tensor-core MMAs, with an online
-//     softmax in the log2 domain:
+//   decode_split_kernel - persistent, one CTA per SM. The flattened tile space
+//     (sequence, kv-head, tile) is cut into one contiguous range per warp
+//     (stream-K), so ragged batches balance to a tile. Each warp streams its range
+//     through private record-sized (14336 bytes for k4v2) bulk-copy stages: one
+//     stage in 12 warps (10 for k4v4) with the tile after next prefetched into L2,
+//     for many (sequence, kv-head) units; two stages in 8 warps (6 for k4v4) for at
+//     most as many units as SMs. It runs its GQA group (up to 8 q-heads) on
+//     m16n8k16 tensor-core MMAs, with an online softmax in the log2 domain:
 //       QK^T: A = q' = q_r r^K s^K per channel, fp16 hi part in rows 0-7 and fp16
 //             lo part in rows 8-15 (q' carried to ~22 bits), B = 4-bit key codes
 //             turned into fp16 in registers; score_j = c^K_j (D_hi + D_lo + beta),
