@@ -89,8 +89,11 @@ struct PrefillSource {
   ItemDiv hd;           // division by hkv
   int64_t num_blocks;
 
+  static constexpr bool kSparse = false;   // every item has a tile
   __device__ bool needs_load(int64_t) const { return true; }
-  __device__ void scatter(int64_t, int, int) const {}
+  __device__ void scatter_all(int) const {}
+  // every item has a tile: the block's next one
+  __device__ int64_t next_item(int64_t w, int) const { return w + gridDim.x; }
   // TMA coordinates (channel, token) of the item's 128 x 128 tile of tensor g
   __device__ void coords(int64_t w, int, int& x, int& y) const {
     const uint32_t chunk = hd.div(w);
@@ -132,6 +135,7 @@ struct AppendSource {
   int max_blocks;
   int64_t num_blocks;
 
+  static constexpr bool kSparse = true;    // only items whose sequence completes a tile
   __device__ bool needs_load(int64_t w) const {
     const int L = seq_lens[hd.div(w)];
     return L >= 0 && (L % kB) == kB - 1;
@@ -140,13 +144,11 @@ struct AppendSource {
     x = 0;
     y = (static_cast<int>(w) * 2 + g) * kB;
   }
-  // Threads t < 16 of group g copy 16 bytes each of item w's new token (tensor g)
-  // into its workspace row L % 128; thread 0 of the key group also writes the new
-  // length of the item's sequence (kv-head 0). The writers fence the global writes
-  // against the async proxy; a group barrier then orders them before the TMA copy
-  // of the tile.
+  // Thread t < 16 copies 16 bytes of item w's new token (tensor g) into its
+  // workspace row L % 128; thread 0 of tensor 0 also writes the new length of the
+  // item's sequence (kv-head 0). The writers fence the global writes against the
+  // async proxy.
   __device__ void scatter(int64_t w, int g, int t) const {
-    if (t < 0 || t >= 16) return;
     const uint32_t s = hd.div(w);
     const uint32_t h = static_cast<uint32_t>(w) - s * hkv;
     const int L = seq_lens[s];
@@ -156,6 +158,24 @@ struct AppendSource {
     *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
     if (g == 0 && h == 0 && t == 0 && seq_lens_out != nullptr) seq_lens_out[s] = L + 1;
     asm volatile("fence.proxy.async.global;" ::: "memory");
+  }
+  // All of the block's items (w = blockIdx.x + j gridDim.x), 32 threads an item (both
+  // tensors), before the block barrier that precedes its first tile copy.
+  __device__ void scatter_all(int tid) const {
+    for (int64_t j0 = 0; static_cast<int64_t>(blockIdx.x) + j0 * gridDim.x < n_items; j0 += kThreads / 32) {
+      const int64_t w = static_cast<int64_t>(blockIdx.x) + (j0 + tid / 32) * gridDim.x;
+      if (w < n_items) scatter(w, (tid >> 4) & 1, tid & 15);
+    }
+  }
+  // The block's next item after w whose tile completes (n_items if none): 32 of the
+  // block's items per round, one per lane, agreed by ballot (all 32 lanes call it).
+  __device__ int64_t next_item(int64_t w, int lane) const {
+    for (int64_t base = w + gridDim.x; base < n_items; base += 32 * static_cast<int64_t>(gridDim.x)) {
+      const int64_t c = base + static_cast<int64_t>(lane) * gridDim.x;
+      const unsigned m = __ballot_sync(0xffffffffu, c < n_items && needs_load(c));
+      if (m) return base + static_cast<int64_t>(__ffs(m) - 1) * gridDim.x;
+    }
+    return n_items;
   }
   struct Check {};
   __device__ Check prepare(int64_t, int) const { return Check{}; }
@@ -215,6 +235,9 @@ __global__ void __maxnreg__(128)
     const int i = e >> 7, kk = e & 127;
     *reinterpret_cast<uint16_t*>(smem + kOffH + sw_offset(i, kk)) = (__popc(i & kk) & 1) ? 0xBC00u : 0x3C00u;
   }
+  // appended tokens into the workspace (the block's items), ordered before any tile
+  // copy by the barrier below
+  src.scatter_all(tid);
   if (tid == 0) {
     for (int b = 0; b < 6; ++b) mbar_init(&mma_bar[b], 1);
     fence_mbar_init();
@@ -240,34 +263,36 @@ __global__ void __maxnreg__(128)
   uint8_t* tiles = smem + kOffIn + grp * 2 * kTileOp;   // this group's [buf]
   constexpr uint32_t kIdesc = idesc_f16_f32(128, 128);
 
-  // The copy of item w's tile is started one item ahead; the slot check of the
-  // next item is agreed on at the barrier that ends the current one.
+  // The block takes the items blockIdx.x + j gridDim.x that have a tile (all of them
+  // for the prefill; for the append, those whose sequence completes one). The copy of
+  // an item's tile is started one item ahead; the slot check of the next item is
+  // agreed on at the barrier that ends the current one.
   int64_t item = blockIdx.x;
+  if (Src::kSparse && !src.needs_load(item)) item = src.next_item(item, t);
   uint32_t pend = 0;               // bit b: a copy into buffer b has not been waited for
   uint32_t load_parity = 0;        // bit b: phase parity of buffer b's barrier
-  // appended tokens go into the workspace two items ahead of their tile's copy
-  src.scatter(item, grp, gt);
-  if (item + gridDim.x < src.n_items) src.scatter(item + gridDim.x, grp, gt - 16);
-  typename Src::Check check = src.prepare(item, gt);
+  const bool has_first = !Src::kSparse || item < src.n_items;
+  typename Src::Check check = has_first ? src.prepare(item, gt) : typename Src::Check{};
   int64_t dst = -1;
-  if (named_bar_and(bar_id, kGroupThreads, src.check_ok(check, gt)))
-    dst = src.target(item, check, gt, flags);
-  else if (gt == 0)
+  if (named_bar_and(bar_id, kGroupThreads, !has_first || src.check_ok(check, gt))) {
+    if (has_first) dst = src.target(item, check, gt, flags);
+  } else if (gt == 0) {
     raise_flag(flags, KVARN_FLAG_BAD_SLOTS);
+  }
   // Async work is spread over three threads of the group so that it overlaps:
   // gt == 0 issues the Hadamard products, gt == kTmaThread the tile copies and
   // gt == kStoreThread the record stores (bulk groups belong to the thread that
   // commits them, so it also waits for them).
   constexpr int kTmaThread = 64, kStoreThread = 32;
-  if (src.needs_load(item)) {
+  if (has_first) {
     if (gt == kTmaThread) issue_tile(src, item, grp, tiles, &load_bar[0]);
     pend = 1;
   }
   uint32_t mma_parity = 0;
   bool mma_inflight = false;       // thread gt == 0: an issued MMA not yet seen complete
-  for (int k = 0; item < src.n_items; ++k, item += gridDim.x) {
+  for (int k = 0; item < src.n_items; ++k) {
     const int buf = k & 1;
-    const int64_t next = item + gridDim.x;
+    const int64_t next = src.next_item(item, t);
     const bool has_next = next < src.n_items;
     bool ok = true;
     if ((pend >> buf) & 1u) {
@@ -293,12 +318,10 @@ __global__ void __maxnreg__(128)
     }
     typename Src::Check check_next{};
     if (has_next) {
-      if (src.needs_load(next)) {   // buffer buf ^ 1 was last read by the previous item
-        if (gt == kTmaThread) issue_tile(src, next, grp, tiles + (buf ^ 1) * kTileOp, &load_bar[buf ^ 1]);
-        pend |= 2u >> buf;
-      }
+      // buffer buf ^ 1 was last read by the previous item
+      if (gt == kTmaThread) issue_tile(src, next, grp, tiles + (buf ^ 1) * kTileOp, &load_bar[buf ^ 1]);
+      pend |= 2u >> buf;
       check_next = src.prepare(next, gt);
-      if (next + gridDim.x < src.n_items) src.scatter(next + gridDim.x, grp, gt);   // before this item's end barrier
     }
     if (dst >= 0) {
       uint8_t* stage = smem + (grp == 0 ? S::kOffStageK + buf * S::kStageK : S::kOffStageV + buf * S::kStageV);
@@ -343,6 +366,7 @@ __global__ void __maxnreg__(128)
       else if (gt == 0)
         raise_flag(flags, KVARN_FLAG_BAD_SLOTS);
     }
+    item = next;
   }
   // after a timeout: let copies and MMAs still in flight finish (bounded) before the
   // shared memory and TMEM are released
