@@ -25,6 +25,9 @@
 // The groups share only the Hadamard operand and the TMEM allocation (256 columns
 // each), so one group's MMA latency and barriers overlap the other's arithmetic.
 // The slot check of an item is agreed on at the barrier that ends the previous one.
+// The decode append runs the same kernel over (sequence, kv-head) items: the block
+// first writes the new tokens of all its items into the workspace, then quantizes
+// only the items whose sequence completes a tile.
 #include <cuda.h>
 
 #include <mutex>
