@@ -216,9 +216,37 @@ __device__ __forceinline__ void issue_tile(const Src& src, int64_t w, int g, uin
   tma_load_2d(dst + kTileOp / 2, map, x + 64, y, bar);
 }
 
+// Thread gt == 0 issues the next item's Hadamard products once the group's last TMEM
+// data of the current item is in registers, so that they run under its codes pass.
+struct NextProducts {
+  static constexpr bool kActive = true;
+  bool go;
+  int gt;
+  uint64_t* load_bar;   // the next tile's copy
+  uint32_t parity;
+  uint32_t sx, sh, d1, d2;
+  uint64_t* mma_bar;
+  unsigned* flags;
+  bool* inflight;
+  __device__ void operator()() const {
+    if (!go || gt != 0) return;
+    if (!mbar_wait(load_bar, parity, flags)) return;
+    constexpr uint32_t kIdesc = idesc_f16_f32(128, 128);
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+      const uint64_t dh = smem_desc_sw128(sw_kstep(sh, s));
+      const uint64_t dx = smem_desc_sw128(sw_kstep(sx, s));
+      umma_f16(d1, dh, dx, kIdesc, s > 0);   // D1[i][j] = sum_k H[i][k] X[j][k]
+      umma_f16(d2, dx, dh, kIdesc, s > 0);   // D2[j][i] = sum_k X[j][k] H[i][k]
+    }
+    umma_commit(mma_bar);
+    *inflight = true;
+  }
+};
+
 // 128 registers a thread (all that 512 threads can hold): a whole sweep in flight
 // needs 64 of them; 112 spilled and measured 5 % slower.
-template <class Src, int KB, int VB, bool kLean>
+template <class Src, int KB, int VB, bool kLean, bool kEarly>
 __global__ void __maxnreg__(128)
     quantize_kernel(const __grid_constant__ Src src, uint8_t* __restrict__ cache, int n_iters, float eps,
                     unsigned* flags) {
@@ -293,6 +321,7 @@ __global__ void __maxnreg__(128)
   }
   uint32_t mma_parity = 0;
   bool mma_inflight = false;       // thread gt == 0: an issued MMA not yet seen complete
+  bool early = false;              // this item's products went out under the previous item's codes
   for (int k = 0; item < src.n_items; ++k) {
     const int buf = k & 1;
     const int64_t next = src.next_item(item, t);
@@ -307,7 +336,7 @@ __global__ void __maxnreg__(128)
     }
     // the item's Hadamard products first, so the next item's bookkeeping below
     // (slot loads, the next tile copy) runs under them
-    if (dst >= 0 && gt == 0 && ok) {
+    if (dst >= 0 && gt == 0 && ok && !early) {
       const uint32_t sx = smem_u32(tiles + buf * kTileOp);
 #pragma unroll
       for (int s = 0; s < 8; ++s) {
@@ -326,6 +355,16 @@ __global__ void __maxnreg__(128)
       pend |= 2u >> buf;
       check_next = src.prepare(next, gt);
     }
+    // kEarly: the next item's products go out under this item's codes pass
+    const bool go_next = kEarly && has_next && ((pend >> (buf ^ 1)) & 1u) != 0;
+    if (dst < 0 && early && ok) {       // products of an item whose slots failed the check: consume them
+      ok = mbar_wait(&mma_bar[grp], mma_parity, flags);
+      if (ok) {
+        mma_parity ^= 1;
+        mma_inflight = false;
+      }
+    }
+    bool early_next = false;
     if (dst >= 0) {
       uint8_t* stage = smem + (grp == 0 ? S::kOffStageK + buf * S::kStageK : S::kOffStageV + buf * S::kStageV);
       if (gt == kStoreThread) bulk_wait_read<1>();   // the stage written two items ago has been stored
@@ -338,10 +377,21 @@ __global__ void __maxnreg__(128)
       }
       tc_fence_after();
       const uint8_t* tile = tiles + buf * kTileOp;
-      if (grp == 0)
-        ok = quantize_group<0, KB, kLean>(vec, stage, tile, ta1, ta2, line, p, n_iters, eps, bar_id, ok);
-      else
-        ok = quantize_group<1, VB, kLean>(vec, stage, tile, ta1, ta2, line, p, n_iters, eps, bar_id, ok);
+      early_next = go_next && ok;
+      if (!kEarly) {
+        if (grp == 0)
+          ok = quantize_group<0, KB, kLean>(vec, stage, tile, ta1, ta2, line, p, n_iters, eps, bar_id, ok);
+        else
+          ok = quantize_group<1, VB, kLean>(vec, stage, tile, ta1, ta2, line, p, n_iters, eps, bar_id, ok);
+      } else {
+        const NextProducts hook{early_next, gt, &load_bar[buf ^ 1], (load_parity >> (buf ^ 1)) & 1u,
+                                smem_u32(tiles + (buf ^ 1) * kTileOp), sh, d1, d2, &mma_bar[grp], flags,
+                                &mma_inflight};
+        if (grp == 0)
+          ok = quantize_group<0, KB, kLean>(vec, stage, tile, ta1, ta2, line, p, n_iters, eps, bar_id, ok, hook);
+        else
+          ok = quantize_group<1, VB, kLean>(vec, stage, tile, ta1, ta2, line, p, n_iters, eps, bar_id, ok, hook);
+      }
       if (!ok) break;                     // a copy or the tensor core never signalled (flag raised)
       fence_proxy_async_smem();
       tc_fence_before();
@@ -370,6 +420,7 @@ __global__ void __maxnreg__(128)
         raise_flag(flags, KVARN_FLAG_BAD_SLOTS);
     }
     item = next;
+    early = early_next;
   }
   // after a timeout: let copies and MMAs still in flight finish (bounded) before the
   // shared memory and TMEM are released
@@ -396,14 +447,27 @@ cudaError_t launch_quantize_bits(const Src& src, uint8_t* cache, int n_iters, fl
                             cudaStream_t stream, int max_ctas) {
   if (src.n_items <= 0) return cudaSuccess;
   if (src.n_items > INT32_MAX) return cudaErrorInvalidValue;
-  static std::atomic<unsigned long long> smem_set{0};
-  cudaError_t err = set_smem_once(quantize_kernel<Src, KB, VB, kLean>, QSmem<KB, VB>::kBytes, smem_set);
-  if (err != cudaSuccess) return err;
   int64_t grid = sm_count();
   if (max_ctas > 0 && grid > max_ctas) grid = max_ctas;
   if (grid > src.n_items) grid = src.n_items;
-  quantize_kernel<Src, KB, VB, kLean><<<static_cast<unsigned>(grid), kThreads, QSmem<KB, VB>::kBytes, stream>>>(src, cache, n_iters, eps,
-                                                                                             flags);
+  // The prefill with 4-bit keys and more than one iteration issues each item's
+  // products under the previous item's codes pass (measured slower for k2v2, for one
+  // iteration and for the append, whose blocks get one or two items).
+  if constexpr (!Src::kSparse && KB == 4) {
+    if (n_iters > 1) {
+      static std::atomic<unsigned long long> smem_set{0};
+      cudaError_t err = set_smem_once(quantize_kernel<Src, KB, VB, kLean, true>, QSmem<KB, VB>::kBytes, smem_set);
+      if (err != cudaSuccess) return err;
+      quantize_kernel<Src, KB, VB, kLean, true><<<static_cast<unsigned>(grid), kThreads, QSmem<KB, VB>::kBytes,
+                                                  stream>>>(src, cache, n_iters, eps, flags);
+      return cudaGetLastError();
+    }
+  }
+  static std::atomic<unsigned long long> smem_set{0};
+  cudaError_t err = set_smem_once(quantize_kernel<Src, KB, VB, kLean, false>, QSmem<KB, VB>::kBytes, smem_set);
+  if (err != cudaSuccess) return err;
+  quantize_kernel<Src, KB, VB, kLean, false><<<static_cast<unsigned>(grid), kThreads, QSmem<KB, VB>::kBytes, stream>>>(
+      src, cache, n_iters, eps, flags);
   return cudaGetLastError();
 }
 

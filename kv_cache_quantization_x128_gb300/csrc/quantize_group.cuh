@@ -175,10 +175,17 @@ __device__ __forceinline__ void group_zero_scale(uint16_t* meta, float* vw, floa
 // writes the group's stage (codes + metadata). `tile` is the item's fp16 operand
 // (canonical layout), `line`/`p` locate the thread's half line, `ta1`/`ta2` are
 // its TMEM addresses of D1 and D2.
-template <int kKind, int kBits, bool kLean>
+// A hook that quantize_group runs once the item's last TMEM data is in registers.
+struct NoHook {
+  static constexpr bool kActive = false;
+  bool go = false;
+  __device__ void operator()() const {}
+};
+
+template <int kKind, int kBits, bool kLean, class Hook = NoHook>
 __device__ __forceinline__ bool quantize_group(float* vec, uint8_t* stage, const uint8_t* tile, uint32_t ta1,
                                                uint32_t ta2, int line, int p, int n_iters, float eps, int bar_id,
-                                               bool ok) {
+                                               bool ok, const Hook& hook = Hook()) {
   float* va = vec + kVA * kVec;
   float* vb = vec + kVB * kVec;
   float* vg = vec + kVG * kVec;
@@ -306,6 +313,12 @@ __device__ __forceinline__ bool quantize_group(float* vec, uint8_t* stage, const
   constexpr float kLevels = static_cast<float>((1 << kBits) - 1);
   const float2 own2 = make_float2(own, own);
   tmem_wait_line(x);
+  if (Hook::kActive && hook.go) {   // the group has read its TMEM for this item: the hook may reuse it
+    tc_fence_before();
+    named_bar(bar_id, kGroupThreads);
+    tc_fence_after();
+    hook();
+  }
 #pragma unroll
   for (int hh = 0; hh < 2; ++hh) {
     const float* xh = x + 32 * hh;
