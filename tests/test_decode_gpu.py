@@ -130,6 +130,34 @@ def test_decode_4x128k_sampled(env):
     _config_case(env, 4, 131072, 8, 64, seed=3, n_pairs=32)
 
 
+def test_ragged_lengths_many_units(env):
+    """More (sequence, kv-head) units than SMs, so the split phase runs its 12-warp,
+    one-stage shape with the L2 prefetch: 200 sequences cycling through empty, one-token,
+    tile-edge and multi-tile lengths (with workspace tails), GQA 8, one kv-head; then
+    the same batch with one block-table entry out of range."""
+    kv, _ = env
+    pattern = [0, 1, 127, 128, 129, 255, 256, 300, 383, 640]
+    lens = np.array([pattern[i % len(pattern)] for i in range(200)], np.int32)
+    cache, bt, ws, nb = oracle_cache(1, lens, seed=36, max_blocks=5)
+    q = synth.queries(len(lens), 8, seed=37)
+    out, flags = gpu_decode(env, q, cache, ws, bt, lens, 1, nb)
+    assert flags == 0
+    pairs = [(s, 0) for s in range(len(lens)) if lens[s] > 0]
+    ref = o.decode(q.astype(np.float64), cache, ws, bt, lens, pairs=pairs)
+    ref[lens == 0] = 0.0
+    assert_decode_close(out, ref, "many units")
+    # one sequence's second block out of range: flagged, that tile skipped, the rest exact
+    s_bad = int(np.nonzero(lens == 640)[0][0])
+    bt_bad = bt.copy()
+    bt_bad[s_bad, 1] = nb + 7
+    out2, flags2 = gpu_decode(env, q, cache, ws, bt_bad, lens, 1, nb)
+    assert flags2 & kv.FLAG_BAD_BLOCK
+    assert np.isfinite(out2).all()
+    keep = np.ones(len(lens), bool)
+    keep[s_bad] = False
+    assert_decode_close(out2[keep], ref[keep], "many units, other sequences")
+
+
 def test_bad_block_is_skipped_and_flagged(env):
     kv, _ = env
     hkv = 1
