@@ -814,6 +814,54 @@ def run_decode_long(args):
                       "tokens_per_s": round(n_seqs / (ms * 1e-3), 1)}), flush=True)
 
 
+# `--case tile`: one tile-head, the latency case (not the headline line): quantize
+# one 128 x 128 fp16 K and V tile (4 outlier key channels x20) into its record, and
+# decode one query over it; each call timed alone (median), L2 flushed before it.
+def run_tile(args):
+    import numpy as np
+    import torch
+    import kvarn_synth as synth
+    import kv_cache_quantization_x128_gb300 as kv
+    torch.cuda.set_device(0)
+    k, v, q = synth.single_tile(0)
+    f16 = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.float16).cuda()
+    kd, vd, qd = f16(k[:, None, :]), f16(v[:, None, :]), f16(q[None])
+    cache = torch.zeros((1, 1, RECORD), dtype=torch.uint8, device="cuda")
+    slots = torch.arange(128, dtype=torch.int64, device="cuda")
+    bt = torch.zeros((1, 1), dtype=torch.int32, device="cuda")
+    lens = torch.full((1,), 128, dtype=torch.int32, device="cuda")
+    out = torch.empty_like(qd)
+    meta = kv.make_meta(1, 1, 1, max_blocks_per_seq=1)
+    scratch = torch.empty(kv.decode_scratch_bytes(meta, 1), dtype=torch.uint8, device="cuda")
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+
+    def timed(fn):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(args.steps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        return float(np.median(ts))
+
+    tq = timed(lambda: kv.kvarn_quantize_tiles(kd, vd, slots, cache, meta))
+    td = timed(lambda: kv.kvarn_decode_attention(qd, cache, None, bt, lens, out, scratch, meta))
+    if kv.kvarn_device_flags() != 0:
+        raise SystemExit("the tile case raised a device flag")
+    print(json.dumps({"metric": "single_tile_latency_us", "value": round((tq + td) * 1e3, 1), "unit": "us",
+                      "steps": args.steps, "warmup": args.warmup, "higher_is_better": False,
+                      "dtype": "f32 statistics and accumulation on fp16 inputs", "data": "synthetic",
+                      "config": {"workload": "single_tile: one 128 x 128 tile-head quantized, one query decoded over it",
+                                 "preset": "kvarn_k4v2_g128", "l2": "flushed"},
+                      "quantize_us": round(tq * 1e3, 1), "decode_us": round(td * 1e3, 1)}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -822,11 +870,12 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--case", default="full", choices=["full", "small", "prefill_attn", "serve", "decode_long"],
+    ap.add_argument("--case", default="full", choices=["full", "small", "prefill_attn", "serve", "decode_long", "tile"],
                     help="small: reduced shapes for profiler captures (not a bench line); "
                          "prefill_attn: the chunked-prefill attention kernel alone; "
                          "serve: the 256-sequence serving step (append + decode); "
-                         "decode_long: the 4 x 131072-token decode alone")
+                         "decode_long: the 4 x 131072-token decode alone; "
+                         "tile: one tile-head quantized and decoded (latency)")
     ap.add_argument("--preset", default="k4v2", choices=sorted(PRESET_RECORD),
                     help="bit preset of the gb300 arm; the default k4v2 is the headline workload")
     args = ap.parse_args()
@@ -846,6 +895,8 @@ def main():
         run_serve(args)
     elif args.case == "decode_long":
         run_decode_long(args)
+    elif args.case == "tile":
+        run_tile(args)
     elif args.impl == "reference":
         run_reference(args)
     else:

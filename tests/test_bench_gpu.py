@@ -1,6 +1,6 @@
 """bench.py prints one JSON line with the keys its consumers read: the profiling
-case of the headline workload, and the prefill-attention, serving-step and
-long-context decode cases, each run briefly."""
+case of the headline workload, and the prefill-attention, serving-step,
+long-context decode and single-tile cases, each run briefly."""
 import json
 import os
 import subprocess
@@ -51,3 +51,9 @@ def test_bench_decode_long_line():
     d = _run("--case", "decode_long", "--steps", "2", "--warmup", "3")
     assert d["metric"] == "decode_attention_gbs" and d["unit"] == "GB/s"
     assert d["value"] > 0 and d["ms_per_call"] > 0 and 0 < d["frac_hbm"] < 2
+
+
+def test_bench_tile_line():
+    d = _run("--case", "tile", "--steps", "3", "--warmup", "3")
+    assert d["metric"] == "single_tile_latency_us" and d["higher_is_better"] is False
+    assert d["quantize_us"] > 0 and d["decode_us"] > 0
