@@ -171,17 +171,19 @@ __device__ __forceinline__ void group_zero_scale(uint16_t* meta, float* vw, floa
   vc0[pl] = fmaf(-z, inv_s, 0.5f) * (1.0f / kLevels);
 }
 
-// Quantize the tensor of group g (0 = K, 1 = V) of the current item from TMEM;
-// writes the group's stage (codes + metadata). `tile` is the item's fp16 operand
-// (canonical layout), `line`/`p` locate the thread's half line, `ta1`/`ta2` are
-// its TMEM addresses of D1 and D2.
-// A hook that quantize_group runs once the item's last TMEM data is in registers.
+// A hook that quantize_group runs, after a group barrier, once the item's last TMEM
+// data is in registers (when kActive and go): the caller may then reuse the group's
+// TMEM. NoHook: none.
 struct NoHook {
   static constexpr bool kActive = false;
   bool go = false;
   __device__ void operator()() const {}
 };
 
+// Quantize the tensor of group g (0 = K, 1 = V) of the current item from TMEM;
+// writes the group's stage (codes + metadata). `tile` is the item's fp16 operand
+// (canonical layout), `line`/`p` locate the thread's half line, `ta1`/`ta2` are
+// its TMEM addresses of D1 and D2.
 template <int kKind, int kBits, bool kLean, class Hook = NoHook>
 __device__ __forceinline__ bool quantize_group(float* vec, uint8_t* stage, const uint8_t* tile, uint32_t ta1,
                                                uint32_t ta2, int line, int p, int n_iters, float eps, int bar_id,
