@@ -137,3 +137,38 @@ def test_serving_step_256_ragged(env):
     for s, h in pairs:
         assert_decode_close(out[s, h * g:(h + 1) * g], ref[s, h * g:(h + 1) * g], f"seq {s} head {h}")
     assert np.isfinite(out).all()
+
+
+def test_append_many_items(env):
+    """More (sequence, kv-head) items than 32 per block (1300 sequences x 4 kv-heads,
+    ~34 items a block), so each block finds its next completing item over more than
+    one ballot round; every 7th sequence completes a tile. The new rows, the lengths,
+    64 sampled completed tiles against the oracle, and every other block untouched."""
+    n_seqs, hkv, max_blocks = 1300, 4, 5
+    rng = np.random.default_rng(43)
+    lens = rng.integers(0, 600, n_seqs).astype(np.int32)
+    lens[::7] = (lens[::7] // 128) * 128 + 127
+    num_blocks = n_seqs * max_blocks
+    bt = synth.block_tables(n_seqs, max_blocks, num_blocks, seed=43)
+    ws = synth.workspace_tokens(n_seqs, hkv, seed=43)
+    cache = np.zeros((num_blocks, hkv, o.RECORD_BYTES), np.uint8)
+    k_new, v_new = synth.prefill_kv(n_seqs, hkv, seed=44)
+    ws_d, cache_d, lens_out, flags = gpu_append(env, k_new, v_new, lens, bt, ws, cache, num_blocks)
+    assert flags == 0 and (lens_out == lens + 1).all()
+    ws_g = dev_to_f16(ws_d)
+    rows = lens % 128
+    s_idx = np.arange(n_seqs)
+    assert np.array_equal(ws_g[s_idx, :, 0, rows], k_new) and np.array_equal(ws_g[s_idx, :, 1, rows], v_new)
+    keep = np.ones(ws.shape, bool)
+    keep[s_idx, :, :, rows] = False
+    assert np.array_equal(ws_g[keep].view(np.int16), ws[keep].view(np.int16))
+    done = np.nonzero(lens % 128 == 127)[0]
+    blocks = bt[done, lens[done] // 128]
+    cache_g = cache_d.cpu().numpy()
+    pick = rng.choice(len(done) * hkv, size=64, replace=False)
+    ss, hh = done[pick // hkv], pick % hkv
+    _, kq, vq = o.quantize_tiles(ws_g[ss, hh, 0], ws_g[ss, hh, 1])
+    print("many items", compare_records(cache_g[blocks[pick // hkv], hh], kq, vq))
+    untouched = np.ones(num_blocks, bool)
+    untouched[blocks] = False
+    assert not cache_g[untouched].any()
