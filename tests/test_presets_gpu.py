@@ -233,3 +233,34 @@ def test_quantize_16x16k_sampled(env, preset):
     blocks = np.array([slots[c * 128] // 128 for c, _ in pairs])
     heads = np.array([h for _, h in pairs])
     print(preset, "16 x 16384", compare_records(got[blocks, heads], kq, vq))
+
+
+@pytest.mark.parametrize("preset", PRESETS)
+def test_decode_4x128k_oracle_pairs(env, preset):
+    """The long-context decode (4 sequences x 131072 tokens, 64 q-heads over 8
+    kv-heads: a few long units, the two-stage split shape and the merge that splits
+    a unit's records four ways) in each preset's layout: 4 sampled (sequence, kv-head)
+    pairs hold oracle-quantized K/V of the prefill distribution in every block, random
+    valid records fill the rest."""
+    from tests.oracle_pool import run_pairs
+    kv, torch = env
+    n_seqs, seq_len, hkv, hq, seed = 4, 131072, 8, 64, 81
+    max_blocks = seq_len // 128
+    num_blocks = n_seqs * max_blocks
+    lay = o.LAYOUTS[preset]
+    bt = synth.block_tables(n_seqs, max_blocks, num_blocks, seed)
+    recs = synth.random_records(num_blocks * hkv, seed, lay.record_bytes, lay.k_code_bytes + lay.v_code_bytes)
+    recs = recs.reshape(num_blocks, hkv, -1)
+    q = synth.queries(n_seqs, hq, seed)
+    g = hq // hkv
+    pairs = [(0, 3), (1, 0), (2, 7), (3, 5)]
+    res = run_pairs([(1_000_003 * seed + 64 * s + h, seq_len, q[s, h * g:(h + 1) * g], preset) for s, h in pairs])
+    for (s, h), (r, _, _) in zip(pairs, res):
+        recs[bt[s], h] = r
+    lens = np.full(n_seqs, seq_len, np.int32)
+    out, flags = _gpu_decode(env, q, torch.from_numpy(recs).cuda(), None, bt, lens, hkv, num_blocks, preset)
+    assert flags == 0 and np.isfinite(out).all()
+    worst = 0.0
+    for (s, h), (_, _, ref) in zip(pairs, res):
+        worst = max(worst, assert_decode_close(out[s, h * g:(h + 1) * g], ref, f"{preset} seq {s} head {h}"))
+    print(preset, f"{len(pairs)} oracle-quantized pairs at 4 x 131072, max |err| {worst:.2e}")
