@@ -149,7 +149,8 @@ def test_serve_step_graph_replay(env):
         assert torch.equal(out.view(torch.int16), want_out.view(torch.int16)), replay
 
 
-def test_serve_step_256_ragged_against_oracle(env):
+@pytest.mark.parametrize("preset", ["k4v2", "k4v4", "k2v2", "k4v2l"])
+def test_serve_step_256_ragged_against_oracle(env, preset):
     """The mixed serving step at its full shape through the one-launch entry point,
     against the oracle: 256 sequences with lengths log-uniform in [1024, 32768] (every
     8th forced to L % 128 == 127, so the append completes its tile), 64 q-heads over
@@ -158,7 +159,8 @@ def test_serve_step_256_ragged_against_oracle(env):
     random valid records and workspace tokens fill the rest. Checked against
     oracle.append + oracle.decode: the whole workspace and the new lengths bit for
     bit, every completed tile within the record tolerances, every other record
-    untouched, and the attention of the sampled pairs within the decode tolerance."""
+    untouched, and the attention of the sampled pairs within the decode tolerance.
+    The other presets sample 8 sequences instead of 24."""
     from tests.oracle_pool import run_pairs
     from tests.parity import assert_decode_close, compare_records
     kv, torch = env
@@ -176,20 +178,22 @@ def test_serve_step_256_ragged_against_oracle(env):
         nb = (lens[s] + 1 + 127) // 128
         bt[s, :nb] = perm[pos:pos + nb]
         pos += nb
-    recs = synth.random_records(num_blocks * hkv, seed, o.RECORD_BYTES, 12288).reshape(num_blocks, hkv, -1)
+    lay = o.LAYOUTS[preset]
+    recs = synth.random_records(num_blocks * hkv, seed, lay.record_bytes, lay.k_code_bytes + lay.v_code_bytes)
+    recs = recs.reshape(num_blocks, hkv, -1)
     ws = synth.workspace_tokens(n_seqs, hkv, seed)
     rng = np.random.default_rng(seed)
     done = [s for s in range(n_seqs) if lens[s] % 128 == 127]
-    seqs = sorted(set(rng.choice(n_seqs, 24, replace=False).tolist()) | set(done[::4]))
+    seqs = sorted(set(rng.choice(n_seqs, 24 if preset == "k4v2" else 8, replace=False).tolist()) | set(done[::4]))
     pairs = [(s, int(rng.integers(0, hkv))) for s in seqs]
-    res = run_pairs([(7_000_001 + 64 * s + h, int(lens[s]), None, "k4v2") for s, h in pairs])
+    res = run_pairs([(7_000_001 + 64 * s + h, int(lens[s]), None, preset) for s, h in pairs])
     for (s, h), (r, tail, _) in zip(pairs, res):
         recs[bt[s, :lens[s] // 128], h] = r
         ws[s, h] = tail
     k_new, v_new = synth.prefill_kv(n_seqs, hkv, seed=seed + 1)
     q = synth.queries(n_seqs, hq, seed)
     f16 = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.float16).cuda()
-    meta = kv.make_meta(hkv, hq, num_blocks, max_blocks_per_seq=max_blocks)
+    meta = kv.make_meta(hkv, hq, num_blocks, max_blocks_per_seq=max_blocks, preset=preset)
     ws_d, cache_d = f16(ws), torch.from_numpy(recs).cuda()
     lens_out = torch.full((n_seqs,), -7, dtype=torch.int32, device="cuda")
     out = torch.full((n_seqs, hq, 128), float("nan"), dtype=torch.float16, device="cuda")
@@ -206,7 +210,7 @@ def test_serve_step_256_ragged_against_oracle(env):
     blocks = np.array([bt[s, lens[s] // 128] for s in done]).repeat(hkv)
     heads = np.tile(np.arange(hkv), len(done))
     _, kq, vq = o.quantize_tiles(np.stack([ws_ref[s, :, 0] for s in done]).reshape(-1, 128, 128),
-                                 np.stack([ws_ref[s, :, 1] for s in done]).reshape(-1, 128, 128))
+                                 np.stack([ws_ref[s, :, 1] for s in done]).reshape(-1, 128, 128), preset=preset)
     print("completed tiles", compare_records(cache_g[blocks, heads], kq, vq))
     untouched = np.ones(cache_g.shape[:2], bool)
     untouched[blocks, heads] = False
