@@ -84,11 +84,13 @@ def test_prefill_small_all_tokens(env, preset):
     print(preset, "prefill max err", assert_decode_close(out[:n], ref[:n], preset))
 
 
-def test_prefill_group_8_long_context_sampled(env):
-    """4 sequences with 4000-6000 cached tokens (random records) and chunks of
-    120-260 tokens, 64 q-heads over 8 kv-heads; sampled (token, kv-head) pairs."""
+@pytest.mark.parametrize("preset", ["k4v2", "k4v4", "k2v2", "k4v2l"])
+def test_prefill_group_8_long_context_sampled(env, preset):
+    """4 sequences with 4000-6000 cached tokens (random records of the preset) and
+    chunks of 120-260 tokens, 64 q-heads over 8 kv-heads; sampled (token, kv-head)
+    pairs."""
     lens, chunks = [4000, 6000, 4352, 5000], [260, 120, 256, 200]
-    c = _case(lens, chunks, hkv=8, group=8, seed=82, random_cache=True)
+    c = _case(lens, chunks, hkv=8, group=8, seed=82, preset=preset, random_cache=True)
     out, flags = _gpu(env, c)
     assert flags == 0 and np.isfinite(out).all()
     rng = np.random.default_rng(82)
