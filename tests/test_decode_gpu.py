@@ -130,16 +130,17 @@ def test_decode_4x128k_sampled(env):
     _config_case(env, 4, 131072, 8, 64, seed=3, n_pairs=32)
 
 
-def test_ragged_lengths_many_units(env):
+@pytest.mark.parametrize("group", [1, 3, 8])
+def test_ragged_lengths_many_units(env, group):
     """More (sequence, kv-head) units than SMs, so the split phase runs its 12-warp,
     one-stage shape with the L2 prefetch: 200 sequences cycling through empty, one-token,
-    tile-edge and multi-tile lengths (with workspace tails), GQA 8, one kv-head; then
-    the same batch with one block-table entry out of range."""
+    tile-edge and multi-tile lengths (with workspace tails), one kv-head with 1, 3 or 8
+    q-heads; then the same batch with one block-table entry out of range."""
     kv, _ = env
     pattern = [0, 1, 127, 128, 129, 255, 256, 300, 383, 640]
     lens = np.array([pattern[i % len(pattern)] for i in range(200)], np.int32)
     cache, bt, ws, nb = oracle_cache(1, lens, seed=36, max_blocks=5)
-    q = synth.queries(len(lens), 8, seed=37)
+    q = synth.queries(len(lens), group, seed=37)
     out, flags = gpu_decode(env, q, cache, ws, bt, lens, 1, nb)
     assert flags == 0
     pairs = [(s, 0) for s in range(len(lens)) if lens[s] > 0]
