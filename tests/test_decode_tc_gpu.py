@@ -41,6 +41,11 @@ def test_bad_block_is_skipped_and_flagged(env, tc):
     D.test_bad_block_is_skipped_and_flagged(env)
 
 
+@pytest.mark.parametrize("group", [1, 8])
+def test_ragged_lengths_many_units(env, tc, group):
+    D.test_ragged_lengths_many_units(env, group)
+
+
 def test_length_beyond_block_table_is_clipped_and_flagged(env, tc):
     D.test_length_beyond_block_table_is_clipped_and_flagged(env)
 
