@@ -246,7 +246,8 @@ cudaError_t launch_decode(const uint16_t* q, const uint8_t* cache, const uint16_
     if (err != cudaSuccess) return err;
   }
   // units with 8 or more partial records on average: the records of a q-head split 4 ways
-  const bool long_units = static_cast<int64_t>(a.n_ctas) * a.warps >= 8 * units;
+  // (a unit has no more records than tiles, so short block tables never qualify)
+  const bool long_units = static_cast<int64_t>(a.n_ctas) * a.warps >= 8 * units && max_blocks >= 8;
   return long_units ? launch_after(decode_merge_kernel<1, 4>, dim3(hkv, n_seqs), dim3(1024), 0, stream, a, ws, out)
                     : launch_after(decode_merge_kernel<4, 1>, dim3(hkv, n_seqs), dim3(256), 0, stream, a, ws, out);
 }
