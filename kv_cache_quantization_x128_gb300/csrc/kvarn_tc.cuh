@@ -32,6 +32,24 @@ __host__ __device__ constexpr uint32_t sw_offset(int r, int k) {
   return static_cast<uint32_t>((k >> 6) * 16384 + (r >> 3) * 1024 + (r & 7) * 128 +
                                ((((k & 63) >> 3) ^ (r & 7)) << 4) + (k & 7) * 2);
 }
+// The Sylvester +-1 Hadamard operand H[r][k] = (-1)^popcount(r & k) (fp16) in that
+// layout, written by threads tid = 0 .. nthreads - 1 one 16-byte chunk (k = 8m .. 8m + 7
+// of row r) at a time: popcount(r & (8m + j)) = popcount(r & 8m) + popcount(r & j)
+// for j < 8, so a chunk is row r's pattern over j, negated when r & 8m has odd parity.
+__device__ __forceinline__ void fill_hadamard_sw128(uint8_t* dst, int tid, int nthreads) {
+  for (int e = tid; e < 128 * 16; e += nthreads) {
+    const int r = e >> 4, m = e & 15;
+    const uint32_t flip = (__popc(r & (8 * m)) & 1) ? 0x80008000u : 0u;
+    uint32_t w[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t lo = (__popc(r & (2 * j)) & 1) ? 0xBC00u : 0x3C00u;
+      const uint32_t hi = (__popc(r & (2 * j + 1)) & 1) ? 0xBC00u : 0x3C00u;
+      w[j] = (lo | (hi << 16)) ^ flip;
+    }
+    *reinterpret_cast<uint4*>(dst + sw_offset(r, 8 * m)) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
 // Shared-memory matrix descriptor of that layout: 8-row groups 1024 B apart
 // (stride byte offset), 128-byte swizzle (mode 2 in bits [61, 64)); the leading
 // byte offset is unused when the K extent of one MMA lies inside the swizzle row.

@@ -260,12 +260,14 @@ __global__ void __maxnreg__(128)
   uint64_t* load_bar = mma_bar + 2 + 2 * grp;   // this group's [buf]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + S::kOffTmem);
   if (static_cast<int64_t>(blockIdx.x) >= src.n_items) return;
+  // Async work is spread over three threads of the group so that it overlaps:
+  // gt == 0 issues the Hadamard products, gt == kTmaThread the tile copies and
+  // gt == kStoreThread the record stores (bulk groups belong to the thread that
+  // commits them, so it also waits for them).
+  constexpr int kTmaThread = 64, kStoreThread = 32;
+  uint8_t* tiles = smem + kOffIn + grp * 2 * kTileOp;   // this group's [buf]
 
-  // Sylvester +-1 Hadamard operand (H[i][k] = (-1)^popcount(i & k)), swizzled layout
-  for (int e = tid; e < kD * kD; e += kThreads) {
-    const int i = e >> 7, kk = e & 127;
-    *reinterpret_cast<uint16_t*>(smem + kOffH + sw_offset(i, kk)) = (__popc(i & kk) & 1) ? 0xBC00u : 0x3C00u;
-  }
+  fill_hadamard_sw128(smem + kOffH, tid, kThreads);   // the +-1 Hadamard operand
   // appended tokens into the workspace (the block's items), ordered before any tile
   // copy by the barrier below
   src.scatter_all(tid);
@@ -291,7 +293,6 @@ __global__ void __maxnreg__(128)
   const uint32_t ta2 = ta1 + 128;
   float* vec = reinterpret_cast<float*>(smem + S::kOffVec) + grp * kNumVec * kVec;
   const uint32_t sh = smem_u32(smem + kOffH);
-  uint8_t* tiles = smem + kOffIn + grp * 2 * kTileOp;   // this group's [buf]
   constexpr uint32_t kIdesc = idesc_f16_f32(128, 128);
 
   // The block takes the items blockIdx.x + j gridDim.x that have a tile (all of them
@@ -310,11 +311,6 @@ __global__ void __maxnreg__(128)
   } else if (gt == 0) {
     raise_flag(flags, KVARN_FLAG_BAD_SLOTS);
   }
-  // Async work is spread over three threads of the group so that it overlaps:
-  // gt == 0 issues the Hadamard products, gt == kTmaThread the tile copies and
-  // gt == kStoreThread the record stores (bulk groups belong to the thread that
-  // commits them, so it also waits for them).
-  constexpr int kTmaThread = 64, kStoreThread = 32;
   if (has_first) {
     if (gt == kTmaThread) issue_tile(src, item, grp, tiles, &load_bar[0]);
     pend = 1;

@@ -159,11 +159,7 @@ __device__ void serve_append(const ServeArgs& sa, uint8_t* smem) {
   float* vec = reinterpret_cast<float*>(smem + S::kOffVec);
   uint8_t* xt = smem + S::kOffX;
 
-  // Sylvester +-1 Hadamard operand (H[i][k] = (-1)^popcount(i & k)), swizzled layout
-  for (int e = tid; e < kD * kD; e += kServeThreads) {
-    const int i = e >> 7, kk = e & 127;
-    *reinterpret_cast<uint16_t*>(smem + S::kOffH + sw_offset(i, kk)) = (__popc(i & kk) & 1) ? 0xBC00u : 0x3C00u;
-  }
+  fill_hadamard_sw128(smem + S::kOffH, tid, kServeThreads);   // the +-1 Hadamard operand
   if (tid == 0) {
     mbar_init(bar, 1);
     fence_mbar_init();
