@@ -108,6 +108,7 @@ def test_append_rejects_aliasing_and_nulls(kv):
     assert ap(A, A, A, None, A, -1, A, A, ctypes.byref(m), None) == 1
     m0 = kv.make_meta(8, 64, 16, max_blocks_per_seq=0)
     assert ap(A, A, A, None, A, 4, A, A, ctypes.byref(m0), None) == 1
+    assert ap(A, A, A, B, A, 0, A, A, ctypes.byref(m), None) == 0      # no sequences: nothing to do
 
 
 def test_decode_rejects_small_scratch(kv):
@@ -115,6 +116,7 @@ def test_decode_rejects_small_scratch(kv):
     need = kv.decode_scratch_bytes(m, 4)
     dec = _raw(kv, "kvarn_decode_attention")
     assert dec(A, A, A, A, A, 4, A, A, need - 16, ctypes.byref(m), None) == 4
+    assert dec(A, A, A, A, A, 0, A, A, 0, ctypes.byref(m), None) == 0          # no sequences: nothing to do
     assert dec(A, A, A, A, A, 4, A, None, need, ctypes.byref(m), None) == 1     # NULL scratch
     assert dec(A, A, A, A, A, 4, None, A, need, ctypes.byref(m), None) == 1     # NULL out
 
