@@ -645,10 +645,10 @@ __device__ __forceinline__ void merge_ws_part(const DecodeArgs& a, const uint16_
 // took its first tile to the one that took its last, as the split phase marked them
 // (ranges are contiguous and ordered; an empty range in between left no record; a
 // unit without both marks, after a timed-out split warp, merges no records).
-__device__ __forceinline__ void covering_warps(const DecodeArgs& a, int s, int64_t u, int64_t& wlo, int64_t& whi) {
+// `cv` is the unit's pair of marks, loaded by the caller with the sequence's length.
+__device__ __forceinline__ void covering_warps(const DecodeArgs& a, int s, int2 cv, int64_t& wlo, int64_t& whi) {
   wlo = whi = 0;
   if (full_tiles(a, s) > 0) {
-    const int2 cv = *reinterpret_cast<const int2*>(a.cover + 2 * u);
     if (cv.x >= 0 && cv.y >= cv.x && cv.y < static_cast<int64_t>(a.n_ctas) * a.warps) {
       wlo = cv.x;
       whi = static_cast<int64_t>(cv.y) + 1;
@@ -792,13 +792,14 @@ __device__ __forceinline__ void merge_body(const DecodeArgs& a, const uint16_t* 
                                            RecShares<kParts>* rs, const int64_t* rg) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gg = warp & 7, share = warp >> 3;
+  const int64_t u = static_cast<int64_t>(s) * a.hkv + h;
+  const int2 cv = *reinterpret_cast<const int2*>(a.cover + 2 * u);   // in flight with the length
   const int n_ws = ws_tokens(a, ws, s, threadIdx.x == 0);
   if (warp < 8) merge_ws_part(a, ws, h, s, n_ws, warp, sm);
-  const int64_t u = static_cast<int64_t>(s) * a.hkv + h;
   float M = -INFINITY, l = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
   if (gg < a.group) {
     int64_t wlo, whi;
-    covering_warps(a, s, u, wlo, whi);
+    covering_warps(a, s, cv, wlo, whi);
     merge_records<kBatch, kParts>(a, rg, u, gg, wlo, whi, share, M, l, acc);
     if (kParts > 1 && share > 0) {
       float* dst = rs->v[share - 1][gg];
