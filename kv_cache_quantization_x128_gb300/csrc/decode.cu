@@ -111,18 +111,26 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_split_kernel(DecodeAr
   decode_tc_body<kLean>(a);
 }
 
+// The merge kernel's wait for the split kernel (its ranges, marks and records).
+struct SplitWait {
+  static constexpr bool kReady = false;
+  __device__ void operator()() const { griddep_wait(); }
+};
+
 // One CTA of 8 kParts warps per (kv-head, sequence). For batches of many short units
 // (a few partial records each): kParts 1 and kMinBlocks 4, so that 4 CTAs (at 64
 // registers) share an SM. For a few long units (tens of records each): kParts 4, the
 // records of a q-head split between 4 warps.
+
 template <int kMinBlocks, int kParts>
 __global__ void __launch_bounds__(256 * kParts, kMinBlocks) decode_merge_kernel(DecodeArgs a,
                                                                                const uint16_t* __restrict__ ws,
                                                                                uint16_t* __restrict__ out) {
   __shared__ WsPart sm;
   __shared__ RecShares<kParts> rs;
-  griddep_wait();                       // the split kernel's ranges and partial records
-  merge_body<8, kParts>(a, ws, out, blockIdx.x, blockIdx.y, sm, &rs, a.ranges);
+  // the workspace tokens first (inputs only), then wait for the split kernel's
+  // ranges and partial records
+  merge_body<8, kParts, SplitWait>(a, ws, out, blockIdx.x, blockIdx.y, sm, &rs, a.ranges);
 }
 
 // Launch with programmatic stream serialization (see griddep_wait).

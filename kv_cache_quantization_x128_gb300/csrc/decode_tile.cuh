@@ -781,21 +781,34 @@ __device__ __forceinline__ void merge_finish(const DecodeArgs& a, uint16_t* __re
       make_uint2(res[0] | (static_cast<uint32_t>(res[1]) << 16), res[2] | (static_cast<uint32_t>(res[3]) << 16));
 }
 
+// The split phase's outputs (marks, ranges, records) are ready when merge_body starts.
+struct SplitDone {
+  static constexpr bool kReady = true;
+  __device__ void operator()() const {}
+};
+
 // Unit (kv-head h, sequence s) with the block's 8 kParts warps: warps 0-7 attend the
 // workspace tokens (merge_ws_part); warp w takes share w / 8 of the partial records
 // for q-head w % 8 (every kParts-th record); after one block barrier the warps of
 // share 0 combine the shares with the workspace part and finish their q-heads. sm and
-// rs are the block's shared memory (rs unused when kParts is 1).
-template <int kBatch = 8, int kParts = 1>
+// rs are the block's shared memory (rs unused when kParts is 1). The workspace part
+// reads only the call's inputs; unless Wait::kReady, wait() runs after it, before
+// anything the split phase wrote is read.
+template <int kBatch = 8, int kParts = 1, class Wait = SplitDone>
 __device__ __forceinline__ void merge_body(const DecodeArgs& a, const uint16_t* __restrict__ ws,
                                            uint16_t* __restrict__ out, int h, int s, WsPart& sm,
-                                           RecShares<kParts>* rs, const int64_t* rg) {
+                                           RecShares<kParts>* rs, const int64_t* rg, const Wait& wait = Wait()) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gg = warp & 7, share = warp >> 3;
   const int64_t u = static_cast<int64_t>(s) * a.hkv + h;
-  const int2 cv = *reinterpret_cast<const int2*>(a.cover + 2 * u);   // in flight with the length
+  int2 cv = make_int2(-1, -1);
+  if (Wait::kReady) cv = *reinterpret_cast<const int2*>(a.cover + 2 * u);   // in flight with the length
   const int n_ws = ws_tokens(a, ws, s, threadIdx.x == 0);
   if (warp < 8) merge_ws_part(a, ws, h, s, n_ws, warp, sm);
+  if (!Wait::kReady) {
+    wait();
+    cv = *reinterpret_cast<const int2*>(a.cover + 2 * u);
+  }
   float M = -INFINITY, l = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
   if (gg < a.group) {
     int64_t wlo, whi;
