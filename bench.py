@@ -39,6 +39,7 @@ PRESET = "k4v2"             # `--preset`: k4v2 (the headline), k4v4, k2v2 or k4v
 PRESET_RECORD = {"k4v2": 14336, "k4v4": 18432, "k2v2": 10240, "k4v2l": 13824}
 WORKLOAD = "prefill_quantize_16x16k + decode_attn_64x16k_gqa64/8"
 E2E_CHUNKS = 8             # slices of the prefill batch in the end-to-end leg
+E2E_WINDOWS = 5            # end-to-end windows of K steps each; the median is reported
 # Reduced shapes for profiler captures (`--case small`): still larger than L2, a
 # few hundred MB on the device, and more (sequence, kv-head) units than SMs so that
 # the decode runs the split kernel in the full bench's shape. Not a bench line.
@@ -322,17 +323,22 @@ def run_gpu(args):
         S["out_h"].copy_(S["out"], non_blocking=True)
     for _ in range(max(1, args.warmup)):
         e2e_step()
-    torch.cuda.synchronize()
-    barrier()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    barrier()
-    e2e_ms = e0.elapsed_time(e1)
+    # A window of K steps moves ~K GB over the host link in tens of milliseconds, so
+    # it is timed E2E_WINDOWS times (each bracketed like the device-timed steps) and
+    # the median window is reported, every window listed beside it.
+    e2e_windows = []
+    for _ in range(E2E_WINDOWS):
+        torch.cuda.synchronize()
+        barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        e2e_windows.append(e0.elapsed_time(e1))
     h2d = sum(S[n].numel() * S[n].element_size() for n in ("kh", "vh", "slots_h", "qh", "bt_h", "lens_h"))
     d2h = S["out_h"].numel() * 2
 
@@ -365,7 +371,8 @@ def run_gpu(args):
         assert kv.kvarn_device_flags() == 0
 
     # max over ranks
-    total_ms, e2e_ms = reduce_max([total_ms, e2e_ms], world)
+    total_ms, *e2e_windows = reduce_max([total_ms, *e2e_windows], world)
+    e2e_ms = float(np.median(e2e_windows))
 
     p, d = PREFILL, DECODE
     q_bytes = p["n_seqs"] * p["seq_len"] * p["n_kv_heads"] * 128 * 2 * 2
@@ -428,6 +435,8 @@ def run_gpu(args):
         "roofline_kernels": [kq, kd],
         "e2e": {"value": round(world * step_bytes / (e2e_ms / args.steps * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                "windows": E2E_WINDOWS,
+                "windows_gbs": [round(world * step_bytes / (w / args.steps * 1e-3) / 1e9, 2) for w in e2e_windows],
                 "h2d_gbs": round(h2d_gbs, 1),
                 "h2d_bound": round(world * step_bytes / (h2d / (h2d_gbs * 1e9)) / 1e9, 1),
                 "h2d_note": "h2d_gbs: a pinned-host to device copy of the prefill batch's K (512 MiB) timed "
