@@ -31,6 +31,8 @@ def test_bench_small_case_line():
     assert d["value"] > 0 and d["ms_per_step"] > 0 and d["gpu_launches"] > 0
     assert d["roofline"]["bound"] in ("alu", "hbm", "tensor") and 0 < d["roofline"]["frac"] < 2
     assert d["e2e"]["value"] > 0 and d["e2e"]["h2d_bytes_per_step"] > 0
+    w = d["e2e"]["windows_gbs"]
+    assert len(w) == d["e2e"]["windows"] and min(w) <= d["e2e"]["value"] <= max(w)   # the median window
 
 
 def test_bench_prefill_attention_line():
