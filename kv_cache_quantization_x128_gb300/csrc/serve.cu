@@ -104,7 +104,7 @@ __device__ bool grid_sync(unsigned* barrier, unsigned n_ctas, unsigned* flags,
     }
     __threadfence();
   }
-  return __syncthreads_and(ok) != 0;   // thread 0's verdict, for the whole CTA
+  return __syncthreads_and(ok) != 0;   // thread 0's result, for the whole CTA
 }
 
 // Length of sequence s after the append (a negative length is left as it is).

@@ -156,7 +156,7 @@ def quantize_tensor(x: np.ndarray, kind: str, n_iters: int = N_ITERS, eps: float
     scale vectors a lean record keeps.
 
     Returns a dict with fp16-valued r [.., 128], c [.., 128], s, z, the codes
-    [.., 128 ch, 128 tok] and the pre-rounding values needed to judge ties."""
+    [.., 128 ch, 128 tok] and the pre-rounding values needed to decide ties."""
     assert kind in ("K", "V")
     if bits is None:
         bits = K_BITS if kind == "K" else V_BITS
