@@ -30,6 +30,7 @@
 // only the items whose sequence completes a tile.
 #include <cuda.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "kvarn_common.cuh"
@@ -49,7 +50,14 @@ static_assert(kOffIn % 1024 == 0, "align");
 // Shared-memory layout after the operands, per preset: a stage (codes + metadata)
 // of each tensor sized to its bit width, double buffered. Sizing the stages to the
 // preset, not to the widest one, was measured 1.5 % faster for k4v2.
-template <int KB, int VB>
+// The append hands the items that complete a tile out by rank (the k-th such item to
+// block k mod grid) when the batch has at most kRankItems items and no block gets more
+// than kRankList of them; each block keeps its list and the per-32-item counts here.
+constexpr int kRankItems = 32768;
+constexpr int kRankList = 216;
+constexpr int kRankBytes = kRankList * 4 + (kRankItems / 32 + 1) * 4;
+
+template <int KB, int VB, bool kRanked = false>
 struct QSmem {
   static constexpr int kStageK = kD * kB * KB / 8 + 1024;
   static constexpr int kStageV = kD * kB * VB / 8 + 1024;
@@ -58,7 +66,8 @@ struct QSmem {
   static constexpr int kOffVec = kOffStageV + 2 * kStageV;              // [group][vector][kVec] fp32
   static constexpr int kOffBar = kOffVec + 2 * kNumVec * kVec * 4;      // mma [group], load [group][buf]
   static constexpr int kOffTmem = kOffBar + 48;
-  static constexpr int kBytes = kOffTmem + 16;
+  static constexpr int kOffRank = kOffTmem + 16;                        // append: item list, chunk prefix
+  static constexpr int kBytes = kOffRank + (kRanked ? kRankBytes : 0);
   static_assert(kBytes <= 232448, "quantize shared memory");
   static_assert(kOffStageV % 16 == 0 && kOffVec % 16 == 0, "align");
 };
@@ -93,10 +102,10 @@ struct PrefillSource {
   int64_t num_blocks;
 
   static constexpr bool kSparse = false;   // every item has a tile
-  __device__ bool needs_load(int64_t) const { return true; }
-  __device__ void scatter_all(int) const {}
+  __device__ int scatter_all(int, uint8_t*) const { return 0; }
   // every item has a tile: the block's next one
   __device__ int64_t next_item(int64_t w, int) const { return w + gridDim.x; }
+  __device__ int64_t next_of(int64_t w, int, int lane, const uint8_t*, int) const { return next_item(w, lane); }
   // TMA coordinates (channel, token) of the item's 128 x 128 tile of tensor g
   __device__ void coords(int64_t w, int, int& x, int& y) const {
     const uint32_t chunk = hd.div(w);
@@ -137,6 +146,7 @@ struct AppendSource {
   ItemDiv hd;                   // division by hkv
   int max_blocks;
   int64_t num_blocks;
+  int ranked;                   // the completing items are handed out by rank (see kRankItems)
 
   static constexpr bool kSparse = true;    // only items whose sequence completes a tile
   __device__ bool needs_load(int64_t w) const {
@@ -162,13 +172,77 @@ struct AppendSource {
     if (g == 0 && h == 0 && t == 0 && seq_lens_out != nullptr) seq_lens_out[s] = L + 1;
     asm volatile("fence.proxy.async.global;" ::: "memory");
   }
-  // All of the block's items (w = blockIdx.x + j gridDim.x), 32 threads an item (both
-  // tensors), before the block barrier that precedes its first tile copy.
-  __device__ void scatter_all(int tid) const {
-    for (int64_t j0 = 0; static_cast<int64_t>(blockIdx.x) + j0 * gridDim.x < n_items; j0 += kThreads / 32) {
-      const int64_t w = static_cast<int64_t>(blockIdx.x) + (j0 + tid / 32) * gridDim.x;
-      if (w < n_items) scatter(w, (tid >> 4) & 1, tid & 15);
+  // The block's items, 32 threads an item (both tensors), before the block barrier
+  // that precedes its first tile copy. Without ranking these are w = blockIdx.x +
+  // j gridDim.x. With ranking, the completing items of ranks blockIdx.x + k gridDim.x
+  // (listed at `rank` in shared memory; their rows are the ones this block's tile
+  // copies read) and the block's w that complete nothing. Returns the list's length.
+  // Every thread of the block calls it.
+  __device__ int scatter_all(int tid, uint8_t* rank) const {
+    const int warp = tid >> 5, lane = tid & 31;
+    constexpr int kWarps = kThreads / 32;
+    int n_mine = 0;
+    if (ranked) {
+      int32_t* list = reinterpret_cast<int32_t*>(rank);
+      uint32_t* pref = reinterpret_cast<uint32_t*>(rank + kRankList * 4);   // [chunk]: completing items before it
+      const int n_chunks = static_cast<int>((n_items + 31) / 32);
+      for (int c = warp; c < n_chunks; c += kWarps) {
+        const int64_t w = 32 * static_cast<int64_t>(c) + lane;
+        const unsigned m = __ballot_sync(0xffffffffu, w < n_items && needs_load(w));
+        if (lane == 0) pref[c] = __popc(m);
+      }
+      __syncthreads();
+      if (warp == 0) {   // exclusive prefix over the chunks, lane l taking a contiguous run
+        const int per = (n_chunks + 31) / 32, c0 = min(lane * per, n_chunks), c1 = min(c0 + per, n_chunks);
+        uint32_t sum = 0;
+        for (int c = c0; c < c1; ++c) sum += pref[c];
+        uint32_t incl = sum;
+        for (int o = 1; o < 32; o <<= 1) {
+          const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += v;
+        }
+        uint32_t run = incl - sum;
+        for (int c = c0; c < c1; ++c) {
+          const uint32_t n = pref[c];
+          pref[c] = run;
+          run += n;
+        }
+        if (lane == 31) pref[n_chunks] = incl;
+      }
+      __syncthreads();
+      const uint32_t total = pref[n_chunks];
+      if (total > blockIdx.x) n_mine = static_cast<int>((total - blockIdx.x + gridDim.x - 1) / gridDim.x);
+      for (int k = warp; k < n_mine; k += kWarps) {
+        const uint32_t r = blockIdx.x + static_cast<uint32_t>(k) * gridDim.x;
+        int lo = 0, hi = n_chunks - 1;   // the last chunk whose prefix is <= r holds rank r
+        while (lo < hi) {
+          const int mid = (lo + hi + 1) >> 1;
+          if (pref[mid] <= r) lo = mid; else hi = mid - 1;
+        }
+        const int64_t w = 32 * static_cast<int64_t>(lo) + lane;
+        unsigned m = __ballot_sync(0xffffffffu, w < n_items && needs_load(w));
+        for (uint32_t i = pref[lo]; i < r; ++i) m &= m - 1;   // drop the lower-ranked items of the chunk
+        if (lane == 0) list[k] = 32 * lo + __ffs(m) - 1;
+      }
+      __syncthreads();
+      for (int k = warp; k < n_mine; k += kWarps) scatter(list[k], (tid >> 4) & 1, tid & 15);
     }
+    for (int64_t j0 = 0; static_cast<int64_t>(blockIdx.x) + j0 * gridDim.x < n_items; j0 += kWarps) {
+      const int64_t w = static_cast<int64_t>(blockIdx.x) + (j0 + warp) * gridDim.x;
+      if (w < n_items && !(ranked && needs_load(w))) scatter(w, (tid >> 4) & 1, tid & 15);
+    }
+    return n_mine;
+  }
+  // The block's first item with a tile (n_items if none).
+  __device__ int64_t first_item(int lane, const uint8_t* rank, int n_mine) const {
+    if (ranked) return n_mine > 0 ? reinterpret_cast<const int32_t*>(rank)[0] : n_items;
+    const int64_t w = blockIdx.x;
+    return needs_load(w) ? w : next_item(w, lane);
+  }
+  // The item after the block's k-th (w).
+  __device__ int64_t next_of(int64_t w, int k, int lane, const uint8_t* rank, int n_mine) const {
+    if (ranked) return k + 1 < n_mine ? reinterpret_cast<const int32_t*>(rank)[k + 1] : n_items;
+    return next_item(w, lane);
   }
   // The block's next item after w whose tile completes (n_items if none): 32 of the
   // block's items per round, one per lane, agreed by ballot (all 32 lanes call it).
@@ -255,7 +329,7 @@ __global__ void __maxnreg__(128)
   const int grp = tid / kGroupThreads;     // 0 = K, 1 = V
   const int gt = tid % kGroupThreads;
   const int bar_id = 1 + grp;
-  using S = QSmem<KB, VB>;
+  using S = QSmem<KB, VB, Src::kSparse>;
   uint64_t* mma_bar = reinterpret_cast<uint64_t*>(smem + S::kOffBar);
   uint64_t* load_bar = mma_bar + 2 + 2 * grp;   // this group's [buf]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + S::kOffTmem);
@@ -270,7 +344,8 @@ __global__ void __maxnreg__(128)
   fill_hadamard_sw128(smem + kOffH, tid, kThreads);   // the +-1 Hadamard operand
   // appended tokens into the workspace (the block's items), ordered before any tile
   // copy by the barrier below
-  src.scatter_all(tid);
+  uint8_t* rank = smem + S::kOffRank;
+  const int n_mine = src.scatter_all(tid, rank);
   if (tid == 0) {
     for (int b = 0; b < 6; ++b) mbar_init(&mma_bar[b], 1);
     fence_mbar_init();
@@ -300,7 +375,7 @@ __global__ void __maxnreg__(128)
   // an item's tile is started one item ahead; the slot check of the next item is
   // agreed on at the barrier that ends the current one.
   int64_t item = blockIdx.x;
-  if (Src::kSparse && !src.needs_load(item)) item = src.next_item(item, t);
+  if constexpr (Src::kSparse) item = src.first_item(t, rank, n_mine);
   uint32_t pend = 0;               // bit b: a copy into buffer b has not been waited for
   uint32_t load_parity = 0;        // bit b: phase parity of buffer b's barrier
   const bool has_first = !Src::kSparse || item < src.n_items;
@@ -320,7 +395,7 @@ __global__ void __maxnreg__(128)
   bool early = false;              // this item's products went out under the previous item's codes
   for (int k = 0; item < src.n_items; ++k) {
     const int buf = k & 1;
-    const int64_t next = src.next_item(item, t);
+    const int64_t next = src.next_of(item, k, t, rank, n_mine);
     const bool has_next = next < src.n_items;
     bool ok = true;
     if ((pend >> buf) & 1u) {
@@ -446,23 +521,24 @@ cudaError_t launch_quantize_bits(const Src& src, uint8_t* cache, int n_iters, fl
   int64_t grid = sm_count();
   if (max_ctas > 0 && grid > max_ctas) grid = max_ctas;
   if (grid > src.n_items) grid = src.n_items;
+  constexpr int kSmem = QSmem<KB, VB, Src::kSparse>::kBytes;
   // The prefill with 4-bit keys and more than one iteration issues each item's
   // products under the previous item's codes pass (measured slower for k2v2, for one
   // iteration and for the append, whose blocks get one or two items).
   if constexpr (!Src::kSparse && KB == 4) {
     if (n_iters > 1) {
       static std::atomic<unsigned long long> smem_set{0};
-      cudaError_t err = set_smem_once(quantize_kernel<Src, KB, VB, kLean, true>, QSmem<KB, VB>::kBytes, smem_set);
+      cudaError_t err = set_smem_once(quantize_kernel<Src, KB, VB, kLean, true>, kSmem, smem_set);
       if (err != cudaSuccess) return err;
-      quantize_kernel<Src, KB, VB, kLean, true><<<static_cast<unsigned>(grid), kThreads, QSmem<KB, VB>::kBytes,
-                                                  stream>>>(src, cache, n_iters, eps, flags);
+      quantize_kernel<Src, KB, VB, kLean, true><<<static_cast<unsigned>(grid), kThreads, kSmem, stream>>>(
+          src, cache, n_iters, eps, flags);
       return cudaGetLastError();
     }
   }
   static std::atomic<unsigned long long> smem_set{0};
-  cudaError_t err = set_smem_once(quantize_kernel<Src, KB, VB, kLean, false>, QSmem<KB, VB>::kBytes, smem_set);
+  cudaError_t err = set_smem_once(quantize_kernel<Src, KB, VB, kLean, false>, kSmem, smem_set);
   if (err != cudaSuccess) return err;
-  quantize_kernel<Src, KB, VB, kLean, false><<<static_cast<unsigned>(grid), kThreads, QSmem<KB, VB>::kBytes, stream>>>(
+  quantize_kernel<Src, KB, VB, kLean, false><<<static_cast<unsigned>(grid), kThreads, kSmem, stream>>>(
       src, cache, n_iters, eps, flags);
   return cudaGetLastError();
 }
@@ -554,6 +630,8 @@ cudaError_t launch_append(const uint16_t* k_new, const uint16_t* v_new, const in
   src.hd = make_item_div(static_cast<uint32_t>(hkv));
   src.max_blocks = max_blocks;
   src.num_blocks = num_blocks;
+  const int64_t grid = std::min<int64_t>(sm_count(), src.n_items);
+  src.ranked = src.n_items <= kRankItems && (src.n_items + grid - 1) / grid <= kRankList;
   return launch_quantize(src, cache, k_bits, v_bits, lean, n_iters, eps, flags, stream, 0);
 }
 
