@@ -26,8 +26,9 @@
 // each), so one group's MMA latency and barriers overlap the other's arithmetic.
 // The slot check of an item is agreed on at the barrier that ends the previous one.
 // The decode append runs the same kernel over (sequence, kv-head) items: the block
-// first writes the new tokens of all its items into the workspace, then quantizes
-// only the items whose sequence completes a tile.
+// first writes the new tokens of its items into the workspace, then quantizes only
+// the items whose sequence completes a tile (for batches of up to kRankItems items,
+// those handed to it by rank, so that blocks get equal shares of them).
 #include <cuda.h>
 
 #include <algorithm>
