@@ -141,9 +141,11 @@ def test_serving_step_256_ragged(env):
 
 def test_append_many_items(env):
     """More (sequence, kv-head) items than 32 per block (1300 sequences x 4 kv-heads,
-    ~34 items a block), so each block finds its next completing item over more than
-    one ballot round; every 7th sequence completes a tile. The new rows, the lengths,
-    64 sampled completed tiles against the oracle, and every other block untouched."""
+    ~34 items a block); every 7th sequence completes a tile, and the completing items
+    are handed out to the blocks by rank (the batch is under 32768 items; the larger
+    batches of tests/test_large_offsets_gpu.py take the ballot path). The new rows,
+    the lengths, 64 sampled completed tiles against the oracle, and every other block
+    untouched."""
     n_seqs, hkv, max_blocks = 1300, 4, 5
     rng = np.random.default_rng(43)
     lens = rng.integers(0, 600, n_seqs).astype(np.int32)
